@@ -1,0 +1,288 @@
+"""fp64 oracle of the MoE expert layer: routing, permutation, grouped FC1 -> GLU -> prob scale
+-> FC2, and its backward, in BF16-operand or MXFP8-operand form.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring). Plain definitions, computed per
+expert with numpy matmul as the only library step; no blocking, fusion or reordering.
+
+Readings of the pages (where they are silent or ambiguous), used consistently below:
+  R1 top-k: larger logit first, ties to the lower expert index; slot j = rank j.
+     Probabilities are the softmax over the k chosen logits (= full softmax renormalised
+     over the top-k).                                           [TE-MoE] Figure 1 (top-2 router)
+  R2 row order: expert ascending, then token ascending - the order in which the per-expert
+     loop's torch.where visits tokens.                          [TE-MoE] Challenge 1 loop
+  R3 expert segments start at offsets padded to `align` rows (32); padding rows are zero
+     and carry probability 0.                  [NV-blog] device-resident per-group token counts
+  R4 W1 logical columns [0,F) are the gate (the Swish side, "W" in the SwiGLU equation),
+     [F,2F) the linear side ("V").                      [NV-blog] SwiGLU equation, b = c = 0
+  R5 the routing probability scales the activation before FC2 (ScaledSwiGLU); FC2 has no
+     bias, so this equals scaling the expert output.             [TE-MoE] Challenge 3
+  R6 GeGLU uses the exact erf GELU; sReLU is the non-gated squared ReLU (FC1 width F).
+  R7 clamped SwiGLU: g' = min(g, gate_max), l' = clip(l, lin_lo, lin_hi),
+     a = (l' + lin_offset) * g' * sigmoid(beta * g'); a clamp passes the gradient at
+     equality (the clamp is active only strictly beyond the limit).
+  R8 MXFP8 operands (all six GEMMs): every GEMM consumes MXFP8 operands blocked along its
+     own reduction dimension, fp32-or-better accumulation; column-wise blocks of the
+     weight-gradient GEMMs start at each expert's first row.
+  R9 d_prob[t, j] = sum_f dA_s * a (a unscaled); d_logits is not part of the layer.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+from scipy.special import erf as _erf
+
+from . import mxfp8
+
+# ----------------------------------------------------------------------------- inputs
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> fp64 (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(
+        np.float64)
+
+
+@dataclass
+class ActParams:
+    kind: str = "swiglu"            # swiglu | clamped_swiglu | geglu | srelu
+    beta: float = 1.0
+    gate_max: float = math.inf
+    lin_lo: float = -math.inf
+    lin_hi: float = math.inf
+    lin_offset: float = 0.0
+
+    @property
+    def gated(self) -> bool:
+        return self.kind != "srelu"
+
+
+# ----------------------------------------------------------------------------- routing
+
+
+def route(logits: np.ndarray, k: int):
+    """Top-k expert choice and renormalised softmax over the chosen logits (R1).
+
+    logits: fp32 [T, E]. Returns ids int64 [T, k], probs fp64 [T, k].
+    [TE-MoE] Figure 1: a top-2 router sends each token to two of eight experts and the
+    outputs are combined as a weighted sum.
+    """
+    lg = np.asarray(logits, dtype=np.float32)
+    T, E = lg.shape
+    # stable sort of the negated logits keeps equal logits in index order
+    ids = np.argsort(-lg, axis=1, kind="stable")[:, :k]
+    chosen = np.take_along_axis(lg, ids, axis=1).astype(np.float64)
+    ex = np.exp(chosen - chosen.max(axis=1, keepdims=True))
+    probs = ex / ex.sum(axis=1, keepdims=True)
+    return ids.astype(np.int64), probs
+
+
+@dataclass
+class Permutation:
+    counts: np.ndarray          # [E]
+    offsets: np.ndarray         # [E+1], padded segment starts
+    row_of: np.ndarray          # [T, k] row of (token, slot)
+    src_of: np.ndarray          # [R_used] flattened t*k+j, -1 for padding rows
+    rows_of_expert: list = field(default_factory=list)   # per expert: (tokens, slots)
+
+
+def permutation(ids: np.ndarray, E: int, align: int) -> Permutation:
+    """Rows sorted by (expert, token) (R2), expert segments padded to `align` (R3).
+
+    [NV-blog] section on removing host-device synchronisation: the grouped GEMM keeps each
+    group's token count in device memory; here counts and padded offsets are the plain
+    histogram and its exclusive scan.
+    """
+    T, k = ids.shape
+    counts = np.bincount(ids.ravel(), minlength=E).astype(np.int64)
+    padded = -(-counts // align) * align
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(padded)
+    row_of = np.full((T, k), -1, dtype=np.int64)
+    src_of = np.full(int(offsets[-1]), -1, dtype=np.int64)
+    rows = []
+    for e in range(E):
+        tok, slot = np.nonzero(ids == e)        # row-major: token ascending
+        r = offsets[e] + np.arange(len(tok))
+        row_of[tok, slot] = r
+        src_of[r] = tok * k + slot
+        rows.append((tok, slot))
+    return Permutation(counts, offsets, row_of, src_of, rows)
+
+
+# ----------------------------------------------------------------------------- activations
+
+
+def _sigmoid(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def _Phi(x):
+    """Standard normal CDF via the library erf."""
+    return 0.5 * (1.0 + _erf(np.asarray(x, dtype=np.float64) / math.sqrt(2.0)))
+
+
+def _phi(x):
+    return np.exp(-0.5 * x * x) / math.sqrt(2.0 * math.pi)
+
+
+def act_forward(p: ActParams, g: np.ndarray, l: np.ndarray | None = None) -> np.ndarray:
+    """GLU activations of [NV-blog] (SwiGLU equation with b = c = 0; GeGLU; sReLU) with
+    optional clamp and scale (R6, R7). For sReLU `g` is the whole FC1 output."""
+    g = np.asarray(g, dtype=np.float64)
+    if p.kind == "swiglu":
+        return l * g * _sigmoid(p.beta * g)
+    if p.kind == "clamped_swiglu":
+        gc = np.minimum(g, p.gate_max)
+        lc = np.clip(l, p.lin_lo, p.lin_hi)
+        return (lc + p.lin_offset) * gc * _sigmoid(p.beta * gc)
+    if p.kind == "geglu":
+        return l * g * _Phi(g)
+    if p.kind == "srelu":
+        r = np.maximum(g, 0.0)
+        return r * r
+    raise ValueError(p.kind)
+
+
+def act_backward(p: ActParams, g, l, dA):
+    """Derivative of act_forward; returns (d_gate, d_linear) (d_linear None for sReLU).
+
+    [NV-blog] GLU-epilogue section: the backward epilogue reads the saved FC1 output and
+    computes dSwiGLU (here also dGeGLU / dsReLU and the clamped variant).
+    """
+    g = np.asarray(g, dtype=np.float64)
+    if p.kind == "swiglu":
+        s = _sigmoid(p.beta * g)
+        return dA * l * s * (1.0 + p.beta * g * (1.0 - s)), dA * g * s
+    if p.kind == "clamped_swiglu":
+        gc = np.minimum(g, p.gate_max)
+        lc = np.clip(l, p.lin_lo, p.lin_hi)
+        s = _sigmoid(p.beta * gc)
+        g_pass = (g <= p.gate_max).astype(np.float64)
+        l_pass = ((l >= p.lin_lo) & (l <= p.lin_hi)).astype(np.float64)
+        dg = dA * (lc + p.lin_offset) * s * (1.0 + p.beta * gc * (1.0 - s)) * g_pass
+        dl = dA * gc * s * l_pass
+        return dg, dl
+    if p.kind == "geglu":
+        return dA * l * (_Phi(g) + g * _phi(g)), dA * g * _Phi(g)
+    if p.kind == "srelu":
+        return dA * 2.0 * np.maximum(g, 0.0), None
+    raise ValueError(p.kind)
+
+
+# ----------------------------------------------------------------------------- one expert
+
+
+def _q(v, axis, mx):
+    return mxfp8.fake_quant(v, axis) if mx else v
+
+
+def _qrows(v, mx):
+    return mxfp8.fake_quant_rows_from(v) if mx else v
+
+
+def expert_forward(X, W1, W2, p, act: ActParams, mx: bool):
+    """One expert's share of the fused forward.
+
+    X [m, H] (its routed rows), W1 [H, N1] logical, W2 [F, H], p [m] routing probs.
+    Z = X W1;  a = act(gate, lin);  a_s = p * a (ScaledSwiGLU, R5);  Y = a_s W2.
+    [TE-MoE] Challenge 3 (GroupedLinear -> ScaledSwiGLU -> GroupedLinear) and [NV-blog]
+    Figure 1 (FC1 + activation + quantise fused, then FC2). In MXFP8 (R8) each GEMM uses
+    MXFP8 operands blocked along its reduction dimension: X and W1 along H, a_s and W2 along F.
+    """
+    F = W2.shape[0]
+    Z = _q(X, 1, mx) @ _q(W1, 0, mx)
+    if act.gated:
+        a = act_forward(act, Z[:, :F], Z[:, F:])
+    else:
+        a = act_forward(act, Z)
+    a_s = p[:, None] * a
+    Y = _q(a_s, 1, mx) @ _q(W2, 0, mx)
+    return Z, a, a_s, Y
+
+
+def expert_backward(X, W1, W2, p, Z, a, a_s, dY, act: ActParams, mx: bool):
+    """One expert's share of the backward ([NV-blog] Figure 1: FC2 dgrad + dActivation +
+    quantise fused; the weight-gradient GEMMs unfused).
+
+      dA_s = dY W2^T;  d_prob = sum_f dA_s * a  (R9);  dA = p * dA_s;
+      (dG, dL) = dact(Z, dA);  dZ = [dG | dL];
+      dW2 = a_s^T dY;  dW1 = X^T dZ;  dX = dZ W1^T.
+    MXFP8 (R8): dY and W2 along H for dgrad; a_s and dY column-wise (along rows) for dW2;
+    dZ along N1 and W1 along N1 for dX; X and dZ column-wise for dW1.
+    """
+    F = W2.shape[0]
+    dA_s = _q(dY, 1, mx) @ _q(W2, 1, mx).T
+    d_prob = (dA_s * a).sum(axis=1)
+    dA = p[:, None] * dA_s
+    if act.gated:
+        dg, dl = act_backward(act, Z[:, :F], Z[:, F:], dA)
+        dZ = np.concatenate([dg, dl], axis=1)
+    else:
+        dZ, _ = act_backward(act, Z, None, dA)
+    dW2 = _qrows(a_s, mx).T @ _qrows(dY, mx)
+    dW1 = _qrows(X, mx).T @ _qrows(dZ, mx)
+    dX = _q(dZ, 1, mx) @ _q(W1, 1, mx).T
+    return dZ, dX, dW1, dW2, d_prob
+
+
+# ----------------------------------------------------------------------------- the layer
+
+
+@dataclass
+class LayerResult:
+    ids: np.ndarray
+    probs: np.ndarray
+    perm: Permutation
+    y: np.ndarray
+    dx: np.ndarray | None = None
+    dW1: np.ndarray | None = None
+    dW2: np.ndarray | None = None
+    d_probs: np.ndarray | None = None
+    per_expert: list = field(default_factory=list)   # dicts of intermediates by expert
+
+
+def layer(logits, x, W1, W2, k: int, act: ActParams, mx: bool = False, align: int = 32,
+          dy=None, keep_intermediates: bool = False, experts=None) -> LayerResult:
+    """Forward (and, when dy is given, backward) of the MoE expert layer.
+
+    logits fp32 [T,E]; x fp64 [T,H]; W1 fp64 [E,H,N1] (or a callable e -> [H,N1]);
+    W2 fp64 [E,F,H] (or callable); dy fp64 [T,H].
+    y[t] = sum_j Y[row_of[t,j]]: the index_add of [TE-MoE] Challenge 1's per-expert loop.
+    `experts` restricts the computation to a subset (y / dx then hold only their share).
+    """
+    T, E = np.asarray(logits).shape
+    ids, probs = route(logits, k)
+    perm = permutation(ids, E, align)
+    H = x.shape[1]
+    w1 = W1 if callable(W1) else (lambda e: W1[e])
+    w2 = W2 if callable(W2) else (lambda e: W2[e])
+    y = np.zeros((T, H))
+    res = LayerResult(ids, probs, perm, y)
+    if dy is not None:
+        res.dx = np.zeros((T, H))
+        res.d_probs = np.zeros((T, k))
+        res.dW1, res.dW2 = {}, {}
+    for e in (range(E) if experts is None else experts):
+        tok, slot = perm.rows_of_expert[e]
+        W1e, W2e = w1(e), w2(e)
+        X = x[tok]
+        p = probs[tok, slot]
+        Z, a, a_s, Y = expert_forward(X, W1e, W2e, p, act, mx)
+        np.add.at(y, tok, Y)
+        inter = dict(Z=Z, a=a, a_s=a_s, Y=Y) if keep_intermediates else {}
+        if dy is not None:
+            dY = dy[tok]
+            dZ, dX, dW1, dW2, d_prob = expert_backward(X, W1e, W2e, p, Z, a, a_s, dY, act, mx)
+            np.add.at(res.dx, tok, dX)
+            res.d_probs[tok, slot] = d_prob
+            res.dW1[e], res.dW2[e] = dW1, dW2
+            if keep_intermediates:
+                inter.update(dZ=dZ, dX=dX, d_prob=d_prob)
+        res.per_expert.append(inter)
+    return res
+
+
+def stack_weight_grads(res: LayerResult, E: int):
+    return np.stack([res.dW1[e] for e in range(E)]), np.stack([res.dW2[e] for e in range(E)])

@@ -1,0 +1,265 @@
+"""Python binding of libmoegmm (the GB300 fused grouped expert MLP).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA kernels. The
+functions below carry the C ABI's names (include/moegmm.h) and accept torch tensors (their
+device pointers are passed) or raw integer addresses. `MoELayer` is plumbing on top: it
+allocates the caller-owned buffers with torch and calls the same entry points.
+
+There is no fallback: if the shared library is missing, `load()` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libmoegmm.so")
+
+PREC = {"bf16": 0, "mxfp8": 1}
+ACT = {"swiglu": 0, "clamped_swiglu": 1, "geglu": 2, "srelu": 3}
+DEVERR = {0: "none", 1: "capacity", 2: "timeout", 3: "bad_id"}
+
+EXPORTS = ("moe_workspace_size", "moe_workspace_layout", "moe_route_permute",
+           "moe_grouped_mlp_fwd", "moe_grouped_mlp_bwd", "mxfp8_quantize", "moe_pack_fc1_weight",
+           "moe_get_error", "moe_clear_error", "moe_gemm_ctas", "moe_launch_count",
+           "moe_last_error_string")
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int32), ("k", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("F", ctypes.c_int32), ("T_max", ctypes.c_int32), ("precision", ctypes.c_int32),
+                ("activation", ctypes.c_int32), ("beta", ctypes.c_float),
+                ("gate_max", ctypes.c_float), ("lin_lo", ctypes.c_float),
+                ("lin_hi", ctypes.c_float), ("lin_offset", ctypes.c_float),
+                ("sm_margin", ctypes.c_int32), ("ilv", ctypes.c_int32), ("align", ctypes.c_int32)]
+
+
+class WsLayout(ctypes.Structure):
+    _fields_ = [("total", ctypes.c_size_t), ("R_cap", ctypes.c_int64), ("err", ctypes.c_size_t),
+                ("offsets", ctypes.c_size_t), ("row_of", ctypes.c_size_t),
+                ("src_of", ctypes.c_size_t), ("row_prob", ctypes.c_size_t),
+                ("x_perm", ctypes.c_size_t), ("z", ctypes.c_size_t), ("a_s", ctypes.c_size_t),
+                ("y_perm", ctypes.c_size_t), ("dy_perm", ctypes.c_size_t),
+                ("dz", ctypes.c_size_t), ("dx_perm", ctypes.c_size_t),
+                ("dprob_part", ctypes.c_size_t), ("mx_base", ctypes.c_size_t)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_DP = ctypes.POINTER(LayerDesc)
+
+
+def load():
+    """Load the shared library (build it first with __graft_entry__.build() or
+    `python -m grouped_gemm_device_gb300.build`). Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libmoegmm.so not built ({LIB_PATH}); run the build step first")
+    lib = ctypes.CDLL(LIB_PATH)
+    sig = {
+        "moe_workspace_size": (_SZ, [_DP]),
+        "moe_workspace_layout": (_I32, [_DP, ctypes.POINTER(WsLayout)]),
+        "moe_route_permute": (_I32, [_DP, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+        "moe_grouped_mlp_fwd": (_I32, [_DP, _I32, _P, _P, _P, _P, _SZ, _P]),
+        "moe_grouped_mlp_bwd": (_I32, [_DP, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+        "mxfp8_quantize": (_I32, [_P, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P]),
+        "moe_pack_fc1_weight": (_I32, [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P]),
+        "moe_get_error": (_I32, [_DP, _P, ctypes.POINTER(_I32), _P]),
+        "moe_clear_error": (_I32, [_DP, _P, _P]),
+        "moe_gemm_ctas": (_I32, [_DP]),
+        "moe_launch_count": (ctypes.c_uint64, []),
+        "moe_last_error_string": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"status {status}: {msg}")
+        self.status = status
+
+
+def _check(st: int):
+    if st != 0:
+        raise MoeError(st, load().moe_last_error_string().decode())
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_desc(E, k, H, F, T_max, precision="bf16", activation="swiglu", beta=1.0,
+              gate_max=math.inf, lin_lo=-math.inf, lin_hi=math.inf, lin_offset=0.0,
+              sm_margin=0, ilv=64, align=32) -> LayerDesc:
+    return LayerDesc(E, k, H, F, T_max, PREC[precision], ACT[activation], beta, gate_max,
+                     lin_lo, lin_hi, lin_offset, sm_margin, ilv, align)
+
+
+def desc_from_config(cfg, T_max=None, sm_margin=0) -> LayerDesc:
+    return make_desc(cfg.E, cfg.k, cfg.H, cfg.F, cfg.T if T_max is None else T_max,
+                     cfg.precision, cfg.activation, cfg.beta, cfg.gate_max, cfg.lin_lo,
+                     cfg.lin_hi, cfg.lin_offset, sm_margin, cfg.ilv, cfg.align)
+
+
+# ------------------------------------------------------------------ C ABI, same names
+def moe_workspace_size(desc: LayerDesc) -> int:
+    n = load().moe_workspace_size(ctypes.byref(desc))
+    if n == 0:
+        raise MoeError(1, load().moe_last_error_string().decode())
+    return n
+
+
+def moe_workspace_layout(desc: LayerDesc) -> WsLayout:
+    out = WsLayout()
+    _check(load().moe_workspace_layout(ctypes.byref(desc), ctypes.byref(out)))
+    return out
+
+
+def moe_route_permute(desc, T, logits, x, topk_ids, topk_probs, counts, ws, ws_bytes,
+                      stream=None):
+    _check(load().moe_route_permute(ctypes.byref(desc), T, _ptr(logits), _ptr(x), _ptr(topk_ids),
+                                    _ptr(topk_probs), _ptr(counts), _ptr(ws), ws_bytes,
+                                    _stream(stream)))
+
+
+def moe_grouped_mlp_fwd(desc, T, w1_packed, w2, y, ws, ws_bytes, stream=None):
+    _check(load().moe_grouped_mlp_fwd(ctypes.byref(desc), T, _ptr(w1_packed), _ptr(w2), _ptr(y),
+                                      _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_grouped_mlp_bwd(desc, T, dy, w1_packed, w2, dx, dw1_packed, dw2, d_probs, ws, ws_bytes,
+                        stream=None):
+    _check(load().moe_grouped_mlp_bwd(ctypes.byref(desc), T, _ptr(dy), _ptr(w1_packed), _ptr(w2),
+                                      _ptr(dx), _ptr(dw1_packed), _ptr(dw2), _ptr(d_probs),
+                                      _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def mxfp8_quantize(inp, M, N, rowwise, colwise, q_row=None, s_row=None, q_col=None, s_col=None,
+                   stream=None):
+    _check(load().mxfp8_quantize(_ptr(inp), M, N, int(rowwise), int(colwise), _ptr(q_row),
+                                 _ptr(s_row), _ptr(q_col), _ptr(s_col), _stream(stream)))
+
+
+def moe_pack_fc1_weight(src, dst, E, H, F, gated, ilv, inverse, stream=None):
+    _check(load().moe_pack_fc1_weight(_ptr(src), _ptr(dst), E, H, F, int(gated), ilv,
+                                      int(inverse), _stream(stream)))
+
+
+def moe_get_error(desc, ws, stream=None) -> int:
+    """Synchronous convenience: enqueue the copy, synchronise the stream, return the code."""
+    import torch
+    code = ctypes.c_int32(-1)
+    _check(load().moe_get_error(ctypes.byref(desc), _ptr(ws), ctypes.byref(code),
+                                _stream(stream)))
+    torch.cuda.synchronize()
+    return code.value
+
+
+def moe_clear_error(desc, ws, stream=None):
+    _check(load().moe_clear_error(ctypes.byref(desc), _ptr(ws), _stream(stream)))
+
+
+def moe_gemm_ctas(desc) -> int:
+    return load().moe_gemm_ctas(ctypes.byref(desc))
+
+
+def moe_launch_count() -> int:
+    return int(load().moe_launch_count())
+
+
+# ------------------------------------------------------------------ buffer plumbing
+class MoELayer:
+    """Owns the caller-side buffers of one layer (allocated with torch) and runs the C ABI
+    calls on them. Weights: w1_packed [E, N1, H] bf16 (packed rows), w2 [E, F, H] bf16."""
+
+    def __init__(self, desc: LayerDesc, device="cuda"):
+        import torch
+        load()
+        self.desc = desc
+        self.device = torch.device(device)
+        self.layout = moe_workspace_layout(desc)
+        self.ws_bytes = self.layout.total
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        d = desc
+        self.N1 = d.F if d.activation == ACT["srelu"] else 2 * d.F
+        T, E, k, H = d.T_max, d.E, d.k, d.H
+        dev = self.device
+        self.topk_ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+        self.topk_probs = torch.empty(T, k, dtype=torch.float32, device=dev)
+        self.counts = torch.zeros(E, dtype=torch.int32, device=dev)
+        self.y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        self.dx = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        self.d_probs = torch.empty(T, k, dtype=torch.float32, device=dev)
+        self.dw1 = None
+        self.dw2 = None
+
+    # views into the workspace -------------------------------------------------------
+    def ws_view(self, name, dtype, shape):
+        import torch
+        off = getattr(self.layout, name)
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return self.ws[off:off + nbytes].view(dtype).view(*shape)
+
+    def offsets(self):
+        import torch
+        return self.ws_view("offsets", torch.int32, (self.desc.E + 1,))
+
+    # calls ---------------------------------------------------------------------------
+    def route_permute(self, logits, x, T=None, stream=None):
+        T = logits.shape[0] if T is None else T
+        moe_route_permute(self.desc, T, logits, x, self.topk_ids, self.topk_probs, self.counts,
+                          self.ws, self.ws_bytes, stream)
+
+    def forward(self, w1_packed, w2, T, stream=None):
+        moe_grouped_mlp_fwd(self.desc, T, w1_packed, w2, self.y, self.ws, self.ws_bytes, stream)
+        return self.y[:T]
+
+    def backward(self, dy, w1_packed, w2, T, stream=None):
+        import torch
+        if self.dw1 is None:
+            d = self.desc
+            self.dw1 = torch.empty(d.E, self.N1, d.H, dtype=torch.bfloat16, device=self.device)
+            self.dw2 = torch.empty(d.E, d.F, d.H, dtype=torch.bfloat16, device=self.device)
+        moe_grouped_mlp_bwd(self.desc, T, dy, w1_packed, w2, self.dx, self.dw1, self.dw2,
+                            self.d_probs, self.ws, self.ws_bytes, stream)
+        return self.dx[:T], self.dw1, self.dw2, self.d_probs[:T]
+
+    def device_error(self, stream=None) -> int:
+        return moe_get_error(self.desc, self.ws, stream)
+
+
+def pack_w1(w1_logical, gated=True, ilv=64, stream=None):
+    """w1_logical bf16 [E, H, N1] (torch, cuda) -> packed [E, N1, H] through the library."""
+    import torch
+    E, H, N1 = w1_logical.shape
+    F = N1 // 2 if gated else N1
+    out = torch.empty(E, N1, H, dtype=w1_logical.dtype, device=w1_logical.device)
+    moe_pack_fc1_weight(w1_logical, out, E, H, F, gated, ilv, 0, stream)
+    return out

@@ -1,0 +1,396 @@
+// C ABI of the library (declared in include/moegmm.h): host-side validation, workspace
+// layout, and the launch sequences of routing, forward and backward. Nothing here allocates
+// device memory or synchronises; everything is enqueued on the caller's stream.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "kernels.cuh"
+
+namespace moe {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+static thread_local std::string g_last_error;
+
+static moe_status_t fail(moe_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+static moe_status_t cuda_fail(cudaError_t e, const char* where) {
+  return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+static int device_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static int cache[64] = {0};
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int64_t r_cap(const moe_layer_desc_t* d) {
+  return (int64_t)d->T_max * d->k + (int64_t)d->E * (d->align - 1);
+}
+static int n1_of(const moe_layer_desc_t* d) {
+  return d->activation == MOE_ACT_SRELU ? d->F : 2 * d->F;
+}
+
+static moe_status_t validate_desc(const moe_layer_desc_t* d) {
+  if (!d) return fail(MOE_ERR_INVALID_ARG, "desc is NULL");
+  if (d->E < 1 || d->E > 256) return fail(MOE_ERR_INVALID_ARG, "E=%d outside [1,256]", d->E);
+  if (d->k < 1 || d->k > 8 || d->k > d->E)
+    return fail(MOE_ERR_INVALID_ARG, "k=%d must be in [1, min(E,8)]", d->k);
+  if (d->H <= 0 || d->F <= 0 || d->T_max < 0)
+    return fail(MOE_ERR_INVALID_ARG, "H, F must be positive and T_max >= 0");
+  if (d->H % 64 || d->F % 64)
+    return fail(MOE_ERR_UNSUPPORTED, "H=%d and F=%d must be multiples of 64", d->H, d->F);
+  if (d->align != 32) return fail(MOE_ERR_UNSUPPORTED, "align must be 32");
+  if (d->precision != MOE_PREC_BF16 && d->precision != MOE_PREC_MXFP8)
+    return fail(MOE_ERR_INVALID_ARG, "unknown precision %d", d->precision);
+  if (d->activation < MOE_ACT_SWIGLU || d->activation > MOE_ACT_SRELU)
+    return fail(MOE_ERR_INVALID_ARG, "unknown activation %d", d->activation);
+  if (d->activation != MOE_ACT_SRELU) {
+    if (d->ilv != 32 && d->ilv != 64 && d->ilv != 128)
+      return fail(MOE_ERR_UNSUPPORTED, "ilv=%d must be 32, 64 or 128", d->ilv);
+    if (d->F % d->ilv) return fail(MOE_ERR_UNSUPPORTED, "F must be a multiple of ilv");
+  }
+  if (d->sm_margin < 0) return fail(MOE_ERR_INVALID_ARG, "sm_margin must be >= 0");
+  if (r_cap(d) > (int64_t)INT32_MAX / 2) return fail(MOE_ERR_UNSUPPORTED, "row capacity too large");
+  if (d->precision == MOE_PREC_MXFP8)
+    return fail(MOE_ERR_UNSUPPORTED, "MXFP8 grouped GEMM path not built in this library version");
+  return MOE_OK;
+}
+
+static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static void compute_layout(const moe_layer_desc_t* d, moe_ws_layout_t* L) {
+  const int64_t R = r_cap(d);
+  const int64_t H = d->H, F = d->F, N1 = n1_of(d), E = d->E;
+  const int64_t nparts = (F + gemm_bn(ROLE_FC2_DGRAD) - 1) / gemm_bn(ROLE_FC2_DGRAD);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = up256(o + bytes);
+    return at;
+  };
+  L->R_cap = R;
+  L->err = take(256);
+  L->offsets = take((E + 1) * 4);
+  L->row_of = take((size_t)d->T_max * d->k * 4);
+  L->src_of = take(R * 4);
+  L->row_prob = take(R * 4);
+  L->x_perm = take(R * H * 2);
+  L->z = take(R * N1 * 2);
+  L->a_s = take(R * F * 2);
+  L->y_perm = take(R * H * 2);
+  L->dx_perm = L->y_perm;  // y_perm is dead once y is combined
+  L->dy_perm = take(R * H * 2);
+  L->dz = take(R * N1 * 2);
+  L->dprob_part = take(R * nparts * 4);
+  L->mx_base = SIZE_MAX;
+  L->total = o;
+}
+
+struct Ws {
+  moe_ws_layout_t L;
+  uint8_t* base;
+  template <class T>
+  T* at(size_t off) const { return reinterpret_cast<T*>(base + off); }
+};
+
+static moe_status_t check_ws(const moe_layer_desc_t* d, void* ws, size_t ws_bytes, Ws& w) {
+  compute_layout(d, &w.L);
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "ws is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) & 255u)
+    return fail(MOE_ERR_INVALID_ARG, "ws must be 256-byte aligned");
+  if (ws_bytes < w.L.total)
+    return fail(MOE_ERR_WORKSPACE, "ws_bytes=%zu < required %zu", ws_bytes, w.L.total);
+  w.base = static_cast<uint8_t*>(ws);
+  return MOE_OK;
+}
+
+static ActDev act_of(const moe_layer_desc_t* d) {
+  ActDev a;
+  a.kind = d->activation;
+  a.beta = d->beta;
+  a.gate_max = d->gate_max;
+  a.lin_lo = d->lin_lo;
+  a.lin_hi = d->lin_hi;
+  a.lin_offset = d->lin_offset;
+  return a;
+}
+
+static int gemm_ctas(const moe_layer_desc_t* d) {
+  int n = device_sms() - d->sm_margin;
+  return n < 1 ? 1 : n;
+}
+
+static GemmProblem base_problem(const moe_layer_desc_t* d, const Ws& w) {
+  GemmProblem p;
+  memset(&p, 0, sizeof(p));
+  p.E = d->E;
+  p.H = d->H;
+  p.F = d->F;
+  p.N1 = n1_of(d);
+  p.R_cap = w.L.R_cap;
+  p.offsets = w.at<int32_t>(w.L.offsets);
+  p.row_prob = w.at<float>(w.L.row_prob);
+  p.x_perm = w.at<void>(w.L.x_perm);
+  p.a_s = w.at<void>(w.L.a_s);
+  p.z = w.at<void>(w.L.z);
+  p.dz = w.at<void>(w.L.dz);
+  p.dy_perm = w.at<void>(w.L.dy_perm);
+  p.gated = d->activation != MOE_ACT_SRELU;
+  p.ilv = d->ilv;
+  p.act = act_of(d);
+  p.err = w.at<int>(w.L.err);
+  p.num_ctas = gemm_ctas(d);
+  return p;
+}
+
+static int grid_for(int64_t work, int per_sm) {
+  int sms = device_sms();
+  if (sms <= 0) sms = 1;
+  int64_t g = std::min<int64_t>(work, (int64_t)sms * per_sm);
+  return (int)std::max<int64_t>(g, 1);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_layer_desc_t* desc) {
+  if (validate_desc(desc) != MOE_OK) return 0;
+  moe_ws_layout_t L;
+  compute_layout(desc, &L);
+  return L.total;
+}
+
+moe_status_t moe_workspace_layout(const moe_layer_desc_t* desc, moe_ws_layout_t* out) {
+  moe_status_t st = validate_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+  compute_layout(desc, out);
+  return MOE_OK;
+}
+
+moe_status_t moe_route_permute(const moe_layer_desc_t* d, int32_t T, const float* logits,
+                               const void* x, int32_t* topk_ids, float* topk_probs,
+                               int32_t* counts, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status_t st = validate_desc(d);
+  if (st != MOE_OK) return st;
+  if (T < 0 || T > d->T_max) return fail(MOE_ERR_INVALID_ARG, "T=%d outside [0, T_max]", T);
+  if ((T > 0 && (!logits || !x || !topk_ids || !topk_probs)) || !counts)
+    return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned16(x)) return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned");
+  Ws w;
+  if ((st = check_ws(d, ws, ws_bytes, w)) != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * d->E, s);
+  if (e != cudaSuccess) return cuda_fail(e, "memset counts");
+  int32_t* offsets = w.at<int32_t>(w.L.offsets);
+  int32_t* row_of = w.at<int32_t>(w.L.row_of);
+  int32_t* src_of = w.at<int32_t>(w.L.src_of);
+  float* row_prob = w.at<float>(w.L.row_prob);
+  int* err = w.at<int>(w.L.err);
+  if (T > 0) {
+    route_topk_kernel<<<grid_for((T + 7) / 8, 8), 256, 0, s>>>(logits, T, d->E, d->k, topk_ids,
+                                                                 topk_probs, counts);
+    count_launch();
+  }
+  assign_rows_kernel<<<d->E, 1024, 0, s>>>(topk_ids, topk_probs, counts, T, d->E, d->k, d->align,
+                                           w.L.R_cap, offsets, row_of, src_of, row_prob, err);
+  count_launch();
+  gather_rows_kernel<<<grid_for(w.L.R_cap, 8), 256, 0, s>>>(
+      static_cast<const uint4*>(x), src_of, offsets, d->E, d->k, d->H / 8, w.L.R_cap,
+      w.at<uint4>(w.L.x_perm));
+  count_launch();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "route_permute launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_grouped_mlp_fwd(const moe_layer_desc_t* d, int32_t T, const void* w1_packed,
+                                 const void* w2, void* y, void* ws, size_t ws_bytes,
+                                 moe_stream_t stream) {
+  moe_status_t st = validate_desc(d);
+  if (st != MOE_OK) return st;
+  if (T < 0 || T > d->T_max) return fail(MOE_ERR_INVALID_ARG, "T=%d outside [0, T_max]", T);
+  if (!w1_packed || !w2 || (T > 0 && !y)) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned16(w1_packed) || !aligned16(w2) || !aligned16(y))
+    return fail(MOE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  Ws w;
+  if ((st = check_ws(d, ws, ws_bytes, w)) != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  GemmProblem p = base_problem(d, w);
+  p.w1p = w1_packed;
+  p.w2 = w2;
+  cudaError_t e;
+  // FC1 + activation + probability scale (kernel family 2)
+  p.role = ROLE_FC1_FPROP;
+  p.out = w.at<void>(w.L.z);
+  p.out2 = w.at<void>(w.L.a_s);
+  if ((e = launch_grouped_gemm(p, s)) != cudaSuccess) return cuda_fail(e, "FC1 grouped GEMM");
+  // FC2 (kernel family 1)
+  p.role = ROLE_FC2_FPROP;
+  p.out = w.at<void>(w.L.y_perm);
+  p.out2 = nullptr;
+  if ((e = launch_grouped_gemm(p, s)) != cudaSuccess) return cuda_fail(e, "FC2 grouped GEMM");
+  if (T > 0) {
+    combine_rows_kernel<<<grid_for(T, 8), 256, 0, s>>>(w.at<uint4>(w.L.y_perm),
+                                                      w.at<int32_t>(w.L.row_of), T, d->k,
+                                                      d->H / 8, static_cast<uint4*>(y));
+    count_launch();
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "fwd launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t* d, int32_t T, const void* dy,
+                                 const void* w1_packed, const void* w2, void* dx,
+                                 void* dw1_packed, void* dw2, float* d_probs, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream) {
+  moe_status_t st = validate_desc(d);
+  if (st != MOE_OK) return st;
+  if (T < 0 || T > d->T_max) return fail(MOE_ERR_INVALID_ARG, "T=%d outside [0, T_max]", T);
+  if (!w1_packed || !w2 || !dw1_packed || !dw2 || (T > 0 && (!dy || !dx || !d_probs)))
+    return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned16(dy) || !aligned16(dx) || !aligned16(w1_packed) || !aligned16(w2) ||
+      !aligned16(dw1_packed) || !aligned16(dw2))
+    return fail(MOE_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  Ws w;
+  if ((st = check_ws(d, ws, ws_bytes, w)) != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  GemmProblem p = base_problem(d, w);
+  p.w1p = w1_packed;
+  p.w2 = w2;
+  const int32_t* row_of = w.at<int32_t>(w.L.row_of);
+  cudaError_t e;
+  // dY gathered into the permuted row order (zero for padding rows)
+  gather_rows_kernel<<<grid_for(w.L.R_cap, 8), 256, 0, s>>>(
+      static_cast<const uint4*>(dy), w.at<int32_t>(w.L.src_of), w.at<int32_t>(w.L.offsets), d->E,
+      d->k, d->H / 8, w.L.R_cap, w.at<uint4>(w.L.dy_perm));
+  count_launch();
+  // FC2 dgrad + dActivation (kernel family 3)
+  p.role = ROLE_FC2_DGRAD;
+  p.out = w.at<void>(w.L.dz);
+  p.dprob_part = w.at<float>(w.L.dprob_part);
+  if ((e = launch_grouped_gemm(p, s)) != cudaSuccess) return cuda_fail(e, "FC2 dgrad GEMM");
+  if (T > 0) {
+    const int nparts = (d->F + gemm_bn(ROLE_FC2_DGRAD) - 1) / gemm_bn(ROLE_FC2_DGRAD);
+    const int n = T * d->k;
+    dprob_reduce_kernel<<<grid_for((n + 255) / 256, 4), 256, 0, s>>>(
+        w.at<float>(w.L.dprob_part), nparts, row_of, n, d_probs);
+    count_launch();
+  }
+  // FC2 wgrad
+  p.role = ROLE_FC2_WGRAD;
+  p.out = dw2;
+  if ((e = launch_grouped_gemm(p, s)) != cudaSuccess) return cuda_fail(e, "FC2 wgrad GEMM");
+  // FC1 dgrad (kernel family 1) and combine
+  p.role = ROLE_FC1_DGRAD;
+  p.out = w.at<void>(w.L.dx_perm);
+  if ((e = launch_grouped_gemm(p, s)) != cudaSuccess) return cuda_fail(e, "FC1 dgrad GEMM");
+  if (T > 0) {
+    combine_rows_kernel<<<grid_for(T, 8), 256, 0, s>>>(w.at<uint4>(w.L.dx_perm), row_of, T,
+                                                      d->k, d->H / 8, static_cast<uint4*>(dx));
+    count_launch();
+  }
+  // FC1 wgrad
+  p.role = ROLE_FC1_WGRAD;
+  p.out = dw1_packed;
+  if ((e = launch_grouped_gemm(p, s)) != cudaSuccess) return cuda_fail(e, "FC1 wgrad GEMM");
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "bwd launch");
+  return MOE_OK;
+}
+
+moe_status_t mxfp8_quantize(const void* in, int64_t M, int64_t N, int32_t rowwise,
+                            int32_t colwise, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                            uint8_t* s_col, moe_stream_t stream) {
+  if (M < 0 || N < 0) return fail(MOE_ERR_INVALID_ARG, "negative size");
+  if (!rowwise && !colwise) return fail(MOE_ERR_INVALID_ARG, "neither rowwise nor colwise");
+  if (M == 0 || N == 0) return MOE_OK;
+  if (!in || !aligned16(in)) return fail(MOE_ERR_INVALID_ARG, "in must be non-NULL, 16B aligned");
+  if (N % 32) return fail(MOE_ERR_UNSUPPORTED, "N must be a multiple of 32");
+  if (colwise && M % 32) return fail(MOE_ERR_UNSUPPORTED, "M must be a multiple of 32 (colwise)");
+  if (rowwise && (!q_row || !s_row || !aligned16(q_row)))
+    return fail(MOE_ERR_INVALID_ARG, "rowwise outputs must be non-NULL (q_row 16B aligned)");
+  if (colwise && (!q_col || !s_col || !aligned16(q_col)))
+    return fail(MOE_ERR_INVALID_ARG, "colwise outputs must be non-NULL (q_col 16B aligned)");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  launch_mxfp8_quantize(in, M, N, rowwise, colwise, q_row, s_row, q_col, s_col,
+                        std::max(device_sms(), 1), s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "mxfp8_quantize launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_pack_fc1_weight(const void* src, void* dst, int32_t E, int32_t H, int32_t F,
+                                 int32_t gated, int32_t ilv, int32_t inverse,
+                                 moe_stream_t stream) {
+  if (!src || !dst) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (src == dst) return fail(MOE_ERR_INVALID_ARG, "in-place repacking is not supported");
+  if (E < 1 || H <= 0 || F <= 0) return fail(MOE_ERR_INVALID_ARG, "bad sizes");
+  if (H % 32 || F % 32) return fail(MOE_ERR_UNSUPPORTED, "H and F must be multiples of 32");
+  if (gated && (ilv <= 0 || ilv % 32 || F % ilv))
+    return fail(MOE_ERR_UNSUPPORTED, "ilv must be a multiple of 32 dividing F");
+  const int N1 = gated ? 2 * F : F;
+  const int64_t tiles = (int64_t)E * (N1 / 32) * (H / 32);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  pack_fc1_kernel<<<grid_for(tiles, 16), 256, 0, s>>>(static_cast<const uint16_t*>(src),
+                                                     static_cast<uint16_t*>(dst), E, H, F, N1,
+                                                     gated ? 1 : 0, ilv, inverse ? 1 : 0);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_get_error(const moe_layer_desc_t* d, const void* ws, int32_t* host_code,
+                           moe_stream_t stream) {
+  if (!ws || !host_code) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  (void)d;  // the error word is at offset 0 of every layout
+  cudaError_t e = cudaMemcpyAsync(host_code, ws, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_get_error copy");
+  return MOE_OK;
+}
+
+moe_status_t moe_clear_error(const moe_layer_desc_t* d, void* ws, moe_stream_t stream) {
+  if (!ws) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  (void)d;
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_clear_error memset");
+  return MOE_OK;
+}
+
+int32_t moe_gemm_ctas(const moe_layer_desc_t* desc) {
+  if (!desc) return 0;
+  return gemm_ctas(desc);
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(); }
+
+const char* moe_last_error_string(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,632 @@
+// Persistent grouped GEMM for sm_103a: TMA -> shared-memory ring -> tcgen05.mma (fp32
+// accumulators in tensor memory) -> warp-specialised epilogue, over a device-resident group
+// table (the padded per-expert row offsets), so the host never learns the token counts.
+//
+// [NV-blog] kernel families: (1) GroupGemm + quantise (FC2 fprop, FC1 dgrad, wgrads),
+// (2) GroupGemm + activation (+ quantise/transpose) for FC1, (3) GroupGemm + dActivation
+// (+ quantise/transpose) for FC2 dgrad; the GLU epilogue relies on the repacked W1 so one
+// 256-column tile holds 128 gate and 128 linear columns (GLU-epilogue section, Figure 2);
+// the persistent tile loop over device offsets is the host-sync section's design; the
+// `num_ctas` cap is the configurable SM margin.
+//
+// CTA = 6 warps: warp 0 issues TMA loads, warp 1 owns the TMEM allocation and issues the
+// MMAs (one thread), warps 2..5 drain the accumulator (warp w reads TMEM lanes 32*(w%4)..).
+// Two TMEM accumulators of BN fp32 columns let the epilogue of tile i overlap the mainloop
+// of tile i+1. Tiles are 128 x BN; k-blocks are 64 bf16 (one 128-byte swizzle row).
+//
+// Two tile spaces:
+//   row-grouped (fprop, dgrad): each expert's padded row segment is cut into 128-row tiles;
+//     K is the same for all experts. Output rows beyond the segment end are not stored.
+//   k-grouped (wgrad): every expert has the same M x N output; K is the expert's row segment.
+//     A k-block that crosses the segment end issues only the in-segment 16-row MMA steps
+//     (segments are 32-row aligned); an expert with no rows gets an all-zero tile.
+#include <mutex>
+
+#include "kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int UMMA_K = 16;
+constexpr int kThreads = 192;
+constexpr int kMaxE = 256;
+
+enum { EPI_STORE = 0, EPI_GLU = 1, EPI_DGLU = 2 };
+
+struct GemmArgs {
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  const int32_t* offsets;
+  int E;
+  int R_cap;
+  int M;   // k-grouped: output rows per expert
+  int N;   // output columns
+  int K;   // row-grouped: reduction length
+  void* out;
+  int64_t ldo;
+  int64_t out_estride;
+  void* out2;
+  int64_t ldo2;
+  const float* row_prob;
+  const uint16_t* z;
+  int64_t ldz;
+  float* dprob_part;
+  int nparts;
+  int gated;
+  int ilv;
+  int F;
+  ActDev act;
+  int* err;
+};
+
+template <int BN, int STAGES>
+struct Smem {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int DATA = STAGES * STAGE_BYTES;
+  static constexpr int CTRL = 4096;
+  static constexpr int TOTAL = DATA + CTRL + 1024;  // + alignment slack
+};
+
+struct Ctrl {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int total_tiles;
+  int off[kMaxE + 1];
+  int prefix[kMaxE + 1];
+};
+
+struct TileInfo {
+  int e, m0, n0, kbeg, klen, nkb, row_end;
+};
+
+// ------------------------------------------------------------------ activations (fp32)
+MOE_DEVICE float phi_cdf(float g) { return 0.5f * (1.0f + erff(g * 0.70710678118654752f)); }
+
+MOE_DEVICE float act_fwd(const ActDev& a, float g, float l) {
+  if (a.kind == MOE_ACT_CLAMPED_SWIGLU) {
+    const float gc = fminf(g, a.gate_max);
+    const float lc = fminf(fmaxf(l, a.lin_lo), a.lin_hi);
+    return (lc + a.lin_offset) * gc * sigmoidf_fast(a.beta * gc);
+  }
+  if (a.kind == MOE_ACT_GEGLU) return l * g * phi_cdf(g);
+  return l * g * sigmoidf_fast(a.beta * g);  // SwiGLU
+}
+
+// returns a (unscaled) and writes d_gate, d_lin for the upstream gradient dA
+MOE_DEVICE float act_bwd(const ActDev& a, float g, float l, float dA, float& dg, float& dl) {
+  if (a.kind == MOE_ACT_CLAMPED_SWIGLU) {
+    const float gc = fminf(g, a.gate_max);
+    const float lc = fminf(fmaxf(l, a.lin_lo), a.lin_hi);
+    const float s = sigmoidf_fast(a.beta * gc);
+    const float sw = gc * s;
+    dg = (g <= a.gate_max) ? dA * (lc + a.lin_offset) * s * (1.0f + a.beta * gc * (1.0f - s))
+                           : 0.0f;
+    dl = (l >= a.lin_lo && l <= a.lin_hi) ? dA * sw : 0.0f;
+    return (lc + a.lin_offset) * sw;
+  }
+  if (a.kind == MOE_ACT_GEGLU) {
+    const float P = phi_cdf(g);
+    const float pdf = 0.39894228040143268f * __expf(-0.5f * g * g);
+    dg = dA * l * (P + g * pdf);
+    dl = dA * g * P;
+    return l * g * P;
+  }
+  const float s = sigmoidf_fast(a.beta * g);
+  dg = dA * l * s * (1.0f + a.beta * g * (1.0f - s));
+  dl = dA * g * s;
+  return l * g * s;
+}
+
+MOE_DEVICE void store_bf16x32(void* dst, const float (&v)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    d[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                      pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+}
+MOE_DEVICE void load_bf16x32(const void* src, float (&v)[32]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 w = s[i];
+    v[8 * i + 0] = bf16_lo(w.x); v[8 * i + 1] = bf16_hi(w.x);
+    v[8 * i + 2] = bf16_lo(w.y); v[8 * i + 3] = bf16_hi(w.y);
+    v[8 * i + 4] = bf16_lo(w.z); v[8 * i + 5] = bf16_hi(w.z);
+    v[8 * i + 6] = bf16_lo(w.w); v[8 * i + 7] = bf16_hi(w.w);
+  }
+}
+MOE_DEVICE void store_zero_bf16x32(void* dst) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = make_uint4(0, 0, 0, 0);
+}
+
+template <int BN, bool KG>
+MOE_DEVICE void decode_tile(int tile, const GemmArgs& p, const Ctrl& c, int MT, int NT,
+                            TileInfo& t) {
+  if (!KG) {
+    int lo = 0, hi = p.E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (c.prefix[mid] <= tile) lo = mid; else hi = mid;
+    }
+    const int e = lo;
+    const int local = tile - c.prefix[e];
+    const int seg = c.off[e + 1] - c.off[e];
+    const int mt = (seg + BM - 1) / BM;
+    t.e = e;
+    t.m0 = c.off[e] + (local % mt) * BM;
+    t.n0 = (local / mt) * BN;
+    t.kbeg = 0;
+    t.klen = p.K;
+    t.nkb = p.K / BK;
+    t.row_end = c.off[e + 1];
+  } else {
+    const int per = MT * NT;
+    const int e = tile / per;
+    const int local = tile - e * per;
+    t.e = e;
+    t.m0 = (local % MT) * BM;
+    t.n0 = (local / MT) * BN;
+    t.kbeg = c.off[e];
+    t.klen = c.off[e + 1] - c.off[e];
+    t.nkb = (t.klen + BK - 1) / BK;
+    t.row_end = p.M;
+  }
+}
+
+template <int BN, int STAGES, bool A_MN, bool B_MN, int EPI, bool KG, bool B3D>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
+  using L = Smem<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  Ctrl& c = *reinterpret_cast<Ctrl*>(smem + L::DATA);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort = &c.abort;
+
+  const int NT = (p.N + BN - 1) / BN;
+  const int MT = KG ? (p.M + BM - 1) / BM : 0;
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&c.full[s], 1);
+      mbar_init(&c.empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c.tfull[i], 1);
+      mbar_init(&c.tempty[i], 4);
+    }
+    mbar_init(&c.drain, 1);
+    fence_mbar_init();
+    c.abort = 0;
+    // group table: validate, then tile prefix
+    bool ok = p.E >= 1 && p.E <= kMaxE;
+    int prev = 0;
+    for (int e = 0; ok && e <= p.E; ++e) {
+      const int o = p.offsets[e];
+      if (o < prev || o > p.R_cap || (e == 0 && o != 0)) ok = false;
+      c.off[e] = o;
+      prev = o;
+    }
+    int total = 0;
+    if (ok) {
+      for (int e = 0; e < p.E; ++e) {
+        c.prefix[e] = total;
+        if (KG) total += MT * NT;
+        else total += ((c.off[e + 1] - c.off[e] + BM - 1) / BM) * NT;
+      }
+      c.prefix[p.E] = total;
+    } else {
+      set_error(p.err, MOE_DEVERR_CAPACITY);
+    }
+    c.total_tiles = total;
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA);
+    tma_prefetch_desc(&p.tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&c.tmem_base, 2 * BN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = c.tmem_base;
+  const int total = c.total_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) armed[s] = -1;
+      for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+        TileInfo t;
+        decode_tile<BN, KG>(tile, p, c, MT, NT, t);
+        for (int kb = 0; kb < t.nkb; ++kb) {
+          if (!mbar_wait(&c.empty[stage], phase ^ 1, abort, p.err)) break;
+          uint8_t* sA = smem + stage * L::STAGE_BYTES;
+          uint8_t* sB = sA + L::A_BYTES;
+          uint64_t* bar = &c.full[stage];
+          mbar_arrive_expect_tx(bar, L::STAGE_BYTES);
+#pragma unroll
+          for (int s = 0; s < STAGES; ++s)
+            if (s == stage) armed[s] = (int)phase;
+          const int k0 = t.kbeg + kb * BK;
+          if (!A_MN) {
+            tma_load_2d(sA, &p.tmA, bar, k0, t.m0);
+          } else {
+            tma_load_2d(sA, &p.tmA, bar, t.m0, k0);
+            tma_load_2d(sA + 64 * 128, &p.tmA, bar, t.m0 + 64, k0);
+          }
+          if (!B_MN) {
+            if (B3D) tma_load_3d(sB, &p.tmB, bar, k0, t.n0, t.e);
+            else tma_load_2d(sB, &p.tmB, bar, k0, t.n0);
+          } else {
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i) {
+              if (B3D) tma_load_3d(sB + i * 64 * 128, &p.tmB, bar, t.n0 + 64 * i, k0, t.e);
+              else tma_load_2d(sB + i * 64 * 128, &p.tmB, bar, t.n0 + 64 * i, k0);
+            }
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // let every load this thread issued land before the CTA can exit
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) {
+        if (armed[s] >= 0) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(smem_u32(&c.full[s]), (uint32_t)armed[s]) &&
+                 globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc_i = 0;
+      bool issued_any = false;
+      for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+        TileInfo t;
+        decode_tile<BN, KG>(tile, p, c, MT, NT, t);
+        if (t.nkb == 0) continue;
+        const int acc = acc_i & 1;
+        const uint32_t acc_phase = (acc_i >> 1) & 1;
+        if (!mbar_wait(&c.tempty[acc], acc_phase ^ 1, abort, p.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < t.nkb; ++kb) {
+          if (!mbar_wait(&c.full[stage], phase, abort, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(smem + stage * L::STAGE_BYTES);
+          const uint32_t sB = sA + L::A_BYTES;
+          int nsub = BK / UMMA_K;
+          if (KG) {
+            const int rem = t.klen - kb * BK;
+            if (rem < BK) nsub = (rem + UMMA_K - 1) / UMMA_K;
+          }
+          for (int ks = 0; ks < nsub; ++ks) {
+            const uint64_t ad = A_MN ? smem_desc_sw128(sA + ks * (UMMA_K * 128), 64 * 128, 1024)
+                                     : smem_desc_sw128(sA + ks * (UMMA_K * 2), 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(sB + ks * (UMMA_K * 128), 64 * 128, 1024)
+                                     : smem_desc_sw128(sB + ks * (UMMA_K * 2), 16, 1024);
+            mma_bf16_ss(d_tmem, ad, bd, IDESC, (kb | ks) != 0 ? 1u : 0u);
+          }
+          issued_any = true;
+          mma_commit(&c.empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&c.tfull[acc]);
+        ++acc_i;
+      }
+      // drain: every MMA this thread issued completes before TMEM is released
+      if (issued_any) {
+        mma_commit(&c.drain);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(&c.drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps 2..5
+    const int q = warp & 3;
+    int acc_i = 0;
+    for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+      TileInfo t;
+      decode_tile<BN, KG>(tile, p, c, MT, NT, t);
+      const int row = t.m0 + q * 32 + lane;
+      const bool row_ok = row < t.row_end;
+      if (t.nkb == 0) {
+        // k-grouped tile of an expert with no rows: exact zeros
+        if (row_ok) {
+          uint16_t* o = static_cast<uint16_t*>(p.out) + (int64_t)t.e * p.out_estride +
+                        (int64_t)row * p.ldo;
+          for (int cc = 0; cc < BN && t.n0 + cc < p.N; cc += 32) store_zero_bf16x32(o + t.n0 + cc);
+        }
+        continue;
+      }
+      const int acc = acc_i & 1;
+      const uint32_t acc_phase = (acc_i >> 1) & 1;
+      if (!mbar_wait(&c.tfull[acc], acc_phase, abort, p.err)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      uint32_t r[32];
+      float v[32];
+      if (EPI == EPI_STORE) {
+        uint16_t* o = static_cast<uint16_t*>(p.out) + (KG ? (int64_t)t.e * p.out_estride : 0) +
+                      (int64_t)row * p.ldo + t.n0;
+        for (int cc = 0; cc < BN; cc += 32) {
+          if (t.n0 + cc >= p.N) break;
+          tmem_ld_32x32b_x32(taddr + cc, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          if (row_ok) store_bf16x32(o + cc, v);
+        }
+      } else if (EPI == EPI_GLU) {
+        const float prob = row_ok ? p.row_prob[row] : 0.f;
+        uint16_t* zrow = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo;
+        uint16_t* arow = static_cast<uint16_t*>(p.out2) + (int64_t)row * p.ldo2;
+        if (p.gated) {
+          for (int cc = 0; cc < BN / 2; cc += 32) {
+            const int gcol = (cc / p.ilv) * 2 * p.ilv + (cc % p.ilv);
+            const int lcol = gcol + p.ilv;
+            if (t.n0 + gcol >= p.N) break;
+            uint32_t rl[32];
+            tmem_ld_32x32b_x32(taddr + gcol, r);
+            tmem_ld_32x32b_x32(taddr + lcol, rl);
+            tmem_ld_wait();
+            float g[32], l[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              g[i] = __uint_as_float(r[i]);
+              l[i] = __uint_as_float(rl[i]);
+              v[i] = prob * act_fwd(p.act, g[i], l[i]);
+            }
+            if (row_ok) {
+              store_bf16x32(zrow + t.n0 + gcol, g);
+              store_bf16x32(zrow + t.n0 + lcol, l);
+              store_bf16x32(arow + t.n0 / 2 + cc, v);
+            }
+          }
+        } else {
+          for (int cc = 0; cc < BN; cc += 32) {
+            if (t.n0 + cc >= p.N) break;
+            tmem_ld_32x32b_x32(taddr + cc, r);
+            tmem_ld_wait();
+            float zz[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              zz[i] = __uint_as_float(r[i]);
+              const float rr = fmaxf(zz[i], 0.f);
+              v[i] = prob * rr * rr;
+            }
+            if (row_ok) {
+              store_bf16x32(zrow + t.n0 + cc, zz);
+              store_bf16x32(arow + t.n0 + cc, v);
+            }
+          }
+        }
+      } else {  // EPI_DGLU: accumulator = dA_s over F columns
+        const float prob = row_ok ? p.row_prob[row] : 0.f;
+        float dp = 0.f;
+        const uint16_t* zrow = p.z + (int64_t)row * p.ldz;
+        uint16_t* dzrow = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo;
+        for (int cc = 0; cc < BN; cc += 32) {
+          const int f0 = t.n0 + cc;
+          if (f0 >= p.N) break;
+          tmem_ld_32x32b_x32(taddr + cc, r);
+          tmem_ld_wait();
+          if (!row_ok) continue;
+          if (p.gated) {
+            const int gcol = (f0 / p.ilv) * 2 * p.ilv + (f0 % p.ilv);
+            const int lcol = gcol + p.ilv;
+            float g[32], l[32];
+            load_bf16x32(zrow + gcol, g);
+            load_bf16x32(zrow + lcol, l);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float das = __uint_as_float(r[i]);
+              float dg, dl;
+              const float a = act_bwd(p.act, g[i], l[i], prob * das, dg, dl);
+              dp += das * a;
+              g[i] = dg;
+              l[i] = dl;
+            }
+            store_bf16x32(dzrow + gcol, g);
+            store_bf16x32(dzrow + lcol, l);
+          } else {
+            float zz[32];
+            load_bf16x32(zrow + f0, zz);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float das = __uint_as_float(r[i]);
+              const float rr = fmaxf(zz[i], 0.f);
+              dp += das * rr * rr;
+              zz[i] = prob * das * 2.f * rr;
+            }
+            store_bf16x32(dzrow + f0, zz);
+          }
+        }
+        if (row_ok) p.dprob_part[(int64_t)row * p.nparts + t.n0 / BN] = dp;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.tempty[acc]);
+      ++acc_i;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 2 * BN);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// bf16 tensor map, 128-byte swizzle. dims/box innermost first; strides in bytes for dims 1..
+bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+               const uint64_t* strides, const uint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
+                  reinterpret_cast<const cuuint64_t*>(dims),
+                  reinterpret_cast<const cuuint64_t*>(strides),
+                  reinterpret_cast<const cuuint32_t*>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_in,
+             uint32_t box_out) {
+  uint64_t dims[2] = {inner, outer};
+  uint64_t strides[1] = {inner * 2};
+  uint32_t box[2] = {box_in, box_out};
+  return make_tmap(m, base, 2, dims, strides, box);
+}
+bool tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+             uint32_t b0, uint32_t b1) {
+  uint64_t dims[3] = {d0, d1, d2};
+  uint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  uint32_t box[3] = {b0, b1, 1};
+  return make_tmap(m, base, 3, dims, strides, box);
+}
+
+template <int BN, int STAGES, bool A_MN, bool B_MN, int EPI, bool KG, bool B3D>
+cudaError_t launch_instance(const GemmArgs& a, int grid, cudaStream_t s) {
+  auto kern = grouped_gemm_kernel<BN, STAGES, A_MN, B_MN, EPI, KG, B3D>;
+  constexpr int smem = Smem<BN, STAGES>::TOTAL;
+  static bool configured = false;  // per instantiation; attribute is per-function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  kern<<<grid, kThreads, smem, s>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+constexpr int kBN = 256;
+constexpr int kStages = 4;
+
+}  // namespace
+
+int gemm_bn(int) { return kBN; }
+
+cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
+  GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  a.offsets = p.offsets;
+  a.E = p.E;
+  a.R_cap = (int)p.R_cap;
+  a.gated = p.gated;
+  a.ilv = p.ilv;
+  a.F = p.F;
+  a.act = p.act;
+  a.err = p.err;
+  a.row_prob = p.row_prob;
+  const uint64_t R = (uint64_t)p.R_cap;
+  const int H = p.H, F = p.F, N1 = p.N1, E = p.E;
+  bool ok = true;
+  int grid = p.num_ctas;
+  switch (p.role) {
+    case ROLE_FC1_FPROP:
+      ok &= tmap_2d(&a.tmA, p.x_perm, H, R, 64, BM);
+      ok &= tmap_3d(&a.tmB, p.w1p, H, N1, E, 64, kBN);
+      a.K = H; a.N = N1;
+      a.out = p.out; a.ldo = N1;
+      a.out2 = p.out2; a.ldo2 = F;
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_instance<kBN, kStages, false, false, EPI_GLU, false, true>(a, grid, s);
+    case ROLE_FC2_FPROP:
+      ok &= tmap_2d(&a.tmA, p.a_s, F, R, 64, BM);
+      ok &= tmap_3d(&a.tmB, p.w2, H, F, E, 64, 64);
+      a.K = F; a.N = H;
+      a.out = p.out; a.ldo = H;
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_instance<kBN, kStages, false, true, EPI_STORE, false, true>(a, grid, s);
+    case ROLE_FC2_DGRAD:
+      ok &= tmap_2d(&a.tmA, p.dy_perm, H, R, 64, BM);
+      ok &= tmap_3d(&a.tmB, p.w2, H, F, E, 64, kBN);
+      a.K = H; a.N = F;
+      a.out = p.out; a.ldo = N1;
+      a.z = static_cast<const uint16_t*>(p.z); a.ldz = N1;
+      a.dprob_part = p.dprob_part; a.nparts = (F + kBN - 1) / kBN;
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_instance<kBN, kStages, false, false, EPI_DGLU, false, true>(a, grid, s);
+    case ROLE_FC1_DGRAD:
+      ok &= tmap_2d(&a.tmA, p.dz, N1, R, 64, BM);
+      ok &= tmap_3d(&a.tmB, p.w1p, H, N1, E, 64, 64);
+      a.K = N1; a.N = H;
+      a.out = p.out; a.ldo = H;
+      if (!ok) return cudaErrorInvalidValue;
+      return launch_instance<kBN, kStages, false, true, EPI_STORE, false, true>(a, grid, s);
+    case ROLE_FC2_WGRAD:
+    case ROLE_FC1_WGRAD: {
+      const bool fc2 = p.role == ROLE_FC2_WGRAD;
+      const int M = fc2 ? F : N1;
+      ok &= tmap_2d(&a.tmA, fc2 ? p.a_s : p.dz, M, R, 64, 64);
+      ok &= tmap_2d(&a.tmB, fc2 ? p.dy_perm : p.x_perm, H, R, 64, 64);
+      a.M = M; a.N = H;
+      a.out = p.out; a.ldo = H; a.out_estride = (int64_t)M * H;
+      if (!ok) return cudaErrorInvalidValue;
+      const int64_t tiles = (int64_t)E * ((M + BM - 1) / BM) * ((H + kBN - 1) / kBN);
+      grid = (int)std::min<int64_t>(grid, tiles);
+      return launch_instance<kBN, kStages, true, true, EPI_STORE, true, false>(a, grid, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

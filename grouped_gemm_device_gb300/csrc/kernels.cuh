@@ -1,0 +1,76 @@
+// Declarations shared between the translation units of the library.
+#pragma once
+
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace moe {
+
+// launch accounting (api.cu)
+void count_launch();
+
+// route.cu
+__global__ void route_topk_kernel(const float* logits, int T, int E, int k, int32_t* ids,
+                                  float* probs, int32_t* counts);
+__global__ void assign_rows_kernel(const int32_t* ids, const float* probs, const int32_t* counts,
+                                   int T, int E, int k, int align, int64_t R_cap,
+                                   int32_t* offsets, int32_t* row_of, int32_t* src_of,
+                                   float* row_prob, int* err);
+__global__ void gather_rows_kernel(const uint4* x, const int32_t* src_of, const int32_t* offsets,
+                                   int E, int k, int H8, int64_t R_cap, uint4* out);
+__global__ void combine_rows_kernel(const uint4* in, const int32_t* row_of, int T, int k, int H8,
+                                    uint4* out);
+__global__ void dprob_reduce_kernel(const float* part, int nparts, const int32_t* row_of, int n,
+                                    float* d_probs);
+__global__ void pack_fc1_kernel(const uint16_t* src, uint16_t* dst, int E, int H, int F, int N1,
+                                int gated, int ilv, int inverse);
+
+// mxfp8.cu
+void launch_mxfp8_quantize(const void* in, int64_t M, int64_t N, int rowwise, int colwise,
+                           uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                           int num_sms, cudaStream_t s);
+
+// gemm.cu --------------------------------------------------------------------------------
+struct ActDev {
+  int kind;  // moe_activation_t
+  float beta, gate_max, lin_lo, lin_hi, lin_offset;
+};
+
+enum GemmRole {
+  ROLE_FC1_FPROP = 0,   // Z = X W1 (+ GLU epilogue -> z, a_s)
+  ROLE_FC2_FPROP = 1,   // Y = a_s W2
+  ROLE_FC2_DGRAD = 2,   // dA_s = dY W2^T (+ dGLU epilogue -> dz, partial d_prob)
+  ROLE_FC2_WGRAD = 3,   // dW2_e = a_s^T dY
+  ROLE_FC1_DGRAD = 4,   // dX = dZ W1^T
+  ROLE_FC1_WGRAD = 5    // dW1_e = dZ^T X (stored [N1, H])
+};
+
+struct GemmProblem {
+  int role;
+  int E, H, F, N1;
+  int64_t R_cap;
+  const int32_t* offsets;  // [E+1] device
+  // operands (bf16)
+  const void* x_perm;      // [R_cap, H]
+  const void* w1p;         // [E, N1, H]
+  const void* w2;          // [E, F, H]
+  const void* a_s;         // [R_cap, F]
+  const void* dy_perm;     // [R_cap, H]
+  const void* dz;          // [R_cap, N1]
+  const void* z;           // [R_cap, N1] (saved, dGLU epilogue input)
+  const float* row_prob;   // [R_cap]
+  // outputs
+  void* out;               // role output (z, y_perm, dz, dW2, dx_perm, dW1)
+  void* out2;              // FC1: a_s
+  float* dprob_part;       // FC2 dgrad: [R_cap, nparts]
+  int gated, ilv;
+  ActDev act;
+  int* err;
+  int num_ctas;            // persistent grid size (SMs - margin)
+};
+
+int gemm_bn(int role);
+cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s);
+
+}  // namespace moe

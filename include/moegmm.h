@@ -1,0 +1,218 @@
+/*
+ * moegmm.h - C ABI of the GB300 (sm_103a) fused grouped expert MLP of a Mixture-of-Experts
+ * layer: routing + permutation, fused FC1 -> GLU -> probability scale -> FC2 forward, the
+ * matching backward, and the standalone MXFP8 quantiser.
+ *
+ * Sources (by page title and section):
+ *   [NV-blog] NVIDIA technical blog "Boosting MoE Training Throughput with Advanced Fusion
+ *             Kernels" (zh-cn 借助高级融合内核提高 MoE 训练吞吐量): the three fused kernel
+ *             families (GroupGemm + quantise; GroupGemm + activation + quantise/transpose;
+ *             GroupGemm + dActivation + quantise/transpose), the SwiGLU equation and GLU weight
+ *             repacking (GLU-epilogue section, Figure 2), device-resident per-group token
+ *             counts (host-sync section), fused MXFP8 quantisation, dynamic scheduling and the
+ *             configurable SM margin (kernel-to-pretraining section).
+ *   [TE-MoE]  "NVIDIA Transformer Engine 优化 MoE 生物基础模型训练" (Transformer Engine MoE
+ *             article): GroupedLinear with per-expert token counts, the per-expert loop with
+ *             index_add (Challenge 1), MXFP8 format (Challenge 2, Figure 3), ScaledSwiGLU and
+ *             the fused GroupedLinear -> ScaledSwiGLU -> GroupedLinear op (Challenge 3, Fig. 4).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers unless a name says host. Layouts are row-major.
+ *     bf16 is passed as void* (2-byte IEEE bfloat16), e4m3 and e8m0 as uint8_t.
+ *   - The caller owns every buffer, including the workspace `ws` (size from
+ *     moe_workspace_size). No entry point allocates device memory or synchronises the host;
+ *     all work is enqueued on `stream` (NULL = legacy default stream), so whole layer steps can
+ *     be captured in a CUDA graph. Token counts and offsets never leave the device.
+ *   - Host-side argument checks run before any launch and return MOE_ERR_INVALID_ARG or
+ *     MOE_ERR_UNSUPPORTED with nothing enqueued. A CUDA launch error returns MOE_ERR_CUDA.
+ *     Conditions only the device can see (routing capacity overflow, a bounded wait that timed
+ *     out inside a kernel) set a sticky error word in the workspace, read by moe_get_error.
+ *     No kernel traps, asserts or spins without a bound.
+ *   - moe_last_error_string() describes the most recent host-side failure of this thread.
+ */
+#ifndef MOEGMM_H_
+#define MOEGMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers (same underlying type). */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer, k > E, ... */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. H not a multiple of 64)   */
+  MOE_ERR_WORKSPACE = 3,    /* ws_bytes smaller than moe_workspace_size                  */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed                       */
+  MOE_ERR_DEVICE = 5        /* moe_get_error found a device-side error code               */
+} moe_status_t;
+
+/* Device error word codes (sticky until moe_clear_error). */
+#define MOE_DEVERR_NONE 0
+#define MOE_DEVERR_CAPACITY 1   /* routed rows exceeded the static capacity R_cap        */
+#define MOE_DEVERR_TIMEOUT 2    /* a bounded barrier wait in a GEMM kernel gave up       */
+#define MOE_DEVERR_BAD_ID 3     /* an expert id outside [0, E)                            */
+
+typedef enum { MOE_PREC_BF16 = 0, MOE_PREC_MXFP8 = 1 } moe_precision_t;
+
+/* Activations of [NV-blog] (SwiGLU, GeGLU, sReLU, "with clamp and scale options"):
+ *   SWIGLU          a = lin * g * sigmoid(beta*g)                  (SwiGLU equation, b=c=0)
+ *   CLAMPED_SWIGLU  g' = min(g, gate_max), l' = clamp(lin, lin_lo, lin_hi),
+ *                   a = (l' + lin_offset) * g' * sigmoid(beta*g')
+ *   GEGLU           a = lin * g * Phi(g)                           (exact erf GELU)
+ *   SRELU           a = max(z, 0)^2, non-gated: FC1 has F (not 2F) output columns
+ * The gradient passes a clamp at equality (the clamp is active strictly beyond a limit). */
+typedef enum {
+  MOE_ACT_SWIGLU = 0,
+  MOE_ACT_CLAMPED_SWIGLU = 1,
+  MOE_ACT_GEGLU = 2,
+  MOE_ACT_SRELU = 3
+} moe_activation_t;
+
+/* Static description of one layer. Capacities are fixed here so that every call has the
+ * same launch shapes (graph-capturable); the per-call token count T must be <= T_max. */
+typedef struct {
+  int32_t E;          /* experts (1..256)                                                */
+  int32_t k;          /* experts per token (1..min(E,8))                                 */
+  int32_t H;          /* hidden size, multiple of 64                                     */
+  int32_t F;          /* expert FFN width, multiple of 64                                */
+  int32_t T_max;      /* token capacity                                                  */
+  int32_t precision;  /* moe_precision_t                                                 */
+  int32_t activation; /* moe_activation_t                                                */
+  float beta;         /* Swish beta (1.0 SwiGLU, 1.702 clamped GPT-OSS form)             */
+  float gate_max;     /* clamped SwiGLU: upper clamp of the gate                         */
+  float lin_lo;       /* clamped SwiGLU: lower clamp of the linear half                  */
+  float lin_hi;       /* clamped SwiGLU: upper clamp of the linear half                  */
+  float lin_offset;   /* clamped SwiGLU: added to the clamped linear half                */
+  int32_t sm_margin;  /* SMs left free for concurrent kernels ([NV-blog] cluster margin) */
+  int32_t ilv;        /* gate/linear interleave block of the packed W1 (32, 64 or 128)   */
+  int32_t align;      /* expert segment alignment in rows; must be 32                    */
+} moe_layer_desc_t;
+
+/* Byte offsets (from ws) of the intermediates that live in the workspace, for inspection
+ * and tests. Offsets that do not apply to the layer's precision are SIZE_MAX. R_cap =
+ * T_max*k + E*(align-1) rows. All row-indexed buffers use the permuted row order:
+ * expert ascending, token ascending within an expert, each expert's segment starting at a
+ * multiple of `align`; padding rows are zero and have probability 0. */
+typedef struct {
+  size_t total;          /* == moe_workspace_size                                        */
+  int64_t R_cap;         /* row capacity                                                 */
+  size_t err;            /* int32 device error word                                      */
+  size_t offsets;        /* int32 [E+1] padded segment starts; offsets[E] = rows in use  */
+  size_t row_of;         /* int32 [T_max*k] row of (token t, slot j) at t*k+j            */
+  size_t src_of;         /* int32 [R_cap] t*k+j of a row, -1 for padding                 */
+  size_t row_prob;       /* fp32 [R_cap] routing probability of a row, 0 for padding     */
+  size_t x_perm;         /* bf16 [R_cap, H] gathered tokens                              */
+  size_t z;              /* bf16 [R_cap, N1] FC1 output saved for backward (packed cols) */
+  size_t a_s;            /* bf16 [R_cap, F] p * act(z), the FC2 input                    */
+  size_t y_perm;         /* bf16 [R_cap, H] FC2 output before combine (shared with dx_perm) */
+  size_t dy_perm;        /* bf16 [R_cap, H] gathered upstream gradient                   */
+  size_t dz;             /* bf16 [R_cap, N1] gradient of z (packed cols)                 */
+  size_t dx_perm;        /* bf16 [R_cap, H] FC1 dgrad output before combine              */
+  size_t dprob_part;     /* fp32 [R_cap, ceil(F/128)] per-column-tile partial d_prob     */
+  size_t mx_base;        /* start of the MXFP8 operand copies (MXFP8 layers only)        */
+} moe_ws_layout_t;
+
+/* Workspace bytes for a layer (0 if the description is invalid). */
+size_t moe_workspace_size(const moe_layer_desc_t *desc);
+/* Fill *out with the workspace layout. */
+moe_status_t moe_workspace_layout(const moe_layer_desc_t *desc, moe_ws_layout_t *out);
+
+/* Route + permute ([TE-MoE] Figure 1 top-k router; [NV-blog] host-sync section: per-group
+ * token counts stay in device memory).
+ *   logits     fp32 [T, E]   router logits
+ *   x          bf16 [T, H]   tokens
+ *   topk_ids   int32 [T, k]  out: experts by descending logit, ties to the lower index
+ *   topk_probs fp32 [T, k]   out: softmax over the k chosen logits
+ *   counts     int32 [E]     out: tokens routed to each expert
+ * Writes offsets, row_of, src_of, row_prob and x_perm (and, for MXFP8 layers, the MXFP8
+ * row-wise and column-wise copies of x_perm) into ws. T in [0, T_max]. */
+moe_status_t moe_route_permute(const moe_layer_desc_t *desc, int32_t T, const float *logits,
+                               const void *x, int32_t *topk_ids, float *topk_probs,
+                               int32_t *counts, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Fused grouped MLP forward ([NV-blog] kernel families 1 and 2, Figure 1; [TE-MoE]
+ * GroupedLinear -> ScaledSwiGLU -> GroupedLinear):
+ *   Z = X_e W1_e (FC1, grouped over experts from the device offsets), a = act(Z),
+ *   a_s = p * a, Y_e = a_s W2_e (FC2), y[t] = sum_j Y[row_of[t,j]].
+ *   w1_packed bf16 [E, N1, H]  FC1 weight, N1 = 2F (gated) or F (sReLU), rows in the packed
+ *                              order of moe_pack_fc1_weight (gate/linear blocks interleaved)
+ *   w2        bf16 [E, F, H]   FC2 weight (logical [F, H] per expert)
+ *   y         bf16 [T, H]      out
+ * Requires a preceding moe_route_permute on the same ws. Saves z and a_s in ws for the
+ * backward. MXFP8 layers also quantise both weights (both directions) into ws first. */
+moe_status_t moe_grouped_mlp_fwd(const moe_layer_desc_t *desc, int32_t T, const void *w1_packed,
+                                 const void *w2, void *y, void *ws, size_t ws_bytes,
+                                 moe_stream_t stream);
+
+/* Fused grouped MLP backward ([NV-blog] kernel family 3: FC2 dgrad + dActivation +
+ * quantise/transpose; unfused weight-gradient GEMMs, Figure 1):
+ *   dA_s = dY W2^T;  d_prob = sum_f dA_s * a;  dA = p * dA_s;  dZ = dact(Z, dA);
+ *   dW2_e = a_s^T dY_e;  dW1_e = X_e^T dZ_e;  dX = dZ W1^T;  dx[t] = sum_j dX[row_of[t,j]].
+ *   dy         bf16 [T, H]       upstream gradient of y
+ *   dx         bf16 [T, H]       out
+ *   dw1_packed bf16 [E, N1, H]   out, same packed row order as w1_packed (an expert with no
+ *                                tokens gets exact zeros)
+ *   dw2        bf16 [E, F, H]    out
+ *   d_probs    fp32 [T, k]       out, gradient of topk_probs
+ * Requires the forward's ws contents. */
+moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t *desc, int32_t T, const void *dy,
+                                 const void *w1_packed, const void *w2, void *dx,
+                                 void *dw1_packed, void *dw2, float *d_probs, void *ws,
+                                 size_t ws_bytes, moe_stream_t stream);
+
+/* Standalone MXFP8 quantiser ([TE-MoE] Challenge 2, Figure 3: E4M3 elements with one E8M0
+ * scale per 32 contiguous values):
+ *   scale exponent e = clamp(floor(log2(amax)) - 8, -127, 127) (e = -127 when amax = 0),
+ *   scale byte e + 127, q = E4M3(v / 2^e) rounded to nearest even, saturating at +-448.
+ *   in      bf16 [M, N]
+ *   rowwise:  q_row  e4m3 [M, N]       blocks of 32 along N; s_row e8m0 [M, N/32]
+ *   colwise:  q_col  e4m3 [N, M]       blocks of 32 along M, stored transposed;
+ *             s_col  e8m0 [N, M/32]    (row groups that start at multiples of 32 rows, as the
+ *                                      permuted expert segments do, restart blocks for free)
+ * N must be a multiple of 32 for rowwise, M a multiple of 32 for colwise; the pointers of
+ * an unused direction may be NULL. Bit-exact: the result does not depend on the launch. */
+moe_status_t mxfp8_quantize(const void *in, int64_t M, int64_t N, int32_t rowwise,
+                            int32_t colwise, uint8_t *q_row, uint8_t *s_row, uint8_t *q_col,
+                            uint8_t *s_col, moe_stream_t stream);
+
+/* GLU weight repacking ([NV-blog] GLU-epilogue section and Figure 2: the gate and linear
+ * columns are repacked so one output tile holds half a tile of each; done once, before
+ * training or at checkpoint load).
+ *   forward (inverse = 0): w1_logical bf16 [E, H, N1] -> w1_packed bf16 [E, N1, H]
+ *   inverse (inverse = 1): w1_packed -> w1_logical
+ * Gated (N1 = 2F): packed row p belongs to block b = p / ilv; even blocks are gate columns
+ * (b/2)*ilv + p%ilv, odd blocks the linear columns F + (b/2)*ilv + p%ilv. sReLU (N1 = F):
+ * packed = transpose. ilv must be a multiple of 32 that divides F. */
+moe_status_t moe_pack_fc1_weight(const void *w1_src, void *w1_dst, int32_t E, int32_t H,
+                                 int32_t F, int32_t gated, int32_t ilv, int32_t inverse,
+                                 moe_stream_t stream);
+
+/* Enqueue a copy of the device error word into *host_code (pinned or pageable host int);
+ * the value is valid once the stream has been synchronised. */
+moe_status_t moe_get_error(const moe_layer_desc_t *desc, const void *ws, int32_t *host_code,
+                           moe_stream_t stream);
+/* Enqueue a reset of the device error word to MOE_DEVERR_NONE. */
+moe_status_t moe_clear_error(const moe_layer_desc_t *desc, void *ws, moe_stream_t stream);
+
+/* Number of SMs the persistent GEMM uses on the current device for this description
+ * (device SM count minus sm_margin, at least 1). */
+int32_t moe_gemm_ctas(const moe_layer_desc_t *desc);
+
+/* Kernels this library enqueued on any stream since load (a monotonically increasing
+ * host-side counter, for launch accounting). */
+uint64_t moe_launch_count(void);
+
+/* Human-readable message for the last host-side error of the calling thread. */
+const char *moe_last_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOEGMM_H_ */

@@ -1,0 +1,442 @@
+"""Benchmark of the fused grouped expert MLP (route + forward + backward) on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one batch of synthetic tokens: route + permute,
+FC1 + GLU + prob scale, FC2, combine, dY gather, FC2 dgrad + dGLU, FC2 wgrad, FC1 dgrad,
+dx combine, FC1 wgrad. The default workload is the Mixtral-8x7B-shaped BF16 layer
+(T=8192, E=8, top-2, H=4096, F=14336, SwiGLU). Inputs are resident in HBM before timing;
+every step reads ~2.8 GB of weights and writes ~2.8 GB of weight gradients, far above the
+129 MB L2, so no explicit flush is needed. Prints one JSON line (rank 0).
+
+Multi-GPU: the layer runs as independent replicas, one per rank (no data-path collective);
+`value` is the sum over ranks of the work divided by the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same workload on the
+host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from grouped_gemm_device_gb300 import synth  # noqa: E402
+
+METRIC = "grouped-MLP fwd+bwd TFLOPS & tokens/s at 1 GB300; % of tensor-core peak"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="mixtral_bf16", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sm-margin", type=int, default=0)
+    ap.add_argument("--tokens", type=int, default=0, help="override T (profiling runs)")
+    ap.add_argument("--experts", type=int, default=0, help="override E (profiling runs)")
+    return ap.parse_args()
+
+
+def config_of(args):
+    cfg = synth.CONFIGS[args.config]
+    if args.tokens:
+        cfg = cfg.with_(T=args.tokens, name=cfg.name + f"_T{args.tokens}")
+    if args.experts:
+        cfg = cfg.with_(E=args.experts, k=min(cfg.k, args.experts),
+                        name=cfg.name + f"_E{args.experts}")
+    return cfg
+
+
+def workload_name(cfg) -> str:
+    return (f"{cfg.name}: T={cfg.T} E={cfg.E} top-{cfg.k} H={cfg.H} F={cfg.F} "
+            f"{cfg.activation} {cfg.precision}")
+
+
+def gemm_flops(cfg):
+    R = cfg.R
+    H, F, N1 = cfg.H, cfg.F, cfg.N1
+    return {
+        "gemm_fc1_fprop": 2.0 * R * H * N1, "gemm_fc2_fprop": 2.0 * R * F * H,
+        "gemm_fc2_dgrad": 2.0 * R * H * F, "gemm_fc2_wgrad": 2.0 * R * F * H,
+        "gemm_fc1_dgrad": 2.0 * R * N1 * H, "gemm_fc1_wgrad": 2.0 * R * H * N1,
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------------------- distributed
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(v: float, ws: int) -> float:
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if re.match(r"^[\d.]+$", r[1])]
+        mx = [float(r[2]) for r in rows if re.match(r"^[\d.]+$", r[2])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------- inputs
+def host_inputs(cfg):
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+        w1 = list(ex.map(lambda e: synth.gen_w1_expert(cfg, e), range(cfg.E)))
+        w2 = list(ex.map(lambda e: synth.gen_w2_expert(cfg, e), range(cfg.E)))
+    return dict(logits=synth.gen_logits(cfg), x=synth.gen_x(cfg), dy=synth.gen_dy(cfg), w1=w1,
+                w2=w2)
+
+
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on the
+    current kernel source (the summary records the sha256 of gemm.cu it was measured on)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_ncu.txt")
+    if not os.path.exists(path):
+        return None
+    src = os.path.join(ROOT, "grouped_gemm_device_gb300", "csrc", "gemm.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    txt = open(path).read()
+    m_sha = re.search(r"gemm\.cu sha256\[:16\]:\s*(\w+)", txt)
+    m_b = re.search(r"dram bytes per launch \(full workload\):\s*([\d.eE+]+)", txt)
+    if not m_sha or not m_b or m_sha.group(1) != sha:
+        return None
+    return float(m_b.group(1))
+
+
+# ------------------------------------------------------------------------- CPU oracle
+def oracle_sample(cfg, rows: int, inputs=None):
+    """fp64 oracle forward+backward of expert 0 on `rows` of its routed tokens. Returns
+    (seconds, flops, description); weights are converted outside the timed part."""
+    from oracle import moe as om
+    lg = inputs["logits"] if inputs else synth.gen_logits(cfg)
+    ids, probs = om.route(lg, cfg.k)
+    tok, slot = np.nonzero(ids == 0)
+    tok, slot = tok[:rows], slot[:rows]
+    xb = inputs["x"] if inputs else synth.gen_x(cfg)
+    dyb = inputs["dy"] if inputs else synth.gen_dy(cfg)
+    w1b = inputs["w1"][0] if inputs else synth.gen_w1_expert(cfg, 0)
+    w2b = inputs["w2"][0] if inputs else synth.gen_w2_expert(cfg, 0)
+    X, dY = om.bf16_to_f64(xb[tok]), om.bf16_to_f64(dyb[tok])
+    W1, W2 = om.bf16_to_f64(w1b), om.bf16_to_f64(w2b)
+    p = probs[tok, slot]
+    act = om.ActParams(cfg.activation, cfg.beta, cfg.gate_max, cfg.lin_lo, cfg.lin_hi,
+                       cfg.lin_offset)
+    mx = cfg.precision == "mxfp8"
+    t0 = time.perf_counter()
+    Z, a, a_s, Y = om.expert_forward(X, W1, W2, p, act, mx)
+    om.expert_backward(X, W1, W2, p, Z, a, a_s, dY, act, mx)
+    dt = time.perf_counter() - t0
+    n = len(tok)
+    flops = 3.0 * (2.0 * n * cfg.H * cfg.N1 + 2.0 * n * cfg.F * cfg.H)
+    desc = (f"oracle fp64 fwd+bwd of expert 0 on {n} routed tokens of {cfg.name} "
+            f"({flops / 1e9:.0f} GFLOP)")
+    return dt, flops, desc, n
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args):
+    ws, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return
+    cfg = config_of(args)
+    inputs = {"logits": synth.gen_logits(cfg), "x": synth.gen_x(cfg), "dy": synth.gen_dy(cfg),
+              "w1": [synth.gen_w1_expert(cfg, 0)], "w2": [synth.gen_w2_expert(cfg, 0)]}
+    rows = 128
+    for _ in range(args.warmup):
+        oracle_sample(cfg, 32, inputs)
+    tot_t = tot_f = 0.0
+    desc = ""
+    tokens = 0
+    for _ in range(args.steps):
+        dt, fl, desc, n = oracle_sample(cfg, rows, inputs)
+        tot_t += dt
+        tot_f += fl
+        tokens += n
+    value = tot_f / tot_t / 1e12
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(cfg), "sample": desc},
+        "tokens_per_s": tokens / tot_t,
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {desc}"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------- our arm
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+
+    import grouped_gemm_device_gb300 as g
+    from grouped_gemm_device_gb300 import build as gbuild
+
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    if rank == 0:
+        gbuild.build()
+    barrier(world)
+    g.load()
+    cfg = config_of(args)
+    if cfg.precision != "bf16":
+        raise SystemExit(f"config {cfg.name}: only the BF16 path is built in this version")
+    dev = torch.device("cuda", local)
+    t_gen = time.time()
+    hin = host_inputs(cfg)
+    t_gen = time.time() - t_gen
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    desc = g.desc_from_config(cfg, sm_margin=args.sm_margin)
+    layer = g.MoELayer(desc, dev)
+    w1_log = torch.stack([bf(w) for w in hin["w1"]]).to(dev)
+    w1p = g.pack_w1(w1_log, gated=cfg.gated, ilv=cfg.ilv)
+    del w1_log
+    w2 = torch.stack([bf(w) for w in hin["w2"]]).to(dev)
+    logits = torch.from_numpy(hin["logits"]).to(dev)
+    x = bf(hin["x"]).to(dev)
+    dy = bf(hin["dy"]).to(dev)
+    T = cfg.T
+
+    def step():
+        layer.route_permute(logits, x, T)
+        layer.forward(w1p, w2, T)
+        layer.backward(dy, w1p, w2, T)
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0, "device error during warm-up"
+
+    per_step_launches = 13
+    tl = g.Timeline(min(4096, args.steps * per_step_launches + 16))
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    n0 = g.moe_launch_count()
+    tl.begin()
+    ev0.record()
+    for _ in range(args.steps):
+        step()
+    ev1.record()
+    torch.cuda.synchronize()
+    n_rec = tl.end()
+    launches = g.moe_launch_count() - n0
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms_max = allreduce_max(ms, world)
+    assert layer.device_error() == 0, "device error during timing"
+
+    flops = cfg.flops_fwd_bwd()
+    value = flops * world / (ms_max / 1e3) / 1e12
+    peaks, peak_src = load_peaks()
+
+    # per-kernel durations from the launch timeline
+    per = {}
+    for name, dur in tl.durations(ev0):
+        per.setdefault(name, []).append(dur)
+    kernel_ms = {k: sum(v) / len(v) for k, v in per.items()}
+    gf = gemm_flops(cfg)
+    dom = max(gf, key=lambda k: sum(per.get(k, [0.0])))
+    dom_ms = kernel_ms[dom]
+    achieved = gf[dom] / (dom_ms / 1e3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", 1700.0)
+    traffic = traffic_for(dom, cfg.name)
+    gemm_total_ms = sum(kernel_ms[k] for k in gf if k in kernel_ms)
+
+    # end to end through the C ABI with host buffers: pinned H2D of the step's inputs and
+    # D2H of its results inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        h_logits = torch.from_numpy(hin["logits"]).pin_memory()
+        h_x = bf(hin["x"]).pin_memory()
+        h_dy = bf(hin["dy"]).pin_memory()
+        h_y = torch.empty(T, cfg.H, dtype=torch.bfloat16).pin_memory()
+        h_dx = torch.empty(T, cfg.H, dtype=torch.bfloat16).pin_memory()
+        h_dp = torch.empty(T, cfg.k, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            logits.copy_(h_logits, non_blocking=True)
+            x.copy_(h_x, non_blocking=True)
+            dy.copy_(h_dy, non_blocking=True)
+            step()
+            h_y.copy_(layer.y[:T], non_blocking=True)
+            h_dx.copy_(layer.dx[:T], non_blocking=True)
+            h_dp.copy_(layer.d_probs[:T], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        k_e2e = max(10, args.steps // 4)
+        e0.record()
+        for _ in range(k_e2e):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        ms_e2e = allreduce_max(e0.elapsed_time(e1) / k_e2e, world)
+        bi = h_logits.numel() * 4 + h_x.numel() * 2 + h_dy.numel() * 2
+        bo = h_y.numel() * 2 + h_dx.numel() * 2 + h_dp.numel() * 4
+        e2e = {"value": flops * world / (ms_e2e / 1e3) / 1e12, "unit": "TFLOPS",
+               "ms_per_step": ms_e2e, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+               "tokens_per_s": T * world / (ms_e2e / 1e3)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        dt, fl, sdesc, _ = oracle_sample(cfg, 512, hin)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOPS", "cores": blas_threads(),
+               "kind": "oracle", "sample": sdesc, "seconds": dt,
+               "tokens_per_s_equiv": (fl / dt) / (flops / T)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": workload_name(cfg), "parallelism": f"replicas x{world}",
+                       "l2": "no flush: each step streams ~5.6 GB of weights and weight "
+                             "gradients, > 129 MB L2", "sm_margin": args.sm_margin,
+                       "flops_per_step": flops},
+            "tokens_per_s": cfg.T * world / (ms_max / 1e3),
+            "pct_tensor_peak": {"value": 100 * value / world / peak, "peak_tflops": peak,
+                                "peak_kind": f"bf16_tflops_sustained ({peak_src})"},
+            "gpu_launches": int(launches),
+            "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                         "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+                         "flops_per_launch": gf[dom], "ms_per_launch": dom_ms},
+            "kernels_ms": {k: round(v, 4) for k, v in sorted(kernel_ms.items())},
+            "gemm_share": gemm_total_ms / ms,
+            "timeline_events": n_rec,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "input_gen_s": round(t_gen, 1),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

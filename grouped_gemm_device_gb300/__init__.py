@@ -20,7 +20,11 @@ PREC = {"bf16": 0, "mxfp8": 1}
 ACT = {"swiglu": 0, "clamped_swiglu": 1, "geglu": 2, "srelu": 3}
 DEVERR = {0: "none", 1: "capacity", 2: "timeout", 3: "bad_id"}
 
-EXPORTS = ("moe_workspace_size", "moe_workspace_layout", "moe_route_permute",
+KERNEL_NAMES = ("route_topk", "assign_rows", "gather_x", "gemm_fc1_fprop", "gemm_fc2_fprop",
+                "combine_y", "gather_dy", "gemm_fc2_dgrad", "dprob_reduce", "gemm_fc2_wgrad",
+                "gemm_fc1_dgrad", "combine_dx", "gemm_fc1_wgrad", "mxfp8_quantize", "pack_fc1")
+
+EXPORTS = ("moe_timeline_begin", "moe_timeline_end", "moe_workspace_size", "moe_workspace_layout", "moe_route_permute",
            "moe_grouped_mlp_fwd", "moe_grouped_mlp_bwd", "mxfp8_quantize", "moe_pack_fc1_weight",
            "moe_get_error", "moe_clear_error", "moe_gemm_ctas", "moe_launch_count",
            "moe_last_error_string")
@@ -75,6 +79,8 @@ def load():
         "moe_gemm_ctas": (_I32, [_DP]),
         "moe_launch_count": (ctypes.c_uint64, []),
         "moe_last_error_string": (ctypes.c_char_p, []),
+        "moe_timeline_begin": (_I32, [ctypes.POINTER(_P), _I32]),
+        "moe_timeline_end": (_I32, [ctypes.POINTER(_I32)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -189,6 +195,39 @@ def moe_gemm_ctas(desc) -> int:
 
 def moe_launch_count() -> int:
     return int(load().moe_launch_count())
+
+
+class Timeline:
+    """Records a CUDA event after every library kernel launch (moe_timeline_begin/end) and
+    turns consecutive event pairs into per-kernel durations."""
+
+    def __init__(self, capacity: int):
+        import torch
+        self.capacity = capacity
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(capacity)]
+        for e in self.events:           # torch creates events lazily: force creation
+            e.record()
+        torch.cuda.synchronize()
+        self._handles = (_P * capacity)(*[e.cuda_event for e in self.events])
+        self.ids = []
+
+    def begin(self):
+        _check(load().moe_timeline_begin(self._handles, self.capacity))
+
+    def end(self) -> int:
+        buf = (_I32 * self.capacity)()
+        n = load().moe_timeline_end(buf)
+        self.ids = list(buf[:n])
+        return n
+
+    def durations(self, start_event):
+        """[(kernel_name, ms)] for each recorded launch, after a synchronize."""
+        out = []
+        prev = start_event
+        for i, kid in enumerate(self.ids):
+            out.append((KERNEL_NAMES[kid], prev.elapsed_time(self.events[i])))
+            prev = self.events[i]
+        return out
 
 
 # ------------------------------------------------------------------ buffer plumbing

@@ -13,7 +13,18 @@
 namespace moe {
 
 static std::atomic<uint64_t> g_launches{0};
-void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+static cudaEvent_t* g_tl_events = nullptr;
+static int g_tl_cap = 0;
+static int g_tl_n = 0;
+static int g_tl_ids[4096];
+
+void count_launch(cudaStream_t s, int kid) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (g_tl_events && g_tl_n < g_tl_cap) {
+    cudaEventRecord(g_tl_events[g_tl_n], s);
+    g_tl_ids[g_tl_n++] = kid;
+  }
+}
 
 static thread_local std::string g_last_error;
 
@@ -214,15 +225,15 @@ moe_status_t moe_route_permute(const moe_layer_desc_t* d, int32_t T, const float
   if (T > 0) {
     route_topk_kernel<<<grid_for((T + 7) / 8, 8), 256, 0, s>>>(logits, T, d->E, d->k, topk_ids,
                                                                  topk_probs, counts);
-    count_launch();
+    count_launch(s, MOE_K_ROUTE_TOPK);
   }
   assign_rows_kernel<<<d->E, 1024, 0, s>>>(topk_ids, topk_probs, counts, T, d->E, d->k, d->align,
                                            w.L.R_cap, offsets, row_of, src_of, row_prob, err);
-  count_launch();
+  count_launch(s, MOE_K_ASSIGN_ROWS);
   gather_rows_kernel<<<grid_for(w.L.R_cap, 8), 256, 0, s>>>(
       static_cast<const uint4*>(x), src_of, offsets, d->E, d->k, d->H / 8, w.L.R_cap,
       w.at<uint4>(w.L.x_perm));
-  count_launch();
+  count_launch(s, MOE_K_GATHER_X);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "route_permute launch");
   return MOE_OK;
@@ -258,7 +269,7 @@ moe_status_t moe_grouped_mlp_fwd(const moe_layer_desc_t* d, int32_t T, const voi
     combine_rows_kernel<<<grid_for(T, 8), 256, 0, s>>>(w.at<uint4>(w.L.y_perm),
                                                       w.at<int32_t>(w.L.row_of), T, d->k,
                                                       d->H / 8, static_cast<uint4*>(y));
-    count_launch();
+    count_launch(s, MOE_K_COMBINE_Y);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "fwd launch");
@@ -289,7 +300,7 @@ moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t* d, int32_t T, const voi
   gather_rows_kernel<<<grid_for(w.L.R_cap, 8), 256, 0, s>>>(
       static_cast<const uint4*>(dy), w.at<int32_t>(w.L.src_of), w.at<int32_t>(w.L.offsets), d->E,
       d->k, d->H / 8, w.L.R_cap, w.at<uint4>(w.L.dy_perm));
-  count_launch();
+  count_launch(s, MOE_K_GATHER_DY);
   // FC2 dgrad + dActivation (kernel family 3)
   p.role = ROLE_FC2_DGRAD;
   p.out = w.at<void>(w.L.dz);
@@ -300,7 +311,7 @@ moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t* d, int32_t T, const voi
     const int n = T * d->k;
     dprob_reduce_kernel<<<grid_for((n + 255) / 256, 4), 256, 0, s>>>(
         w.at<float>(w.L.dprob_part), nparts, row_of, n, d_probs);
-    count_launch();
+    count_launch(s, MOE_K_DPROB_REDUCE);
   }
   // FC2 wgrad
   p.role = ROLE_FC2_WGRAD;
@@ -313,7 +324,7 @@ moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t* d, int32_t T, const voi
   if (T > 0) {
     combine_rows_kernel<<<grid_for(T, 8), 256, 0, s>>>(w.at<uint4>(w.L.dx_perm), row_of, T,
                                                       d->k, d->H / 8, static_cast<uint4*>(dx));
-    count_launch();
+    count_launch(s, MOE_K_COMBINE_DX);
   }
   // FC1 wgrad
   p.role = ROLE_FC1_WGRAD;
@@ -360,7 +371,7 @@ moe_status_t moe_pack_fc1_weight(const void* src, void* dst, int32_t E, int32_t 
   pack_fc1_kernel<<<grid_for(tiles, 16), 256, 0, s>>>(static_cast<const uint16_t*>(src),
                                                      static_cast<uint16_t*>(dst), E, H, F, N1,
                                                      gated ? 1 : 0, ilv, inverse ? 1 : 0);
-  count_launch();
+  count_launch(s, MOE_K_PACK_FC1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "pack launch");
   return MOE_OK;
@@ -390,6 +401,25 @@ int32_t moe_gemm_ctas(const moe_layer_desc_t* desc) {
 }
 
 uint64_t moe_launch_count(void) { return g_launches.load(); }
+
+moe_status_t moe_timeline_begin(void* const* events, int32_t capacity) {
+  if (!events || capacity <= 0) return fail(MOE_ERR_INVALID_ARG, "timeline needs events");
+  if (capacity > 4096) return fail(MOE_ERR_UNSUPPORTED, "timeline capacity above 4096");
+  g_tl_events = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(events));
+  g_tl_cap = capacity;
+  g_tl_n = 0;
+  return MOE_OK;
+}
+
+int32_t moe_timeline_end(int32_t* kernel_ids) {
+  const int n = g_tl_n;
+  if (kernel_ids)
+    for (int i = 0; i < n; ++i) kernel_ids[i] = g_tl_ids[i];
+  g_tl_events = nullptr;
+  g_tl_cap = 0;
+  g_tl_n = 0;
+  return n;
+}
 
 const char* moe_last_error_string(void) { return g_last_error.c_str(); }
 

@@ -543,7 +543,7 @@ bool tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_
 }
 
 template <int BN, int STAGES, bool A_MN, bool B_MN, int EPI, bool KG, bool B3D>
-cudaError_t launch_instance(const GemmArgs& a, int grid, cudaStream_t s) {
+cudaError_t launch_instance(const GemmArgs& a, int grid, cudaStream_t s, int kid) {
   auto kern = grouped_gemm_kernel<BN, STAGES, A_MN, B_MN, EPI, KG, B3D>;
   constexpr int smem = Smem<BN, STAGES>::TOTAL;
   static bool configured = false;  // per instantiation; attribute is per-function
@@ -553,7 +553,7 @@ cudaError_t launch_instance(const GemmArgs& a, int grid, cudaStream_t s) {
     configured = true;
   }
   kern<<<grid, kThreads, smem, s>>>(a);
-  count_launch();
+  count_launch(s, kid);
   return cudaGetLastError();
 }
 
@@ -576,6 +576,10 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
   a.act = p.act;
   a.err = p.err;
   a.row_prob = p.row_prob;
+  static const int kKid[6] = {MOE_K_GEMM_FC1_FPROP, MOE_K_GEMM_FC2_FPROP, MOE_K_GEMM_FC2_DGRAD,
+                              MOE_K_GEMM_FC2_WGRAD, MOE_K_GEMM_FC1_DGRAD, MOE_K_GEMM_FC1_WGRAD};
+  if (p.role < 0 || p.role > 5) return cudaErrorInvalidValue;
+  const int kid = kKid[p.role];
   const uint64_t R = (uint64_t)p.R_cap;
   const int H = p.H, F = p.F, N1 = p.N1, E = p.E;
   bool ok = true;
@@ -588,14 +592,14 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       a.out = p.out; a.ldo = N1;
       a.out2 = p.out2; a.ldo2 = F;
       if (!ok) return cudaErrorInvalidValue;
-      return launch_instance<kBN, kStages, false, false, EPI_GLU, false, true>(a, grid, s);
+      return launch_instance<kBN, kStages, false, false, EPI_GLU, false, true>(a, grid, s, kid);
     case ROLE_FC2_FPROP:
       ok &= tmap_2d(&a.tmA, p.a_s, F, R, 64, BM);
       ok &= tmap_3d(&a.tmB, p.w2, H, F, E, 64, 64);
       a.K = F; a.N = H;
       a.out = p.out; a.ldo = H;
       if (!ok) return cudaErrorInvalidValue;
-      return launch_instance<kBN, kStages, false, true, EPI_STORE, false, true>(a, grid, s);
+      return launch_instance<kBN, kStages, false, true, EPI_STORE, false, true>(a, grid, s, kid);
     case ROLE_FC2_DGRAD:
       ok &= tmap_2d(&a.tmA, p.dy_perm, H, R, 64, BM);
       ok &= tmap_3d(&a.tmB, p.w2, H, F, E, 64, kBN);
@@ -604,14 +608,14 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       a.z = static_cast<const uint16_t*>(p.z); a.ldz = N1;
       a.dprob_part = p.dprob_part; a.nparts = (F + kBN - 1) / kBN;
       if (!ok) return cudaErrorInvalidValue;
-      return launch_instance<kBN, kStages, false, false, EPI_DGLU, false, true>(a, grid, s);
+      return launch_instance<kBN, kStages, false, false, EPI_DGLU, false, true>(a, grid, s, kid);
     case ROLE_FC1_DGRAD:
       ok &= tmap_2d(&a.tmA, p.dz, N1, R, 64, BM);
       ok &= tmap_3d(&a.tmB, p.w1p, H, N1, E, 64, 64);
       a.K = N1; a.N = H;
       a.out = p.out; a.ldo = H;
       if (!ok) return cudaErrorInvalidValue;
-      return launch_instance<kBN, kStages, false, true, EPI_STORE, false, true>(a, grid, s);
+      return launch_instance<kBN, kStages, false, true, EPI_STORE, false, true>(a, grid, s, kid);
     case ROLE_FC2_WGRAD:
     case ROLE_FC1_WGRAD: {
       const bool fc2 = p.role == ROLE_FC2_WGRAD;
@@ -623,7 +627,7 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       if (!ok) return cudaErrorInvalidValue;
       const int64_t tiles = (int64_t)E * ((M + BM - 1) / BM) * ((H + kBN - 1) / kBN);
       grid = (int)std::min<int64_t>(grid, tiles);
-      return launch_instance<kBN, kStages, true, true, EPI_STORE, true, false>(a, grid, s);
+      return launch_instance<kBN, kStages, true, true, EPI_STORE, true, false>(a, grid, s, kid);
     }
   }
   return cudaErrorInvalidValue;

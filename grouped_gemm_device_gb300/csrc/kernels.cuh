@@ -7,8 +7,8 @@
 
 namespace moe {
 
-// launch accounting (api.cu)
-void count_launch();
+// launch accounting and the optional event timeline (api.cu); kid is a moe_kernel_id_t
+void count_launch(cudaStream_t s, int kid);
 
 // route.cu
 __global__ void route_topk_kernel(const float* logits, int T, int E, int k, int32_t* ids,

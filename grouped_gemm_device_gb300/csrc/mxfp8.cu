@@ -86,7 +86,7 @@ void launch_mxfp8_quantize(const void* in, int64_t M, int64_t N, int rowwise, in
   int grid = (int)std::min<int64_t>(tiles, (int64_t)num_sms * 8);
   mxfp8_quantize_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(in), M, N, rowwise,
                                              colwise, q_row, s_row, q_col, s_col);
-  count_launch();
+  count_launch(s, MOE_K_MXFP8_QUANTIZE);
 }
 
 }  // namespace moe

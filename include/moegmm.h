@@ -208,6 +208,36 @@ int32_t moe_gemm_ctas(const moe_layer_desc_t *desc);
  * host-side counter, for launch accounting). */
 uint64_t moe_launch_count(void);
 
+/* Kernel identifiers reported by the launch timeline. */
+typedef enum {
+  MOE_K_ROUTE_TOPK = 0,
+  MOE_K_ASSIGN_ROWS = 1,
+  MOE_K_GATHER_X = 2,
+  MOE_K_GEMM_FC1_FPROP = 3,
+  MOE_K_GEMM_FC2_FPROP = 4,
+  MOE_K_COMBINE_Y = 5,
+  MOE_K_GATHER_DY = 6,
+  MOE_K_GEMM_FC2_DGRAD = 7,
+  MOE_K_DPROB_REDUCE = 8,
+  MOE_K_GEMM_FC2_WGRAD = 9,
+  MOE_K_GEMM_FC1_DGRAD = 10,
+  MOE_K_COMBINE_DX = 11,
+  MOE_K_GEMM_FC1_WGRAD = 12,
+  MOE_K_MXFP8_QUANTIZE = 13,
+  MOE_K_PACK_FC1 = 14,
+  MOE_K_COUNT = 15
+} moe_kernel_id_t;
+
+/* Launch timeline, for measurement. Between moe_timeline_begin and moe_timeline_end the
+ * library records events[i] (caller-created cudaEvent_t handles, passed as void*) on the
+ * launching stream right after its i-th kernel launch, for i < capacity, and remembers the
+ * kernel's moe_kernel_id_t. Kernels of one stream run in order, so the elapsed time between
+ * consecutive events is the duration of the later kernel. Process-wide; not thread-safe.
+ * moe_timeline_end copies the ids into kernel_ids (capacity entries, may be NULL), stops
+ * recording and returns how many events were recorded. */
+moe_status_t moe_timeline_begin(void *const *events, int32_t capacity);
+int32_t moe_timeline_end(int32_t *kernel_ids);
+
 /* Human-readable message for the last host-side error of the calling thread. */
 const char *moe_last_error_string(void);
 

@@ -81,6 +81,7 @@ def load():
         "moe_last_error_string": (ctypes.c_char_p, []),
         "moe_timeline_begin": (_I32, [ctypes.POINTER(_P), _I32]),
         "moe_timeline_end": (_I32, [ctypes.POINTER(_I32)]),
+        "moe_route_permute_noalloc": (_I32, [_DP, _I32, _P, _P, _P, _P, _P, _P, _P, _I64, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -150,6 +151,16 @@ def moe_route_permute(desc, T, logits, x, topk_ids, topk_probs, counts, ws, ws_b
     _check(load().moe_route_permute(ctypes.byref(desc), T, _ptr(logits), _ptr(x), _ptr(topk_ids),
                                     _ptr(topk_probs), _ptr(counts), _ptr(ws), ws_bytes,
                                     _stream(stream)))
+
+
+def moe_route_permute_noalloc(desc, T, logits, x, topk_ids, topk_probs, counts, offsets,
+                              x_perm, x_perm_rows, stream=None):
+    """Route + permute into caller buffers with no workspace and no device allocation (the
+    library keeps its small scratch in a static device array; see include/moegmm.h)."""
+    _check(load().moe_route_permute_noalloc(ctypes.byref(desc), T, _ptr(logits), _ptr(x),
+                                            _ptr(topk_ids), _ptr(topk_probs), _ptr(counts),
+                                            _ptr(offsets), _ptr(x_perm), x_perm_rows,
+                                            _stream(stream)))
 
 
 def moe_grouped_mlp_fwd(desc, T, w1_packed, w2, y, ws, ws_bytes, stream=None):

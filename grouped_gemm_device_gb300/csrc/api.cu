@@ -38,6 +38,8 @@ static moe_status_t fail(moe_status_t st, const char* fmt, ...) {
   return st;
 }
 
+void set_last_error(const char* msg) { g_last_error = msg; }
+
 static moe_status_t cuda_fail(cudaError_t e, const char* where) {
   return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
 }

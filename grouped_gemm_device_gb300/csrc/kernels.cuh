@@ -9,6 +9,8 @@ namespace moe {
 
 // launch accounting and the optional event timeline (api.cu); kid is a moe_kernel_id_t
 void count_launch(cudaStream_t s, int kid);
+// set the message returned by moe_last_error_string for this thread (api.cu)
+void set_last_error(const char* msg);
 
 // route.cu
 __global__ void route_topk_kernel(const float* logits, int T, int E, int k, int32_t* ids,

@@ -1,0 +1,132 @@
+// moe_route_permute_noalloc: the route + permute step for callers that cannot allocate device
+// memory. Its scratch (the per-pair row map, the per-row source index and probability, and a
+// device error word) lives in one file-scope __device__ array below instead of a caller
+// workspace; the caller still passes every input and output.
+//
+// The array is a module global: every GPU that loads this library holds it until the process
+// exits, and every call on a device shares it (the contents of the previous call remain), so
+// calls whose execution overlaps on the GPU race on it.
+#include <mutex>
+
+#include "kernels.cuh"
+
+namespace moe {
+
+// Limits of the static scratch.
+constexpr int64_t kNoallocMaxPairs = 131072;                 // T_max * k
+constexpr int64_t kNoallocMaxRows = kNoallocMaxPairs + 256 * 31;  // R_cap with E <= 256
+constexpr size_t kNoallocErrBytes = 256;
+constexpr size_t kNoallocBytes =
+    kNoallocErrBytes + (size_t)kNoallocMaxPairs * 4 + (size_t)kNoallocMaxRows * 4 * 2;
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocBytes];
+
+// Host-side device addresses of g_noalloc_scratch, one per device (the symbol's name in host
+// code is only a host stand-in; the device address must come from cudaGetSymbolAddress).
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_ptr[128];
+
+static moe_status_t noalloc_scratch(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 128) {
+    set_last_error("moe_route_permute_noalloc: no usable current device");
+    return MOE_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      set_last_error("moe_route_permute_noalloc: cudaGetSymbolAddress failed");
+      return MOE_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status_t moe_route_permute_noalloc(const moe_layer_desc_t* d, int32_t T,
+                                                  const float* logits, const void* x,
+                                                  int32_t* topk_ids, float* topk_probs,
+                                                  int32_t* counts, int32_t* offsets,
+                                                  void* x_perm, int64_t x_perm_rows,
+                                                  moe_stream_t stream) {
+  if (!d) {
+    set_last_error("moe_route_permute_noalloc: desc is NULL");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (moe_workspace_size(d) == 0) return MOE_ERR_INVALID_ARG;  // message set by validation
+  if (d->precision != MOE_PREC_BF16) {
+    set_last_error("moe_route_permute_noalloc: only BF16 x_perm is produced");
+    return MOE_ERR_UNSUPPORTED;
+  }
+  const int64_t pairs = (int64_t)d->T_max * d->k;
+  const int64_t R_cap = pairs + (int64_t)d->E * (d->align - 1);
+  if (pairs > kNoallocMaxPairs || R_cap > kNoallocMaxRows) {
+    set_last_error("moe_route_permute_noalloc: T_max*k exceeds the static scratch limit of "
+                   "131072 routed (token, expert) pairs");
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (T < 0 || T > d->T_max) {
+    set_last_error("moe_route_permute_noalloc: T outside [0, T_max]");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if ((T > 0 && (!logits || !x || !topk_ids || !topk_probs)) || !counts || !offsets ||
+      !x_perm) {
+    set_last_error("moe_route_permute_noalloc: NULL tensor pointer");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(x_perm) & 15u)) {
+    set_last_error("moe_route_permute_noalloc: x and x_perm must be 16-byte aligned");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (x_perm_rows < R_cap) {
+    set_last_error("moe_route_permute_noalloc: x_perm needs T_max*k + E*(align-1) rows");
+    return MOE_ERR_INVALID_ARG;
+  }
+  void* base = nullptr;
+  moe_status_t st = noalloc_scratch(&base);
+  if (st != MOE_OK) return st;
+  uint8_t* b = static_cast<uint8_t*>(base);
+  int* err = reinterpret_cast<int*>(b);
+  int32_t* row_of = reinterpret_cast<int32_t*>(b + kNoallocErrBytes);
+  int32_t* src_of = row_of + kNoallocMaxPairs;
+  float* row_prob = reinterpret_cast<float*>(src_of + kNoallocMaxRows);
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 1;
+  // the error word and the counts start at zero on every call
+  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * d->E, s);
+  if (e != cudaSuccess) {
+    set_last_error("moe_route_permute_noalloc: memset failed");
+    return MOE_ERR_CUDA;
+  }
+  if (T > 0) {
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((T + 7) / 8, (int64_t)sms * 8));
+    route_topk_kernel<<<grid, 256, 0, s>>>(logits, T, d->E, d->k, topk_ids, topk_probs, counts);
+    count_launch(s, MOE_K_ROUTE_TOPK);
+  }
+  assign_rows_kernel<<<d->E, 1024, 0, s>>>(topk_ids, topk_probs, counts, T, d->E, d->k, d->align,
+                                           R_cap, offsets, row_of, src_of, row_prob, err);
+  count_launch(s, MOE_K_ASSIGN_ROWS);
+  const int ggrid = (int)std::max<int64_t>(1, std::min<int64_t>(R_cap, (int64_t)sms * 8));
+  gather_rows_kernel<<<ggrid, 256, 0, s>>>(static_cast<const uint4*>(x), src_of, offsets, d->E,
+                                           d->k, d->H / 8, R_cap, static_cast<uint4*>(x_perm));
+  count_launch(s, MOE_K_GATHER_X);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_last_error(cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}

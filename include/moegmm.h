@@ -166,6 +166,31 @@ moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t *desc, int32_t T, const 
                                  void *dw1_packed, void *dw2, float *d_probs, void *ws,
                                  size_t ws_bytes, moe_stream_t stream);
 
+/* Route + permute without any device allocation and without a workspace. The pages have no
+ * counterpart of this entry point; it exists for callers that cannot call cudaMalloc, such as
+ * plugins hosted by a framework that owns the whole device memory pool and forbids
+ * allocations of its own, or code that runs where an allocation would stall or is not
+ * allowed (for example while a CUDA graph is being recorded).
+ * It computes the same results as moe_route_permute (topk_ids, topk_probs, counts, and the
+ * gathered tokens) but writes the padded offsets and the gathered tokens to caller buffers:
+ *   offsets  int32 [E+1]                  out: padded expert segment starts
+ *   x_perm   bf16  [x_perm_rows, H]       out: x_perm_rows >= T_max*k + E*(align-1); same
+ *                                          rows as moe_route_permute's workspace x_perm
+ * Its scratch (row map, per-row source and probability, an error word) is a fixed
+ * file-scope device array of about 1.6 MB inside the library, held by every GPU that loads
+ * the library until the process exits. Limit: T_max*k <= 131072 routed (token, expert)
+ * pairs (E <= 256); larger descriptions return MOE_ERR_UNSUPPORTED before any launch. Only
+ * BF16 layers. The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ * capture. All calls on a device share the array and it keeps the last call's contents: the
+ * error word and counts are cleared at the start of every call, and calls whose execution
+ * overlaps on the GPU (for example on two streams) race. Capacity errors detected on the
+ * device are not reported by this entry point (they cannot occur when T <= T_max). */
+moe_status_t moe_route_permute_noalloc(const moe_layer_desc_t *desc, int32_t T,
+                                       const float *logits, const void *x, int32_t *topk_ids,
+                                       float *topk_probs, int32_t *counts, int32_t *offsets,
+                                       void *x_perm, int64_t x_perm_rows, moe_stream_t stream);
+
 /* Standalone MXFP8 quantiser ([TE-MoE] Challenge 2, Figure 3: E4M3 elements with one E8M0
  * scale per 32 contiguous values):
  *   scale exponent e = clamp(floor(log2(amax)) - 8, -127, 127) (e = -127 when amax = 0),

@@ -95,7 +95,7 @@ static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 static void compute_layout(const moe_layer_desc_t* d, moe_ws_layout_t* L) {
   const int64_t R = r_cap(d);
   const int64_t H = d->H, F = d->F, N1 = n1_of(d), E = d->E;
-  const int64_t nparts = (F + gemm_bn(ROLE_FC2_DGRAD) - 1) / gemm_bn(ROLE_FC2_DGRAD);
+  const int64_t nparts = dprob_parts((int)F);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -309,7 +309,7 @@ moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t* d, int32_t T, const voi
   p.dprob_part = w.at<float>(w.L.dprob_part);
   if ((e = launch_grouped_gemm(p, s)) != cudaSuccess) return cuda_fail(e, "FC2 dgrad GEMM");
   if (T > 0) {
-    const int nparts = (d->F + gemm_bn(ROLE_FC2_DGRAD) - 1) / gemm_bn(ROLE_FC2_DGRAD);
+    const int nparts = dprob_parts(d->F);
     const int n = T * d->k;
     dprob_reduce_kernel<<<grid_for((n + 255) / 256, 4), 256, 0, s>>>(
         w.at<float>(w.L.dprob_part), nparts, row_of, n, d_probs);

@@ -31,7 +31,8 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // TMA warp, MMA warp, epilogue warps
 constexpr int kMaxE = 256;
 
 enum { EPI_STORE = 0, EPI_GLU = 1, EPI_DGLU = 2 };
@@ -172,12 +173,14 @@ MOE_DEVICE void decode_tile(int tile, const GemmArgs& p, const Ctrl& c, int MT, 
     t.nkb = p.K / BK;
     t.row_end = c.off[e + 1];
   } else {
+    // n fastest: the CTAs of one wave share a few 128-column slices of A (read once from
+    // DRAM) and re-read the expert's narrow B (the N side, few tiles) from L2
     const int per = MT * NT;
     const int e = tile / per;
     const int local = tile - e * per;
     t.e = e;
-    t.m0 = (local % MT) * BM;
-    t.n0 = (local / MT) * BN;
+    t.m0 = (local / NT) * BM;
+    t.n0 = (local % NT) * BN;
     t.kbeg = c.off[e];
     t.klen = c.off[e + 1] - c.off[e];
     t.nkb = (t.klen + BK - 1) / BK;
@@ -207,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c.tfull[i], 1);
-      mbar_init(&c.tempty[i], 4);
+      mbar_init(&c.tempty[i], kEpiWarps);
     }
     mbar_init(&c.drain, 1);
     fence_mbar_init();
@@ -360,20 +363,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue warps 2..5
+    // ------------------------------------------------------------ epilogue warps 2..9
+    // warp w reads TMEM lanes 32*(w%4).. (its lane quadrant) and half (w-2)/4 of the columns
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     int acc_i = 0;
     for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
       TileInfo t;
       decode_tile<BN, KG>(tile, p, c, MT, NT, t);
       const int row = t.m0 + q * 32 + lane;
       const bool row_ok = row < t.row_end;
+      const int c0 = half * (BN / 2), c1 = c0 + BN / 2;  // this warp's accumulator columns
       if (t.nkb == 0) {
         // k-grouped tile of an expert with no rows: exact zeros
         if (row_ok) {
           uint16_t* o = static_cast<uint16_t*>(p.out) + (int64_t)t.e * p.out_estride +
                         (int64_t)row * p.ldo;
-          for (int cc = 0; cc < BN && t.n0 + cc < p.N; cc += 32) store_zero_bf16x32(o + t.n0 + cc);
+          for (int cc = c0; cc < c1 && t.n0 + cc < p.N; cc += 32) store_zero_bf16x32(o + t.n0 + cc);
         }
         continue;
       }
@@ -387,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (EPI == EPI_STORE) {
         uint16_t* o = static_cast<uint16_t*>(p.out) + (KG ? (int64_t)t.e * p.out_estride : 0) +
                       (int64_t)row * p.ldo + t.n0;
-        for (int cc = 0; cc < BN; cc += 32) {
+        for (int cc = c0; cc < c1; cc += 32) {
           if (t.n0 + cc >= p.N) break;
           tmem_ld_32x32b_x32(taddr + cc, r);
           tmem_ld_wait();
@@ -400,7 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint16_t* zrow = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo;
         uint16_t* arow = static_cast<uint16_t*>(p.out2) + (int64_t)row * p.ldo2;
         if (p.gated) {
-          for (int cc = 0; cc < BN / 2; cc += 32) {
+          // a-columns [half*BN/4, (half+1)*BN/4) of the tile's BN/2 GLU outputs
+          for (int cc = half * (BN / 4); cc < (half + 1) * (BN / 4); cc += 32) {
             const int gcol = (cc / p.ilv) * 2 * p.ilv + (cc % p.ilv);
             const int lcol = gcol + p.ilv;
             if (t.n0 + gcol >= p.N) break;
@@ -422,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-          for (int cc = 0; cc < BN; cc += 32) {
+          for (int cc = c0; cc < c1; cc += 32) {
             if (t.n0 + cc >= p.N) break;
             tmem_ld_32x32b_x32(taddr + cc, r);
             tmem_ld_wait();
@@ -444,18 +451,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         float dp = 0.f;
         const uint16_t* zrow = p.z + (int64_t)row * p.ldz;
         uint16_t* dzrow = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo;
-        for (int cc = 0; cc < BN; cc += 32) {
+        for (int cc = c0; cc < c1; cc += 32) {
           const int f0 = t.n0 + cc;
           if (f0 >= p.N) break;
-          tmem_ld_32x32b_x32(taddr + cc, r);
-          tmem_ld_wait();
-          if (!row_ok) continue;
           if (p.gated) {
             const int gcol = (f0 / p.ilv) * 2 * p.ilv + (f0 % p.ilv);
             const int lcol = gcol + p.ilv;
             float g[32], l[32];
-            load_bf16x32(zrow + gcol, g);
-            load_bf16x32(zrow + lcol, l);
+            // the saved-Z loads are issued before the TMEM load so their latencies overlap
+            if (row_ok) {
+              load_bf16x32(zrow + gcol, g);
+              load_bf16x32(zrow + lcol, l);
+            }
+            tmem_ld_32x32b_x32(taddr + cc, r);
+            tmem_ld_wait();
+            if (!row_ok) continue;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float das = __uint_as_float(r[i]);
@@ -469,7 +479,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             store_bf16x32(dzrow + lcol, l);
           } else {
             float zz[32];
-            load_bf16x32(zrow + f0, zz);
+            if (row_ok) load_bf16x32(zrow + f0, zz);
+            tmem_ld_32x32b_x32(taddr + cc, r);
+            tmem_ld_wait();
+            if (!row_ok) continue;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float das = __uint_as_float(r[i]);
@@ -480,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             store_bf16x32(dzrow + f0, zz);
           }
         }
-        if (row_ok) p.dprob_part[(int64_t)row * p.nparts + t.n0 / BN] = dp;
+        if (row_ok) p.dprob_part[(int64_t)row * p.nparts + (t.n0 / BN) * 2 + half] = dp;
       }
       tc_fence_before();
       __syncwarp();
@@ -564,6 +577,9 @@ constexpr int kStages = 4;
 
 int gemm_bn(int) { return kBN; }
 
+// two epilogue warps (column halves) contribute a partial d_prob per 256-column tile
+int dprob_parts(int F) { return 2 * ((F + kBN - 1) / kBN); }
+
 cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
   GemmArgs a;
   memset(&a, 0, sizeof(a));
@@ -606,7 +622,7 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       a.K = H; a.N = F;
       a.out = p.out; a.ldo = N1;
       a.z = static_cast<const uint16_t*>(p.z); a.ldz = N1;
-      a.dprob_part = p.dprob_part; a.nparts = (F + kBN - 1) / kBN;
+      a.dprob_part = p.dprob_part; a.nparts = dprob_parts(F);
       if (!ok) return cudaErrorInvalidValue;
       return launch_instance<kBN, kStages, false, false, EPI_DGLU, false, true>(a, grid, s, kid);
     case ROLE_FC1_DGRAD:

@@ -73,6 +73,7 @@ struct GemmProblem {
 };
 
 int gemm_bn(int role);
+int dprob_parts(int F);  // partial d_prob columns per row written by the FC2 dgrad epilogue
 cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s);
 
 }  // namespace moe

@@ -58,8 +58,11 @@ static int device_sms() {
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 static int64_t r_cap(const moe_layer_desc_t* d) {
-  return (int64_t)d->T_max * d->k + (int64_t)d->E * (d->align - 1);
+  const int64_t r = (int64_t)d->T_max * d->k + (int64_t)d->E * (d->align - 1);
+  // MXFP8: every permuted buffer spans whole 128-row scale slabs
+  return d->precision == MOE_PREC_MXFP8 ? (r + 127) / 128 * 128 : r;
 }
+static int64_t round128(int64_t v) { return (v + 127) / 128 * 128; }
 static int n1_of(const moe_layer_desc_t* d) {
   return d->activation == MOE_ACT_SRELU ? d->F : 2 * d->F;
 }
@@ -73,7 +76,13 @@ static moe_status_t validate_desc(const moe_layer_desc_t* d) {
     return fail(MOE_ERR_INVALID_ARG, "H, F must be positive and T_max >= 0");
   if (d->H % 64 || d->F % 64)
     return fail(MOE_ERR_UNSUPPORTED, "H=%d and F=%d must be multiples of 64", d->H, d->F);
-  if (d->align != 32) return fail(MOE_ERR_UNSUPPORTED, "align must be 32");
+  if (d->precision == MOE_PREC_BF16 && d->align != 32 && d->align != 64 && d->align != 128)
+    return fail(MOE_ERR_UNSUPPORTED, "align must be 32, 64 or 128");
+  if (d->precision == MOE_PREC_MXFP8 && d->align != 128)
+    return fail(MOE_ERR_UNSUPPORTED, "MXFP8 layers need align = 128 (whole scale slabs)");
+  if (d->precision == MOE_PREC_MXFP8 && d->activation != MOE_ACT_SRELU && d->ilv != 32 &&
+      d->ilv != 64)
+    return fail(MOE_ERR_UNSUPPORTED, "MXFP8 layers need ilv = 32 or 64");
   if (d->precision != MOE_PREC_BF16 && d->precision != MOE_PREC_MXFP8)
     return fail(MOE_ERR_INVALID_ARG, "unknown precision %d", d->precision);
   if (d->activation < MOE_ACT_SWIGLU || d->activation > MOE_ACT_SRELU)
@@ -85,17 +94,59 @@ static moe_status_t validate_desc(const moe_layer_desc_t* d) {
   }
   if (d->sm_margin < 0) return fail(MOE_ERR_INVALID_ARG, "sm_margin must be >= 0");
   if (r_cap(d) > (int64_t)INT32_MAX / 2) return fail(MOE_ERR_UNSUPPORTED, "row capacity too large");
-  if (d->precision == MOE_PREC_MXFP8)
-    return fail(MOE_ERR_UNSUPPORTED, "MXFP8 grouped GEMM path not built in this library version");
+  if (d->precision == MOE_PREC_MXFP8 &&
+      (int64_t)d->E * round128(n1_of(d)) * d->H > (int64_t)INT32_MAX * 8)
+    return fail(MOE_ERR_UNSUPPORTED, "MXFP8 weight copies too large");
   return MOE_OK;
 }
 
 static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// The MXFP8 operand copies, in order after mx_base: for each GEMM input the row-wise copy
+// [rows, K] and the column-wise transposed copy, each with its slab-layout scales.
+struct MxOps {
+  MxOperand x, xt, a, at, dy, dyt, dz, dzt, w1, w1t, w2, w2t;
+  int N1p, Fp;
+};
+
+static size_t mx_sf_bytes(int64_t rows, int64_t cols) {
+  return (size_t)((cols / 32 + 3) / 4) * (size_t)round128(rows) * 4;
+}
+
+// Lay the operands out from `base` (an address or 0 for offsets); returns the end offset.
+static size_t mx_ops(const moe_layer_desc_t* d, int64_t R, uint8_t* base, size_t o, MxOps& m) {
+  const int64_t H = d->H, F = d->F, N1 = n1_of(d), E = d->E;
+  m.N1p = (int)round128(N1);
+  m.Fp = (int)round128(F);
+  auto op = [&](MxOperand& t, int64_t rows, int64_t cols) {
+    t.rows = rows;
+    t.cols = cols;
+    t.s_pad = round128(rows);
+    t.q = base + o;
+    o = up256(o + (size_t)rows * cols);
+    t.s = base + o;
+    o = up256(o + mx_sf_bytes(rows, cols));
+  };
+  op(m.x, R, H);
+  op(m.xt, H, R);
+  op(m.a, R, F);
+  op(m.at, F, R);
+  op(m.dy, R, H);
+  op(m.dyt, H, R);
+  op(m.dz, R, N1);
+  op(m.dzt, N1, R);
+  op(m.w1, E * m.N1p, H);
+  op(m.w1t, H, E * m.N1p);
+  op(m.w2, E * m.Fp, H);
+  op(m.w2t, H, E * m.Fp);
+  return o;
+}
+
 static void compute_layout(const moe_layer_desc_t* d, moe_ws_layout_t* L) {
   const int64_t R = r_cap(d);
   const int64_t H = d->H, F = d->F, N1 = n1_of(d), E = d->E;
-  const int64_t nparts = dprob_parts((int)F);
+  const bool mx = d->precision == MOE_PREC_MXFP8;
+  const int64_t nparts = mx ? dprob_parts_mx((int)F) : dprob_parts((int)F);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -110,13 +161,19 @@ static void compute_layout(const moe_layer_desc_t* d, moe_ws_layout_t* L) {
   L->row_prob = take(R * 4);
   L->x_perm = take(R * H * 2);
   L->z = take(R * N1 * 2);
-  L->a_s = take(R * F * 2);
+  // bf16 a_s and dz exist only in the BF16 path (MXFP8 keeps them as MXFP8 copies)
+  L->a_s = mx ? SIZE_MAX : take(R * F * 2);
   L->y_perm = take(R * H * 2);
   L->dx_perm = L->y_perm;  // y_perm is dead once y is combined
   L->dy_perm = take(R * H * 2);
-  L->dz = take(R * N1 * 2);
+  L->dz = mx ? SIZE_MAX : take(R * N1 * 2);
   L->dprob_part = take(R * nparts * 4);
   L->mx_base = SIZE_MAX;
+  if (mx) {
+    MxOps m;
+    L->mx_base = o;
+    o = mx_ops(d, R, nullptr, o, m);
+  }
   L->total = o;
 }
 
@@ -165,9 +222,9 @@ static GemmProblem base_problem(const moe_layer_desc_t* d, const Ws& w) {
   p.offsets = w.at<int32_t>(w.L.offsets);
   p.row_prob = w.at<float>(w.L.row_prob);
   p.x_perm = w.at<void>(w.L.x_perm);
-  p.a_s = w.at<void>(w.L.a_s);
+  p.a_s = w.L.a_s == SIZE_MAX ? nullptr : w.at<void>(w.L.a_s);
   p.z = w.at<void>(w.L.z);
-  p.dz = w.at<void>(w.L.dz);
+  p.dz = w.L.dz == SIZE_MAX ? nullptr : w.at<void>(w.L.dz);
   p.dy_perm = w.at<void>(w.L.dy_perm);
   p.gated = d->activation != MOE_ACT_SRELU;
   p.ilv = d->ilv;
@@ -182,6 +239,39 @@ static int grid_for(int64_t work, int per_sm) {
   if (sms <= 0) sms = 1;
   int64_t g = std::min<int64_t>(work, (int64_t)sms * per_sm);
   return (int)std::max<int64_t>(g, 1);
+}
+
+static MxProblem mx_problem(const moe_layer_desc_t* d, const Ws& w) {
+  MxProblem p;
+  memset(&p, 0, sizeof(p));
+  MxOps m;
+  mx_ops(d, w.L.R_cap, w.base, w.L.mx_base, m);
+  p.E = d->E;
+  p.H = d->H;
+  p.F = d->F;
+  p.N1 = n1_of(d);
+  p.N1p = m.N1p;
+  p.Fp = m.Fp;
+  p.R_cap = w.L.R_cap;
+  p.offsets = w.at<int32_t>(w.L.offsets);
+  p.x = m.x; p.xt = m.xt; p.a = m.a; p.at = m.at; p.dy = m.dy; p.dyt = m.dyt;
+  p.dz = m.dz; p.dzt = m.dzt; p.w1 = m.w1; p.w1t = m.w1t; p.w2 = m.w2; p.w2t = m.w2t;
+  p.row_prob = w.at<float>(w.L.row_prob);
+  p.z = w.at<void>(w.L.z);
+  p.gated = d->activation != MOE_ACT_SRELU;
+  p.ilv = d->ilv;
+  p.act = act_of(d);
+  p.err = w.at<int>(w.L.err);
+  p.num_ctas = gemm_ctas(d);
+  return p;
+}
+
+// Quantise a bf16 matrix [M, N] (row groups G padded to Gp) into the row-wise and the
+// column-wise (transposed) MXFP8 operands of the block-scaled GEMM.
+static void mx_quantize_operands(const void* in, int64_t M, int64_t N, int64_t G, int64_t Gp,
+                                 const MxOperand& row, const MxOperand& col, cudaStream_t s) {
+  launch_mxfp8_quantize_mma(in, M, N, G, Gp, row.q, row.s, col.q, col.s,
+                            std::max(device_sms(), 1), s);
 }
 
 }  // namespace moe
@@ -236,6 +326,12 @@ moe_status_t moe_route_permute(const moe_layer_desc_t* d, int32_t T, const float
       static_cast<const uint4*>(x), src_of, offsets, d->E, d->k, d->H / 8, w.L.R_cap,
       w.at<uint4>(w.L.x_perm));
   count_launch(s, MOE_K_GATHER_X);
+  if (d->precision == MOE_PREC_MXFP8) {
+    // X along H for FC1 and column-wise (along the expert's rows) for the FC1 weight gradient
+    const MxProblem m = mx_problem(d, w);
+    mx_quantize_operands(w.at<void>(w.L.x_perm), w.L.R_cap, d->H, w.L.R_cap, w.L.R_cap, m.x,
+                         m.xt, s);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "route_permute launch");
   return MOE_OK;
@@ -253,10 +349,32 @@ moe_status_t moe_grouped_mlp_fwd(const moe_layer_desc_t* d, int32_t T, const voi
   Ws w;
   if ((st = check_ws(d, ws, ws_bytes, w)) != MOE_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (d->precision == MOE_PREC_MXFP8) {
+    MxProblem m = mx_problem(d, w);
+    // BF16 master weights -> MXFP8 along both reduction directions ([TE-MoE] Challenge 3)
+    mx_quantize_operands(w1_packed, (int64_t)d->E * m.N1, d->H, m.N1, m.N1p, m.w1, m.w1t, s);
+    mx_quantize_operands(w2, (int64_t)d->E * d->F, d->H, d->F, m.Fp, m.w2, m.w2t, s);
+    // FC1 + activation + probability scale + MXFP8 quantise/transpose (kernel family 2)
+    m.role = ROLE_FC1_FPROP;
+    m.out = w.at<void>(w.L.z);
+    if ((e = launch_grouped_gemm_mx(m, s)) != cudaSuccess) return cuda_fail(e, "FC1 MX GEMM");
+    m.role = ROLE_FC2_FPROP;
+    m.out = w.at<void>(w.L.y_perm);
+    if ((e = launch_grouped_gemm_mx(m, s)) != cudaSuccess) return cuda_fail(e, "FC2 MX GEMM");
+    if (T > 0) {
+      combine_rows_kernel<<<grid_for(T, 8), 256, 0, s>>>(w.at<uint4>(w.L.y_perm),
+                                                        w.at<int32_t>(w.L.row_of), T, d->k,
+                                                        d->H / 8, static_cast<uint4*>(y));
+      count_launch(s, MOE_K_COMBINE_Y);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "fwd launch");
+    return MOE_OK;
+  }
   GemmProblem p = base_problem(d, w);
   p.w1p = w1_packed;
   p.w2 = w2;
-  cudaError_t e;
   // FC1 + activation + probability scale (kernel family 2)
   p.role = ROLE_FC1_FPROP;
   p.out = w.at<void>(w.L.z);
@@ -303,6 +421,38 @@ moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t* d, int32_t T, const voi
       static_cast<const uint4*>(dy), w.at<int32_t>(w.L.src_of), w.at<int32_t>(w.L.offsets), d->E,
       d->k, d->H / 8, w.L.R_cap, w.at<uint4>(w.L.dy_perm));
   count_launch(s, MOE_K_GATHER_DY);
+  if (d->precision == MOE_PREC_MXFP8) {
+    MxProblem m = mx_problem(d, w);
+    mx_quantize_operands(w.at<void>(w.L.dy_perm), w.L.R_cap, d->H, w.L.R_cap, w.L.R_cap, m.dy,
+                         m.dyt, s);
+    // FC2 dgrad + dActivation + MXFP8 quantise/transpose of dZ (kernel family 3)
+    m.role = ROLE_FC2_DGRAD;
+    m.dprob_part = w.at<float>(w.L.dprob_part);
+    if ((e = launch_grouped_gemm_mx(m, s)) != cudaSuccess) return cuda_fail(e, "FC2 dgrad MX");
+    if (T > 0) {
+      const int n = T * d->k;
+      dprob_reduce_kernel<<<grid_for((n + 255) / 256, 4), 256, 0, s>>>(
+          w.at<float>(w.L.dprob_part), dprob_parts_mx(d->F), row_of, n, d_probs);
+      count_launch(s, MOE_K_DPROB_REDUCE);
+    }
+    m.role = ROLE_FC2_WGRAD;
+    m.out = dw2;
+    if ((e = launch_grouped_gemm_mx(m, s)) != cudaSuccess) return cuda_fail(e, "FC2 wgrad MX");
+    m.role = ROLE_FC1_DGRAD;
+    m.out = w.at<void>(w.L.dx_perm);
+    if ((e = launch_grouped_gemm_mx(m, s)) != cudaSuccess) return cuda_fail(e, "FC1 dgrad MX");
+    if (T > 0) {
+      combine_rows_kernel<<<grid_for(T, 8), 256, 0, s>>>(w.at<uint4>(w.L.dx_perm), row_of, T,
+                                                        d->k, d->H / 8, static_cast<uint4*>(dx));
+      count_launch(s, MOE_K_COMBINE_DX);
+    }
+    m.role = ROLE_FC1_WGRAD;
+    m.out = dw1_packed;
+    if ((e = launch_grouped_gemm_mx(m, s)) != cudaSuccess) return cuda_fail(e, "FC1 wgrad MX");
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "bwd launch");
+    return MOE_OK;
+  }
   // FC2 dgrad + dActivation (kernel family 3)
   p.role = ROLE_FC2_DGRAD;
   p.out = w.at<void>(w.L.dz);

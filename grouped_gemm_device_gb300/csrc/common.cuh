@@ -56,6 +56,23 @@ MOE_DEVICE uint32_t cvt_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Quantise 32 fp32 values (one block) into 32 E4M3 bytes (as 8 words) and return the scale
+// byte.
+MOE_DEVICE uint32_t mx_quant_block(const float (&v)[32], uint32_t (&q)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int e = mx_block_exponent(amax);
+  const float inv = mx_inv_scale(e);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t lo = cvt_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv);
+    uint32_t hi = cvt_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+    q[i] = lo | (hi << 16);
+  }
+  return (uint32_t)(e + 127);
+}
+
 // ----------------------------------------------------------------------------- smem / timer
 MOE_DEVICE uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -207,6 +224,59 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
          | (1u << 10)                    // B format bf16
          | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ----------------------------------------------------------------------------- MXFP8 MMA
+// Instruction descriptor, kind::mxf8f6f4 block-scaled: E4M3 A and B (format 0), K-major,
+// scale factors E8M0 (bit 23), a_sf_id at bits 29..30 and b_sf_id at bits 4..5 select which
+// byte of the 32-bit scale-factor column a K=32 step uses.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sf_id) {
+  return ((uint32_t)(sf_id & 3) << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(M >> 4) << 24) | ((uint32_t)(sf_id & 3) << 29);
+}
+// D[tmem] (+)= (A * 2^SFA) (B * 2^SFB)^T, E4M3 inputs with per-32 E8M0 scales in TMEM.
+MOE_DEVICE void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+          "r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Copy a 32-row x 16-byte shared-memory matrix into TMEM (4 columns), replicated into all
+// four 32-lane quadrants.
+MOE_DEVICE void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+// Shared-memory descriptor without swizzle (8-row x 16-byte core matrices, SBO between
+// consecutive 8-row groups).
+MOE_DEVICE uint64_t smem_desc_noswizzle(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+// 1-D bulk copy global -> shared, completion counted on an mbarrier (bytes, 16-aligned).
+MOE_DEVICE void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Byte offset of scale factor (row, kb) in the MMA-ready scale layout: slabs of 128 rows x 4
+// k-blocks (512 bytes), slab (kb/4, row/128) at ((kb/4) * rows_pad + row/128*128) * 4; inside a
+// slab, row r = 32*j + i sits in 16-byte line i at bytes 4*j .. 4*j+3 (one per k-block). This is
+// the order in which tcgen05.cp.32x128b.warpx4 hands 128 rows x 4 scale bytes to the MMA.
+__host__ __device__ inline int64_t sf_mma_offset(int64_t row, int64_t kb, int64_t rows_pad) {
+  const int64_t perm = (row & ~(int64_t)127) | ((row & 31) << 2) | ((row >> 5) & 3);
+  return ((kb >> 2) * rows_pad + perm) * 4 + (kb & 3);
 }
 
 // ----------------------------------------------------------------------------- math

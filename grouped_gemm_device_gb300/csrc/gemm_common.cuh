@@ -1,0 +1,120 @@
+// Helpers shared by the grouped GEMM kernels (bf16 and MXFP8): fp32 activation math of the
+// GLU epilogues, 32-wide bf16 load/store, and host-side TMA tensor-map construction.
+#pragma once
+
+#include <mutex>
+
+#include "kernels.cuh"
+
+namespace moe {
+
+// ------------------------------------------------------------------ activations (fp32)
+MOE_DEVICE float phi_cdf(float g) { return 0.5f * (1.0f + erff(g * 0.70710678118654752f)); }
+
+MOE_DEVICE float act_fwd(const ActDev& a, float g, float l) {
+  if (a.kind == MOE_ACT_CLAMPED_SWIGLU) {
+    const float gc = fminf(g, a.gate_max);
+    const float lc = fminf(fmaxf(l, a.lin_lo), a.lin_hi);
+    return (lc + a.lin_offset) * gc * sigmoidf_fast(a.beta * gc);
+  }
+  if (a.kind == MOE_ACT_GEGLU) return l * g * phi_cdf(g);
+  return l * g * sigmoidf_fast(a.beta * g);  // SwiGLU
+}
+
+// returns a (unscaled) and writes d_gate, d_lin for the upstream gradient dA
+MOE_DEVICE float act_bwd(const ActDev& a, float g, float l, float dA, float& dg, float& dl) {
+  if (a.kind == MOE_ACT_CLAMPED_SWIGLU) {
+    const float gc = fminf(g, a.gate_max);
+    const float lc = fminf(fmaxf(l, a.lin_lo), a.lin_hi);
+    const float s = sigmoidf_fast(a.beta * gc);
+    const float sw = gc * s;
+    dg = (g <= a.gate_max) ? dA * (lc + a.lin_offset) * s * (1.0f + a.beta * gc * (1.0f - s))
+                           : 0.0f;
+    dl = (l >= a.lin_lo && l <= a.lin_hi) ? dA * sw : 0.0f;
+    return (lc + a.lin_offset) * sw;
+  }
+  if (a.kind == MOE_ACT_GEGLU) {
+    const float P = phi_cdf(g);
+    const float pdf = 0.39894228040143268f * __expf(-0.5f * g * g);
+    dg = dA * l * (P + g * pdf);
+    dl = dA * g * P;
+    return l * g * P;
+  }
+  const float s = sigmoidf_fast(a.beta * g);
+  dg = dA * l * s * (1.0f + a.beta * g * (1.0f - s));
+  dl = dA * g * s;
+  return l * g * s;
+}
+
+MOE_DEVICE void store_bf16x32(void* dst, const float (&v)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    d[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                      pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+}
+MOE_DEVICE void load_bf16x32(const void* src, float (&v)[32]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 w = s[i];
+    v[8 * i + 0] = bf16_lo(w.x); v[8 * i + 1] = bf16_hi(w.x);
+    v[8 * i + 2] = bf16_lo(w.y); v[8 * i + 3] = bf16_hi(w.y);
+    v[8 * i + 4] = bf16_lo(w.z); v[8 * i + 5] = bf16_hi(w.z);
+    v[8 * i + 6] = bf16_lo(w.w); v[8 * i + 7] = bf16_hi(w.w);
+  }
+}
+MOE_DEVICE void store_zero_bf16x32(void* dst) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = make_uint4(0, 0, 0, 0);
+}
+
+
+// ------------------------------------------------------------------ tensor maps (host)
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// bf16 tensor map, 128-byte swizzle. dims/box innermost first; strides in bytes for dims 1..
+inline bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+               const uint64_t* strides, const uint32_t* box, CUtensorMapDataType dt) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void*>(base),
+                  reinterpret_cast<const cuuint64_t*>(dims),
+                  reinterpret_cast<const cuuint64_t*>(strides),
+                  reinterpret_cast<const cuuint32_t*>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+inline bool tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_in,
+             uint32_t box_out) {
+  uint64_t dims[2] = {inner, outer};
+  uint64_t strides[1] = {inner * 2};
+  uint32_t box[2] = {box_in, box_out};
+  return make_tmap(m, base, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+}
+inline bool tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+             uint32_t b0, uint32_t b1) {
+  uint64_t dims[3] = {d0, d1, d2};
+  uint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  uint32_t box[3] = {b0, b1, 1};
+  return make_tmap(m, base, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+}
+
+
+}  // namespace moe

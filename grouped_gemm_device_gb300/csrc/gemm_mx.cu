@@ -1,0 +1,558 @@
+// Persistent block-scaled (MXFP8) grouped GEMM for sm_103a.
+//
+// [NV-blog] kernel families in the MXFP8 recipe: (1) GroupGemm + quantise, (2) FC1 +
+// activation + quantise/transpose, (3) FC2 dgrad + dActivation + quantise/transpose; [TE-MoE]
+// Challenge 2 (MXFP8: E4M3 with one E8M0 scale per 32 values, tensor-core accelerated).
+//
+// Every operand is an E4M3 matrix quantised along its own reduction dimension and stored
+// K-major ([rows, K]); its scales sit in the MMA slab layout (sf_mma_offset). A CTA:
+//   warp 0   TMA of the A and B k-blocks (128 x 128 bytes each) and a 1-D bulk copy of their two
+//            512-byte scale slabs, all counted on one mbarrier,
+//   warp 1   TMEM owner; one thread copies the stage's scales into TMEM (tcgen05.cp) and issues
+//            four tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each, scale byte = K step),
+//   warps 2-9 epilogue: bf16 store, or GLU / dGLU with fused row-wise and column-wise
+//            (transposed) MXFP8 quantisation of the result: a row's 32-column block is one
+//            thread's registers; a column's 32-row block is the 32 lanes of one warp.
+// Tiles are 128 x 128 with two TMEM accumulators (256 columns) plus 8 scale columns per
+// stage. Expert segments are padded to 128 rows so that every tile starts on a scale slab.
+#include "gemm_common.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int BK = 128;  // fp8 elements (bytes) per k-block: one 128-byte swizzle row
+constexpr int MMA_K = 32;
+constexpr int STAGES = 6;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kMaxE = 256;
+constexpr int kSfCol = 2 * BN;  // first TMEM column of the per-stage scale factors
+constexpr int kTmemCols = 512;
+
+enum { EPI_STORE = 0, EPI_GLU = 1, EPI_DGLU = 2 };
+
+struct MxArgs {
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  const uint8_t* sfa;
+  int64_t sfa_pad;
+  const uint8_t* sfb;
+  int64_t sfb_pad;
+  const int32_t* offsets;
+  int E;
+  int R_cap;
+  int M, N, K;
+  int a_row_e, a_k_e, b_row_e, b_k_e;  // per-expert row / k offsets of A and B
+  void* out;                           // bf16 output (STORE) or saved Z (GLU)
+  int64_t ldo;
+  int64_t out_estride;
+  uint8_t* q_row;                      // GLU: a_s, DGLU: dZ, row-wise MXFP8 [R, ld_q_row]
+  uint8_t* s_row;
+  int64_t ld_q_row;
+  int64_t s_row_pad;
+  uint8_t* q_col;                      // column-wise MXFP8, transposed [cols, ld_q_col]
+  uint8_t* s_col;
+  int64_t ld_q_col;
+  int64_t s_col_pad;
+  const float* row_prob;
+  const uint16_t* z;                   // DGLU: saved Z (bf16, packed columns)
+  int64_t ldz;
+  float* dprob_part;
+  int nparts;
+  int gated;
+  int ilv;
+  ActDev act;
+  int* err;
+};
+
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int SF_BYTES = 512;                      // per operand per stage
+constexpr int DATA = STAGES * STAGE_BYTES;
+constexpr int SF_OFF = DATA;
+constexpr int CTRL_OFF = SF_OFF + STAGES * 2 * SF_BYTES;
+constexpr int SMEM_TOTAL = CTRL_OFF + 4096 + 1024;
+
+struct Ctrl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int total_tiles;
+  int off[kMaxE + 1];
+  int prefix[kMaxE + 1];
+};
+
+struct TileInfo {
+  int e, m0, n0, kbeg, klen, nkb, row_end;
+};
+
+template <bool KG>
+MOE_DEVICE void decode_tile(int tile, const MxArgs& p, const Ctrl& c, int MT, int NT, TileInfo& t) {
+  if (!KG) {
+    int lo = 0, hi = p.E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (c.prefix[mid] <= tile) lo = mid; else hi = mid;
+    }
+    const int e = lo;
+    const int local = tile - c.prefix[e];
+    const int mt = (c.off[e + 1] - c.off[e] + BM - 1) / BM;
+    t.e = e;
+    t.m0 = c.off[e] + (local % mt) * BM;
+    t.n0 = (local / mt) * BN;
+    t.kbeg = 0;
+    t.klen = p.K;
+    t.nkb = (p.K + BK - 1) / BK;
+    t.row_end = c.off[e + 1];
+  } else {
+    const int per = MT * NT;
+    const int e = tile / per;
+    const int local = tile - e * per;
+    t.e = e;
+    t.m0 = (local / NT) * BM;
+    t.n0 = (local % NT) * BN;
+    t.kbeg = c.off[e];
+    t.klen = c.off[e + 1] - c.off[e];
+    t.nkb = (t.klen + BK - 1) / BK;
+    t.row_end = p.M;
+  }
+}
+
+// Row-wise MXFP8 of one 32-column block held by this thread.
+MOE_DEVICE void mx_store_row_block(const float (&v)[32], uint8_t* q, uint8_t* s_row, int64_t row,
+                                   int64_t col, int64_t ld, int64_t s_pad) {
+  uint32_t w[8];
+  const uint32_t sb = mx_quant_block(v, w);
+  uint4* dst = reinterpret_cast<uint4*>(q + row * ld + col);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  s_row[sf_mma_offset(row, col / 32, s_pad)] = (uint8_t)sb;
+}
+
+// Column-wise MXFP8 of the warp's 32 rows x 32 columns (this lane holds one row): each column's
+// block maximum is a warp reduction; the column's 32 codes are stored as one 32-byte run of the
+// transposed output q[col][row0 .. row0+31].
+MOE_DEVICE void mx_store_col_blocks(const float (&v)[32], uint8_t* q, uint8_t* s_col, int64_t row0,
+                                    int64_t col0, int64_t ld, int64_t s_pad, int lane) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float m = fabsf(v[j]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+    const int e = mx_block_exponent(m);
+    const uint32_t code = cvt_e4m3x2(v[j] * mx_inv_scale(e), 0.f) & 0xFFu;
+    q[(col0 + j) * ld + row0 + lane] = (uint8_t)code;
+    if (lane == j) s_col[sf_mma_offset(col0 + j, row0 / 32, s_pad)] = (uint8_t)(e + 127);
+  }
+}
+
+template <int EPI, bool KG>
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __grid_constant__ MxArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  Ctrl& c = *reinterpret_cast<Ctrl*>(smem + CTRL_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort = &c.abort;
+  const int NT = (p.N + BN - 1) / BN;
+  const int MT = KG ? (p.M + BM - 1) / BM : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&c.full[s], 1);
+      mbar_init(&c.empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c.tfull[i], 1);
+      mbar_init(&c.tempty[i], kEpiWarps);
+    }
+    mbar_init(&c.drain, 1);
+    fence_mbar_init();
+    c.abort = 0;
+    bool ok = p.E >= 1 && p.E <= kMaxE;
+    int prev = 0;
+    for (int e = 0; ok && e <= p.E; ++e) {
+      const int o = p.offsets[e];
+      // segments must start on 128-row boundaries (scale slabs)
+      if (o < prev || o > p.R_cap || (o & (BM - 1)) || (e == 0 && o != 0)) ok = false;
+      c.off[e] = o;
+      prev = o;
+    }
+    int total = 0;
+    if (ok) {
+      for (int e = 0; e < p.E; ++e) {
+        c.prefix[e] = total;
+        total += KG ? MT * NT : ((c.off[e + 1] - c.off[e] + BM - 1) / BM) * NT;
+      }
+      c.prefix[p.E] = total;
+    } else {
+      set_error(p.err, MOE_DEVERR_CAPACITY);
+    }
+    c.total_tiles = total;
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA);
+    tma_prefetch_desc(&p.tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&c.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = c.tmem_base;
+  const int total = c.total_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) armed[s] = -1;
+      for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+        TileInfo t;
+        decode_tile<KG>(tile, p, c, MT, NT, t);
+        const int a_row = t.m0 + t.e * p.a_row_e;
+        const int b_row = t.n0 + t.e * p.b_row_e;
+        for (int kb = 0; kb < t.nkb; ++kb) {
+          if (!mbar_wait(&c.empty[stage], phase ^ 1, abort, p.err)) break;
+          uint8_t* sA = smem + stage * STAGE_BYTES;
+          uint8_t* sB = sA + A_BYTES;
+          uint8_t* sfA = smem + SF_OFF + stage * 2 * SF_BYTES;
+          uint64_t* bar = &c.full[stage];
+          mbar_arrive_expect_tx(bar, STAGE_BYTES + 2 * SF_BYTES);
+#pragma unroll
+          for (int s = 0; s < STAGES; ++s)
+            if (s == stage) armed[s] = (int)phase;
+          const int k0 = t.kbeg + kb * BK;
+          const int a_k = k0 + t.e * p.a_k_e;
+          const int b_k = k0 + t.e * p.b_k_e;
+          tma_load_2d(sA, &p.tmA, bar, a_k, a_row);
+          tma_load_2d(sB, &p.tmB, bar, b_k, b_row);
+          bulk_load(sfA, p.sfa + ((int64_t)(a_k / BK) * p.sfa_pad + a_row) * 4, SF_BYTES, bar);
+          bulk_load(sfA + SF_BYTES, p.sfb + ((int64_t)(b_k / BK) * p.sfb_pad + b_row) * 4,
+                    SF_BYTES, bar);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) {
+        if (armed[s] >= 0) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(smem_u32(&c.full[s]), (uint32_t)armed[s]) &&
+                 globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ scale copy + MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc_i = 0;
+      bool issued_any = false;
+      for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+        TileInfo t;
+        decode_tile<KG>(tile, p, c, MT, NT, t);
+        if (t.nkb == 0) continue;
+        const int acc = acc_i & 1;
+        const uint32_t acc_phase = (acc_i >> 1) & 1;
+        if (!mbar_wait(&c.tempty[acc], acc_phase ^ 1, abort, p.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < t.nkb; ++kb) {
+          if (!mbar_wait(&c.full[stage], phase, abort, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sB = sA + A_BYTES;
+          const uint32_t sfA = smem_u32(smem + SF_OFF + stage * 2 * SF_BYTES);
+          const uint32_t sfa_t = tmem_base + kSfCol + stage * 8;
+          const uint32_t sfb_t = sfa_t + 4;
+          tmem_cp_32x128b_warpx4(sfa_t, smem_desc_noswizzle(sfA, 0, 128));
+          tmem_cp_32x128b_warpx4(sfb_t, smem_desc_noswizzle(sfA + SF_BYTES, 0, 128));
+          const int rem = t.klen - kb * BK;
+          const int nsub = rem >= BK ? BK / MMA_K : (rem + MMA_K - 1) / MMA_K;
+          for (int ks = 0; ks < nsub; ++ks) {
+            const uint64_t ad = smem_desc_sw128(sA + ks * MMA_K, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(sB + ks * MMA_K, 16, 1024);
+            mma_mxf8_ss(d_tmem, ad, bd, idesc_mxf8(BM, BN, ks), sfa_t, sfb_t,
+                        (kb | ks) != 0 ? 1u : 0u);
+          }
+          issued_any = true;
+          mma_commit(&c.empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&c.tfull[acc]);
+        ++acc_i;
+      }
+      if (issued_any) {
+        mma_commit(&c.drain);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(&c.drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps 2..9
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    int acc_i = 0;
+    for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+      TileInfo t;
+      decode_tile<KG>(tile, p, c, MT, NT, t);
+      const int row0 = t.m0 + q * 32;  // first row of this warp's 32-row block
+      const int row = row0 + lane;
+      const bool row_ok = row < t.row_end;
+      const int c0 = half * (BN / 2), c1 = c0 + BN / 2;
+      if (t.nkb == 0) {
+        if (row_ok) {
+          uint16_t* o = static_cast<uint16_t*>(p.out) + (int64_t)t.e * p.out_estride +
+                        (int64_t)row * p.ldo;
+          for (int cc = c0; cc < c1 && t.n0 + cc < p.N; cc += 32) store_zero_bf16x32(o + t.n0 + cc);
+        }
+        continue;
+      }
+      const int acc = acc_i & 1;
+      const uint32_t acc_phase = (acc_i >> 1) & 1;
+      if (!mbar_wait(&c.tfull[acc], acc_phase, abort, p.err)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      uint32_t r[32];
+      float v[32];
+      if (EPI == EPI_STORE) {
+        uint16_t* o = static_cast<uint16_t*>(p.out) + (KG ? (int64_t)t.e * p.out_estride : 0) +
+                      (int64_t)row * p.ldo + t.n0;
+        for (int cc = c0; cc < c1; cc += 32) {
+          if (t.n0 + cc >= p.N) break;
+          tmem_ld_32x32b_x32(taddr + cc, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          if (row_ok) store_bf16x32(o + cc, v);
+        }
+      } else if (EPI == EPI_GLU) {
+        // segments are 128-row aligned, so every row of the tile is inside its segment
+        const float prob = p.row_prob[row];
+        uint16_t* zrow = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo;
+        const int per_half = p.gated ? BN / 4 : BN / 2;  // output columns per warp
+        for (int cc = half * per_half; cc < (half + 1) * per_half; cc += 32) {
+          int zcol, acol;
+          if (p.gated) {
+            const int gcol = (cc / p.ilv) * 2 * p.ilv + (cc % p.ilv);
+            if (t.n0 + gcol >= p.N) break;
+            uint32_t rl[32];
+            tmem_ld_32x32b_x32(taddr + gcol, r);
+            tmem_ld_32x32b_x32(taddr + gcol + p.ilv, rl);
+            tmem_ld_wait();
+            float g[32], l[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              g[i] = __uint_as_float(r[i]);
+              l[i] = __uint_as_float(rl[i]);
+              v[i] = prob * act_fwd(p.act, g[i], l[i]);
+            }
+            store_bf16x32(zrow + t.n0 + gcol, g);
+            store_bf16x32(zrow + t.n0 + gcol + p.ilv, l);
+            zcol = gcol;
+            acol = t.n0 / 2 + cc;
+          } else {
+            if (t.n0 + cc >= p.N) break;
+            tmem_ld_32x32b_x32(taddr + cc, r);
+            tmem_ld_wait();
+            float zz[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              zz[i] = __uint_as_float(r[i]);
+              const float rr = fmaxf(zz[i], 0.f);
+              v[i] = prob * rr * rr;
+            }
+            store_bf16x32(zrow + t.n0 + cc, zz);
+            zcol = cc;
+            acol = t.n0 + cc;
+          }
+          (void)zcol;
+          mx_store_row_block(v, p.q_row, p.s_row, row, acol, p.ld_q_row, p.s_row_pad);
+          mx_store_col_blocks(v, p.q_col, p.s_col, row0, acol, p.ld_q_col, p.s_col_pad, lane);
+        }
+      } else {  // EPI_DGLU: accumulator = dA_s over F columns
+        const float prob = p.row_prob[row];
+        float dp = 0.f;
+        const uint16_t* zrow = p.z + (int64_t)row * p.ldz;
+        for (int cc = c0; cc < c1; cc += 32) {
+          const int f0 = t.n0 + cc;
+          if (f0 >= p.N) break;
+          if (p.gated) {
+            const int gcol = (f0 / p.ilv) * 2 * p.ilv + (f0 % p.ilv);
+            const int lcol = gcol + p.ilv;
+            float g[32], l[32];
+            load_bf16x32(zrow + gcol, g);
+            load_bf16x32(zrow + lcol, l);
+            tmem_ld_32x32b_x32(taddr + cc, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float das = __uint_as_float(r[i]);
+              float dg, dl;
+              const float a = act_bwd(p.act, g[i], l[i], prob * das, dg, dl);
+              dp += das * a;
+              g[i] = dg;
+              l[i] = dl;
+            }
+            mx_store_row_block(g, p.q_row, p.s_row, row, gcol, p.ld_q_row, p.s_row_pad);
+            mx_store_row_block(l, p.q_row, p.s_row, row, lcol, p.ld_q_row, p.s_row_pad);
+            mx_store_col_blocks(g, p.q_col, p.s_col, row0, gcol, p.ld_q_col, p.s_col_pad, lane);
+            mx_store_col_blocks(l, p.q_col, p.s_col, row0, lcol, p.ld_q_col, p.s_col_pad, lane);
+          } else {
+            float zz[32];
+            load_bf16x32(zrow + f0, zz);
+            tmem_ld_32x32b_x32(taddr + cc, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float das = __uint_as_float(r[i]);
+              const float rr = fmaxf(zz[i], 0.f);
+              dp += das * rr * rr;
+              zz[i] = prob * das * 2.f * rr;
+            }
+            mx_store_row_block(zz, p.q_row, p.s_row, row, f0, p.ld_q_row, p.s_row_pad);
+            mx_store_col_blocks(zz, p.q_col, p.s_col, row0, f0, p.ld_q_col, p.s_col_pad, lane);
+          }
+        }
+        p.dprob_part[(int64_t)row * p.nparts + (t.n0 / BN) * 2 + half] = dp;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.tempty[acc]);
+      ++acc_i;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+bool tmap_fp8(CUtensorMap* m, const MxOperand& t) {
+  uint64_t dims[2] = {(uint64_t)t.cols, (uint64_t)t.rows};
+  uint64_t strides[1] = {(uint64_t)t.cols};
+  uint32_t box[2] = {BK, 128};
+  return make_tmap(m, t.q, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+
+template <int EPI, bool KG>
+cudaError_t launch_mx(const MxArgs& a, int grid, cudaStream_t s, int kid) {
+  auto kern = grouped_gemm_mx_kernel<EPI, KG>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  kern<<<grid, kThreads, SMEM_TOTAL, s>>>(a);
+  count_launch(s, kid);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int dprob_parts_mx(int F) { return 2 * ((F + BN - 1) / BN); }
+
+cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s) {
+  static const int kKid[6] = {MOE_K_GEMM_FC1_FPROP, MOE_K_GEMM_FC2_FPROP, MOE_K_GEMM_FC2_DGRAD,
+                              MOE_K_GEMM_FC2_WGRAD, MOE_K_GEMM_FC1_DGRAD, MOE_K_GEMM_FC1_WGRAD};
+  if (p.role < 0 || p.role > 5) return cudaErrorInvalidValue;
+  MxArgs a;
+  memset(&a, 0, sizeof(a));
+  a.offsets = p.offsets;
+  a.E = p.E;
+  a.R_cap = (int)p.R_cap;
+  a.gated = p.gated;
+  a.ilv = p.ilv;
+  a.act = p.act;
+  a.err = p.err;
+  a.row_prob = p.row_prob;
+  const int H = p.H, F = p.F, N1 = p.N1;
+  const MxOperand *A = nullptr, *B = nullptr;
+  int grid = p.num_ctas;
+  switch (p.role) {
+    case ROLE_FC1_FPROP:  // X (rows) x W1 (rows e*N1p + n), K = H
+      A = &p.x; B = &p.w1;
+      a.K = H; a.N = N1; a.b_row_e = p.N1p;
+      a.out = p.out; a.ldo = N1;
+      a.q_row = p.a.q; a.s_row = p.a.s; a.ld_q_row = F; a.s_row_pad = p.a.s_pad;
+      a.q_col = p.at.q; a.s_col = p.at.s; a.ld_q_col = p.R_cap; a.s_col_pad = p.at.s_pad;
+      break;
+    case ROLE_FC2_FPROP:  // a_s x W2^T (W2 column-wise copy [H, E*Fp]), K = F
+      A = &p.a; B = &p.w2t;
+      a.K = F; a.N = H; a.b_k_e = p.Fp;
+      a.out = p.out; a.ldo = H;
+      break;
+    case ROLE_FC2_DGRAD:  // dY x W2 (rows e*Fp + f), K = H
+      A = &p.dy; B = &p.w2;
+      a.K = H; a.N = F; a.b_row_e = p.Fp;
+      a.z = static_cast<const uint16_t*>(p.z); a.ldz = N1;
+      a.q_row = p.dz.q; a.s_row = p.dz.s; a.ld_q_row = N1; a.s_row_pad = p.dz.s_pad;
+      a.q_col = p.dzt.q; a.s_col = p.dzt.s; a.ld_q_col = p.R_cap; a.s_col_pad = p.dzt.s_pad;
+      a.dprob_part = p.dprob_part; a.nparts = dprob_parts_mx(F);
+      break;
+    case ROLE_FC1_DGRAD:  // dZ x W1^T (W1 column-wise copy [H, E*N1p]), K = N1
+      A = &p.dz; B = &p.w1t;
+      a.K = N1; a.N = H; a.b_k_e = p.N1p;
+      a.out = p.out; a.ldo = H;
+      break;
+    case ROLE_FC2_WGRAD:  // dW2_e [F, H] = a_s^T dY over the expert's rows
+      A = &p.at; B = &p.dyt;
+      a.M = F; a.N = H;
+      a.out = p.out; a.ldo = H; a.out_estride = (int64_t)F * H;
+      break;
+    case ROLE_FC1_WGRAD:  // dW1_e [N1, H] = dZ^T X over the expert's rows
+      A = &p.dzt; B = &p.xt;
+      a.M = N1; a.N = H;
+      a.out = p.out; a.ldo = H; a.out_estride = (int64_t)N1 * H;
+      break;
+  }
+  if (!tmap_fp8(&a.tmA, *A) || !tmap_fp8(&a.tmB, *B)) return cudaErrorInvalidValue;
+  a.sfa = A->s; a.sfa_pad = A->s_pad;
+  a.sfb = B->s; a.sfb_pad = B->s_pad;
+  const int kid = kKid[p.role];
+  switch (p.role) {
+    case ROLE_FC1_FPROP: return launch_mx<EPI_GLU, false>(a, grid, s, kid);
+    case ROLE_FC2_DGRAD: return launch_mx<EPI_DGLU, false>(a, grid, s, kid);
+    case ROLE_FC2_FPROP:
+    case ROLE_FC1_DGRAD: return launch_mx<EPI_STORE, false>(a, grid, s, kid);
+    default: {
+      const int64_t tiles = (int64_t)p.E * ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
+      grid = (int)std::min<int64_t>(grid, tiles);
+      return launch_mx<EPI_STORE, true>(a, grid, s, kid);
+    }
+  }
+}
+
+}  // namespace moe

@@ -32,6 +32,12 @@ __global__ void pack_fc1_kernel(const uint16_t* src, uint16_t* dst, int E, int H
 void launch_mxfp8_quantize(const void* in, int64_t M, int64_t N, int rowwise, int colwise,
                            uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                            int num_sms, cudaStream_t s);
+// Operand quantisation for the block-scaled GEMM: input rows grouped by G (output stride Gp,
+// padding rows zero), scales in the MMA slab layout (rows padded to 128). A NULL q_row or
+// q_col skips that direction.
+void launch_mxfp8_quantize_mma(const void* in, int64_t M, int64_t N, int64_t G, int64_t Gp,
+                               uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                               int num_sms, cudaStream_t s);
 
 // gemm.cu --------------------------------------------------------------------------------
 struct ActDev {
@@ -75,5 +81,34 @@ struct GemmProblem {
 int gemm_bn(int role);
 int dprob_parts(int F);  // partial d_prob columns per row written by the FC2 dgrad epilogue
 cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s);
+
+// gemm_mx.cu ------------------------------------------------------------------------------
+// One MXFP8 GEMM operand: E4M3 codes [rows, cols] (cols = the reduction dimension) and its
+// scales in the MMA slab layout with rows padded to s_pad (a multiple of 128).
+struct MxOperand {
+  uint8_t* q;
+  uint8_t* s;
+  int64_t rows, cols, s_pad;
+};
+
+struct MxProblem {
+  int role;  // GemmRole
+  int E, H, F, N1, N1p, Fp;  // N1p, Fp: per-expert weight rows padded to 128
+  int64_t R_cap;             // rows of every permuted buffer (multiple of 128)
+  const int32_t* offsets;    // [E+1], segments 128-row aligned
+  // row-wise (K = last dim) and column-wise transposed copies of each GEMM input
+  MxOperand x, xt, a, at, dy, dyt, dz, dzt, w1, w1t, w2, w2t;
+  const float* row_prob;
+  const void* z;             // bf16 [R_cap, N1] saved FC1 output
+  void* out;                 // bf16 role output (z for FC1, y_perm, dx_perm, dW2, dW1)
+  float* dprob_part;
+  int gated, ilv;
+  ActDev act;
+  int* err;
+  int num_ctas;
+};
+
+int dprob_parts_mx(int F);
+cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s);
 
 }  // namespace moe

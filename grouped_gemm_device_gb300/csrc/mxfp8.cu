@@ -6,44 +6,47 @@
 // 0..127 produce the row-wise blocks (64 rows x 2 blocks) and threads 128..255 the
 // column-wise blocks (64 columns x 2 blocks) written transposed, so each output block is one
 // contiguous 32-byte run in global memory.
+//
+// Rows may be grouped: input row g*G + i (i < G) becomes output row g*Gp + i, and rows
+// g*Gp + G .. g*Gp + Gp - 1 are written as zeros (per-expert padding of the operands of the
+// block-scaled grouped GEMM). Scales are written either in the logical layout
+// ([rows, cols/32], [cols, rows/32]) or in the MMA-ready slab layout of sf_mma_offset.
 #include "kernels.cuh"
 
 namespace moe {
 
-// Quantise 32 fp32 values (one block) into 32 E4M3 bytes (as 8 words) and return the scale
-// byte.
-MOE_DEVICE uint32_t mx_quant_block(const float (&v)[32], uint32_t (&q)[8]) {
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  const int e = mx_block_exponent(amax);
-  const float inv = mx_inv_scale(e);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint32_t lo = cvt_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv);
-    uint32_t hi = cvt_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv);
-    q[i] = lo | (hi << 16);
-  }
-  return (uint32_t)(e + 127);
-}
+struct MxQuantArgs {
+  const uint16_t* in;
+  int64_t M, N;     // input [M, N] bf16
+  int64_t G, Gp;    // row groups of G input rows, output group stride Gp (>= G)
+  int rowwise, colwise;
+  uint8_t* q_row;   // [Mv, N]       Mv = (M / G) * Gp
+  uint8_t* s_row;
+  uint8_t* q_col;   // [N, Mv]
+  uint8_t* s_col;
+  int sf_mma;       // 0: logical scale layout, 1: MMA slab layout
+  int64_t srow_pad; // MMA layout: padded row count of the row-wise scales (multiple of 128)
+  int64_t scol_pad; // MMA layout: padded row count of the column-wise scales
+};
 
-__global__ void __launch_bounds__(256) mxfp8_quantize_kernel(
-    const uint16_t* __restrict__ in, int64_t M, int64_t N, int rowwise, int colwise,
-    uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col,
-    uint8_t* __restrict__ s_col) {
+__global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const MxQuantArgs a) {
   __shared__ __align__(16) uint16_t tile[64][64 + 8];
-  const int64_t tiles_m = (M + 63) / 64, tiles_n = (N + 63) / 64;
+  const int64_t Mv = (a.M / a.G) * a.Gp;
+  const int64_t tiles_m = (Mv + 63) / 64, tiles_n = (a.N + 63) / 64;
   const int tid = threadIdx.x;
   for (int64_t t = blockIdx.x; t < tiles_m * tiles_n; t += gridDim.x) {
     const int64_t r0 = (t / tiles_n) * 64, c0 = (t % tiles_n) * 64;
     __syncthreads();
-    // stage: 64 rows x 8 uint4 (8 bf16 each); out-of-range parts are zero
+    // stage: 64 (virtual) rows x 8 uint4 (8 bf16 each); padding and out-of-range parts are 0
     for (int i = tid; i < 64 * 8; i += 256) {
       const int rr = i >> 3, cc = (i & 7) * 8;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r0 + rr < M && c0 + cc < N)
-        v = *reinterpret_cast<const uint4*>(in + (r0 + rr) * N + c0 + cc);
-      *reinterpret_cast<uint4*>(&tile[rr][cc]) = v;
+      const int64_t v = r0 + rr;
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (v < Mv && c0 + cc < a.N) {
+        const int64_t g = v / a.Gp, k = v - g * a.Gp;
+        if (k < a.G) val = *reinterpret_cast<const uint4*>(a.in + (g * a.G + k) * a.N + c0 + cc);
+      }
+      *reinterpret_cast<uint4*>(&tile[rr][cc]) = val;
     }
     __syncthreads();
     float v[32];
@@ -51,42 +54,67 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(
     if (tid < 128) {
       const int rr = tid >> 1, blk = tid & 1;
       const int64_t row = r0 + rr, col = c0 + blk * 32;
-      if (rowwise && row < M && col < N) {
+      if (a.rowwise && row < Mv && col < a.N) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          v[i] = __uint_as_float((uint32_t)tile[rr][blk * 32 + i] << 16);
-        uint32_t s = mx_quant_block(v, q);
-        uint4* dst = reinterpret_cast<uint4*>(q_row + row * N + col);
+        for (int i = 0; i < 4; ++i) {
+          const uint4 w = *reinterpret_cast<const uint4*>(&tile[rr][blk * 32 + 8 * i]);
+          v[8 * i + 0] = bf16_lo(w.x); v[8 * i + 1] = bf16_hi(w.x);
+          v[8 * i + 2] = bf16_lo(w.y); v[8 * i + 3] = bf16_hi(w.y);
+          v[8 * i + 4] = bf16_lo(w.z); v[8 * i + 5] = bf16_hi(w.z);
+          v[8 * i + 6] = bf16_lo(w.w); v[8 * i + 7] = bf16_hi(w.w);
+        }
+        const uint32_t s = mx_quant_block(v, q);
+        uint4* dst = reinterpret_cast<uint4*>(a.q_row + row * a.N + col);
         dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
         dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-        s_row[row * (N / 32) + col / 32] = (uint8_t)s;
+        const int64_t so = a.sf_mma ? sf_mma_offset(row, col / 32, a.srow_pad)
+                                    : row * (a.N / 32) + col / 32;
+        a.s_row[so] = (uint8_t)s;
       }
     } else {
       const int cc = (tid - 128) & 63, rb = (tid - 128) >> 6;
       const int64_t col = c0 + cc, row = r0 + rb * 32;
-      if (colwise && col < N && row < M) {
+      if (a.colwise && col < a.N && row < Mv) {
 #pragma unroll
         for (int i = 0; i < 32; ++i)
           v[i] = __uint_as_float((uint32_t)tile[rb * 32 + i][cc] << 16);
-        uint32_t s = mx_quant_block(v, q);
-        uint4* dst = reinterpret_cast<uint4*>(q_col + col * M + row);
+        const uint32_t s = mx_quant_block(v, q);
+        uint4* dst = reinterpret_cast<uint4*>(a.q_col + col * Mv + row);
         dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
         dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-        s_col[col * (M / 32) + row / 32] = (uint8_t)s;
+        const int64_t so = a.sf_mma ? sf_mma_offset(col, row / 32, a.scol_pad)
+                                    : col * (Mv / 32) + row / 32;
+        a.s_col[so] = (uint8_t)s;
       }
     }
   }
 }
 
+static void launch(const MxQuantArgs& a, int num_sms, cudaStream_t s) {
+  const int64_t Mv = (a.M / a.G) * a.Gp;
+  const int64_t tiles = ((Mv + 63) / 64) * ((a.N + 63) / 64);
+  if (tiles == 0) return;
+  const int grid = (int)std::min<int64_t>(tiles, (int64_t)num_sms * 8);
+  mxfp8_quantize_kernel<<<grid, 256, 0, s>>>(a);
+  count_launch(s, MOE_K_MXFP8_QUANTIZE);
+}
+
 void launch_mxfp8_quantize(const void* in, int64_t M, int64_t N, int rowwise, int colwise,
                            uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                            int num_sms, cudaStream_t s) {
-  const int64_t tiles = ((M + 63) / 64) * ((N + 63) / 64);
-  if (tiles == 0) return;
-  int grid = (int)std::min<int64_t>(tiles, (int64_t)num_sms * 8);
-  mxfp8_quantize_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(in), M, N, rowwise,
-                                             colwise, q_row, s_row, q_col, s_col);
-  count_launch(s, MOE_K_MXFP8_QUANTIZE);
+  MxQuantArgs a{static_cast<const uint16_t*>(in), M, N, M, M, rowwise, colwise,
+                q_row, s_row, q_col, s_col, 0, 0, 0};
+  launch(a, num_sms, s);
+}
+
+void launch_mxfp8_quantize_mma(const void* in, int64_t M, int64_t N, int64_t G, int64_t Gp,
+                               uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                               int num_sms, cudaStream_t s) {
+  const int64_t Mv = (M / G) * Gp;
+  MxQuantArgs a{static_cast<const uint16_t*>(in), M, N, G, Gp, q_row != nullptr,
+                q_col != nullptr, q_row, s_row, q_col, s_col, 1, (Mv + 127) / 128 * 128,
+                (N + 127) / 128 * 128};
+  launch(a, num_sms, s);
 }
 
 }  // namespace moe

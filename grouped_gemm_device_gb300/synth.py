@@ -81,13 +81,13 @@ CONFIGS = {
     "tiny": LayerConfig("tiny", T=512, E=4, k=2, H=128, F=256, seed=0),
     "mixtral_bf16": LayerConfig("mixtral_bf16", T=8192, E=8, k=2, H=4096, F=14336, seed=1),
     "mixtral_mxfp8": LayerConfig("mixtral_mxfp8", T=16384, E=8, k=2, H=4096, F=14336,
-                                 precision="mxfp8", seed=2),
+                                 precision="mxfp8", seed=2, align=128),
     "dsv3_mxfp8": LayerConfig("dsv3_mxfp8", T=4096, E=256, k=8, H=7168, F=2048,
-                              precision="mxfp8", seed=3, zipf_s=1.1),
+                              precision="mxfp8", seed=3, zipf_s=1.1, align=128),
     "gptoss_bf16": LayerConfig("gptoss_bf16", T=16384, E=128, k=4, H=2880, F=2880, seed=4,
                                **_CLAMP),
     "gptoss_mxfp8": LayerConfig("gptoss_mxfp8", T=16384, E=128, k=4, H=2880, F=2880, seed=4,
-                                precision="mxfp8", **_CLAMP),
+                                precision="mxfp8", align=128, **_CLAMP),
 }
 
 

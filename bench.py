@@ -79,6 +79,41 @@ def gemm_flops(cfg):
     }
 
 
+QUANT_NAMES = ("mxfp8_quant_x", "mxfp8_quant_w1", "mxfp8_quant_w2", "mxfp8_quant_dy")
+
+
+def kernel_bytes(cfg):
+    """Algorithmic HBM bytes per launch: each operand read once, each result written once
+    (R = routed rows; MXFP8 data is 1 byte plus one scale byte per 32)."""
+    R, T, E = cfg.R, cfg.T, cfg.E
+    H, F, N1 = cfg.H, cfg.F, cfg.N1
+    R_cap = cfg.R_cap
+    if cfg.precision == "mxfp8":
+        s = 33.0 / 32.0
+        return {
+            "gemm_fc1_fprop": R * H * s + E * N1 * H * s + R * N1 * 2 + 2 * R * F * s,
+            "gemm_fc2_fprop": R * F * s + E * F * H * s + R * H * 2,
+            "gemm_fc2_dgrad": R * H * s + E * F * H * s + R * N1 * 2 + 2 * R * N1 * s,
+            "gemm_fc2_wgrad": R * F * s + R * H * s + E * F * H * 2,
+            "gemm_fc1_dgrad": R * N1 * s + E * N1 * H * s + R * H * 2,
+            "gemm_fc1_wgrad": R * N1 * s + R * H * s + E * N1 * H * 2,
+            "gather_x": R_cap * H * 2 + R * H * 2, "gather_dy": R_cap * H * 2 + R * H * 2,
+            "combine_y": R * H * 2 + T * H * 2, "combine_dx": R * H * 2 + T * H * 2,
+            "mxfp8_quant_x": R_cap * H * (2 + 2 * s), "mxfp8_quant_dy": R_cap * H * (2 + 2 * s),
+            "mxfp8_quant_w1": E * N1 * H * (2 + 2 * s), "mxfp8_quant_w2": E * F * H * (2 + 2 * s),
+        }
+    return {
+        "gemm_fc1_fprop": (R * H + E * N1 * H + R * N1 + R * F) * 2,
+        "gemm_fc2_fprop": (R * F + E * F * H + R * H) * 2,
+        "gemm_fc2_dgrad": (R * H + E * F * H + 2 * R * N1) * 2,
+        "gemm_fc2_wgrad": (R * F + R * H + E * F * H) * 2,
+        "gemm_fc1_dgrad": (R * N1 + E * N1 * H + R * H) * 2,
+        "gemm_fc1_wgrad": (R * N1 + R * H + E * N1 * H) * 2,
+        "gather_x": (R_cap * H + R * H) * 2, "gather_dy": (R_cap * H + R * H) * 2,
+        "combine_y": (R * H + T * H) * 2, "combine_dx": (R * H + T * H) * 2,
+    }
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -286,8 +321,7 @@ def main():
     barrier(world)
     g.load()
     cfg = config_of(args)
-    if cfg.precision != "bf16":
-        raise SystemExit(f"config {cfg.name}: only the BF16 path is built in this version")
+    mx = cfg.precision == "mxfp8"
     dev = torch.device("cuda", local)
     t_gen = time.time()
     hin = host_inputs(cfg)
@@ -312,12 +346,13 @@ def main():
         layer.forward(w1p, w2, T)
         layer.backward(dy, w1p, w2, T)
 
+    n_w = g.moe_launch_count()
     for _ in range(max(args.warmup, 1)):
         step()
     torch.cuda.synchronize()
+    per_step_launches = (g.moe_launch_count() - n_w) // max(args.warmup, 1)
     assert layer.device_error() == 0, "device error during warm-up"
 
-    per_step_launches = 13
     tl = g.Timeline(min(4096, args.steps * per_step_launches + 16))
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -347,18 +382,44 @@ def main():
     value = flops * world / (ms_max / 1e3) / 1e12
     peaks, peak_src = load_peaks()
 
-    # per-kernel durations from the launch timeline
+    # per-kernel durations from the launch timeline; repeated kernels of one step (the four
+    # MXFP8 quantiser launches) are told apart by their order within the step
     per = {}
-    for name, dur in tl.durations(ev0):
-        per.setdefault(name, []).append(dur)
+    seen = {}
+    for i, (name, dur) in enumerate(tl.durations(ev0)):
+        if i % per_step_launches == 0:
+            seen = {}
+        j = seen.get(name, 0)
+        seen[name] = j + 1
+        per.setdefault(name if name != "mxfp8_quantize" else QUANT_NAMES[j], []).append(dur)
     kernel_ms = {k: sum(v) / len(v) for k, v in per.items()}
     gf = gemm_flops(cfg)
-    dom = max(gf, key=lambda k: sum(per.get(k, [0.0])))
+    kb = kernel_bytes(cfg)
+    # the GEMMs are timed inside a long step: sustained tensor peak; fp8 = 2x bf16 (nominal)
+    p_tc = peaks.get("bf16_tflops_sustained", 1700.0) * (2.0 if mx else 1.0)
+    p_bw = peaks.get("hbm_gbs", 6800.0)
+    dom = max((k for k in kernel_ms if k in gf or k in kb), key=lambda k: sum(per[k]))
     dom_ms = kernel_ms[dom]
-    achieved = gf[dom] / (dom_ms / 1e3) / 1e12
-    peak = peaks.get("bf16_tflops_sustained", 1700.0)
+    t_tc = gf.get(dom, 0.0) / (p_tc * 1e12)
+    t_bw = kb.get(dom, 0.0) / (p_bw * 1e9)
+    if t_tc >= t_bw:
+        bound, achieved, peak, unit = "tensor", gf[dom] / (dom_ms / 1e3) / 1e12, p_tc, "TFLOP/s"
+    else:
+        bound, achieved, peak, unit = "hbm", kb[dom] / (dom_ms / 1e3) / 1e9, p_bw, "GB/s"
     traffic = traffic_for(dom, cfg.name)
     gemm_total_ms = sum(kernel_ms[k] for k in gf if k in kernel_ms)
+    step_bytes = sum(kb.values())
+    step_ideal_ms = 1e3 * max(flops / (p_tc * 1e12), step_bytes / (p_bw * 1e9))
+    per_kernel = {}
+    for k, v in sorted(kernel_ms.items()):
+        ent = {"ms": round(v, 4)}
+        if k in gf:
+            ent["tflops"] = round(gf[k] / (v / 1e3) / 1e12, 1)
+            ent["frac_tensor"] = round(gf[k] / (v / 1e3) / 1e12 / p_tc, 3)
+        if k in kb:
+            ent["gbs"] = round(kb[k] / (v / 1e3) / 1e9, 1)
+            ent["frac_hbm"] = round(kb[k] / (v / 1e3) / 1e9 / p_bw, 3)
+        per_kernel[k] = ent
 
     # end to end through the C ABI with host buffers: pinned H2D of the step's inputs and
     # D2H of its results inside the timed region
@@ -407,24 +468,33 @@ def main():
                "tokens_per_s_equiv": (fl / dt) / (flops / T)}
 
     if rank == 0:
+        tc_kind = ("2 x bf16_tflops_sustained (fp8/bf16 nominal ratio)" if mx
+                   else "bf16_tflops_sustained") + f" ({peak_src})"
+        w_bytes = 2 * 2 * cfg.E * (cfg.N1 + cfg.F) * cfg.H
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3+e8m0 (fp32 accumulate)" if mx else "bf16",
             "data": "synthetic",
             "config": {"workload": workload_name(cfg), "parallelism": f"replicas x{world}",
-                       "l2": "no flush: each step streams ~5.6 GB of weights and weight "
-                             "gradients, > 129 MB L2", "sm_margin": args.sm_margin,
-                       "flops_per_step": flops},
+                       "l2": f"no flush: each step streams {w_bytes / 1e9:.1f} GB of bf16 "
+                             "weights and weight gradients, > 129 MB L2",
+                       "sm_margin": args.sm_margin, "flops_per_step": flops},
             "tokens_per_s": cfg.T * world / (ms_max / 1e3),
-            "pct_tensor_peak": {"value": 100 * value / world / peak, "peak_tflops": peak,
-                                "peak_kind": f"bf16_tflops_sustained ({peak_src})"},
+            "pct_tensor_peak": {"value": 100 * value / world / p_tc, "peak_tflops": p_tc,
+                                "peak_kind": tc_kind},
+            "step_roofline": {"ideal_ms": step_ideal_ms, "frac": step_ideal_ms / ms,
+                              "bytes": step_bytes,
+                              "bound": "tensor" if flops / (p_tc * 1e12) >=
+                              step_bytes / (p_bw * 1e9) else "hbm"},
             "gpu_launches": int(launches),
-            "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                         "peak_kind": f"bf16_tflops_sustained ({peak_src})",
-                         "flops_per_launch": gf[dom], "ms_per_launch": dom_ms},
-            "kernels_ms": {k: round(v, 4) for k, v in sorted(kernel_ms.items())},
+            "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
+                         "unit": unit, "frac": achieved / peak, "traffic": traffic,
+                         "peak_kind": tc_kind if bound == "tensor" else f"hbm_gbs ({peak_src})",
+                         "flops_per_launch": gf.get(dom), "bytes_per_launch": kb.get(dom),
+                         "ms_per_launch": dom_ms},
+            "kernels": per_kernel,
             "gemm_share": gemm_total_ms / ms,
             "timeline_events": n_rec,
             "e2e": e2e,

@@ -109,8 +109,11 @@ struct MxOps {
   int N1p, Fp;
 };
 
+// Scales of an operand [rows, cols] in the slab layout, plus 1 KB: the B operand's scales
+// are fetched 256 rows at a time, so the last tile of the last k-group may read up to 128
+// rows past the padded end.
 static size_t mx_sf_bytes(int64_t rows, int64_t cols) {
-  return (size_t)((cols / 32 + 3) / 4) * (size_t)round128(rows) * 4;
+  return (size_t)((cols / 32 + 3) / 4) * (size_t)round128(rows) * 4 + 1024;
 }
 
 // Lay the operands out from `base` (an address or 0 for offsets); returns the end offset.

@@ -358,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) {
               g[i] = __uint_as_float(r[i]);
               l[i] = __uint_as_float(rl[i]);
-              v[i] = prob * act_fwd(p.act, g[i], l[i]);
             }
+            glu_fwd32(p.act, prob, g, l, v);
             if (row_ok) {
               store_bf16x32(zrow + t.n0 + gcol, g);
               store_bf16x32(zrow + t.n0 + lcol, l);
@@ -404,15 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_32x32b_x32(taddr + cc, r);
             tmem_ld_wait();
             if (!row_ok) continue;
+            float das[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float das = __uint_as_float(r[i]);
-              float dg, dl;
-              const float a = act_bwd(p.act, g[i], l[i], prob * das, dg, dl);
-              dp += das * a;
-              g[i] = dg;
-              l[i] = dl;
-            }
+            for (int i = 0; i < 32; ++i) das[i] = __uint_as_float(r[i]);
+            dp += glu_bwd32(p.act, prob, das, g, l);
             store_bf16x32(dzrow + gcol, g);
             store_bf16x32(dzrow + lcol, l);
           } else {

@@ -11,19 +11,21 @@ namespace moe {
 // ------------------------------------------------------------------ activations (fp32)
 MOE_DEVICE float phi_cdf(float g) { return 0.5f * (1.0f + erff(g * 0.70710678118654752f)); }
 
-MOE_DEVICE float act_fwd(const ActDev& a, float g, float l) {
-  if (a.kind == MOE_ACT_CLAMPED_SWIGLU) {
+template <int KIND>
+MOE_DEVICE float act_fwd_k(const ActDev& a, float g, float l) {
+  if (KIND == MOE_ACT_CLAMPED_SWIGLU) {
     const float gc = fminf(g, a.gate_max);
     const float lc = fminf(fmaxf(l, a.lin_lo), a.lin_hi);
     return (lc + a.lin_offset) * gc * sigmoidf_fast(a.beta * gc);
   }
-  if (a.kind == MOE_ACT_GEGLU) return l * g * phi_cdf(g);
+  if (KIND == MOE_ACT_GEGLU) return l * g * phi_cdf(g);
   return l * g * sigmoidf_fast(a.beta * g);  // SwiGLU
 }
 
 // returns a (unscaled) and writes d_gate, d_lin for the upstream gradient dA
-MOE_DEVICE float act_bwd(const ActDev& a, float g, float l, float dA, float& dg, float& dl) {
-  if (a.kind == MOE_ACT_CLAMPED_SWIGLU) {
+template <int KIND>
+MOE_DEVICE float act_bwd_k(const ActDev& a, float g, float l, float dA, float& dg, float& dl) {
+  if (KIND == MOE_ACT_CLAMPED_SWIGLU) {
     const float gc = fminf(g, a.gate_max);
     const float lc = fminf(fmaxf(l, a.lin_lo), a.lin_hi);
     const float s = sigmoidf_fast(a.beta * gc);
@@ -33,7 +35,7 @@ MOE_DEVICE float act_bwd(const ActDev& a, float g, float l, float dA, float& dg,
     dl = (l >= a.lin_lo && l <= a.lin_hi) ? dA * sw : 0.0f;
     return (lc + a.lin_offset) * sw;
   }
-  if (a.kind == MOE_ACT_GEGLU) {
+  if (KIND == MOE_ACT_GEGLU) {
     const float P = phi_cdf(g);
     const float pdf = 0.39894228040143268f * __expf(-0.5f * g * g);
     dg = dA * l * (P + g * pdf);
@@ -44,6 +46,58 @@ MOE_DEVICE float act_bwd(const ActDev& a, float g, float l, float dA, float& dg,
   dg = dA * l * s * (1.0f + a.beta * g * (1.0f - s));
   dl = dA * g * s;
   return l * g * s;
+}
+
+MOE_DEVICE float act_fwd(const ActDev& a, float g, float l) {
+  if (a.kind == MOE_ACT_CLAMPED_SWIGLU) return act_fwd_k<MOE_ACT_CLAMPED_SWIGLU>(a, g, l);
+  if (a.kind == MOE_ACT_GEGLU) return act_fwd_k<MOE_ACT_GEGLU>(a, g, l);
+  return act_fwd_k<MOE_ACT_SWIGLU>(a, g, l);
+}
+
+MOE_DEVICE float act_bwd(const ActDev& a, float g, float l, float dA, float& dg, float& dl) {
+  if (a.kind == MOE_ACT_CLAMPED_SWIGLU) return act_bwd_k<MOE_ACT_CLAMPED_SWIGLU>(a, g, l, dA, dg, dl);
+  if (a.kind == MOE_ACT_GEGLU) return act_bwd_k<MOE_ACT_GEGLU>(a, g, l, dA, dg, dl);
+  return act_bwd_k<MOE_ACT_SWIGLU>(a, g, l, dA, dg, dl);
+}
+
+// 32-wide forms with the activation chosen once per block (keeps the unrolled code of one
+// activation contiguous instead of interleaving all three per element).
+// v[i] = prob * act(g[i], l[i])
+MOE_DEVICE void glu_fwd32(const ActDev& a, float prob, const float* g, const float* l,
+                          float (&v)[32]) {
+  if (a.kind == MOE_ACT_CLAMPED_SWIGLU) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = prob * act_fwd_k<MOE_ACT_CLAMPED_SWIGLU>(a, g[i], l[i]);
+  } else if (a.kind == MOE_ACT_GEGLU) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = prob * act_fwd_k<MOE_ACT_GEGLU>(a, g[i], l[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = prob * act_fwd_k<MOE_ACT_SWIGLU>(a, g[i], l[i]);
+  }
+}
+
+// In place: g <- d_gate, l <- d_linear for dA = prob * das; returns sum_i das[i] * a[i].
+template <int KIND>
+MOE_DEVICE float glu_bwd32_k(const ActDev& a, float prob, const float (&das)[32],
+                             float (&g)[32], float (&l)[32]) {
+  float dp = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float dg, dl;
+    const float av = act_bwd_k<KIND>(a, g[i], l[i], prob * das[i], dg, dl);
+    dp += das[i] * av;
+    g[i] = dg;
+    l[i] = dl;
+  }
+  return dp;
+}
+MOE_DEVICE float glu_bwd32(const ActDev& a, float prob, const float (&das)[32], float (&g)[32],
+                           float (&l)[32]) {
+  if (a.kind == MOE_ACT_CLAMPED_SWIGLU)
+    return glu_bwd32_k<MOE_ACT_CLAMPED_SWIGLU>(a, prob, das, g, l);
+  if (a.kind == MOE_ACT_GEGLU) return glu_bwd32_k<MOE_ACT_GEGLU>(a, prob, das, g, l);
+  return glu_bwd32_k<MOE_ACT_SWIGLU>(a, prob, das, g, l);
 }
 
 MOE_DEVICE void store_bf16x32(void* dst, const float (&v)[32]) {

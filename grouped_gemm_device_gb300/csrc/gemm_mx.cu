@@ -6,15 +6,17 @@
 //
 // Every operand is an E4M3 matrix quantised along its own reduction dimension and stored
 // K-major ([rows, K]); its scales sit in the MMA slab layout (sf_mma_offset). A CTA:
-//   warp 0   TMA of the A and B k-blocks (128 x 128 bytes each) and a 1-D bulk copy of their two
-//            512-byte scale slabs, all counted on one mbarrier,
+//   warp 0   TMA of the A (128 x 128 B) and B (256 x 128 B) k-blocks and one 1-D bulk copy of
+//            their 512 + 1024 bytes of scale slabs, all counted on one mbarrier,
 //   warp 1   TMEM owner; one thread copies the stage's scales into TMEM (tcgen05.cp) and issues
-//            four tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each, scale byte = K step),
-//   warps 2-9 epilogue: bf16 store, or GLU / dGLU with fused row-wise and column-wise
-//            (transposed) MXFP8 quantisation of the result: a row's 32-column block is one
-//            thread's registers; a column's 32-row block is the 32 lanes of one warp.
-// Tiles are 128 x 128 with two TMEM accumulators (256 columns) plus 8 scale columns per
-// stage. Expert segments are padded to 128 rows so that every tile starts on a scale slab.
+//            four tcgen05.mma.kind::mxf8f6f4.block_scale 128x256x32 (scale byte = K step),
+//   warps 2-9 epilogue: drain the accumulator into registers as packed bf16 (warp w takes TMEM
+//            lanes 32*(w%4).. and 128 of the 256 columns), release TMEM, then bf16 store, or
+//            GLU / dGLU with fused row-wise and column-wise (transposed) MXFP8 quantisation.
+// The tile is 128 x 256 because a 128 x 256 x 32 MMA runs at the full fp8 rate while 128-wide
+// ones do not; TMEM then holds one accumulator (256 columns) plus 12 scale columns per stage,
+// and the register drain lets the next tile's MMAs start while the epilogue works. Expert
+// segments are padded to 128 rows so that every tile starts on a scale slab.
 #include "gemm_common.cuh"
 
 namespace moe {
@@ -22,14 +24,14 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 128;
+constexpr int BN = 256;
 constexpr int BK = 128;  // fp8 elements (bytes) per k-block: one 128-byte swizzle row
 constexpr int MMA_K = 32;
-constexpr int STAGES = 6;
+constexpr int STAGES = 3;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxE = 256;
-constexpr int kSfCol = 2 * BN;  // first TMEM column of the per-stage scale factors
+constexpr int kSfCol = BN;  // first TMEM column of the per-stage scale factors
 constexpr int kTmemCols = 512;
 
 enum { EPI_STORE = 0, EPI_GLU = 1, EPI_DGLU = 2 };
@@ -63,7 +65,6 @@ struct MxArgs {
   float* dprob_part;
   int nparts;
   int gated;
-  int ilv;
   ActDev act;
   int* err;
 };
@@ -71,17 +72,20 @@ struct MxArgs {
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SF_BYTES = 512;                      // per operand per stage
+constexpr int SFA_BYTES = 512;   // 128 rows x 4 k-blocks
+constexpr int SFB_BYTES = 1024;  // 256 rows x 4 k-blocks
 constexpr int DATA = STAGES * STAGE_BYTES;
 constexpr int SF_OFF = DATA;
-constexpr int CTRL_OFF = SF_OFF + STAGES * 2 * SF_BYTES;
+constexpr int XPOSE_OFF = SF_OFF + STAGES * (SFA_BYTES + SFB_BYTES);
+constexpr int XPOSE_WARP_BYTES = 32 * 33 * 4;  // 32 x 32 fp32 transpose, padded rows
+constexpr int CTRL_OFF = XPOSE_OFF + kEpiWarps * XPOSE_WARP_BYTES;
 constexpr int SMEM_TOTAL = CTRL_OFF + 4096 + 1024;
 
 struct Ctrl {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t tfull;
+  uint64_t tempty;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -137,24 +141,36 @@ MOE_DEVICE void mx_store_row_block(const float (&v)[32], uint8_t* q, uint8_t* s_
   s_row[sf_mma_offset(row, col / 32, s_pad)] = (uint8_t)sb;
 }
 
-// Column-wise MXFP8 of the warp's 32 rows x 32 columns (this lane holds one row): each column's
-// block maximum is a warp reduction; the column's 32 codes are stored as one 32-byte run of the
-// transposed output q[col][row0 .. row0+31].
-MOE_DEVICE void mx_store_col_blocks(const float (&v)[32], uint8_t* q, uint8_t* s_col, int64_t row0,
-                                    int64_t col0, int64_t ld, int64_t s_pad, int lane) {
+// Column-wise MXFP8 of the warp's 32 rows x 32 columns (this lane holds one row): the block is
+// transposed through the warp's shared-memory tile, lane j then quantises column col0 + j and
+// stores its 32 codes as one run of the transposed output q[col][row0 .. row0+31].
+MOE_DEVICE void mx_store_col_blocks(const float (&v)[32], float* xp, uint8_t* q, uint8_t* s_col,
+                                    int64_t row0, int64_t col0, int64_t ld, int64_t s_pad,
+                                    int lane) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    float m = fabsf(v[j]);
+  for (int i = 0; i < 32; ++i) xp[lane * 33 + i] = v[i];
+  __syncwarp();
+  float w[32];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-    const int e = mx_block_exponent(m);
-    const uint32_t code = cvt_e4m3x2(v[j] * mx_inv_scale(e), 0.f) & 0xFFu;
-    q[(col0 + j) * ld + row0 + lane] = (uint8_t)code;
-    if (lane == j) s_col[sf_mma_offset(col0 + j, row0 / 32, s_pad)] = (uint8_t)(e + 127);
+  for (int i = 0; i < 32; ++i) w[i] = xp[i * 33 + lane];
+  __syncwarp();
+  uint32_t qq[8];
+  const uint32_t sb = mx_quant_block(w, qq);
+  uint4* dst = reinterpret_cast<uint4*>(q + (col0 + lane) * ld + row0);
+  dst[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
+  dst[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
+  s_col[sf_mma_offset(col0 + lane, row0 / 32, s_pad)] = (uint8_t)sb;
+}
+
+MOE_DEVICE void unpack32(const uint32_t* pk, float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[2 * i] = bf16_lo(pk[i]);
+    v[2 * i + 1] = bf16_hi(pk[i]);
   }
 }
 
-template <int EPI, bool KG>
+template <int EPI, bool KG, int ILV>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __grid_constant__ MxArgs p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -170,10 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
       mbar_init(&c.full[s], 1);
       mbar_init(&c.empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&c.tfull[i], 1);
-      mbar_init(&c.tempty[i], kEpiWarps);
-    }
+    mbar_init(&c.tfull, 1);
+    mbar_init(&c.tempty, kEpiWarps);
     mbar_init(&c.drain, 1);
     fence_mbar_init();
     c.abort = 0;
@@ -229,9 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
           if (!mbar_wait(&c.empty[stage], phase ^ 1, abort, p.err)) break;
           uint8_t* sA = smem + stage * STAGE_BYTES;
           uint8_t* sB = sA + A_BYTES;
-          uint8_t* sfA = smem + SF_OFF + stage * 2 * SF_BYTES;
+          uint8_t* sfA = smem + SF_OFF + stage * (SFA_BYTES + SFB_BYTES);
           uint64_t* bar = &c.full[stage];
-          mbar_arrive_expect_tx(bar, STAGE_BYTES + 2 * SF_BYTES);
+          mbar_arrive_expect_tx(bar, STAGE_BYTES + SFA_BYTES + SFB_BYTES);
 #pragma unroll
           for (int s = 0; s < STAGES; ++s)
             if (s == stage) armed[s] = (int)phase;
@@ -240,9 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
           const int b_k = k0 + t.e * p.b_k_e;
           tma_load_2d(sA, &p.tmA, bar, a_k, a_row);
           tma_load_2d(sB, &p.tmB, bar, b_k, b_row);
-          bulk_load(sfA, p.sfa + ((int64_t)(a_k / BK) * p.sfa_pad + a_row) * 4, SF_BYTES, bar);
-          bulk_load(sfA + SF_BYTES, p.sfb + ((int64_t)(b_k / BK) * p.sfb_pad + b_row) * 4,
-                    SF_BYTES, bar);
+          tma_load_2d(sB + B_BYTES / 2, &p.tmB, bar, b_k, b_row + 128);
+          bulk_load(sfA, p.sfa + ((int64_t)(a_k / BK) * p.sfa_pad + a_row) * 4, SFA_BYTES, bar);
+          bulk_load(sfA + SFA_BYTES, p.sfb + ((int64_t)(b_k / BK) * p.sfb_pad + b_row) * 4,
+                    SFB_BYTES, bar);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -270,11 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
         TileInfo t;
         decode_tile<KG>(tile, p, c, MT, NT, t);
         if (t.nkb == 0) continue;
-        const int acc = acc_i & 1;
-        const uint32_t acc_phase = (acc_i >> 1) & 1;
-        if (!mbar_wait(&c.tempty[acc], acc_phase ^ 1, abort, p.err)) break;
+        // the single accumulator is free once every epilogue warp drained the last tile
+        if (!mbar_wait(&c.tempty, (acc_i & 1) ^ 1, abort, p.err)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
         bool ok = true;
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(&c.full[stage], phase, abort, p.err)) {
@@ -284,17 +297,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
           tc_fence_after();
           const uint32_t sA = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sB = sA + A_BYTES;
-          const uint32_t sfA = smem_u32(smem + SF_OFF + stage * 2 * SF_BYTES);
-          const uint32_t sfa_t = tmem_base + kSfCol + stage * 8;
+          const uint32_t sfA = smem_u32(smem + SF_OFF + stage * (SFA_BYTES + SFB_BYTES));
+          const uint32_t sfa_t = tmem_base + kSfCol + stage * 12;
           const uint32_t sfb_t = sfa_t + 4;
           tmem_cp_32x128b_warpx4(sfa_t, smem_desc_noswizzle(sfA, 0, 128));
-          tmem_cp_32x128b_warpx4(sfb_t, smem_desc_noswizzle(sfA + SF_BYTES, 0, 128));
+          tmem_cp_32x128b_warpx4(sfb_t, smem_desc_noswizzle(sfA + SFA_BYTES, 0, 128));
+          tmem_cp_32x128b_warpx4(sfb_t + 4, smem_desc_noswizzle(sfA + SFA_BYTES + 512, 0, 128));
           const int rem = t.klen - kb * BK;
           const int nsub = rem >= BK ? BK / MMA_K : (rem + MMA_K - 1) / MMA_K;
           for (int ks = 0; ks < nsub; ++ks) {
             const uint64_t ad = smem_desc_sw128(sA + ks * MMA_K, 16, 1024);
             const uint64_t bd = smem_desc_sw128(sB + ks * MMA_K, 16, 1024);
-            mma_mxf8_ss(d_tmem, ad, bd, idesc_mxf8(BM, BN, ks), sfa_t, sfb_t,
+            mma_mxf8_ss(tmem_base, ad, bd, idesc_mxf8(BM, BN, ks), sfa_t, sfb_t,
                         (kb | ks) != 0 ? 1u : 0u);
           }
           issued_any = true;
@@ -305,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
           }
         }
         if (!ok) break;
-        mma_commit(&c.tfull[acc]);
+        mma_commit(&c.tfull);
         ++acc_i;
       }
       if (issued_any) {
@@ -318,7 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
   } else {
     // ------------------------------------------------------------ epilogue warps 2..9
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int half = (warp - 2) >> 2;  // columns [128*half, 128*half + 128) of the tile
+    float* xp = reinterpret_cast<float*>(smem + XPOSE_OFF + (warp - 2) * XPOSE_WARP_BYTES);
     int acc_i = 0;
     for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
       TileInfo t;
@@ -326,127 +341,174 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
       const int row0 = t.m0 + q * 32;  // first row of this warp's 32-row block
       const int row = row0 + lane;
       const bool row_ok = row < t.row_end;
-      const int c0 = half * (BN / 2), c1 = c0 + BN / 2;
+      const int cb = half * 128;       // first tile column of this warp
       if (t.nkb == 0) {
         if (row_ok) {
           uint16_t* o = static_cast<uint16_t*>(p.out) + (int64_t)t.e * p.out_estride +
                         (int64_t)row * p.ldo;
-          for (int cc = c0; cc < c1 && t.n0 + cc < p.N; cc += 32) store_zero_bf16x32(o + t.n0 + cc);
+          for (int cc = cb; cc < cb + 128 && t.n0 + cc < p.N; cc += 32)
+            store_zero_bf16x32(o + t.n0 + cc);
         }
         continue;
       }
-      const int acc = acc_i & 1;
-      const uint32_t acc_phase = (acc_i >> 1) & 1;
-      if (!mbar_wait(&c.tfull[acc], acc_phase, abort, p.err)) break;
+      if (!mbar_wait(&c.tfull, acc_i & 1, abort, p.err)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      uint32_t r[32];
-      float v[32];
-      if (EPI == EPI_STORE) {
-        uint16_t* o = static_cast<uint16_t*>(p.out) + (KG ? (int64_t)t.e * p.out_estride : 0) +
-                      (int64_t)row * p.ldo + t.n0;
-        for (int cc = c0; cc < c1; cc += 32) {
-          if (t.n0 + cc >= p.N) break;
-          tmem_ld_32x32b_x32(taddr + cc, r);
-          tmem_ld_wait();
+      if (EPI == EPI_GLU) {
+        // GLU: drain the 128 columns as fp32 (the activation and its MXFP8 blocks are computed
+        // from the fp32 accumulator), free TMEM, then work from registers
+        float acc[128];
+        {
+          const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + cb;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-          if (row_ok) store_bf16x32(o + cc, v);
+          for (int j = 0; j < 4; ++j) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + 32 * j, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[32 * j + i] = __uint_as_float(r[i]);
+          }
         }
-      } else if (EPI == EPI_GLU) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.tempty);
+        ++acc_i;
         // segments are 128-row aligned, so every row of the tile is inside its segment
         const float prob = p.row_prob[row];
-        uint16_t* zrow = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo;
-        const int per_half = p.gated ? BN / 4 : BN / 2;  // output columns per warp
-        for (int cc = half * per_half; cc < (half + 1) * per_half; cc += 32) {
-          int zcol, acol;
-          if (p.gated) {
-            const int gcol = (cc / p.ilv) * 2 * p.ilv + (cc % p.ilv);
-            if (t.n0 + gcol >= p.N) break;
-            uint32_t rl[32];
-            tmem_ld_32x32b_x32(taddr + gcol, r);
-            tmem_ld_32x32b_x32(taddr + gcol + p.ilv, rl);
-            tmem_ld_wait();
-            float g[32], l[32];
+        uint16_t* zrow = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo + t.n0 + cb;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              g[i] = __uint_as_float(r[i]);
-              l[i] = __uint_as_float(rl[i]);
-              v[i] = prob * act_fwd(p.act, g[i], l[i]);
-            }
-            store_bf16x32(zrow + t.n0 + gcol, g);
-            store_bf16x32(zrow + t.n0 + gcol + p.ilv, l);
-            zcol = gcol;
-            acol = t.n0 / 2 + cc;
-          } else {
-            if (t.n0 + cc >= p.N) break;
-            tmem_ld_32x32b_x32(taddr + cc, r);
-            tmem_ld_wait();
+        for (int j = 0; j < 4; ++j) {  // the saved Z (bf16)
+          if (t.n0 + cb + 32 * j < p.N) {
             float zz[32];
 #pragma unroll
+            for (int i = 0; i < 32; ++i) zz[i] = acc[32 * j + i];
+            store_bf16x32(zrow + 32 * j, zz);
+          }
+        }
+        if (p.gated) {
+          // this half holds 64 gate and 64 linear columns: two 32-wide output blocks
+#pragma unroll
+          for (int c32 = 0; c32 < 2; ++c32) {
+            const int g_off = (c32 * 32 / ILV) * 2 * ILV + (c32 * 32) % ILV;  // within the half
+            const int acol = (t.n0 + cb) / 2 + c32 * 32;
+            if (t.n0 + cb + g_off >= p.N) break;
+            float v[32];
+            glu_fwd32(p.act, prob, &acc[g_off], &acc[g_off + ILV], v);
+            mx_store_row_block(v, p.q_row, p.s_row, row, acol, p.ld_q_row, p.s_row_pad);
+            mx_store_col_blocks(v, xp, p.q_col, p.s_col, row0, acol, p.ld_q_col, p.s_col_pad,
+                                lane);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int acol = t.n0 + cb + 32 * j;
+            if (acol >= p.N) break;
+            float v[32];
+#pragma unroll
             for (int i = 0; i < 32; ++i) {
-              zz[i] = __uint_as_float(r[i]);
-              const float rr = fmaxf(zz[i], 0.f);
+              const float rr = fmaxf(acc[32 * j + i], 0.f);
               v[i] = prob * rr * rr;
             }
-            store_bf16x32(zrow + t.n0 + cc, zz);
-            zcol = cc;
-            acol = t.n0 + cc;
+            mx_store_row_block(v, p.q_row, p.s_row, row, acol, p.ld_q_row, p.s_row_pad);
+            mx_store_col_blocks(v, xp, p.q_col, p.s_col, row0, acol, p.ld_q_col, p.s_col_pad,
+                                lane);
           }
-          (void)zcol;
-          mx_store_row_block(v, p.q_row, p.s_row, row, acol, p.ld_q_row, p.s_row_pad);
-          mx_store_col_blocks(v, p.q_col, p.s_col, row0, acol, p.ld_q_col, p.s_col_pad, lane);
+        }
+        continue;
+      }
+      // drain 128 accumulator columns into registers as packed bf16, then free TMEM
+      uint32_t pk[64];
+      {
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + cb;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + 32 * j, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[16 * j + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.tempty);
+      ++acc_i;
+
+      if (EPI == EPI_STORE) {
+        if (row_ok) {
+          uint16_t* o = static_cast<uint16_t*>(p.out) + (KG ? (int64_t)t.e * p.out_estride : 0) +
+                        (int64_t)row * p.ldo + t.n0 + cb;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (t.n0 + cb + 32 * j < p.N) {
+              uint4* d = reinterpret_cast<uint4*>(o + 32 * j);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                d[i] = make_uint4(pk[16 * j + 4 * i], pk[16 * j + 4 * i + 1],
+                                  pk[16 * j + 4 * i + 2], pk[16 * j + 4 * i + 3]);
+            }
+          }
         }
       } else {  // EPI_DGLU: accumulator = dA_s over F columns
         const float prob = p.row_prob[row];
         float dp = 0.f;
         const uint16_t* zrow = p.z + (int64_t)row * p.ldz;
-        for (int cc = c0; cc < c1; cc += 32) {
-          const int f0 = t.n0 + cc;
+        // one copy of the chunk body (keeps the kernel inside the instruction cache); the
+        // chunk's 16 packed registers are picked by a switch so they stay in registers
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          const int f0 = t.n0 + cb + 32 * j;
           if (f0 >= p.N) break;
+          uint32_t cur[16];
+          switch (j) {
+            case 0:
+#pragma unroll
+              for (int i = 0; i < 16; ++i) cur[i] = pk[i];
+              break;
+            case 1:
+#pragma unroll
+              for (int i = 0; i < 16; ++i) cur[i] = pk[16 + i];
+              break;
+            case 2:
+#pragma unroll
+              for (int i = 0; i < 16; ++i) cur[i] = pk[32 + i];
+              break;
+            default:
+#pragma unroll
+              for (int i = 0; i < 16; ++i) cur[i] = pk[48 + i];
+              break;
+          }
+          float das[32];
+          unpack32(cur, das);
           if (p.gated) {
-            const int gcol = (f0 / p.ilv) * 2 * p.ilv + (f0 % p.ilv);
-            const int lcol = gcol + p.ilv;
+            const int gcol = (f0 / ILV) * 2 * ILV + (f0 % ILV);
+            const int lcol = gcol + ILV;
             float g[32], l[32];
             load_bf16x32(zrow + gcol, g);
             load_bf16x32(zrow + lcol, l);
-            tmem_ld_32x32b_x32(taddr + cc, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float das = __uint_as_float(r[i]);
-              float dg, dl;
-              const float a = act_bwd(p.act, g[i], l[i], prob * das, dg, dl);
-              dp += das * a;
-              g[i] = dg;
-              l[i] = dl;
-            }
+            dp += glu_bwd32(p.act, prob, das, g, l);
             mx_store_row_block(g, p.q_row, p.s_row, row, gcol, p.ld_q_row, p.s_row_pad);
             mx_store_row_block(l, p.q_row, p.s_row, row, lcol, p.ld_q_row, p.s_row_pad);
-            mx_store_col_blocks(g, p.q_col, p.s_col, row0, gcol, p.ld_q_col, p.s_col_pad, lane);
-            mx_store_col_blocks(l, p.q_col, p.s_col, row0, lcol, p.ld_q_col, p.s_col_pad, lane);
+            mx_store_col_blocks(g, xp, p.q_col, p.s_col, row0, gcol, p.ld_q_col, p.s_col_pad,
+                                lane);
+            mx_store_col_blocks(l, xp, p.q_col, p.s_col, row0, lcol, p.ld_q_col, p.s_col_pad,
+                                lane);
           } else {
             float zz[32];
             load_bf16x32(zrow + f0, zz);
-            tmem_ld_32x32b_x32(taddr + cc, r);
-            tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float das = __uint_as_float(r[i]);
               const float rr = fmaxf(zz[i], 0.f);
-              dp += das * rr * rr;
-              zz[i] = prob * das * 2.f * rr;
+              dp += das[i] * rr * rr;
+              zz[i] = prob * das[i] * 2.f * rr;
             }
             mx_store_row_block(zz, p.q_row, p.s_row, row, f0, p.ld_q_row, p.s_row_pad);
-            mx_store_col_blocks(zz, p.q_col, p.s_col, row0, f0, p.ld_q_col, p.s_col_pad, lane);
+            mx_store_col_blocks(zz, xp, p.q_col, p.s_col, row0, f0, p.ld_q_col, p.s_col_pad,
+                                lane);
           }
         }
         p.dprob_part[(int64_t)row * p.nparts + (t.n0 / BN) * 2 + half] = dp;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&c.tempty[acc]);
-      ++acc_i;
     }
   }
 
@@ -465,9 +527,9 @@ bool tmap_fp8(CUtensorMap* m, const MxOperand& t) {
   return make_tmap(m, t.q, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8);
 }
 
-template <int EPI, bool KG>
+template <int EPI, bool KG, int ILV>
 cudaError_t launch_mx(const MxArgs& a, int grid, cudaStream_t s, int kid) {
-  auto kern = grouped_gemm_mx_kernel<EPI, KG>;
+  auto kern = grouped_gemm_mx_kernel<EPI, KG, ILV>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e =
@@ -480,6 +542,12 @@ cudaError_t launch_mx(const MxArgs& a, int grid, cudaStream_t s, int kid) {
   return cudaGetLastError();
 }
 
+template <int EPI>
+cudaError_t launch_mx_ilv(const MxArgs& a, int ilv, int grid, cudaStream_t s, int kid) {
+  return ilv == 32 ? launch_mx<EPI, false, 32>(a, grid, s, kid)
+                   : launch_mx<EPI, false, 64>(a, grid, s, kid);
+}
+
 }  // namespace
 
 int dprob_parts_mx(int F) { return 2 * ((F + BN - 1) / BN); }
@@ -488,13 +556,13 @@ cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s) {
   static const int kKid[6] = {MOE_K_GEMM_FC1_FPROP, MOE_K_GEMM_FC2_FPROP, MOE_K_GEMM_FC2_DGRAD,
                               MOE_K_GEMM_FC2_WGRAD, MOE_K_GEMM_FC1_DGRAD, MOE_K_GEMM_FC1_WGRAD};
   if (p.role < 0 || p.role > 5) return cudaErrorInvalidValue;
+  if (p.gated && p.ilv != 32 && p.ilv != 64) return cudaErrorInvalidValue;
   MxArgs a;
   memset(&a, 0, sizeof(a));
   a.offsets = p.offsets;
   a.E = p.E;
   a.R_cap = (int)p.R_cap;
   a.gated = p.gated;
-  a.ilv = p.ilv;
   a.act = p.act;
   a.err = p.err;
   a.row_prob = p.row_prob;
@@ -543,14 +611,14 @@ cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s) {
   a.sfb = B->s; a.sfb_pad = B->s_pad;
   const int kid = kKid[p.role];
   switch (p.role) {
-    case ROLE_FC1_FPROP: return launch_mx<EPI_GLU, false>(a, grid, s, kid);
-    case ROLE_FC2_DGRAD: return launch_mx<EPI_DGLU, false>(a, grid, s, kid);
+    case ROLE_FC1_FPROP: return launch_mx_ilv<EPI_GLU>(a, p.ilv, grid, s, kid);
+    case ROLE_FC2_DGRAD: return launch_mx_ilv<EPI_DGLU>(a, p.ilv, grid, s, kid);
     case ROLE_FC2_FPROP:
-    case ROLE_FC1_DGRAD: return launch_mx<EPI_STORE, false>(a, grid, s, kid);
+    case ROLE_FC1_DGRAD: return launch_mx<EPI_STORE, false, 64>(a, grid, s, kid);
     default: {
       const int64_t tiles = (int64_t)p.E * ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
       grid = (int)std::min<int64_t>(grid, tiles);
-      return launch_mx<EPI_STORE, true>(a, grid, s, kid);
+      return launch_mx<EPI_STORE, true, 64>(a, grid, s, kid);
     }
   }
 }

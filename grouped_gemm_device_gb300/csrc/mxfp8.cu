@@ -29,29 +29,50 @@ struct MxQuantArgs {
   int64_t scol_pad; // MMA layout: padded row count of the column-wise scales
 };
 
+// Tile: 128 (virtual) rows x 64 columns. Each thread loads 4 x 16 bytes of the NEXT tile into
+// registers while it quantises the current one from shared memory (one row-wise block and one
+// column-wise block per thread), so a CTA keeps 16 KB of loads in flight.
+constexpr int QT_ROWS = 128;
+constexpr int QT_COLS = 64;
+
+MOE_DEVICE void quant_tile_load(const MxQuantArgs& a, int64_t Mv, int64_t tiles_n, int64_t t,
+                                int tid, uint4 (&buf)[4]) {
+  const int64_t r0 = (t / tiles_n) * QT_ROWS, c0 = (t % tiles_n) * QT_COLS;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = tid + 256 * j;
+    const int rr = i >> 3, cc = (i & 7) * 8;
+    const int64_t v = r0 + rr;
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (v < Mv && c0 + cc < a.N) {
+      const int64_t g = v / a.Gp, k = v - g * a.Gp;
+      if (k < a.G) val = __ldcs(reinterpret_cast<const uint4*>(a.in + (g * a.G + k) * a.N + c0 + cc));
+    }
+    buf[j] = val;
+  }
+}
+
 __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const MxQuantArgs a) {
-  __shared__ __align__(16) uint16_t tile[64][64 + 8];
+  __shared__ __align__(16) uint16_t tile[QT_ROWS][QT_COLS + 8];
   const int64_t Mv = (a.M / a.G) * a.Gp;
-  const int64_t tiles_m = (Mv + 63) / 64, tiles_n = (a.N + 63) / 64;
+  const int64_t tiles_m = (Mv + QT_ROWS - 1) / QT_ROWS, tiles_n = (a.N + QT_COLS - 1) / QT_COLS;
+  const int64_t ntiles = tiles_m * tiles_n;
   const int tid = threadIdx.x;
-  for (int64_t t = blockIdx.x; t < tiles_m * tiles_n; t += gridDim.x) {
-    const int64_t r0 = (t / tiles_n) * 64, c0 = (t % tiles_n) * 64;
+  uint4 buf[4];
+  if (blockIdx.x < ntiles) quant_tile_load(a, Mv, tiles_n, blockIdx.x, tid, buf);
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const int64_t r0 = (t / tiles_n) * QT_ROWS, c0 = (t % tiles_n) * QT_COLS;
     __syncthreads();
-    // stage: 64 (virtual) rows x 8 uint4 (8 bf16 each); padding and out-of-range parts are 0
-    for (int i = tid; i < 64 * 8; i += 256) {
-      const int rr = i >> 3, cc = (i & 7) * 8;
-      const int64_t v = r0 + rr;
-      uint4 val = make_uint4(0, 0, 0, 0);
-      if (v < Mv && c0 + cc < a.N) {
-        const int64_t g = v / a.Gp, k = v - g * a.Gp;
-        if (k < a.G) val = *reinterpret_cast<const uint4*>(a.in + (g * a.G + k) * a.N + c0 + cc);
-      }
-      *reinterpret_cast<uint4*>(&tile[rr][cc]) = val;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = tid + 256 * j;
+      *reinterpret_cast<uint4*>(&tile[i >> 3][(i & 7) * 8]) = buf[j];
     }
     __syncthreads();
+    if (t + gridDim.x < ntiles) quant_tile_load(a, Mv, tiles_n, t + gridDim.x, tid, buf);
     float v[32];
     uint32_t q[8];
-    if (tid < 128) {
+    {
       const int rr = tid >> 1, blk = tid & 1;
       const int64_t row = r0 + rr, col = c0 + blk * 32;
       if (a.rowwise && row < Mv && col < a.N) {
@@ -71,8 +92,9 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const MxQuantArgs a
                                     : row * (a.N / 32) + col / 32;
         a.s_row[so] = (uint8_t)s;
       }
-    } else {
-      const int cc = (tid - 128) & 63, rb = (tid - 128) >> 6;
+    }
+    {
+      const int cc = tid & 63, rb = tid >> 6;
       const int64_t col = c0 + cc, row = r0 + rb * 32;
       if (a.colwise && col < a.N && row < Mv) {
 #pragma unroll
@@ -92,9 +114,9 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const MxQuantArgs a
 
 static void launch(const MxQuantArgs& a, int num_sms, cudaStream_t s) {
   const int64_t Mv = (a.M / a.G) * a.Gp;
-  const int64_t tiles = ((Mv + 63) / 64) * ((a.N + 63) / 64);
+  const int64_t tiles = ((Mv + QT_ROWS - 1) / QT_ROWS) * ((a.N + QT_COLS - 1) / QT_COLS);
   if (tiles == 0) return;
-  const int grid = (int)std::min<int64_t>(tiles, (int64_t)num_sms * 8);
+  const int grid = (int)std::min<int64_t>(tiles, (int64_t)num_sms * 4);
   mxfp8_quantize_kernel<<<grid, 256, 0, s>>>(a);
   count_launch(s, MOE_K_MXFP8_QUANTIZE);
 }

@@ -74,6 +74,7 @@ def test_workspace_layout_is_consistent(lib):
     (dict(E=0), 1), (dict(E=300), 1), (dict(k=0), 1), (dict(k=9, E=16), 1), (dict(k=5, E=4), 1),
     (dict(H=100), 2), (dict(F=96), 2), (dict(align=16), 2), (dict(ilv=48), 2),
     (dict(F=64 * 3, ilv=128), 2), (dict(sm_margin=-1), 1),
+    (dict(precision="mxfp8"), 2), (dict(precision="mxfp8", align=128, ilv=128), 2),
 ])
 def test_invalid_descriptions_rejected(lib, kw, status):
     d = _desc(**kw)

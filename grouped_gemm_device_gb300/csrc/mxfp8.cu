@@ -29,47 +29,56 @@ struct MxQuantArgs {
   int64_t scol_pad; // MMA layout: padded row count of the column-wise scales
 };
 
-// Tile: 128 (virtual) rows x 64 columns. Each thread loads 4 x 16 bytes of the NEXT tile into
-// registers while it quantises the current one from shared memory (one row-wise block and one
-// column-wise block per thread), so a CTA keeps 16 KB of loads in flight.
+// Tile: 128 (virtual) rows x 64 columns, double-buffered in shared memory and filled with
+// cp.async (16-byte asynchronous copies, zero-fill for padding rows and tails), so the next
+// tile's 16 KB are in flight while the current one is quantised (one row-wise and one
+// column-wise block per thread) and no registers hold in-flight data.
 constexpr int QT_ROWS = 128;
 constexpr int QT_COLS = 64;
+constexpr int QT_LD = QT_COLS + 8;  // padded row (bf16 elements): conflict-free column reads
 
-MOE_DEVICE void quant_tile_load(const MxQuantArgs& a, int64_t Mv, int64_t tiles_n, int64_t t,
-                                int tid, uint4 (&buf)[4]) {
+MOE_DEVICE void quant_tile_issue(const MxQuantArgs& a, int64_t Mv, int64_t tiles_n, int64_t t,
+                                 int tid, uint16_t (*buf)[QT_LD]) {
   const int64_t r0 = (t / tiles_n) * QT_ROWS, c0 = (t % tiles_n) * QT_COLS;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int i = tid + 256 * j;
     const int rr = i >> 3, cc = (i & 7) * 8;
     const int64_t v = r0 + rr;
-    uint4 val = make_uint4(0, 0, 0, 0);
+    const uint16_t* src = a.in;  // any valid address when nothing is copied
+    uint32_t bytes = 0;
     if (v < Mv && c0 + cc < a.N) {
       const int64_t g = v / a.Gp, k = v - g * a.Gp;
-      if (k < a.G) val = __ldcs(reinterpret_cast<const uint4*>(a.in + (g * a.G + k) * a.N + c0 + cc));
+      if (k < a.G) {
+        src = a.in + (g * a.G + k) * a.N + c0 + cc;
+        bytes = 16;
+      }
     }
-    buf[j] = val;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(&buf[rr][cc])),
+                 "l"(src), "r"(bytes)
+                 : "memory");
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
 __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const MxQuantArgs a) {
-  __shared__ __align__(16) uint16_t tile[QT_ROWS][QT_COLS + 8];
+  __shared__ __align__(16) uint16_t tiles[2][QT_ROWS][QT_LD];
   const int64_t Mv = (a.M / a.G) * a.Gp;
   const int64_t tiles_m = (Mv + QT_ROWS - 1) / QT_ROWS, tiles_n = (a.N + QT_COLS - 1) / QT_COLS;
   const int64_t ntiles = tiles_m * tiles_n;
   const int tid = threadIdx.x;
-  uint4 buf[4];
-  if (blockIdx.x < ntiles) quant_tile_load(a, Mv, tiles_n, blockIdx.x, tid, buf);
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+  if (blockIdx.x < ntiles) quant_tile_issue(a, Mv, tiles_n, blockIdx.x, tid, tiles[0]);
+  int it = 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
     const int64_t r0 = (t / tiles_n) * QT_ROWS, c0 = (t % tiles_n) * QT_COLS;
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = tid + 256 * j;
-      *reinterpret_cast<uint4*>(&tile[i >> 3][(i & 7) * 8]) = buf[j];
+    uint16_t (*tile)[QT_LD] = tiles[it & 1];
+    if (t + gridDim.x < ntiles) {
+      quant_tile_issue(a, Mv, tiles_n, t + gridDim.x, tid, tiles[(it + 1) & 1]);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
     __syncthreads();
-    if (t + gridDim.x < ntiles) quant_tile_load(a, Mv, tiles_n, t + gridDim.x, tid, buf);
     float v[32];
     uint32_t q[8];
     {
@@ -109,6 +118,7 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const MxQuantArgs a
         a.s_col[so] = (uint8_t)s;
       }
     }
+    __syncthreads();  // this buffer is refilled by the next iteration's copies
   }
 }
 

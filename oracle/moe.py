@@ -182,7 +182,19 @@ def _qrows(v, mx):
     return mxfp8.fake_quant_rows_from(v) if mx else v
 
 
-def expert_forward(X, W1, W2, p, act: ActParams, mx: bool):
+class ExpertWeights:
+    """One expert's weights and, in MXFP8, their quantised copies along each reduction
+    direction (computed once, so sampled checks can reuse them across many rows)."""
+
+    def __init__(self, W1, W2, mx: bool):
+        self.W1, self.W2 = W1, W2
+        self.w1_h = _q(W1, 0, mx)   # FC1 fprop: along H
+        self.w1_n = _q(W1, 1, mx)   # FC1 dgrad: along N1
+        self.w2_f = _q(W2, 0, mx)   # FC2 fprop: along F
+        self.w2_h = _q(W2, 1, mx)   # FC2 dgrad: along H
+
+
+def expert_forward(X, W1, W2, p, act: ActParams, mx: bool, wq: ExpertWeights | None = None):
     """One expert's share of the fused forward.
 
     X [m, H] (its routed rows), W1 [H, N1] logical, W2 [F, H], p [m] routing probs.
@@ -190,19 +202,22 @@ def expert_forward(X, W1, W2, p, act: ActParams, mx: bool):
     [TE-MoE] Challenge 3 (GroupedLinear -> ScaledSwiGLU -> GroupedLinear) and [NV-blog]
     Figure 1 (FC1 + activation + quantise fused, then FC2). In MXFP8 (R8) each GEMM uses
     MXFP8 operands blocked along its reduction dimension: X and W1 along H, a_s and W2 along F.
+    `wq` optionally supplies the weights' quantised copies (ExpertWeights of W1, W2).
     """
+    wq = wq or ExpertWeights(W1, W2, mx)
     F = W2.shape[0]
-    Z = _q(X, 1, mx) @ _q(W1, 0, mx)
+    Z = _q(X, 1, mx) @ wq.w1_h
     if act.gated:
         a = act_forward(act, Z[:, :F], Z[:, F:])
     else:
         a = act_forward(act, Z)
     a_s = p[:, None] * a
-    Y = _q(a_s, 1, mx) @ _q(W2, 0, mx)
+    Y = _q(a_s, 1, mx) @ wq.w2_f
     return Z, a, a_s, Y
 
 
-def expert_backward(X, W1, W2, p, Z, a, a_s, dY, act: ActParams, mx: bool):
+def expert_backward(X, W1, W2, p, Z, a, a_s, dY, act: ActParams, mx: bool,
+                    wq: ExpertWeights | None = None):
     """One expert's share of the backward ([NV-blog] Figure 1: FC2 dgrad + dActivation +
     quantise fused; the weight-gradient GEMMs unfused).
 
@@ -212,8 +227,9 @@ def expert_backward(X, W1, W2, p, Z, a, a_s, dY, act: ActParams, mx: bool):
     MXFP8 (R8): dY and W2 along H for dgrad; a_s and dY column-wise (along rows) for dW2;
     dZ along N1 and W1 along N1 for dX; X and dZ column-wise for dW1.
     """
+    wq = wq or ExpertWeights(W1, W2, mx)
     F = W2.shape[0]
-    dA_s = _q(dY, 1, mx) @ _q(W2, 1, mx).T
+    dA_s = _q(dY, 1, mx) @ wq.w2_h.T
     d_prob = (dA_s * a).sum(axis=1)
     dA = p[:, None] * dA_s
     if act.gated:
@@ -223,7 +239,7 @@ def expert_backward(X, W1, W2, p, Z, a, a_s, dY, act: ActParams, mx: bool):
         dZ, _ = act_backward(act, Z, None, dA)
     dW2 = _qrows(a_s, mx).T @ _qrows(dY, mx)
     dW1 = _qrows(X, mx).T @ _qrows(dZ, mx)
-    dX = _q(dZ, 1, mx) @ _q(W1, 1, mx).T
+    dX = _q(dZ, 1, mx) @ wq.w1_n.T
     return dZ, dX, dW1, dW2, d_prob
 
 
@@ -267,14 +283,16 @@ def layer(logits, x, W1, W2, k: int, act: ActParams, mx: bool = False, align: in
     for e in (range(E) if experts is None else experts):
         tok, slot = perm.rows_of_expert[e]
         W1e, W2e = w1(e), w2(e)
+        wq = ExpertWeights(W1e, W2e, mx)
         X = x[tok]
         p = probs[tok, slot]
-        Z, a, a_s, Y = expert_forward(X, W1e, W2e, p, act, mx)
+        Z, a, a_s, Y = expert_forward(X, W1e, W2e, p, act, mx, wq)
         np.add.at(y, tok, Y)
         inter = dict(Z=Z, a=a, a_s=a_s, Y=Y) if keep_intermediates else {}
         if dy is not None:
             dY = dy[tok]
-            dZ, dX, dW1, dW2, d_prob = expert_backward(X, W1e, W2e, p, Z, a, a_s, dY, act, mx)
+            dZ, dX, dW1, dW2, d_prob = expert_backward(X, W1e, W2e, p, Z, a, a_s, dY, act, mx,
+                                                       wq)
             np.add.at(res.dx, tok, dX)
             res.d_probs[tok, slot] = d_prob
             res.dW1[e], res.dW2[e] = dW1, dW2

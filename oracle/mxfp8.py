@@ -56,11 +56,12 @@ def e4m3_round(v: np.ndarray) -> np.ndarray:
     """
     v = np.asarray(v, dtype=np.float64)
     a = np.abs(v)
-    _, ex = np.frexp(a)                      # a = m * 2^ex, m in [0.5, 1)
-    E = np.maximum(ex - 1, -6)               # floor(log2 a), floored at the subnormal binade
-    E = np.where(a == 0, -6, E)
-    quantum = np.ldexp(1.0, E - 3)
-    r = np.rint(a / quantum) * quantum       # rint: half to even
+    # floor(log2 a) from the fp64 exponent field (zero and fp64 subnormals give -1023, whose
+    # quantum is the subnormal one and which round to 0), floored at the subnormal binade
+    E = np.maximum(((a.view(np.int64) >> 52) & 0x7FF) - 1023, -6)
+    quantum = ((E - 3 + 1023) << 52).view(np.float64)      # 2^(E-3), exact
+    inv_quantum = ((3 - E + 1023) << 52).view(np.float64)  # 2^(3-E), exact
+    r = np.rint(a * inv_quantum) * quantum    # rint: half to even
     r = np.minimum(r, E4M3_MAX)
     return np.copysign(r, v)
 
@@ -120,9 +121,20 @@ def dequantize_blocks(codes: np.ndarray, scale_bytes: np.ndarray, axis: int) -> 
 
 
 def fake_quant(v: np.ndarray, axis: int) -> np.ndarray:
-    """Quantise to MXFP8 along `axis` and return the dequantised fp64 values."""
-    c, s = quantize_blocks(v, axis)
-    return dequantize_blocks(c, s, axis)
+    """Quantise to MXFP8 along `axis` and return the dequantised fp64 values:
+    2^e * E4M3_RNE(v / 2^e) per block of 32, the same values quantize_blocks encodes (taken
+    straight from the rounding, without the code-table round trip, so that it is fast on
+    full-size weights)."""
+    v = np.asarray(v, dtype=np.float64)
+    axis = axis % v.ndim
+    n = v.shape[axis]
+    if n % BLOCK:
+        raise ValueError("blocked axis must be a multiple of 32")
+    vm = np.moveaxis(v, axis, -1)
+    blocks = vm.reshape(vm.shape[:-1] + (n // BLOCK, BLOCK))
+    scale = np.ldexp(1.0, block_exponent(np.abs(blocks).max(axis=-1)))[..., None]
+    out = e4m3_round(blocks / scale) * scale
+    return np.moveaxis(out.reshape(vm.shape), -1, axis)
 
 
 def fake_quant_rows_from(v: np.ndarray) -> np.ndarray:

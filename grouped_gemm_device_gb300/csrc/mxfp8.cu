@@ -29,12 +29,16 @@ struct MxQuantArgs {
   int64_t scol_pad; // MMA layout: padded row count of the column-wise scales
 };
 
-// Tile: 128 (virtual) rows x 64 columns, double-buffered in shared memory and filled with
-// cp.async (16-byte asynchronous copies, zero-fill for padding rows and tails), so the next
-// tile's 16 KB are in flight while the current one is quantised (one row-wise and one
-// column-wise block per thread) and no registers hold in-flight data.
+// Tile: 128 (virtual) rows x 64 columns (128-byte runs for both the row reads and the
+// transposed column writes), buffered in shared memory and filled with cp.async (16-byte
+// asynchronous copies, zero-fill for padding rows and tails), so later tiles are in flight
+// while the current one is quantised (one row-wise and one column-wise block per thread) and
+// no registers hold in-flight data.
 constexpr int QT_ROWS = 128;
 constexpr int QT_COLS = 64;
+constexpr int QT_U4 = QT_COLS / 8;        // 16-byte pieces per tile row
+constexpr int QT_RBLK = QT_COLS / 32;     // row-wise blocks per tile row
+static_assert(QT_ROWS * QT_RBLK == 256 && QT_COLS * (QT_ROWS / 32) == 256, "one task each");
 constexpr int QT_LD = QT_COLS + 8;  // padded row (bf16 elements): conflict-free column reads
 
 MOE_DEVICE void quant_tile_issue(const MxQuantArgs& a, int64_t Mv, int64_t tiles_n, int64_t t,
@@ -43,7 +47,7 @@ MOE_DEVICE void quant_tile_issue(const MxQuantArgs& a, int64_t Mv, int64_t tiles
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int i = tid + 256 * j;
-    const int rr = i >> 3, cc = (i & 7) * 8;
+    const int rr = i / QT_U4, cc = (i % QT_U4) * 8;
     const int64_t v = r0 + rr;
     const uint16_t* src = a.in;  // any valid address when nothing is copied
     uint32_t bytes = 0;
@@ -61,28 +65,36 @@ MOE_DEVICE void quant_tile_issue(const MxQuantArgs& a, int64_t Mv, int64_t tiles
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
+constexpr int QT_BUFS = 3;  // tiles in flight per CTA: the current one and two ahead
+constexpr int QT_SMEM = QT_BUFS * QT_ROWS * QT_LD * 2;
+
 __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const MxQuantArgs a) {
-  __shared__ __align__(16) uint16_t tiles[2][QT_ROWS][QT_LD];
+  extern __shared__ __align__(16) uint16_t qsmem[];
+  auto tiles = reinterpret_cast<uint16_t (*)[QT_ROWS][QT_LD]>(qsmem);
   const int64_t Mv = (a.M / a.G) * a.Gp;
   const int64_t tiles_m = (Mv + QT_ROWS - 1) / QT_ROWS, tiles_n = (a.N + QT_COLS - 1) / QT_COLS;
   const int64_t ntiles = tiles_m * tiles_n;
   const int tid = threadIdx.x;
-  if (blockIdx.x < ntiles) quant_tile_issue(a, Mv, tiles_n, blockIdx.x, tid, tiles[0]);
+  // one commit group per tile slot (possibly empty), so "wait until 2 groups remain" always
+  // means "the current tile has landed"
+  for (int j = 0; j < QT_BUFS - 1; ++j) {
+    const int64_t tj = blockIdx.x + (int64_t)j * gridDim.x;
+    if (tj < ntiles) quant_tile_issue(a, Mv, tiles_n, tj, tid, tiles[j]);
+    else asm volatile("cp.async.commit_group;" ::: "memory");
+  }
   int it = 0;
   for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
     const int64_t r0 = (t / tiles_n) * QT_ROWS, c0 = (t % tiles_n) * QT_COLS;
-    uint16_t (*tile)[QT_LD] = tiles[it & 1];
-    if (t + gridDim.x < ntiles) {
-      quant_tile_issue(a, Mv, tiles_n, t + gridDim.x, tid, tiles[(it + 1) & 1]);
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-    } else {
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-    }
+    uint16_t (*tile)[QT_LD] = tiles[it % QT_BUFS];
+    const int64_t tn = t + (int64_t)(QT_BUFS - 1) * gridDim.x;
+    if (tn < ntiles) quant_tile_issue(a, Mv, tiles_n, tn, tid, tiles[(it + QT_BUFS - 1) % QT_BUFS]);
+    else asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group %0;" ::"n"(QT_BUFS - 1) : "memory");
     __syncthreads();
     float v[32];
     uint32_t q[8];
     {
-      const int rr = tid >> 1, blk = tid & 1;
+      const int rr = tid % QT_ROWS, blk = tid / QT_ROWS;  // a quarter-warp spans 8 rows
       const int64_t row = r0 + rr, col = c0 + blk * 32;
       if (a.rowwise && row < Mv && col < a.N) {
 #pragma unroll
@@ -103,7 +115,7 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const MxQuantArgs a
       }
     }
     {
-      const int cc = tid & 63, rb = tid >> 6;
+      const int cc = tid % QT_COLS, rb = tid / QT_COLS;
       const int64_t col = c0 + cc, row = r0 + rb * 32;
       if (a.colwise && col < a.N && row < Mv) {
 #pragma unroll
@@ -126,8 +138,15 @@ static void launch(const MxQuantArgs& a, int num_sms, cudaStream_t s) {
   const int64_t Mv = (a.M / a.G) * a.Gp;
   const int64_t tiles = ((Mv + QT_ROWS - 1) / QT_ROWS) * ((a.N + QT_COLS - 1) / QT_COLS);
   if (tiles == 0) return;
+  static bool configured = false;
+  if (!configured) {
+    // on failure the launch below fails too and the caller reports the CUDA error
+    configured = cudaFuncSetAttribute(mxfp8_quantize_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      QT_SMEM) == cudaSuccess;
+  }
   const int grid = (int)std::min<int64_t>(tiles, (int64_t)num_sms * 4);
-  mxfp8_quantize_kernel<<<grid, 256, 0, s>>>(a);
+  mxfp8_quantize_kernel<<<grid, 256, QT_SMEM, s>>>(a);
   count_launch(s, MOE_K_MXFP8_QUANTIZE);
 }
 

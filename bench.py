@@ -212,16 +212,17 @@ def host_inputs(cfg):
 
 
 def traffic_for(kernel: str, workload: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on the
-    current kernel source (the summary records the sha256 of gemm.cu it was measured on)."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_ncu.txt")
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu table for the
+    workload, if it was taken on the current kernel source (the table records the sha256 of
+    gemm.cu it was measured on); None otherwise."""
+    path = os.path.join(ROOT, "profiles", f"gemm_dram_traffic_{workload}.txt")
     if not os.path.exists(path):
         return None
     src = os.path.join(ROOT, "grouped_gemm_device_gb300", "csrc", "gemm.cu")
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     txt = open(path).read()
     m_sha = re.search(r"gemm\.cu sha256\[:16\]:\s*(\w+)", txt)
-    m_b = re.search(r"dram bytes per launch \(full workload\):\s*([\d.eE+]+)", txt)
+    m_b = re.search(rf"^{re.escape(kernel)}\s+[\d.]+\s+[\d.]+\s+(\d+)", txt, re.M)
     if not m_sha or not m_b or m_sha.group(1) != sha:
         return None
     return float(m_b.group(1))

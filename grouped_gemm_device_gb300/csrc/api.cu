@@ -103,7 +103,10 @@ static moe_status_t validate_desc(const moe_layer_desc_t* d) {
 static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // The MXFP8 operand copies, in order after mx_base: for each GEMM input the row-wise copy
-// [rows, K] and the column-wise transposed copy, each with its slab-layout scales.
+// (blocks along a row, read K-major) and the column-wise copy (blocks down a column), each
+// with its slab-layout scales. rows/cols of a column-wise copy name the MMA view (rows = the
+// source's columns, cols = the reduction length); its bytes keep the source's row-major
+// layout, which the GEMM reads as an MN-major operand.
 struct MxOps {
   MxOperand x, xt, a, at, dy, dyt, dz, dzt, w1, w1t, w2, w2t;
   int N1p, Fp;
@@ -270,7 +273,7 @@ static MxProblem mx_problem(const moe_layer_desc_t* d, const Ws& w) {
 }
 
 // Quantise a bf16 matrix [M, N] (row groups G padded to Gp) into the row-wise and the
-// column-wise (transposed) MXFP8 operands of the block-scaled GEMM.
+// column-wise MXFP8 operands of the block-scaled GEMM (both in the source's layout).
 static void mx_quantize_operands(const void* in, int64_t M, int64_t N, int64_t G, int64_t Gp,
                                  const MxOperand& row, const MxOperand& col, cudaStream_t s) {
   launch_mxfp8_quantize_mma(in, M, N, G, Gp, row.q, row.s, col.q, col.s,

@@ -230,9 +230,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
 // Instruction descriptor, kind::mxf8f6f4 block-scaled: E4M3 A and B (format 0), K-major,
 // scale factors E8M0 (bit 23), a_sf_id at bits 29..30 and b_sf_id at bits 4..5 select which
 // byte of the 32-bit scale-factor column a K=32 step uses.
-__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sf_id) {
-  return ((uint32_t)(sf_id & 3) << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
-         ((uint32_t)(M >> 4) << 24) | ((uint32_t)(sf_id & 3) << 29);
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sf_id, bool a_mn = false,
+                                                  bool b_mn = false) {
+  return ((uint32_t)(sf_id & 3) << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) |
+         ((uint32_t)(sf_id & 3) << 29);
 }
 // D[tmem] (+)= (A * 2^SFA) (B * 2^SFB)^T, E4M3 inputs with per-32 E8M0 scales in TMEM.
 MOE_DEVICE void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,

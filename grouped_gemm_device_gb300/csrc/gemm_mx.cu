@@ -4,15 +4,17 @@
 // activation + quantise/transpose, (3) FC2 dgrad + dActivation + quantise/transpose; [TE-MoE]
 // Challenge 2 (MXFP8: E4M3 with one E8M0 scale per 32 values, tensor-core accelerated).
 //
-// Every operand is an E4M3 matrix quantised along its own reduction dimension and stored
-// K-major ([rows, K]); its scales sit in the MMA slab layout (sf_mma_offset). A CTA:
+// Every operand is an E4M3 matrix quantised along its own reduction dimension. A row-wise copy
+// ([rows, K] row-major) is read K-major; a column-wise copy keeps its source's row-major
+// layout ([K, rows]) and is read MN-major, so no copy is ever transposed in memory. Scales sit
+// in the MMA slab layout (sf_mma_offset). A CTA:
 //   warp 0   TMA of the A (128 x 128 B) and B (256 x 128 B) k-blocks and one 1-D bulk copy of
 //            their 512 + 1024 bytes of scale slabs, all counted on one mbarrier,
 //   warp 1   TMEM owner; one thread copies the stage's scales into TMEM (tcgen05.cp) and issues
 //            four tcgen05.mma.kind::mxf8f6f4.block_scale 128x256x32 (scale byte = K step),
 //   warps 2-9 epilogue: drain the accumulator into registers as packed bf16 (warp w takes TMEM
 //            lanes 32*(w%4).. and 128 of the 256 columns), release TMEM, then bf16 store, or
-//            GLU / dGLU with fused row-wise and column-wise (transposed) MXFP8 quantisation.
+//            GLU / dGLU with fused row-wise and column-wise MXFP8 quantisation.
 // The tile is 128 x 256 because a 128 x 256 x 32 MMA runs at the full fp8 rate while 128-wide
 // ones do not; TMEM then holds one accumulator (256 columns) plus 12 scale columns per stage,
 // and the register drain lets the next tile's MMAs start while the epilogue works. Expert
@@ -55,7 +57,7 @@ struct MxArgs {
   uint8_t* s_row;
   int64_t ld_q_row;
   int64_t s_row_pad;
-  uint8_t* q_col;                      // column-wise MXFP8, transposed [cols, ld_q_col]
+  uint8_t* q_col;                      // column-wise MXFP8, natural layout [R, ld_q_col]
   uint8_t* s_col;
   int64_t ld_q_col;
   int64_t s_col_pad;
@@ -77,7 +79,7 @@ constexpr int SFB_BYTES = 1024;  // 256 rows x 4 k-blocks
 constexpr int DATA = STAGES * STAGE_BYTES;
 constexpr int SF_OFF = DATA;
 constexpr int XPOSE_OFF = SF_OFF + STAGES * (SFA_BYTES + SFB_BYTES);
-constexpr int XPOSE_WARP_BYTES = 32 * 33 * 4;  // 32 x 32 fp32 transpose, padded rows
+constexpr int XPOSE_WARP_BYTES = 32 * 33 * 4;  // 32 x 32 fp32 staging, padded rows
 constexpr int CTRL_OFF = XPOSE_OFF + kEpiWarps * XPOSE_WARP_BYTES;
 constexpr int SMEM_TOTAL = CTRL_OFF + 4096 + 1024;
 
@@ -141,25 +143,38 @@ MOE_DEVICE void mx_store_row_block(const float (&v)[32], uint8_t* q, uint8_t* s_
   s_row[sf_mma_offset(row, col / 32, s_pad)] = (uint8_t)sb;
 }
 
-// Column-wise MXFP8 of the warp's 32 rows x 32 columns (this lane holds one row): the block is
-// transposed through the warp's shared-memory tile, lane j then quantises column col0 + j and
-// stores its 32 codes as one run of the transposed output q[col][row0 .. row0+31].
+// Column-wise MXFP8 of the warp's 32 rows x 32 columns (this lane holds one row), stored in the
+// natural row-major layout q[row][col]: lane j finds column col0 + j's block maximum through the
+// warp's shared-memory tile and publishes its exponent; every lane then quantises its own row
+// with the 32 column scales and stores one 32-byte run.
 MOE_DEVICE void mx_store_col_blocks(const float (&v)[32], float* xp, uint8_t* q, uint8_t* s_col,
                                     int64_t row0, int64_t col0, int64_t ld, int64_t s_pad,
                                     int lane) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) xp[lane * 33 + i] = v[i];
   __syncwarp();
-  float w[32];
+  float amax = 0.f;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) w[i] = xp[i * 33 + lane];
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(xp[i * 33 + lane]));
+  const int e = mx_block_exponent(amax);
+  s_col[sf_mma_offset(col0 + lane, row0 / 32, s_pad)] = (uint8_t)(e + 127);
+  __syncwarp();
+  int* xe = reinterpret_cast<int*>(xp);  // the 32 column exponents, reusing the tile
+  xe[lane] = e;
   __syncwarp();
   uint32_t qq[8];
-  const uint32_t sb = mx_quant_block(w, qq);
-  uint4* dst = reinterpret_cast<uint4*>(q + (col0 + lane) * ld + row0);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int4 e4 = *reinterpret_cast<const int4*>(xe + 4 * i);
+    const uint32_t lo = cvt_e4m3x2(v[4 * i] * mx_inv_scale(e4.x), v[4 * i + 1] * mx_inv_scale(e4.y));
+    const uint32_t hi =
+        cvt_e4m3x2(v[4 * i + 2] * mx_inv_scale(e4.z), v[4 * i + 3] * mx_inv_scale(e4.w));
+    qq[i] = lo | (hi << 16);
+  }
+  __syncwarp();
+  uint4* dst = reinterpret_cast<uint4*>(q + (row0 + lane) * ld + col0);
   dst[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
   dst[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
-  s_col[sf_mma_offset(col0 + lane, row0 / 32, s_pad)] = (uint8_t)sb;
 }
 
 MOE_DEVICE void unpack32(const uint32_t* pk, float (&v)[32]) {
@@ -170,7 +185,9 @@ MOE_DEVICE void unpack32(const uint32_t* pk, float (&v)[32]) {
   }
 }
 
-template <int EPI, bool KG, int ILV>
+// A_MN / B_MN: the operand is a column-wise copy stored [K rows, M or N columns] (MN-major);
+// otherwise it is [M or N rows, K] (K-major).
+template <int EPI, bool KG, int ILV, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __grid_constant__ MxArgs p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -252,9 +269,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
           const int k0 = t.kbeg + kb * BK;
           const int a_k = k0 + t.e * p.a_k_e;
           const int b_k = k0 + t.e * p.b_k_e;
-          tma_load_2d(sA, &p.tmA, bar, a_k, a_row);
-          tma_load_2d(sB, &p.tmB, bar, b_k, b_row);
-          tma_load_2d(sB + B_BYTES / 2, &p.tmB, bar, b_k, b_row + 128);
+          // boxes are 128 x 128 bytes: K-major {k, row}, MN-major {mn, k}
+          if (!A_MN) tma_load_2d(sA, &p.tmA, bar, a_k, a_row);
+          else tma_load_2d(sA, &p.tmA, bar, a_row, a_k);
+          if (!B_MN) {
+            tma_load_2d(sB, &p.tmB, bar, b_k, b_row);
+            tma_load_2d(sB + B_BYTES / 2, &p.tmB, bar, b_k, b_row + 128);
+          } else {
+            tma_load_2d(sB, &p.tmB, bar, b_row, b_k);
+            tma_load_2d(sB + B_BYTES / 2, &p.tmB, bar, b_row + 128, b_k);
+          }
           bulk_load(sfA, p.sfa + ((int64_t)(a_k / BK) * p.sfa_pad + a_row) * 4, SFA_BYTES, bar);
           bulk_load(sfA + SFA_BYTES, p.sfb + ((int64_t)(b_k / BK) * p.sfb_pad + b_row) * 4,
                     SFB_BYTES, bar);
@@ -306,9 +330,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
           const int rem = t.klen - kb * BK;
           const int nsub = rem >= BK ? BK / MMA_K : (rem + MMA_K - 1) / MMA_K;
           for (int ks = 0; ks < nsub; ++ks) {
-            const uint64_t ad = smem_desc_sw128(sA + ks * MMA_K, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(sB + ks * MMA_K, 16, 1024);
-            mma_mxf8_ss(tmem_base, ad, bd, idesc_mxf8(BM, BN, ks), sfa_t, sfb_t,
+            // K-major: a K step is 32 bytes along the swizzled row; MN-major: 32 rows of 128
+            // bytes, with the 128-element MN chunks of B 16 KB apart (LBO) and 8-row groups
+            // 1024 bytes apart (SBO)
+            const uint64_t ad = A_MN ? smem_desc_sw128(sA + ks * (MMA_K * 128), A_BYTES, 1024)
+                                     : smem_desc_sw128(sA + ks * MMA_K, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(sB + ks * (MMA_K * 128), B_BYTES / 2, 1024)
+                                     : smem_desc_sw128(sB + ks * MMA_K, 16, 1024);
+            mma_mxf8_ss(tmem_base, ad, bd, idesc_mxf8(BM, BN, ks, A_MN, B_MN), sfa_t, sfb_t,
                         (kb | ks) != 0 ? 1u : 0u);
           }
           issued_any = true;
@@ -520,16 +549,19 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
   }
 }
 
-bool tmap_fp8(CUtensorMap* m, const MxOperand& t) {
-  uint64_t dims[2] = {(uint64_t)t.cols, (uint64_t)t.rows};
-  uint64_t strides[1] = {(uint64_t)t.cols};
-  uint32_t box[2] = {BK, 128};
+// An operand t has t.rows M/N indices and t.cols K indices. K-major data is [rows, cols]; the
+// column-wise copies are MN-major, stored [cols (K), rows (M or N)].
+bool tmap_fp8(CUtensorMap* m, const MxOperand& t, bool mn_major) {
+  const uint64_t inner = mn_major ? t.rows : t.cols, outer = mn_major ? t.cols : t.rows;
+  uint64_t dims[2] = {inner, outer};
+  uint64_t strides[1] = {inner};
+  uint32_t box[2] = {128, 128};
   return make_tmap(m, t.q, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8);
 }
 
-template <int EPI, bool KG, int ILV>
+template <int EPI, bool KG, int ILV, bool A_MN, bool B_MN>
 cudaError_t launch_mx(const MxArgs& a, int grid, cudaStream_t s, int kid) {
-  auto kern = grouped_gemm_mx_kernel<EPI, KG, ILV>;
+  auto kern = grouped_gemm_mx_kernel<EPI, KG, ILV, A_MN, B_MN>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e =
@@ -544,8 +576,8 @@ cudaError_t launch_mx(const MxArgs& a, int grid, cudaStream_t s, int kid) {
 
 template <int EPI>
 cudaError_t launch_mx_ilv(const MxArgs& a, int ilv, int grid, cudaStream_t s, int kid) {
-  return ilv == 32 ? launch_mx<EPI, false, 32>(a, grid, s, kid)
-                   : launch_mx<EPI, false, 64>(a, grid, s, kid);
+  return ilv == 32 ? launch_mx<EPI, false, 32, false, false>(a, grid, s, kid)
+                   : launch_mx<EPI, false, 64, false, false>(a, grid, s, kid);
 }
 
 }  // namespace
@@ -575,9 +607,9 @@ cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s) {
       a.K = H; a.N = N1; a.b_row_e = p.N1p;
       a.out = p.out; a.ldo = N1;
       a.q_row = p.a.q; a.s_row = p.a.s; a.ld_q_row = F; a.s_row_pad = p.a.s_pad;
-      a.q_col = p.at.q; a.s_col = p.at.s; a.ld_q_col = p.R_cap; a.s_col_pad = p.at.s_pad;
+      a.q_col = p.at.q; a.s_col = p.at.s; a.ld_q_col = F; a.s_col_pad = p.at.s_pad;
       break;
-    case ROLE_FC2_FPROP:  // a_s x W2^T (W2 column-wise copy [H, E*Fp]), K = F
+    case ROLE_FC2_FPROP:  // a_s x W2 (column-wise copy [E*Fp, H], MN-major), K = F
       A = &p.a; B = &p.w2t;
       a.K = F; a.N = H; a.b_k_e = p.Fp;
       a.out = p.out; a.ldo = H;
@@ -587,10 +619,10 @@ cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s) {
       a.K = H; a.N = F; a.b_row_e = p.Fp;
       a.z = static_cast<const uint16_t*>(p.z); a.ldz = N1;
       a.q_row = p.dz.q; a.s_row = p.dz.s; a.ld_q_row = N1; a.s_row_pad = p.dz.s_pad;
-      a.q_col = p.dzt.q; a.s_col = p.dzt.s; a.ld_q_col = p.R_cap; a.s_col_pad = p.dzt.s_pad;
+      a.q_col = p.dzt.q; a.s_col = p.dzt.s; a.ld_q_col = N1; a.s_col_pad = p.dzt.s_pad;
       a.dprob_part = p.dprob_part; a.nparts = dprob_parts_mx(F);
       break;
-    case ROLE_FC1_DGRAD:  // dZ x W1^T (W1 column-wise copy [H, E*N1p]), K = N1
+    case ROLE_FC1_DGRAD:  // dZ x W1 (column-wise copy [E*N1p, H], MN-major), K = N1
       A = &p.dz; B = &p.w1t;
       a.K = N1; a.N = H; a.b_k_e = p.N1p;
       a.out = p.out; a.ldo = H;
@@ -606,7 +638,9 @@ cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s) {
       a.out = p.out; a.ldo = H; a.out_estride = (int64_t)N1 * H;
       break;
   }
-  if (!tmap_fp8(&a.tmA, *A) || !tmap_fp8(&a.tmB, *B)) return cudaErrorInvalidValue;
+  const bool kg = p.role == ROLE_FC2_WGRAD || p.role == ROLE_FC1_WGRAD;
+  const bool b_mn = kg || p.role == ROLE_FC2_FPROP || p.role == ROLE_FC1_DGRAD;
+  if (!tmap_fp8(&a.tmA, *A, kg) || !tmap_fp8(&a.tmB, *B, b_mn)) return cudaErrorInvalidValue;
   a.sfa = A->s; a.sfa_pad = A->s_pad;
   a.sfb = B->s; a.sfb_pad = B->s_pad;
   const int kid = kKid[p.role];
@@ -614,11 +648,11 @@ cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s) {
     case ROLE_FC1_FPROP: return launch_mx_ilv<EPI_GLU>(a, p.ilv, grid, s, kid);
     case ROLE_FC2_DGRAD: return launch_mx_ilv<EPI_DGLU>(a, p.ilv, grid, s, kid);
     case ROLE_FC2_FPROP:
-    case ROLE_FC1_DGRAD: return launch_mx<EPI_STORE, false, 64>(a, grid, s, kid);
+    case ROLE_FC1_DGRAD: return launch_mx<EPI_STORE, false, 64, false, true>(a, grid, s, kid);
     default: {
       const int64_t tiles = (int64_t)p.E * ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
       grid = (int)std::min<int64_t>(grid, tiles);
-      return launch_mx<EPI_STORE, true, 64>(a, grid, s, kid);
+      return launch_mx<EPI_STORE, true, 64, true, true>(a, grid, s, kid);
     }
   }
 }

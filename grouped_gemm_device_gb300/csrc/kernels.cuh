@@ -96,7 +96,8 @@ struct MxProblem {
   int E, H, F, N1, N1p, Fp;  // N1p, Fp: per-expert weight rows padded to 128
   int64_t R_cap;             // rows of every permuted buffer (multiple of 128)
   const int32_t* offsets;    // [E+1], segments 128-row aligned
-  // row-wise (K = last dim) and column-wise transposed copies of each GEMM input
+  // row-wise (K = last dim, read K-major) and column-wise (source layout, read MN-major)
+  // copies of each GEMM input
   MxOperand x, xt, a, at, dy, dyt, dz, dzt, w1, w1t, w2, w2t;
   const float* row_prob;
   const void* z;             // bf16 [R_cap, N1] saved FC1 output

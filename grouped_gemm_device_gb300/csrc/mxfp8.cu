@@ -2,10 +2,12 @@
 // contiguous values). Scale exponent e = clamp(floor(log2 amax) - 8, -127, 127) (-127 for an
 // all-zero block), element = E4M3(v * 2^-e) rounded to nearest even with saturation.
 //
-// One CTA quantises 64x64 tiles (grid-stride): the tile is staged in shared memory, threads
-// 0..127 produce the row-wise blocks (64 rows x 2 blocks) and threads 128..255 the
-// column-wise blocks (64 columns x 2 blocks) written transposed, so each output block is one
-// contiguous 32-byte run in global memory.
+// Both outputs keep the input's row-major layout: the row-wise copy has blocks of 32 along a
+// row, the column-wise copy blocks of 32 rows of one column. Per 128-row x 64-column tile
+// (staged in shared memory): phase 1, one thread per (column, 32-row block) finds the column
+// block's exponent; phase 2, one thread per (row, 32-column block) quantises its 32 values
+// twice - with its own row scale and with the 32 column scales - and stores two 32-byte runs.
+// Every global store is therefore a contiguous row segment.
 //
 // Rows may be grouped: input row g*G + i (i < G) becomes output row g*Gp + i, and rows
 // g*Gp + G .. g*Gp + Gp - 1 are written as zeros (per-expert padding of the operands of the
@@ -20,26 +22,25 @@ struct MxQuantArgs {
   int64_t M, N;     // input [M, N] bf16
   int64_t G, Gp;    // row groups of G input rows, output group stride Gp (>= G)
   int rowwise, colwise;
-  uint8_t* q_row;   // [Mv, N]       Mv = (M / G) * Gp
+  uint8_t* q_row;   // [Mv, N]       Mv = (M / G) * Gp, blocks along N
   uint8_t* s_row;
-  uint8_t* q_col;   // [N, Mv]
+  uint8_t* q_col;   // [Mv, N]       blocks along Mv
   uint8_t* s_col;
   int sf_mma;       // 0: logical scale layout, 1: MMA slab layout
   int64_t srow_pad; // MMA layout: padded row count of the row-wise scales (multiple of 128)
   int64_t scol_pad; // MMA layout: padded row count of the column-wise scales
 };
 
-// Tile: 128 (virtual) rows x 64 columns (128-byte runs for both the row reads and the
-// transposed column writes), buffered in shared memory and filled with cp.async (16-byte
-// asynchronous copies, zero-fill for padding rows and tails), so later tiles are in flight
-// while the current one is quantised (one row-wise and one column-wise block per thread) and
-// no registers hold in-flight data.
+// Tile: 128 (virtual) rows x 64 columns, buffered in shared memory and filled with cp.async
+// (16-byte asynchronous copies, zero-fill for padding rows and tails), so later tiles are in
+// flight while the current one is quantised and no registers hold in-flight data.
 constexpr int QT_ROWS = 128;
 constexpr int QT_COLS = 64;
-constexpr int QT_U4 = QT_COLS / 8;        // 16-byte pieces per tile row
-constexpr int QT_RBLK = QT_COLS / 32;     // row-wise blocks per tile row
-static_assert(QT_ROWS * QT_RBLK == 256 && QT_COLS * (QT_ROWS / 32) == 256, "one task each");
 constexpr int QT_LD = QT_COLS + 8;  // padded row (bf16 elements): conflict-free column reads
+constexpr int QT_BUFS = 3;          // tiles in flight per CTA: the current one and two ahead
+constexpr int QT_TILE_BYTES = QT_ROWS * QT_LD * 2;
+constexpr int QT_EXP_BYTES = (QT_ROWS / 32) * QT_COLS * 4;
+constexpr int QT_SMEM = QT_BUFS * QT_TILE_BYTES + QT_EXP_BYTES;
 
 MOE_DEVICE void quant_tile_issue(const MxQuantArgs& a, int64_t Mv, int64_t tiles_n, int64_t t,
                                  int tid, uint16_t (*buf)[QT_LD]) {
@@ -47,7 +48,7 @@ MOE_DEVICE void quant_tile_issue(const MxQuantArgs& a, int64_t Mv, int64_t tiles
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int i = tid + 256 * j;
-    const int rr = i / QT_U4, cc = (i % QT_U4) * 8;
+    const int rr = i >> 3, cc = (i & 7) * 8;
     const int64_t v = r0 + rr;
     const uint16_t* src = a.in;  // any valid address when nothing is copied
     uint32_t bytes = 0;
@@ -65,12 +66,10 @@ MOE_DEVICE void quant_tile_issue(const MxQuantArgs& a, int64_t Mv, int64_t tiles
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-constexpr int QT_BUFS = 3;  // tiles in flight per CTA: the current one and two ahead
-constexpr int QT_SMEM = QT_BUFS * QT_ROWS * QT_LD * 2;
-
 __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const MxQuantArgs a) {
-  extern __shared__ __align__(16) uint16_t qsmem[];
+  extern __shared__ __align__(16) uint8_t qsmem[];
   auto tiles = reinterpret_cast<uint16_t (*)[QT_ROWS][QT_LD]>(qsmem);
+  int* cexp = reinterpret_cast<int*>(qsmem + QT_BUFS * QT_TILE_BYTES);  // [4][64]
   const int64_t Mv = (a.M / a.G) * a.Gp;
   const int64_t tiles_m = (Mv + QT_ROWS - 1) / QT_ROWS, tiles_n = (a.N + QT_COLS - 1) / QT_COLS;
   const int64_t ntiles = tiles_m * tiles_n;
@@ -91,12 +90,29 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const MxQuantArgs a
     else asm volatile("cp.async.commit_group;" ::: "memory");
     asm volatile("cp.async.wait_group %0;" ::"n"(QT_BUFS - 1) : "memory");
     __syncthreads();
-    float v[32];
-    uint32_t q[8];
+    // ---- phase 1: exponent of each (column, 32-row block)
+    if (a.colwise) {
+      const int cc = tid & 63, rb = tid >> 6;
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)tile[rb * 32 + i][cc] << 16)));
+      const int e = mx_block_exponent(amax);
+      cexp[rb * 64 + cc] = e;
+      const int64_t col = c0 + cc, row = r0 + rb * 32;
+      if (col < a.N && row < Mv) {
+        const int64_t so = a.sf_mma ? sf_mma_offset(col, row / 32, a.scol_pad)
+                                    : col * (Mv / 32) + row / 32;
+        a.s_col[so] = (uint8_t)(e + 127);
+      }
+    }
+    __syncthreads();
+    // ---- phase 2: one (row, 32-column block) per thread; a warp spans 32 consecutive rows
     {
-      const int rr = tid % QT_ROWS, blk = tid / QT_ROWS;  // a quarter-warp spans 8 rows
+      const int rr = tid & 127, blk = tid >> 7;
       const int64_t row = r0 + rr, col = c0 + blk * 32;
-      if (a.rowwise && row < Mv && col < a.N) {
+      if (row < Mv && col < a.N) {
+        float v[32];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint4 w = *reinterpret_cast<const uint4*>(&tile[rr][blk * 32 + 8 * i]);
@@ -105,32 +121,34 @@ __global__ void __launch_bounds__(256) mxfp8_quantize_kernel(const MxQuantArgs a
           v[8 * i + 4] = bf16_lo(w.z); v[8 * i + 5] = bf16_hi(w.z);
           v[8 * i + 6] = bf16_lo(w.w); v[8 * i + 7] = bf16_hi(w.w);
         }
-        const uint32_t s = mx_quant_block(v, q);
-        uint4* dst = reinterpret_cast<uint4*>(a.q_row + row * a.N + col);
-        dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-        dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-        const int64_t so = a.sf_mma ? sf_mma_offset(row, col / 32, a.srow_pad)
-                                    : row * (a.N / 32) + col / 32;
-        a.s_row[so] = (uint8_t)s;
-      }
-    }
-    {
-      const int cc = tid % QT_COLS, rb = tid / QT_COLS;
-      const int64_t col = c0 + cc, row = r0 + rb * 32;
-      if (a.colwise && col < a.N && row < Mv) {
+        uint32_t q[8];
+        if (a.rowwise) {
+          const uint32_t s = mx_quant_block(v, q);
+          uint4* dst = reinterpret_cast<uint4*>(a.q_row + row * a.N + col);
+          dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+          dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+          const int64_t so = a.sf_mma ? sf_mma_offset(row, col / 32, a.srow_pad)
+                                      : row * (a.N / 32) + col / 32;
+          a.s_row[so] = (uint8_t)s;
+        }
+        if (a.colwise) {
+          const int* ce = cexp + (rr >> 5) * 64 + blk * 32;  // same address across the warp
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          v[i] = __uint_as_float((uint32_t)tile[rb * 32 + i][cc] << 16);
-        const uint32_t s = mx_quant_block(v, q);
-        uint4* dst = reinterpret_cast<uint4*>(a.q_col + col * Mv + row);
-        dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-        dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-        const int64_t so = a.sf_mma ? sf_mma_offset(col, row / 32, a.scol_pad)
-                                    : col * (Mv / 32) + row / 32;
-        a.s_col[so] = (uint8_t)s;
+          for (int i = 0; i < 8; ++i) {
+            const int4 e4 = *reinterpret_cast<const int4*>(ce + 4 * i);
+            const uint32_t lo = cvt_e4m3x2(v[4 * i] * mx_inv_scale(e4.x),
+                                           v[4 * i + 1] * mx_inv_scale(e4.y));
+            const uint32_t hi = cvt_e4m3x2(v[4 * i + 2] * mx_inv_scale(e4.z),
+                                           v[4 * i + 3] * mx_inv_scale(e4.w));
+            q[i] = lo | (hi << 16);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(a.q_col + row * a.N + col);
+          dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+          dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+        }
       }
     }
-    __syncthreads();  // this buffer is refilled by the next iteration's copies
+    __syncthreads();  // this buffer (and cexp) are reused by the next iteration
   }
 }
 

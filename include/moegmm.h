@@ -197,7 +197,7 @@ moe_status_t moe_route_permute_noalloc(const moe_layer_desc_t *desc, int32_t T,
  *   scale byte e + 127, q = E4M3(v / 2^e) rounded to nearest even, saturating at +-448.
  *   in      bf16 [M, N]
  *   rowwise:  q_row  e4m3 [M, N]       blocks of 32 along N; s_row e8m0 [M, N/32]
- *   colwise:  q_col  e4m3 [N, M]       blocks of 32 along M, stored transposed;
+ *   colwise:  q_col  e4m3 [M, N]       blocks of 32 along M (same layout as in);
  *             s_col  e8m0 [N, M/32]    (row groups that start at multiples of 32 rows, as the
  *                                      permuted expert segments do, restart blocks for free)
  * N must be a multiple of 32 for rowwise, M a multiple of 32 for colwise; the pointers of

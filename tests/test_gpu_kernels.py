@@ -23,7 +23,7 @@ def test_mxfp8_quantize_bit_exact(lib, M, N, scale, outliers):
     x = bf16_dev(a)
     q_row = torch.empty(M, N, dtype=torch.uint8, device="cuda")
     s_row = torch.empty(M, N // 32, dtype=torch.uint8, device="cuda")
-    q_col = torch.empty(N, M, dtype=torch.uint8, device="cuda")
+    q_col = torch.empty(M, N, dtype=torch.uint8, device="cuda")
     s_col = torch.empty(N, M // 32, dtype=torch.uint8, device="cuda")
     g.mxfp8_quantize(x, M, N, 1, 1, q_row, s_row, q_col, s_col)
     torch.cuda.synchronize()
@@ -33,7 +33,7 @@ def test_mxfp8_quantize_bit_exact(lib, M, N, scale, outliers):
     assert np.array_equal(s_row.cpu().numpy(), s_r)
     assert np.array_equal(q_row.cpu().numpy(), c_r)
     assert np.array_equal(s_col.cpu().numpy(), s_c.T)
-    assert np.array_equal(q_col.cpu().numpy(), c_c.T)
+    assert np.array_equal(q_col.cpu().numpy(), c_c)
 
 
 def test_mxfp8_quantize_one_direction_only(lib):

@@ -502,6 +502,7 @@ moe_status_t mxfp8_quantize(const void* in, int64_t M, int64_t N, int32_t rowwis
   if (!in || !aligned16(in)) return fail(MOE_ERR_INVALID_ARG, "in must be non-NULL, 16B aligned");
   if (N % 32) return fail(MOE_ERR_UNSUPPORTED, "N must be a multiple of 32");
   if (colwise && M % 32) return fail(MOE_ERR_UNSUPPORTED, "M must be a multiple of 32 (colwise)");
+  if (!mxfp8_quantize_size_ok(M, N)) return fail(MOE_ERR_UNSUPPORTED, "M or N too large");
   if (rowwise && (!q_row || !s_row || !aligned16(q_row)))
     return fail(MOE_ERR_INVALID_ARG, "rowwise outputs must be non-NULL (q_row 16B aligned)");
   if (colwise && (!q_col || !s_col || !aligned16(q_col)))

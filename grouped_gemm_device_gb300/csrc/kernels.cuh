@@ -29,6 +29,8 @@ __global__ void pack_fc1_kernel(const uint16_t* src, uint16_t* dst, int E, int H
                                 int gated, int ilv, int inverse);
 
 // mxfp8.cu
+// Sizes the quantiser's 32-bit tile indexing covers (M rows < 2^31, tile count < 2^31).
+bool mxfp8_quantize_size_ok(int64_t M, int64_t N);
 void launch_mxfp8_quantize(const void* in, int64_t M, int64_t N, int rowwise, int colwise,
                            uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                            int num_sms, cudaStream_t s);

@@ -48,6 +48,27 @@ def test_mxfp8_quantize_one_direction_only(lib):
     assert np.array_equal(q_row.cpu().numpy(), c_r) and np.array_equal(s_row.cpu().numpy(), s_r)
 
 
+def test_mxfp8_quantize_16_byte_aligned_outputs(lib):
+    """Outputs that are 16- but not 32-byte aligned take the 128-bit store path."""
+    M, N = 160, 224
+    a = synth.gen_bf16_matrix(9, M, N, outlier_rows=3)
+    x = bf16_dev(a)
+    q_row_buf = torch.zeros(M * N + 16, dtype=torch.uint8, device="cuda")
+    q_col_buf = torch.zeros(M * N + 16, dtype=torch.uint8, device="cuda")
+    q_row, q_col = q_row_buf[16:].view(M, N), q_col_buf[16:].view(M, N)
+    assert q_row.data_ptr() % 32 == 16 and q_col.data_ptr() % 32 == 16
+    s_row = torch.empty(M, N // 32, dtype=torch.uint8, device="cuda")
+    s_col = torch.empty(N, M // 32, dtype=torch.uint8, device="cuda")
+    g.mxfp8_quantize(x, M, N, 1, 1, q_row, s_row, q_col, s_col)
+    torch.cuda.synchronize()
+    v = om.bf16_to_f64(a)
+    c_r, s_r = omx.quantize_blocks(v, axis=1)
+    c_c, s_c = omx.quantize_blocks(v, axis=0)
+    assert np.array_equal(q_row.cpu().numpy(), c_r) and np.array_equal(s_row.cpu().numpy(), s_r)
+    assert np.array_equal(q_col.cpu().numpy(), c_c) and np.array_equal(s_col.cpu().numpy(), s_c.T)
+    assert not q_row_buf[:16].any() and not q_col_buf[:16].any()
+
+
 ROUTE_CASES = {
     "tiny": synth.CONFIGS["tiny"],
     "ragged_T": synth.LayerConfig("r", T=301, E=6, k=2, H=64, F=64, seed=11),

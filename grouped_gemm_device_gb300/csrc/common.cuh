@@ -58,11 +58,21 @@ MOE_DEVICE uint32_t cvt_e4m3x2(float lo, float hi) {
 
 // Quantise 32 fp32 values (one block) into 32 E4M3 bytes (as 8 words) and return the scale
 // byte.
-MOE_DEVICE uint32_t mx_quant_block(const float (&v)[32], uint32_t (&q)[8]) {
-  float amax = 0.f;
+MOE_DEVICE float amax32(const float (&v)[32]) {
+  // four independent chains (max is exact, so the grouping does not change the result)
+  float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  const int e = mx_block_exponent(amax);
+  for (int i = 0; i < 32; i += 4) {
+    m0 = fmaxf(m0, fabsf(v[i]));
+    m1 = fmaxf(m1, fabsf(v[i + 1]));
+    m2 = fmaxf(m2, fabsf(v[i + 2]));
+    m3 = fmaxf(m3, fabsf(v[i + 3]));
+  }
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
+MOE_DEVICE uint32_t mx_quant_block(const float (&v)[32], uint32_t (&q)[8]) {
+  const int e = mx_block_exponent(amax32(v));
   const float inv = mx_inv_scale(e);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -71,6 +81,14 @@ MOE_DEVICE uint32_t mx_quant_block(const float (&v)[32], uint32_t (&q)[8]) {
     q[i] = lo | (hi << 16);
   }
   return (uint32_t)(e + 127);
+}
+
+// ----------------------------------------------------------------------------- 256-bit global
+// 32 bytes at a 32-byte aligned global address in one access (sm_100 and later).
+MOE_DEVICE void st_global_v8(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
 }
 
 // ----------------------------------------------------------------------------- smem / timer

@@ -59,6 +59,7 @@ struct GemmArgs {
   int gated;
   int ilv;
   int F;
+  int wide;  // out and out2 are 32-byte aligned with 16-element strides: 256-bit stores
   ActDev act;
   int* err;
 };
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-          if (row_ok) store_bf16x32(o + cc, v);
+          if (row_ok) store_bf16x32w(o + cc, v, p.wide);
         }
       } else if (EPI == EPI_GLU) {
         const float prob = row_ok ? p.row_prob[row] : 0.f;
@@ -361,9 +362,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             glu_fwd32(p.act, prob, g, l, v);
             if (row_ok) {
-              store_bf16x32(zrow + t.n0 + gcol, g);
-              store_bf16x32(zrow + t.n0 + lcol, l);
-              store_bf16x32(arow + t.n0 / 2 + cc, v);
+              store_bf16x32w(zrow + t.n0 + gcol, g, p.wide);
+              store_bf16x32w(zrow + t.n0 + lcol, l, p.wide);
+              store_bf16x32w(arow + t.n0 / 2 + cc, v, p.wide);
             }
           }
         } else {
@@ -379,8 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               v[i] = prob * rr * rr;
             }
             if (row_ok) {
-              store_bf16x32(zrow + t.n0 + cc, zz);
-              store_bf16x32(arow + t.n0 + cc, v);
+              store_bf16x32w(zrow + t.n0 + cc, zz, p.wide);
+              store_bf16x32w(arow + t.n0 + cc, v, p.wide);
             }
           }
         }
@@ -408,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) das[i] = __uint_as_float(r[i]);
             dp += glu_bwd32(p.act, prob, das, g, l);
-            store_bf16x32(dzrow + gcol, g);
-            store_bf16x32(dzrow + lcol, l);
+            store_bf16x32w(dzrow + gcol, g, p.wide);
+            store_bf16x32w(dzrow + lcol, l, p.wide);
           } else {
             float zz[32];
             if (row_ok) load_bf16x32(zrow + f0, zz);
@@ -423,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               dp += das * rr * rr;
               zz[i] = prob * das * 2.f * rr;
             }
-            store_bf16x32(dzrow + f0, zz);
+            store_bf16x32w(dzrow + f0, zz, p.wide);
           }
         }
         if (row_ok) p.dprob_part[(int64_t)row * p.nparts + (t.n0 / BN) * 2 + half] = dp;
@@ -485,6 +486,7 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
   if (p.role < 0 || p.role > 5) return cudaErrorInvalidValue;
   const int kid = kKid[p.role];
   const uint64_t R = (uint64_t)p.R_cap;
+  auto aligned32 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 31) == 0; };
   const int H = p.H, F = p.F, N1 = p.N1, E = p.E;
   bool ok = true;
   int grid = p.num_ctas;
@@ -496,6 +498,8 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       a.out = p.out; a.ldo = N1;
       a.out2 = p.out2; a.ldo2 = F;
       if (!ok) return cudaErrorInvalidValue;
+      a.wide = aligned32(a.out) && aligned32(a.out2) && a.ldo % 16 == 0 && a.ldo2 % 16 == 0 &&
+               a.out_estride % 16 == 0;
       return launch_instance<kBN, kStages, false, false, EPI_GLU, false, true>(a, grid, s, kid);
     case ROLE_FC2_FPROP:
       ok &= tmap_2d(&a.tmA, p.a_s, F, R, 64, BM);
@@ -503,6 +507,8 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       a.K = F; a.N = H;
       a.out = p.out; a.ldo = H;
       if (!ok) return cudaErrorInvalidValue;
+      a.wide = aligned32(a.out) && aligned32(a.out2) && a.ldo % 16 == 0 && a.ldo2 % 16 == 0 &&
+               a.out_estride % 16 == 0;
       return launch_instance<kBN, kStages, false, true, EPI_STORE, false, true>(a, grid, s, kid);
     case ROLE_FC2_DGRAD:
       ok &= tmap_2d(&a.tmA, p.dy_perm, H, R, 64, BM);
@@ -512,6 +518,8 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       a.z = static_cast<const uint16_t*>(p.z); a.ldz = N1;
       a.dprob_part = p.dprob_part; a.nparts = dprob_parts(F);
       if (!ok) return cudaErrorInvalidValue;
+      a.wide = aligned32(a.out) && aligned32(a.out2) && a.ldo % 16 == 0 && a.ldo2 % 16 == 0 &&
+               a.out_estride % 16 == 0;
       return launch_instance<kBN, kStages, false, false, EPI_DGLU, false, true>(a, grid, s, kid);
     case ROLE_FC1_DGRAD:
       ok &= tmap_2d(&a.tmA, p.dz, N1, R, 64, BM);
@@ -519,6 +527,8 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       a.K = N1; a.N = H;
       a.out = p.out; a.ldo = H;
       if (!ok) return cudaErrorInvalidValue;
+      a.wide = aligned32(a.out) && aligned32(a.out2) && a.ldo % 16 == 0 && a.ldo2 % 16 == 0 &&
+               a.out_estride % 16 == 0;
       return launch_instance<kBN, kStages, false, true, EPI_STORE, false, true>(a, grid, s, kid);
     case ROLE_FC2_WGRAD:
     case ROLE_FC1_WGRAD: {
@@ -529,6 +539,7 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       a.M = M; a.N = H;
       a.out = p.out; a.ldo = H; a.out_estride = (int64_t)M * H;
       if (!ok) return cudaErrorInvalidValue;
+      a.wide = aligned32(a.out) && a.ldo % 16 == 0 && a.out_estride % 16 == 0;
       const int64_t tiles = (int64_t)E * ((M + BM - 1) / BM) * ((H + kBN - 1) / kBN);
       grid = (int)std::min<int64_t>(grid, tiles);
       return launch_instance<kBN, kStages, true, true, EPI_STORE, true, false>(a, grid, s, kid);

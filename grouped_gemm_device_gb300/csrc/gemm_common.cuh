@@ -107,6 +107,19 @@ MOE_DEVICE void store_bf16x32(void* dst, const float (&v)[32]) {
     d[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
                       pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
 }
+// 32 fp32 -> 64 bytes of bf16 at a 32-byte aligned address: two 256-bit stores.
+MOE_DEVICE void store_bf16x32_v8(void* dst, const float* v) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+  st_global_v8(dst, w);
+  st_global_v8(static_cast<uint8_t*>(dst) + 32, w + 8);
+}
+// Either form: wide = dst is 32-byte aligned.
+MOE_DEVICE void store_bf16x32w(void* dst, const float (&v)[32], bool wide) {
+  if (wide) store_bf16x32_v8(dst, v);
+  else store_bf16x32(dst, v);
+}
 MOE_DEVICE void load_bf16x32(const void* src, float (&v)[32]) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
 #pragma unroll

@@ -12,13 +12,16 @@
 //            their 512 + 1024 bytes of scale slabs, all counted on one mbarrier,
 //   warp 1   TMEM owner; one thread copies the stage's scales into TMEM (tcgen05.cp) and issues
 //            four tcgen05.mma.kind::mxf8f6f4.block_scale 128x256x32 (scale byte = K step),
-//   warps 2-9 epilogue: drain the accumulator into registers as packed bf16 (warp w takes TMEM
-//            lanes 32*(w%4).. and 128 of the 256 columns), release TMEM, then bf16 store, or
-//            GLU / dGLU with fused row-wise and column-wise MXFP8 quantisation.
+//   warps 2-9 epilogue: drain the accumulator into registers (warp w takes TMEM lanes
+//            32*(w%4).. and 128 of the 256 columns), release TMEM, then bf16 store, or GLU /
+//            dGLU with fused row-wise and column-wise MXFP8 quantisation. Every 32-byte E4M3
+//            run and every 64-byte bf16 run leaves in 256-bit stores; the dGLU epilogue stages
+//            the saved Z of its next 32 columns in shared memory (cp.async) while it quantises.
 // The tile is 128 x 256 because a 128 x 256 x 32 MMA runs at the full fp8 rate while 128-wide
 // ones do not; TMEM then holds one accumulator (256 columns) plus 12 scale columns per stage,
 // and the register drain lets the next tile's MMAs start while the epilogue works. Expert
-// segments are padded to 128 rows so that every tile starts on a scale slab.
+// segments are padded to 128 rows so that every tile starts on a scale slab. The activation
+// is a template parameter, so each kernel carries the epilogue code of one activation only.
 #include "gemm_common.cuh"
 
 namespace moe {
@@ -66,7 +69,8 @@ struct MxArgs {
   int64_t ldz;
   float* dprob_part;
   int nparts;
-  int gated;
+  int ilv;                             // gate/linear interleave of the packed columns
+  int wide;                            // STORE: out is 32-byte aligned (256-bit stores)
   ActDev act;
   int* err;
 };
@@ -78,10 +82,16 @@ constexpr int SFA_BYTES = 512;   // 128 rows x 4 k-blocks
 constexpr int SFB_BYTES = 1024;  // 256 rows x 4 k-blocks
 constexpr int DATA = STAGES * STAGE_BYTES;
 constexpr int SF_OFF = DATA;
+constexpr int XP_LD = 36;  // fp32 row of the per-warp 32 x 32 staging tile (144 B, 16-B aligned)
 constexpr int XPOSE_OFF = SF_OFF + STAGES * (SFA_BYTES + SFB_BYTES);
-constexpr int XPOSE_WARP_BYTES = 32 * 33 * 4;  // 32 x 32 fp32 staging, padded rows
-constexpr int CTRL_OFF = XPOSE_OFF + kEpiWarps * XPOSE_WARP_BYTES;
+constexpr int XPOSE_WARP_BYTES = 32 * XP_LD * 4 + 32 * 4;  // staging tile + 32 column 2^-e
+constexpr int ZST_OFF = XPOSE_OFF + kEpiWarps * XPOSE_WARP_BYTES;
+constexpr int ZST_WARP_BYTES = 32 * 128;  // dGLU: saved Z of one chunk, 32 rows x 64 bf16
+constexpr int CTRL_OFF = ZST_OFF + kEpiWarps * ZST_WARP_BYTES;
 constexpr int SMEM_TOTAL = CTRL_OFF + 4096 + 1024;
+static_assert(SMEM_TOTAL <= 232448, "shared memory above the sm_100 per-block limit");
+static_assert(XPOSE_OFF % 16 == 0 && XPOSE_WARP_BYTES % 16 == 0 && ZST_OFF % 128 == 0 &&
+              CTRL_OFF % 8 == 0, "smem alignment");
 
 struct Ctrl {
   uint64_t full[STAGES];
@@ -132,63 +142,83 @@ MOE_DEVICE void decode_tile(int tile, const MxArgs& p, const Ctrl& c, int MT, in
   }
 }
 
-// Row-wise MXFP8 of one 32-column block held by this thread.
-MOE_DEVICE void mx_store_row_block(const float (&v)[32], uint8_t* q, uint8_t* s_row, int64_t row,
-                                   int64_t col, int64_t ld, int64_t s_pad) {
+// Row-wise MXFP8 of one 32-column block held by this thread: one 32-byte run and its scale.
+MOE_DEVICE void mx_row_block(const float (&v)[32], uint8_t* qdst, uint8_t* sdst) {
   uint32_t w[8];
-  const uint32_t sb = mx_quant_block(v, w);
-  uint4* dst = reinterpret_cast<uint4*>(q + row * ld + col);
-  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  s_row[sf_mma_offset(row, col / 32, s_pad)] = (uint8_t)sb;
+  *sdst = (uint8_t)mx_quant_block(v, w);
+  st_global_v8(qdst, w);
 }
 
 // Column-wise MXFP8 of the warp's 32 rows x 32 columns (this lane holds one row), stored in the
-// natural row-major layout q[row][col]: lane j finds column col0 + j's block maximum through the
-// warp's shared-memory tile and publishes its exponent; every lane then quantises its own row
-// with the 32 column scales and stores one 32-byte run.
-MOE_DEVICE void mx_store_col_blocks(const float (&v)[32], float* xp, uint8_t* q, uint8_t* s_col,
-                                    int64_t row0, int64_t col0, int64_t ld, int64_t s_pad,
-                                    int lane) {
+// natural row-major layout. Lane j takes column j's maximum from the warp's shared-memory tile
+// and publishes 2^-e; every lane then quantises its own row with the 32 column factors and
+// stores one 32-byte run. The tile and the factors are rewritten only after every lane has
+// passed the next call's first warp barrier, so two barriers per call suffice.
+MOE_DEVICE void mx_col_block(const float (&v)[32], float* xp, uint8_t* qdst, uint8_t* sdst,
+                             int lane) {
+  float* xinv = xp + 32 * XP_LD;
+  float4* mine = reinterpret_cast<float4*>(xp + lane * XP_LD);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) xp[lane * 33 + i] = v[i];
+  for (int k = 0; k < 8; ++k)
+    mine[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
   __syncwarp();
-  float amax = 0.f;
+  float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(xp[i * 33 + lane]));
-  const int e = mx_block_exponent(amax);
-  s_col[sf_mma_offset(col0 + lane, row0 / 32, s_pad)] = (uint8_t)(e + 127);
-  __syncwarp();
-  int* xe = reinterpret_cast<int*>(xp);  // the 32 column exponents, reusing the tile
-  xe[lane] = e;
-  __syncwarp();
-  uint32_t qq[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int4 e4 = *reinterpret_cast<const int4*>(xe + 4 * i);
-    const uint32_t lo = cvt_e4m3x2(v[4 * i] * mx_inv_scale(e4.x), v[4 * i + 1] * mx_inv_scale(e4.y));
-    const uint32_t hi =
-        cvt_e4m3x2(v[4 * i + 2] * mx_inv_scale(e4.z), v[4 * i + 3] * mx_inv_scale(e4.w));
-    qq[i] = lo | (hi << 16);
+  for (int i = 0; i < 32; i += 4) {
+    m0 = fmaxf(m0, fabsf(xp[(i + 0) * XP_LD + lane]));
+    m1 = fmaxf(m1, fabsf(xp[(i + 1) * XP_LD + lane]));
+    m2 = fmaxf(m2, fabsf(xp[(i + 2) * XP_LD + lane]));
+    m3 = fmaxf(m3, fabsf(xp[(i + 3) * XP_LD + lane]));
   }
+  const int e = mx_block_exponent(fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)));
+  *sdst = (uint8_t)(e + 127);
+  xinv[lane] = mx_inv_scale(e);
   __syncwarp();
-  uint4* dst = reinterpret_cast<uint4*>(q + (row0 + lane) * ld + col0);
-  dst[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
-  dst[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
+  uint32_t w[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float4 f = reinterpret_cast<const float4*>(xinv)[k];
+    w[k] = cvt_e4m3x2(v[4 * k] * f.x, v[4 * k + 1] * f.y) |
+           (cvt_e4m3x2(v[4 * k + 2] * f.z, v[4 * k + 3] * f.w) << 16);
+  }
+  st_global_v8(qdst, w);
 }
 
-MOE_DEVICE void unpack32(const uint32_t* pk, float (&v)[32]) {
+// dGLU: this lane's row of one chunk of saved Z, copied into the warp's shared buffer with
+// cp.async. Pieces 0-3 (16 bytes each) come from src0 (gate columns, or the only half when not
+// gated), pieces 4-7 from src1 (linear columns). Piece c of row r sits at r*128 +
+// ((c ^ (r & 7)) * 16), so 8 rows reading the same piece touch 8 different bank groups.
+MOE_DEVICE void zst_issue(uint32_t buf, const uint16_t* src0, const uint16_t* src1, int lane,
+                          bool two) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    v[2 * i] = bf16_lo(pk[i]);
-    v[2 * i + 1] = bf16_hi(pk[i]);
+  for (int c = 0; c < 8; ++c) {
+    if (c >= 4 && !two) break;
+    const uint16_t* src = c < 4 ? src0 + 8 * c : src1 + 8 * (c - 4);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     buf + lane * 128 + ((c ^ (lane & 7)) * 16)),
+                 "l"(src)
+                 : "memory");
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
 }
+MOE_DEVICE void zst_piece(const uint8_t* buf, int c, int lane, uint32_t* w) {
+  const uint4 v = *reinterpret_cast<const uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) * 16));
+  w[0] = v.x;
+  w[1] = v.y;
+  w[2] = v.z;
+  w[3] = v.w;
+}
+
+// Gate and linear columns of dA column f in the packed Z layout (blocks of ilv gate columns
+// followed by ilv linear columns; ilv a power of two).
+MOE_DEVICE int gate_col(int f, int ilv) { return ((f & ~(ilv - 1)) << 1) | (f & (ilv - 1)); }
 
 // A_MN / B_MN: the operand is a column-wise copy stored [K rows, M or N columns] (MN-major);
-// otherwise it is [M or N rows, K] (K-major).
-template <int EPI, bool KG, int ILV, bool A_MN, bool B_MN>
+// otherwise it is [M or N rows, K] (K-major). KIND: the activation of the GLU / dGLU epilogue
+// (moe_activation_t; unused by STORE). ILV: the gate/linear interleave of the GLU epilogue.
+template <int EPI, int KIND, bool KG, int ILV, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __grid_constant__ MxArgs p) {
+  constexpr bool kGated = KIND != MOE_ACT_SRELU;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -363,6 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;  // columns [128*half, 128*half + 128) of the tile
     float* xp = reinterpret_cast<float*>(smem + XPOSE_OFF + (warp - 2) * XPOSE_WARP_BYTES);
+    const uint8_t* zst = smem + ZST_OFF + (warp - 2) * ZST_WARP_BYTES;
+    const uint32_t zst_a = smem_u32(zst);
     int acc_i = 0;
     for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
       TileInfo t;
@@ -380,9 +412,19 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
         }
         continue;
       }
+      const uint16_t* zrow = p.z + (int64_t)row * p.ldz;
+      if constexpr (EPI == EPI_DGLU) {
+        // the saved Z of the first chunk comes in while the MMAs run
+        const int f0 = t.n0 + cb;
+        if (f0 < p.N) {
+          const int gc = kGated ? gate_col(f0, p.ilv) : f0;
+          zst_issue(zst_a, zrow + gc, zrow + gc + p.ilv, lane, kGated);
+        }
+      }
+      const float prob = EPI == EPI_STORE ? 0.f : p.row_prob[row];
       if (!mbar_wait(&c.tfull, acc_i & 1, abort, p.err)) break;
       tc_fence_after();
-      if (EPI == EPI_GLU) {
+      if constexpr (EPI == EPI_GLU) {
         // GLU: drain the 128 columns as fp32 (the activation and its MXFP8 blocks are computed
         // from the fp32 accumulator), free TMEM, then work from registers
         float acc[128];
@@ -402,18 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
         if (lane == 0) mbar_arrive(&c.tempty);
         ++acc_i;
         // segments are 128-row aligned, so every row of the tile is inside its segment
-        const float prob = p.row_prob[row];
-        uint16_t* zrow = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo + t.n0 + cb;
+        uint16_t* zout = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo + t.n0 + cb;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {  // the saved Z (bf16)
-          if (t.n0 + cb + 32 * j < p.N) {
-            float zz[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) zz[i] = acc[32 * j + i];
-            store_bf16x32(zrow + 32 * j, zz);
-          }
-        }
-        if (p.gated) {
+        for (int j = 0; j < 4; ++j)  // the saved Z (bf16)
+          if (t.n0 + cb + 32 * j < p.N) store_bf16x32_v8(zout + 32 * j, &acc[32 * j]);
+        uint8_t* qr = p.q_row + (int64_t)row * p.ld_q_row;
+        uint8_t* qc = p.q_col + (int64_t)row * p.ld_q_col;
+        if constexpr (kGated) {
           // this half holds 64 gate and 64 linear columns: two 32-wide output blocks
 #pragma unroll
           for (int c32 = 0; c32 < 2; ++c32) {
@@ -421,10 +458,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
             const int acol = (t.n0 + cb) / 2 + c32 * 32;
             if (t.n0 + cb + g_off >= p.N) break;
             float v[32];
-            glu_fwd32(p.act, prob, &acc[g_off], &acc[g_off + ILV], v);
-            mx_store_row_block(v, p.q_row, p.s_row, row, acol, p.ld_q_row, p.s_row_pad);
-            mx_store_col_blocks(v, xp, p.q_col, p.s_col, row0, acol, p.ld_q_col, p.s_col_pad,
-                                lane);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              v[i] = prob * act_fwd_k<KIND>(p.act, acc[g_off + i], acc[g_off + ILV + i]);
+            mx_row_block(v, qr + acol, p.s_row + sf_mma_offset(row, acol / 32, p.s_row_pad));
+            mx_col_block(v, xp, qc + acol,
+                         p.s_col + sf_mma_offset(acol + lane, row0 / 32, p.s_col_pad), lane);
           }
         } else {
 #pragma unroll
@@ -437,9 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
               const float rr = fmaxf(acc[32 * j + i], 0.f);
               v[i] = prob * rr * rr;
             }
-            mx_store_row_block(v, p.q_row, p.s_row, row, acol, p.ld_q_row, p.s_row_pad);
-            mx_store_col_blocks(v, xp, p.q_col, p.s_col, row0, acol, p.ld_q_col, p.s_col_pad,
-                                lane);
+            mx_row_block(v, qr + acol, p.s_row + sf_mma_offset(row, acol / 32, p.s_row_pad));
+            mx_col_block(v, xp, qc + acol,
+                         p.s_col + sf_mma_offset(acol + lane, row0 / 32, p.s_col_pad), lane);
           }
         }
         continue;
@@ -463,82 +502,92 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
       if (lane == 0) mbar_arrive(&c.tempty);
       ++acc_i;
 
-      if (EPI == EPI_STORE) {
+      if constexpr (EPI == EPI_STORE) {
         if (row_ok) {
           uint16_t* o = static_cast<uint16_t*>(p.out) + (KG ? (int64_t)t.e * p.out_estride : 0) +
                         (int64_t)row * p.ldo + t.n0 + cb;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             if (t.n0 + cb + 32 * j < p.N) {
-              uint4* d = reinterpret_cast<uint4*>(o + 32 * j);
+              if (p.wide) {
+                st_global_v8(o + 32 * j, &pk[16 * j]);
+                st_global_v8(o + 32 * j + 16, &pk[16 * j + 8]);
+              } else {
+                uint4* d = reinterpret_cast<uint4*>(o + 32 * j);
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                d[i] = make_uint4(pk[16 * j + 4 * i], pk[16 * j + 4 * i + 1],
-                                  pk[16 * j + 4 * i + 2], pk[16 * j + 4 * i + 3]);
+                for (int i = 0; i < 4; ++i)
+                  d[i] = make_uint4(pk[16 * j + 4 * i], pk[16 * j + 4 * i + 1],
+                                    pk[16 * j + 4 * i + 2], pk[16 * j + 4 * i + 3]);
+              }
             }
           }
         }
       } else {  // EPI_DGLU: accumulator = dA_s over F columns
-        const float prob = p.row_prob[row];
-        float dp = 0.f;
-        const uint16_t* zrow = p.z + (int64_t)row * p.ldz;
+        float dp0 = 0.f, dp1 = 0.f, dp2 = 0.f, dp3 = 0.f;
+        uint8_t* qr = p.q_row + (int64_t)row * p.ld_q_row;
+        uint8_t* qc = p.q_col + (int64_t)row * p.ld_q_col;
         // one copy of the chunk body (keeps the kernel inside the instruction cache); the
-        // chunk's 16 packed registers are picked by a switch so they stay in registers
+        // packed accumulator shifts down by one chunk per iteration, so chunk j is always
+        // pk[0..15] and no register is indexed at run time
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
           const int f0 = t.n0 + cb + 32 * j;
           if (f0 >= p.N) break;
-          uint32_t cur[16];
-          switch (j) {
-            case 0:
+          const uint32_t* cur = pk;
+          const int gcol = kGated ? gate_col(f0, p.ilv) : f0;
+          const int lcol = gcol + p.ilv;
+          float dg[32], dl[32];
+          // this lane's own pieces of the chunk (each lane reads only the row it copied)
+          asm volatile("cp.async.wait_all;" ::: "memory");
 #pragma unroll
-              for (int i = 0; i < 16; ++i) cur[i] = pk[i];
-              break;
-            case 1:
-#pragma unroll
-              for (int i = 0; i < 16; ++i) cur[i] = pk[16 + i];
-              break;
-            case 2:
-#pragma unroll
-              for (int i = 0; i < 16; ++i) cur[i] = pk[32 + i];
-              break;
-            default:
-#pragma unroll
-              for (int i = 0; i < 16; ++i) cur[i] = pk[48 + i];
-              break;
-          }
-          float das[32];
-          unpack32(cur, das);
-          if (p.gated) {
-            const int gcol = (f0 / ILV) * 2 * ILV + (f0 % ILV);
-            const int lcol = gcol + ILV;
-            float g[32], l[32];
-            load_bf16x32(zrow + gcol, g);
-            load_bf16x32(zrow + lcol, l);
-            dp += glu_bwd32(p.act, prob, das, g, l);
-            mx_store_row_block(g, p.q_row, p.s_row, row, gcol, p.ld_q_row, p.s_row_pad);
-            mx_store_row_block(l, p.q_row, p.s_row, row, lcol, p.ld_q_row, p.s_row_pad);
-            mx_store_col_blocks(g, xp, p.q_col, p.s_col, row0, gcol, p.ld_q_col, p.s_col_pad,
-                                lane);
-            mx_store_col_blocks(l, xp, p.q_col, p.s_col, row0, lcol, p.ld_q_col, p.s_col_pad,
-                                lane);
-          } else {
-            float zz[32];
-            load_bf16x32(zrow + f0, zz);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float rr = fmaxf(zz[i], 0.f);
-              dp += das[i] * rr * rr;
-              zz[i] = prob * das[i] * 2.f * rr;
+          for (int h = 0; h < 2; ++h) {
+            uint32_t gw[8], lw[8];
+            zst_piece(zst, 2 * h, lane, gw);
+            zst_piece(zst, 2 * h + 1, lane, gw + 4);
+            if (kGated) {
+              zst_piece(zst, 4 + 2 * h, lane, lw);
+              zst_piece(zst, 5 + 2 * h, lane, lw + 4);
             }
-            mx_store_row_block(zz, p.q_row, p.s_row, row, f0, p.ld_q_row, p.s_row_pad);
-            mx_store_col_blocks(zz, xp, p.q_col, p.s_col, row0, f0, p.ld_q_col, p.s_col_pad,
-                                lane);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int k = 16 * h + i;
+              const float d = (k & 1) ? bf16_hi(cur[k >> 1]) : bf16_lo(cur[k >> 1]);
+              const float g = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
+              float contrib;
+              if constexpr (kGated) {
+                const float l = (i & 1) ? bf16_hi(lw[i >> 1]) : bf16_lo(lw[i >> 1]);
+                contrib = d * act_bwd_k<KIND>(p.act, g, l, prob * d, dg[k], dl[k]);
+              } else {
+                const float rr = fmaxf(g, 0.f);
+                contrib = d * rr * rr;
+                dg[k] = prob * d * 2.f * rr;
+              }
+              if ((k & 3) == 0) dp0 += contrib;
+              else if ((k & 3) == 1) dp1 += contrib;
+              else if ((k & 3) == 2) dp2 += contrib;
+              else dp3 += contrib;
+            }
           }
+          // the next chunk's Z goes into the same buffer: this lane has read its row already
+          if (j + 1 < 4 && f0 + 32 < p.N) {
+            const int gn = kGated ? gate_col(f0 + 32, p.ilv) : f0 + 32;
+            zst_issue(zst_a, zrow + gn, zrow + gn + p.ilv, lane, kGated);
+          }
+#pragma unroll
+          for (int i = 0; i < 48; ++i) pk[i] = pk[i + 16];
+          mx_row_block(dg, qr + gcol, p.s_row + sf_mma_offset(row, gcol / 32, p.s_row_pad));
+          if constexpr (kGated)
+            mx_row_block(dl, qr + lcol, p.s_row + sf_mma_offset(row, lcol / 32, p.s_row_pad));
+          mx_col_block(dg, xp, qc + gcol,
+                       p.s_col + sf_mma_offset(gcol + lane, row0 / 32, p.s_col_pad), lane);
+          if constexpr (kGated)
+            mx_col_block(dl, xp, qc + lcol,
+                         p.s_col + sf_mma_offset(lcol + lane, row0 / 32, p.s_col_pad), lane);
         }
-        p.dprob_part[(int64_t)row * p.nparts + (t.n0 / BN) * 2 + half] = dp;
+        p.dprob_part[(int64_t)row * p.nparts + (t.n0 / BN) * 2 + half] = (dp0 + dp1) + (dp2 + dp3);
       }
     }
+    if constexpr (EPI == EPI_DGLU) asm volatile("cp.async.wait_all;" ::: "memory");
   }
 
   tc_fence_before();
@@ -559,9 +608,9 @@ bool tmap_fp8(CUtensorMap* m, const MxOperand& t, bool mn_major) {
   return make_tmap(m, t.q, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8);
 }
 
-template <int EPI, bool KG, int ILV, bool A_MN, bool B_MN>
+template <int EPI, int KIND, bool KG, int ILV, bool A_MN, bool B_MN>
 cudaError_t launch_mx(const MxArgs& a, int grid, cudaStream_t s, int kid) {
-  auto kern = grouped_gemm_mx_kernel<EPI, KG, ILV, A_MN, B_MN>;
+  auto kern = grouped_gemm_mx_kernel<EPI, KIND, KG, ILV, A_MN, B_MN>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e =
@@ -574,10 +623,27 @@ cudaError_t launch_mx(const MxArgs& a, int grid, cudaStream_t s, int kid) {
   return cudaGetLastError();
 }
 
+// GLU / dGLU kernels for one activation. The dGLU epilogue takes the interleave at run time;
+// the GLU epilogue indexes its registers with it, so it is compiled for 32 and 64.
+template <int EPI, int KIND>
+cudaError_t launch_act(const MxArgs& a, int grid, cudaStream_t s, int kid) {
+  if constexpr (EPI == EPI_DGLU || KIND == MOE_ACT_SRELU) {
+    return launch_mx<EPI, KIND, false, 64, false, false>(a, grid, s, kid);
+  } else {
+    return a.ilv == 32 ? launch_mx<EPI, KIND, false, 32, false, false>(a, grid, s, kid)
+                       : launch_mx<EPI, KIND, false, 64, false, false>(a, grid, s, kid);
+  }
+}
+
 template <int EPI>
-cudaError_t launch_mx_ilv(const MxArgs& a, int ilv, int grid, cudaStream_t s, int kid) {
-  return ilv == 32 ? launch_mx<EPI, false, 32, false, false>(a, grid, s, kid)
-                   : launch_mx<EPI, false, 64, false, false>(a, grid, s, kid);
+cudaError_t launch_glu_family(const MxArgs& a, int kind, int grid, cudaStream_t s, int kid) {
+  switch (kind) {
+    case MOE_ACT_SWIGLU: return launch_act<EPI, MOE_ACT_SWIGLU>(a, grid, s, kid);
+    case MOE_ACT_CLAMPED_SWIGLU: return launch_act<EPI, MOE_ACT_CLAMPED_SWIGLU>(a, grid, s, kid);
+    case MOE_ACT_GEGLU: return launch_act<EPI, MOE_ACT_GEGLU>(a, grid, s, kid);
+    case MOE_ACT_SRELU: return launch_act<EPI, MOE_ACT_SRELU>(a, grid, s, kid);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
@@ -589,12 +655,13 @@ cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s) {
                               MOE_K_GEMM_FC2_WGRAD, MOE_K_GEMM_FC1_DGRAD, MOE_K_GEMM_FC1_WGRAD};
   if (p.role < 0 || p.role > 5) return cudaErrorInvalidValue;
   if (p.gated && p.ilv != 32 && p.ilv != 64) return cudaErrorInvalidValue;
+  if (p.gated != (p.act.kind != MOE_ACT_SRELU)) return cudaErrorInvalidValue;
   MxArgs a;
   memset(&a, 0, sizeof(a));
   a.offsets = p.offsets;
   a.E = p.E;
   a.R_cap = (int)p.R_cap;
-  a.gated = p.gated;
+  a.ilv = p.ilv;
   a.act = p.act;
   a.err = p.err;
   a.row_prob = p.row_prob;
@@ -643,16 +710,19 @@ cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s) {
   if (!tmap_fp8(&a.tmA, *A, kg) || !tmap_fp8(&a.tmB, *B, b_mn)) return cudaErrorInvalidValue;
   a.sfa = A->s; a.sfa_pad = A->s_pad;
   a.sfb = B->s; a.sfb_pad = B->s_pad;
+  a.wide = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0 && a.ldo % 16 == 0 &&
+           a.out_estride % 16 == 0;
   const int kid = kKid[p.role];
   switch (p.role) {
-    case ROLE_FC1_FPROP: return launch_mx_ilv<EPI_GLU>(a, p.ilv, grid, s, kid);
-    case ROLE_FC2_DGRAD: return launch_mx_ilv<EPI_DGLU>(a, p.ilv, grid, s, kid);
+    case ROLE_FC1_FPROP: return launch_glu_family<EPI_GLU>(a, p.act.kind, grid, s, kid);
+    case ROLE_FC2_DGRAD: return launch_glu_family<EPI_DGLU>(a, p.act.kind, grid, s, kid);
     case ROLE_FC2_FPROP:
-    case ROLE_FC1_DGRAD: return launch_mx<EPI_STORE, false, 64, false, true>(a, grid, s, kid);
+    case ROLE_FC1_DGRAD:
+      return launch_mx<EPI_STORE, 0, false, 64, false, true>(a, grid, s, kid);
     default: {
       const int64_t tiles = (int64_t)p.E * ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
       grid = (int)std::min<int64_t>(grid, tiles);
-      return launch_mx<EPI_STORE, true, 64, true, true>(a, grid, s, kid);
+      return launch_mx<EPI_STORE, 0, true, 64, true, true>(a, grid, s, kid);
     }
   }
 }

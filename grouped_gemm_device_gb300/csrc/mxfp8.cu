@@ -93,10 +93,7 @@ MOE_DEVICE uint32_t bf16x2_max(uint32_t a, uint32_t b) {
 // One 32-byte run: a single 256-bit store when the destination is 32-byte aligned.
 MOE_DEVICE void store_run32(uint8_t* dst, const uint32_t (&q)[8], bool wide) {
   if (wide) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst),
-                 "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3]), "r"(q[4]), "r"(q[5]), "r"(q[6]),
-                 "r"(q[7])
-                 : "memory");
+    st_global_v8(dst, q);
   } else {
     uint4* d = reinterpret_cast<uint4*>(dst);
     d[0] = make_uint4(q[0], q[1], q[2], q[3]);

@@ -105,3 +105,19 @@ class GpuRun:
         out = np.empty_like(packed)
         out[:, logical] = packed
         return out
+
+
+def check_weight_grads_16_byte_aligned(cfg):
+    """Weight gradients written to buffers that are 16- but not 32-byte aligned take the
+    128-bit store path of the GEMM epilogue; they must equal the 256-bit path bit for bit."""
+    run = GpuRun(Inputs(cfg))
+    dw1, dw2 = run.dw1p.clone(), run.dw2.clone()
+    L = run.layer
+    b1 = torch.zeros(L.dw1.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    b2 = torch.zeros(L.dw2.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    L.dw1 = b1[8:].view(L.dw1.shape)
+    L.dw2 = b2[8:].view(L.dw2.shape)
+    assert L.dw1.data_ptr() % 32 == 16 and L.dw2.data_ptr() % 32 == 16
+    run.run()
+    assert torch.equal(run.dw1p, dw1) and torch.equal(run.dw2, dw2)
+    assert not b1[:8].any() and not b2[:8].any()

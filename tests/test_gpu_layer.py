@@ -7,7 +7,8 @@ import torch
 
 from grouped_gemm_device_gb300 import synth
 
-from .gpu_helpers import BF16_TOL, GpuRun, Inputs, rel_fro, to_np
+from .gpu_helpers import (BF16_TOL, GpuRun, Inputs, check_weight_grads_16_byte_aligned, rel_fro,
+                          to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -72,6 +73,10 @@ def test_saved_intermediates_match_oracle(lib):
         assert rel_fro(a_s[seg], d["a_s"]) < BF16_TOL
         assert rel_fro(dz[seg], d["dZ"]) < BF16_TOL
         assert np.all(a_s[pad] == 0) and np.all(dz[pad] == 0) and np.all(z[pad] == 0)
+
+
+def test_weight_grads_into_16_byte_aligned_buffers(lib):
+    check_weight_grads_16_byte_aligned(CASES["multi_tile"])
 
 
 def test_sm_margin_and_rerun_are_deterministic(lib):

@@ -7,7 +7,8 @@ import torch
 
 from grouped_gemm_device_gb300 import synth
 
-from .gpu_helpers import MX_TOL, GpuRun, Inputs, rel_fro, to_np
+from .gpu_helpers import (MX_TOL, GpuRun, Inputs, check_weight_grads_16_byte_aligned, rel_fro,
+                          to_np)
 from .test_gpu_layer import check_layer
 
 pytestmark = pytest.mark.gpu
@@ -50,3 +51,7 @@ def test_mx_fc1_output_matches_oracle(lib):
 @pytest.mark.parametrize("name", list(CASES))
 def test_mx_layer_fwd_bwd_matches_oracle(lib, name):
     check_layer(CASES[name], tol=MX_TOL)
+
+
+def test_mx_weight_grads_into_16_byte_aligned_buffers(lib):
+    check_weight_grads_16_byte_aligned(CASES["mx_tails"])

@@ -37,7 +37,9 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxE = 256;
 constexpr int kSfCol = BN;  // first TMEM column of the per-stage scale factors
+constexpr int kPackCol = 320;  // dGLU: the drained accumulator as packed bf16 (128 columns)
 constexpr int kTmemCols = 512;
+static_assert(kSfCol + 12 * STAGES <= kPackCol && kPackCol + BN / 2 <= kTmemCols, "TMEM map");
 
 enum { EPI_STORE = 0, EPI_GLU = 1, EPI_DGLU = 2 };
 
@@ -483,20 +485,29 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
         }
         continue;
       }
-      // drain 128 accumulator columns into registers as packed bf16, then free TMEM
-      uint32_t pk[64];
-      {
-        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + cb;
+      // STORE: drain 128 accumulator columns into registers as packed bf16; dGLU: pack them
+      // into this warp's 64 columns of the TMEM packed area instead (registers stay free for
+      // the dGLU math). Either way the fp32 accumulator is released before any other work.
+      const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + cb;
+      const uint32_t tpk = tmem_base + ((uint32_t)(q * 32) << 16) + kPackCol + half * 64;
+      uint32_t pk[EPI == EPI_STORE ? 64 : 1];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(taddr + 32 * j, r);
-          tmem_ld_wait();
+      for (int j = 0; j < 4; ++j) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tacc + 32 * j, r);
+        tmem_ld_wait();
+        uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[16 * j + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+        if constexpr (EPI == EPI_STORE) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[16 * j + i] = w[i];
+        } else {
+          tmem_st_32x32b_x16(tpk + 16 * j, w);
         }
       }
+      if constexpr (EPI != EPI_STORE) tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.tempty);
@@ -526,14 +537,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
         float dp0 = 0.f, dp1 = 0.f, dp2 = 0.f, dp3 = 0.f;
         uint8_t* qr = p.q_row + (int64_t)row * p.ld_q_row;
         uint8_t* qc = p.q_col + (int64_t)row * p.ld_q_col;
-        // one copy of the chunk body (keeps the kernel inside the instruction cache); the
-        // packed accumulator shifts down by one chunk per iteration, so chunk j is always
-        // pk[0..15] and no register is indexed at run time
+        // one copy of the chunk body (keeps the kernel inside the instruction cache); chunk j
+        // of the packed accumulator comes back from TMEM
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
           const int f0 = t.n0 + cb + 32 * j;
           if (f0 >= p.N) break;
-          const uint32_t* cur = pk;
+          uint32_t cur[16];
+          tmem_ld_32x32b_x16(tpk + 16 * j, cur);
+          tmem_ld_wait();
           const int gcol = kGated ? gate_col(f0, p.ilv) : f0;
           const int lcol = gcol + p.ilv;
           float dg[32], dl[32];
@@ -573,8 +585,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
             const int gn = kGated ? gate_col(f0 + 32, p.ilv) : f0 + 32;
             zst_issue(zst_a, zrow + gn, zrow + gn + p.ilv, lane, kGated);
           }
-#pragma unroll
-          for (int i = 0; i < 48; ++i) pk[i] = pk[i + 16];
           mx_row_block(dg, qr + gcol, p.s_row + sf_mma_offset(row, gcol / 32, p.s_row_pad));
           if constexpr (kGated)
             mx_row_block(dl, qr + lcol, p.s_row + sf_mma_offset(row, lcol / 32, p.s_row_pad));

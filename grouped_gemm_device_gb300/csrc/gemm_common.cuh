@@ -138,6 +138,32 @@ MOE_DEVICE void store_zero_bf16x32(void* dst) {
 }
 
 
+// dGLU: this lane's row of one chunk of saved Z (32 columns of gate and of linear values),
+// copied into the warp's 4 KB shared buffer with cp.async. Pieces 0-3 (16 bytes each) come from src0 (gate columns, or the only half when not
+// gated), pieces 4-7 from src1 (linear columns). Piece c of row r sits at r*128 +
+// ((c ^ (r & 7)) * 16), so 8 rows reading the same piece touch 8 different bank groups.
+MOE_DEVICE void zst_issue(uint32_t buf, const uint16_t* src0, const uint16_t* src1, int lane,
+                          bool two, bool valid = true) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    if (c >= 4 && !two) break;
+    const uint16_t* src = c < 4 ? src0 + 8 * c : src1 + 8 * (c - 4);
+    // an invalid row copies nothing and reads no global memory (zero fill)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                     buf + lane * 128 + ((c ^ (lane & 7)) * 16)),
+                 "l"(valid ? src : src0), "r"(valid ? 16 : 0)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+MOE_DEVICE void zst_piece(const uint8_t* buf, int c, int lane, uint32_t* w) {
+  const uint4 v = *reinterpret_cast<const uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) * 16));
+  w[0] = v.x;
+  w[1] = v.y;
+  w[2] = v.z;
+  w[3] = v.w;
+}
+
 // ------------------------------------------------------------------ tensor maps (host)
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;

@@ -32,14 +32,14 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 128;  // fp8 elements (bytes) per k-block: one 128-byte swizzle row
 constexpr int MMA_K = 32;
-constexpr int STAGES = 3;
+constexpr int kMaxStages = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxE = 256;
 constexpr int kSfCol = BN;  // first TMEM column of the per-stage scale factors
 constexpr int kPackCol = 320;  // dGLU: the drained accumulator as packed bf16 (128 columns)
 constexpr int kTmemCols = 512;
-static_assert(kSfCol + 12 * STAGES <= kPackCol && kPackCol + BN / 2 <= kTmemCols, "TMEM map");
+static_assert(kSfCol + 12 * kMaxStages <= kPackCol && kPackCol + BN / 2 <= kTmemCols, "TMEM map");
 
 enum { EPI_STORE = 0, EPI_GLU = 1, EPI_DGLU = 2 };
 
@@ -82,22 +82,29 @@ constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SFA_BYTES = 512;   // 128 rows x 4 k-blocks
 constexpr int SFB_BYTES = 1024;  // 256 rows x 4 k-blocks
-constexpr int DATA = STAGES * STAGE_BYTES;
-constexpr int SF_OFF = DATA;
 constexpr int XP_LD = 36;  // fp32 row of the per-warp 32 x 32 staging tile (144 B, 16-B aligned)
-constexpr int XPOSE_OFF = SF_OFF + STAGES * (SFA_BYTES + SFB_BYTES);
 constexpr int XPOSE_WARP_BYTES = 32 * XP_LD * 4 + 32 * 4;  // staging tile + 32 column 2^-e
-constexpr int ZST_OFF = XPOSE_OFF + kEpiWarps * XPOSE_WARP_BYTES;
 constexpr int ZST_WARP_BYTES = 32 * 128;  // dGLU: saved Z of one chunk, 32 rows x 64 bf16
-constexpr int CTRL_OFF = ZST_OFF + kEpiWarps * ZST_WARP_BYTES;
-constexpr int SMEM_TOTAL = CTRL_OFF + 4096 + 1024;
-static_assert(SMEM_TOTAL <= 232448, "shared memory above the sm_100 per-block limit");
-static_assert(XPOSE_OFF % 16 == 0 && XPOSE_WARP_BYTES % 16 == 0 && ZST_OFF % 128 == 0 &&
-              CTRL_OFF % 8 == 0, "smem alignment");
+
+// Shared-memory map of one kernel. STORE epilogues need neither the quantisation staging tiles
+// nor the Z buffer, so they get a fourth pipeline stage in that space.
+template <int EPI>
+struct MxSmem {
+  static constexpr int STAGES = EPI == 0 ? 4 : 3;
+  static constexpr int DATA = STAGES * STAGE_BYTES;
+  static constexpr int SF_OFF = DATA;
+  static constexpr int XPOSE_OFF = SF_OFF + STAGES * (SFA_BYTES + SFB_BYTES);
+  static constexpr int ZST_OFF = XPOSE_OFF + (EPI == 0 ? 0 : kEpiWarps * XPOSE_WARP_BYTES);
+  static constexpr int CTRL_OFF = ZST_OFF + (EPI == 2 ? kEpiWarps * ZST_WARP_BYTES : 0);
+  static constexpr int TOTAL = CTRL_OFF + 4096 + 1024;
+  static_assert(TOTAL <= 232448, "shared memory above the sm_100 per-block limit");
+  static_assert(XPOSE_OFF % 16 == 0 && ZST_OFF % 128 == 0 && CTRL_OFF % 8 == 0, "alignment");
+  static_assert(STAGES <= kMaxStages, "TMEM scale columns");
+};
 
 struct Ctrl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull;
   uint64_t tempty;
   uint64_t drain;
@@ -186,31 +193,6 @@ MOE_DEVICE void mx_col_block(const float (&v)[32], float* xp, uint8_t* qdst, uin
   st_global_v8(qdst, w);
 }
 
-// dGLU: this lane's row of one chunk of saved Z, copied into the warp's shared buffer with
-// cp.async. Pieces 0-3 (16 bytes each) come from src0 (gate columns, or the only half when not
-// gated), pieces 4-7 from src1 (linear columns). Piece c of row r sits at r*128 +
-// ((c ^ (r & 7)) * 16), so 8 rows reading the same piece touch 8 different bank groups.
-MOE_DEVICE void zst_issue(uint32_t buf, const uint16_t* src0, const uint16_t* src1, int lane,
-                          bool two) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    if (c >= 4 && !two) break;
-    const uint16_t* src = c < 4 ? src0 + 8 * c : src1 + 8 * (c - 4);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                     buf + lane * 128 + ((c ^ (lane & 7)) * 16)),
-                 "l"(src)
-                 : "memory");
-  }
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-MOE_DEVICE void zst_piece(const uint8_t* buf, int c, int lane, uint32_t* w) {
-  const uint4 v = *reinterpret_cast<const uint4*>(buf + lane * 128 + ((c ^ (lane & 7)) * 16));
-  w[0] = v.x;
-  w[1] = v.y;
-  w[2] = v.z;
-  w[3] = v.w;
-}
-
 // Gate and linear columns of dA column f in the packed Z layout (blocks of ilv gate columns
 // followed by ilv linear columns; ilv a power of two).
 MOE_DEVICE int gate_col(int f, int ilv) { return ((f & ~(ilv - 1)) << 1) | (f & (ilv - 1)); }
@@ -221,10 +203,12 @@ MOE_DEVICE int gate_col(int f, int ilv) { return ((f & ~(ilv - 1)) << 1) | (f & 
 template <int EPI, int KIND, bool KG, int ILV, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __grid_constant__ MxArgs p) {
   constexpr bool kGated = KIND != MOE_ACT_SRELU;
+  using L = MxSmem<EPI>;
+  constexpr int STAGES = L::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  Ctrl& c = *reinterpret_cast<Ctrl*>(smem + CTRL_OFF);
+  Ctrl& c = *reinterpret_cast<Ctrl*>(smem + L::CTRL_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &c.abort;
   const int NT = (p.N + BN - 1) / BN;
@@ -292,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
           if (!mbar_wait(&c.empty[stage], phase ^ 1, abort, p.err)) break;
           uint8_t* sA = smem + stage * STAGE_BYTES;
           uint8_t* sB = sA + A_BYTES;
-          uint8_t* sfA = smem + SF_OFF + stage * (SFA_BYTES + SFB_BYTES);
+          uint8_t* sfA = smem + L::SF_OFF + stage * (SFA_BYTES + SFB_BYTES);
           uint64_t* bar = &c.full[stage];
           mbar_arrive_expect_tx(bar, STAGE_BYTES + SFA_BYTES + SFB_BYTES);
 #pragma unroll
@@ -353,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
           tc_fence_after();
           const uint32_t sA = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t sB = sA + A_BYTES;
-          const uint32_t sfA = smem_u32(smem + SF_OFF + stage * (SFA_BYTES + SFB_BYTES));
+          const uint32_t sfA = smem_u32(smem + L::SF_OFF + stage * (SFA_BYTES + SFB_BYTES));
           const uint32_t sfa_t = tmem_base + kSfCol + stage * 12;
           const uint32_t sfb_t = sfa_t + 4;
           tmem_cp_32x128b_warpx4(sfa_t, smem_desc_noswizzle(sfA, 0, 128));
@@ -394,8 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
     // ------------------------------------------------------------ epilogue warps 2..9
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;  // columns [128*half, 128*half + 128) of the tile
-    float* xp = reinterpret_cast<float*>(smem + XPOSE_OFF + (warp - 2) * XPOSE_WARP_BYTES);
-    const uint8_t* zst = smem + ZST_OFF + (warp - 2) * ZST_WARP_BYTES;
+    float* xp = reinterpret_cast<float*>(smem + L::XPOSE_OFF + (warp - 2) * XPOSE_WARP_BYTES);
+    const uint8_t* zst = smem + L::ZST_OFF + (warp - 2) * ZST_WARP_BYTES;
     const uint32_t zst_a = smem_u32(zst);
     int acc_i = 0;
     for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
@@ -624,11 +608,11 @@ cudaError_t launch_mx(const MxArgs& a, int grid, cudaStream_t s, int kid) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, MxSmem<EPI>::TOTAL);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<grid, kThreads, SMEM_TOTAL, s>>>(a);
+  kern<<<grid, kThreads, MxSmem<EPI>::TOTAL, s>>>(a);
   count_launch(s, kid);
   return cudaGetLastError();
 }

@@ -218,12 +218,16 @@ def traffic_for(kernel: str, workload: str):
     path = os.path.join(ROOT, "profiles", f"gemm_dram_traffic_{workload}.txt")
     if not os.path.exists(path):
         return None
-    src = os.path.join(ROOT, "grouped_gemm_device_gb300", "csrc", "gemm.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     txt = open(path).read()
-    m_sha = re.search(r"gemm\.cu sha256\[:16\]:\s*(\w+)", txt)
+    m_sha = re.search(r"(\w+\.cu) sha256\[:16\]:\s*(\w+)", txt)
     m_b = re.search(rf"^{re.escape(kernel)}\s+[\d.]+\s+[\d.]+\s+(\d+)", txt, re.M)
-    if not m_sha or not m_b or m_sha.group(1) != sha:
+    if not m_sha or not m_b:
+        return None
+    src = os.path.join(ROOT, "grouped_gemm_device_gb300", "csrc", m_sha.group(1))
+    if not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if m_sha.group(2) != sha:
         return None
     return float(m_b.group(1))
 

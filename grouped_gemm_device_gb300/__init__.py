@@ -27,7 +27,7 @@ KERNEL_NAMES = ("route_topk", "assign_rows", "gather_x", "gemm_fc1_fprop", "gemm
 EXPORTS = ("moe_timeline_begin", "moe_timeline_end", "moe_workspace_size", "moe_workspace_layout", "moe_route_permute",
            "moe_grouped_mlp_fwd", "moe_grouped_mlp_bwd", "mxfp8_quantize", "moe_pack_fc1_weight",
            "moe_get_error", "moe_clear_error", "moe_gemm_ctas", "moe_launch_count",
-           "moe_last_error_string")
+           "moe_last_error_string", "moe_selftest_wait_timeout")
 
 
 class LayerDesc(ctypes.Structure):
@@ -82,6 +82,7 @@ def load():
         "moe_timeline_begin": (_I32, [ctypes.POINTER(_P), _I32]),
         "moe_timeline_end": (_I32, [ctypes.POINTER(_I32)]),
         "moe_route_permute_noalloc": (_I32, [_DP, _I32, _P, _P, _P, _P, _P, _P, _P, _I64, _P]),
+        "moe_selftest_wait_timeout": (_I32, [_P, ctypes.c_uint64, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -184,6 +185,12 @@ def mxfp8_quantize(inp, M, N, rowwise, colwise, q_row=None, s_row=None, q_col=No
 def moe_pack_fc1_weight(src, dst, E, H, F, gated, ilv, inverse, stream=None):
     _check(load().moe_pack_fc1_weight(_ptr(src), _ptr(dst), E, H, F, int(gated), ilv,
                                       int(inverse), _stream(stream)))
+
+
+def moe_selftest_wait_timeout(err, limit_ns, stream=None):
+    """Enqueue the bounded-wait self-test: a wait nothing completes gives up after limit_ns
+    and writes the timeout code into the device int32 `err`."""
+    _check(load().moe_selftest_wait_timeout(_ptr(err), int(limit_ns), _stream(stream)))
 
 
 def moe_get_error(desc, ws, stream=None) -> int:

@@ -280,6 +280,20 @@ static void mx_quantize_operands(const void* in, int64_t M, int64_t N, int64_t G
                             std::max(device_sms(), 1), s);
 }
 
+// One thread waits, with the bounded wait every GEMM uses, on an mbarrier that expects one
+// arrival nobody makes; the wait gives up after limit_ns, records MOE_DEVERR_TIMEOUT and the
+// kernel returns normally.
+__global__ void selftest_wait_timeout_kernel(int* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    abort_flag = 0;
+    mbar_wait(&bar, 0, &abort_flag, err, limit_ns);
+  }
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -490,6 +504,16 @@ moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t* d, int32_t T, const voi
   if ((e = launch_grouped_gemm(p, s)) != cudaSuccess) return cuda_fail(e, "FC1 wgrad GEMM");
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "bwd launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_selftest_wait_timeout(int32_t* err, uint64_t limit_ns, moe_stream_t stream) {
+  if (!err) return fail(MOE_ERR_INVALID_ARG, "err is NULL");
+  if (limit_ns < 1000000ull || limit_ns > 10000000000ull)
+    return fail(MOE_ERR_INVALID_ARG, "limit_ns must be in [1 ms, 10 s]");
+  selftest_wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err, limit_ns);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
   return MOE_OK;
 }
 

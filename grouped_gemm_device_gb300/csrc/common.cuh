@@ -132,14 +132,15 @@ MOE_DEVICE bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
 // A wait on a barrier phase that gives up after `limit_ns`, or as soon as another role of
 // the CTA has given up (*abort != 0). On giving up it records MOE_DEVERR_TIMEOUT.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
-MOE_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
+MOE_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
+                          uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       set_error(err, MOE_DEVERR_TIMEOUT);
       return false;

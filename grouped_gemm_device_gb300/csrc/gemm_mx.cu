@@ -82,15 +82,15 @@ constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SFA_BYTES = 512;   // 128 rows x 4 k-blocks
 constexpr int SFB_BYTES = 1024;  // 256 rows x 4 k-blocks
-constexpr int XP_LD = 36;  // fp32 row of the per-warp 32 x 32 staging tile (144 B, 16-B aligned)
-constexpr int XPOSE_WARP_BYTES = 32 * XP_LD * 4 + 32 * 4;  // staging tile + 32 column 2^-e
+constexpr int XP_ROW = 80;  // bytes per row of the per-warp 32 x 32 bf16 staging tile (+16 pad)
+constexpr int XPOSE_WARP_BYTES = 32 * XP_ROW + 32 * 4;  // staging tile + 32 column 2^-e
 constexpr int ZST_WARP_BYTES = 32 * 128;  // dGLU: saved Z of one chunk, 32 rows x 64 bf16
 
-// Shared-memory map of one kernel. STORE epilogues need neither the quantisation staging tiles
-// nor the Z buffer, so they get a fourth pipeline stage in that space.
+// Shared-memory map of one kernel: four pipeline stages, except for the dGLU kernel, whose Z
+// buffer takes the fourth stage's space. STORE kernels have no quantisation staging tiles.
 template <int EPI>
 struct MxSmem {
-  static constexpr int STAGES = EPI == 0 ? 4 : 3;
+  static constexpr int STAGES = EPI == 2 ? 3 : 4;
   static constexpr int DATA = STAGES * STAGE_BYTES;
   static constexpr int SF_OFF = DATA;
   static constexpr int XPOSE_OFF = SF_OFF + STAGES * (SFA_BYTES + SFB_BYTES);
@@ -159,29 +159,47 @@ MOE_DEVICE void mx_row_block(const float (&v)[32], uint8_t* qdst, uint8_t* sdst)
 }
 
 // Column-wise MXFP8 of the warp's 32 rows x 32 columns (this lane holds one row), stored in the
-// natural row-major layout. Lane j takes column j's maximum from the warp's shared-memory tile
-// and publishes 2^-e; every lane then quantises its own row with the 32 column factors and
-// stores one 32-byte run. The tile and the factors are rewritten only after every lane has
-// passed the next call's first warp barrier, so two barriers per call suffice.
-MOE_DEVICE void mx_col_block(const float (&v)[32], float* xp, uint8_t* qdst, uint8_t* sdst,
-                             int lane) {
-  float* xinv = xp + 32 * XP_LD;
-  float4* mine = reinterpret_cast<float4*>(xp + lane * XP_LD);
+// natural row-major layout. A block's exponent depends only on the exponent bits of its
+// maximum |v|, and truncating |v| to bf16 keeps those bits (values small enough to lose them
+// clamp to e = -127 either way), so the column maxima are taken over a bf16 staging tile:
+// lanes j and j + 16 scan column pair j over rows 0-15 and 16-31 with packed 16-bit maxima,
+// one shuffle combines them, lane j publishes 2^-e of column 2j + (j >= 16) and writes its
+// scale byte; every lane then quantises its own fp32 row with the 32 factors and stores one
+// 32-byte run. The tile and the factors are rewritten only after every lane has passed the
+// next call's first warp barrier, so two barriers per call suffice.
+MOE_DEVICE void mx_col_block(const float (&v)[32], uint8_t* xs, uint8_t* qdst, uint8_t* s_col,
+                             int64_t col0, int64_t kb, int64_t s_pad, int lane) {
+  float* xinv = reinterpret_cast<float*>(xs + 32 * XP_ROW);
+  uint4* mine = reinterpret_cast<uint4*>(xs + lane * XP_ROW);
 #pragma unroll
-  for (int k = 0; k < 8; ++k)
-    mine[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-  __syncwarp();
-  float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;
+  for (int k = 0; k < 4; ++k) {
+    uint32_t w[4];
 #pragma unroll
-  for (int i = 0; i < 32; i += 4) {
-    m0 = fmaxf(m0, fabsf(xp[(i + 0) * XP_LD + lane]));
-    m1 = fmaxf(m1, fabsf(xp[(i + 1) * XP_LD + lane]));
-    m2 = fmaxf(m2, fabsf(xp[(i + 2) * XP_LD + lane]));
-    m3 = fmaxf(m3, fabsf(xp[(i + 3) * XP_LD + lane]));
+    for (int i = 0; i < 4; ++i)
+      w[i] = __byte_perm(__float_as_uint(v[8 * k + 2 * i]), __float_as_uint(v[8 * k + 2 * i + 1]),
+                         0x7632) & 0x7FFF7FFFu;
+    mine[k] = make_uint4(w[0], w[1], w[2], w[3]);
   }
-  const int e = mx_block_exponent(fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)));
-  *sdst = (uint8_t)(e + 127);
-  xinv[lane] = mx_inv_scale(e);
+  __syncwarp();
+  const int jp = lane & 15, rh = lane >> 4;
+  const uint8_t* col = xs + rh * 16 * XP_ROW + 4 * jp;
+  uint32_t m0 = 0, m1 = 0;
+#pragma unroll
+  for (int r = 0; r < 16; r += 2) {
+    uint32_t t0, t1;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(t0) : "r"(m0), "r"(*reinterpret_cast<const uint32_t*>(col + r * XP_ROW)));
+    asm("max.u16x2 %0, %1, %2;" : "=r"(t1) : "r"(m1), "r"(*reinterpret_cast<const uint32_t*>(col + (r + 1) * XP_ROW)));
+    m0 = t0;
+    m1 = t1;
+  }
+  uint32_t m;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(m0), "r"(m1));
+  const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, m, 16);
+  asm("max.u16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(other));
+  const int c = 2 * jp + rh;  // this lane's column of the block
+  const int e = mx_block_exponent(__uint_as_float(rh ? (m & 0xFFFF0000u) : (m << 16)));
+  s_col[sf_mma_offset(col0 + c, kb, s_pad)] = (uint8_t)(e + 127);
+  xinv[c] = mx_inv_scale(e);
   __syncwarp();
   uint32_t w[8];
 #pragma unroll
@@ -378,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
     // ------------------------------------------------------------ epilogue warps 2..9
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;  // columns [128*half, 128*half + 128) of the tile
-    float* xp = reinterpret_cast<float*>(smem + L::XPOSE_OFF + (warp - 2) * XPOSE_WARP_BYTES);
+    uint8_t* xs = smem + L::XPOSE_OFF + (warp - 2) * XPOSE_WARP_BYTES;
     const uint8_t* zst = smem + L::ZST_OFF + (warp - 2) * ZST_WARP_BYTES;
     const uint32_t zst_a = smem_u32(zst);
     int acc_i = 0;
@@ -448,8 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
             for (int i = 0; i < 32; ++i)
               v[i] = prob * act_fwd_k<KIND>(p.act, acc[g_off + i], acc[g_off + ILV + i]);
             mx_row_block(v, qr + acol, p.s_row + sf_mma_offset(row, acol / 32, p.s_row_pad));
-            mx_col_block(v, xp, qc + acol,
-                         p.s_col + sf_mma_offset(acol + lane, row0 / 32, p.s_col_pad), lane);
+            mx_col_block(v, xs, qc + acol, p.s_col, acol, row0 / 32, p.s_col_pad, lane);
           }
         } else {
 #pragma unroll
@@ -463,8 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
               v[i] = prob * rr * rr;
             }
             mx_row_block(v, qr + acol, p.s_row + sf_mma_offset(row, acol / 32, p.s_row_pad));
-            mx_col_block(v, xp, qc + acol,
-                         p.s_col + sf_mma_offset(acol + lane, row0 / 32, p.s_col_pad), lane);
+            mx_col_block(v, xs, qc + acol, p.s_col, acol, row0 / 32, p.s_col_pad, lane);
           }
         }
         continue;
@@ -572,11 +588,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
           mx_row_block(dg, qr + gcol, p.s_row + sf_mma_offset(row, gcol / 32, p.s_row_pad));
           if constexpr (kGated)
             mx_row_block(dl, qr + lcol, p.s_row + sf_mma_offset(row, lcol / 32, p.s_row_pad));
-          mx_col_block(dg, xp, qc + gcol,
-                       p.s_col + sf_mma_offset(gcol + lane, row0 / 32, p.s_col_pad), lane);
+          mx_col_block(dg, xs, qc + gcol, p.s_col, gcol, row0 / 32, p.s_col_pad, lane);
           if constexpr (kGated)
-            mx_col_block(dl, xp, qc + lcol,
-                         p.s_col + sf_mma_offset(lcol + lane, row0 / 32, p.s_col_pad), lane);
+            mx_col_block(dl, xs, qc + lcol, p.s_col, lcol, row0 / 32, p.s_col_pad, lane);
         }
         p.dprob_part[(int64_t)row * p.nparts + (t.n0 / BN) * 2 + half] = (dp0 + dp1) + (dp2 + dp3);
       }

@@ -225,6 +225,14 @@ moe_status_t moe_get_error(const moe_layer_desc_t *desc, const void *ws, int32_t
 /* Enqueue a reset of the device error word to MOE_DEVERR_NONE. */
 moe_status_t moe_clear_error(const moe_layer_desc_t *desc, void *ws, moe_stream_t stream);
 
+/* Failure-detection self-test (no counterpart on the pages; it exercises this library's own
+ * bounded waits). Enqueues one kernel whose single barrier wait can never complete: the same
+ * bounded wait the GEMM kernels use gives up after limit_ns nanoseconds (1 ms .. 10 s) and
+ * writes MOE_DEVERR_TIMEOUT into *err (device int32; written only if it holds 0). The kernel
+ * then returns normally, so the context stays usable; no fault, trap or endless loop is
+ * involved. Returns MOE_ERR_INVALID_ARG for a NULL err or a limit outside the range. */
+moe_status_t moe_selftest_wait_timeout(int32_t *err, uint64_t limit_ns, moe_stream_t stream);
+
 /* Number of SMs the persistent GEMM uses on the current device for this description
  * (device SM count minus sm_margin, at least 1). */
 int32_t moe_gemm_ctas(const moe_layer_desc_t *desc);

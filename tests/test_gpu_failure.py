@@ -1,0 +1,45 @@
+"""Failure detection on the GPU without a fault: a bounded barrier wait that can never complete
+gives up after its limit, records the timeout in a device error word and returns; the context
+stays usable for a normal layer step afterwards."""
+import time
+
+import pytest
+import torch
+
+import grouped_gemm_device_gb300 as g
+from grouped_gemm_device_gb300 import synth
+
+from .gpu_helpers import BF16_TOL, GpuRun, Inputs, rel_fro, to_np
+
+pytestmark = pytest.mark.gpu
+
+TIMEOUT = 2  # MOE_DEVERR_TIMEOUT
+
+
+def test_bounded_wait_gives_up_and_reports_timeout(lib):
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    limit_ns = 50_000_000  # 50 ms
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    g.moe_selftest_wait_timeout(err, limit_ns)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert int(err.item()) == TIMEOUT
+    assert elapsed >= limit_ns * 1e-9
+    # sticky: a second expiry keeps the first code, a cleared word records again
+    err.fill_(7)
+    g.moe_selftest_wait_timeout(err, 2_000_000)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 7
+
+
+def test_context_usable_after_a_timeout(lib):
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g.moe_selftest_wait_timeout(err, 5_000_000)
+    cfg = synth.CONFIGS["tiny"]
+    inp = Inputs(cfg)
+    run = GpuRun(inp)
+    assert int(err.item()) == TIMEOUT
+    assert run.layer.device_error() == 0
+    ref = inp.oracle(backward=False)
+    assert rel_fro(to_np(run.y), ref.y) < BF16_TOL

@@ -122,6 +122,12 @@ def test_calls_validate_before_touching_the_device(lib):
         g.moe_pack_fc1_weight(256, 512, 2, 64, 96, 1, 64, 0, 0)
     assert e.value.status == 2
     assert "ilv" in lib.moe_last_error_string().decode()
+    with pytest.raises(g.MoeError) as e:
+        g.moe_selftest_wait_timeout(None, 10**8, 0)
+    assert e.value.status == 1
+    with pytest.raises(g.MoeError) as e:
+        g.moe_selftest_wait_timeout(256, 10**3, 0)
+    assert e.value.status == 1
 
 
 def test_config_table_matches_workloads():

@@ -426,8 +426,11 @@ def main():
             ent["frac_hbm"] = round(kb[k] / (v / 1e3) / 1e9 / p_bw, 3)
         per_kernel[k] = ent
 
-    # end to end through the C ABI with host buffers: pinned H2D of the step's inputs and
-    # D2H of its results inside the timed region
+    # end to end through the C ABI with host buffers: every step copies its inputs from pinned
+    # host memory and its results back, inside the timed region. The copies run on two side
+    # streams ordered by events so they overlap the layer's kernels: the next step's logits
+    # and x load once this step's routing has gathered x, dy loads during the forward, y
+    # returns during the backward, dx and d_probs during the next step.
     e2e = None
     if not args.no_e2e:
         h_logits = torch.from_numpy(hin["logits"]).pin_memory()
@@ -436,26 +439,61 @@ def main():
         h_y = torch.empty(T, cfg.H, dtype=torch.bfloat16).pin_memory()
         h_dx = torch.empty(T, cfg.H, dtype=torch.bfloat16).pin_memory()
         h_dp = torch.empty(T, cfg.k, dtype=torch.float32).pin_memory()
+        main = torch.cuda.current_stream()
+        h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+        ev = {n: torch.cuda.Event() for n in
+              ("in", "routed", "dy", "fwd", "bwd", "y_out", "dx_out", "start")}
+
+        def load_inputs():
+            with torch.cuda.stream(h2d):
+                logits.copy_(h_logits, non_blocking=True)
+                x.copy_(h_x, non_blocking=True)
+                ev["in"].record(h2d)
 
         def e2e_step():
-            logits.copy_(h_logits, non_blocking=True)
-            x.copy_(h_x, non_blocking=True)
-            dy.copy_(h_dy, non_blocking=True)
-            step()
-            h_y.copy_(layer.y[:T], non_blocking=True)
-            h_dx.copy_(layer.dx[:T], non_blocking=True)
-            h_dp.copy_(layer.d_probs[:T], non_blocking=True)
+            main.wait_event(ev["in"])
+            layer.route_permute(logits, x, T)
+            ev["routed"].record(main)
+            with torch.cuda.stream(h2d):
+                h2d.wait_event(ev["bwd"])       # the previous backward has read dy
+                dy.copy_(h_dy, non_blocking=True)
+                ev["dy"].record(h2d)
+            load_inputs()                       # next step's inputs; x and logits are free
+            main.wait_event(ev["y_out"])        # the previous y has left the device
+            layer.forward(w1p, w2, T)
+            ev["fwd"].record(main)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(ev["fwd"])
+                h_y.copy_(layer.y[:T], non_blocking=True)
+                ev["y_out"].record(d2h)
+            main.wait_event(ev["dy"])
+            main.wait_event(ev["dx_out"])       # the previous dx / d_probs have left
+            layer.backward(dy, w1p, w2, T)
+            ev["bwd"].record(main)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(ev["bwd"])
+                h_dx.copy_(layer.dx[:T], non_blocking=True)
+                h_dp.copy_(layer.d_probs[:T], non_blocking=True)
+                ev["dx_out"].record(d2h)
 
-        for _ in range(3):
-            e2e_step()
+        def e2e_run(n):
+            for e in ("bwd", "y_out", "dx_out", "start"):
+                ev[e].record(main)
+            h2d.wait_event(ev["start"])
+            load_inputs()
+            for _ in range(n):
+                e2e_step()
+            main.wait_stream(h2d)
+            main.wait_stream(d2h)
+
+        e2e_run(3)
         torch.cuda.synchronize()
         barrier(world)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         k_e2e = max(10, args.steps // 4)
         e0.record()
-        for _ in range(k_e2e):
-            e2e_step()
+        e2e_run(k_e2e)
         e1.record()
         torch.cuda.synchronize()
         ms_e2e = allreduce_max(e0.elapsed_time(e1) / k_e2e, world)

@@ -399,8 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             float g[32], l[32];
             // the saved-Z loads are issued before the TMEM load so their latencies overlap
             if (row_ok) {
-              load_bf16x32(zrow + gcol, g);
-              load_bf16x32(zrow + lcol, l);
+              load_bf16x32_v8(zrow + gcol, g);
+              load_bf16x32_v8(zrow + lcol, l);
             }
             tmem_ld_32x32b_x32(taddr + cc, r);
             tmem_ld_wait();
@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             store_bf16x32w(dzrow + lcol, l, p.wide);
           } else {
             float zz[32];
-            if (row_ok) load_bf16x32(zrow + f0, zz);
+            if (row_ok) load_bf16x32_v8(zrow + f0, zz);
             tmem_ld_32x32b_x32(taddr + cc, r);
             tmem_ld_wait();
             if (!row_ok) continue;

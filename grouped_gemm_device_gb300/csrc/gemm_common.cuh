@@ -131,6 +131,22 @@ MOE_DEVICE void load_bf16x32(const void* src, float (&v)[32]) {
     v[8 * i + 6] = bf16_lo(w.w); v[8 * i + 7] = bf16_hi(w.w);
   }
 }
+// 32 bf16 at a 32-byte aligned address in two 256-bit loads, unpacked to fp32.
+MOE_DEVICE void load_bf16x32_v8(const void* src, float (&v)[32]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t w[8];
+    asm volatile("ld.global.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                   "=r"(w[6]), "=r"(w[7])
+                 : "l"(static_cast<const uint8_t*>(src) + 32 * h));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[16 * h + 2 * i] = bf16_lo(w[i]);
+      v[16 * h + 2 * i + 1] = bf16_hi(w[i]);
+    }
+  }
+}
 MOE_DEVICE void store_zero_bf16x32(void* dst) {
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll

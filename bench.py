@@ -124,15 +124,27 @@ def load_peaks():
 
 
 # ------------------------------------------------------------------------- distributed
-def dist_setup(args):
+def dist_backend() -> str:
+    """nccl for GPU replicas; gloo where no GPU is visible (the host-side path is tested that
+    way). MOE_DIST_BACKEND overrides."""
+    import torch
+    return os.environ.get("MOE_DIST_BACKEND") or ("nccl" if torch.cuda.is_available() else "gloo")
+
+
+def dist_setup(args=None):
+    """Join the process group torchrun describes (WORLD_SIZE, RANK, LOCAL_RANK, MASTER_*);
+    one process per GPU, each an independent replica of the layer."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        backend = dist_backend()
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        if not dist.is_initialized():
+            dist.init_process_group(backend)
     return ws, rank, local
 
 
@@ -143,13 +155,21 @@ def barrier(ws):
 
 
 def allreduce_max(v: float, ws: int) -> float:
+    """The slowest rank's value: the job's step time is the max over replicas."""
     if ws == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank: float, ms_max: float, world: int) -> float:
+    """Weak scaling: every rank processes the same units; the job's rate is all ranks' units
+    over the slowest rank's time."""
+    return units_per_rank * world / (ms_max / 1e3)
 
 
 # ------------------------------------------------------------------------- clocks
@@ -384,7 +404,7 @@ def main():
     assert layer.device_error() == 0, "device error during timing"
 
     flops = cfg.flops_fwd_bwd()
-    value = flops * world / (ms_max / 1e3) / 1e12
+    value = job_throughput(flops, ms_max, world) / 1e12
     peaks, peak_src = load_peaks()
 
     # per-kernel durations from the launch timeline; repeated kernels of one step (the four
@@ -499,7 +519,7 @@ def main():
         ms_e2e = allreduce_max(e0.elapsed_time(e1) / k_e2e, world)
         bi = h_logits.numel() * 4 + h_x.numel() * 2 + h_dy.numel() * 2
         bo = h_y.numel() * 2 + h_dx.numel() * 2 + h_dp.numel() * 4
-        e2e = {"value": flops * world / (ms_e2e / 1e3) / 1e12, "unit": "TFLOPS",
+        e2e = {"value": job_throughput(flops, ms_e2e, world) / 1e12, "unit": "TFLOPS",
                "ms_per_step": ms_e2e, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                "tokens_per_s": T * world / (ms_e2e / 1e3)}
 

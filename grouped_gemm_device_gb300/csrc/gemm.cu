@@ -127,6 +127,25 @@ MOE_DEVICE void decode_tile(int tile, const GemmArgs& p, const Ctrl& c, int MT, 
   }
 }
 
+// dGLU: the saved Z (packed bf16) of dA columns f0 .. f0+15 of one row: the gate columns into
+// g and, when gated, the linear columns into l (one 256-bit load each).
+MOE_DEVICE void z_load16(const GemmArgs& p, const uint16_t* zrow, int f0, uint32_t (&g)[8],
+                         uint32_t (&l)[8]) {
+  const int gcol = p.gated ? (f0 / p.ilv) * 2 * p.ilv + (f0 % p.ilv) : f0;
+  ld_v8_noalloc(zrow + gcol, g);
+  if (p.gated) ld_v8_noalloc(zrow + gcol + p.ilv, l);
+}
+// 16 bf16 (8 packed words) at dst: one 256-bit store when 32-byte aligned.
+MOE_DEVICE void st_bf16x16(void* dst, const uint32_t (&w)[8], bool wide) {
+  if (wide) {
+    st_global_v8(dst, w);
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
 template <int BN, int STAGES, bool A_MN, bool B_MN, int EPI, bool KG, bool B3D>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
@@ -322,6 +341,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
+      // dGLU: the saved Z of the first two 16-column steps is requested while the MMAs run
+      const uint16_t* zrow = p.z + (int64_t)row * p.ldz;
+      uint32_t z0g[8], z0l[8], z1g[8], z1l[8], z2g[8], z2l[8];
+      if constexpr (EPI == EPI_DGLU) {
+        if (row_ok && t.n0 + c0 < p.N) z_load16(p, zrow, t.n0 + c0, z0g, z0l);
+        if (row_ok && t.n0 + c0 + 16 < p.N) z_load16(p, zrow, t.n0 + c0 + 16, z1g, z1l);
+      }
       const int acc = acc_i & 1;
       const uint32_t acc_phase = (acc_i >> 1) & 1;
       if (!mbar_wait(&c.tfull[acc], acc_phase, abort, p.err)) break;
@@ -386,45 +412,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {  // EPI_DGLU: accumulator = dA_s over F columns
+        // 16-column steps with the saved Z of the next two steps already requested (8 + 8
+        // packed words each), so its load latency overlaps two steps of dGLU math
         const float prob = row_ok ? p.row_prob[row] : 0.f;
         float dp = 0.f;
-        const uint16_t* zrow = p.z + (int64_t)row * p.ldz;
         uint16_t* dzrow = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo;
-        for (int cc = c0; cc < c1; cc += 32) {
+        // the accumulator columns of the next step are loaded from TMEM while this one computes
+        uint32_t das[16], nxt[16];
+        tmem_ld_32x32b_x16(taddr + c0, das);
+        tmem_ld_wait();
+#pragma unroll 1
+        for (int cc = c0; cc < c1; cc += 16) {
           const int f0 = t.n0 + cc;
           if (f0 >= p.N) break;
-          if (p.gated) {
-            const int gcol = (f0 / p.ilv) * 2 * p.ilv + (f0 % p.ilv);
-            const int lcol = gcol + p.ilv;
-            float g[32], l[32];
-            // the saved-Z loads are issued before the TMEM load so their latencies overlap
-            if (row_ok) {
-              load_bf16x32_v8(zrow + gcol, g);
-              load_bf16x32_v8(zrow + lcol, l);
-            }
-            tmem_ld_32x32b_x32(taddr + cc, r);
-            tmem_ld_wait();
-            if (!row_ok) continue;
-            float das[32];
+          const bool more = cc + 16 < c1 && f0 + 16 < p.N;
+          if (more) tmem_ld_32x32b_x16(taddr + cc + 16, nxt);
+          if (row_ok && cc + 32 < c1 && f0 + 32 < p.N) z_load16(p, zrow, f0 + 32, z2g, z2l);
+          if (row_ok) {
+            const int gcol = p.gated ? (f0 / p.ilv) * 2 * p.ilv + (f0 % p.ilv) : f0;
+            uint32_t dgw[8], dlw[8];
+            if (p.gated) {
+              dp += glu_bwd16(p.act, prob, das, z0g, z0l, dgw, dlw);
+              st_bf16x16(dzrow + gcol, dgw, p.wide);
+              st_bf16x16(dzrow + gcol + p.ilv, dlw, p.wide);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) das[i] = __uint_as_float(r[i]);
-            dp += glu_bwd32(p.act, prob, das, g, l);
-            store_bf16x32w(dzrow + gcol, g, p.wide);
-            store_bf16x32w(dzrow + lcol, l, p.wide);
-          } else {
-            float zz[32];
-            if (row_ok) load_bf16x32_v8(zrow + f0, zz);
-            tmem_ld_32x32b_x32(taddr + cc, r);
-            tmem_ld_wait();
-            if (!row_ok) continue;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float das = __uint_as_float(r[i]);
-              const float rr = fmaxf(zz[i], 0.f);
-              dp += das * rr * rr;
-              zz[i] = prob * das * 2.f * rr;
+              for (int i = 0; i < 8; ++i) {
+                const float d0 = __uint_as_float(das[2 * i]), d1 = __uint_as_float(das[2 * i + 1]);
+                const float r0 = fmaxf(bf16_lo(z0g[i]), 0.f), r1 = fmaxf(bf16_hi(z0g[i]), 0.f);
+                dp += d0 * r0 * r0 + d1 * r1 * r1;
+                dgw[i] = pack_bf16x2(prob * d0 * 2.f * r0, prob * d1 * 2.f * r1);
+              }
+              st_bf16x16(dzrow + f0, dgw, p.wide);
             }
-            store_bf16x32w(dzrow + f0, zz, p.wide);
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            z0g[i] = z1g[i]; z0l[i] = z1l[i];
+            z1g[i] = z2g[i]; z1l[i] = z2l[i];
+          }
+          if (more) {
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) das[i] = nxt[i];
           }
         }
         if (row_ok) p.dprob_part[(int64_t)row * p.nparts + (t.n0 / BN) * 2 + half] = dp;

@@ -100,6 +100,42 @@ MOE_DEVICE float glu_bwd32(const ActDev& a, float prob, const float (&das)[32], 
   return glu_bwd32_k<MOE_ACT_SWIGLU>(a, prob, das, g, l);
 }
 
+// 16-wide form of glu_bwd32 (packed bf16 inputs): g/l words hold the saved gate and linear
+// values, das the upstream gradient; writes the packed bf16 d_gate / d_linear words and
+// returns sum_i das[i] * a[i].
+template <int KIND>
+MOE_DEVICE float glu_bwd16_k(const ActDev& a, float prob, const uint32_t (&das)[16],
+                             const uint32_t (&gw)[8], const uint32_t (&lw)[8], uint32_t (&dgw)[8],
+                             uint32_t (&dlw)[8]) {
+  float dp = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float dg0, dl0, dg1, dl1;
+    const float d0 = __uint_as_float(das[2 * i]), d1 = __uint_as_float(das[2 * i + 1]);
+    const float a0 = act_bwd_k<KIND>(a, bf16_lo(gw[i]), bf16_lo(lw[i]), prob * d0, dg0, dl0);
+    const float a1 = act_bwd_k<KIND>(a, bf16_hi(gw[i]), bf16_hi(lw[i]), prob * d1, dg1, dl1);
+    dp += d0 * a0 + d1 * a1;
+    dgw[i] = pack_bf16x2(dg0, dg1);
+    dlw[i] = pack_bf16x2(dl0, dl1);
+  }
+  return dp;
+}
+MOE_DEVICE float glu_bwd16(const ActDev& a, float prob, const uint32_t (&das)[16],
+                           const uint32_t (&gw)[8], const uint32_t (&lw)[8], uint32_t (&dgw)[8],
+                           uint32_t (&dlw)[8]) {
+  if (a.kind == MOE_ACT_CLAMPED_SWIGLU)
+    return glu_bwd16_k<MOE_ACT_CLAMPED_SWIGLU>(a, prob, das, gw, lw, dgw, dlw);
+  if (a.kind == MOE_ACT_GEGLU) return glu_bwd16_k<MOE_ACT_GEGLU>(a, prob, das, gw, lw, dgw, dlw);
+  return glu_bwd16_k<MOE_ACT_SWIGLU>(a, prob, das, gw, lw, dgw, dlw);
+}
+// 32 bytes at a 32-byte aligned global address, not allocated in L1.
+MOE_DEVICE void ld_v8_noalloc(const void* src, uint32_t (&w)[8]) {
+  asm volatile("ld.global.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                 "=r"(w[6]), "=r"(w[7])
+               : "l"(src));
+}
+
 MOE_DEVICE void store_bf16x32(void* dst, const float (&v)[32]) {
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll

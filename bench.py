@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--sm-margin", type=int, default=0)
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling runs)")
     ap.add_argument("--experts", type=int, default=0, help="override E (profiling runs)")
+    ap.add_argument("--recompute", action="store_true",
+                    help="keep no FC1 output; the FC2-dgrad kernel recomputes it (BF16)")
     return ap.parse_args()
 
 
@@ -69,12 +71,15 @@ def workload_name(cfg) -> str:
             f"{cfg.activation} {cfg.precision}")
 
 
-def gemm_flops(cfg):
+def gemm_flops(cfg, recompute=False):
+    """Executed flops per GEMM launch (with recomputation the FC2-dgrad kernel also rebuilds
+    the FC1 output); the step metric counts the model's flops only."""
     R = cfg.R
     H, F, N1 = cfg.H, cfg.F, cfg.N1
     return {
         "gemm_fc1_fprop": 2.0 * R * H * N1, "gemm_fc2_fprop": 2.0 * R * F * H,
-        "gemm_fc2_dgrad": 2.0 * R * H * F, "gemm_fc2_wgrad": 2.0 * R * F * H,
+        "gemm_fc2_dgrad": 2.0 * R * H * F + (2.0 * R * H * N1 if recompute else 0.0),
+        "gemm_fc2_wgrad": 2.0 * R * F * H,
         "gemm_fc1_dgrad": 2.0 * R * N1 * H, "gemm_fc1_wgrad": 2.0 * R * H * N1,
     }
 
@@ -82,9 +87,10 @@ def gemm_flops(cfg):
 QUANT_NAMES = ("mxfp8_quant_x", "mxfp8_quant_w1", "mxfp8_quant_w2", "mxfp8_quant_dy")
 
 
-def kernel_bytes(cfg):
+def kernel_bytes(cfg, recompute=False):
     """Algorithmic HBM bytes per launch: each operand read once, each result written once
-    (R = routed rows; MXFP8 data is 1 byte plus one scale byte per 32)."""
+    (R = routed rows; MXFP8 data is 1 byte plus one scale byte per 32). With recomputation the
+    FC1 kernel writes no Z and the FC2-dgrad kernel reads X and W1 instead of Z."""
     R, T, E = cfg.R, cfg.T, cfg.E
     H, F, N1 = cfg.H, cfg.F, cfg.N1
     R_cap = cfg.R_cap
@@ -102,10 +108,16 @@ def kernel_bytes(cfg):
             "mxfp8_quant_x": R_cap * H * (2 + 2 * s), "mxfp8_quant_dy": R_cap * H * (2 + 2 * s),
             "mxfp8_quant_w1": E * N1 * H * (2 + 2 * s), "mxfp8_quant_w2": E * F * H * (2 + 2 * s),
         }
+    if recompute:
+        fc1 = (R * H + E * N1 * H + R * F) * 2
+        dgrad = (R * H + E * F * H + R * H + E * N1 * H + R * N1) * 2
+    else:
+        fc1 = (R * H + E * N1 * H + R * N1 + R * F) * 2
+        dgrad = (R * H + E * F * H + 2 * R * N1) * 2
     return {
-        "gemm_fc1_fprop": (R * H + E * N1 * H + R * N1 + R * F) * 2,
+        "gemm_fc1_fprop": fc1,
         "gemm_fc2_fprop": (R * F + E * F * H + R * H) * 2,
-        "gemm_fc2_dgrad": (R * H + E * F * H + 2 * R * N1) * 2,
+        "gemm_fc2_dgrad": dgrad,
         "gemm_fc2_wgrad": (R * F + R * H + E * F * H) * 2,
         "gemm_fc1_dgrad": (R * N1 + E * N1 * H + R * H) * 2,
         "gemm_fc1_wgrad": (R * N1 + R * H + E * N1 * H) * 2,
@@ -355,7 +367,7 @@ def main():
     def bf(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
 
-    desc = g.desc_from_config(cfg, sm_margin=args.sm_margin)
+    desc = g.desc_from_config(cfg, sm_margin=args.sm_margin, recompute=args.recompute)
     layer = g.MoELayer(desc, dev)
     w1_log = torch.stack([bf(w) for w in hin["w1"]]).to(dev)
     w1p = g.pack_w1(w1_log, gated=cfg.gated, ilv=cfg.ilv)
@@ -418,8 +430,8 @@ def main():
         seen[name] = j + 1
         per.setdefault(name if name != "mxfp8_quantize" else QUANT_NAMES[j], []).append(dur)
     kernel_ms = {k: sum(v) / len(v) for k, v in per.items()}
-    gf = gemm_flops(cfg)
-    kb = kernel_bytes(cfg)
+    gf = gemm_flops(cfg, args.recompute)
+    kb = kernel_bytes(cfg, args.recompute)
     # the GEMMs are timed inside a long step: sustained tensor peak; fp8 = 2x bf16 (nominal)
     p_tc = peaks.get("bf16_tflops_sustained", 1700.0) * (2.0 if mx else 1.0)
     p_bw = peaks.get("hbm_gbs", 6800.0)
@@ -543,7 +555,8 @@ def main():
             "config": {"workload": workload_name(cfg), "parallelism": f"replicas x{world}",
                        "l2": f"no flush: each step streams {w_bytes / 1e9:.1f} GB of bf16 "
                              "weights and weight gradients, > 129 MB L2",
-                       "sm_margin": args.sm_margin, "flops_per_step": flops},
+                       "sm_margin": args.sm_margin, "flops_per_step": flops,
+                       "recompute": bool(args.recompute), "workspace_bytes": layer.ws_bytes},
             "tokens_per_s": cfg.T * world / (ms_max / 1e3),
             "pct_tensor_peak": {"value": 100 * value / world / p_tc, "peak_tflops": p_tc,
                                 "peak_kind": tc_kind},

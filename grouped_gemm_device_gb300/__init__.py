@@ -36,7 +36,8 @@ class LayerDesc(ctypes.Structure):
                 ("activation", ctypes.c_int32), ("beta", ctypes.c_float),
                 ("gate_max", ctypes.c_float), ("lin_lo", ctypes.c_float),
                 ("lin_hi", ctypes.c_float), ("lin_offset", ctypes.c_float),
-                ("sm_margin", ctypes.c_int32), ("ilv", ctypes.c_int32), ("align", ctypes.c_int32)]
+                ("sm_margin", ctypes.c_int32), ("ilv", ctypes.c_int32), ("align", ctypes.c_int32),
+                ("recompute", ctypes.c_int32)]
 
 
 class WsLayout(ctypes.Structure):
@@ -122,15 +123,15 @@ def _stream(stream) -> int | None:
 
 def make_desc(E, k, H, F, T_max, precision="bf16", activation="swiglu", beta=1.0,
               gate_max=math.inf, lin_lo=-math.inf, lin_hi=math.inf, lin_offset=0.0,
-              sm_margin=0, ilv=64, align=32) -> LayerDesc:
+              sm_margin=0, ilv=64, align=32, recompute=False) -> LayerDesc:
     return LayerDesc(E, k, H, F, T_max, PREC[precision], ACT[activation], beta, gate_max,
-                     lin_lo, lin_hi, lin_offset, sm_margin, ilv, align)
+                     lin_lo, lin_hi, lin_offset, sm_margin, ilv, align, int(recompute))
 
 
-def desc_from_config(cfg, T_max=None, sm_margin=0) -> LayerDesc:
+def desc_from_config(cfg, T_max=None, sm_margin=0, recompute=False) -> LayerDesc:
     return make_desc(cfg.E, cfg.k, cfg.H, cfg.F, cfg.T if T_max is None else T_max,
                      cfg.precision, cfg.activation, cfg.beta, cfg.gate_max, cfg.lin_lo,
-                     cfg.lin_hi, cfg.lin_offset, sm_margin, cfg.ilv, cfg.align)
+                     cfg.lin_hi, cfg.lin_offset, sm_margin, cfg.ilv, cfg.align, recompute)
 
 
 # ------------------------------------------------------------------ C ABI, same names

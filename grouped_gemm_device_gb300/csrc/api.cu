@@ -93,6 +93,10 @@ static moe_status_t validate_desc(const moe_layer_desc_t* d) {
     if (d->F % d->ilv) return fail(MOE_ERR_UNSUPPORTED, "F must be a multiple of ilv");
   }
   if (d->sm_margin < 0) return fail(MOE_ERR_INVALID_ARG, "sm_margin must be >= 0");
+  if (d->recompute != 0 && d->recompute != 1)
+    return fail(MOE_ERR_INVALID_ARG, "recompute must be 0 or 1");
+  if (d->recompute && (d->precision != MOE_PREC_BF16 || d->activation == MOE_ACT_SRELU))
+    return fail(MOE_ERR_UNSUPPORTED, "recompute needs a BF16 layer with a gated activation");
   if (r_cap(d) > (int64_t)INT32_MAX / 2) return fail(MOE_ERR_UNSUPPORTED, "row capacity too large");
   if (d->precision == MOE_PREC_MXFP8 &&
       (int64_t)d->E * round128(n1_of(d)) * d->H > (int64_t)INT32_MAX * 8)
@@ -152,7 +156,8 @@ static void compute_layout(const moe_layer_desc_t* d, moe_ws_layout_t* L) {
   const int64_t R = r_cap(d);
   const int64_t H = d->H, F = d->F, N1 = n1_of(d), E = d->E;
   const bool mx = d->precision == MOE_PREC_MXFP8;
-  const int64_t nparts = mx ? dprob_parts_mx((int)F) : dprob_parts((int)F);
+  const int64_t nparts = mx ? dprob_parts_mx((int)F)
+                            : (d->recompute ? dprob_parts_recompute((int)F) : dprob_parts((int)F));
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -166,7 +171,7 @@ static void compute_layout(const moe_layer_desc_t* d, moe_ws_layout_t* L) {
   L->src_of = take(R * 4);
   L->row_prob = take(R * 4);
   L->x_perm = take(R * H * 2);
-  L->z = take(R * N1 * 2);
+  L->z = d->recompute ? SIZE_MAX : take(R * N1 * 2);
   // bf16 a_s and dz exist only in the BF16 path (MXFP8 keeps them as MXFP8 copies)
   L->a_s = mx ? SIZE_MAX : take(R * F * 2);
   L->y_perm = take(R * H * 2);
@@ -229,7 +234,7 @@ static GemmProblem base_problem(const moe_layer_desc_t* d, const Ws& w) {
   p.row_prob = w.at<float>(w.L.row_prob);
   p.x_perm = w.at<void>(w.L.x_perm);
   p.a_s = w.L.a_s == SIZE_MAX ? nullptr : w.at<void>(w.L.a_s);
-  p.z = w.at<void>(w.L.z);
+  p.z = w.L.z == SIZE_MAX ? nullptr : w.at<void>(w.L.z);
   p.dz = w.L.dz == SIZE_MAX ? nullptr : w.at<void>(w.L.dz);
   p.dy_perm = w.at<void>(w.L.dy_perm);
   p.gated = d->activation != MOE_ACT_SRELU;
@@ -263,7 +268,7 @@ static MxProblem mx_problem(const moe_layer_desc_t* d, const Ws& w) {
   p.x = m.x; p.xt = m.xt; p.a = m.a; p.at = m.at; p.dy = m.dy; p.dyt = m.dyt;
   p.dz = m.dz; p.dzt = m.dzt; p.w1 = m.w1; p.w1t = m.w1t; p.w2 = m.w2; p.w2t = m.w2t;
   p.row_prob = w.at<float>(w.L.row_prob);
-  p.z = w.at<void>(w.L.z);
+  p.z = w.L.z == SIZE_MAX ? nullptr : w.at<void>(w.L.z);
   p.gated = d->activation != MOE_ACT_SRELU;
   p.ilv = d->ilv;
   p.act = act_of(d);
@@ -397,7 +402,7 @@ moe_status_t moe_grouped_mlp_fwd(const moe_layer_desc_t* d, int32_t T, const voi
   p.w2 = w2;
   // FC1 + activation + probability scale (kernel family 2)
   p.role = ROLE_FC1_FPROP;
-  p.out = w.at<void>(w.L.z);
+  p.out = d->recompute ? nullptr : w.at<void>(w.L.z);  // NULL: Z is not kept
   p.out2 = w.at<void>(w.L.a_s);
   if ((e = launch_grouped_gemm(p, s)) != cudaSuccess) return cuda_fail(e, "FC1 grouped GEMM");
   // FC2 (kernel family 1)
@@ -473,13 +478,19 @@ moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t* d, int32_t T, const voi
     if (e != cudaSuccess) return cuda_fail(e, "bwd launch");
     return MOE_OK;
   }
-  // FC2 dgrad + dActivation (kernel family 3)
+  // FC2 dgrad + dActivation (kernel family 3); with recomputation the same kernel rebuilds Z
   p.role = ROLE_FC2_DGRAD;
   p.out = w.at<void>(w.L.dz);
   p.dprob_part = w.at<float>(w.L.dprob_part);
-  if ((e = launch_grouped_gemm(p, s)) != cudaSuccess) return cuda_fail(e, "FC2 dgrad GEMM");
+  if (d->recompute) {
+    p.w1p = w1_packed;
+    if ((e = launch_fc2_dgrad_recompute(p, s)) != cudaSuccess)
+      return cuda_fail(e, "FC2 dgrad recompute GEMM");
+  } else if ((e = launch_grouped_gemm(p, s)) != cudaSuccess) {
+    return cuda_fail(e, "FC2 dgrad GEMM");
+  }
   if (T > 0) {
-    const int nparts = dprob_parts(d->F);
+    const int nparts = d->recompute ? dprob_parts_recompute(d->F) : dprob_parts(d->F);
     const int n = T * d->k;
     dprob_reduce_kernel<<<grid_for((n + 255) / 256, 4), 256, 0, s>>>(
         w.at<float>(w.L.dprob_part), nparts, row_of, n, d_probs);

@@ -388,8 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             glu_fwd32(p.act, prob, g, l, v);
             if (row_ok) {
-              store_bf16x32w(zrow + t.n0 + gcol, g, p.wide);
-              store_bf16x32w(zrow + t.n0 + lcol, l, p.wide);
+              if (p.out) {  // the saved Z (absent when the backward recomputes it)
+                store_bf16x32w(zrow + t.n0 + gcol, g, p.wide);
+                store_bf16x32w(zrow + t.n0 + lcol, l, p.wide);
+              }
               store_bf16x32w(arow + t.n0 / 2 + cc, v, p.wide);
             }
           }

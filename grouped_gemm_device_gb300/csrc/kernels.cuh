@@ -81,6 +81,9 @@ struct GemmProblem {
 };
 
 int gemm_bn(int role);
+// gemm_rc.cu: FC2 dgrad + dGLU with the FC1 output recomputed in the same kernel (BF16)
+int dprob_parts_recompute(int F);
+cudaError_t launch_fc2_dgrad_recompute(const GemmProblem& p, cudaStream_t s);
 int dprob_parts(int F);  // partial d_prob columns per row written by the FC2 dgrad epilogue
 cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s);
 

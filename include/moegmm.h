@@ -92,6 +92,9 @@ typedef struct {
   int32_t sm_margin;  /* SMs left free for concurrent kernels ([NV-blog] cluster margin) */
   int32_t ilv;        /* gate/linear interleave block of the packed W1 (32, 64 or 128)   */
   int32_t align;      /* expert segment alignment in rows; must be 32                    */
+  int32_t recompute;  /* 1: keep no FC1 output between forward and backward; the FC2-dgrad
+                         kernel recomputes it ([NV-blog] "What's next": activation
+                         recomputation). BF16 gated activations only; 0 otherwise          */
 } moe_layer_desc_t;
 
 /* Byte offsets (from ws) of the intermediates that live in the workspace, for inspection
@@ -108,7 +111,8 @@ typedef struct {
   size_t src_of;         /* int32 [R_cap] t*k+j of a row, -1 for padding                 */
   size_t row_prob;       /* fp32 [R_cap] routing probability of a row, 0 for padding     */
   size_t x_perm;         /* bf16 [R_cap, H] gathered tokens                              */
-  size_t z;              /* bf16 [R_cap, N1] FC1 output saved for backward (packed cols) */
+  size_t z;              /* bf16 [R_cap, N1] FC1 output saved for backward (packed cols);
+                            SIZE_MAX when the layer recomputes it                        */
   size_t a_s;            /* bf16 [R_cap, F] p * act(z), the FC2 input                    */
   size_t y_perm;         /* bf16 [R_cap, H] FC2 output before combine (shared with dx_perm) */
   size_t dy_perm;        /* bf16 [R_cap, H] gathered upstream gradient                   */

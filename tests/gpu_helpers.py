@@ -58,10 +58,10 @@ class Inputs:
 class GpuRun:
     """Runs route -> fwd -> bwd for the inputs on cuda and keeps the results."""
 
-    def __init__(self, inp: Inputs, T_max=None, sm_margin=0, backward=True):
+    def __init__(self, inp: Inputs, T_max=None, sm_margin=0, backward=True, recompute=False):
         cfg = inp.cfg
         self.cfg = cfg
-        self.desc = g.desc_from_config(cfg, T_max=T_max, sm_margin=sm_margin)
+        self.desc = g.desc_from_config(cfg, T_max=T_max, sm_margin=sm_margin, recompute=recompute)
         self.layer = g.MoELayer(self.desc)
         self.w1p = g.pack_w1(bf16_dev(inp.w1), gated=cfg.gated, ilv=cfg.ilv)
         self.w2 = bf16_dev(inp.w2)

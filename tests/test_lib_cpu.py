@@ -42,8 +42,8 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_desc_struct_layout_matches_header(lib):
-    # 15 four-byte fields, no padding
-    assert ctypes.sizeof(g.LayerDesc) == 60
+    # 16 four-byte fields, no padding
+    assert ctypes.sizeof(g.LayerDesc) == 64
     assert ctypes.sizeof(g.WsLayout) == 16 * 8
 
 
@@ -70,11 +70,22 @@ def test_workspace_layout_is_consistent(lib):
     assert L.total >= L.dprob_part + R * 2 * 4
 
 
+def test_recompute_keeps_no_z_in_the_workspace(lib):
+    keep, rc = _desc(), _desc(recompute=True)
+    Lk, Lr = g.moe_workspace_layout(keep), g.moe_workspace_layout(rc)
+    assert Lr.z == 2 ** 64 - 1  # SIZE_MAX: no saved FC1 output
+    # the saved Z is R_cap x N1 bf16; the recomputing d_prob partials use 128-column tiles
+    saved = Lk.R_cap * 1024 * 2
+    assert Lk.total - Lr.total >= saved - Lk.R_cap * 8 * 4 - 4096
+
+
 @pytest.mark.parametrize("kw,status", [
     (dict(E=0), 1), (dict(E=300), 1), (dict(k=0), 1), (dict(k=9, E=16), 1), (dict(k=5, E=4), 1),
     (dict(H=100), 2), (dict(F=96), 2), (dict(align=16), 2), (dict(ilv=48), 2),
     (dict(F=64 * 3, ilv=128), 2), (dict(sm_margin=-1), 1),
     (dict(precision="mxfp8"), 2), (dict(precision="mxfp8", align=128, ilv=128), 2),
+    (dict(recompute=2), 1), (dict(recompute=1, precision="mxfp8", align=128), 2),
+    (dict(recompute=1, activation="srelu"), 2),
 ])
 def test_invalid_descriptions_rejected(lib, kw, status):
     d = _desc(**kw)

@@ -51,6 +51,10 @@ def parse():
     ap.add_argument("--sm-margin", type=int, default=0)
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling runs)")
     ap.add_argument("--experts", type=int, default=0, help="override E (profiling runs)")
+    ap.add_argument("--overlap-sweep", default="",
+                    help="comma-separated SM margins: time the layer step, a concurrent "
+                         "memory-bound job (device copies on another stream) and both "
+                         "together at each margin; prints one JSON line")
     ap.add_argument("--recompute", action="store_true",
                     help="keep no FC1 output; the FC2-dgrad kernel recomputes it (BF16)")
     return ap.parse_args()
@@ -341,8 +345,93 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------------- our arm
+def overlap_sweep(args):
+    """[NV-blog] 'configurable SM margin': the persistent GEMMs leave `margin` SMs to other
+    kernels. For each margin, time K layer steps alone, a memory-bound job alone (repeated
+    1 GiB device copies on a second stream), and both started together; 'hidden' is the share
+    of the job's own time that the overlap removed."""
+    import torch
+
+    import grouped_gemm_device_gb300 as g
+    from grouped_gemm_device_gb300 import build as gbuild
+
+    gbuild.build()
+    g.load()
+    cfg = config_of(args)
+    margins = [int(m) for m in args.overlap_sweep.split(",") if m.strip()]
+    hin = host_inputs(cfg)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    dev = torch.device("cuda", 0)
+    w1_log = torch.stack([bf(w) for w in hin["w1"]]).to(dev)
+    w1p = g.pack_w1(w1_log, gated=cfg.gated, ilv=cfg.ilv)
+    del w1_log
+    w2 = torch.stack([bf(w) for w in hin["w2"]]).to(dev)
+    logits = torch.from_numpy(hin["logits"]).to(dev)
+    x = bf(hin["x"]).to(dev)
+    dy = bf(hin["dy"]).to(dev)
+    # the concurrent job: a 1 GiB device-to-device copy (short-lived blocks, like the
+    # communication kernels the margin is meant for)
+    src = torch.empty(1 << 30, dtype=torch.uint8, device=dev).fill_(1)
+    dst = torch.empty_like(src)
+    side = torch.cuda.Stream()
+    main_s = torch.cuda.current_stream()
+    steps = max(3, args.steps)
+
+    def timed(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        fn()
+        main_s.wait_stream(side)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    out = []
+    for m in margins:
+        layer = g.MoELayer(g.desc_from_config(cfg, sm_margin=m), dev)
+
+        def layer_steps():
+            for _ in range(steps):
+                layer.route_permute(logits, x, cfg.T)
+                layer.forward(w1p, w2, cfg.T)
+                layer.backward(dy, w1p, w2, cfg.T)
+
+        def job(n):
+            side.wait_stream(main_s)
+            with torch.cuda.stream(side):
+                for _ in range(n):
+                    dst.copy_(src, non_blocking=True)
+
+        layer_steps()  # warm-up (and the kernels' one-time set-up)
+        t_layer = timed(layer_steps)
+        t_one = timed(lambda: job(1))
+        n_job = max(1, int(round(0.8 * t_layer / max(t_one, 1e-3))))
+        t_job = timed(lambda: job(n_job))
+
+        def both():
+            job(n_job)
+            layer_steps()
+
+        t_both = timed(both)
+        assert layer.device_error() == 0
+        out.append({"sm_margin": m, "layer_ms": round(t_layer, 3), "job_ms": round(t_job, 3),
+                    "both_ms": round(t_both, 3), "job_launches": n_job,
+                    "hidden": round((t_layer + t_job - t_both) / t_job, 3)})
+        del layer
+    print(json.dumps({"mode": "overlap_sweep", "workload": workload_name(cfg),
+                      "steps": steps, "job": "1 GiB device-to-device copies on a second stream",
+                      "results": out}), flush=True)
+
+
 def main():
     args = parse()
+    if args.overlap_sweep:
+        overlap_sweep(args)
+        return
     if args.impl == "reference":
         run_reference(args)
         return

@@ -194,11 +194,16 @@ class ExpertWeights:
         self.w2_h = _q(W2, 1, mx)   # FC2 dgrad: along H
 
 
-def expert_forward(X, W1, W2, p, act: ActParams, mx: bool, wq: ExpertWeights | None = None):
+def expert_forward(X, W1, W2, p, act: ActParams, mx: bool, wq: ExpertWeights | None = None,
+                   b1=None, s=None):
     """One expert's share of the fused forward.
 
     X [m, H] (its routed rows), W1 [H, N1] logical, W2 [F, H], p [m] routing probs.
-    Z = X W1;  a = act(gate, lin);  a_s = p * a (ScaledSwiGLU, R5);  Y = a_s W2.
+    Z = X W1 (+ b1);  a = act(gate, lin);  a_s = p * (s * a) (ScaledSwiGLU, R5);  Y = a_s W2.
+    Optional epilogue extras ([NV-blog] GLU-epilogue section: bias-vector addition and
+    feature scaling; the SwiGLU equation's b and c; reading R13): b1 [N1] logical
+    [gate | linear] bias added to Z (which is what the backward sees as the saved Z), s [F] a
+    per-feature scale of the activation output. The returned `a` is the unscaled activation.
     [TE-MoE] Challenge 3 (GroupedLinear -> ScaledSwiGLU -> GroupedLinear) and [NV-blog]
     Figure 1 (FC1 + activation + quantise fused, then FC2). In MXFP8 (R8) each GEMM uses
     MXFP8 operands blocked along its reduction dimension: X and W1 along H, a_s and W2 along F.
@@ -207,31 +212,36 @@ def expert_forward(X, W1, W2, p, act: ActParams, mx: bool, wq: ExpertWeights | N
     wq = wq or ExpertWeights(W1, W2, mx)
     F = W2.shape[0]
     Z = _q(X, 1, mx) @ wq.w1_h
+    if b1 is not None:
+        Z = Z + b1[None, :]
     if act.gated:
         a = act_forward(act, Z[:, :F], Z[:, F:])
     else:
         a = act_forward(act, Z)
-    a_s = p[:, None] * a
+    a_s = p[:, None] * (a * s[None, :] if s is not None else a)
     Y = _q(a_s, 1, mx) @ wq.w2_f
     return Z, a, a_s, Y
 
 
 def expert_backward(X, W1, W2, p, Z, a, a_s, dY, act: ActParams, mx: bool,
-                    wq: ExpertWeights | None = None):
+                    wq: ExpertWeights | None = None, s=None, extras: dict | None = None):
     """One expert's share of the backward ([NV-blog] Figure 1: FC2 dgrad + dActivation +
     quantise fused; the weight-gradient GEMMs unfused).
 
-      dA_s = dY W2^T;  d_prob = sum_f dA_s * a  (R9);  dA = p * dA_s;
+      dA_s = dY W2^T;  d_prob = sum_f dA_s * s * a  (R9);  dA = p * s * dA_s;
       (dG, dL) = dact(Z, dA);  dZ = [dG | dL];
       dW2 = a_s^T dY;  dW1 = X^T dZ;  dX = dZ W1^T.
+    With the epilogue extras (s the feature scale, 1 when absent) `extras` receives
+    db1 = sum over rows of dZ and ds = sum over rows of p * dA_s * a.
     MXFP8 (R8): dY and W2 along H for dgrad; a_s and dY column-wise (along rows) for dW2;
     dZ along N1 and W1 along N1 for dX; X and dZ column-wise for dW1.
     """
     wq = wq or ExpertWeights(W1, W2, mx)
     F = W2.shape[0]
     dA_s = _q(dY, 1, mx) @ wq.w2_h.T
-    d_prob = (dA_s * a).sum(axis=1)
-    dA = p[:, None] * dA_s
+    sa = a * s[None, :] if s is not None else a
+    d_prob = (dA_s * sa).sum(axis=1)
+    dA = p[:, None] * (dA_s * s[None, :] if s is not None else dA_s)
     if act.gated:
         dg, dl = act_backward(act, Z[:, :F], Z[:, F:], dA)
         dZ = np.concatenate([dg, dl], axis=1)
@@ -240,6 +250,9 @@ def expert_backward(X, W1, W2, p, Z, a, a_s, dY, act: ActParams, mx: bool,
     dW2 = _qrows(a_s, mx).T @ _qrows(dY, mx)
     dW1 = _qrows(X, mx).T @ _qrows(dZ, mx)
     dX = _q(dZ, 1, mx) @ wq.w1_n.T
+    if extras is not None:
+        extras["db1"] = dZ.sum(axis=0)
+        extras["ds"] = (p[:, None] * dA_s * a).sum(axis=0)
     return dZ, dX, dW1, dW2, d_prob
 
 
@@ -256,17 +269,21 @@ class LayerResult:
     dW1: np.ndarray | None = None
     dW2: np.ndarray | None = None
     d_probs: np.ndarray | None = None
+    db1: np.ndarray | None = None      # [E, N1] FC1 bias gradient (when a bias is given)
+    ds: np.ndarray | None = None       # [E, F] feature-scale gradient (when a scale is given)
     per_expert: list = field(default_factory=list)   # dicts of intermediates by expert
 
 
 def layer(logits, x, W1, W2, k: int, act: ActParams, mx: bool = False, align: int = 32,
-          dy=None, keep_intermediates: bool = False, experts=None) -> LayerResult:
+          dy=None, keep_intermediates: bool = False, experts=None, b1=None,
+          s=None) -> LayerResult:
     """Forward (and, when dy is given, backward) of the MoE expert layer.
 
     logits fp32 [T,E]; x fp64 [T,H]; W1 fp64 [E,H,N1] (or a callable e -> [H,N1]);
     W2 fp64 [E,F,H] (or callable); dy fp64 [T,H].
     y[t] = sum_j Y[row_of[t,j]]: the index_add of [TE-MoE] Challenge 1's per-expert loop.
     `experts` restricts the computation to a subset (y / dx then hold only their share).
+    b1 [E, N1] and s [E, F] are the optional epilogue extras (expert_forward).
     """
     T, E = np.asarray(logits).shape
     ids, probs = route(logits, k)
@@ -280,19 +297,30 @@ def layer(logits, x, W1, W2, k: int, act: ActParams, mx: bool = False, align: in
         res.dx = np.zeros((T, H))
         res.d_probs = np.zeros((T, k))
         res.dW1, res.dW2 = {}, {}
+        if b1 is not None:
+            res.db1 = np.zeros_like(np.asarray(b1, dtype=np.float64))
+        if s is not None:
+            res.ds = np.zeros_like(np.asarray(s, dtype=np.float64))
     for e in (range(E) if experts is None else experts):
         tok, slot = perm.rows_of_expert[e]
         W1e, W2e = w1(e), w2(e)
         wq = ExpertWeights(W1e, W2e, mx)
         X = x[tok]
         p = probs[tok, slot]
-        Z, a, a_s, Y = expert_forward(X, W1e, W2e, p, act, mx, wq)
+        b1e = None if b1 is None else b1[e]
+        se = None if s is None else s[e]
+        Z, a, a_s, Y = expert_forward(X, W1e, W2e, p, act, mx, wq, b1=b1e, s=se)
         np.add.at(y, tok, Y)
         inter = dict(Z=Z, a=a, a_s=a_s, Y=Y) if keep_intermediates else {}
         if dy is not None:
             dY = dy[tok]
+            ex = {}
             dZ, dX, dW1, dW2, d_prob = expert_backward(X, W1e, W2e, p, Z, a, a_s, dY, act, mx,
-                                                       wq)
+                                                       wq, s=se, extras=ex)
+            if b1 is not None:
+                res.db1[e] = ex["db1"]
+            if s is not None:
+                res.ds[e] = ex["ds"]
             np.add.at(res.dx, tok, dX)
             res.d_probs[tok, slot] = d_prob
             res.dW1[e], res.dW2[e] = dW1, dW2

@@ -342,3 +342,54 @@ def test_mx_expert_matches_scalar_brute_force():
     assert np.allclose(dW2, q(asb, True).T @ q(dY, True), rtol=1e-12, atol=1e-12)
     assert np.allclose(dW1, q(X, True).T @ q(dZb, True), rtol=1e-12, atol=1e-12)
     assert np.allclose(dX, q(dZb, False) @ q(W1, False).T, rtol=1e-12, atol=1e-12)
+
+
+def torch_layer_extras(lg, x, W1, W2, b1, sc, k, name):
+    """torch_layer with the FC1 bias added to z and the feature scale on the activation."""
+    ids, _ = moe.route(lg, k)
+    lt = torch.tensor(lg.astype(np.float64))
+    chosen = torch.gather(lt, 1, torch.tensor(ids))
+    probs = torch.softmax(chosen, dim=1).detach().requires_grad_(True)
+    xt = torch.tensor(x, requires_grad=True)
+    w1 = torch.tensor(W1, requires_grad=True)
+    w2 = torch.tensor(W2, requires_grad=True)
+    bt = torch.tensor(b1, requires_grad=True)
+    st = torch.tensor(sc, requires_grad=True)
+    F = W2.shape[1]
+    y = torch.zeros_like(xt)
+    for j in range(k):
+        e = ids[:, j]
+        z = torch.einsum("th,thn->tn", xt, w1[e]) + bt[e]
+        a = torch_act(name, z[:, :F], z[:, F:]) * st[e]
+        y = y + probs[:, j:j + 1] * torch.einsum("tf,tfh->th", a, w2[e])
+    return y, probs, xt, w1, w2, bt, st
+
+
+@pytest.mark.parametrize("name", ["swiglu", "clamped_swiglu", "geglu"])
+def test_bias_and_feature_scale_vs_torch_autograd(name):
+    cfg, lg, x, W1, W2, dy = small_inputs(act=name, E=5, k=3, T=48)
+    p = ACTS[name]
+    rng = np.random.default_rng(7)
+    b1 = 0.3 * rng.standard_normal((cfg.E, W1.shape[2]))
+    sc = 1.0 + 0.5 * rng.standard_normal((cfg.E, W2.shape[1]))
+    r = moe.layer(lg, x, W1, W2, cfg.k, p, dy=dy, b1=b1, s=sc)
+    y, probs, xt, w1, w2, bt, st = torch_layer_extras(lg, x, W1, W2, b1, sc, cfg.k, name)
+    assert np.allclose(r.y, y.detach().numpy(), rtol=1e-11, atol=1e-12)
+    y.backward(torch.tensor(dy))
+    dW1, dW2 = moe.stack_weight_grads(r, cfg.E)
+    assert np.allclose(r.dx, xt.grad.numpy(), rtol=1e-10, atol=1e-11)
+    assert np.allclose(dW1, w1.grad.numpy(), rtol=1e-10, atol=1e-11)
+    assert np.allclose(dW2, w2.grad.numpy(), rtol=1e-10, atol=1e-11)
+    assert np.allclose(r.d_probs, probs.grad.numpy(), rtol=1e-10, atol=1e-11)
+    assert np.allclose(r.db1, bt.grad.numpy(), rtol=1e-10, atol=1e-11)
+    assert np.allclose(r.ds, st.grad.numpy(), rtol=1e-10, atol=1e-11)
+
+
+def test_zero_bias_unit_scale_change_nothing():
+    cfg, lg, x, W1, W2, dy = small_inputs(act="swiglu", E=4, k=2, T=40)
+    p = ACTS["swiglu"]
+    plain = moe.layer(lg, x, W1, W2, cfg.k, p, dy=dy)
+    ext = moe.layer(lg, x, W1, W2, cfg.k, p, dy=dy, b1=np.zeros((cfg.E, W1.shape[2])),
+                    s=np.ones((cfg.E, W2.shape[1])))
+    for a, b in ((plain.y, ext.y), (plain.dx, ext.dx), (plain.d_probs, ext.d_probs)):
+        assert np.array_equal(a, b)

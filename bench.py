@@ -55,6 +55,8 @@ def parse():
                     help="comma-separated SM margins: time the layer step, a concurrent "
                          "memory-bound job (device copies on another stream) and both "
                          "together at each margin; prints one JSON line")
+    ap.add_argument("--extras", type=int, default=0,
+                    help="epilogue extras bits: 1 FC1 bias, 2 feature scale (BF16 gated)")
     ap.add_argument("--recompute", action="store_true",
                     help="keep no FC1 output; the FC2-dgrad kernel recomputes it (BF16)")
     return ap.parse_args()
@@ -456,8 +458,13 @@ def main():
     def bf(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
 
-    desc = g.desc_from_config(cfg, sm_margin=args.sm_margin, recompute=args.recompute)
+    desc = g.desc_from_config(cfg, sm_margin=args.sm_margin, recompute=args.recompute,
+                              extras=args.extras)
     layer = g.MoELayer(desc, dev)
+    fc1_bias = (torch.from_numpy(synth.gen_fc1_bias(cfg)).to(dev)
+                if args.extras & g.EXTRA_BIAS else None)
+    feat_scale = (torch.from_numpy(synth.gen_feat_scale(cfg)).to(dev)
+                  if args.extras & g.EXTRA_SCALE else None)
     w1_log = torch.stack([bf(w) for w in hin["w1"]]).to(dev)
     w1p = g.pack_w1(w1_log, gated=cfg.gated, ilv=cfg.ilv)
     del w1_log
@@ -469,8 +476,8 @@ def main():
 
     def step():
         layer.route_permute(logits, x, T)
-        layer.forward(w1p, w2, T)
-        layer.backward(dy, w1p, w2, T)
+        layer.forward(w1p, w2, T, fc1_bias=fc1_bias, feat_scale=feat_scale)
+        layer.backward(dy, w1p, w2, T, feat_scale=feat_scale)
 
     n_w = g.moe_launch_count()
     for _ in range(max(args.warmup, 1)):
@@ -581,7 +588,7 @@ def main():
                 ev["dy"].record(h2d)
             load_inputs()                       # next step's inputs; x and logits are free
             main.wait_event(ev["y_out"])        # the previous y has left the device
-            layer.forward(w1p, w2, T)
+            layer.forward(w1p, w2, T, fc1_bias=fc1_bias, feat_scale=feat_scale)
             ev["fwd"].record(main)
             with torch.cuda.stream(d2h):
                 d2h.wait_event(ev["fwd"])
@@ -589,7 +596,7 @@ def main():
                 ev["y_out"].record(d2h)
             main.wait_event(ev["dy"])
             main.wait_event(ev["dx_out"])       # the previous dx / d_probs have left
-            layer.backward(dy, w1p, w2, T)
+            layer.backward(dy, w1p, w2, T, feat_scale=feat_scale)
             ev["bwd"].record(main)
             with torch.cuda.stream(d2h):
                 d2h.wait_event(ev["bwd"])
@@ -645,7 +652,8 @@ def main():
                        "l2": f"no flush: each step streams {w_bytes / 1e9:.1f} GB of bf16 "
                              "weights and weight gradients, > 129 MB L2",
                        "sm_margin": args.sm_margin, "flops_per_step": flops,
-                       "recompute": bool(args.recompute), "workspace_bytes": layer.ws_bytes},
+                       "recompute": bool(args.recompute), "extras": args.extras,
+                       "workspace_bytes": layer.ws_bytes},
             "tokens_per_s": cfg.T * world / (ms_max / 1e3),
             "pct_tensor_peak": {"value": 100 * value / world / p_tc, "peak_tflops": p_tc,
                                 "peak_kind": tc_kind},

@@ -18,16 +18,19 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libmoegmm.so")
 
 PREC = {"bf16": 0, "mxfp8": 1}
 ACT = {"swiglu": 0, "clamped_swiglu": 1, "geglu": 2, "srelu": 3}
+EXTRA_BIAS, EXTRA_SCALE = 1, 2  # moe_layer_desc_t.extras bits
 DEVERR = {0: "none", 1: "capacity", 2: "timeout", 3: "bad_id"}
 
 KERNEL_NAMES = ("route_topk", "assign_rows", "gather_x", "gemm_fc1_fprop", "gemm_fc2_fprop",
                 "combine_y", "gather_dy", "gemm_fc2_dgrad", "dprob_reduce", "gemm_fc2_wgrad",
-                "gemm_fc1_dgrad", "combine_dx", "gemm_fc1_wgrad", "mxfp8_quantize", "pack_fc1")
+                "gemm_fc1_dgrad", "combine_dx", "gemm_fc1_wgrad", "mxfp8_quantize", "pack_fc1",
+                "extras_reduce")
 
 EXPORTS = ("moe_timeline_begin", "moe_timeline_end", "moe_workspace_size", "moe_workspace_layout", "moe_route_permute",
            "moe_grouped_mlp_fwd", "moe_grouped_mlp_bwd", "mxfp8_quantize", "moe_pack_fc1_weight",
            "moe_get_error", "moe_clear_error", "moe_gemm_ctas", "moe_launch_count",
-           "moe_last_error_string", "moe_selftest_wait_timeout")
+           "moe_last_error_string", "moe_selftest_wait_timeout", "moe_grouped_mlp_fwd_ex",
+           "moe_grouped_mlp_bwd_ex")
 
 
 class LayerDesc(ctypes.Structure):
@@ -37,7 +40,7 @@ class LayerDesc(ctypes.Structure):
                 ("gate_max", ctypes.c_float), ("lin_lo", ctypes.c_float),
                 ("lin_hi", ctypes.c_float), ("lin_offset", ctypes.c_float),
                 ("sm_margin", ctypes.c_int32), ("ilv", ctypes.c_int32), ("align", ctypes.c_int32),
-                ("recompute", ctypes.c_int32)]
+                ("recompute", ctypes.c_int32), ("extras", ctypes.c_int32)]
 
 
 class WsLayout(ctypes.Structure):
@@ -47,7 +50,8 @@ class WsLayout(ctypes.Structure):
                 ("x_perm", ctypes.c_size_t), ("z", ctypes.c_size_t), ("a_s", ctypes.c_size_t),
                 ("y_perm", ctypes.c_size_t), ("dy_perm", ctypes.c_size_t),
                 ("dz", ctypes.c_size_t), ("dx_perm", ctypes.c_size_t),
-                ("dprob_part", ctypes.c_size_t), ("mx_base", ctypes.c_size_t)]
+                ("dprob_part", ctypes.c_size_t), ("ext_part", ctypes.c_size_t),
+                ("mx_base", ctypes.c_size_t)]
 
 
 _lib = None
@@ -84,6 +88,9 @@ def load():
         "moe_timeline_end": (_I32, [ctypes.POINTER(_I32)]),
         "moe_route_permute_noalloc": (_I32, [_DP, _I32, _P, _P, _P, _P, _P, _P, _P, _I64, _P]),
         "moe_selftest_wait_timeout": (_I32, [_P, ctypes.c_uint64, _P]),
+        "moe_grouped_mlp_fwd_ex": (_I32, [_DP, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+        "moe_grouped_mlp_bwd_ex": (_I32, [_DP, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                          _SZ, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -123,15 +130,18 @@ def _stream(stream) -> int | None:
 
 def make_desc(E, k, H, F, T_max, precision="bf16", activation="swiglu", beta=1.0,
               gate_max=math.inf, lin_lo=-math.inf, lin_hi=math.inf, lin_offset=0.0,
-              sm_margin=0, ilv=64, align=32, recompute=False) -> LayerDesc:
+              sm_margin=0, ilv=64, align=32, recompute=False, extras=0) -> LayerDesc:
+    """extras: bit 0 FC1 bias, bit 1 feature scale (EXTRA_BIAS | EXTRA_SCALE)."""
     return LayerDesc(E, k, H, F, T_max, PREC[precision], ACT[activation], beta, gate_max,
-                     lin_lo, lin_hi, lin_offset, sm_margin, ilv, align, int(recompute))
+                     lin_lo, lin_hi, lin_offset, sm_margin, ilv, align, int(recompute),
+                     int(extras))
 
 
-def desc_from_config(cfg, T_max=None, sm_margin=0, recompute=False) -> LayerDesc:
+def desc_from_config(cfg, T_max=None, sm_margin=0, recompute=False, extras=0) -> LayerDesc:
     return make_desc(cfg.E, cfg.k, cfg.H, cfg.F, cfg.T if T_max is None else T_max,
                      cfg.precision, cfg.activation, cfg.beta, cfg.gate_max, cfg.lin_lo,
-                     cfg.lin_hi, cfg.lin_offset, sm_margin, cfg.ilv, cfg.align, recompute)
+                     cfg.lin_hi, cfg.lin_offset, sm_margin, cfg.ilv, cfg.align, recompute,
+                     extras)
 
 
 # ------------------------------------------------------------------ C ABI, same names
@@ -175,6 +185,21 @@ def moe_grouped_mlp_bwd(desc, T, dy, w1_packed, w2, dx, dw1_packed, dw2, d_probs
     _check(load().moe_grouped_mlp_bwd(ctypes.byref(desc), T, _ptr(dy), _ptr(w1_packed), _ptr(w2),
                                       _ptr(dx), _ptr(dw1_packed), _ptr(dw2), _ptr(d_probs),
                                       _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_grouped_mlp_fwd_ex(desc, T, w1_packed, w2, fc1_bias, feat_scale, y, ws, ws_bytes,
+                           stream=None):
+    _check(load().moe_grouped_mlp_fwd_ex(ctypes.byref(desc), T, _ptr(w1_packed), _ptr(w2),
+                                         _ptr(fc1_bias), _ptr(feat_scale), _ptr(y), _ptr(ws),
+                                         ws_bytes, _stream(stream)))
+
+
+def moe_grouped_mlp_bwd_ex(desc, T, dy, w1_packed, w2, feat_scale, dx, dw1_packed, dw2, d_probs,
+                           d_fc1_bias, d_feat_scale, ws, ws_bytes, stream=None):
+    _check(load().moe_grouped_mlp_bwd_ex(ctypes.byref(desc), T, _ptr(dy), _ptr(w1_packed),
+                                         _ptr(w2), _ptr(feat_scale), _ptr(dx), _ptr(dw1_packed),
+                                         _ptr(dw2), _ptr(d_probs), _ptr(d_fc1_bias),
+                                         _ptr(d_feat_scale), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def mxfp8_quantize(inp, M, N, rowwise, colwise, q_row=None, s_row=None, q_col=None, s_col=None,
@@ -274,6 +299,8 @@ class MoELayer:
         self.d_probs = torch.empty(T, k, dtype=torch.float32, device=dev)
         self.dw1 = None
         self.dw2 = None
+        self.d_fc1_bias = None     # extras: [E, N1] fp32, logical order
+        self.d_feat_scale = None   # extras: [E, F] fp32
 
     # views into the workspace -------------------------------------------------------
     def ws_view(self, name, dtype, shape):
@@ -295,18 +322,36 @@ class MoELayer:
         moe_route_permute(self.desc, T, logits, x, self.topk_ids, self.topk_probs, self.counts,
                           self.ws, self.ws_bytes, stream)
 
-    def forward(self, w1_packed, w2, T, stream=None):
-        moe_grouped_mlp_fwd(self.desc, T, w1_packed, w2, self.y, self.ws, self.ws_bytes, stream)
+    def forward(self, w1_packed, w2, T, stream=None, fc1_bias=None, feat_scale=None):
+        """fc1_bias fp32 [E, N1] (logical order) and feat_scale fp32 [E, F] for a layer made
+        with the matching extras bits."""
+        if self.desc.extras:
+            moe_grouped_mlp_fwd_ex(self.desc, T, w1_packed, w2, fc1_bias, feat_scale, self.y,
+                                   self.ws, self.ws_bytes, stream)
+        else:
+            moe_grouped_mlp_fwd(self.desc, T, w1_packed, w2, self.y, self.ws, self.ws_bytes,
+                                stream)
         return self.y[:T]
 
-    def backward(self, dy, w1_packed, w2, T, stream=None):
+    def backward(self, dy, w1_packed, w2, T, stream=None, feat_scale=None):
         import torch
         if self.dw1 is None:
             d = self.desc
             self.dw1 = torch.empty(d.E, self.N1, d.H, dtype=torch.bfloat16, device=self.device)
             self.dw2 = torch.empty(d.E, d.F, d.H, dtype=torch.bfloat16, device=self.device)
-        moe_grouped_mlp_bwd(self.desc, T, dy, w1_packed, w2, self.dx, self.dw1, self.dw2,
-                            self.d_probs, self.ws, self.ws_bytes, stream)
+        if self.desc.extras:
+            if self.d_fc1_bias is None:
+                d = self.desc
+                self.d_fc1_bias = (torch.empty(d.E, self.N1, dtype=torch.float32,
+                                               device=self.device) if d.extras & 1 else None)
+                self.d_feat_scale = (torch.empty(d.E, d.F, dtype=torch.float32,
+                                                 device=self.device) if d.extras & 2 else None)
+            moe_grouped_mlp_bwd_ex(self.desc, T, dy, w1_packed, w2, feat_scale, self.dx,
+                                   self.dw1, self.dw2, self.d_probs, self.d_fc1_bias,
+                                   self.d_feat_scale, self.ws, self.ws_bytes, stream)
+        else:
+            moe_grouped_mlp_bwd(self.desc, T, dy, w1_packed, w2, self.dx, self.dw1, self.dw2,
+                                self.d_probs, self.ws, self.ws_bytes, stream)
         return self.dx[:T], self.dw1, self.dw2, self.d_probs[:T]
 
     def device_error(self, stream=None) -> int:

@@ -97,6 +97,11 @@ static moe_status_t validate_desc(const moe_layer_desc_t* d) {
     return fail(MOE_ERR_INVALID_ARG, "recompute must be 0 or 1");
   if (d->recompute && (d->precision != MOE_PREC_BF16 || d->activation == MOE_ACT_SRELU))
     return fail(MOE_ERR_UNSUPPORTED, "recompute needs a BF16 layer with a gated activation");
+  if (d->extras & ~3) return fail(MOE_ERR_INVALID_ARG, "extras has unknown bits");
+  if (d->extras && (d->precision != MOE_PREC_BF16 || d->activation == MOE_ACT_SRELU ||
+                    d->recompute))
+    return fail(MOE_ERR_UNSUPPORTED,
+                "epilogue extras need a BF16 layer with a gated activation, no recompute");
   if (r_cap(d) > (int64_t)INT32_MAX / 2) return fail(MOE_ERR_UNSUPPORTED, "row capacity too large");
   if (d->precision == MOE_PREC_MXFP8 &&
       (int64_t)d->E * round128(n1_of(d)) * d->H > (int64_t)INT32_MAX * 8)
@@ -179,6 +184,7 @@ static void compute_layout(const moe_layer_desc_t* d, moe_ws_layout_t* L) {
   L->dy_perm = take(R * H * 2);
   L->dz = mx ? SIZE_MAX : take(R * N1 * 2);
   L->dprob_part = take(R * nparts * 4);
+  L->ext_part = d->extras ? take((R + 31) / 32 * (N1 + F) * 4) : SIZE_MAX;
   L->mx_base = SIZE_MAX;
   if (mx) {
     MxOps m;
@@ -362,11 +368,14 @@ moe_status_t moe_route_permute(const moe_layer_desc_t* d, int32_t T, const float
   return MOE_OK;
 }
 
-moe_status_t moe_grouped_mlp_fwd(const moe_layer_desc_t* d, int32_t T, const void* w1_packed,
-                                 const void* w2, void* y, void* ws, size_t ws_bytes,
-                                 moe_stream_t stream) {
+static moe_status_t fwd_impl(const moe_layer_desc_t* d, int32_t T, const void* w1_packed,
+                             const void* w2, const float* fc1_bias, const float* feat_scale,
+                             void* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
   moe_status_t st = validate_desc(d);
   if (st != MOE_OK) return st;
+  if (((d->extras & 1) != 0) != (fc1_bias != nullptr) ||
+      ((d->extras & 2) != 0) != (feat_scale != nullptr))
+    return fail(MOE_ERR_INVALID_ARG, "fc1_bias / feat_scale must match desc->extras");
   if (T < 0 || T > d->T_max) return fail(MOE_ERR_INVALID_ARG, "T=%d outside [0, T_max]", T);
   if (!w1_packed || !w2 || (T > 0 && !y)) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
   if (!aligned16(w1_packed) || !aligned16(w2) || !aligned16(y))
@@ -400,6 +409,8 @@ moe_status_t moe_grouped_mlp_fwd(const moe_layer_desc_t* d, int32_t T, const voi
   GemmProblem p = base_problem(d, w);
   p.w1p = w1_packed;
   p.w2 = w2;
+  p.fc1_bias = fc1_bias;
+  p.fscale = feat_scale;
   // FC1 + activation + probability scale (kernel family 2)
   p.role = ROLE_FC1_FPROP;
   p.out = d->recompute ? nullptr : w.at<void>(w.L.z);  // NULL: Z is not kept
@@ -409,6 +420,7 @@ moe_status_t moe_grouped_mlp_fwd(const moe_layer_desc_t* d, int32_t T, const voi
   p.role = ROLE_FC2_FPROP;
   p.out = w.at<void>(w.L.y_perm);
   p.out2 = nullptr;
+  p.fc1_bias = p.fscale = nullptr;
   if ((e = launch_grouped_gemm(p, s)) != cudaSuccess) return cuda_fail(e, "FC2 grouped GEMM");
   if (T > 0) {
     combine_rows_kernel<<<grid_for(T, 8), 256, 0, s>>>(w.at<uint4>(w.L.y_perm),
@@ -421,12 +433,17 @@ moe_status_t moe_grouped_mlp_fwd(const moe_layer_desc_t* d, int32_t T, const voi
   return MOE_OK;
 }
 
-moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t* d, int32_t T, const void* dy,
-                                 const void* w1_packed, const void* w2, void* dx,
-                                 void* dw1_packed, void* dw2, float* d_probs, void* ws,
-                                 size_t ws_bytes, moe_stream_t stream) {
+static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* dy,
+                             const void* w1_packed, const void* w2, const float* feat_scale,
+                             void* dx, void* dw1_packed, void* dw2, float* d_probs,
+                             float* d_fc1_bias, float* d_feat_scale, void* ws, size_t ws_bytes,
+                             moe_stream_t stream) {
   moe_status_t st = validate_desc(d);
   if (st != MOE_OK) return st;
+  if (((d->extras & 1) != 0) != (d_fc1_bias != nullptr) ||
+      ((d->extras & 2) != 0) != (feat_scale != nullptr && d_feat_scale != nullptr) ||
+      ((d->extras & 2) == 0 && (feat_scale || d_feat_scale)))
+    return fail(MOE_ERR_INVALID_ARG, "extras pointers must match desc->extras");
   if (T < 0 || T > d->T_max) return fail(MOE_ERR_INVALID_ARG, "T=%d outside [0, T_max]", T);
   if (!w1_packed || !w2 || !dw1_packed || !dw2 || (T > 0 && (!dy || !dx || !d_probs)))
     return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
@@ -482,6 +499,10 @@ moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t* d, int32_t T, const voi
   p.role = ROLE_FC2_DGRAD;
   p.out = w.at<void>(w.L.dz);
   p.dprob_part = w.at<float>(w.L.dprob_part);
+  if (d->extras) {
+    p.fscale = feat_scale;
+    p.ext_part = w.at<float>(w.L.ext_part);
+  }
   if (d->recompute) {
     p.w1p = w1_packed;
     if ((e = launch_fc2_dgrad_recompute(p, s)) != cudaSuccess)
@@ -495,6 +516,23 @@ moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t* d, int32_t T, const voi
     dprob_reduce_kernel<<<grid_for((n + 255) / 256, 4), 256, 0, s>>>(
         w.at<float>(w.L.dprob_part), nparts, row_of, n, d_probs);
     count_launch(s, MOE_K_DPROB_REDUCE);
+  }
+  if (d->extras) {
+    // per-expert sums of the dGLU epilogue's per-32-row column sums
+    const int N1 = n1_of(d), ld = N1 + d->F;
+    const int32_t* off = w.at<int32_t>(w.L.offsets);
+    if (d_fc1_bias) {
+      group_colsum_kernel<<<dim3((N1 + 255) / 256, d->E), 256, 0, s>>>(
+          w.at<float>(w.L.ext_part), ld, 0, N1, off, d_fc1_bias);
+      count_launch(s, MOE_K_EXTRAS_REDUCE);
+    }
+    if (d_feat_scale) {
+      group_colsum_kernel<<<dim3((d->F + 255) / 256, d->E), 256, 0, s>>>(
+          w.at<float>(w.L.ext_part), ld, N1, d->F, off, d_feat_scale);
+      count_launch(s, MOE_K_EXTRAS_REDUCE);
+    }
+    p.fscale = nullptr;
+    p.ext_part = nullptr;
   }
   // FC2 wgrad
   p.role = ROLE_FC2_WGRAD;
@@ -516,6 +554,39 @@ moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t* d, int32_t T, const voi
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "bwd launch");
   return MOE_OK;
+}
+
+moe_status_t moe_grouped_mlp_fwd(const moe_layer_desc_t* d, int32_t T, const void* w1_packed,
+                                 const void* w2, void* y, void* ws, size_t ws_bytes,
+                                 moe_stream_t stream) {
+  if (d && d->extras) return fail(MOE_ERR_UNSUPPORTED, "a layer with extras uses moe_grouped_mlp_fwd_ex");
+  return fwd_impl(d, T, w1_packed, w2, nullptr, nullptr, y, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_grouped_mlp_fwd_ex(const moe_layer_desc_t* d, int32_t T, const void* w1_packed,
+                                    const void* w2, const float* fc1_bias,
+                                    const float* feat_scale, void* y, void* ws, size_t ws_bytes,
+                                    moe_stream_t stream) {
+  return fwd_impl(d, T, w1_packed, w2, fc1_bias, feat_scale, y, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t* d, int32_t T, const void* dy,
+                                 const void* w1_packed, const void* w2, void* dx,
+                                 void* dw1_packed, void* dw2, float* d_probs, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream) {
+  if (d && d->extras) return fail(MOE_ERR_UNSUPPORTED, "a layer with extras uses moe_grouped_mlp_bwd_ex");
+  return bwd_impl(d, T, dy, w1_packed, w2, nullptr, dx, dw1_packed, dw2, d_probs, nullptr,
+                  nullptr, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_grouped_mlp_bwd_ex(const moe_layer_desc_t* d, int32_t T, const void* dy,
+                                    const void* w1_packed, const void* w2,
+                                    const float* feat_scale, void* dx, void* dw1_packed,
+                                    void* dw2, float* d_probs, float* d_fc1_bias,
+                                    float* d_feat_scale, void* ws, size_t ws_bytes,
+                                    moe_stream_t stream) {
+  return bwd_impl(d, T, dy, w1_packed, w2, feat_scale, dx, dw1_packed, dw2, d_probs, d_fc1_bias,
+                  d_feat_scale, ws, ws_bytes, stream);
 }
 
 moe_status_t moe_selftest_wait_timeout(int32_t* err, uint64_t limit_ns, moe_stream_t stream) {

@@ -60,6 +60,13 @@ struct GemmArgs {
   int ilv;
   int F;
   int wide;  // out and out2 are 32-byte aligned with 16-element strides: 256-bit stores
+  // epilogue extras (gated BF16): FC1 bias [E, N1] in logical [gate | linear] order and
+  // feature scale [E, F] (fp32, NULL when absent); the dGLU epilogue writes per-32-row column
+  // sums of dZ and of p * dA_s * a into ext_part [R_cap / 32, N1 + F]
+  const float* fc1_bias;
+  const float* fscale;
+  float* ext_part;
+  int N1;  // FC1 output columns (2F gated)
   ActDev act;
   int* err;
 };
@@ -127,6 +134,69 @@ MOE_DEVICE void decode_tile(int tile, const GemmArgs& p, const Ctrl& c, int MT, 
   }
 }
 
+// Column sums over the warp's 32 rows: v[i] of every lane in, the sum of v[lane] out (a
+// butterfly that halves the values each lane keeps: 31 shuffles for 32 columns).
+MOE_DEVICE float warp_colsum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool hi = lane & w;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = hi ? v[i] : v[i + w];
+      const float keep = hi ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, w);
+    }
+  }
+  return v[0];
+}
+
+// dGLU with the epilogue extras for one 16-column step: the feature scale s enters as
+// dA = p * s * dA_s and d_prob += dA_s * s * a; the step's column sums over the warp's rows of
+// dZ (bias gradient) and of p * dA_s * a (scale gradient) are stored to the row group's
+// partials (gate columns at f, linear at F + f, scale at N1 + f).
+template <int KIND>
+MOE_DEVICE float dglu16_extras(const GemmArgs& p, float prob, const uint32_t (&das)[16],
+                               const uint32_t (&gw)[8], const uint32_t (&lw)[8], int e, int f,
+                               uint32_t (&dgw)[8], uint32_t (&dlw)[8], float* part, int lane) {
+  float v[32], t[32];
+  float dp = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float d = __uint_as_float(das[i]);
+    const float sc = p.fscale ? p.fscale[(int64_t)e * p.F + f + i] : 1.f;
+    const float g = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
+    const float l = (i & 1) ? bf16_hi(lw[i >> 1]) : bf16_lo(lw[i >> 1]);
+    float dg, dl;
+    const float a = act_bwd_k<KIND>(p.act, g, l, prob * sc * d, dg, dl);
+    dp += d * sc * a;
+    v[i] = dg;
+    v[16 + i] = dl;
+    t[i] = prob * d * a;
+    t[16 + i] = 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    dgw[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    dlw[i] = pack_bf16x2(v[16 + 2 * i], v[16 + 2 * i + 1]);
+  }
+  if (part) {
+    const float sb = warp_colsum32(v, lane);
+    part[lane < 16 ? f + lane : p.F + f + lane - 16] = sb;
+    const float ss = warp_colsum32(t, lane);
+    if (lane < 16) part[p.N1 + f + lane] = ss;
+  }
+  return dp;
+}
+MOE_DEVICE float dglu16_extras_any(const GemmArgs& p, float prob, const uint32_t (&das)[16],
+                                   const uint32_t (&gw)[8], const uint32_t (&lw)[8], int e, int f,
+                                   uint32_t (&dgw)[8], uint32_t (&dlw)[8], float* part, int lane) {
+  if (p.act.kind == MOE_ACT_CLAMPED_SWIGLU)
+    return dglu16_extras<MOE_ACT_CLAMPED_SWIGLU>(p, prob, das, gw, lw, e, f, dgw, dlw, part, lane);
+  if (p.act.kind == MOE_ACT_GEGLU)
+    return dglu16_extras<MOE_ACT_GEGLU>(p, prob, das, gw, lw, e, f, dgw, dlw, part, lane);
+  return dglu16_extras<MOE_ACT_SWIGLU>(p, prob, das, gw, lw, e, f, dgw, dlw, part, lane);
+}
+
 // dGLU: the saved Z (packed bf16) of dA columns f0 .. f0+15 of one row: the gate columns into
 // g and, when gated, the linear columns into l (one 256-bit load each).
 MOE_DEVICE void z_load16(const GemmArgs& p, const uint16_t* zrow, int f0, uint32_t (&g)[8],
@@ -146,7 +216,9 @@ MOE_DEVICE void st_bf16x16(void* dst, const uint32_t (&w)[8], bool wide) {
   }
 }
 
-template <int BN, int STAGES, bool A_MN, bool B_MN, int EPI, bool KG, bool B3D>
+// EXT: the GLU / dGLU epilogue with the bias and feature-scale extras (a separate
+// instantiation, so the plain kernels carry none of its code or registers).
+template <int BN, int STAGES, bool A_MN, bool B_MN, int EPI, bool KG, bool B3D, bool EXT = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
   using L = Smem<BN, STAGES>;
@@ -386,7 +458,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               g[i] = __uint_as_float(r[i]);
               l[i] = __uint_as_float(rl[i]);
             }
+            const int fa = t.n0 / 2 + cc;  // logical activation column of g[0] / l[0]
+            if (EXT && p.fc1_bias) {
+              const float* b = p.fc1_bias + (int64_t)t.e * p.N;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                g[i] += b[fa + i];
+                l[i] += b[p.F + fa + i];
+              }
+            }
             glu_fwd32(p.act, prob, g, l, v);
+            if (EXT && p.fscale) {
+              const float* sc = p.fscale + (int64_t)t.e * p.F;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] *= sc[fa + i];
+            }
             if (row_ok) {
               if (p.out) {  // the saved Z (absent when the backward recomputes it)
                 store_bf16x32w(zrow + t.n0 + gcol, g, p.wide);
@@ -430,7 +516,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool more = cc + 16 < c1 && f0 + 16 < p.N;
           if (more) tmem_ld_32x32b_x16(taddr + cc + 16, nxt);
           if (row_ok && cc + 32 < c1 && f0 + 32 < p.N) z_load16(p, zrow, f0 + 32, z2g, z2l);
-          if (row_ok) {
+          if (EXT && p.gated) {
+            // extras: every lane of the warp takes part in the column sums; the warp's 32 rows
+            // are all inside the segment or all outside (32-row aligned), and only inside
+            // groups own their partials
+            const int gcol = (f0 / p.ilv) * 2 * p.ilv + (f0 % p.ilv);
+            uint32_t dgw[8], dlw[8];
+            float* part = (t.m0 + q * 32 < t.row_end)
+                              ? p.ext_part + (int64_t)((t.m0 + q * 32) >> 5) * (p.N1 + p.F)
+                              : nullptr;
+            dp += dglu16_extras_any(p, prob, das, z0g, z0l, t.e, f0, dgw, dlw, part, lane);
+            if (row_ok) {
+              st_bf16x16(dzrow + gcol, dgw, p.wide);
+              st_bf16x16(dzrow + gcol + p.ilv, dlw, p.wide);
+            }
+          } else if (row_ok) {
             const int gcol = p.gated ? (f0 / p.ilv) * 2 * p.ilv + (f0 % p.ilv) : f0;
             uint32_t dgw[8], dlw[8];
             if (p.gated) {
@@ -476,9 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int STAGES, bool A_MN, bool B_MN, int EPI, bool KG, bool B3D>
+template <int BN, int STAGES, bool A_MN, bool B_MN, int EPI, bool KG, bool B3D, bool EXT = false>
 cudaError_t launch_instance(const GemmArgs& a, int grid, cudaStream_t s, int kid) {
-  auto kern = grouped_gemm_kernel<BN, STAGES, A_MN, B_MN, EPI, KG, B3D>;
+  auto kern = grouped_gemm_kernel<BN, STAGES, A_MN, B_MN, EPI, KG, B3D, EXT>;
   constexpr int smem = Smem<BN, STAGES>::TOTAL;
   static bool configured = false;  // per instantiation; attribute is per-function
   if (!configured) {
@@ -510,6 +610,10 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
   a.gated = p.gated;
   a.ilv = p.ilv;
   a.F = p.F;
+  a.N1 = p.N1;
+  a.fc1_bias = p.fc1_bias;
+  a.fscale = p.fscale;
+  a.ext_part = p.ext_part;
   a.act = p.act;
   a.err = p.err;
   a.row_prob = p.row_prob;
@@ -532,6 +636,9 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       if (!ok) return cudaErrorInvalidValue;
       a.wide = aligned32(a.out) && aligned32(a.out2) && a.ldo % 16 == 0 && a.ldo2 % 16 == 0 &&
                a.out_estride % 16 == 0;
+      if (a.fc1_bias || a.fscale)
+        return launch_instance<kBN, kStages, false, false, EPI_GLU, false, true, true>(a, grid, s,
+                                                                                      kid);
       return launch_instance<kBN, kStages, false, false, EPI_GLU, false, true>(a, grid, s, kid);
     case ROLE_FC2_FPROP:
       ok &= tmap_2d(&a.tmA, p.a_s, F, R, 64, BM);
@@ -552,6 +659,9 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       if (!ok) return cudaErrorInvalidValue;
       a.wide = aligned32(a.out) && aligned32(a.out2) && a.ldo % 16 == 0 && a.ldo2 % 16 == 0 &&
                a.out_estride % 16 == 0;
+      if (a.ext_part)
+        return launch_instance<kBN, kStages, false, false, EPI_DGLU, false, true, true>(a, grid, s,
+                                                                                       kid);
       return launch_instance<kBN, kStages, false, false, EPI_DGLU, false, true>(a, grid, s, kid);
     case ROLE_FC1_DGRAD:
       ok &= tmap_2d(&a.tmA, p.dz, N1, R, 64, BM);

@@ -28,6 +28,9 @@ __global__ void dprob_reduce_kernel(const float* part, int nparts, const int32_t
 __global__ void pack_fc1_kernel(const uint16_t* src, uint16_t* dst, int E, int H, int F, int N1,
                                 int gated, int ilv, int inverse);
 
+__global__ void group_colsum_kernel(const float* part, int ld, int col0, int ncols,
+                                    const int32_t* offsets, float* out);
+
 // mxfp8.cu
 // Sizes the quantiser's 32-bit tile indexing covers (M rows < 2^31, tile count < 2^31).
 bool mxfp8_quantize_size_ok(int64_t M, int64_t N);
@@ -74,6 +77,11 @@ struct GemmProblem {
   void* out;               // role output (z, y_perm, dz, dW2, dx_perm, dW1)
   void* out2;              // FC1: a_s
   float* dprob_part;       // FC2 dgrad: [R_cap, nparts]
+  // epilogue extras (BF16 gated; NULL when absent): FC1 bias [E, N1] logical order, feature
+  // scale [E, F]; FC2 dgrad writes per-32-row column sums into ext_part [R_cap/32, N1 + F]
+  const float* fc1_bias;
+  const float* fscale;
+  float* ext_part;
   int gated, ilv;
   ActDev act;
   int* err;

@@ -5,6 +5,8 @@
 //   combine_rows_kernel    out[t] = sum_j in[row_of[t, j]] in fp32, j ascending
 //   dprob_reduce_kernel    d_probs[t, j] = sum over column tiles of the partial d_prob
 //   pack_fc1_kernel        GLU weight repacking ([NV-blog] GLU-epilogue section, Figure 2)
+//   group_colsum_kernel    per-expert sums of the dGLU epilogue's per-32-row column sums
+//                          (the FC1 bias and feature-scale gradients)
 // Sources: [TE-MoE] Figure 1 (top-2 router, weighted sum) and Challenge 1 (per-expert loop
 // with index_add: the row order here is the order torch.where visits tokens); [NV-blog]
 // host-sync section (per-group token counts kept in device memory).
@@ -274,6 +276,26 @@ __global__ void __launch_bounds__(256) pack_fc1_kernel(const uint16_t* __restric
       for (int i = ty; i < 32; i += 8) d[(int64_t)(h0 + i) * N1 + c0 + tx] = tile[tx][i];
     }
   }
+}
+
+}  // namespace moe
+
+namespace moe {
+
+// out[e][c] = sum over the 32-row groups g of expert e (g in [off[e]/32, off[e+1]/32); the
+// segments are 32-row aligned) of part[g][col0 + c], for c < ncols. One thread per (column,
+// expert), groups in ascending order: deterministic.
+__global__ void __launch_bounds__(256) group_colsum_kernel(const float* __restrict__ part,
+                                                           int ld, int col0, int ncols,
+                                                           const int32_t* __restrict__ offsets,
+                                                           float* __restrict__ out) {
+  const int e = blockIdx.y;
+  const int c = blockIdx.x * 256 + threadIdx.x;
+  if (c >= ncols) return;
+  const int g0 = offsets[e] >> 5, g1 = offsets[e + 1] >> 5;
+  float acc = 0.f;
+  for (int g = g0; g < g1; ++g) acc += part[(int64_t)g * ld + col0 + c];
+  out[(int64_t)e * ncols + c] = acc;
 }
 
 }  // namespace moe

@@ -145,6 +145,16 @@ def gen_w2(cfg: LayerConfig) -> np.ndarray:
     return np.stack([gen_w2_expert(cfg, e) for e in range(cfg.E)])
 
 
+def gen_fc1_bias(cfg: LayerConfig) -> np.ndarray:
+    """Optional FC1 bias, fp32 [E, N1] in the logical [gate | linear] order: 0.1 N(0,1)."""
+    return (0.1 * _rng(cfg.seed, 6).standard_normal((cfg.E, cfg.N1))).astype(np.float32)
+
+
+def gen_feat_scale(cfg: LayerConfig) -> np.ndarray:
+    """Optional per-feature scale of the activation, fp32 [E, F]: 1 + 0.25 N(0,1)."""
+    return (1.0 + 0.25 * _rng(cfg.seed, 7).standard_normal((cfg.E, cfg.F))).astype(np.float32)
+
+
 def gen_bf16_matrix(seed: int, M: int, N: int, scale: float = 1.0, outlier_rows: int = 0):
     """A standalone bf16 matrix for quantiser tests: N(0,1)*scale, with a few rows carrying
     large-magnitude outliers and exact zeros so every scale-exponent path is exercised."""

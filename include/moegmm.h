@@ -95,6 +95,10 @@ typedef struct {
   int32_t recompute;  /* 1: keep no FC1 output between forward and backward; the FC2-dgrad
                          kernel recomputes it ([NV-blog] "What's next": activation
                          recomputation). BF16 gated activations only; 0 otherwise          */
+  int32_t extras;     /* epilogue extras ([NV-blog] GLU-epilogue section: bias-vector addition
+                         and feature scaling): bit 0 FC1 bias, bit 1 per-feature scale of the
+                         activation output; used through the _ex entry points. BF16 gated,
+                         without recompute; 0 otherwise                                      */
 } moe_layer_desc_t;
 
 /* Byte offsets (from ws) of the intermediates that live in the workspace, for inspection
@@ -119,6 +123,8 @@ typedef struct {
   size_t dz;             /* bf16 [R_cap, N1] gradient of z (packed cols)                 */
   size_t dx_perm;        /* bf16 [R_cap, H] FC1 dgrad output before combine              */
   size_t dprob_part;     /* fp32 [R_cap, ceil(F/128)] per-column-tile partial d_prob     */
+  size_t ext_part;       /* fp32 [R_cap/32, N1 + F] per-32-row column sums of dZ and of
+                            p * dA_s * a (extras only; SIZE_MAX otherwise)                 */
   size_t mx_base;        /* start of the MXFP8 operand copies (MXFP8 layers only)        */
 } moe_ws_layout_t;
 
@@ -169,6 +175,30 @@ moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t *desc, int32_t T, const 
                                  const void *w1_packed, const void *w2, void *dx,
                                  void *dw1_packed, void *dw2, float *d_probs, void *ws,
                                  size_t ws_bytes, moe_stream_t stream);
+
+/* Forward and backward with the epilogue extras (desc->extras; [NV-blog] GLU-epilogue
+ * section: bias-vector addition and feature scaling; the SwiGLU equation's b and c):
+ *   Z = X_e W1_e + b1_e (the bias in logical [gate | linear] column order, saved with Z),
+ *   a_s = p * s_e * act(Z)  (s the per-feature scale of the activation output);
+ *   backward: dA = p * s * dA_s, d_prob = sum_f dA_s * s * a,
+ *             d_fc1_bias_e = sum over the expert's rows of dZ,
+ *             d_feat_scale_e = sum over the expert's rows of p * dA_s * a.
+ *   fc1_bias     fp32 [E, N1] logical order (bit 0 of extras; NULL otherwise)
+ *   feat_scale   fp32 [E, F]  (bit 1; NULL otherwise)
+ *   d_fc1_bias   fp32 [E, N1] out (bit 0; NULL otherwise)
+ *   d_feat_scale fp32 [E, F]  out (bit 1; NULL otherwise)
+ * Other arguments as moe_grouped_mlp_fwd / moe_grouped_mlp_bwd, which return
+ * MOE_ERR_UNSUPPORTED for a layer with extras. The backward needs no bias (Z includes it). */
+moe_status_t moe_grouped_mlp_fwd_ex(const moe_layer_desc_t *desc, int32_t T,
+                                    const void *w1_packed, const void *w2,
+                                    const float *fc1_bias, const float *feat_scale, void *y,
+                                    void *ws, size_t ws_bytes, moe_stream_t stream);
+moe_status_t moe_grouped_mlp_bwd_ex(const moe_layer_desc_t *desc, int32_t T, const void *dy,
+                                    const void *w1_packed, const void *w2,
+                                    const float *feat_scale, void *dx, void *dw1_packed,
+                                    void *dw2, float *d_probs, float *d_fc1_bias,
+                                    float *d_feat_scale, void *ws, size_t ws_bytes,
+                                    moe_stream_t stream);
 
 /* Route + permute without any device allocation and without a workspace. The pages have no
  * counterpart of this entry point; it exists for callers that cannot call cudaMalloc, such as
@@ -262,7 +292,8 @@ typedef enum {
   MOE_K_GEMM_FC1_WGRAD = 12,
   MOE_K_MXFP8_QUANTIZE = 13,
   MOE_K_PACK_FC1 = 14,
-  MOE_K_COUNT = 15
+  MOE_K_EXTRAS_REDUCE = 15,
+  MOE_K_COUNT = 16
 } moe_kernel_id_t;
 
 /* Launch timeline, for measurement. Between moe_timeline_begin and moe_timeline_end the

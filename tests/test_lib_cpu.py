@@ -42,9 +42,9 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_desc_struct_layout_matches_header(lib):
-    # 16 four-byte fields, no padding
-    assert ctypes.sizeof(g.LayerDesc) == 64
-    assert ctypes.sizeof(g.WsLayout) == 16 * 8
+    # 17 four-byte fields, no padding
+    assert ctypes.sizeof(g.LayerDesc) == 68
+    assert ctypes.sizeof(g.WsLayout) == 17 * 8
 
 
 def _desc(**kw):
@@ -86,6 +86,8 @@ def test_recompute_keeps_no_z_in_the_workspace(lib):
     (dict(precision="mxfp8"), 2), (dict(precision="mxfp8", align=128, ilv=128), 2),
     (dict(recompute=2), 1), (dict(recompute=1, precision="mxfp8", align=128), 2),
     (dict(recompute=1, activation="srelu"), 2),
+    (dict(extras=4), 1), (dict(extras=1, activation="srelu"), 2),
+    (dict(extras=3, precision="mxfp8", align=128), 2), (dict(extras=1, recompute=1), 2),
 ])
 def test_invalid_descriptions_rejected(lib, kw, status):
     d = _desc(**kw)

@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <set>
 #include <string>
 
 #include "kernels.cuh"
@@ -39,6 +40,19 @@ static moe_status_t fail(moe_status_t st, const char* fmt, ...) {
 }
 
 void set_last_error(const char* msg) { g_last_error = msg; }
+
+cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({kernel, dev})) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({kernel, dev});
+  return e;
+}
 
 static moe_status_t cuda_fail(cudaError_t e, const char* where) {
   return fail(MOE_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));

@@ -580,12 +580,8 @@ template <int BN, int STAGES, bool A_MN, bool B_MN, int EPI, bool KG, bool B3D, 
 cudaError_t launch_instance(const GemmArgs& a, int grid, cudaStream_t s, int kid) {
   auto kern = grouped_gemm_kernel<BN, STAGES, A_MN, B_MN, EPI, KG, B3D, EXT>;
   constexpr int smem = Smem<BN, STAGES>::TOTAL;
-  static bool configured = false;  // per instantiation; attribute is per-function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, smem, s>>>(a);
   count_launch(s, kid);
   return cudaGetLastError();

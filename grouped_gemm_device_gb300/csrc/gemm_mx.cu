@@ -619,13 +619,8 @@ bool tmap_fp8(CUtensorMap* m, const MxOperand& t, bool mn_major) {
 template <int EPI, int KIND, bool KG, int ILV, bool A_MN, bool B_MN>
 cudaError_t launch_mx(const MxArgs& a, int grid, cudaStream_t s, int kid) {
   auto kern = grouped_gemm_mx_kernel<EPI, KIND, KG, ILV, A_MN, B_MN>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, MxSmem<EPI>::TOTAL);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), MxSmem<EPI>::TOTAL);
+  if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, MxSmem<EPI>::TOTAL, s>>>(a);
   count_launch(s, kid);
   return cudaGetLastError();

@@ -315,13 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int KIND>
 cudaError_t launch_kind(const RcArgs& a, int grid, cudaStream_t s) {
   auto kern = fc2_dgrad_recompute_kernel<KIND>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TOTAL);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), SMEM_TOTAL);
+  if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, SMEM_TOTAL, s>>>(a);
   count_launch(s, MOE_K_GEMM_FC2_DGRAD);
   return cudaGetLastError();

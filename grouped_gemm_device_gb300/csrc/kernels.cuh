@@ -31,6 +31,10 @@ __global__ void pack_fc1_kernel(const uint16_t* src, uint16_t* dst, int E, int H
 __global__ void group_colsum_kernel(const float* part, int ld, int col0, int ncols,
                                     const int32_t* offsets, float* out);
 
+// Sets a kernel's dynamic shared-memory limit once per (kernel, device); thread-safe. The
+// attribute belongs to the device's context, so a process driving several GPUs sets it on each.
+cudaError_t ensure_smem_attr(const void* kernel, int bytes);
+
 // mxfp8.cu
 // Sizes the quantiser's 32-bit tile indexing covers (M rows < 2^31, tile count < 2^31).
 bool mxfp8_quantize_size_ok(int64_t M, int64_t N);

@@ -224,13 +224,8 @@ static void launch(MxQuantArgs a, int num_sms, cudaStream_t s) {
   if (tiles == 0) return;
   a.wide = (!a.rowwise || aligned32(a.q_row)) && (!a.colwise || aligned32(a.q_col)) &&
            a.N % 32 == 0;
-  static bool configured = false;
-  if (!configured) {
-    // on failure the launch below fails too and the caller reports the CUDA error
-    configured = cudaFuncSetAttribute(mxfp8_quantize_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      QT_SMEM) == cudaSuccess;
-  }
+  // on failure the launch below fails too and the caller reports the CUDA error
+  ensure_smem_attr(reinterpret_cast<const void*>(mxfp8_quantize_kernel), QT_SMEM);
   const int grid = (int)std::min<int64_t>(tiles, (int64_t)num_sms * 2);
   mxfp8_quantize_kernel<<<grid, QT_THREADS, QT_SMEM, s>>>(a);
   count_launch(s, MOE_K_MXFP8_QUANTIZE);

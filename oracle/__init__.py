@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the fused grouped expert MLP (forward + backward, BF16 and MXFP8).
+"""fp64 CPU oracle for the fused grouped expert MLP (forward + backward, BF16, MXFP8, NVFP4).
 
 TEST INFRASTRUCTURE ONLY. Only the test-suite, the smoke check and the benchmark's CPU
 baseline leg may import this package. The product (the CUDA library and its Python binding)
@@ -15,10 +15,15 @@ Sources (cited by page title and section):
              semantics, the MXFP8 format (Challenge 2, Figure 3), ScaledSwiGLU routing-weight
              scaling and the fused GroupedLinear -> ScaledSwiGLU -> GroupedLinear op
              (Challenge 3, Figure 4).
+  [MoE-summary] setupai.cc summary page "Boosting MoE Training Throughput with Advanced
+             Fusion Kernels" (zh-hant): the NVIDIA hardware list (Blackwell: NVFP4).
 
 Modules:
   oracle.mxfp8 - E4M3 encoding, E8M0 block scales, MXFP8 quantise / dequantise.
-  oracle.moe   - routing, permutation maps, activations, grouped forward and backward.
+  oracle.nvfp4 - E2M1 encoding, E4M3 block scales, per-tensor scale, NVFP4 quantise /
+                 dequantise, the 16-point random Hadamard rotation.
+  oracle.moe   - routing, permutation maps, activations, grouped forward and backward
+                 (BF16 / MXFP8 per expert; NVFP4 stage by stage, layer_nvfp4).
 
 Every function here is pinned by a CPU test against something other than itself (closed
 forms, finite differences, torch autograd in fp64, brute force, exhaustive enumeration, or

@@ -332,3 +332,123 @@ def layer(logits, x, W1, W2, k: int, act: ActParams, mx: bool = False, align: in
 
 def stack_weight_grads(res: LayerResult, E: int):
     return np.stack([res.dW1[e] for e in range(E)]), np.stack([res.dW2[e] for e in range(E)])
+
+
+# ----------------------------------------------------------------------------- NVFP4 layer
+
+
+def bf16_round(v: np.ndarray) -> np.ndarray:
+    """Round to fp32 and then to the nearest bf16 (ties to even), the kernels' order of
+    conversions for a value held in fp32; returned as fp64."""
+    u = np.asarray(v, dtype=np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return bf16_to_f64(u.astype(np.uint16))
+
+
+@dataclass
+class Nvfp4Result:
+    ids: np.ndarray
+    probs: np.ndarray
+    perm: Permutation
+    y: np.ndarray
+    amax: dict                                   # per-tensor amax of every NVFP4 copy
+    dx: np.ndarray | None = None
+    dW1: np.ndarray | None = None                # [E, H, N1] logical
+    dW2: np.ndarray | None = None                # [E, F, H]
+    d_probs: np.ndarray | None = None
+    Z: list = field(default_factory=list)        # per expert: FC1 output, bf16-rounded
+    A: list = field(default_factory=list)        # per expert: a_s, bf16-rounded
+    dZ: list = field(default_factory=list)       # per expert: dZ, bf16-rounded
+
+
+def layer_nvfp4(logits, x, W1, W2, k: int, act: ActParams, mask: int, dy=None,
+                align: int = 128) -> Nvfp4Result:
+    """Forward (and, with dy, backward) of the expert layer with NVFP4 GEMM operands.
+
+    The same layer as `layer` (R1-R9), with every GEMM consuming NVFP4 copies of its operands
+    (oracle.nvfp4, readings N1-N6) blocked along its reduction dimension, and with the BF16
+    tensors that the fused kernels emit ([NV-blog] section "fused MXFP8 and NVFP4
+    quantisation") rounded to bf16 where the pipeline stores them:
+      forward:  Z = Q(X) Q_H(W1)            saved in bf16 (the backward reads the saved Z)
+                a_s = bf16(p * act(Z))      the FC1 kernel's BF16 output, with amax(a_s)
+                Y = Q(a_s) Q_F(W2)
+      backward: dA_s = Q(dY) Q_H(W2)^T, d_prob = sum_f dA_s * a,
+                dZ = bf16(dact(bf16 Z, p * dA_s))   the FC2-dgrad kernel's BF16 output, with
+                                            the amax of its Hadamard-rotated transpose
+                dX = Q(dZ) Q_N1(W1)^T
+                dW2 = Q_rows(RHT(a_s))^T Q_rows(RHT(dY)),  dW1 = Q_rows(RHT(dZ))^T Q_rows(RHT(X))
+    Q(.) quantises along the row (the reduction dimension of the row-grouped GEMMs) with its
+    tensor's encode scale; Q_rows(RHT(.)) rotates each expert's rows in blocks of 16 from the
+    expert's first row (zero rows pad the last block) and quantises down the columns. Every
+    per-tensor amax is taken over the whole tensor (all experts). Weights: W1 [E, H, N1]
+    logical, W2 [E, F, H]; W1's amax is shared by its two copies, W2's likewise.
+    """
+    from . import nvfp4 as nv
+
+    lg = np.asarray(logits, dtype=np.float32)
+    T, E = lg.shape
+    ids, probs = route(lg, k)
+    perm = permutation(ids, E, align)
+    H = x.shape[1]
+    F = W2.shape[1]
+    segs = perm.rows_of_expert
+    Xs = [x[tok] for tok, _ in segs]
+    Ps = [probs[tok, slot] for tok, slot in segs]
+    am = {"x": nv.amax(x), "w1": nv.amax(W1), "w2": nv.amax(W2)}
+    S = lambda name: nv.encode_scale(am[name])  # noqa: E731
+    xq = nv.fake_quant(x, 1, S("x")) if T else x
+    y = np.zeros((T, H))
+    res = Nvfp4Result(ids, probs, perm, y, am)
+    acts = []
+    for e in range(E):
+        tok, _ = segs[e]
+        Ze = xq[tok] @ nv.fake_quant(W1[e], 0, S("w1"))
+        ae = act_forward(act, Ze[:, :F], Ze[:, F:]) if act.gated else act_forward(act, Ze)
+        acts.append(ae)
+        res.Z.append(bf16_round(Ze))
+        res.A.append(bf16_round(Ps[e][:, None] * ae))
+    am["a"] = max([nv.amax(a) for a in res.A] + [0.0])
+    am["at"] = nv.rht_amax_segments(res.A, mask)
+    for e in range(E):
+        tok, _ = segs[e]
+        if len(tok):
+            Ye = nv.fake_quant(res.A[e], 1, S("a")) @ nv.fake_quant(W2[e], 0, S("w2"))
+            np.add.at(y, tok, Ye)
+    if dy is None:
+        return res
+    dy = np.asarray(dy, dtype=np.float64)
+    DYs = [dy[tok] for tok, _ in segs]
+    am["dy"] = nv.amax(dy)
+    am["dyt"] = nv.rht_amax_segments(DYs, mask)
+    am["xt"] = nv.rht_amax_segments(Xs, mask)
+    dyq = nv.fake_quant(dy, 1, S("dy")) if T else dy
+    res.dx = np.zeros((T, H))
+    res.d_probs = np.zeros((T, k))
+    res.dW1 = np.zeros((E,) + W1.shape[1:])
+    res.dW2 = np.zeros((E,) + W2.shape[1:])
+    for e in range(E):
+        tok, slot = segs[e]
+        dA_s = dyq[tok] @ nv.fake_quant(W2[e], 1, S("w2")).T
+        res.d_probs[tok, slot] = (dA_s * acts[e]).sum(axis=1)
+        dA = Ps[e][:, None] * dA_s
+        Zb = res.Z[e]
+        if act.gated:
+            dg, dl = act_backward(act, Zb[:, :F], Zb[:, F:], dA)
+            dZe = np.concatenate([dg, dl], axis=1)
+        else:
+            dZe, _ = act_backward(act, Zb, None, dA)
+        res.dZ.append(bf16_round(dZe))
+    am["dz"] = max([nv.amax(d) for d in res.dZ] + [0.0])
+    am["dzt"] = nv.rht_amax_segments(res.dZ, mask)
+    at_q = nv.colwise_rht_segments(res.A, mask, S("at"))
+    dyt_q = nv.colwise_rht_segments(DYs, mask, S("dyt"))
+    dzt_q = nv.colwise_rht_segments(res.dZ, mask, S("dzt"))
+    xt_q = nv.colwise_rht_segments(Xs, mask, S("xt"))
+    for e in range(E):
+        tok, _ = segs[e]
+        if len(tok):
+            dXe = nv.fake_quant(res.dZ[e], 1, S("dz")) @ nv.fake_quant(W1[e], 1, S("w1")).T
+            np.add.at(res.dx, tok, dXe)
+        res.dW2[e] = at_q[e].T @ dyt_q[e]
+        res.dW1[e] = xt_q[e].T @ dzt_q[e]
+    return res

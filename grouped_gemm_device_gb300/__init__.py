@@ -16,7 +16,7 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libmoegmm.so")
 
-PREC = {"bf16": 0, "mxfp8": 1}
+PREC = {"bf16": 0, "mxfp8": 1, "nvfp4": 2}
 ACT = {"swiglu": 0, "clamped_swiglu": 1, "geglu": 2, "srelu": 3}
 EXTRA_BIAS, EXTRA_SCALE = 1, 2  # moe_layer_desc_t.extras bits
 DEVERR = {0: "none", 1: "capacity", 2: "timeout", 3: "bad_id"}
@@ -24,13 +24,15 @@ DEVERR = {0: "none", 1: "capacity", 2: "timeout", 3: "bad_id"}
 KERNEL_NAMES = ("route_topk", "assign_rows", "gather_x", "gemm_fc1_fprop", "gemm_fc2_fprop",
                 "combine_y", "gather_dy", "gemm_fc2_dgrad", "dprob_reduce", "gemm_fc2_wgrad",
                 "gemm_fc1_dgrad", "combine_dx", "gemm_fc1_wgrad", "mxfp8_quantize", "pack_fc1",
-                "extras_reduce")
+                "extras_reduce", "nvfp4_amax", "nvfp4_quantize")
+# moe_ws_layout_t.nv_amax slots (fp32 [16], first 10 used)
+NV_AMAX = ("x", "xt", "w1", "w2", "a", "at", "dy", "dyt", "dz", "dzt")
 
 EXPORTS = ("moe_timeline_begin", "moe_timeline_end", "moe_workspace_size", "moe_workspace_layout", "moe_route_permute",
            "moe_grouped_mlp_fwd", "moe_grouped_mlp_bwd", "mxfp8_quantize", "moe_pack_fc1_weight",
            "moe_get_error", "moe_clear_error", "moe_gemm_ctas", "moe_launch_count",
            "moe_last_error_string", "moe_selftest_wait_timeout", "moe_grouped_mlp_fwd_ex",
-           "moe_grouped_mlp_bwd_ex")
+           "moe_grouped_mlp_bwd_ex", "nvfp4_amax", "nvfp4_quantize")
 
 
 class LayerDesc(ctypes.Structure):
@@ -40,7 +42,8 @@ class LayerDesc(ctypes.Structure):
                 ("gate_max", ctypes.c_float), ("lin_lo", ctypes.c_float),
                 ("lin_hi", ctypes.c_float), ("lin_offset", ctypes.c_float),
                 ("sm_margin", ctypes.c_int32), ("ilv", ctypes.c_int32), ("align", ctypes.c_int32),
-                ("recompute", ctypes.c_int32), ("extras", ctypes.c_int32)]
+                ("recompute", ctypes.c_int32), ("extras", ctypes.c_int32),
+                ("rht_mask", ctypes.c_uint32)]
 
 
 class WsLayout(ctypes.Structure):
@@ -51,7 +54,8 @@ class WsLayout(ctypes.Structure):
                 ("y_perm", ctypes.c_size_t), ("dy_perm", ctypes.c_size_t),
                 ("dz", ctypes.c_size_t), ("dx_perm", ctypes.c_size_t),
                 ("dprob_part", ctypes.c_size_t), ("ext_part", ctypes.c_size_t),
-                ("mx_base", ctypes.c_size_t)]
+                ("mx_base", ctypes.c_size_t), ("nv_amax", ctypes.c_size_t),
+                ("nv_base", ctypes.c_size_t)]
 
 
 _lib = None
@@ -78,6 +82,9 @@ def load():
         "moe_grouped_mlp_fwd": (_I32, [_DP, _I32, _P, _P, _P, _P, _SZ, _P]),
         "moe_grouped_mlp_bwd": (_I32, [_DP, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
         "mxfp8_quantize": (_I32, [_P, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P]),
+        "nvfp4_amax": (_I32, [_P, _I64, _I64, ctypes.c_uint32, _P, _P, _P]),
+        "nvfp4_quantize": (_I32, [_P, _I64, _I64, _P, _P, _I32, ctypes.c_uint32, _P, _P, _P, _P,
+                                  _P]),
         "moe_pack_fc1_weight": (_I32, [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P]),
         "moe_get_error": (_I32, [_DP, _P, ctypes.POINTER(_I32), _P]),
         "moe_clear_error": (_I32, [_DP, _P, _P]),
@@ -130,18 +137,26 @@ def _stream(stream) -> int | None:
 
 def make_desc(E, k, H, F, T_max, precision="bf16", activation="swiglu", beta=1.0,
               gate_max=math.inf, lin_lo=-math.inf, lin_hi=math.inf, lin_offset=0.0,
-              sm_margin=0, ilv=64, align=32, recompute=False, extras=0) -> LayerDesc:
-    """extras: bit 0 FC1 bias, bit 1 feature scale (EXTRA_BIAS | EXTRA_SCALE)."""
+              sm_margin=0, ilv=64, align=32, recompute=False, extras=0,
+              rht_mask=0) -> LayerDesc:
+    """extras: bit 0 FC1 bias, bit 1 feature scale (EXTRA_BIAS | EXTRA_SCALE). rht_mask: the
+    16 signs of the NVFP4 weight-gradient rotation (bit j set: row j of a block negated)."""
     return LayerDesc(E, k, H, F, T_max, PREC[precision], ACT[activation], beta, gate_max,
                      lin_lo, lin_hi, lin_offset, sm_margin, ilv, align, int(recompute),
-                     int(extras))
+                     int(extras), int(rht_mask) & 0xFFFF)
 
 
-def desc_from_config(cfg, T_max=None, sm_margin=0, recompute=False, extras=0) -> LayerDesc:
+def desc_from_config(cfg, T_max=None, sm_margin=0, recompute=False, extras=0,
+                     rht_mask=None) -> LayerDesc:
+    """A description of a synthetic workload (synth.LayerConfig); an NVFP4 layer takes the
+    workload's seeded rotation signs unless rht_mask is given."""
+    if rht_mask is None:
+        from . import synth
+        rht_mask = synth.gen_rht_mask(cfg) if cfg.precision == "nvfp4" else 0
     return make_desc(cfg.E, cfg.k, cfg.H, cfg.F, cfg.T if T_max is None else T_max,
                      cfg.precision, cfg.activation, cfg.beta, cfg.gate_max, cfg.lin_lo,
                      cfg.lin_hi, cfg.lin_offset, sm_margin, cfg.ilv, cfg.align, recompute,
-                     extras)
+                     extras, rht_mask)
 
 
 # ------------------------------------------------------------------ C ABI, same names
@@ -206,6 +221,18 @@ def mxfp8_quantize(inp, M, N, rowwise, colwise, q_row=None, s_row=None, q_col=No
                    stream=None):
     _check(load().mxfp8_quantize(_ptr(inp), M, N, int(rowwise), int(colwise), _ptr(q_row),
                                  _ptr(s_row), _ptr(q_col), _ptr(s_col), _stream(stream)))
+
+
+def nvfp4_amax(inp, M, N, sign_mask, amax, amax_rht=None, stream=None):
+    _check(load().nvfp4_amax(_ptr(inp), M, N, int(sign_mask) & 0xFFFF, _ptr(amax),
+                             _ptr(amax_rht), _stream(stream)))
+
+
+def nvfp4_quantize(inp, M, N, amax_row, amax_col, rht, sign_mask, q_row=None, s_row=None,
+                   q_col=None, s_col=None, stream=None):
+    _check(load().nvfp4_quantize(_ptr(inp), M, N, _ptr(amax_row), _ptr(amax_col), int(rht),
+                                 int(sign_mask) & 0xFFFF, _ptr(q_row), _ptr(s_row), _ptr(q_col),
+                                 _ptr(s_col), _stream(stream)))
 
 
 def moe_pack_fc1_weight(src, dst, E, H, F, gated, ilv, inverse, stream=None):

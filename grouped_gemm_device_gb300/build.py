@@ -13,7 +13,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libmoegmm.so")
-SOURCES = ["api.cu", "route.cu", "mxfp8.cu", "gemm.cu", "gemm_mx.cu", "gemm_rc.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "route.cu", "mxfp8.cu", "gemm.cu", "gemm_mx.cu", "gemm_rc.cu", "noalloc.cu",
+           "nvfp4.cu", "gemm_fp4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -10,6 +10,7 @@
 #include <string>
 
 #include "kernels.cuh"
+#include "nvfp4.cuh"
 
 namespace moe {
 
@@ -73,8 +74,8 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 static int64_t r_cap(const moe_layer_desc_t* d) {
   const int64_t r = (int64_t)d->T_max * d->k + (int64_t)d->E * (d->align - 1);
-  // MXFP8: every permuted buffer spans whole 128-row scale slabs
-  return d->precision == MOE_PREC_MXFP8 ? (r + 127) / 128 * 128 : r;
+  // MXFP8 / NVFP4: every permuted buffer spans whole 128-row scale slabs
+  return d->precision != MOE_PREC_BF16 ? (r + 127) / 128 * 128 : r;
 }
 static int64_t round128(int64_t v) { return (v + 127) / 128 * 128; }
 static int n1_of(const moe_layer_desc_t* d) {
@@ -97,8 +98,13 @@ static moe_status_t validate_desc(const moe_layer_desc_t* d) {
   if (d->precision == MOE_PREC_MXFP8 && d->activation != MOE_ACT_SRELU && d->ilv != 32 &&
       d->ilv != 64)
     return fail(MOE_ERR_UNSUPPORTED, "MXFP8 layers need ilv = 32 or 64");
-  if (d->precision != MOE_PREC_BF16 && d->precision != MOE_PREC_MXFP8)
+  if (d->precision != MOE_PREC_BF16 && d->precision != MOE_PREC_MXFP8 &&
+      d->precision != MOE_PREC_NVFP4)
     return fail(MOE_ERR_INVALID_ARG, "unknown precision %d", d->precision);
+  if (d->precision == MOE_PREC_NVFP4 && d->align != 128)
+    return fail(MOE_ERR_UNSUPPORTED, "NVFP4 layers need align = 128 (whole scale slabs)");
+  if (d->precision == MOE_PREC_NVFP4 && d->activation != MOE_ACT_SRELU && d->ilv != 64)
+    return fail(MOE_ERR_UNSUPPORTED, "NVFP4 layers need ilv = 64");
   if (d->activation < MOE_ACT_SWIGLU || d->activation > MOE_ACT_SRELU)
     return fail(MOE_ERR_INVALID_ARG, "unknown activation %d", d->activation);
   if (d->activation != MOE_ACT_SRELU) {
@@ -117,9 +123,9 @@ static moe_status_t validate_desc(const moe_layer_desc_t* d) {
     return fail(MOE_ERR_UNSUPPORTED,
                 "epilogue extras need a BF16 layer with a gated activation, no recompute");
   if (r_cap(d) > (int64_t)INT32_MAX / 2) return fail(MOE_ERR_UNSUPPORTED, "row capacity too large");
-  if (d->precision == MOE_PREC_MXFP8 &&
+  if (d->precision != MOE_PREC_BF16 &&
       (int64_t)d->E * round128(n1_of(d)) * d->H > (int64_t)INT32_MAX * 8)
-    return fail(MOE_ERR_UNSUPPORTED, "MXFP8 weight copies too large");
+    return fail(MOE_ERR_UNSUPPORTED, "block-scaled weight copies too large");
   return MOE_OK;
 }
 
@@ -171,12 +177,47 @@ static size_t mx_ops(const moe_layer_desc_t* d, int64_t R, uint8_t* base, size_t
   return o;
 }
 
+// The NVFP4 operand copies, in order after nv_base: the same twelve operands as MXFP8, each
+// K-major: packed E2M1 codes [rows, cols / 2] and E4M3 scales in the slab layout (16-value
+// blocks), with the transposed copies holding rows = features and cols = the reduction
+// (tokens for the weight-gradient operands, the weight's other dimension otherwise).
+static size_t nv_ops(const moe_layer_desc_t* d, int64_t R, uint8_t* base, size_t o, MxOps& m) {
+  const int64_t H = d->H, F = d->F, N1 = n1_of(d), E = d->E;
+  m.N1p = (int)round128(N1);
+  m.Fp = (int)round128(F);
+  auto op = [&](MxOperand& t, int64_t rows, int64_t cols) {
+    t.rows = rows;
+    t.cols = cols;
+    t.s_pad = round128(rows);
+    t.q = base + o;
+    o = up256(o + (size_t)(rows * cols / 2));
+    t.s = base + o;
+    o = up256(o + (size_t)nvfp4_sf_bytes(rows, cols));
+  };
+  op(m.x, R, H);
+  op(m.xt, H, R);
+  op(m.a, R, F);
+  op(m.at, F, R);
+  op(m.dy, R, H);
+  op(m.dyt, H, R);
+  op(m.dz, R, N1);
+  op(m.dzt, N1, R);
+  op(m.w1, E * m.N1p, H);
+  op(m.w1t, H, E * m.N1p);
+  op(m.w2, E * m.Fp, H);
+  op(m.w2t, H, E * m.Fp);
+  return o;
+}
+
 static void compute_layout(const moe_layer_desc_t* d, moe_ws_layout_t* L) {
   const int64_t R = r_cap(d);
   const int64_t H = d->H, F = d->F, N1 = n1_of(d), E = d->E;
   const bool mx = d->precision == MOE_PREC_MXFP8;
+  const bool nv = d->precision == MOE_PREC_NVFP4;
   const int64_t nparts = mx ? dprob_parts_mx((int)F)
-                            : (d->recompute ? dprob_parts_recompute((int)F) : dprob_parts((int)F));
+                         : nv ? dprob_parts_fp4((int)F)
+                              : (d->recompute ? dprob_parts_recompute((int)F)
+                                              : dprob_parts((int)F));
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -204,6 +245,14 @@ static void compute_layout(const moe_layer_desc_t* d, moe_ws_layout_t* L) {
     MxOps m;
     L->mx_base = o;
     o = mx_ops(d, R, nullptr, o, m);
+  }
+  L->nv_amax = SIZE_MAX;
+  L->nv_base = SIZE_MAX;
+  if (nv) {
+    MxOps m;
+    L->nv_amax = take(16 * sizeof(float));
+    L->nv_base = o;
+    o = nv_ops(d, R, nullptr, o, m);
   }
   L->total = o;
 }
@@ -297,6 +346,61 @@ static MxProblem mx_problem(const moe_layer_desc_t* d, const Ws& w) {
   return p;
 }
 
+static Fp4Problem fp4_problem(const moe_layer_desc_t* d, const Ws& w) {
+  Fp4Problem p;
+  memset(&p, 0, sizeof(p));
+  MxOps m;
+  nv_ops(d, w.L.R_cap, w.base, w.L.nv_base, m);
+  p.E = d->E;
+  p.H = d->H;
+  p.F = d->F;
+  p.N1 = n1_of(d);
+  p.N1p = m.N1p;
+  p.Fp = m.Fp;
+  p.R_cap = w.L.R_cap;
+  p.offsets = w.at<int32_t>(w.L.offsets);
+  p.x = m.x; p.xt = m.xt; p.a = m.a; p.at = m.at; p.dy = m.dy; p.dyt = m.dyt;
+  p.dz = m.dz; p.dzt = m.dzt; p.w1 = m.w1; p.w1t = m.w1t; p.w2 = m.w2; p.w2t = m.w2t;
+  p.amax = w.at<float>(w.L.nv_amax);
+  p.row_prob = w.at<float>(w.L.row_prob);
+  p.z = w.at<void>(w.L.z);
+  p.gated = d->activation != MOE_ACT_SRELU;
+  p.ilv = d->ilv;
+  p.rht_mask = d->rht_mask & 0xFFFFu;
+  p.act = act_of(d);
+  p.err = w.at<int>(w.L.err);
+  p.num_ctas = gemm_ctas(d);
+  return p;
+}
+
+// NVFP4 copies of a bf16 matrix [M, N] (input row groups G stored at stride Gp; rows at or
+// beyond *row_limit zero when given): the row-wise copy `row` with the encode scale of
+// amax[row_slot] and the transposed copy `col` with that of amax[col_slot], rotated when rht.
+static void nv_quantize(const void* in, int64_t M, int64_t N, int64_t G, int64_t Gp,
+                        const int32_t* row_limit, const Fp4Problem& p, int row_slot,
+                        int col_slot, const MxOperand& row, const MxOperand& col, int rht,
+                        cudaStream_t s) {
+  Nvfp4QuantArgs a;
+  memset(&a, 0, sizeof(a));
+  a.in = in;
+  a.M = M;
+  a.N = N;
+  a.G = G;
+  a.Gp = Gp;
+  a.row_limit = row_limit;
+  a.amax_row = p.amax + row_slot;
+  a.amax_col = p.amax + col_slot;
+  a.q_row = row.q;
+  a.s_row = row.s;
+  a.s_row_pad = row.s_pad;
+  a.q_col = col.q;
+  a.s_col = col.s;
+  a.s_col_pad = col.s_pad;
+  a.rht = rht;
+  a.rht_mask = p.rht_mask;
+  launch_nvfp4_quantize(a, std::max(device_sms(), 1), s);
+}
+
 // Quantise a bf16 matrix [M, N] (row groups G padded to Gp) into the row-wise and the
 // column-wise MXFP8 operands of the block-scaled GEMM (both in the source's layout).
 static void mx_quantize_operands(const void* in, int64_t M, int64_t N, int64_t G, int64_t Gp,
@@ -377,6 +481,17 @@ moe_status_t moe_route_permute(const moe_layer_desc_t* d, int32_t T, const float
     mx_quantize_operands(w.at<void>(w.L.x_perm), w.L.R_cap, d->H, w.L.R_cap, w.L.R_cap, m.x,
                          m.xt, s);
   }
+  if (d->precision == MOE_PREC_NVFP4) {
+    // X's amax and rotated amax, then its copies: along H for FC1 and transposed, rotated
+    // along the expert's rows, for the FC1 weight gradient
+    const Fp4Problem p = fp4_problem(d, w);
+    e = cudaMemsetAsync(p.amax + AM_X, 0, 2 * sizeof(float), s);
+    if (e != cudaSuccess) return cuda_fail(e, "memset amax");
+    launch_nvfp4_rht_amax(w.at<void>(w.L.x_perm), w.L.R_cap, d->H, p.rht_mask, p.amax + AM_X,
+                          p.amax + AM_XT, s);
+    nv_quantize(w.at<void>(w.L.x_perm), w.L.R_cap, d->H, w.L.R_cap, w.L.R_cap, nullptr, p, AM_X,
+                AM_XT, p.x, p.xt, 1, s);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "route_permute launch");
   return MOE_OK;
@@ -410,6 +525,39 @@ static moe_status_t fwd_impl(const moe_layer_desc_t* d, int32_t T, const void* w
     m.role = ROLE_FC2_FPROP;
     m.out = w.at<void>(w.L.y_perm);
     if ((e = launch_grouped_gemm_mx(m, s)) != cudaSuccess) return cuda_fail(e, "FC2 MX GEMM");
+    if (T > 0) {
+      combine_rows_kernel<<<grid_for(T, 8), 256, 0, s>>>(w.at<uint4>(w.L.y_perm),
+                                                        w.at<int32_t>(w.L.row_of), T, d->k,
+                                                        d->H / 8, static_cast<uint4*>(y));
+      count_launch(s, MOE_K_COMBINE_Y);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "fwd launch");
+    return MOE_OK;
+  }
+  if (d->precision == MOE_PREC_NVFP4) {
+    Fp4Problem m = fp4_problem(d, w);
+    const int32_t* live = w.at<int32_t>(w.L.offsets) + d->E;  // rows in use
+    // BF16 master weights -> NVFP4 along both reduction directions (per-tensor amax first)
+    if ((e = cudaMemsetAsync(m.amax + AM_W1, 0, 4 * sizeof(float), s)) != cudaSuccess)
+      return cuda_fail(e, "memset amax");
+    launch_nvfp4_amax(w1_packed, (int64_t)d->E * m.N1 * d->H, m.amax + AM_W1, device_sms(), s);
+    launch_nvfp4_amax(w2, (int64_t)d->E * d->F * d->H, m.amax + AM_W2, device_sms(), s);
+    nv_quantize(w1_packed, (int64_t)d->E * m.N1p, d->H, m.N1, m.N1p, nullptr, m, AM_W1, AM_W1,
+                m.w1, m.w1t, 0, s);
+    nv_quantize(w2, (int64_t)d->E * m.Fp, d->H, d->F, m.Fp, nullptr, m, AM_W2, AM_W2, m.w2,
+                m.w2t, 0, s);
+    // FC1 + activation + probability scale, BF16 a_s plus its amax and rotated amax
+    m.role = ROLE_FC1_FPROP;
+    m.out = w.at<void>(w.L.z);
+    m.out2 = w.at<void>(w.L.a_s);
+    if ((e = launch_grouped_gemm_fp4(m, s)) != cudaSuccess) return cuda_fail(e, "FC1 FP4 GEMM");
+    nv_quantize(w.at<void>(w.L.a_s), w.L.R_cap, d->F, w.L.R_cap, w.L.R_cap, live, m, AM_A, AM_AT,
+                m.a, m.at, 1, s);
+    m.role = ROLE_FC2_FPROP;
+    m.out = w.at<void>(w.L.y_perm);
+    m.out2 = nullptr;
+    if ((e = launch_grouped_gemm_fp4(m, s)) != cudaSuccess) return cuda_fail(e, "FC2 FP4 GEMM");
     if (T > 0) {
       combine_rows_kernel<<<grid_for(T, 8), 256, 0, s>>>(w.at<uint4>(w.L.y_perm),
                                                         w.at<int32_t>(w.L.row_of), T, d->k,
@@ -505,6 +653,46 @@ static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* d
     m.role = ROLE_FC1_WGRAD;
     m.out = dw1_packed;
     if ((e = launch_grouped_gemm_mx(m, s)) != cudaSuccess) return cuda_fail(e, "FC1 wgrad MX");
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "bwd launch");
+    return MOE_OK;
+  }
+  if (d->precision == MOE_PREC_NVFP4) {
+    Fp4Problem m = fp4_problem(d, w);
+    const int32_t* live = w.at<int32_t>(w.L.offsets) + d->E;
+    if ((e = cudaMemsetAsync(m.amax + AM_DY, 0, 4 * sizeof(float), s)) != cudaSuccess)
+      return cuda_fail(e, "memset amax");
+    launch_nvfp4_rht_amax(w.at<void>(w.L.dy_perm), w.L.R_cap, d->H, m.rht_mask, m.amax + AM_DY,
+                          m.amax + AM_DYT, s);
+    nv_quantize(w.at<void>(w.L.dy_perm), w.L.R_cap, d->H, w.L.R_cap, w.L.R_cap, nullptr, m,
+                AM_DY, AM_DYT, m.dy, m.dyt, 1, s);
+    // FC2 dgrad + dActivation: BF16 dZ plus its amax and the amax of its rotated transpose
+    m.role = ROLE_FC2_DGRAD;
+    m.out = w.at<void>(w.L.dz);
+    m.dprob_part = w.at<float>(w.L.dprob_part);
+    if ((e = launch_grouped_gemm_fp4(m, s)) != cudaSuccess) return cuda_fail(e, "FC2 dgrad FP4");
+    if (T > 0) {
+      const int n = T * d->k;
+      dprob_reduce_kernel<<<grid_for((n + 255) / 256, 4), 256, 0, s>>>(
+          w.at<float>(w.L.dprob_part), dprob_parts_fp4(d->F), row_of, n, d_probs);
+      count_launch(s, MOE_K_DPROB_REDUCE);
+    }
+    nv_quantize(w.at<void>(w.L.dz), w.L.R_cap, m.N1, w.L.R_cap, w.L.R_cap, live, m, AM_DZ,
+                AM_DZT, m.dz, m.dzt, 1, s);
+    m.role = ROLE_FC2_WGRAD;
+    m.out = dw2;
+    if ((e = launch_grouped_gemm_fp4(m, s)) != cudaSuccess) return cuda_fail(e, "FC2 wgrad FP4");
+    m.role = ROLE_FC1_DGRAD;
+    m.out = w.at<void>(w.L.dx_perm);
+    if ((e = launch_grouped_gemm_fp4(m, s)) != cudaSuccess) return cuda_fail(e, "FC1 dgrad FP4");
+    if (T > 0) {
+      combine_rows_kernel<<<grid_for(T, 8), 256, 0, s>>>(w.at<uint4>(w.L.dx_perm), row_of, T,
+                                                        d->k, d->H / 8, static_cast<uint4*>(dx));
+      count_launch(s, MOE_K_COMBINE_DX);
+    }
+    m.role = ROLE_FC1_WGRAD;
+    m.out = dw1_packed;
+    if ((e = launch_grouped_gemm_fp4(m, s)) != cudaSuccess) return cuda_fail(e, "FC1 wgrad FP4");
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "bwd launch");
     return MOE_OK;
@@ -632,6 +820,71 @@ moe_status_t mxfp8_quantize(const void* in, int64_t M, int64_t N, int32_t rowwis
                         std::max(device_sms(), 1), s);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "mxfp8_quantize launch");
+  return MOE_OK;
+}
+
+moe_status_t nvfp4_amax(const void* in, int64_t M, int64_t N, uint32_t sign_mask, float* amax,
+                        float* amax_rht, moe_stream_t stream) {
+  if (M < 0 || N < 0) return fail(MOE_ERR_INVALID_ARG, "negative size");
+  if (!amax) return fail(MOE_ERR_INVALID_ARG, "amax is NULL");
+  if (N % 64) return fail(MOE_ERR_UNSUPPORTED, "N must be a multiple of 64");
+  if (amax_rht && M % 16) return fail(MOE_ERR_UNSUPPORTED, "M must be a multiple of 16");
+  if (N / 64 > 65535) return fail(MOE_ERR_UNSUPPORTED, "N too large");
+  if (M > 0 && N > 0 && (!in || !aligned16(in)))
+    return fail(MOE_ERR_INVALID_ARG, "in must be non-NULL, 16B aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), s);
+  if (e == cudaSuccess && amax_rht) e = cudaMemsetAsync(amax_rht, 0, sizeof(float), s);
+  if (e != cudaSuccess) return cuda_fail(e, "memset amax");
+  if (M > 0 && N > 0) {
+    if (amax_rht)
+      launch_nvfp4_rht_amax(in, M, N, sign_mask & 0xFFFFu, amax, amax_rht, s);
+    else
+      launch_nvfp4_amax(in, M * N, amax, device_sms(), s);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "nvfp4_amax launch");
+  return MOE_OK;
+}
+
+moe_status_t nvfp4_quantize(const void* in, int64_t M, int64_t N, const float* amax_row,
+                            const float* amax_col, int32_t rht, uint32_t sign_mask,
+                            uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                            moe_stream_t stream) {
+  const bool row = q_row || s_row, col = q_col || s_col;
+  if (!row && !col) return fail(MOE_ERR_INVALID_ARG, "neither copy requested");
+  if (!nvfp4_quantize_shape_ok(M, N))
+    return fail(MOE_ERR_UNSUPPORTED, "M must be a positive multiple of 128, N of 64");
+  if (!in || !aligned16(in)) return fail(MOE_ERR_INVALID_ARG, "in must be non-NULL, 16B aligned");
+  auto a32 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; };
+  auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if (row && (!q_row || !s_row || !amax_row || !a32(q_row) || !a4(s_row)))
+    return fail(MOE_ERR_INVALID_ARG,
+                "row-wise copy needs q_row (32B aligned), s_row (4B aligned) and amax_row");
+  if (col && (!q_col || !s_col || !amax_col || !a32(q_col) || !a4(s_col)))
+    return fail(MOE_ERR_INVALID_ARG,
+                "transposed copy needs q_col (32B aligned), s_col (4B aligned) and amax_col");
+  Nvfp4QuantArgs a;
+  memset(&a, 0, sizeof(a));
+  a.in = in;
+  a.M = M;
+  a.N = N;
+  a.G = M;
+  a.Gp = M;
+  a.amax_row = amax_row;
+  a.amax_col = amax_col;
+  a.q_row = row ? q_row : nullptr;
+  a.s_row = s_row;
+  a.s_row_pad = M;
+  a.q_col = col ? q_col : nullptr;
+  a.s_col = s_col;
+  a.s_col_pad = round128(N);
+  a.rht = rht ? 1 : 0;
+  a.rht_mask = sign_mask & 0xFFFFu;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  launch_nvfp4_quantize(a, std::max(device_sms(), 1), s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "nvfp4_quantize launch");
   return MOE_OK;
 }
 

@@ -129,4 +129,70 @@ struct MxProblem {
 int dprob_parts_mx(int F);
 cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s);
 
+// nvfp4.cu --------------------------------------------------------------------------------
+// NVFP4 quantiser arguments: in bf16 [G-row groups of the input, N]; output rows M = groups *
+// Gp (padding rows zero), rows at or beyond *row_limit (when given) zero. Row-wise copy
+// q_row [M, N/2] + s_row (slab layout, rows padded to s_row_pad); transposed copy q_col
+// [N, M/2] + s_col (rows N padded to s_col_pad), rotated along M when rht. NULL q_row / q_col
+// skips that copy. amax_* are device pointers to the per-tensor amax of each copy.
+struct Nvfp4QuantArgs {
+  const void* in;
+  int64_t M, N, G, Gp;
+  const int32_t* row_limit;
+  const float* amax_row;
+  const float* amax_col;
+  uint8_t* q_row;
+  uint8_t* s_row;
+  int64_t s_row_pad;
+  uint8_t* q_col;
+  uint8_t* s_col;
+  int64_t s_col_pad;
+  int rht;
+  uint32_t rht_mask;
+};
+bool nvfp4_quantize_shape_ok(int64_t M, int64_t N);  // M % 128 == 0, N % 64 == 0
+// scale bytes of an NVFP4 GEMM operand [rows, cols] in the slab layout, with the slack the
+// 256-element k-blocks and 256-row B fetches of the FP4 GEMM read past the end
+int64_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
+void launch_nvfp4_quantize(const Nvfp4QuantArgs& a, int num_sms, cudaStream_t s);
+// amax of n bf16 values (n % 8 == 0) max-merged into *out (caller zeroes it)
+void launch_nvfp4_amax(const void* in, int64_t n, float* out, int num_sms, cudaStream_t s);
+// amax and amax of the 16-row Hadamard rotation along the rows of [M, N] (M % 16 == 0,
+// N % 64 == 0), max-merged into *out and *out_rht
+void launch_nvfp4_rht_amax(const void* in, int64_t M, int64_t N, uint32_t mask, float* out,
+                           float* out_rht, cudaStream_t s);
+
+// gemm_fp4.cu -----------------------------------------------------------------------------
+// Per-tensor amax slots of an NVFP4 layer (workspace nv_amax), in the public order.
+enum Nvfp4AmaxSlot {
+  AM_X = 0, AM_XT = 1, AM_W1 = 2, AM_W2 = 3, AM_A = 4, AM_AT = 5, AM_DY = 6, AM_DYT = 7,
+  AM_DZ = 8, AM_DZT = 9, AM_COUNT = 10
+};
+
+// An NVFP4 GEMM operand reuses MxOperand: q = packed E2M1 codes [rows, cols/2] (the reduction
+// dimension cols innermost, read K-major), s = E4M3 scales in the slab layout (16-element
+// blocks), rows padded to s_pad.
+struct Fp4Problem {
+  int role;  // GemmRole
+  int E, H, F, N1, N1p, Fp;
+  int64_t R_cap;
+  const int32_t* offsets;
+  // row-wise copies (K = the row) and transposed copies (rows = features, K = tokens or the
+  // weight's other dimension); every copy is K-major
+  MxOperand x, xt, a, at, dy, dyt, dz, dzt, w1, w1t, w2, w2t;
+  float* amax;               // [AM_COUNT] per-tensor amax slots
+  const float* row_prob;
+  const void* z;             // bf16 [R_cap, N1] saved FC1 output (dGLU input)
+  void* out;                 // bf16 role output (z for FC1, y_perm, dz, dx_perm, dW2, dW1)
+  void* out2;                // FC1: bf16 a_s [R_cap, F]
+  float* dprob_part;
+  int gated, ilv;
+  uint32_t rht_mask;
+  ActDev act;
+  int* err;
+  int num_ctas;
+};
+int dprob_parts_fp4(int F);
+cudaError_t launch_grouped_gemm_fp4(const Fp4Problem& p, cudaStream_t s);
+
 }  // namespace moe

@@ -1,0 +1,184 @@
+// NVFP4 quantiser and per-tensor amax kernels (scaling rule and layouts in nvfp4.cuh).
+//
+// [NV-blog] section "fused MXFP8 and NVFP4 quantisation": the quantisation of an NVFP4 GEMM
+// operand needs the tensor's amax before any block can be encoded, so it is a second pass over
+// a BF16 tensor whose amax is already known: for the FC1 output a_s and for dZ the GEMM
+// epilogues provide it; for the routed input, dY and the weights the amax kernels below do.
+//
+// Quantiser: a CTA of 128 threads walks 128-row x 64-column tiles of a bf16 matrix, staged in
+// shared memory (144-byte rows, so that both the row reads and the column reads are free of
+// bank conflicts). Thread t then quantises
+//   row-wise    row t's 64 values (four 16-blocks along the row, the reduction dimension of
+//               the row-grouped GEMMs) into one 32-byte run and one 32-bit word of scales;
+//   transposed  column t % 64 over rows 64 * (t / 64) .. + 63 (four 16-blocks along the rows,
+//               optionally Hadamard-rotated first) into one 32-byte run of the transposed copy
+//               [N, M / 2] and one scale word: the K-major operand of the weight-gradient GEMMs.
+// Input rows are grouped (G rows per group in the input, Gp in the output, zero padding rows)
+// and optionally cut at a device-side row count (rows at or beyond it read as zero).
+#include "kernels.cuh"
+#include "nvfp4.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int QT_ROWS = 128;
+constexpr int QT_COLS = 64;
+constexpr int QT_LD = 144;  // bytes per staged row: 128 + 16
+constexpr int QT_THREADS = 128;
+
+__global__ void __launch_bounds__(QT_THREADS) nvfp4_quantize_kernel(const Nvfp4QuantArgs p) {
+  __shared__ __align__(16) uint8_t tile[QT_ROWS * QT_LD];
+  const int t = threadIdx.x;
+  const int64_t ntr = p.M / QT_ROWS, ntc = p.N / QT_COLS;
+  const int64_t ntiles = ntr * ntc;
+  const int64_t limit = p.row_limit ? (int64_t)*p.row_limit : p.M;
+  const float s_row = p.q_row ? nvfp4_encode_scale(*p.amax_row) : 0.f;
+  const float s_col = p.q_col ? nvfp4_encode_scale(*p.amax_col) : 0.f;
+  const uint16_t* in = static_cast<const uint16_t*>(p.in);
+  for (int64_t tile_i = blockIdx.x; tile_i < ntiles; tile_i += gridDim.x) {
+    const int64_t r0 = (tile_i / ntc) * QT_ROWS;
+    const int64_t c0 = (tile_i % ntc) * QT_COLS;
+    // stage: 128 rows x 8 pieces of 16 bytes; 8 consecutive threads read one row's 128 bytes
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int v = t + QT_THREADS * i;
+      const int r = v >> 3, piece = v & 7;
+      const int64_t orow = r0 + r;
+      const int64_t g = orow / p.Gp, gi = orow - g * p.Gp;
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (gi < p.G && orow < limit)
+        val = *reinterpret_cast<const uint4*>(in + (g * p.G + gi) * p.N + c0 + piece * 8);
+      *reinterpret_cast<uint4*>(tile + r * QT_LD + piece * 16) = val;
+    }
+    __syncthreads();
+    if (p.q_row) {
+      const uint8_t* src = tile + t * QT_LD;
+      uint32_t codes[8], scales = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint4 w0 = *reinterpret_cast<const uint4*>(src + 32 * b);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(src + 32 * b + 16);
+        const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          v[2 * i] = bf16_lo(w[i]);
+          v[2 * i + 1] = bf16_hi(w[i]);
+        }
+        uint32_t q[2];
+        scales |= nvfp4_quant16(v, s_row, q) << (8 * b);
+        codes[2 * b] = q[0];
+        codes[2 * b + 1] = q[1];
+      }
+      const int64_t row = r0 + t;
+      st_global_v8(p.q_row + row * (p.N / 2) + c0 / 2, codes);
+      *reinterpret_cast<uint32_t*>(p.s_row + sf_mma_offset(row, c0 / 16, p.s_row_pad)) = scales;
+    }
+    if (p.q_col) {
+      const int c = t & (QT_COLS - 1), h = t >> 6;
+      const uint8_t* src = tile + (h * 64) * QT_LD + 2 * c;
+      uint32_t codes[8], scales = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          v[i] = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(
+                                     src + (16 * b + i) * QT_LD)
+                                 << 16);
+        if (p.rht) rht16_regs(v, p.rht_mask);
+        uint32_t q[2];
+        scales |= nvfp4_quant16(v, s_col, q) << (8 * b);
+        codes[2 * b] = q[0];
+        codes[2 * b + 1] = q[1];
+      }
+      const int64_t col = c0 + c, rr = r0 + h * 64;
+      st_global_v8(p.q_col + col * (p.M / 2) + rr / 2, codes);
+      *reinterpret_cast<uint32_t*>(p.s_col + sf_mma_offset(col, rr / 16, p.s_col_pad)) = scales;
+    }
+    __syncthreads();
+  }
+}
+
+// Plain amax of n bf16 values (n a multiple of 8, 16-byte aligned).
+__global__ void __launch_bounds__(256) nvfp4_amax_kernel(const uint4* in, int64_t n8, float* out) {
+  float m = 0.f;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 w = in[i];
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(ws[j])), fabsf(bf16_hi(ws[j]))));
+  }
+  amax_flush_warp(m, out);
+}
+
+// amax and amax of the 16-row-block rotation along the rows of a bf16 [M, N] matrix (M a
+// multiple of 16, N of 64, N / 64 < 65536). A CTA of 8 warps covers 128 rows (grid x) x 64
+// columns (grid y): lane l of warp w takes columns 2l, 2l+1 of rows 16w .. 16w+15 (4-byte
+// loads, 128 contiguous bytes a warp).
+__global__ void __launch_bounds__(256) nvfp4_rht_amax_kernel(const uint16_t* in, int64_t M,
+                                                             int64_t N, uint32_t mask,
+                                                             float* out, float* out_rht) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t c = blockIdx.y * 64 + 2 * lane;
+  const int64_t r0 = blockIdx.x * 128 + w * 16;
+  float m = 0.f, mr = 0.f;
+  if (r0 < M) {
+    float a[16], b[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(in + (r0 + i) * N + c);
+      a[i] = bf16_lo(v);
+      b[i] = bf16_hi(v);
+      m = fmaxf(m, fmaxf(fabsf(a[i]), fabsf(b[i])));
+    }
+    rht16_regs(a, mask);
+    rht16_regs(b, mask);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mr = fmaxf(mr, fmaxf(fabsf(a[i]), fabsf(b[i])));
+  }
+  amax_flush_warp(m, out);
+  amax_flush_warp(mr, out_rht);
+}
+
+}  // namespace
+
+bool nvfp4_quantize_shape_ok(int64_t M, int64_t N) {
+  return M > 0 && N > 0 && M % QT_ROWS == 0 && N % QT_COLS == 0;
+}
+
+int64_t nvfp4_sf_bytes(int64_t rows, int64_t cols) {
+  // slabs of 64 elements, plus four: a 256-element k-block fetches four slabs from the one it
+  // starts in, and may start in the last; plus 1 KB for a 256-row B fetch past the end
+  const int64_t slabs = (cols + 63) / 64 + 4;
+  return slabs * ((rows + 127) / 128 * 128) * 4 + 1024;
+}
+
+void launch_nvfp4_quantize(const Nvfp4QuantArgs& a, int num_sms, cudaStream_t s) {
+  const int64_t tiles = (a.M / QT_ROWS) * (a.N / QT_COLS);
+  if (tiles <= 0) return;
+  const int grid = (int)std::min<int64_t>(tiles, (int64_t)std::max(num_sms, 1) * 8);
+  nvfp4_quantize_kernel<<<grid, QT_THREADS, 0, s>>>(a);
+  count_launch(s, MOE_K_NVFP4_QUANTIZE);
+}
+
+void launch_nvfp4_amax(const void* in, int64_t n, float* out, int num_sms, cudaStream_t s) {
+  const int64_t n8 = n / 8;
+  if (n8 <= 0) return;
+  const int grid = (int)std::min<int64_t>((n8 + 255) / 256, (int64_t)std::max(num_sms, 1) * 8);
+  nvfp4_amax_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(in), n8, out);
+  count_launch(s, MOE_K_NVFP4_AMAX);
+}
+
+void launch_nvfp4_rht_amax(const void* in, int64_t M, int64_t N, uint32_t mask, float* out,
+                           float* out_rht, cudaStream_t s) {
+  if (M <= 0 || N <= 0) return;
+  const dim3 grid((unsigned)((M + 127) / 128), (unsigned)(N / 64));
+  nvfp4_rht_amax_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(in), M, N, mask, out,
+                                             out_rht);
+  count_launch(s, MOE_K_NVFP4_AMAX);
+}
+
+}  // namespace moe

@@ -1,0 +1,112 @@
+// NVFP4 device helpers shared by the quantiser / amax kernels (nvfp4.cu) and the FP4 grouped
+// GEMM (gemm_fp4.cu).
+//
+// [NV-blog] section "fused MXFP8 and NVFP4 quantisation": for NVFP4 the fused kernels emit a
+// BF16 output plus a per-tensor amax (forward) and the amax of the Hadamard-rotated transposed
+// output (backward), so that the quantiser needs no extra pass for them. The format is the
+// published NVFP4 one: E2M1 elements, one unsigned E4M3 scale per 16 values along the
+// reduction dimension, one fp32 encode scale per tensor. Every scaling step is one IEEE fp32
+// operation, round to nearest even, in this order:
+//   S   = min(2688 / amax, FLT_MAX)           (2688 = 6 * 448; amax == 0 -> FLT_MAX)
+//   s_b = E4M3_sat(fp32(amax_b / 6) * S)
+//   q   = E2M1_sat(x * fp32(S / s_b))          (factor 0 when s_b == 0)
+// and a GEMM of two NVFP4 operands multiplies its fp32 accumulator by 1 / (S_a * S_b).
+// Scales sit in the MMA slab layout of sf_mma_offset with the k index counting 16-element
+// blocks: one 512-byte slab per 128 rows x 64 elements, exactly what one
+// tcgen05.mma.kind::mxf4nvf4 (scale_vec::4X, K = 64) consumes per 128 rows.
+//
+// Random Hadamard transform (RHT) of the weight-gradient operands: y = (1/4) H16 diag(d) x over
+// 16 consecutive token rows, H16 the Sylvester Hadamard matrix and d a +-1 vector given as a
+// 16-bit mask (bit j set: d_j = -1). Computed as four butterfly stages (pair distance 1, 2, 4,
+// 8; the lower index takes a + b, the upper a - b) and a final exact * 0.25; the register and
+// the warp-shuffle forms below perform the same fp32 operations on the same operands, so they
+// give identical results.
+#pragma once
+
+#include <cfloat>
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr float kNvfp4ScaleNum = 2688.0f;  // 6 (largest E2M1) * 448 (largest E4M3)
+
+MOE_DEVICE float nvfp4_encode_scale(float amax) {
+  return fminf(__fdiv_rn(kNvfp4ScaleNum, amax), FLT_MAX);
+}
+
+// Value of an E4M3 byte of a non-negative scale (the sign bit is 0), exact.
+MOE_DEVICE float e4m3_pos_value(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  return e == 0 ? (float)m * 0.001953125f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// Eight fp32 -> eight E2M1 codes, round to nearest even, saturating to +-6; v[0] lands in the
+// lowest nibble (element order of a packed FP4 operand).
+MOE_DEVICE uint32_t cvt_e2m1x8(const float* v) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
+// One 16-value block: its 16 E2M1 codes in q[0..1] and its E4M3 scale byte (returned).
+MOE_DEVICE uint32_t nvfp4_quant16(const float* v, float S, uint32_t (&q)[2]) {
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+  const uint32_t sb = cvt_e4m3x2(__fmul_rn(__fdiv_rn(m, 6.0f), S), 0.f) & 0xFFu;
+  const float sbf = e4m3_pos_value(sb);
+  const float enc = sbf > 0.f ? __fdiv_rn(S, sbf) : 0.f;
+  float w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = __fmul_rn(v[i], enc);
+  q[0] = cvt_e2m1x8(w);
+  q[1] = cvt_e2m1x8(w + 8);
+  return sb;
+}
+
+// RHT of 16 values held by one thread (index = row within the block).
+MOE_DEVICE void rht16_regs(float (&v)[16], uint32_t mask) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    if ((mask >> i) & 1u) v[i] = -v[i];
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i & m) continue;
+      const float a = v[i], b = v[i | m];
+      v[i] = a + b;
+      v[i | m] = a - b;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] *= 0.25f;
+}
+
+// RHT across the 16 lanes of a half-warp: lane l holds row (l & 15) of the block; returns the
+// rotated value of that row. All 32 lanes must call it.
+MOE_DEVICE float rht16_lanes(float x, uint32_t mask, int lane) {
+  float v = ((mask >> (lane & 15)) & 1u) ? -x : x;
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1) {
+    const float o = __shfl_xor_sync(0xFFFFFFFFu, v, m);
+    v = (lane & m) ? o - v : v + o;
+  }
+  return v * 0.25f;
+}
+
+// Running max of non-negative floats, merged into a global slot with one atomic per warp.
+MOE_DEVICE void amax_flush_warp(float m, float* slot) {
+  const uint32_t w = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m));
+  if ((threadIdx.x & 31) == 0 && w != 0u) atomicMax(reinterpret_cast<unsigned int*>(slot), w);
+}
+
+}  // namespace moe

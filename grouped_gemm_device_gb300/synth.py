@@ -16,6 +16,7 @@ a subset of experts can be regenerated alone for sampled checks):
             N1 = F for the non-gated squared ReLU
   W2_e    ~ 0.02*N(0,1) -> bf16 [F, H] logical       stream (seed, 3, e)
   dy      ~ N(0,1) -> bf16 [T, H]                    stream (seed, 4)
+  rht signs (NVFP4) 16 fair bits -> uint16 mask        stream (seed, 8)
 
 The workload shapes follow the Mixtral-8x7B, DeepSeek-V3 and GPT-OSS expert layers named on
 the NVIDIA blog "Boosting MoE Training Throughput with Advanced Fusion Kernels" (section on
@@ -37,7 +38,7 @@ class LayerConfig:
     k: int
     H: int
     F: int
-    precision: str = "bf16"          # "bf16" | "mxfp8"
+    precision: str = "bf16"          # "bf16" | "mxfp8" | "nvfp4"
     activation: str = "swiglu"       # swiglu | clamped_swiglu | geglu | srelu
     seed: int = 0
     zipf_s: float = 0.0              # 0 = no popularity bias
@@ -88,6 +89,10 @@ CONFIGS = {
                                **_CLAMP),
     "gptoss_mxfp8": LayerConfig("gptoss_mxfp8", T=16384, E=128, k=4, H=2880, F=2880, seed=4,
                                 precision="mxfp8", align=128, **_CLAMP),
+    "mixtral_nvfp4": LayerConfig("mixtral_nvfp4", T=16384, E=8, k=2, H=4096, F=14336,
+                                 precision="nvfp4", seed=5, align=128),
+    "gptoss_nvfp4": LayerConfig("gptoss_nvfp4", T=16384, E=128, k=4, H=2880, F=2880, seed=4,
+                                precision="nvfp4", align=128, **_CLAMP),
 }
 
 
@@ -153,6 +158,11 @@ def gen_fc1_bias(cfg: LayerConfig) -> np.ndarray:
 def gen_feat_scale(cfg: LayerConfig) -> np.ndarray:
     """Optional per-feature scale of the activation, fp32 [E, F]: 1 + 0.25 N(0,1)."""
     return (1.0 + 0.25 * _rng(cfg.seed, 7).standard_normal((cfg.E, cfg.F))).astype(np.float32)
+
+
+def gen_rht_mask(cfg: LayerConfig) -> int:
+    """The 16 random signs of the NVFP4 weight-gradient rotation, as a mask (bit j set: -1)."""
+    return int(np.dot(_rng(cfg.seed, 8).integers(0, 2, 16), 1 << np.arange(16)))
 
 
 def gen_bf16_matrix(seed: int, M: int, N: int, scale: float = 1.0, outlier_rows: int = 0):

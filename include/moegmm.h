@@ -1,7 +1,8 @@
 /*
  * moegmm.h - C ABI of the GB300 (sm_103a) fused grouped expert MLP of a Mixture-of-Experts
  * layer: routing + permutation, fused FC1 -> GLU -> probability scale -> FC2 forward, the
- * matching backward, and the standalone MXFP8 quantiser.
+ * matching backward (BF16, MXFP8 or NVFP4 GEMM operands), and the standalone MXFP8 and NVFP4
+ * quantisers.
  *
  * Sources (by page title and section):
  *   [NV-blog] NVIDIA technical blog "Boosting MoE Training Throughput with Advanced Fusion
@@ -15,6 +16,10 @@
  *             article): GroupedLinear with per-expert token counts, the per-expert loop with
  *             index_add (Challenge 1), MXFP8 format (Challenge 2, Figure 3), ScaledSwiGLU and
  *             the fused GroupedLinear -> ScaledSwiGLU -> GroupedLinear op (Challenge 3, Fig. 4).
+ *   NVFP4 is named by [NV-blog] ("fused MXFP8 and NVFP4 quantisation": the forward kernel
+ *   emits BF16 output plus a per-tensor amax, the backward kernel the amax of the
+ *   Hadamard-rotated transposed output) but not defined there; the published format is used:
+ *   E2M1 values, one unsigned E4M3 scale per 16 values, one fp32 scale per tensor (below).
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers unless a name says host. Layouts are row-major.
@@ -58,7 +63,11 @@ typedef enum {
 #define MOE_DEVERR_TIMEOUT 2    /* a bounded barrier wait in a GEMM kernel gave up       */
 #define MOE_DEVERR_BAD_ID 3     /* an expert id outside [0, E)                            */
 
-typedef enum { MOE_PREC_BF16 = 0, MOE_PREC_MXFP8 = 1 } moe_precision_t;
+/* GEMM operand precision. BF16: bf16 operands. MXFP8: E4M3 with one E8M0 scale per 32 values
+ * (see mxfp8_quantize). NVFP4: E2M1 with one E4M3 scale per 16 values and one fp32 scale per
+ * tensor (see nvfp4_quantize); the weight-gradient operands are Hadamard-rotated along the
+ * tokens first (desc.rht_mask). Outputs and the saved FC1 output are bf16 in every case. */
+typedef enum { MOE_PREC_BF16 = 0, MOE_PREC_MXFP8 = 1, MOE_PREC_NVFP4 = 2 } moe_precision_t;
 
 /* Activations of [NV-blog] (SwiGLU, GeGLU, sReLU, "with clamp and scale options"):
  *   SWIGLU          a = lin * g * sigmoid(beta*g)                  (SwiGLU equation, b=c=0)
@@ -91,7 +100,8 @@ typedef struct {
   float lin_offset;   /* clamped SwiGLU: added to the clamped linear half                */
   int32_t sm_margin;  /* SMs left free for concurrent kernels ([NV-blog] cluster margin) */
   int32_t ilv;        /* gate/linear interleave block of the packed W1 (32, 64 or 128)   */
-  int32_t align;      /* expert segment alignment in rows; must be 32                    */
+  int32_t align;      /* expert segment alignment in rows: 32, 64 or 128 (BF16); 128
+                         (MXFP8, NVFP4: segments start on 128-row scale slabs)            */
   int32_t recompute;  /* 1: keep no FC1 output between forward and backward; the FC2-dgrad
                          kernel recomputes it ([NV-blog] "What's next": activation
                          recomputation). BF16 gated activations only; 0 otherwise          */
@@ -99,6 +109,10 @@ typedef struct {
                          and feature scaling): bit 0 FC1 bias, bit 1 per-feature scale of the
                          activation output; used through the _ex entry points. BF16 gated,
                          without recompute; 0 otherwise                                      */
+  uint32_t rht_mask;  /* NVFP4: signs of the 16-point random Hadamard rotation applied along
+                         the tokens to the weight-gradient operands (bit j set: the j-th row
+                         of each 16-row block is negated before H16 / 4); drawn once by the
+                         caller. Ignored by the other precisions                             */
 } moe_layer_desc_t;
 
 /* Byte offsets (from ws) of the intermediates that live in the workspace, for inspection
@@ -126,6 +140,10 @@ typedef struct {
   size_t ext_part;       /* fp32 [R_cap/32, N1 + F] per-32-row column sums of dZ and of
                             p * dA_s * a (extras only; SIZE_MAX otherwise)                 */
   size_t mx_base;        /* start of the MXFP8 operand copies (MXFP8 layers only)        */
+  size_t nv_amax;        /* NVFP4 only: fp32 [16] per-tensor amax of each NVFP4 copy, in the
+                            order x, x^T (rotated), W1, W2, a_s, a_s^T (rotated), dY, dY^T
+                            (rotated), dZ, dZ^T (rotated); SIZE_MAX otherwise               */
+  size_t nv_base;        /* start of the NVFP4 operand copies (NVFP4 layers only)        */
 } moe_ws_layout_t;
 
 /* Workspace bytes for a layer (0 if the description is invalid). */
@@ -240,6 +258,41 @@ moe_status_t mxfp8_quantize(const void *in, int64_t M, int64_t N, int32_t rowwis
                             int32_t colwise, uint8_t *q_row, uint8_t *s_row, uint8_t *q_col,
                             uint8_t *s_col, moe_stream_t stream);
 
+/* NVFP4 per-tensor amax ([NV-blog] "fused MXFP8 and NVFP4 quantisation": the scale of an NVFP4
+ * tensor needs its amax first).
+ *   in        bf16 [M, N]
+ *   amax      fp32 [1] out: max |in|
+ *   amax_rht  fp32 [1] out (may be NULL): max |y| over y = (1/4) H16 diag(d) x for every
+ *             column and every block of 16 consecutive rows (x the block's 16 values, H16
+ *             the Sylvester Hadamard matrix, d_j = -1 where bit j of sign_mask is set)
+ * Both outputs are overwritten (the call zeroes them first). N must be a multiple of 64 (and
+ * below 64 * 65536); M a multiple of 16 when amax_rht is given. M = 0 gives 0. */
+moe_status_t nvfp4_amax(const void *in, int64_t M, int64_t N, uint32_t sign_mask, float *amax,
+                        float *amax_rht, moe_stream_t stream);
+
+/* Standalone NVFP4 quantiser. Per tensor S = min(2688 / amax, FLT_MAX) (2688 = 6 * 448); per
+ * block of 16 values s_b = E4M3(fp32(amax_b / 6) * S) (round to nearest even, saturating);
+ * per value q = E2M1(v * fp32(S / s_b)) (nearest even, saturating at +-6; factor 0 when
+ * s_b = 0). Each step is one IEEE fp32 operation. The value represented is E2M1(q) * s_b / S.
+ *   in        bf16 [M, N]
+ *   amax_row  fp32 [1] device: the amax S is computed from for the row-wise copy
+ *   amax_col  fp32 [1] device: the same for the transposed copy (the rotated amax when rht)
+ *   row-wise:    q_row  [M, N/2] bytes, two E2M1 codes a byte (even index in the low nibble),
+ *                       blocks of 16 along N;
+ *                s_row  E4M3 scales in the MMA slab layout: the scale of (row r, block j) at
+ *                       byte ((j/4) * M + perm(r)) * 4 + j%4, perm(r) = (r & ~127) |
+ *                       ((r & 31) << 2) | ((r >> 5) & 3); (N/64) * M * 4 bytes
+ *   transposed:  q_col  [N, M/2] bytes: row n holds column n of in, blocks of 16 along M,
+ *                       each block first rotated as in nvfp4_amax when rht != 0;
+ *                s_col  slab layout of (row n, block j): (M/64) * round128(N) * 4 bytes
+ * M must be a positive multiple of 128 and N of 64; q_row and q_col 32-byte aligned, s_row
+ * and s_col 4-byte aligned. q_row/s_row or q_col/s_col may both be NULL to skip that copy (its
+ * amax pointer may then be NULL). Bit-exact: the result does not depend on the launch. */
+moe_status_t nvfp4_quantize(const void *in, int64_t M, int64_t N, const float *amax_row,
+                            const float *amax_col, int32_t rht, uint32_t sign_mask,
+                            uint8_t *q_row, uint8_t *s_row, uint8_t *q_col, uint8_t *s_col,
+                            moe_stream_t stream);
+
 /* GLU weight repacking ([NV-blog] GLU-epilogue section and Figure 2: the gate and linear
  * columns are repacked so one output tile holds half a tile of each; done once, before
  * training or at checkpoint load).
@@ -293,7 +346,9 @@ typedef enum {
   MOE_K_MXFP8_QUANTIZE = 13,
   MOE_K_PACK_FC1 = 14,
   MOE_K_EXTRAS_REDUCE = 15,
-  MOE_K_COUNT = 16
+  MOE_K_NVFP4_AMAX = 16,
+  MOE_K_NVFP4_QUANTIZE = 17,
+  MOE_K_COUNT = 18
 } moe_kernel_id_t;
 
 /* Launch timeline, for measurement. Between moe_timeline_begin and moe_timeline_end the

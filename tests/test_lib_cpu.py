@@ -42,9 +42,9 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_desc_struct_layout_matches_header(lib):
-    # 17 four-byte fields, no padding
-    assert ctypes.sizeof(g.LayerDesc) == 68
-    assert ctypes.sizeof(g.WsLayout) == 17 * 8
+    # 18 four-byte fields, no padding
+    assert ctypes.sizeof(g.LayerDesc) == 72
+    assert ctypes.sizeof(g.WsLayout) == 19 * 8
 
 
 def _desc(**kw):
@@ -88,6 +88,9 @@ def test_recompute_keeps_no_z_in_the_workspace(lib):
     (dict(recompute=1, activation="srelu"), 2),
     (dict(extras=4), 1), (dict(extras=1, activation="srelu"), 2),
     (dict(extras=3, precision="mxfp8", align=128), 2), (dict(extras=1, recompute=1), 2),
+    (dict(precision="nvfp4"), 2), (dict(precision="nvfp4", align=128, ilv=32), 2),
+    (dict(precision="nvfp4", align=128, recompute=1), 2),
+    (dict(precision="nvfp4", align=128, extras=1), 2),
 ])
 def test_invalid_descriptions_rejected(lib, kw, status):
     d = _desc(**kw)
@@ -95,6 +98,45 @@ def test_invalid_descriptions_rejected(lib, kw, status):
     with pytest.raises(g.MoeError) as ei:
         g.moe_workspace_layout(d)
     assert ei.value.status == status
+
+
+def test_nvfp4_layout(lib):
+    d = _desc(precision="nvfp4", align=128, rht_mask=0x1234)
+    L = g.moe_workspace_layout(d)
+    R, H, F, N1, E = L.R_cap, 256, 512, 1024, 8
+    assert R % 128 == 0 and R >= 1000 * 2 + 8 * 127
+    assert L.mx_base == 2 ** 64 - 1 and L.nv_amax != 2 ** 64 - 1
+    assert L.a_s != 2 ** 64 - 1 and L.dz != 2 ** 64 - 1 and L.z != 2 ** 64 - 1
+    assert L.nv_amax % 256 == 0 and L.nv_base >= L.nv_amax + 16 * 4
+    # twelve operand copies at half a byte a value, each with its scales
+    values = 2 * (R * H + R * F + R * H + R * N1) + 2 * (E * N1 * H + E * F * H)
+    assert L.total - L.nv_base >= values // 2 + values // 16
+    sd = g.moe_workspace_layout(_desc(precision="nvfp4", align=128, activation="srelu", ilv=0))
+    assert sd.total < L.total
+
+
+def test_nvfp4_entry_points_validate_on_the_host(lib):
+    with pytest.raises(g.MoeError) as e:   # M not a multiple of 128
+        g.nvfp4_quantize(256, 100, 64, 256, 256, 0, 0, 256, 256, None, None, 0)
+    assert e.value.status == 2
+    with pytest.raises(g.MoeError) as e:   # N not a multiple of 64
+        g.nvfp4_quantize(256, 128, 96, 256, 256, 0, 0, 256, 256, None, None, 0)
+    assert e.value.status == 2
+    with pytest.raises(g.MoeError) as e:   # no copy requested
+        g.nvfp4_quantize(256, 128, 64, 256, 256, 0, 0, None, None, None, None, 0)
+    assert e.value.status == 1
+    with pytest.raises(g.MoeError) as e:   # q_row not 32-byte aligned
+        g.nvfp4_quantize(256, 128, 64, 256, 256, 0, 0, 272, 256, None, None, 0)
+    assert e.value.status == 1
+    with pytest.raises(g.MoeError) as e:   # transposed copy without its amax
+        g.nvfp4_quantize(256, 128, 64, 256, None, 1, 0, None, None, 256, 256, 0)
+    assert e.value.status == 1
+    with pytest.raises(g.MoeError) as e:   # rotated amax needs whole 16-row blocks
+        g.nvfp4_amax(256, 24, 64, 0, 256, 512, 0)
+    assert e.value.status == 2
+    with pytest.raises(g.MoeError) as e:
+        g.nvfp4_amax(256, 16, 64, 0, None, None, 0)
+    assert e.value.status == 1
 
 
 def test_srelu_allows_any_ilv(lib):

@@ -90,7 +90,18 @@ def gemm_flops(cfg, recompute=False):
     }
 
 
-QUANT_NAMES = ("mxfp8_quant_x", "mxfp8_quant_w1", "mxfp8_quant_w2", "mxfp8_quant_dy")
+# launches of one kernel that recur within a step, named by their order in the step
+REPEATED = {
+    "mxfp8_quantize": ("mxfp8_quant_x", "mxfp8_quant_w1", "mxfp8_quant_w2", "mxfp8_quant_dy"),
+    "nvfp4_quantize": ("nvfp4_quant_x", "nvfp4_quant_w1", "nvfp4_quant_w2", "nvfp4_quant_a",
+                       "nvfp4_quant_dy", "nvfp4_quant_dz"),
+    "nvfp4_amax": ("nvfp4_amax_x", "nvfp4_amax_w1", "nvfp4_amax_w2", "nvfp4_amax_dy"),
+}
+# dense tensor-core rate of the operand type relative to bf16 (nominal: fp8 4.5 and fp4
+# 13.5 PFLOP/s against bf16's 2.25)
+TENSOR_RATIO = {"bf16": 1.0, "mxfp8": 2.0, "nvfp4": 6.0}
+DTYPE = {"bf16": "bf16", "mxfp8": "e4m3+e8m0 (fp32 accumulate)",
+         "nvfp4": "e2m1+e4m3+fp32 scale (fp32 accumulate)"}
 
 
 def kernel_bytes(cfg, recompute=False):
@@ -100,6 +111,24 @@ def kernel_bytes(cfg, recompute=False):
     R, T, E = cfg.R, cfg.T, cfg.E
     H, F, N1 = cfg.H, cfg.F, cfg.N1
     R_cap = cfg.R_cap
+    if cfg.precision == "nvfp4":
+        s = 0.5 + 1.0 / 16.0   # half a byte a value plus one E4M3 scale per 16
+        return {
+            "gemm_fc1_fprop": R * H * s + E * N1 * H * s + R * N1 * 2 + R * F * 2,
+            "gemm_fc2_fprop": R * F * s + E * F * H * s + R * H * 2,
+            "gemm_fc2_dgrad": R * H * s + E * F * H * s + R * N1 * 2 + R * N1 * 2,
+            "gemm_fc2_wgrad": R * F * s + R * H * s + E * F * H * 2,
+            "gemm_fc1_dgrad": R * N1 * s + E * N1 * H * s + R * H * 2,
+            "gemm_fc1_wgrad": R * N1 * s + R * H * s + E * N1 * H * 2,
+            "gather_x": R_cap * H * 2 + R * H * 2, "gather_dy": R_cap * H * 2 + R * H * 2,
+            "combine_y": R * H * 2 + T * H * 2, "combine_dx": R * H * 2 + T * H * 2,
+            # bf16 in, row-wise and transposed copies out
+            "nvfp4_quant_x": R_cap * H * (2 + 2 * s), "nvfp4_quant_dy": R_cap * H * (2 + 2 * s),
+            "nvfp4_quant_a": R_cap * F * (2 + 2 * s), "nvfp4_quant_dz": R_cap * N1 * (2 + 2 * s),
+            "nvfp4_quant_w1": E * N1 * H * (2 + 2 * s), "nvfp4_quant_w2": E * F * H * (2 + 2 * s),
+            "nvfp4_amax_x": R_cap * H * 2, "nvfp4_amax_dy": R_cap * H * 2,
+            "nvfp4_amax_w1": E * N1 * H * 2, "nvfp4_amax_w2": E * F * H * 2,
+        }
     if cfg.precision == "mxfp8":
         s = 33.0 / 32.0
         return {
@@ -290,12 +319,20 @@ def oracle_sample(cfg, rows: int, inputs=None):
                        cfg.lin_offset)
     mx = cfg.precision == "mxfp8"
     t0 = time.perf_counter()
-    Z, a, a_s, Y = om.expert_forward(X, W1, W2, p, act, mx)
-    om.expert_backward(X, W1, W2, p, Z, a, a_s, dY, act, mx)
+    if cfg.precision == "nvfp4":
+        # the stage-by-stage NVFP4 oracle on a one-expert layer made of these rows (every
+        # quantisation of expert 0's operands included)
+        om.layer_nvfp4(np.zeros((len(tok), 1), np.float32), X, W1[None], W2[None], 1, act,
+                       synth.gen_rht_mask(cfg), dy=dY, align=cfg.align)
+        kind = "NVFP4 oracle (one-expert layer)"
+    else:
+        Z, a, a_s, Y = om.expert_forward(X, W1, W2, p, act, mx)
+        om.expert_backward(X, W1, W2, p, Z, a, a_s, dY, act, mx)
+        kind = "oracle"
     dt = time.perf_counter() - t0
     n = len(tok)
     flops = 3.0 * (2.0 * n * cfg.H * cfg.N1 + 2.0 * n * cfg.F * cfg.H)
-    desc = (f"oracle fp64 fwd+bwd of expert 0 on {n} routed tokens of {cfg.name} "
+    desc = (f"{kind} fp64 fwd+bwd of expert 0 on {n} routed tokens of {cfg.name} "
             f"({flops / 1e9:.0f} GFLOP)")
     return dt, flops, desc, n
 
@@ -449,7 +486,6 @@ def main():
     barrier(world)
     g.load()
     cfg = config_of(args)
-    mx = cfg.precision == "mxfp8"
     dev = torch.device("cuda", local)
     t_gen = time.time()
     hin = host_inputs(cfg)
@@ -524,12 +560,13 @@ def main():
             seen = {}
         j = seen.get(name, 0)
         seen[name] = j + 1
-        per.setdefault(name if name != "mxfp8_quantize" else QUANT_NAMES[j], []).append(dur)
+        per.setdefault(REPEATED[name][j] if name in REPEATED else name, []).append(dur)
     kernel_ms = {k: sum(v) / len(v) for k, v in per.items()}
     gf = gemm_flops(cfg, args.recompute)
     kb = kernel_bytes(cfg, args.recompute)
-    # the GEMMs are timed inside a long step: sustained tensor peak; fp8 = 2x bf16 (nominal)
-    p_tc = peaks.get("bf16_tflops_sustained", 1700.0) * (2.0 if mx else 1.0)
+    # the GEMMs are timed inside a long step: sustained tensor peak of the operand type (the
+    # measured bf16 figure times the nominal rate ratio)
+    p_tc = peaks.get("bf16_tflops_sustained", 1700.0) * TENSOR_RATIO[cfg.precision]
     p_bw = peaks.get("hbm_gbs", 6800.0)
     dom = max((k for k in kernel_ms if k in gf or k in kb), key=lambda k: sum(per[k]))
     dom_ms = kernel_ms[dom]
@@ -639,14 +676,15 @@ def main():
                "tokens_per_s_equiv": (fl / dt) / (flops / T)}
 
     if rank == 0:
-        tc_kind = ("2 x bf16_tflops_sustained (fp8/bf16 nominal ratio)" if mx
-                   else "bf16_tflops_sustained") + f" ({peak_src})"
+        ratio = TENSOR_RATIO[cfg.precision]
+        tc_kind = (f"{ratio:g} x bf16_tflops_sustained ({cfg.precision}/bf16 nominal ratio)"
+                   if ratio != 1.0 else "bf16_tflops_sustained") + f" ({peak_src})"
         w_bytes = 2 * 2 * cfg.E * (cfg.N1 + cfg.F) * cfg.H
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3+e8m0 (fp32 accumulate)" if mx else "bf16",
+            "dtype": DTYPE[cfg.precision],
             "data": "synthetic",
             "config": {"workload": workload_name(cfg), "parallelism": f"replicas x{world}",
                        "l2": f"no flush: each step streams {w_bytes / 1e9:.1f} GB of bf16 "

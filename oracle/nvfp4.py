@@ -114,17 +114,14 @@ def _blocks(v: np.ndarray, axis: int):
     return vm.reshape(vm.shape[:-1] + (n // BLOCK, BLOCK)), vm.shape, axis
 
 
-def quantize_blocks(v: np.ndarray, axis: int, S):
-    """N2, N3: NVFP4-quantise along `axis` (a multiple of 16 long) with encode scale S.
-
-    v must hold fp32-representable values (the kernels quantise fp32 values). Returns
-    (E2M1 codes uint8 with v's shape, E4M3 scale values fp64 with v's shape except axis/16).
-    """
+def _round_blocks(v: np.ndarray, axis: int, S):
+    """N2, N3 up to the E2M1 rounding: returns (the rounded E2M1 values per block [..., n/16,
+    16] fp64, the E4M3 scale values [..., n/16] fp64, v's moved shape, axis)."""
     S = np.float32(S)
     b, shape, axis = _blocks(v, axis)
     b32 = b.astype(np.float32)
     if not np.array_equal(b32.astype(np.float64), b):
-        raise ValueError("quantize_blocks takes fp32-representable values")
+        raise ValueError("NVFP4 quantisation takes fp32-representable values")
     amax_b = np.abs(b32).max(axis=-1)
     t = (amax_b / np.float32(6.0)).astype(np.float32) * S          # fp32 products
     sb = e4m3_round(t.astype(np.float32).astype(np.float64))       # RNE + saturation
@@ -132,7 +129,17 @@ def quantize_blocks(v: np.ndarray, axis: int, S):
     with np.errstate(divide="ignore"):
         enc = np.where(sb32 > 0, S / np.where(sb32 > 0, sb32, np.float32(1)), np.float32(0))
     w = (b32 * enc.astype(np.float32)[..., None]).astype(np.float32)
-    codes = e2m1_encode(w.astype(np.float64)).reshape(shape)
+    return e2m1_round(w.astype(np.float64)), sb, shape, axis
+
+
+def quantize_blocks(v: np.ndarray, axis: int, S):
+    """N2, N3: NVFP4-quantise along `axis` (a multiple of 16 long) with encode scale S.
+
+    v must hold fp32-representable values (the kernels quantise fp32 values). Returns
+    (E2M1 codes uint8 with v's shape, E4M3 scale values fp64 with v's shape except axis/16).
+    """
+    r, sb, shape, axis = _round_blocks(v, axis, S)
+    codes = e2m1_encode(r).reshape(shape)
     return np.moveaxis(codes, -1, axis), np.moveaxis(sb, -1, axis)
 
 
@@ -148,9 +155,12 @@ def dequantize_blocks(codes: np.ndarray, sb: np.ndarray, axis: int, S) -> np.nda
 
 
 def fake_quant(v: np.ndarray, axis: int, S) -> np.ndarray:
-    """Quantise along `axis` and return the dequantised fp64 values."""
-    codes, sb = quantize_blocks(v, axis, S)
-    return dequantize_blocks(codes, sb, axis, S)
+    """Quantise along `axis` and return the dequantised fp64 values, E2M1(q) * s_b / S: the
+    values quantize_blocks encodes, taken straight from the rounding (no code-table round
+    trip, so that it is fast on full-size weights)."""
+    r, sb, shape, axis = _round_blocks(v, axis, S)
+    out = r * sb[..., None] / float(np.float32(S))
+    return np.moveaxis(out.reshape(shape), -1, axis)
 
 
 def amax(v: np.ndarray) -> float:

@@ -237,3 +237,12 @@ def test_layer_amaxes_are_those_of_the_stored_tensors():
     assert r.amax["dz"] == max(np.abs(d).max() for d in r.dZ if d.size)
     for a in r.A + r.dZ:
         assert np.array_equal(om.bf16_round(a), a)
+
+
+def test_fake_quant_is_the_dequantised_encoding():
+    rng = np.random.default_rng(11)
+    v = om.bf16_round(rng.standard_normal((48, 128)) * np.exp(rng.uniform(-6, 6, (48, 1))))
+    S = nv.encode_scale(nv.amax(v))
+    for axis in (0, 1):
+        c, sb = nv.quantize_blocks(v, axis, S)
+        assert np.array_equal(nv.fake_quant(v, axis, S), nv.dequantize_blocks(c, sb, axis, S))

@@ -15,11 +15,20 @@
 //   warp 1   TMEM owner; one thread copies the stage's scales into TMEM (tcgen05.cp, 48
 //            columns a stage) and issues four tcgen05.mma.kind::mxf4nvf4.block_scale
 //            (scale_vec::4X) 128x256x64, each with its own 512-byte scale slab per 128 rows;
-//   warps 2-9 epilogue: drain the accumulator into registers (warp w takes TMEM lanes
-//            32*(w%4).. and 128 of the 256 columns) times 1 / (S_a S_b), release TMEM, then
-//            bf16 store, GLU or dGLU.
-// TMEM: one 256-column fp32 accumulator plus 4 x 48 scale columns. Expert segments are padded
-// to 128 rows, so every row-grouped tile lies inside one segment (padding rows carry
+//   warps 2-9 epilogue (warp w reads TMEM lanes 32*(w%4)..): results times 1 / (S_a S_b).
+// Two tile shapes:
+//   STORE and GLU (FC2 fprop, FC1 dgrad, wgrads; FC1 fprop): 128 x 256 tiles (a 128 x 256 x 64
+//     MMA costs about what a 128-wide one does), one 256-column accumulator that the epilogue
+//     drains into registers (128 columns a warp) and releases at once; 4 stages;
+//   dGLU (FC2 dgrad), whose epilogue is several times heavier than its mainloop: 128 x 128
+//     tiles and two 128-column accumulators, so that the epilogue reads TMEM step by step with
+//     no accumulator in registers while the next tile's MMAs run; 4 stages, the fifth stage's
+//     space holding the saved-Z staging and the rotation transposes.
+// The rotated amax goes across lanes by shuffles in the GLU epilogue (64 values a thread and
+// tile) and through a per-warp shared-memory transpose in the dGLU epilogue (each lane rotates
+// a column of 16 rows in registers); both perform the quantiser's fp32 butterflies.
+// TMEM: 256 accumulator columns, then the scale columns of every stage. Expert segments are
+// padded to 128 rows, so every row-grouped tile lies inside one segment (padding rows carry
 // probability 0 and zero operands) and every weight-gradient k range starts on a scale slab.
 #include "gemm_common.cuh"
 #include "nvfp4.cuh"
@@ -29,33 +38,48 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 256;       // E2M1 values per k-block: one 128-byte swizzle row
 constexpr int BKB = BK / 2;   // bytes per k-block row
 constexpr int MMA_K = 64;     // values per MMA: 32 bytes along the swizzled row
-constexpr int STAGES = 4;
+constexpr int kMaxStages = 5;
 constexpr int ILV = 64;       // gate/linear interleave of the packed FC1 columns
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxE = 256;
-constexpr int kSfCol = BN;              // first TMEM column of the scale factors
-constexpr int kSfColsPerMma = 12;       // 4 (A, 128 rows) + 8 (B, 256 rows)
-constexpr int kSfColsPerStage = 4 * kSfColsPerMma;
 constexpr int kTmemCols = 512;
-static_assert(kSfCol + STAGES * kSfColsPerStage <= kTmemCols, "TMEM map");
 
 enum { EPI_STORE = 0, EPI_GLU = 1, EPI_DGLU = 2 };
 
 constexpr int A_BYTES = BM * BKB;
-constexpr int B_BYTES = BN * BKB;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SFA_SLAB = 512;    // 128 rows x 4 blocks of 16 values
-constexpr int SFB_SLAB = 1024;   // 256 rows x 4 blocks
-constexpr int SF_STAGE = 4 * (SFA_SLAB + SFB_SLAB);
-constexpr int SF_OFF = STAGES * STAGE_BYTES;
-constexpr int CTRL_OFF = SF_OFF + STAGES * SF_STAGE;
-constexpr int SMEM_TOTAL = CTRL_OFF + 4096 + 1024;
-static_assert(SMEM_TOTAL <= 232448, "shared memory above the per-block limit");
+constexpr int SFA_SLAB = 512;            // 128 rows x 4 blocks of 16 values
+constexpr int ZQ_BUF = 32 * 64;          // dGLU: one 16-column step of saved Z, 32 rows
+constexpr int ZQ_WARP = 2 * ZQ_BUF;      //   double-buffered per epilogue warp
+constexpr int XT_PITCH = 20;             // words per row of the rotation transpose tile
+constexpr int XT_WARP = (32 * XT_PITCH + 16) * 4;  // rows 16..31 shifted by 16 words
+
+// Tile shape, pipeline depth and shared-memory / TMEM maps of one epilogue kind.
+template <int EPI>
+struct Fp4Cfg {
+  static constexpr int BN = EPI == EPI_DGLU ? 128 : 256;
+  static constexpr int NACC = EPI == EPI_DGLU ? 2 : 1;
+  static constexpr int STAGES = 4;
+  static constexpr int B_BYTES = BN * BKB;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SFB_SLAB = BN * 4;
+  static constexpr int SF_STAGE = 4 * (SFA_SLAB + SFB_SLAB);
+  static constexpr int SF_COLS_MMA = 4 + 4 * (BN / 128);  // A's 128 rows + B's BN rows
+  static constexpr int SF_COLS_STAGE = 4 * SF_COLS_MMA;
+  static constexpr int SF_COL0 = NACC * BN;
+  static constexpr int SF_OFF = STAGES * STAGE_BYTES;
+  static constexpr int ZQ_OFF = SF_OFF + STAGES * SF_STAGE;
+  static constexpr int XT_OFF = ZQ_OFF + (EPI == EPI_DGLU ? kEpiWarps * ZQ_WARP : 0);
+  static constexpr int CTRL_OFF = XT_OFF + (EPI == EPI_DGLU ? kEpiWarps * XT_WARP : 0);
+  static constexpr int TOTAL = CTRL_OFF + 4096 + 1024;
+  static_assert(TOTAL <= 232448, "shared memory above the per-block limit");
+  static_assert(SF_COL0 + STAGES * SF_COLS_STAGE <= kTmemCols, "TMEM map");
+  static_assert(STAGES <= kMaxStages, "barrier arrays");
+  static_assert(ZQ_OFF % 16 == 0 && XT_OFF % 16 == 0 && CTRL_OFF % 8 == 0, "alignment");
+};
 
 struct Fp4Args {
   CUtensorMap tmA;
@@ -90,10 +114,10 @@ struct Fp4Args {
 };
 
 struct Ctrl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tfull;
-  uint64_t tempty;
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -107,7 +131,7 @@ struct TileInfo {
   int e, m0, n0, kbeg, klen, nkb, row_end;
 };
 
-template <bool KG>
+template <int BN, bool KG>
 MOE_DEVICE void decode_tile(int tile, const Fp4Args& p, const Ctrl& c, int MT, int NT,
                             TileInfo& t) {
   if (!KG) {
@@ -160,14 +184,51 @@ MOE_DEVICE void mma_nvf4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, u
       : "memory");
 }
 
-MOE_DEVICE float bf16r(float x) { return bf16_lo(pack_bf16x2(x, 0.f)); }
-
-// 16 floats (already bf16 values) -> 32 bytes of bf16 at a 32-byte aligned address.
-MOE_DEVICE void store_bf16x16_v8(void* dst, const float (&v)[16]) {
-  uint32_t w[8];
+// dGLU saved-Z staging: each lane copies its own row's 16 gate (and 16 linear) values of one
+// 16-column step, four 16-byte pieces, into a 64-byte slot of the warp's buffer (pieces
+// XOR-rotated by lane so that the 16-byte reads of eight lanes hit distinct banks).
+MOE_DEVICE uint32_t zq_slot(int lane, int piece) {
+  return lane * 64 + ((piece ^ ((lane >> 1) & 3)) * 16);
+}
+MOE_DEVICE void zq_issue(uint32_t buf, const uint16_t* src, bool gated, int lane) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-  st_global_v8(dst, w);
+  for (int pc = 0; pc < 4; ++pc) {
+    if (pc >= 2 && !gated) break;
+    const uint16_t* g = src + (pc >= 2 ? ILV : 0) + (pc & 1) * 8;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(buf + zq_slot(lane, pc)),
+                 "l"(g)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Max |rotated value| of the warp's 32 rows x 32 bf16 columns (lane = row; w = its 32 values
+// as bf16 pairs): the tile goes through shared memory, then lane l rotates columns
+// 2 (l % 16) and 2 (l % 16) + 1 over rows 16 (l / 16) .. + 15 with the register butterflies.
+MOE_DEVICE float rht_amax_tile32(uint32_t* xt, const uint32_t (&w)[16], uint32_t mask,
+                                 int lane) {
+  uint32_t* row = xt + lane * XT_PITCH + (lane >= 16 ? 16 : 0);
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    *reinterpret_cast<uint4*>(row + 4 * k) =
+        make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+  __syncwarp();
+  const int cw = lane & 15, h = lane >> 4;
+  const uint32_t* col = xt + (16 * h) * XT_PITCH + 16 * h + cw;
+  float a[16], b[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t v = col[i * XT_PITCH];
+    a[i] = bf16_lo(v);
+    b[i] = bf16_hi(v);
+  }
+  __syncwarp();  // every lane has read the tile before the next call rewrites it
+  rht16_regs(a, mask);
+  rht16_regs(b, mask);
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fmaxf(fabsf(a[i]), fabsf(b[i])));
+  return m;
 }
 
 // Gate column of dA column f in the packed Z layout (blocks of ILV gate columns followed by
@@ -177,10 +238,14 @@ MOE_DEVICE int gate_col(int f) { return ((f & ~(ILV - 1)) << 1) | (f & (ILV - 1)
 template <int EPI, int KIND, bool KG>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __grid_constant__ Fp4Args p) {
   constexpr bool kGated = KIND != MOE_ACT_SRELU;
+  using L = Fp4Cfg<EPI>;
+  constexpr int BN = L::BN;
+  constexpr int NACC = L::NACC;
+  constexpr int STAGES = L::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  Ctrl& c = *reinterpret_cast<Ctrl*>(smem + CTRL_OFF);
+  Ctrl& c = *reinterpret_cast<Ctrl*>(smem + L::CTRL_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &c.abort;
   const int NT = (p.N + BN - 1) / BN;
@@ -191,8 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
       mbar_init(&c.full[s], 1);
       mbar_init(&c.empty[s], 1);
     }
-    mbar_init(&c.tfull, 1);
-    mbar_init(&c.tempty, kEpiWarps);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c.tfull[i], 1);
+      mbar_init(&c.tempty[i], kEpiWarps);
+    }
     mbar_init(&c.drain, 1);
     fence_mbar_init();
     c.abort = 0;
@@ -241,16 +308,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
       for (int s = 0; s < STAGES; ++s) armed[s] = -1;
       for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
         TileInfo t;
-        decode_tile<KG>(tile, p, c, MT, NT, t);
+        decode_tile<BN, KG>(tile, p, c, MT, NT, t);
         const int a_row = t.m0 + t.e * p.a_row_e;
         const int b_row = t.n0 + t.e * p.b_row_e;
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(&c.empty[stage], phase ^ 1, abort, p.err)) break;
-          uint8_t* sA = smem + stage * STAGE_BYTES;
+          uint8_t* sA = smem + stage * L::STAGE_BYTES;
           uint8_t* sB = sA + A_BYTES;
-          uint8_t* sf = smem + SF_OFF + stage * SF_STAGE;
+          uint8_t* sf = smem + L::SF_OFF + stage * L::SF_STAGE;
           uint64_t* bar = &c.full[stage];
-          mbar_arrive_expect_tx(bar, STAGE_BYTES + SF_STAGE);
+          mbar_arrive_expect_tx(bar, L::STAGE_BYTES + L::SF_STAGE);
 #pragma unroll
           for (int s = 0; s < STAGES; ++s)
             if (s == stage) armed[s] = (int)phase;
@@ -259,16 +326,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
           const int b_k = k0 + t.e * p.b_k_e;
           // boxes of 128 rows x 128 bytes at byte column k / 2 (a multiple of 32)
           tma_load_2d(sA, &p.tmA, bar, a_k / 2, a_row);
-          tma_load_2d(sB, &p.tmB, bar, b_k / 2, b_row);
-          tma_load_2d(sB + B_BYTES / 2, &p.tmB, bar, b_k / 2, b_row + 128);
-          // four 64-value scale slabs of each operand: A's 128 rows, B's 256 rows
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)
+            tma_load_2d(sB + h * (128 * BKB), &p.tmB, bar, b_k / 2, b_row + 128 * h);
+          // four 64-value scale slabs of each operand: A's 128 rows, B's BN rows
 #pragma unroll
           for (int s = 0; s < 4; ++s) {
             bulk_load(sf + s * SFA_SLAB,
                       p.sfa + ((int64_t)(a_k / MMA_K + s) * p.sfa_pad + a_row) * 4, SFA_SLAB,
                       bar);
-            bulk_load(sf + 4 * SFA_SLAB + s * SFB_SLAB,
-                      p.sfb + ((int64_t)(b_k / MMA_K + s) * p.sfb_pad + b_row) * 4, SFB_SLAB,
+            bulk_load(sf + 4 * SFA_SLAB + s * L::SFB_SLAB,
+                      p.sfb + ((int64_t)(b_k / MMA_K + s) * p.sfb_pad + b_row) * 4, L::SFB_SLAB,
                       bar);
           }
           if (++stage == STAGES) {
@@ -297,11 +365,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
       bool issued_any = false;
       for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
         TileInfo t;
-        decode_tile<KG>(tile, p, c, MT, NT, t);
+        decode_tile<BN, KG>(tile, p, c, MT, NT, t);
         if (t.nkb == 0) continue;
-        // the single accumulator is free once every epilogue warp drained the last tile
-        if (!mbar_wait(&c.tempty, (acc_i & 1) ^ 1, abort, p.err)) break;
+        const int acc = acc_i % NACC;
+        const uint32_t acc_phase = (acc_i / NACC) & 1;
+        // the accumulator is free once every epilogue warp has finished with its last tile
+        if (!mbar_wait(&c.tempty[acc], acc_phase ^ 1, abort, p.err)) break;
         tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
         bool ok = true;
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(&c.full[stage], phase, abort, p.err)) {
@@ -309,23 +380,24 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
             break;
           }
           tc_fence_after();
-          const uint32_t sA = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sA = smem_u32(smem + stage * L::STAGE_BYTES);
           const uint32_t sB = sA + A_BYTES;
-          const uint32_t sf = smem_u32(smem + SF_OFF + stage * SF_STAGE);
-          const uint32_t sft = tmem_base + kSfCol + stage * kSfColsPerStage;
+          const uint32_t sf = smem_u32(smem + L::SF_OFF + stage * L::SF_STAGE);
+          const uint32_t sft = tmem_base + L::SF_COL0 + stage * L::SF_COLS_STAGE;
           const int rem = t.klen - kb * BK;
           const int nsub = rem >= BK ? BK / MMA_K : (rem + MMA_K - 1) / MMA_K;
           for (int s = 0; s < nsub; ++s) {
-            const uint32_t col = sft + s * kSfColsPerMma;
+            const uint32_t col = sft + s * L::SF_COLS_MMA;
             tmem_cp_32x128b_warpx4(col, smem_desc_noswizzle(sf + s * SFA_SLAB, 0, 128));
-            tmem_cp_32x128b_warpx4(col + 4, smem_desc_noswizzle(sf + 4 * SFA_SLAB + s * SFB_SLAB,
-                                                                0, 128));
-            tmem_cp_32x128b_warpx4(col + 8, smem_desc_noswizzle(
-                                                sf + 4 * SFA_SLAB + s * SFB_SLAB + 512, 0, 128));
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+              tmem_cp_32x128b_warpx4(
+                  col + 4 + 4 * h,
+                  smem_desc_noswizzle(sf + 4 * SFA_SLAB + s * L::SFB_SLAB + 512 * h, 0, 128));
           }
           for (int s = 0; s < nsub; ++s) {
-            const uint32_t col = sft + s * kSfColsPerMma;
-            mma_nvf4_ss(tmem_base, smem_desc_sw128(sA + s * (MMA_K / 2), 16, 1024),
+            const uint32_t col = sft + s * L::SF_COLS_MMA;
+            mma_nvf4_ss(d_tmem, smem_desc_sw128(sA + s * (MMA_K / 2), 16, 1024),
                         smem_desc_sw128(sB + s * (MMA_K / 2), 16, 1024), IDESC, col, col + 4,
                         (kb | s) != 0 ? 1u : 0u);
           }
@@ -337,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
           }
         }
         if (!ok) break;
-        mma_commit(&c.tfull);
+        mma_commit(&c.tfull[acc]);
         ++acc_i;
       }
       if (issued_any) {
@@ -349,9 +421,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
     }
   } else {
     // ------------------------------------------------------------ epilogue warps 2..9
-    // Control flow stays warp-uniform (the rotation amax exchanges values across lanes).
+    // Control flow stays warp-uniform (the shared-memory transposes are warp-wide).
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;  // columns [128*half, 128*half + 128) of the tile
+    const int half = (warp - 2) >> 2;
+    const uint32_t zq = smem_u32(smem + L::ZQ_OFF + (warp - 2) * ZQ_WARP);
+    const uint8_t* zq_ptr = smem + L::ZQ_OFF + (warp - 2) * ZQ_WARP;
+    uint32_t* xt = reinterpret_cast<uint32_t*>(smem + L::XT_OFF + (warp - 2) * XT_WARP);
     const float alpha =
         __frcp_rn(__fmul_rn(nvfp4_encode_scale(*p.amax_a), nvfp4_encode_scale(*p.amax_b)));
     float m_out = 0.f, m_rht = 0.f;
@@ -359,31 +434,41 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       if (__shfl_sync(0xFFFFFFFFu, *abort, 0)) break;
       TileInfo t;
-      decode_tile<KG>(tile, p, c, MT, NT, t);
+      decode_tile<BN, KG>(tile, p, c, MT, NT, t);
       const int row0 = t.m0 + q * 32;
       const int row = row0 + lane;
       const bool row_ok = row < t.row_end;
-      const int cb = half * 128;
       if (t.nkb == 0) {
         if (row_ok) {
+          const int cb = half * (BN / 2);
           uint16_t* o = static_cast<uint16_t*>(p.out) + (int64_t)t.e * p.out_estride +
                         (int64_t)row * p.ldo;
-          for (int cc = cb; cc < cb + 128 && t.n0 + cc < p.N; cc += 32)
+          for (int cc = cb; cc < cb + BN / 2 && t.n0 + cc < p.N; cc += 32)
             store_zero_bf16x32(o + t.n0 + cc);
         }
         continue;
       }
       const float prob = EPI == EPI_STORE ? 0.f : p.row_prob[row];
-      const bool got = mbar_wait(&c.tfull, acc_i & 1, abort, p.err);
+      if constexpr (EPI == EPI_DGLU) {
+        // the first step's saved Z comes in while the MMAs run
+        const int f0 = t.n0 + half * 64;
+        if (f0 < p.N)
+          zq_issue(zq, p.z + (int64_t)row * p.ldz + (kGated ? gate_col(f0) : f0), kGated, lane);
+      }
+      const int acc = acc_i % NACC;
+      const uint32_t acc_phase = (acc_i / NACC) & 1;
+      const bool got = mbar_wait(&c.tfull[acc], acc_phase, abort, p.err);
       if (!__all_sync(0xFFFFFFFFu, got)) break;
       tc_fence_after();
-      const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + cb;
+      const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       if constexpr (EPI == EPI_STORE) {
+        // drain 128 columns as packed bf16 and release the accumulator at once
+        const int cb = half * 128;
         uint32_t pk[64];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint32_t r[32];
-          tmem_ld_32x32b_x32(tacc + 32 * j, r);
+          tmem_ld_32x32b_x32(tacc + cb + 32 * j, r);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -392,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&c.tempty);
+        if (lane == 0) mbar_arrive(&c.tempty[acc]);
         ++acc_i;
         if (row_ok) {
           uint16_t* o = static_cast<uint16_t*>(p.out) + (KG ? (int64_t)t.e * p.out_estride : 0) +
@@ -413,27 +498,28 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
             }
           }
         }
-      } else {
-      // GLU / dGLU: the 128 columns as fp32 (activation math from the fp32 accumulator)
-      float acc[128];
+      } else if constexpr (EPI == EPI_GLU) {
+        // drain the 128 columns as fp32 (the activation is computed from the fp32
+        // accumulator), free TMEM, then work from registers. Row-grouped segments are 128-row
+        // aligned: every row of the tile is in its segment.
+        const int cb = half * 128;
+        float acc_r[128];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tacc + 32 * j, r);
-        tmem_ld_wait();
+        for (int j = 0; j < 4; ++j) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tacc + cb + 32 * j, r);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[32 * j + i] = alpha * __uint_as_float(r[i]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&c.tempty);
-      ++acc_i;
-      // row-grouped segments are 128-row aligned: every row of the tile is in its segment
-      if constexpr (EPI == EPI_GLU) {
+          for (int i = 0; i < 32; ++i) acc_r[32 * j + i] = alpha * __uint_as_float(r[i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.tempty[acc]);
+        ++acc_i;
         uint16_t* zout = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo + t.n0 + cb;
 #pragma unroll
         for (int j = 0; j < 4; ++j)  // the saved Z (bf16)
-          if (t.n0 + cb + 32 * j < p.N) store_bf16x32_v8(zout + 32 * j, &acc[32 * j]);
+          if (t.n0 + cb + 32 * j < p.N) store_bf16x32_v8(zout + 32 * j, &acc_r[32 * j]);
         uint16_t* aout = static_cast<uint16_t*>(p.out2) + (int64_t)row * p.ldo2;
         // gated: this half holds 64 gate and 64 linear columns, two 32-wide output blocks;
         // sReLU: four 32-wide blocks
@@ -447,12 +533,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
           for (int i = 0; i < 32; ++i) {
             float a;
             if constexpr (kGated) {
-              a = act_fwd_k<KIND>(p.act, acc[g_off + i], acc[g_off + ILV + i]);
+              a = act_fwd_k<KIND>(p.act, acc_r[g_off + i], acc_r[g_off + ILV + i]);
             } else {
-              const float rr = fmaxf(acc[g_off + i], 0.f);
+              const float rr = fmaxf(acc_r[g_off + i], 0.f);
               a = rr * rr;
             }
-            v[i] = bf16r(prob * a);
+            v[i] = bf16_lo(pack_bf16x2(prob * a, 0.f));
           }
           store_bf16x32_v8(aout + acol, v);
 #pragma unroll
@@ -461,50 +547,85 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
             m_rht = fmaxf(m_rht, fabsf(rht16_lanes(v[i], p.rht_mask, lane)));
           }
         }
-      } else {  // EPI_DGLU: accumulator = dA_s over F columns
+      } else {  // EPI_DGLU: accumulator = dA_s over F columns; this half: 64 of them
         const uint16_t* zrow = p.z + (int64_t)row * p.ldz;
         uint16_t* dzrow = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo;
         float dp = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int f0 = t.n0 + cb + 16 * j;
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          const int f0 = t.n0 + half * 64 + 16 * j;
           if (f0 >= p.N) break;
           const int gc = kGated ? gate_col(f0) : f0;
-          uint32_t gw[8], lw[8];
-          ld_v8_noalloc(zrow + gc, gw);
-          if constexpr (kGated) ld_v8_noalloc(zrow + gc + ILV, lw);
-          float dg[16], dl[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float d = acc[16 * j + i];
-            const float g = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
-            if constexpr (kGated) {
-              const float l = (i & 1) ? bf16_hi(lw[i >> 1]) : bf16_lo(lw[i >> 1]);
-              dp += d * act_bwd_k<KIND>(p.act, g, l, prob * d, dg[i], dl[i]);
-              dl[i] = bf16r(dl[i]);
-            } else {
-              const float rr = fmaxf(g, 0.f);
-              dp += d * rr * rr;
-              dg[i] = prob * d * 2.f * rr;
-            }
-            dg[i] = bf16r(dg[i]);
+          // next step's Z into the other buffer (this lane finished reading it in the previous
+          // step), then wait for this step's
+          const bool more = j + 1 < 4 && f0 + 16 < p.N;
+          if (more) {
+            zq_issue(zq + ((j + 1) & 1) * ZQ_BUF, zrow + (kGated ? gate_col(f0 + 16) : f0 + 16),
+                     kGated, lane);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+          } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
           }
-          store_bf16x16_v8(dzrow + gc, dg);
-          if constexpr (kGated) store_bf16x16_v8(dzrow + gc + ILV, dl);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            m_out = fmaxf(m_out, fabsf(dg[i]));
-            m_rht = fmaxf(m_rht, fabsf(rht16_lanes(dg[i], p.rht_mask, lane)));
+          uint32_t dr[16];
+          tmem_ld_32x32b_x16(tacc + half * 64 + 16 * j, dr);
+          uint32_t gw[8], lw[8];
+          {
+            const uint8_t* b = zq_ptr + (j & 1) * ZQ_BUF;
+            const uint4 g0 = *reinterpret_cast<const uint4*>(b + zq_slot(lane, 0));
+            const uint4 g1 = *reinterpret_cast<const uint4*>(b + zq_slot(lane, 1));
+            gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w;
+            gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
             if constexpr (kGated) {
-              m_out = fmaxf(m_out, fabsf(dl[i]));
-              m_rht = fmaxf(m_rht, fabsf(rht16_lanes(dl[i], p.rht_mask, lane)));
+              const uint4 l0 = *reinterpret_cast<const uint4*>(b + zq_slot(lane, 2));
+              const uint4 l1 = *reinterpret_cast<const uint4*>(b + zq_slot(lane, 3));
+              lw[0] = l0.x; lw[1] = l0.y; lw[2] = l0.z; lw[3] = l0.w;
+              lw[4] = l1.x; lw[5] = l1.y; lw[6] = l1.z; lw[7] = l1.w;
             }
+          }
+          tmem_ld_wait();
+          uint32_t w[16];  // dG pairs in w[0..7], dL pairs in w[8..15]
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            float dg[2], dl[2] = {0.f, 0.f};
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const float d = alpha * __uint_as_float(dr[i + u]);
+              const float g = u ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
+              if constexpr (kGated) {
+                const float l = u ? bf16_hi(lw[i >> 1]) : bf16_lo(lw[i >> 1]);
+                dp += d * act_bwd_k<KIND>(p.act, g, l, prob * d, dg[u], dl[u]);
+              } else {
+                const float rr = fmaxf(g, 0.f);
+                dp += d * rr * rr;
+                dg[u] = prob * d * 2.f * rr;
+              }
+            }
+            w[i >> 1] = pack_bf16x2(dg[0], dg[1]);
+            w[8 + (i >> 1)] = pack_bf16x2(dl[0], dl[1]);
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            m_out = fmaxf(m_out, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+          st_global_v8(dzrow + gc, w);
+          if constexpr (kGated) {
+            st_global_v8(dzrow + gc + ILV, w + 8);
+            m_rht = fmaxf(m_rht, rht_amax_tile32(xt, w, p.rht_mask, lane));
+          } else {
+            // sReLU: no linear half; rotate the 16 dG columns (the other 16 are zero)
+            uint32_t w2[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w2[i] = i < 8 ? w[i] : 0u;
+            m_rht = fmaxf(m_rht, rht_amax_tile32(xt, w2, p.rht_mask, lane));
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.tempty[acc]);
+        ++acc_i;
         p.dprob_part[(int64_t)row * p.nparts + (t.n0 / BN) * 2 + half] = dp;
       }
-      }  // GLU / dGLU
     }
+    if constexpr (EPI == EPI_DGLU) asm volatile("cp.async.wait_all;" ::: "memory");
     if constexpr (EPI != EPI_STORE) {
       amax_flush_warp(m_out, p.amax_out);
       amax_flush_warp(m_rht, p.amax_out_rht);
@@ -530,9 +651,9 @@ bool tmap_fp4(CUtensorMap* m, const MxOperand& t) {
 template <int EPI, int KIND, bool KG>
 cudaError_t launch_fp4(const Fp4Args& a, int grid, cudaStream_t s, int kid) {
   auto kern = grouped_gemm_fp4_kernel<EPI, KIND, KG>;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), SMEM_TOTAL);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), Fp4Cfg<EPI>::TOTAL);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, SMEM_TOTAL, s>>>(a);
+  kern<<<grid, kThreads, Fp4Cfg<EPI>::TOTAL, s>>>(a);
   count_launch(s, kid);
   return cudaGetLastError();
 }
@@ -551,7 +672,10 @@ cudaError_t launch_act_family(const Fp4Args& a, int kind, int grid, cudaStream_t
 
 }  // namespace
 
-int dprob_parts_fp4(int F) { return 2 * ((F + BN - 1) / BN); }
+int dprob_parts_fp4(int F) {
+  constexpr int bn = Fp4Cfg<EPI_DGLU>::BN;
+  return 2 * ((F + bn - 1) / bn);
+}
 
 cudaError_t launch_grouped_gemm_fp4(const Fp4Problem& p, cudaStream_t s) {
   static const int kKid[6] = {MOE_K_GEMM_FC1_FPROP, MOE_K_GEMM_FC2_FPROP, MOE_K_GEMM_FC2_DGRAD,
@@ -627,7 +751,8 @@ cudaError_t launch_grouped_gemm_fp4(const Fp4Problem& p, cudaStream_t s) {
     case ROLE_FC1_DGRAD:
       return launch_fp4<EPI_STORE, 0, false>(a, grid, s, kid);
     default: {
-      const int64_t tiles = (int64_t)p.E * ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
+      constexpr int bn = Fp4Cfg<EPI_STORE>::BN;
+      const int64_t tiles = (int64_t)p.E * ((a.M + BM - 1) / BM) * ((a.N + bn - 1) / bn);
       grid = (int)std::min<int64_t>(grid, std::max<int64_t>(tiles, 1));
       return launch_fp4<EPI_STORE, 0, true>(a, grid, s, kid);
     }

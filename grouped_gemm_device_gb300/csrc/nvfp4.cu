@@ -10,9 +10,10 @@
 // bank conflicts). Thread t then quantises
 //   row-wise    row t's 64 values (four 16-blocks along the row, the reduction dimension of
 //               the row-grouped GEMMs) into one 32-byte run and one 32-bit word of scales;
-//   transposed  column t % 64 over rows 64 * (t / 64) .. + 63 (four 16-blocks along the rows,
-//               optionally Hadamard-rotated first) into one 32-byte run of the transposed copy
-//               [N, M / 2] and one scale word: the K-major operand of the weight-gradient GEMMs.
+//   transposed  columns 2 (t % 32), 2 (t % 32) + 1 over rows 32 (t / 32) .. + 31 (two 16-blocks
+//               along the rows per column, optionally Hadamard-rotated first) into a 16-byte
+//               run and a 16-bit scale pair per column of the transposed copy [N, M / 2]: the
+//               K-major operand of the weight-gradient GEMMs.
 // Input rows are grouped (G rows per group in the input, Gp in the output, zero padding rows)
 // and optionally cut at a device-side row count (rows at or beyond it read as zero).
 #include "kernels.cuh"
@@ -27,8 +28,30 @@ constexpr int QT_COLS = 64;
 constexpr int QT_LD = 144;  // bytes per staged row: 128 + 16
 constexpr int QT_THREADS = 128;
 
-__global__ void __launch_bounds__(QT_THREADS) nvfp4_quantize_kernel(const Nvfp4QuantArgs p) {
-  __shared__ __align__(16) uint8_t tile[QT_ROWS * QT_LD];
+// Stage one tile: 128 rows x 8 pieces of 16 bytes, 8 consecutive threads a row's 128 bytes;
+// a zero row (group padding or past the row limit) copies nothing and reads no global memory.
+MOE_DEVICE void stage_tile(const Nvfp4QuantArgs& p, const uint16_t* in, int64_t tile_i,
+                           int64_t ntc, int64_t limit, uint32_t dst, int t) {
+  const int64_t r0 = (tile_i / ntc) * QT_ROWS;
+  const int64_t c0 = (tile_i % ntc) * QT_COLS;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int v = t + QT_THREADS * i;
+    const int r = v >> 3, piece = v & 7;
+    const int64_t orow = r0 + r;
+    const int64_t g = orow / p.Gp, gi = orow - g * p.Gp;
+    const bool live = gi < p.G && orow < limit;
+    const uint16_t* src = live ? in + (g * p.G + gi) * p.N + c0 + piece * 8 : in;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + r * QT_LD +
+                                                                          piece * 16),
+                 "l"(src), "r"(live ? 16 : 0)
+                 : "memory");
+  }
+}
+
+__global__ void __launch_bounds__(QT_THREADS, 8) nvfp4_quantize_kernel(const Nvfp4QuantArgs p) {
+  // two tile buffers: the next tile streams in while this one is quantised
+  __shared__ __align__(16) uint8_t tiles[2][QT_ROWS * QT_LD];
   const int t = threadIdx.x;
   const int64_t ntr = p.M / QT_ROWS, ntc = p.N / QT_COLS;
   const int64_t ntiles = ntr * ntc;
@@ -36,21 +59,18 @@ __global__ void __launch_bounds__(QT_THREADS) nvfp4_quantize_kernel(const Nvfp4Q
   const float s_row = p.q_row ? nvfp4_encode_scale(*p.amax_row) : 0.f;
   const float s_col = p.q_col ? nvfp4_encode_scale(*p.amax_col) : 0.f;
   const uint16_t* in = static_cast<const uint16_t*>(p.in);
-  for (int64_t tile_i = blockIdx.x; tile_i < ntiles; tile_i += gridDim.x) {
+  if ((int64_t)blockIdx.x < ntiles)
+    stage_tile(p, in, blockIdx.x, ntc, limit, smem_u32(tiles[0]), t);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  int k = 0;
+  for (int64_t tile_i = blockIdx.x; tile_i < ntiles; tile_i += gridDim.x, ++k) {
+    const int64_t next = tile_i + gridDim.x;
+    if (next < ntiles) stage_tile(p, in, next, ntc, limit, smem_u32(tiles[(k + 1) & 1]), t);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
     const int64_t r0 = (tile_i / ntc) * QT_ROWS;
     const int64_t c0 = (tile_i % ntc) * QT_COLS;
-    // stage: 128 rows x 8 pieces of 16 bytes; 8 consecutive threads read one row's 128 bytes
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int v = t + QT_THREADS * i;
-      const int r = v >> 3, piece = v & 7;
-      const int64_t orow = r0 + r;
-      const int64_t g = orow / p.Gp, gi = orow - g * p.Gp;
-      uint4 val = make_uint4(0, 0, 0, 0);
-      if (gi < p.G && orow < limit)
-        val = *reinterpret_cast<const uint4*>(in + (g * p.G + gi) * p.N + c0 + piece * 8);
-      *reinterpret_cast<uint4*>(tile + r * QT_LD + piece * 16) = val;
-    }
+    const uint8_t* tile = tiles[k & 1];
     __syncthreads();
     if (p.q_row) {
       const uint8_t* src = tile + t * QT_LD;
@@ -76,29 +96,46 @@ __global__ void __launch_bounds__(QT_THREADS) nvfp4_quantize_kernel(const Nvfp4Q
       *reinterpret_cast<uint32_t*>(p.s_row + sf_mma_offset(row, c0 / 16, p.s_row_pad)) = scales;
     }
     if (p.q_col) {
-      const int c = t & (QT_COLS - 1), h = t >> 6;
-      const uint8_t* src = tile + (h * 64) * QT_LD + 2 * c;
-      uint32_t codes[8], scales = 0;
+      // thread t: columns 2 (t % 32) and 2 (t % 32) + 1, rows 32 (t / 32) .. + 31 (two blocks
+      // of 16 per column); a warp's 32-bit reads of one staged row are 128 contiguous bytes
+      const int cp = t & 31, h = t >> 5;
+      const uint8_t* src = tile + (h * 32) * QT_LD + 4 * cp;
+      uint32_t codes[2][4], scales[2] = {0, 0};
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        float v[16];
+      for (int b = 0; b < 2; ++b) {
+        float v0[16], v1[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          v[i] = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(
-                                     src + (16 * b + i) * QT_LD)
-                                 << 16);
-        if (p.rht) rht16_regs(v, p.rht_mask);
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(src + (16 * b + i) * QT_LD);
+          v0[i] = bf16_lo(w);
+          v1[i] = bf16_hi(w);
+        }
+        if (p.rht) {
+          rht16_regs(v0, p.rht_mask);
+          rht16_regs(v1, p.rht_mask);
+        }
         uint32_t q[2];
-        scales |= nvfp4_quant16(v, s_col, q) << (8 * b);
-        codes[2 * b] = q[0];
-        codes[2 * b + 1] = q[1];
+        scales[0] |= nvfp4_quant16(v0, s_col, q) << (8 * b);
+        codes[0][2 * b] = q[0];
+        codes[0][2 * b + 1] = q[1];
+        scales[1] |= nvfp4_quant16(v1, s_col, q) << (8 * b);
+        codes[1][2 * b] = q[0];
+        codes[1][2 * b + 1] = q[1];
       }
-      const int64_t col = c0 + c, rr = r0 + h * 64;
-      st_global_v8(p.q_col + col * (p.M / 2) + rr / 2, codes);
-      *reinterpret_cast<uint32_t*>(p.s_col + sf_mma_offset(col, rr / 16, p.s_col_pad)) = scales;
+      const int64_t rr = r0 + h * 32;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int64_t col = c0 + 2 * cp + k;
+        *reinterpret_cast<uint4*>(p.q_col + col * (p.M / 2) + rr / 2) =
+            make_uint4(codes[k][0], codes[k][1], codes[k][2], codes[k][3]);
+        *reinterpret_cast<uint16_t*>(p.s_col + sf_mma_offset(col, rr / 16, p.s_col_pad)) =
+            (uint16_t)scales[k];
+      }
     }
+    // every thread is done with this buffer before the next iteration refills it
     __syncthreads();
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // Plain amax of n bf16 values (n a multiple of 8, 16-byte aligned).
@@ -115,29 +152,33 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const uint4* in, int64_
 }
 
 // amax and amax of the 16-row-block rotation along the rows of a bf16 [M, N] matrix (M a
-// multiple of 16, N of 64, N / 64 < 65536). A CTA of 8 warps covers 128 rows (grid x) x 64
-// columns (grid y): lane l of warp w takes columns 2l, 2l+1 of rows 16w .. 16w+15 (4-byte
-// loads, 128 contiguous bytes a warp).
+// multiple of 16, N of 64, N / 128 < 65536). A CTA of 8 warps covers 128 rows (grid x) x 128
+// columns (grid y): lane l of warp w takes columns 4l .. 4l+3 of rows 16w .. 16w+15 (8-byte
+// loads, 256 contiguous bytes a warp and row).
 __global__ void __launch_bounds__(256) nvfp4_rht_amax_kernel(const uint16_t* in, int64_t M,
                                                              int64_t N, uint32_t mask,
                                                              float* out, float* out_rht) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int64_t c = blockIdx.y * 64 + 2 * lane;
+  const int64_t c = blockIdx.y * 128 + 4 * lane;
   const int64_t r0 = blockIdx.x * 128 + w * 16;
   float m = 0.f, mr = 0.f;
-  if (r0 < M) {
-    float a[16], b[16];
+  if (r0 < M && c < N) {
+    uint2 raw[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t v = *reinterpret_cast<const uint32_t*>(in + (r0 + i) * N + c);
-      a[i] = bf16_lo(v);
-      b[i] = bf16_hi(v);
-      m = fmaxf(m, fmaxf(fabsf(a[i]), fabsf(b[i])));
+    for (int i = 0; i < 16; ++i) raw[i] = *reinterpret_cast<const uint2*>(in + (r0 + i) * N + c);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t word = (k < 2) ? raw[i].x : raw[i].y;
+        v[i] = (k & 1) ? bf16_hi(word) : bf16_lo(word);
+        m = fmaxf(m, fabsf(v[i]));
+      }
+      rht16_regs(v, mask);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) mr = fmaxf(mr, fabsf(v[i]));
     }
-    rht16_regs(a, mask);
-    rht16_regs(b, mask);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) mr = fmaxf(mr, fmaxf(fabsf(a[i]), fabsf(b[i])));
   }
   amax_flush_warp(m, out);
   amax_flush_warp(mr, out_rht);
@@ -159,7 +200,8 @@ int64_t nvfp4_sf_bytes(int64_t rows, int64_t cols) {
 void launch_nvfp4_quantize(const Nvfp4QuantArgs& a, int num_sms, cudaStream_t s) {
   const int64_t tiles = (a.M / QT_ROWS) * (a.N / QT_COLS);
   if (tiles <= 0) return;
-  const int grid = (int)std::min<int64_t>(tiles, (int64_t)std::max(num_sms, 1) * 8);
+  // 36 KB of tile buffers a CTA: six CTAs per SM
+  const int grid = (int)std::min<int64_t>(tiles, (int64_t)std::max(num_sms, 1) * 6);
   nvfp4_quantize_kernel<<<grid, QT_THREADS, 0, s>>>(a);
   count_launch(s, MOE_K_NVFP4_QUANTIZE);
 }
@@ -175,7 +217,7 @@ void launch_nvfp4_amax(const void* in, int64_t n, float* out, int num_sms, cudaS
 void launch_nvfp4_rht_amax(const void* in, int64_t M, int64_t N, uint32_t mask, float* out,
                            float* out_rht, cudaStream_t s) {
   if (M <= 0 || N <= 0) return;
-  const dim3 grid((unsigned)((M + 127) / 128), (unsigned)(N / 64));
+  const dim3 grid((unsigned)((M + 127) / 128), (unsigned)((N + 127) / 128));
   nvfp4_rht_amax_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(in), M, N, mask, out,
                                              out_rht);
   count_launch(s, MOE_K_NVFP4_AMAX);

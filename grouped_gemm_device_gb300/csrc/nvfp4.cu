@@ -49,15 +49,18 @@ MOE_DEVICE void stage_tile(const Nvfp4QuantArgs& p, const uint16_t* in, int64_t 
   }
 }
 
-__global__ void __launch_bounds__(QT_THREADS, 8) nvfp4_quantize_kernel(const Nvfp4QuantArgs p) {
+__global__ void __launch_bounds__(QT_THREADS, 6) nvfp4_quantize_kernel(const Nvfp4QuantArgs p) {
   // two tile buffers: the next tile streams in while this one is quantised
   __shared__ __align__(16) uint8_t tiles[2][QT_ROWS * QT_LD];
+  __shared__ float enc_row[128], enc_col[128];
   const int t = threadIdx.x;
   const int64_t ntr = p.M / QT_ROWS, ntc = p.N / QT_COLS;
   const int64_t ntiles = ntr * ntc;
   const int64_t limit = p.row_limit ? (int64_t)*p.row_limit : p.M;
   const float s_row = p.q_row ? nvfp4_encode_scale(*p.amax_row) : 0.f;
   const float s_col = p.q_col ? nvfp4_encode_scale(*p.amax_col) : 0.f;
+  nvfp4_fill_enc_table(enc_row, s_row, t, QT_THREADS);
+  nvfp4_fill_enc_table(enc_col, s_col, t, QT_THREADS);  // visible after the first barrier
   const uint16_t* in = static_cast<const uint16_t*>(p.in);
   if ((int64_t)blockIdx.x < ntiles)
     stage_tile(p, in, blockIdx.x, ntc, limit, smem_u32(tiles[0]), t);
@@ -80,14 +83,8 @@ __global__ void __launch_bounds__(QT_THREADS, 8) nvfp4_quantize_kernel(const Nvf
         const uint4 w0 = *reinterpret_cast<const uint4*>(src + 32 * b);
         const uint4 w1 = *reinterpret_cast<const uint4*>(src + 32 * b + 16);
         const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        float v[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          v[2 * i] = bf16_lo(w[i]);
-          v[2 * i + 1] = bf16_hi(w[i]);
-        }
         uint32_t q[2];
-        scales |= nvfp4_quant16(v, s_row, q) << (8 * b);
+        scales |= nvfp4_quant16_bf16(w, s_row, enc_row, q) << (8 * b);
         codes[2 * b] = q[0];
         codes[2 * b + 1] = q[1];
       }
@@ -97,30 +94,28 @@ __global__ void __launch_bounds__(QT_THREADS, 8) nvfp4_quantize_kernel(const Nvf
     }
     if (p.q_col) {
       // thread t: columns 2 (t % 32) and 2 (t % 32) + 1, rows 32 (t / 32) .. + 31 (two blocks
-      // of 16 per column); a warp's 32-bit reads of one staged row are 128 contiguous bytes
+      // of 16 per column, the two columns as fp32 pairs); a warp's 32-bit reads of one staged
+      // row are 128 contiguous bytes
       const int cp = t & 31, h = t >> 5;
       const uint8_t* src = tile + (h * 32) * QT_LD + 4 * cp;
       uint32_t codes[2][4], scales[2] = {0, 0};
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
-        float v0[16], v1[16];
+        uint64_t x[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const uint32_t w = *reinterpret_cast<const uint32_t*>(src + (16 * b + i) * QT_LD);
-          v0[i] = bf16_lo(w);
-          v1[i] = bf16_hi(w);
+          x[i] = pack_f32x2(bf16_lo(w), bf16_hi(w));
         }
-        if (p.rht) {
-          rht16_regs(v0, p.rht_mask);
-          rht16_regs(v1, p.rht_mask);
-        }
-        uint32_t q[2];
-        scales[0] |= nvfp4_quant16(v0, s_col, q) << (8 * b);
-        codes[0][2 * b] = q[0];
-        codes[0][2 * b + 1] = q[1];
-        scales[1] |= nvfp4_quant16(v1, s_col, q) << (8 * b);
-        codes[1][2 * b] = q[0];
-        codes[1][2 * b + 1] = q[1];
+        if (p.rht) rht16_pair(x, p.rht_mask);
+        uint32_t qa[2], qb[2];
+        const uint32_t sc = nvfp4_quant16_pair(x, s_col, enc_col, qa, qb);
+        scales[0] |= (sc & 0xFFu) << (8 * b);
+        scales[1] |= (sc >> 8) << (8 * b);
+        codes[0][2 * b] = qa[0];
+        codes[0][2 * b + 1] = qa[1];
+        codes[1][2 * b] = qb[0];
+        codes[1][2 * b + 1] = qb[1];
       }
       const int64_t rr = r0 + h * 32;
 #pragma unroll

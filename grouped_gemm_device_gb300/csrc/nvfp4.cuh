@@ -72,6 +72,117 @@ MOE_DEVICE uint32_t nvfp4_quant16(const float* v, float S, uint32_t (&q)[2]) {
   return sb;
 }
 
+// ----------------------------------------------------------------- packed fp32 pairs
+// Two fp32 values in one 64-bit register; add / sub / mul of pairs are two independent IEEE
+// fp32 operations (round to nearest even), so they give exactly the scalar results.
+MOE_DEVICE uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+MOE_DEVICE float f32x2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+MOE_DEVICE float f32x2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+MOE_DEVICE uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+MOE_DEVICE uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+MOE_DEVICE uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// The encoding factors fp32(S / s_b) of one tensor for every E4M3 scale byte b < 127 (0 for
+// b = 0), so that a block's factor is a table read instead of a division; the same values
+// nvfp4_quant16 computes. Filled by `nthreads` threads; the caller synchronises.
+MOE_DEVICE void nvfp4_fill_enc_table(float* tab, float S, int tid, int nthreads) {
+  for (int b = tid; b < 128; b += nthreads) {
+    const float v = b < 127 ? e4m3_pos_value((uint32_t)b) : 0.f;
+    tab[b] = v > 0.f ? __fdiv_rn(S, v) : 0.f;
+  }
+}
+
+// One 16-value block of a row, given as 8 bf16 pairs: its codes in q[0..1], its scale byte
+// returned (enc_tab: the tensor's factor table).
+MOE_DEVICE uint32_t nvfp4_quant16_bf16(const uint32_t (&bw)[8], float S, const float* enc_tab,
+                                       uint32_t (&q)[2]) {
+  float m = 0.f;
+  uint64_t x[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float lo = bf16_lo(bw[i]), hi = bf16_hi(bw[i]);
+    m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
+    x[i] = pack_f32x2(lo, hi);
+  }
+  const uint32_t sb = cvt_e4m3x2(__fmul_rn(__fdiv_rn(m, 6.0f), S), 0.f) & 0xFFu;
+  const float e = enc_tab[sb];
+  const uint64_t e2 = pack_f32x2(e, e);
+  float w[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint64_t p = mul_f32x2(x[i], e2);
+    w[2 * i] = f32x2_lo(p);
+    w[2 * i + 1] = f32x2_hi(p);
+  }
+  q[0] = cvt_e2m1x8(w);
+  q[1] = cvt_e2m1x8(w + 8);
+  return sb;
+}
+
+// RHT of two columns at once: x[i] = (column a, column b) of row i of the block; the same
+// fp32 operations as rht16_regs on each column.
+MOE_DEVICE void rht16_pair(uint64_t (&x)[16], uint32_t mask) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    if ((mask >> i) & 1u) x[i] ^= 0x8000000080000000ull;
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i & m) continue;
+      const uint64_t a = x[i], b = x[i | m];
+      x[i] = add_f32x2(a, b);
+      x[i | m] = sub_f32x2(a, b);
+    }
+  }
+  const uint64_t quarter = pack_f32x2(0.25f, 0.25f);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) x[i] = mul_f32x2(x[i], quarter);
+}
+
+// Two 16-value column blocks held as pairs (x[i] = (a_i, b_i)): codes of column a in qa, of
+// column b in qb; returns the scale bytes (a in bits 0-7, b in bits 8-15).
+MOE_DEVICE uint32_t nvfp4_quant16_pair(const uint64_t (&x)[16], float S, const float* enc_tab,
+                                       uint32_t (&qa)[2], uint32_t (&qb)[2]) {
+  float ma = 0.f, mb = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    ma = fmaxf(ma, fabsf(f32x2_lo(x[i])));
+    mb = fmaxf(mb, fabsf(f32x2_hi(x[i])));
+  }
+  const uint32_t sa = cvt_e4m3x2(__fmul_rn(__fdiv_rn(ma, 6.0f), S), 0.f) & 0xFFu;
+  const uint32_t sb = cvt_e4m3x2(__fmul_rn(__fdiv_rn(mb, 6.0f), S), 0.f) & 0xFFu;
+  const uint64_t e2 = pack_f32x2(enc_tab[sa], enc_tab[sb]);
+  float wa[16], wb[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint64_t p = mul_f32x2(x[i], e2);
+    wa[i] = f32x2_lo(p);
+    wb[i] = f32x2_hi(p);
+  }
+  qa[0] = cvt_e2m1x8(wa);
+  qa[1] = cvt_e2m1x8(wa + 8);
+  qb[0] = cvt_e2m1x8(wb);
+  qb[1] = cvt_e2m1x8(wb + 8);
+  return sa | (sb << 8);
+}
+
 // RHT of 16 values held by one thread (index = row within the block).
 MOE_DEVICE void rht16_regs(float (&v)[16], uint32_t mask) {
 #pragma unroll

@@ -95,7 +95,7 @@ REPEATED = {
     "mxfp8_quantize": ("mxfp8_quant_x", "mxfp8_quant_w1", "mxfp8_quant_w2", "mxfp8_quant_dy"),
     "nvfp4_quantize": ("nvfp4_quant_x", "nvfp4_quant_w1", "nvfp4_quant_w2", "nvfp4_quant_a",
                        "nvfp4_quant_dy", "nvfp4_quant_dz"),
-    "nvfp4_amax": ("nvfp4_amax_x", "nvfp4_amax_w1", "nvfp4_amax_w2", "nvfp4_amax_dy"),
+    "nvfp4_amax": ("nvfp4_amax_w1", "nvfp4_amax_w2"),
 }
 # dense tensor-core rate of the operand type relative to bf16 (nominal: fp8 4.5 and fp4
 # 13.5 PFLOP/s against bf16's 2.25)
@@ -126,7 +126,6 @@ def kernel_bytes(cfg, recompute=False):
             "nvfp4_quant_x": R_cap * H * (2 + 2 * s), "nvfp4_quant_dy": R_cap * H * (2 + 2 * s),
             "nvfp4_quant_a": R_cap * F * (2 + 2 * s), "nvfp4_quant_dz": R_cap * N1 * (2 + 2 * s),
             "nvfp4_quant_w1": E * N1 * H * (2 + 2 * s), "nvfp4_quant_w2": E * F * H * (2 + 2 * s),
-            "nvfp4_amax_x": R_cap * H * 2, "nvfp4_amax_dy": R_cap * H * 2,
             "nvfp4_amax_w1": E * N1 * H * 2, "nvfp4_amax_w2": E * F * H * 2,
         }
     if cfg.precision == "mxfp8":

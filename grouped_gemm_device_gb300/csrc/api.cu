@@ -471,6 +471,21 @@ moe_status_t moe_route_permute(const moe_layer_desc_t* d, int32_t T, const float
   assign_rows_kernel<<<d->E, 1024, 0, s>>>(topk_ids, topk_probs, counts, T, d->E, d->k, d->align,
                                            w.L.R_cap, offsets, row_of, src_of, row_prob, err);
   count_launch(s, MOE_K_ASSIGN_ROWS);
+  if (d->precision == MOE_PREC_NVFP4) {
+    // gather fused with X's amax and rotated amax, then its copies: along H for FC1 and
+    // transposed, rotated along the expert's rows, for the FC1 weight gradient
+    const Fp4Problem p = fp4_problem(d, w);
+    e = cudaMemsetAsync(p.amax + AM_X, 0, 2 * sizeof(float), s);
+    if (e != cudaSuccess) return cuda_fail(e, "memset amax");
+    launch_gather_rows_amax(x, src_of, offsets, d->E, d->k, d->H, w.L.R_cap, p.rht_mask,
+                            w.at<void>(w.L.x_perm), p.amax + AM_X, p.amax + AM_XT, device_sms(),
+                            MOE_K_GATHER_X, s);
+    nv_quantize(w.at<void>(w.L.x_perm), w.L.R_cap, d->H, w.L.R_cap, w.L.R_cap, nullptr, p, AM_X,
+                AM_XT, p.x, p.xt, 1, s);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "route_permute launch");
+    return MOE_OK;
+  }
   gather_rows_kernel<<<grid_for(w.L.R_cap, 8), 256, 0, s>>>(
       static_cast<const uint4*>(x), src_of, offsets, d->E, d->k, d->H / 8, w.L.R_cap,
       w.at<uint4>(w.L.x_perm));
@@ -480,17 +495,6 @@ moe_status_t moe_route_permute(const moe_layer_desc_t* d, int32_t T, const float
     const MxProblem m = mx_problem(d, w);
     mx_quantize_operands(w.at<void>(w.L.x_perm), w.L.R_cap, d->H, w.L.R_cap, w.L.R_cap, m.x,
                          m.xt, s);
-  }
-  if (d->precision == MOE_PREC_NVFP4) {
-    // X's amax and rotated amax, then its copies: along H for FC1 and transposed, rotated
-    // along the expert's rows, for the FC1 weight gradient
-    const Fp4Problem p = fp4_problem(d, w);
-    e = cudaMemsetAsync(p.amax + AM_X, 0, 2 * sizeof(float), s);
-    if (e != cudaSuccess) return cuda_fail(e, "memset amax");
-    launch_nvfp4_rht_amax(w.at<void>(w.L.x_perm), w.L.R_cap, d->H, p.rht_mask, p.amax + AM_X,
-                          p.amax + AM_XT, s);
-    nv_quantize(w.at<void>(w.L.x_perm), w.L.R_cap, d->H, w.L.R_cap, w.L.R_cap, nullptr, p, AM_X,
-                AM_XT, p.x, p.xt, 1, s);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "route_permute launch");
@@ -620,11 +624,21 @@ static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* d
   p.w2 = w2;
   const int32_t* row_of = w.at<int32_t>(w.L.row_of);
   cudaError_t e;
-  // dY gathered into the permuted row order (zero for padding rows)
-  gather_rows_kernel<<<grid_for(w.L.R_cap, 8), 256, 0, s>>>(
-      static_cast<const uint4*>(dy), w.at<int32_t>(w.L.src_of), w.at<int32_t>(w.L.offsets), d->E,
-      d->k, d->H / 8, w.L.R_cap, w.at<uint4>(w.L.dy_perm));
-  count_launch(s, MOE_K_GATHER_DY);
+  // dY gathered into the permuted row order (zero for padding rows); for NVFP4 together with
+  // its amax and rotated amax
+  if (d->precision == MOE_PREC_NVFP4) {
+    float* am = w.at<float>(w.L.nv_amax);
+    if ((e = cudaMemsetAsync(am + AM_DY, 0, 4 * sizeof(float), s)) != cudaSuccess)
+      return cuda_fail(e, "memset amax");
+    launch_gather_rows_amax(dy, w.at<int32_t>(w.L.src_of), w.at<int32_t>(w.L.offsets), d->E,
+                            d->k, d->H, w.L.R_cap, d->rht_mask & 0xFFFFu, w.at<void>(w.L.dy_perm),
+                            am + AM_DY, am + AM_DYT, device_sms(), MOE_K_GATHER_DY, s);
+  } else {
+    gather_rows_kernel<<<grid_for(w.L.R_cap, 8), 256, 0, s>>>(
+        static_cast<const uint4*>(dy), w.at<int32_t>(w.L.src_of), w.at<int32_t>(w.L.offsets),
+        d->E, d->k, d->H / 8, w.L.R_cap, w.at<uint4>(w.L.dy_perm));
+    count_launch(s, MOE_K_GATHER_DY);
+  }
   if (d->precision == MOE_PREC_MXFP8) {
     MxProblem m = mx_problem(d, w);
     mx_quantize_operands(w.at<void>(w.L.dy_perm), w.L.R_cap, d->H, w.L.R_cap, w.L.R_cap, m.dy,
@@ -660,10 +674,6 @@ static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* d
   if (d->precision == MOE_PREC_NVFP4) {
     Fp4Problem m = fp4_problem(d, w);
     const int32_t* live = w.at<int32_t>(w.L.offsets) + d->E;
-    if ((e = cudaMemsetAsync(m.amax + AM_DY, 0, 4 * sizeof(float), s)) != cudaSuccess)
-      return cuda_fail(e, "memset amax");
-    launch_nvfp4_rht_amax(w.at<void>(w.L.dy_perm), w.L.R_cap, d->H, m.rht_mask, m.amax + AM_DY,
-                          m.amax + AM_DYT, s);
     nv_quantize(w.at<void>(w.L.dy_perm), w.L.R_cap, d->H, w.L.R_cap, w.L.R_cap, nullptr, m,
                 AM_DY, AM_DYT, m.dy, m.dyt, 1, s);
     // FC2 dgrad + dActivation: BF16 dZ plus its amax and the amax of its rotated transpose

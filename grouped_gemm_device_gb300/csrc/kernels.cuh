@@ -157,6 +157,12 @@ int64_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
 void launch_nvfp4_quantize(const Nvfp4QuantArgs& a, int num_sms, cudaStream_t s);
 // amax of n bf16 values (n % 8 == 0) max-merged into *out (caller zeroes it)
 void launch_nvfp4_amax(const void* in, int64_t n, float* out, int num_sms, cudaStream_t s);
+// NVFP4 layers: the gather of route / backward (x_perm[r] = x[token(r)], padding rows zero)
+// fused with the amax and the 16-row rotated amax of its output, max-merged into *amax and
+// *amax_rht (R_cap a multiple of 16, H of 8); kid is the launch's moe_kernel_id_t
+void launch_gather_rows_amax(const void* x, const int32_t* src_of, const int32_t* offsets, int E,
+                             int k, int H, int64_t R_cap, uint32_t mask, void* out, float* amax,
+                             float* amax_rht, int num_sms, int kid, cudaStream_t s);
 // amax and amax of the 16-row Hadamard rotation along the rows of [M, N] (M % 16 == 0,
 // N % 64 == 0), max-merged into *out and *out_rht
 void launch_nvfp4_rht_amax(const void* in, int64_t M, int64_t N, uint32_t mask, float* out,

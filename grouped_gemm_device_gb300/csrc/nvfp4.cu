@@ -179,7 +179,72 @@ __global__ void __launch_bounds__(256) nvfp4_rht_amax_kernel(const uint16_t* in,
   amax_flush_warp(mr, out_rht);
 }
 
+// Gather for an NVFP4 layer: x_perm[r] = x[token(r)] (zero for padding rows), as the plain
+// gather, plus the amax of x_perm and of its 16-row-block rotation, so that no separate pass
+// reads x_perm for them. A CTA takes 16 consecutive rows (one rotation block; R_cap is a
+// multiple of 128); thread t copies the 16-byte column pieces t, t + 256, ... of the 16 rows
+// and rotates its 8 columns as four fp32 pairs.
+__global__ void __launch_bounds__(256) gather_rows_amax_kernel(const uint4* __restrict__ x,
+                                                               const int32_t* __restrict__ src_of,
+                                                               const int32_t* __restrict__ offsets,
+                                                               int E, int k, int H8, int64_t R_cap,
+                                                               uint32_t mask,
+                                                               uint4* __restrict__ out,
+                                                               float* amax, float* amax_rht) {
+  __shared__ int64_t src_row[16];
+  const int used = offsets[E];
+  float m = 0.f, mr = 0.f;
+  for (int64_t r0 = (int64_t)blockIdx.x * 16; r0 < R_cap; r0 += (int64_t)gridDim.x * 16) {
+    __syncthreads();  // the previous block's rows are no longer read
+    if (threadIdx.x < 16) {
+      const int64_t r = r0 + threadIdx.x;
+      const int src = r < used ? src_of[r] : -1;
+      src_row[threadIdx.x] = src >= 0 ? (int64_t)(src / k) : -1;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < H8; i += blockDim.x) {
+      uint4 v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int64_t sr = src_row[j];
+        v[j] = sr >= 0 ? x[sr * H8 + i] : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) out[(r0 + j) * H8 + i] = v[j];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint64_t col[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t word = w == 0 ? v[j].x : w == 1 ? v[j].y : w == 2 ? v[j].z : v[j].w;
+          const float lo = bf16_lo(word), hi = bf16_hi(word);
+          m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
+          col[j] = pack_f32x2(lo, hi);
+        }
+        rht16_pair(col, mask);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          mr = fmaxf(mr, fmaxf(fabsf(f32x2_lo(col[j])), fabsf(f32x2_hi(col[j]))));
+      }
+    }
+  }
+  amax_flush_warp(m, amax);
+  amax_flush_warp(mr, amax_rht);
+}
+
 }  // namespace
+
+void launch_gather_rows_amax(const void* x, const int32_t* src_of, const int32_t* offsets, int E,
+                             int k, int H, int64_t R_cap, uint32_t mask, void* out, float* amax,
+                             float* amax_rht, int num_sms, int kid, cudaStream_t s) {
+  const int64_t blocks = R_cap / 16;
+  if (blocks <= 0) return;
+  const int grid = (int)std::min<int64_t>(blocks, (int64_t)std::max(num_sms, 1) * 8);
+  gather_rows_amax_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(x), src_of, offsets, E,
+                                               k, H / 8, R_cap, mask, static_cast<uint4*>(out),
+                                               amax, amax_rht);
+  count_launch(s, kid);
+}
 
 bool nvfp4_quantize_shape_ok(int64_t M, int64_t N) {
   return M > 0 && N > 0 && M % QT_ROWS == 0 && N % QT_COLS == 0;

@@ -159,7 +159,9 @@ moe_status_t moe_workspace_layout(const moe_layer_desc_t *desc, moe_ws_layout_t 
  *   topk_probs fp32 [T, k]   out: softmax over the k chosen logits
  *   counts     int32 [E]     out: tokens routed to each expert
  * Writes offsets, row_of, src_of, row_prob and x_perm (and, for MXFP8 layers, the MXFP8
- * row-wise and column-wise copies of x_perm) into ws. T in [0, T_max]. */
+ * row-wise and column-wise copies of x_perm; for NVFP4 layers the amax and rotated amax of
+ * x_perm, taken during the gather, and its row-wise and rotated transposed NVFP4 copies) into
+ * ws. T in [0, T_max]. */
 moe_status_t moe_route_permute(const moe_layer_desc_t *desc, int32_t T, const float *logits,
                                const void *x, int32_t *topk_ids, float *topk_probs,
                                int32_t *counts, void *ws, size_t ws_bytes, moe_stream_t stream);
@@ -173,7 +175,10 @@ moe_status_t moe_route_permute(const moe_layer_desc_t *desc, int32_t T, const fl
  *   w2        bf16 [E, F, H]   FC2 weight (logical [F, H] per expert)
  *   y         bf16 [T, H]      out
  * Requires a preceding moe_route_permute on the same ws. Saves z and a_s in ws for the
- * backward. MXFP8 layers also quantise both weights (both directions) into ws first. */
+ * backward. MXFP8 layers also quantise both weights (both directions) into ws first. NVFP4
+ * layers take the weights' amax and NVFP4 copies (both directions) first; their FC1 kernel
+ * also writes the amax and the rotated amax of a_s into ws (nv_amax), from which a_s's NVFP4
+ * copies are made for FC2 and for the FC2 weight gradient. */
 moe_status_t moe_grouped_mlp_fwd(const moe_layer_desc_t *desc, int32_t T, const void *w1_packed,
                                  const void *w2, void *y, void *ws, size_t ws_bytes,
                                  moe_stream_t stream);
@@ -188,7 +193,9 @@ moe_status_t moe_grouped_mlp_fwd(const moe_layer_desc_t *desc, int32_t T, const 
  *                                tokens gets exact zeros)
  *   dw2        bf16 [E, F, H]    out
  *   d_probs    fp32 [T, k]       out, gradient of topk_probs
- * Requires the forward's ws contents. */
+ * Requires the forward's ws contents. NVFP4 layers gather dY together with its amax and
+ * rotated amax, and their FC2-dgrad kernel writes dZ with its amax and rotated amax; every
+ * GEMM then reads NVFP4 copies, the weight-gradient operands rotated along the tokens. */
 moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t *desc, int32_t T, const void *dy,
                                  const void *w1_packed, const void *w2, void *dx,
                                  void *dw1_packed, void *dw2, float *d_probs, void *ws,

@@ -56,22 +56,6 @@ MOE_DEVICE uint32_t cvt_e2m1x8(const float* v) {
   return r;
 }
 
-// One 16-value block: its 16 E2M1 codes in q[0..1] and its E4M3 scale byte (returned).
-MOE_DEVICE uint32_t nvfp4_quant16(const float* v, float S, uint32_t (&q)[2]) {
-  float m = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
-  const uint32_t sb = cvt_e4m3x2(__fmul_rn(__fdiv_rn(m, 6.0f), S), 0.f) & 0xFFu;
-  const float sbf = e4m3_pos_value(sb);
-  const float enc = sbf > 0.f ? __fdiv_rn(S, sbf) : 0.f;
-  float w[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) w[i] = __fmul_rn(v[i], enc);
-  q[0] = cvt_e2m1x8(w);
-  q[1] = cvt_e2m1x8(w + 8);
-  return sb;
-}
-
 // ----------------------------------------------------------------- packed fp32 pairs
 // Two fp32 values in one 64-bit register; add / sub / mul of pairs are two independent IEEE
 // fp32 operations (round to nearest even), so they give exactly the scalar results.
@@ -99,8 +83,8 @@ MOE_DEVICE uint64_t mul_f32x2(uint64_t a, uint64_t b) {
 }
 
 // The encoding factors fp32(S / s_b) of one tensor for every E4M3 scale byte b < 127 (0 for
-// b = 0), so that a block's factor is a table read instead of a division; the same values
-// nvfp4_quant16 computes. Filled by `nthreads` threads; the caller synchronises.
+// b = 0: the block is all zeros), so that a block's factor is a table read instead of a
+// division, with the same IEEE result. Filled by `nthreads` threads; the caller synchronises.
 MOE_DEVICE void nvfp4_fill_enc_table(float* tab, float S, int tid, int nthreads) {
   for (int b = tid; b < 128; b += nthreads) {
     const float v = b < 127 ? e4m3_pos_value((uint32_t)b) : 0.f;

@@ -201,17 +201,35 @@ def _small_layer(seed=8, T=48, E=4, H=64, F=64, k=2):
     return lg, x, W1, W2, dy, k
 
 
-def test_layer_without_quantisers_is_the_bf16_oracle(monkeypatch):
+_ACTS = {
+    "swiglu": om.ActParams(),
+    "clamped_swiglu": om.ActParams("clamped_swiglu", 1.702, 2.0, -2.0, 2.0, 1.0),
+    "geglu": om.ActParams("geglu"),
+    "srelu": om.ActParams("srelu"),
+}
+
+
+@pytest.mark.parametrize("kind,skew", [("swiglu", False), ("clamped_swiglu", True),
+                                       ("geglu", False), ("srelu", True)])
+def test_layer_without_quantisers_is_the_bf16_oracle(monkeypatch, kind, skew):
     """Taking out the quantisers and the bf16 roundings leaves the plain layer: this pins the
     stage-by-stage plumbing (segments, the d_prob and weight-gradient products, the rotation
-    of both weight-gradient operands, which cancels)."""
-    lg, x, W1, W2, dy, k = _small_layer()
-    act = om.ActParams()
+    of both weight-gradient operands, which cancels), for every activation, and with routing
+    skewed so that some experts get no tokens."""
+    lg, x, W1, W2, dy, k = _small_layer(E=8 if skew else 4)
+    if skew:
+        lg = lg.copy()
+        lg[:, :3] += 4.0        # experts 0-2 take (nearly) every token
+    act = _ACTS[kind]
+    if not act.gated:
+        W1 = W1[:, :, :W2.shape[1]]
     monkeypatch.setattr(nv, "fake_quant", lambda v, axis, S: np.asarray(v, dtype=np.float64))
     monkeypatch.setattr(nv, "to_f32", lambda v: np.asarray(v, dtype=np.float64))
     monkeypatch.setattr(om, "bf16_round", lambda v: np.asarray(v, dtype=np.float64))
     got = om.layer_nvfp4(lg, x, W1, W2, k, act, 0x3C5A, dy=dy)
     ref = om.layer(lg, x, W1, W2, k, act, dy=dy)
+    if skew:
+        assert (np.bincount(got.ids.ravel(), minlength=W1.shape[0]) == 0).any()
     dW1, dW2 = om.stack_weight_grads(ref, W1.shape[0])
     for a, b in [(got.y, ref.y), (got.dx, ref.dx), (got.dW1, dW1), (got.dW2, dW2),
                  (got.d_probs, ref.d_probs)]:

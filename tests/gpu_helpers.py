@@ -55,7 +55,7 @@ class Inputs:
                         keep_intermediates=keep)
 
 
-class GpuRun:
+class LayerRun:
     """Runs route -> fwd -> bwd for the inputs on cuda and keeps the results."""
 
     def __init__(self, inp: Inputs, T_max=None, sm_margin=0, backward=True, recompute=False):
@@ -110,7 +110,7 @@ class GpuRun:
 def check_weight_grads_16_byte_aligned(cfg):
     """Weight gradients written to buffers that are 16- but not 32-byte aligned take the
     128-bit store path of the GEMM epilogue; they must equal the 256-bit path bit for bit."""
-    run = GpuRun(Inputs(cfg))
+    run = LayerRun(Inputs(cfg))
     dw1, dw2 = run.dw1p.clone(), run.dw2.clone()
     L = run.layer
     b1 = torch.zeros(L.dw1.numel() + 8, dtype=torch.bfloat16, device="cuda")

@@ -8,7 +8,7 @@ import torch
 from grouped_gemm_device_gb300 import synth
 from oracle import moe as om
 
-from .gpu_helpers import GpuRun, Inputs, act_params, rel_fro, to_np
+from .gpu_helpers import LayerRun, Inputs, act_params, rel_fro, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -20,7 +20,7 @@ def _cfg(prec, T):
 
 @pytest.mark.parametrize("prec", ["bf16", "mxfp8", "nvfp4"])
 def test_step_with_no_tokens(lib, prec):
-    run = GpuRun(Inputs(_cfg(prec, 0)), T_max=64)
+    run = LayerRun(Inputs(_cfg(prec, 0)), T_max=64)
     assert run.y.shape[0] == 0 and run.dx.shape[0] == 0 and run.d_probs.shape[0] == 0
     assert not run.dw1p.any() and not run.dw2.any()
     assert torch.isfinite(run.dw1p.float()).all() and torch.isfinite(run.dw2.float()).all()
@@ -30,7 +30,7 @@ def test_step_with_no_tokens(lib, prec):
 def test_nvfp4_single_token(lib):
     cfg = _cfg("nvfp4", 1)
     inp = Inputs(cfg)
-    run = GpuRun(inp, T_max=64)
+    run = LayerRun(inp, T_max=64)
     r = om.layer_nvfp4(inp.logits, om.bf16_to_f64(inp.x), om.bf16_to_f64(inp.w1),
                        om.bf16_to_f64(inp.w2), cfg.k, act_params(cfg), synth.gen_rht_mask(cfg),
                        dy=om.bf16_to_f64(inp.dy), align=cfg.align)

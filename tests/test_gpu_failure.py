@@ -9,7 +9,7 @@ import torch
 import grouped_gemm_device_gb300 as g
 from grouped_gemm_device_gb300 import synth
 
-from .gpu_helpers import BF16_TOL, GpuRun, Inputs, rel_fro, to_np
+from .gpu_helpers import BF16_TOL, LayerRun, Inputs, rel_fro, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -38,7 +38,7 @@ def test_context_usable_after_a_timeout(lib):
     g.moe_selftest_wait_timeout(err, 5_000_000)
     cfg = synth.CONFIGS["tiny"]
     inp = Inputs(cfg)
-    run = GpuRun(inp)
+    run = LayerRun(inp)
     assert int(err.item()) == TIMEOUT
     assert run.layer.device_error() == 0
     ref = inp.oracle(backward=False)

@@ -7,7 +7,7 @@ import torch
 
 from grouped_gemm_device_gb300 import synth
 
-from .gpu_helpers import (BF16_TOL, GpuRun, Inputs, check_weight_grads_16_byte_aligned, rel_fro,
+from .gpu_helpers import (BF16_TOL, LayerRun, Inputs, check_weight_grads_16_byte_aligned, rel_fro,
                           to_np)
 
 pytestmark = pytest.mark.gpu
@@ -33,7 +33,7 @@ CASES = {
 def check_layer(cfg, inp=None, run=None, tol=BF16_TOL):
     inp = inp or Inputs(cfg)
     ref = inp.oracle()
-    run = run or GpuRun(inp)
+    run = run or LayerRun(inp)
     assert run.layer.device_error() == 0
     errs = {"y": rel_fro(to_np(run.y), ref.y), "dx": rel_fro(to_np(run.dx), ref.dx),
             "d_probs": rel_fro(to_np(run.d_probs), ref.d_probs)}
@@ -59,7 +59,7 @@ def test_saved_intermediates_match_oracle(lib):
     cfg = CASES["multi_tile"]
     inp = Inputs(cfg)
     ref = inp.oracle()
-    run = GpuRun(inp)
+    run = LayerRun(inp)
     off = run.layer.offsets().cpu().numpy()
     z = run.unpack_cols(to_np(run.ws("z", torch.bfloat16, cfg.N1)))
     a_s = to_np(run.ws("a_s", torch.bfloat16, cfg.F))
@@ -82,8 +82,8 @@ def test_weight_grads_into_16_byte_aligned_buffers(lib):
 def test_sm_margin_and_rerun_are_deterministic(lib):
     cfg = CASES["multi_tile"]
     inp = Inputs(cfg)
-    r1 = GpuRun(inp, sm_margin=0)
-    r2 = GpuRun(inp, sm_margin=100)
+    r1 = LayerRun(inp, sm_margin=0)
+    r2 = LayerRun(inp, sm_margin=100)
     assert torch.equal(r1.y, r2.y) and torch.equal(r1.dx, r2.dx)
     assert torch.equal(r1.dw1p, r2.dw1p) and torch.equal(r1.dw2, r2.dw2)
     assert torch.equal(r1.d_probs, r2.d_probs)
@@ -97,7 +97,7 @@ def test_cuda_graph_capture_and_replay_with_new_routing(lib):
     it after overwriting the logits in place - the new routing must be used."""
     cfg = CASES["skewed"]
     inp = Inputs(cfg)
-    run = GpuRun(inp)
+    run = LayerRun(inp)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     graph = torch.cuda.CUDAGraph()

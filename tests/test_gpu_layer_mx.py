@@ -7,7 +7,7 @@ import torch
 
 from grouped_gemm_device_gb300 import synth
 
-from .gpu_helpers import (MX_TOL, GpuRun, Inputs, check_weight_grads_16_byte_aligned, rel_fro,
+from .gpu_helpers import (MX_TOL, LayerRun, Inputs, check_weight_grads_16_byte_aligned, rel_fro,
                           to_np)
 from .test_gpu_layer import check_layer
 
@@ -37,7 +37,7 @@ def test_mx_fc1_output_matches_oracle(lib):
     cfg = CASES["mx_small"]
     inp = Inputs(cfg)
     ref = inp.oracle(backward=False)
-    run = GpuRun(inp, backward=False)
+    run = LayerRun(inp, backward=False)
     assert run.layer.device_error() == 0
     off = run.layer.offsets().cpu().numpy()
     assert np.all(off % 128 == 0)

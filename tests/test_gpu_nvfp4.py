@@ -22,7 +22,7 @@ from oracle import moe as om
 from oracle import mxfp8 as omx
 from oracle import nvfp4 as nv
 
-from .gpu_helpers import BF16_TOL, GpuRun, Inputs, act_params, bf16_dev, rel_fro, to_np
+from .gpu_helpers import BF16_TOL, LayerRun, Inputs, act_params, bf16_dev, rel_fro, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -140,7 +140,7 @@ CASES = {
 def test_nvfp4_layer_parity(lib, name):
     cfg = CASES[name]
     inp = Inputs(cfg)
-    run = GpuRun(inp)
+    run = LayerRun(inp)
     mask = synth.gen_rht_mask(cfg)
     r = om.layer_nvfp4(inp.logits, om.bf16_to_f64(inp.x), om.bf16_to_f64(inp.w1),
                        om.bf16_to_f64(inp.w2), cfg.k, act_params(cfg), mask,
@@ -180,14 +180,14 @@ def test_nvfp4_layer_is_not_the_bf16_layer(lib):
     """The tolerance discriminates: the same layer without quantisation is far outside it."""
     cfg = CASES["swiglu"]
     inp = Inputs(cfg)
-    run = GpuRun(inp, backward=False)
+    run = LayerRun(inp, backward=False)
     ref = om.layer(inp.logits, om.bf16_to_f64(inp.x), om.bf16_to_f64(inp.w1),
                    om.bf16_to_f64(inp.w2), cfg.k, act_params(cfg), align=cfg.align)
     assert rel_fro(to_np(run.y), ref.y) > 10 * NV_TOL
 
 
 def test_nvfp4_layer_repeat_is_deterministic(lib):
-    run = GpuRun(Inputs(CASES["geglu_ragged"]))
+    run = LayerRun(Inputs(CASES["geglu_ragged"]))
     y, dx, dw1, dw2, dp = (t.clone() for t in (run.y, run.dx, run.dw1p, run.dw2, run.d_probs))
     run.run()
     assert torch.equal(run.y, y) and torch.equal(run.dx, dx) and torch.equal(run.dw2, dw2)

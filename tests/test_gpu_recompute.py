@@ -8,7 +8,7 @@ import torch
 import grouped_gemm_device_gb300 as g
 from grouped_gemm_device_gb300 import synth
 
-from .gpu_helpers import BF16_TOL, GpuRun, Inputs, rel_fro, to_np
+from .gpu_helpers import BF16_TOL, LayerRun, Inputs, rel_fro, to_np
 from .test_gpu_layer import check_layer
 
 pytestmark = pytest.mark.gpu
@@ -30,7 +30,7 @@ CASES = {
 def test_recompute_layer_matches_oracle(lib, name):
     cfg = CASES[name]
     inp = Inputs(cfg)
-    run = GpuRun(inp, recompute=True)
+    run = LayerRun(inp, recompute=True)
     assert run.layer.layout.z == 2 ** 64 - 1
     check_layer(cfg, inp=inp, run=run)
 
@@ -41,8 +41,8 @@ def test_recompute_agrees_with_saved_z(lib):
     Each path is within 5e-3 of the oracle, so they are within 2 x 5e-3 of each other."""
     cfg = CASES["multi_tile"]
     inp = Inputs(cfg)
-    keep = GpuRun(inp)
-    rc = GpuRun(inp, recompute=True)
+    keep = LayerRun(inp)
+    rc = LayerRun(inp, recompute=True)
     assert torch.equal(keep.y, rc.y)
     assert torch.equal(keep.dw2, rc.dw2)
     for a, b in ((rc.dx, keep.dx), (rc.d_probs, keep.d_probs), (rc.dw1p, keep.dw1p)):

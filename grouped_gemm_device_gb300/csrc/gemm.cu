@@ -9,8 +9,9 @@
 // the persistent tile loop over device offsets is the host-sync section's design; the
 // `num_ctas` cap is the configurable SM margin.
 //
-// CTA = 6 warps: warp 0 issues TMA loads, warp 1 owns the TMEM allocation and issues the
-// MMAs (one thread), warps 2..5 drain the accumulator (warp w reads TMEM lanes 32*(w%4)..).
+// CTA = 10 warps: warp 0 issues TMA loads, warp 1 owns the TMEM allocation and issues the
+// MMAs (one thread), warps 2..9 drain the accumulator (warp w reads TMEM lanes 32*(w%4)..
+// and one half of the tile's columns).
 // Two TMEM accumulators of BN fp32 columns let the epilogue of tile i overlap the mainloop
 // of tile i+1. Tiles are 128 x BN; k-blocks are 64 bf16 (one 128-byte swizzle row).
 //
@@ -398,7 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     int acc_i = 0;
-    for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      // every give-up decision is warp-uniform: the epilogue uses full-warp TMEM loads,
+      // shuffles and __syncwarp, which all 32 lanes must reach together
+      if (__shfl_sync(0xFFFFFFFFu, *abort, 0)) break;
       TileInfo t;
       decode_tile<BN, KG>(tile, p, c, MT, NT, t);
       const int row = t.m0 + q * 32 + lane;
@@ -422,7 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int acc = acc_i & 1;
       const uint32_t acc_phase = (acc_i >> 1) & 1;
-      if (!mbar_wait(&c.tfull[acc], acc_phase, abort, p.err)) break;
+      const bool got = mbar_wait(&c.tfull[acc], acc_phase, abort, p.err);
+      if (!__all_sync(0xFFFFFFFFu, got)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       uint32_t r[32];

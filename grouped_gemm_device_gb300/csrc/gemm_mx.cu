@@ -400,7 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
     const uint8_t* zst = smem + L::ZST_OFF + (warp - 2) * ZST_WARP_BYTES;
     const uint32_t zst_a = smem_u32(zst);
     int acc_i = 0;
-    for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      // every give-up decision is warp-uniform (full-warp TMEM loads, shuffles, __syncwarp)
+      if (__shfl_sync(0xFFFFFFFFu, *abort, 0)) break;
       TileInfo t;
       decode_tile<KG>(tile, p, c, MT, NT, t);
       const int row0 = t.m0 + q * 32;  // first row of this warp's 32-row block
@@ -426,7 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
         }
       }
       const float prob = EPI == EPI_STORE ? 0.f : p.row_prob[row];
-      if (!mbar_wait(&c.tfull, acc_i & 1, abort, p.err)) break;
+      const bool got = mbar_wait(&c.tfull, acc_i & 1, abort, p.err);
+      if (!__all_sync(0xFFFFFFFFu, got)) break;
       tc_fence_after();
       if constexpr (EPI == EPI_GLU) {
         // GLU: drain the 128 columns as fp32 (the activation and its MXFP8 blocks are computed

@@ -269,13 +269,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;  // dA_s columns [64 * half, 64 * half + 64) of the tile
     const int ilv = p.ilv;
     int acc_i = 0;
-    for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      // every give-up decision is warp-uniform (full-warp TMEM loads and __syncwarp)
+      if (__shfl_sync(0xFFFFFFFFu, *abort, 0)) break;
       Tile t;
       decode(tile, p, c, NT, t);
       const int row = t.m0 + q * 32 + lane;
       const bool row_ok = row < t.row_end;
       const float prob = row_ok ? p.row_prob[row] : 0.f;
-      if (!mbar_wait(&c.tfull, acc_i & 1, abort, p.err)) break;
+      const bool got = mbar_wait(&c.tfull, acc_i & 1, abort, p.err);
+      if (!__all_sync(0xFFFFFFFFu, got)) break;
       tc_fence_after();
       const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
       uint16_t* dzrow = p.dz + (int64_t)row * p.N1 + 2 * t.n0;

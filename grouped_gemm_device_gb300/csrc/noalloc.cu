@@ -12,9 +12,10 @@
 
 namespace moe {
 
-// Limits of the static scratch.
-constexpr int64_t kNoallocMaxPairs = 131072;                 // T_max * k
-constexpr int64_t kNoallocMaxRows = kNoallocMaxPairs + 256 * 31;  // R_cap with E <= 256
+// Limits of the static scratch: T_max * k routed pairs, and R_cap = T_max * k + E * (align-1)
+// rows for E <= 256 experts and any BF16 segment alignment (32, 64 or 128).
+constexpr int64_t kNoallocMaxPairs = 131072;
+constexpr int64_t kNoallocMaxRows = kNoallocMaxPairs + 256 * 127;
 constexpr size_t kNoallocErrBytes = 256;
 constexpr size_t kNoallocBytes =
     kNoallocErrBytes + (size_t)kNoallocMaxPairs * 4 + (size_t)kNoallocMaxRows * 4 * 2;
@@ -22,9 +23,44 @@ constexpr size_t kNoallocBytes =
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocBytes];
 
 // Host-side device addresses of g_noalloc_scratch, one per device (the symbol's name in host
-// code is only a host stand-in; the device address must come from cudaGetSymbolAddress).
+// code is only a host stand-in; the device address must come from cudaGetSymbolAddress),
+// each with the id of the CUDA context it was looked up in. A context that is destroyed and
+// created again (cudaDeviceReset, a primary context reset) loads the module again, possibly
+// at another address: a call whose current context has another id looks the address up again.
 static std::mutex g_noalloc_mu;
 static void* g_noalloc_ptr[128];
+static unsigned long long g_noalloc_ctx[128];
+
+// Id of the calling thread's current context (0 when none is current or the driver entry
+// points are unavailable), through the runtime's driver entry-point lookup so that the
+// library does not link the driver library itself.
+typedef int (*ctx_get_current_fn)(void**);
+typedef int (*ctx_get_id_fn)(void*, unsigned long long*);
+static unsigned long long current_ctx_id() {
+  static ctx_get_current_fn get_cur = nullptr;
+  static ctx_get_id_fn get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    void* f0 = nullptr;
+    void* f1 = nullptr;
+    cudaDriverEntryPointQueryResult q0, q1;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f0, 12000, cudaEnableDefault,
+                                         &q0) == cudaSuccess &&
+        q0 == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f1, 12000, cudaEnableDefault, &q1) ==
+            cudaSuccess &&
+        q1 == cudaDriverEntryPointSuccess) {
+      get_cur = reinterpret_cast<ctx_get_current_fn>(f0);
+      get_id = reinterpret_cast<ctx_get_id_fn>(f1);
+    }
+    looked_up = true;
+  }
+  if (!get_cur || !get_id) return 0;
+  void* ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_cur(&ctx) != 0 || ctx == nullptr || get_id(ctx, &id) != 0) return 0;
+  return id;
+}
 
 static moe_status_t noalloc_scratch(void** out) {
   int dev = -1;
@@ -34,7 +70,8 @@ static moe_status_t noalloc_scratch(void** out) {
     return MOE_ERR_CUDA;
   }
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  const unsigned long long ctx = current_ctx_id();
+  if (!g_noalloc_ptr[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) {
@@ -42,6 +79,8 @@ static moe_status_t noalloc_scratch(void** out) {
       return MOE_ERR_CUDA;
     }
     g_noalloc_ptr[dev] = p;
+    // the look-up made the device's primary context current if none was
+    g_noalloc_ctx[dev] = current_ctx_id();
   }
   *out = g_noalloc_ptr[dev];
   return MOE_OK;
@@ -68,9 +107,14 @@ extern "C" moe_status_t moe_route_permute_noalloc(const moe_layer_desc_t* d, int
   }
   const int64_t pairs = (int64_t)d->T_max * d->k;
   const int64_t R_cap = pairs + (int64_t)d->E * (d->align - 1);
-  if (pairs > kNoallocMaxPairs || R_cap > kNoallocMaxRows) {
+  if (pairs > kNoallocMaxPairs) {
     set_last_error("moe_route_permute_noalloc: T_max*k exceeds the static scratch limit of "
                    "131072 routed (token, expert) pairs");
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (R_cap > kNoallocMaxRows) {
+    set_last_error("moe_route_permute_noalloc: T_max*k + E*(align-1) exceeds the static "
+                   "scratch limit of 163584 permuted rows");
     return MOE_ERR_UNSUPPORTED;
   }
   if (T < 0 || T > d->T_max) {

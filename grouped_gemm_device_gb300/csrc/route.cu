@@ -17,6 +17,10 @@ namespace moe {
 // One warp per token. Each lane keeps E/32 logits; k rounds of a warp arg-max pick the
 // experts (larger logit first, ties to the lower index). Probabilities are the softmax over
 // the chosen logits. Expert counts are accumulated in a block histogram, then globally.
+// Non-finite logits: a NaN is read as -inf, so every round picks an untaken expert in [0, E)
+// (its arg-max starts from -inf, which any untaken expert equals or beats); a chosen logit
+// equal to the chosen maximum gets weight 1 (exp(0) for finite ones), which is the limit of
+// the softmax when the maximum is +inf (shared among the +inf ones) or -inf (uniform).
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
                                                          int E, int k, int32_t* __restrict__ ids,
                                                          float* __restrict__ probs,
@@ -33,7 +37,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       int e = i * 32 + lane;
-      v[i] = (i < per_lane && e < E) ? logits[(size_t)t * E + e] : -INFINITY;
+      const float lv = (i < per_lane && e < E) ? logits[(size_t)t * E + e] : -INFINITY;
+      v[i] = lv == lv ? lv : -INFINITY;
     }
     bool taken[8];
 #pragma unroll
@@ -71,7 +76,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
       float w[8];
       float s = 0.f;
       for (int j = 0; j < k; ++j) {
-        w[j] = expf(sel_v[j] - m);
+        w[j] = sel_v[j] == m ? 1.0f : expf(sel_v[j] - m);
         s += w[j];
       }
       const float inv = 1.0f / s;

@@ -238,10 +238,13 @@ moe_status_t moe_grouped_mlp_bwd_ex(const moe_layer_desc_t *desc, int32_t T, con
  * Its scratch (row map, per-row source and probability, an error word) is a fixed
  * file-scope device array of about 1.6 MB inside the library, held by every GPU that loads
  * the library until the process exits. Limit: T_max*k <= 131072 routed (token, expert)
- * pairs (E <= 256); larger descriptions return MOE_ERR_UNSUPPORTED before any launch. Only
+ * pairs, which with E <= 256 and any segment alignment (32, 64, 128) keeps R_cap within the
+ * array's 163584 rows; larger descriptions return MOE_ERR_UNSUPPORTED before any launch. Only
  * BF16 layers. The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before any stream
- * capture. All calls on a device share the array and it keeps the last call's contents: the
+ * (cudaGetSymbolAddress) with that device current, and looks it up again when the device's
+ * context has changed since (after cudaDeviceReset, for example); make the first call after
+ * such a change before any stream capture. All calls on a device share the array and it keeps
+ * the last call's contents: the
  * error word and counts are cleared at the start of every call, and calls whose execution
  * overlaps on the GPU (for example on two streams) race. Capacity errors detected on the
  * device are not reported by this entry point (they cannot occur when T <= T_max). */

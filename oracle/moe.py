@@ -67,13 +67,20 @@ def route(logits: np.ndarray, k: int):
     logits: fp32 [T, E]. Returns ids int64 [T, k], probs fp64 [T, k].
     [TE-MoE] Figure 1: a top-2 router sends each token to two of eight experts and the
     outputs are combined as a weighted sum.
+
+    Non-finite logits (R1): a NaN logit counts as -inf; a chosen logit equal to the chosen
+    maximum has weight 1, the others exp(l - max) - the limit of the softmax when the maximum
+    is +inf (weight shared by the +inf logits) or -inf (uniform over the k chosen).
     """
     lg = np.asarray(logits, dtype=np.float32)
+    lg = np.where(np.isnan(lg), np.float32(-np.inf), lg)
     T, E = lg.shape
     # stable sort of the negated logits keeps equal logits in index order
     ids = np.argsort(-lg, axis=1, kind="stable")[:, :k]
     chosen = np.take_along_axis(lg, ids, axis=1).astype(np.float64)
-    ex = np.exp(chosen - chosen.max(axis=1, keepdims=True))
+    m = chosen.max(axis=1, keepdims=True)
+    with np.errstate(invalid="ignore"):
+        ex = np.where(chosen == m, 1.0, np.exp(chosen - m))
     probs = ex / ex.sum(axis=1, keepdims=True)
     return ids.astype(np.int64), probs
 

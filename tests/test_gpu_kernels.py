@@ -125,6 +125,23 @@ def test_route_all_tokens_one_expert_and_ties(lib):
     _route_check(cfg, lg)
 
 
+def test_route_non_finite_logits(lib):
+    # NaN logits count as -inf; every chosen id stays in [0, E) and the probabilities are the
+    # softmax's limits (uniform when every chosen logit is -inf)
+    cfg = synth.LayerConfig("nan", T=300, E=40, k=4, H=64, F=64, seed=23)
+    lg = synth.gen_logits(cfg)
+    lg[0, :] = np.nan
+    lg[1, :] = -np.inf
+    lg[2, ::3] = np.nan
+    lg[3, [5, 17]] = np.inf
+    lg[4, :37] = np.nan
+    lg[5, 1::2] = -np.inf
+    lg[5, ::2] = np.nan
+    lg[6, 39] = np.inf
+    lg[7, :] = np.inf
+    _route_check(cfg, lg)
+
+
 def test_route_with_T_below_capacity_and_reuse(lib):
     cfg = synth.LayerConfig("cap", T=96, E=4, k=2, H=64, F=64, seed=22)
     d = g.desc_from_config(cfg, T_max=200)

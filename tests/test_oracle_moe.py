@@ -46,6 +46,34 @@ def test_route_brute_force_with_ties():
             assert np.allclose(probs[t], p, rtol=1e-14, atol=0)
 
 
+def test_route_non_finite_logits_are_limits_of_finite_ones():
+    # NaN behaves as -inf; +-inf behave as the limit of very large finite logits: brute force
+    # on the row with +-inf (and NaN) replaced by +-1e300 in fp64 gives the same choice and
+    # the same probabilities (exp of a difference of two such values is exactly 1 or 0)
+    rng = np.random.default_rng(3)
+    lg = rng.standard_normal((64, 8)).astype(np.float32)
+    lg[0, [1, 4]] = np.nan
+    lg[1, :] = np.nan
+    lg[2, [0, 5]] = np.inf
+    lg[3, :] = -np.inf
+    lg[4, [2, 3, 6]] = -np.inf
+    lg[5, :] = np.nan
+    lg[5, 7] = -np.inf
+    lg[6, 3] = np.inf
+    lg[6, 5] = np.nan
+    lg[7, ::2] = np.nan
+    lg[7, 1::2] = np.inf
+    big = np.where(np.isnan(lg), -1e300, np.where(np.isinf(lg), np.sign(lg).astype(np.float64) * 1e300,
+                                                  lg.astype(np.float64)))
+    for k in (1, 2, 3, 8):
+        ids, probs = moe.route(lg, k)
+        assert np.all((ids >= 0) & (ids < 8))
+        for t in range(lg.shape[0]):
+            o, p = brute_topk(big[t], k)
+            assert list(ids[t]) == o, (t, k)
+            assert np.allclose(probs[t], p, rtol=1e-14, atol=0), (t, k)
+
+
 def test_route_softmax_equals_renormalised_full_softmax():
     rng = np.random.default_rng(1)
     lg = rng.standard_normal((50, 16)).astype(np.float32) * 3

@@ -30,7 +30,10 @@ def _reference(cfg, logits, x):
 
 def test_noalloc_route_permute_matches_workspace_version_twice(lib):
     for cfg in (synth.LayerConfig("na1", T=700, E=64, k=4, H=256, F=64, seed=41, zipf_s=1.1),
-                synth.LayerConfig("na2", T=513, E=8, k=2, H=128, F=64, seed=42)):
+                synth.LayerConfig("na2", T=513, E=8, k=2, H=128, F=64, seed=42),
+                # 128-row segments over 256 experts: the largest padding the scratch holds
+                synth.LayerConfig("na3", T=300, E=256, k=8, H=64, F=64, seed=43, zipf_s=1.1,
+                                  align=128)):
         d = g.desc_from_config(cfg)
         R = cfg.T * cfg.k + cfg.E * (cfg.align - 1)
         ids = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device="cuda")
@@ -60,3 +63,9 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
         g.moe_route_permute_noalloc(d, 1, 256, 256, 256, 256, 256, 256, 256, 1 << 20)
     assert e.value.status == 2
     assert "131072" in g.load().moe_last_error_string().decode()
+    # at the pair limit with 128-row segments over 256 experts the rows still fit
+    d = g.make_desc(E=256, k=8, H=64, F=64, T_max=16384, align=128)
+    with pytest.raises(g.MoeError) as e:
+        g.moe_route_permute_noalloc(d, 1, 256, 256, 256, 256, 256, 256, 256, 1)  # x_perm short
+    assert e.value.status == 1
+    assert "x_perm" in g.load().moe_last_error_string().decode()

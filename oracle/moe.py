@@ -24,6 +24,9 @@ Readings of the pages (where they are silent or ambiguous), used consistently be
      own reduction dimension, fp32-or-better accumulation; column-wise blocks of the
      weight-gradient GEMMs start at each expert's first row.
   R9 d_prob[t, j] = sum_f dA_s * a (a unscaled); d_logits is not part of the layer.
+  R10 MXFP8 backward: dZ, whose E4M3 codes are integer decisions the pages give no precision
+     for, is formed from the fused dGLU epilogue's inputs in the precision the epilogue reads
+     them: the saved FC1 output in bf16 and dA_s rounded to bf16.
 """
 from __future__ import annotations
 
@@ -242,18 +245,23 @@ def expert_backward(X, W1, W2, p, Z, a, a_s, dY, act: ActParams, mx: bool,
     db1 = sum over rows of dZ and ds = sum over rows of p * dA_s * a.
     MXFP8 (R8): dY and W2 along H for dgrad; a_s and dY column-wise (along rows) for dW2;
     dZ along N1 and W1 along N1 for dX; X and dZ column-wise for dW1.
+    MXFP8, R10: the E4M3 codes of dZ are integer decisions taken on the values the fused dGLU
+    epilogue reads, so the oracle forms dZ from the same inputs: the saved FC1 output in bf16
+    (the saved activation is bf16) and the FC2-dgrad result dA_s rounded to bf16 (the
+    precision in which the epilogue holds it); d_prob keeps the plain definition.
     """
     wq = wq or ExpertWeights(W1, W2, mx)
     F = W2.shape[0]
     dA_s = _q(dY, 1, mx) @ wq.w2_h.T
     sa = a * s[None, :] if s is not None else a
     d_prob = (dA_s * sa).sum(axis=1)
-    dA = p[:, None] * (dA_s * s[None, :] if s is not None else dA_s)
+    dA_in, Z_in = (bf16_round(dA_s), bf16_round(Z)) if mx else (dA_s, Z)
+    dA = p[:, None] * (dA_in * s[None, :] if s is not None else dA_in)
     if act.gated:
-        dg, dl = act_backward(act, Z[:, :F], Z[:, F:], dA)
+        dg, dl = act_backward(act, Z_in[:, :F], Z_in[:, F:], dA)
         dZ = np.concatenate([dg, dl], axis=1)
     else:
-        dZ, _ = act_backward(act, Z, None, dA)
+        dZ, _ = act_backward(act, Z_in, None, dA)
     dW2 = _qrows(a_s, mx).T @ _qrows(dY, mx)
     dW1 = _qrows(X, mx).T @ _qrows(dZ, mx)
     dX = _q(dZ, 1, mx) @ wq.w1_n.T

@@ -362,9 +362,16 @@ def test_mx_expert_matches_scalar_brute_force():
     assert np.allclose(Z, Zb, rtol=1e-13, atol=1e-13)
     assert np.allclose(Y, Yb, rtol=1e-12, atol=1e-12)
     dAs = q(dY, False) @ q(W2, False).T
-    s = 1 / (1 + np.exp(-Zb[:, :F]))
-    dA = p[:, None] * dAs
-    dZb = np.concatenate([dA * Zb[:, F:] * s * (1 + Zb[:, :F] * (1 - s)), dA * Zb[:, :F] * s], 1)
+    # dZ from the dGLU's inputs as the epilogue holds them: bf16 Z and bf16 dA_s, each
+    # rounded here through fp32 by truncation plus the round-to-nearest-even carry
+    def bf16(v):
+        u = np.asarray(v, np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+        return ((((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16).astype(np.uint32)
+                .view(np.float32).astype(np.float64))
+    Zr = bf16(Zb)
+    s = 1 / (1 + np.exp(-Zr[:, :F]))
+    dA = p[:, None] * bf16(dAs)
+    dZb = np.concatenate([dA * Zr[:, F:] * s * (1 + Zr[:, :F] * (1 - s)), dA * Zr[:, :F] * s], 1)
     assert np.allclose(d_prob, (dAs * ab).sum(1), rtol=1e-12, atol=1e-12)
     assert np.allclose(dZ, dZb, rtol=1e-12, atol=1e-12)
     assert np.allclose(dW2, q(asb, True).T @ q(dY, True), rtol=1e-12, atol=1e-12)

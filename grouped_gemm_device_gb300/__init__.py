@@ -43,7 +43,7 @@ class LayerDesc(ctypes.Structure):
                 ("lin_hi", ctypes.c_float), ("lin_offset", ctypes.c_float),
                 ("sm_margin", ctypes.c_int32), ("ilv", ctypes.c_int32), ("align", ctypes.c_int32),
                 ("recompute", ctypes.c_int32), ("extras", ctypes.c_int32),
-                ("rht_mask", ctypes.c_uint32)]
+                ("rht_mask", ctypes.c_uint32), ("reuse_weights", ctypes.c_int32)]
 
 
 class WsLayout(ctypes.Structure):
@@ -81,7 +81,7 @@ def load():
         "moe_route_permute": (_I32, [_DP, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
         "moe_grouped_mlp_fwd": (_I32, [_DP, _I32, _P, _P, _P, _P, _SZ, _P]),
         "moe_grouped_mlp_bwd": (_I32, [_DP, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
-        "mxfp8_quantize": (_I32, [_P, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P]),
+        "mxfp8_quantize": (_I32, [_P, _I64, _I64, _I32, _I32, _P, _I32, _P, _P, _P, _P, _P]),
         "nvfp4_amax": (_I32, [_P, _I64, _I64, ctypes.c_uint32, _P, _P, _P]),
         "nvfp4_quantize": (_I32, [_P, _I64, _I64, _P, _P, _I32, ctypes.c_uint32, _P, _P, _P, _P,
                                   _P]),
@@ -138,12 +138,13 @@ def _stream(stream) -> int | None:
 def make_desc(E, k, H, F, T_max, precision="bf16", activation="swiglu", beta=1.0,
               gate_max=math.inf, lin_lo=-math.inf, lin_hi=math.inf, lin_offset=0.0,
               sm_margin=0, ilv=64, align=32, recompute=False, extras=0,
-              rht_mask=0) -> LayerDesc:
+              rht_mask=0, reuse_weights=False) -> LayerDesc:
     """extras: bit 0 FC1 bias, bit 1 feature scale (EXTRA_BIAS | EXTRA_SCALE). rht_mask: the
-    16 signs of the NVFP4 weight-gradient rotation (bit j set: row j of a block negated)."""
+    16 signs of the NVFP4 weight-gradient rotation (bit j set: row j of a block negated).
+    reuse_weights: the forward reuses the workspace's block-scaled weight copies."""
     return LayerDesc(E, k, H, F, T_max, PREC[precision], ACT[activation], beta, gate_max,
                      lin_lo, lin_hi, lin_offset, sm_margin, ilv, align, int(recompute),
-                     int(extras), int(rht_mask) & 0xFFFF)
+                     int(extras), int(rht_mask) & 0xFFFF, int(reuse_weights))
 
 
 def desc_from_config(cfg, T_max=None, sm_margin=0, recompute=False, extras=0,
@@ -218,9 +219,17 @@ def moe_grouped_mlp_bwd_ex(desc, T, dy, w1_packed, w2, feat_scale, dx, dw1_packe
 
 
 def mxfp8_quantize(inp, M, N, rowwise, colwise, q_row=None, s_row=None, q_col=None, s_col=None,
-                   stream=None):
-    _check(load().mxfp8_quantize(_ptr(inp), M, N, int(rowwise), int(colwise), _ptr(q_row),
-                                 _ptr(s_row), _ptr(q_col), _ptr(s_col), _stream(stream)))
+                   stream=None, group_offsets=None, num_groups=0):
+    """group_offsets: int32 device tensor [num_groups + 1]; column-wise blocks then restart at
+    each group's first row and s_col is [N, mxfp8_grouped_scale_cols(M, num_groups)]."""
+    _check(load().mxfp8_quantize(_ptr(inp), M, N, int(rowwise), int(colwise),
+                                 _ptr(group_offsets), int(num_groups), _ptr(q_row), _ptr(s_row),
+                                 _ptr(q_col), _ptr(s_col), _stream(stream)))
+
+
+def mxfp8_grouped_scale_cols(M, num_groups) -> int:
+    """Entries per column of the grouped column-wise scales (include/moegmm.h)."""
+    return 4 * ((-(-M // 32) + num_groups + 3) // 4)
 
 
 def nvfp4_amax(inp, M, N, sign_mask, amax, amax_rht=None, stream=None):

@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <set>
 #include <string>
@@ -53,6 +54,25 @@ cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess) done.insert({kernel, dev});
   return e;
+}
+
+int max_resident_pairs(const void* kernel, const cudaLaunchConfig_t* cfg) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find({kernel, dev});
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t c = *cfg;
+  c.gridDim = dim3(2, 1, 1);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &c) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of a failed query
+    n = 0;
+  }
+  cache[{kernel, dev}] = n;
+  return n;
 }
 
 static moe_status_t cuda_fail(cudaError_t e, const char* where) {
@@ -118,6 +138,8 @@ static moe_status_t validate_desc(const moe_layer_desc_t* d) {
   if (d->recompute && (d->precision != MOE_PREC_BF16 || d->activation == MOE_ACT_SRELU))
     return fail(MOE_ERR_UNSUPPORTED, "recompute needs a BF16 layer with a gated activation");
   if (d->extras & ~3) return fail(MOE_ERR_INVALID_ARG, "extras has unknown bits");
+  if (d->reuse_weights != 0 && d->reuse_weights != 1)
+    return fail(MOE_ERR_INVALID_ARG, "reuse_weights must be 0 or 1");
   if (d->extras && (d->precision != MOE_PREC_BF16 || d->activation == MOE_ACT_SRELU ||
                     d->recompute))
     return fail(MOE_ERR_UNSUPPORTED,
@@ -519,9 +541,12 @@ static moe_status_t fwd_impl(const moe_layer_desc_t* d, int32_t T, const void* w
   cudaError_t e;
   if (d->precision == MOE_PREC_MXFP8) {
     MxProblem m = mx_problem(d, w);
-    // BF16 master weights -> MXFP8 along both reduction directions ([TE-MoE] Challenge 3)
-    mx_quantize_operands(w1_packed, (int64_t)d->E * m.N1, d->H, m.N1, m.N1p, m.w1, m.w1t, s);
-    mx_quantize_operands(w2, (int64_t)d->E * d->F, d->H, d->F, m.Fp, m.w2, m.w2t, s);
+    // BF16 master weights -> MXFP8 along both reduction directions ([TE-MoE] Challenge 3),
+    // unless the copies of an earlier forward are reused
+    if (!d->reuse_weights) {
+      mx_quantize_operands(w1_packed, (int64_t)d->E * m.N1, d->H, m.N1, m.N1p, m.w1, m.w1t, s);
+      mx_quantize_operands(w2, (int64_t)d->E * d->F, d->H, d->F, m.Fp, m.w2, m.w2t, s);
+    }
     // FC1 + activation + probability scale + MXFP8 quantise/transpose (kernel family 2)
     m.role = ROLE_FC1_FPROP;
     m.out = w.at<void>(w.L.z);
@@ -542,15 +567,22 @@ static moe_status_t fwd_impl(const moe_layer_desc_t* d, int32_t T, const void* w
   if (d->precision == MOE_PREC_NVFP4) {
     Fp4Problem m = fp4_problem(d, w);
     const int32_t* live = w.at<int32_t>(w.L.offsets) + d->E;  // rows in use
-    // BF16 master weights -> NVFP4 along both reduction directions (per-tensor amax first)
-    if ((e = cudaMemsetAsync(m.amax + AM_W1, 0, 4 * sizeof(float), s)) != cudaSuccess)
+    // BF16 master weights -> NVFP4 along both reduction directions (per-tensor amax first),
+    // unless the copies and amaxes of an earlier forward are reused; the FC1 epilogue's
+    // amax slots (a_s and its rotation) start at zero either way
+    static_assert(AM_W2 == AM_W1 + 1 && AM_A == AM_W1 + 2 && AM_AT == AM_W1 + 3,
+                  "amax slot order");
+    if ((e = cudaMemsetAsync(m.amax + (d->reuse_weights ? AM_A : AM_W1), 0,
+                             (d->reuse_weights ? 2 : 4) * sizeof(float), s)) != cudaSuccess)
       return cuda_fail(e, "memset amax");
-    launch_nvfp4_amax(w1_packed, (int64_t)d->E * m.N1 * d->H, m.amax + AM_W1, device_sms(), s);
-    launch_nvfp4_amax(w2, (int64_t)d->E * d->F * d->H, m.amax + AM_W2, device_sms(), s);
-    nv_quantize(w1_packed, (int64_t)d->E * m.N1p, d->H, m.N1, m.N1p, nullptr, m, AM_W1, AM_W1,
-                m.w1, m.w1t, 0, s);
-    nv_quantize(w2, (int64_t)d->E * m.Fp, d->H, d->F, m.Fp, nullptr, m, AM_W2, AM_W2, m.w2,
-                m.w2t, 0, s);
+    if (!d->reuse_weights) {
+      launch_nvfp4_amax(w1_packed, (int64_t)d->E * m.N1 * d->H, m.amax + AM_W1, device_sms(), s);
+      launch_nvfp4_amax(w2, (int64_t)d->E * d->F * d->H, m.amax + AM_W2, device_sms(), s);
+      nv_quantize(w1_packed, (int64_t)d->E * m.N1p, d->H, m.N1, m.N1p, nullptr, m, AM_W1, AM_W1,
+                  m.w1, m.w1t, 0, s);
+      nv_quantize(w2, (int64_t)d->E * m.Fp, d->H, d->F, m.Fp, nullptr, m, AM_W2, AM_W2, m.w2,
+                  m.w2t, 0, s);
+    }
     // FC1 + activation + probability scale, BF16 a_s plus its amax and rotated amax
     m.role = ROLE_FC1_FPROP;
     m.out = w.at<void>(w.L.z);
@@ -812,22 +844,35 @@ moe_status_t moe_selftest_wait_timeout(int32_t* err, uint64_t limit_ns, moe_stre
 }
 
 moe_status_t mxfp8_quantize(const void* in, int64_t M, int64_t N, int32_t rowwise,
-                            int32_t colwise, uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
-                            uint8_t* s_col, moe_stream_t stream) {
+                            int32_t colwise, const int32_t* group_offsets, int32_t num_groups,
+                            uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                            moe_stream_t stream) {
   if (M < 0 || N < 0) return fail(MOE_ERR_INVALID_ARG, "negative size");
   if (!rowwise && !colwise) return fail(MOE_ERR_INVALID_ARG, "neither rowwise nor colwise");
+  const bool grouped = group_offsets != nullptr;
+  if (grouped && (num_groups < 1 || num_groups > 65536))
+    return fail(MOE_ERR_INVALID_ARG, "num_groups must be in [1, 65536] with group_offsets");
   if (M == 0 || N == 0) return MOE_OK;
   if (!in || !aligned16(in)) return fail(MOE_ERR_INVALID_ARG, "in must be non-NULL, 16B aligned");
   if (N % 32) return fail(MOE_ERR_UNSUPPORTED, "N must be a multiple of 32");
-  if (colwise && M % 32) return fail(MOE_ERR_UNSUPPORTED, "M must be a multiple of 32 (colwise)");
+  if (colwise && !grouped && M % 32)
+    return fail(MOE_ERR_UNSUPPORTED, "M must be a multiple of 32 (colwise without groups)");
   if (!mxfp8_quantize_size_ok(M, N)) return fail(MOE_ERR_UNSUPPORTED, "M or N too large");
   if (rowwise && (!q_row || !s_row || !aligned16(q_row)))
     return fail(MOE_ERR_INVALID_ARG, "rowwise outputs must be non-NULL (q_row 16B aligned)");
   if (colwise && (!q_col || !s_col || !aligned16(q_col)))
     return fail(MOE_ERR_INVALID_ARG, "colwise outputs must be non-NULL (q_col 16B aligned)");
+  if (colwise && grouped && (reinterpret_cast<uintptr_t>(s_col) & 3u))
+    return fail(MOE_ERR_INVALID_ARG, "s_col must be 4-byte aligned with group_offsets");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  launch_mxfp8_quantize(in, M, N, rowwise, colwise, q_row, s_row, q_col, s_col,
-                        std::max(device_sms(), 1), s);
+  const int sms = std::max(device_sms(), 1);
+  if (colwise && grouped) {
+    if (rowwise)
+      launch_mxfp8_quantize(in, M, N, 1, 0, q_row, s_row, nullptr, nullptr, sms, s);
+    launch_mxfp8_colwise_grouped(in, M, N, group_offsets, num_groups, q_col, s_col, sms, s);
+  } else {
+    launch_mxfp8_quantize(in, M, N, rowwise, colwise, q_row, s_row, q_col, s_col, sms, s);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "mxfp8_quantize launch");
   return MOE_OK;

@@ -34,10 +34,18 @@ __global__ void group_colsum_kernel(const float* part, int ld, int col0, int nco
 // Sets a kernel's dynamic shared-memory limit once per (kernel, device); thread-safe. The
 // attribute belongs to the device's context, so a process driving several GPUs sets it on each.
 cudaError_t ensure_smem_attr(const void* kernel, int bytes);
+// clusters of two CTAs of `kernel` (launched with `cfg`) that fit on the device at once, cached
+// per (kernel, device); 0 when the query fails
+int max_resident_pairs(const void* kernel, const cudaLaunchConfig_t* cfg);
 
 // mxfp8.cu
 // Sizes the quantiser's 32-bit tile indexing covers (M rows < 2^31, tile count < 2^31).
 bool mxfp8_quantize_size_ok(int64_t M, int64_t N);
+// column-wise blocks restarting at device-resident group offsets; s_col [N, scale_cols]
+int64_t mxfp8_grouped_scale_cols(int64_t M, int G);
+void launch_mxfp8_colwise_grouped(const void* in, int64_t M, int64_t N, const int32_t* offsets,
+                                  int G, uint8_t* q_col, uint8_t* s_col, int num_sms,
+                                  cudaStream_t s);
 void launch_mxfp8_quantize(const void* in, int64_t M, int64_t N, int rowwise, int colwise,
                            uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                            int num_sms, cudaStream_t s);

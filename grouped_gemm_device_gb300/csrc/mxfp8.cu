@@ -231,6 +231,89 @@ static void launch(MxQuantArgs a, int num_sms, cudaStream_t s) {
   count_launch(s, MOE_K_MXFP8_QUANTIZE);
 }
 
+// Column-wise MXFP8 with blocks that restart at each group's first row (group offsets in
+// device memory, any alignment): group g holds rows [off[g], off[g+1]); its i-th block is rows
+// off[g] + 32 i .. min(off[g] + 32 i + 32, off[g+1]) (a short last block is quantised as if
+// padded with zeros, which leave the block's amax unchanged). The scale of (column c,
+// block (g, i)) sits at s[c * nb + off[g] / 32 + g + i]: the start index off[g] / 32 + g grows
+// by at least the previous group's block count, so blocks never share an entry; entries no
+// block owns are written 0. nb (a multiple of 4) >= ceil(M / 32) + G.
+//
+// Work item: four consecutive scale entries b0 .. b0+3 (one 32-bit scale word per column)
+// over 256 columns; a thread owns a column pair. Offsets are clamped into [0, M] as they are
+// read, so invalid offsets cannot take an access outside the buffers.
+constexpr int QG_THREADS = 128;
+__global__ void __launch_bounds__(QG_THREADS) mxfp8_colwise_grouped_kernel(
+    const uint16_t* __restrict__ in, int64_t M, int64_t N, const int32_t* __restrict__ off,
+    int G, int64_t nb, uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+  __shared__ int64_t s_rb[4], s_re[4];
+  const int64_t col_items = (N + 2 * QG_THREADS - 1) / (2 * QG_THREADS);
+  const int64_t items = (nb / 4) * col_items;
+  auto o = [&](int g) -> int64_t {
+    const int64_t v = off[g];
+    return v < 0 ? 0 : (v > M ? M : v);
+  };
+  for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+    const int64_t b0 = (it / col_items) * 4;
+    const int64_t c = (it % col_items) * (2 * QG_THREADS) + 2 * threadIdx.x;
+    __syncthreads();  // the previous item's block bounds have been read
+    if (threadIdx.x < 4) {
+      // the block of scale entry b: the last group whose start index is <= b
+      const int64_t b = b0 + threadIdx.x;
+      int lo = 0, hi = G;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (o(mid) / 32 + mid <= b) lo = mid; else hi = mid;
+      }
+      const int64_t i = b - (o(lo) / 32 + lo);
+      int64_t rb = o(lo) + 32 * i, re = o(lo + 1);
+      if (i < 0 || rb >= re) rb = re = 0;  // no block owns this entry
+      s_rb[threadIdx.x] = rb;
+      s_re[threadIdx.x] = rb + 32 < re ? rb + 32 : re;
+    }
+    __syncthreads();
+    if (c >= N) continue;
+    uint32_t sc0 = 0, sc1 = 0;  // scale words of columns c and c + 1 (byte j: entry b0 + j)
+#pragma unroll 1
+    for (int j = 0; j < 4; ++j) {
+      const int64_t rb = s_rb[j], n = s_re[j] - rb;
+      if (n <= 0) continue;
+      uint32_t w[32];
+      uint32_t m = 0;
+#pragma unroll
+      for (int r = 0; r < 32; ++r) {
+        w[r] = r < n ? *reinterpret_cast<const uint32_t*>(in + (rb + r) * N + c) : 0u;
+        m = bf16x2_max(m, w[r] & 0x7FFF7FFFu);
+      }
+      const int e0 = mx_block_exponent(bf16_lo(m)), e1 = mx_block_exponent(bf16_hi(m));
+      const float i0 = mx_inv_scale(e0), i1 = mx_inv_scale(e1);
+#pragma unroll
+      for (int r = 0; r < 32; ++r)
+        if (r < n)
+          *reinterpret_cast<uint16_t*>(q + (rb + r) * N + c) =
+              (uint16_t)cvt_e4m3x2(bf16_lo(w[r]) * i0, bf16_hi(w[r]) * i1);
+      sc0 |= (uint32_t)(e0 + 127) << (8 * j);
+      sc1 |= (uint32_t)(e1 + 127) << (8 * j);
+    }
+    *reinterpret_cast<uint32_t*>(s + c * nb + b0) = sc0;
+    *reinterpret_cast<uint32_t*>(s + (c + 1) * nb + b0) = sc1;
+  }
+}
+
+int64_t mxfp8_grouped_scale_cols(int64_t M, int G) { return ((M + 31) / 32 + G + 3) / 4 * 4; }
+
+void launch_mxfp8_colwise_grouped(const void* in, int64_t M, int64_t N, const int32_t* offsets,
+                                  int G, uint8_t* q_col, uint8_t* s_col, int num_sms,
+                                  cudaStream_t s) {
+  const int64_t nb = mxfp8_grouped_scale_cols(M, G);
+  const int64_t items = (nb / 4) * ((N + 2 * QG_THREADS - 1) / (2 * QG_THREADS));
+  if (items == 0) return;
+  const int grid = (int)std::min<int64_t>(items, (int64_t)num_sms * 8);
+  mxfp8_colwise_grouped_kernel<<<grid, QG_THREADS, 0, s>>>(
+      static_cast<const uint16_t*>(in), M, N, offsets, G, nb, q_col, s_col);
+  count_launch(s, MOE_K_MXFP8_QUANTIZE);
+}
+
 bool mxfp8_quantize_size_ok(int64_t M, int64_t N) {
   const int64_t tm = (M + QT_ROWS - 1) / QT_ROWS, tn = (N + QT_COLS - 1) / QT_COLS;
   return M <= (int64_t)INT32_MAX - QT_ROWS && N <= (int64_t)INT32_MAX &&

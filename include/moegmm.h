@@ -113,6 +113,14 @@ typedef struct {
                          the tokens to the weight-gradient operands (bit j set: the j-th row
                          of each 16-row block is negated before H16 / 4); drawn once by the
                          caller. Ignored by the other precisions                             */
+  int32_t reuse_weights; /* MXFP8 / NVFP4: 1 = the forward does not quantise W1 and W2 again
+                         but uses the block-scaled weight copies (and, NVFP4, their per-tensor
+                         amaxes) that an earlier forward on the same workspace made from the
+                         same BF16 master weights - the micro-batches of one gradient
+                         accumulation step share them ([TE-MoE] Challenge 2: BF16 master
+                         weights quantised before the low-precision GEMMs). The caller
+                         guarantees the weights did not change since. 0 = quantise (always
+                         correct). Ignored by BF16 layers                                    */
 } moe_layer_desc_t;
 
 /* Byte offsets (from ws) of the intermediates that live in the workspace, for inspection
@@ -260,13 +268,26 @@ moe_status_t moe_route_permute_noalloc(const moe_layer_desc_t *desc, int32_t T,
  *   in      bf16 [M, N]
  *   rowwise:  q_row  e4m3 [M, N]       blocks of 32 along N; s_row e8m0 [M, N/32]
  *   colwise:  q_col  e4m3 [M, N]       blocks of 32 along M (same layout as in);
- *             s_col  e8m0 [N, M/32]    (row groups that start at multiples of 32 rows, as the
- *                                      permuted expert segments do, restart blocks for free)
- * N must be a multiple of 32 for rowwise, M a multiple of 32 for colwise; the pointers of
+ *             s_col  e8m0 [N, M/32]    without groups: blocks start at every 32nd row
+ *   group_offsets  int32 [num_groups + 1], DEVICE memory, or NULL: rows [off[g], off[g+1])
+ *             form group g (off[0] = 0, non-decreasing, off[num_groups] = M; the per-expert
+ *             token counts of a GroupedLinear, [TE-MoE] Challenge 1, need not be multiples
+ *             of 32). Column-wise blocks then restart at each group's first row: block i of
+ *             group g is rows off[g] + 32i .. min(off[g] + 32i + 32, off[g+1]) (a short last
+ *             block is quantised as if padded with zeros), and
+ *             s_col e8m0 [N, nb], nb = 4 * ceil((ceil(M/32) + num_groups) / 4): the scale of
+ *             column c, block (g, i) is s_col[c * nb + off[g]/32 + g + i] (integer division);
+ *             entries no block owns are written 0. The offsets are read on the device only
+ *             (no host sync); offsets outside [0, M] are clamped, and offsets that break the
+ *             rules above give unspecified (but in-bounds) results. The row-wise copy does not
+ *             depend on the groups. num_groups must be in [1, 65536] when group_offsets is set.
+ * N must be a multiple of 32; M a multiple of 32 for colwise without groups (any M with
+ * groups); in and q_col 16-byte aligned and s_col 4-byte aligned with groups; the pointers of
  * an unused direction may be NULL. Bit-exact: the result does not depend on the launch. */
 moe_status_t mxfp8_quantize(const void *in, int64_t M, int64_t N, int32_t rowwise,
-                            int32_t colwise, uint8_t *q_row, uint8_t *s_row, uint8_t *q_col,
-                            uint8_t *s_col, moe_stream_t stream);
+                            int32_t colwise, const int32_t *group_offsets, int32_t num_groups,
+                            uint8_t *q_row, uint8_t *s_row, uint8_t *q_col, uint8_t *s_col,
+                            moe_stream_t stream);
 
 /* NVFP4 per-tensor amax ([NV-blog] "fused MXFP8 and NVFP4 quantisation": the scale of an NVFP4
  * tensor needs its amax first).

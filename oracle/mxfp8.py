@@ -149,3 +149,33 @@ def fake_quant_rows_from(v: np.ndarray) -> np.ndarray:
     pad = np.zeros((mp,) + v.shape[1:], dtype=np.float64)
     pad[:m] = v
     return fake_quant(pad, 0)[:m]
+
+
+def quantize_colwise_groups(v: np.ndarray, offsets) -> tuple:
+    """Column-wise (along axis 0) MXFP8 of row groups of any size: group g is rows
+    [offsets[g], offsets[g+1]); its blocks of 32 rows start at the group's first row (the last
+    one padded with zeros, which do not change a block's amax), as for the per-expert token
+    groups of a GroupedLinear ([TE-MoE] Challenge 1) quantised for the weight gradients.
+
+    Returns (codes uint8 [M, N], scale bytes uint8 [N, nb]) with the scale of column c and
+    block i of group g at [c, offsets[g] // 32 + g + i], nb = 4 * ceil((ceil(M/32) + G) / 4),
+    and 0 in the entries no block owns (the layout of the library's grouped quantiser)."""
+    v = np.asarray(v, dtype=np.float64)
+    M, N = v.shape
+    G = len(offsets) - 1
+    nb = 4 * ((-(-M // BLOCK) + G + 3) // 4)
+    codes = np.zeros((M, N), dtype=np.uint8)
+    scales = np.zeros((N, nb), dtype=np.uint8)
+    for g in range(G):
+        a, b = int(offsets[g]), int(offsets[g + 1])
+        m = b - a
+        if m <= 0:
+            continue
+        mp = -(-m // BLOCK) * BLOCK
+        pad = np.zeros((mp, N))
+        pad[:m] = v[a:b]
+        c, sb = quantize_blocks(pad, axis=0)          # sb [mp / 32, N]
+        codes[a:b] = c[:m]
+        base = a // BLOCK + g
+        scales[:, base:base + mp // BLOCK] = sb.T
+    return codes, scales

@@ -36,6 +36,38 @@ def test_mxfp8_quantize_bit_exact(lib, M, N, scale, outliers):
     assert np.array_equal(q_col.cpu().numpy(), c_c)
 
 
+@pytest.mark.parametrize("M,N,groups", [
+    (150, 64, [0, 7, 7, 40, 45, 113, 150]),              # ragged, an empty group, short blocks
+    (4096 + 77, 2880, None),                               # None: seeded ragged split of 37
+    (33, 96, [0, 33]),                                     # one group, one full + one 1-row block
+    (256, 4096, [0, 0, 0, 256]),                           # leading empty groups
+])
+def test_mxfp8_quantize_grouped_colwise_bit_exact(lib, M, N, groups):
+    if groups is None:
+        r = np.random.default_rng(M)
+        cuts = np.sort(r.integers(0, M + 1, size=36))
+        groups = [0, *cuts.tolist(), M]
+    G = len(groups) - 1
+    a = synth.gen_bf16_matrix(M + N, M, N, scale=1.0, outlier_rows=max(1, M // 40))
+    x = bf16_dev(a)
+    nb = g.mxfp8_grouped_scale_cols(M, G)
+    off = torch.tensor(groups, dtype=torch.int32, device="cuda")
+    q_row = torch.empty(M, N, dtype=torch.uint8, device="cuda")
+    s_row = torch.empty(M, N // 32, dtype=torch.uint8, device="cuda")
+    q_col = torch.full((M, N), 0x55, dtype=torch.uint8, device="cuda")
+    s_col = torch.full((N, nb), 0x55, dtype=torch.uint8, device="cuda")
+    g.mxfp8_quantize(x, M, N, 1, 1, q_row, s_row, q_col, s_col, group_offsets=off,
+                     num_groups=G)
+    torch.cuda.synchronize()
+    v = om.bf16_to_f64(a)
+    c_c, s_c = omx.quantize_colwise_groups(v, groups)
+    c_r, s_r = omx.quantize_blocks(v, axis=1)
+    assert np.array_equal(q_col.cpu().numpy(), c_c)
+    assert np.array_equal(s_col.cpu().numpy(), s_c)
+    assert np.array_equal(q_row.cpu().numpy(), c_r)
+    assert np.array_equal(s_row.cpu().numpy(), s_r)
+
+
 def test_mxfp8_quantize_one_direction_only(lib):
     M, N = 64, 96
     a = synth.gen_bf16_matrix(5, M, N)

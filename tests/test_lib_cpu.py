@@ -41,10 +41,21 @@ def test_exports_every_declared_symbol(lib):
     assert set(g.EXPORTS) <= exported
 
 
-def test_desc_struct_layout_matches_header(lib):
-    # 18 four-byte fields, no padding
-    assert ctypes.sizeof(g.LayerDesc) == 72
-    assert ctypes.sizeof(g.WsLayout) == 19 * 8
+def test_desc_struct_layout_matches_header(lib, tmp_path):
+    # the binding's ctypes structures against the C compiler's view of the header
+    src = tmp_path / "sz.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "moegmm.h"\n'
+                   'int main(void) { printf("%zu %zu %zu\\n", sizeof(moe_layer_desc_t), '
+                   'sizeof(moe_ws_layout_t), offsetof(moe_layer_desc_t, reuse_weights));'
+                   ' return 0; }\n')
+    exe = tmp_path / "sz"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    desc, ws, reuse = map(int, subprocess.run([str(exe)], capture_output=True, text=True,
+                                              check=True).stdout.split())
+    assert ctypes.sizeof(g.LayerDesc) == desc == 19 * 4
+    assert g.LayerDesc.reuse_weights.offset == reuse
+    assert ctypes.sizeof(g.WsLayout) == ws == 19 * 8
 
 
 def _desc(**kw):

@@ -187,3 +187,44 @@ def test_zero_block_and_padding_rows():
     full = np.zeros((64, 32))
     full[:40] = x
     assert np.array_equal(fq, mxfp8.fake_quant(full, 0)[:40])
+
+
+def test_grouped_colwise_reduces_to_plain_blocks_on_32_aligned_groups():
+    # groups that start on multiples of 32 rows and hold multiples of 32 rows: the codes are
+    # the plain column-wise codes, and group g's scales are the plain ones shifted by g entries
+    rng = np.random.default_rng(5)
+    v = rng.standard_normal((192, 64)) * 2.0 ** rng.integers(-20, 20, size=(192, 1))
+    off = [0, 64, 64, 160, 192]
+    c, s = mxfp8.quantize_colwise_groups(v, off)
+    c0, s0 = mxfp8.quantize_blocks(v, axis=0)
+    assert np.array_equal(c, c0)
+    assert s.shape == (64, 4 * ((6 + 4 + 3) // 4))
+    for g in range(4):
+        for blk in range(off[g] // 32, off[g + 1] // 32):
+            assert np.array_equal(s[:, blk + g], s0[blk])
+    owned = {blk + g for g in range(4) for blk in range(off[g] // 32, off[g + 1] // 32)}
+    assert not s[:, [j for j in range(s.shape[1]) if j not in owned]].any()
+
+
+def test_grouped_colwise_brute_force_on_ragged_groups():
+    # every element against its own block, found by scanning: amax over the block's rows,
+    # exponent by the definition, E4M3 of v / 2^e; empty groups own no entry
+    rng = np.random.default_rng(6)
+    M, N = 150, 32
+    v = rng.standard_normal((M, N)) * 2.0 ** rng.integers(-8, 8, size=(M, 1))
+    v[40:45] = 0.0
+    off = [0, 7, 7, 40, 45, 113, 150]
+    c, s = mxfp8.quantize_colwise_groups(v, off)
+    owned = np.zeros(s.shape[1], bool)
+    for g in range(len(off) - 1):
+        for r in range(off[g], off[g + 1]):
+            i = (r - off[g]) // 32
+            lo, hi = off[g] + 32 * i, min(off[g] + 32 * i + 32, off[g + 1])
+            j = off[g] // 32 + g + i
+            owned[j] = True
+            for col in range(N):
+                amax = max(abs(v[q, col]) for q in range(lo, hi))
+                e = -127 if amax == 0 else max(-127, min(127, math.floor(math.log2(amax)) - 8))
+                assert s[col, j] == e + 127
+                assert c[r, col] == mxfp8.e4m3_encode(np.array([v[r, col] / 2.0 ** e]))[0]
+    assert not s[:, ~owned].any()

@@ -32,6 +32,12 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# the CPU baseline (the fp64 oracle) uses every host core: BLAS threads are set explicitly,
+# before numpy loads its BLAS
+HOST_CORES = os.cpu_count() or 1
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(HOST_CORES))
+
 import numpy as np  # noqa: E402
 
 from grouped_gemm_device_gb300 import synth  # noqa: E402
@@ -59,6 +65,11 @@ def parse():
                     help="epilogue extras bits: 1 FC1 bias, 2 feature scale (BF16 gated)")
     ap.add_argument("--recompute", action="store_true",
                     help="keep no FC1 output; the FC2-dgrad kernel recomputes it (BF16)")
+    ap.add_argument("--workloads", default="auto",
+                    help="extra workloads timed after the headline one, each with its own "
+                         "entry under 'workloads': 'auto' (every other configuration when the "
+                         "headline is the default one), 'none', or a comma-separated list")
+    ap.add_argument("--workload-steps", type=int, default=20)
     return ap.parse_args()
 
 
@@ -100,6 +111,20 @@ REPEATED = {
 # dense tensor-core rate of the operand type relative to bf16 (nominal: fp8 4.5 and fp4
 # 13.5 PFLOP/s against bf16's 2.25)
 TENSOR_RATIO = {"bf16": 1.0, "mxfp8": 2.0, "nvfp4": 6.0}
+# GB300 nominal dense tensor peaks (TFLOP/s) and HBM3e bandwidth (GB/s), for context beside
+# the measured denominators
+NOMINAL_TFLOPS = {"bf16": 2250.0, "mxfp8": 4500.0, "nvfp4": 13500.0}
+NOMINAL_HBM_GBS = 7900.0
+# weight quantisation kernels of a step (re-run from the BF16 masters by every forward unless
+# the forward reuses the copies)
+WEIGHT_QUANT = ("mxfp8_quant_w1", "mxfp8_quant_w2", "nvfp4_quant_w1", "nvfp4_quant_w2",
+                "nvfp4_amax_w1", "nvfp4_amax_w2")
+HEADLINE = "mixtral_bf16"
+# the other workloads a default run times too (Mixtral MXFP8, DeepSeek-V3 MXFP8, GPT-OSS BF16
+# and MXFP8 with the activation sweep, NVFP4)
+EXTRA_WORKLOADS = ("mixtral_mxfp8", "dsv3_mxfp8", "gptoss_bf16", "gptoss_mxfp8",
+                   "gptoss_geglu_bf16", "gptoss_srelu_bf16", "gptoss_geglu_mxfp8",
+                   "gptoss_srelu_mxfp8", "mixtral_nvfp4", "gptoss_nvfp4")
 DTYPE = {"bf16": "bf16", "mxfp8": "e4m3+e8m0 (fp32 accumulate)",
          "nvfp4": "e2m1+e4m3+fp32 scale (fp32 accumulate)"}
 
@@ -337,6 +362,8 @@ def oracle_sample(cfg, rows: int, inputs=None):
 
 
 def blas_threads() -> int:
+    """BLAS threads in use: threadpoolctl's report where it is installed, else the thread
+    count this script set for OpenBLAS before numpy loaded."""
     try:
         from threadpoolctl import threadpool_info
         n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
@@ -344,7 +371,21 @@ def blas_threads() -> int:
             return int(n[0])
     except Exception:
         pass
-    return os.cpu_count() or 1
+    return int(os.environ.get("OPENBLAS_NUM_THREADS", HOST_CORES))
+
+
+def tensor_peak(peaks, precision, clocks):
+    """Tensor roofline of the operand type at the clock the timed region held: the measured
+    bf16 burst rate x the nominal operand-type ratio x (median SM clock / max SM clock).
+    Returns (TFLOP/s, description)."""
+    burst = peaks.get("bf16_tflops", 1900.0)
+    ratio = TENSOR_RATIO[precision]
+    scale = 1.0
+    if clocks and clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
+        scale = min(1.0, clocks["sm_mhz"] / clocks["sm_max_mhz"])
+    kind = (f"bf16_tflops (burst) x {ratio:g} ({precision}/bf16 nominal ratio) x "
+            f"{scale:.3f} (median/max SM clock)")
+    return burst * ratio * scale, kind
 
 
 def run_reference(args):
@@ -367,14 +408,16 @@ def run_reference(args):
         tokens += n
     value = tot_f / tot_t / 1e12
     cores = blas_threads()
+    world_n = int(os.environ.get("WORLD_SIZE", "1"))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": max(args.gpus, world_n), "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": workload_name(cfg), "sample": desc},
         "tokens_per_s": tokens / tot_t,
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "host_cpu_count": HOST_CORES, "blas_threads": cores,
                          "sample": f"per step: {desc}"},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -465,11 +508,314 @@ def overlap_sweep(args):
                       "results": out}), flush=True)
 
 
+def bf16_host(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+
+def per_kernel_table(cfg, per, kernel_ms, recompute, p_tc, p_bw):
+    gf = gemm_flops(cfg, recompute)
+    kb = kernel_bytes(cfg, recompute)
+    out = {}
+    for k, v in sorted(kernel_ms.items()):
+        ent = {"ms": round(v, 4)}
+        if k in gf:
+            ent["tflops"] = round(gf[k] / (v / 1e3) / 1e12, 1)
+            ent["frac_tensor"] = round(gf[k] / (v / 1e3) / 1e12 / p_tc, 3)
+        if k in kb:
+            ent["gbs"] = round(kb[k] / (v / 1e3) / 1e9, 1)
+            ent["frac_hbm"] = round(kb[k] / (v / 1e3) / 1e9 / p_bw, 3)
+        out[k] = ent
+    return out
+
+
+def dominant_roofline(cfg, per, kernel_ms, recompute, p_tc, p_bw, tc_kind, peak_src):
+    """Roofline of the kernel with the largest share of the step: algorithmic flops or bytes
+    per launch over its mean live duration, against the bound its arithmetic intensity sets."""
+    gf = gemm_flops(cfg, recompute)
+    kb = kernel_bytes(cfg, recompute)
+    dom = max((k for k in kernel_ms if k in gf or k in kb), key=lambda k: sum(per[k]))
+    dom_ms = kernel_ms[dom]
+    t_tc = gf.get(dom, 0.0) / (p_tc * 1e12)
+    t_bw = kb.get(dom, 0.0) / (p_bw * 1e9)
+    if t_tc >= t_bw:
+        bound, achieved, peak, unit = "tensor", gf[dom] / (dom_ms / 1e3) / 1e12, p_tc, "TFLOP/s"
+        nominal = NOMINAL_TFLOPS[cfg.precision]
+    else:
+        bound, achieved, peak, unit = "hbm", kb[dom] / (dom_ms / 1e3) / 1e9, p_bw, "GB/s"
+        nominal = NOMINAL_HBM_GBS
+    return {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": traffic_for(dom, cfg.name),
+            "peak_kind": tc_kind if bound == "tensor" else f"hbm_gbs ({peak_src})",
+            "frac_of_nominal": achieved / nominal, "nominal_peak": nominal,
+            "flops_per_launch": gf.get(dom), "bytes_per_launch": kb.get(dom),
+            "ms_per_launch": dom_ms}
+
+
+def measure(cfg, args, world, local, steps, warmup, with_e2e):
+    """Time `steps` layer steps (route + forward + backward) of workload `cfg` on this rank's
+    GPU, after `warmup` untimed ones; per-kernel durations come from the library's launch
+    timeline (CUDA events on the launching stream). Returns a dict of measurements."""
+    import torch
+
+    import grouped_gemm_device_gb300 as g
+
+    dev = torch.device("cuda", local)
+    t_gen = time.time()
+    hin = host_inputs(cfg)
+    t_gen = time.time() - t_gen
+    desc = g.desc_from_config(cfg, sm_margin=args.sm_margin, recompute=args.recompute,
+                              extras=args.extras)
+    layer = g.MoELayer(desc, dev)
+    fc1_bias = (torch.from_numpy(synth.gen_fc1_bias(cfg)).to(dev)
+                if args.extras & g.EXTRA_BIAS else None)
+    feat_scale = (torch.from_numpy(synth.gen_feat_scale(cfg)).to(dev)
+                  if args.extras & g.EXTRA_SCALE else None)
+    w1_log = torch.stack([bf16_host(w) for w in hin["w1"]]).to(dev)
+    w1p = g.pack_w1(w1_log, gated=cfg.gated, ilv=cfg.ilv)
+    del w1_log
+    w2 = torch.stack([bf16_host(w) for w in hin["w2"]]).to(dev)
+    logits = torch.from_numpy(hin["logits"]).to(dev)
+    x = bf16_host(hin["x"]).to(dev)
+    dy = bf16_host(hin["dy"]).to(dev)
+    T = cfg.T
+
+    def step():
+        layer.route_permute(logits, x, T)
+        layer.forward(w1p, w2, T, fc1_bias=fc1_bias, feat_scale=feat_scale)
+        layer.backward(dy, w1p, w2, T, feat_scale=feat_scale)
+
+    n_w = g.moe_launch_count()
+    for _ in range(max(warmup, 1)):
+        step()
+    torch.cuda.synchronize()
+    per_step_launches = (g.moe_launch_count() - n_w) // max(warmup, 1)
+    assert layer.device_error() == 0, "device error during warm-up"
+
+    tl = g.Timeline(min(8192, steps * per_step_launches + 16))
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    n0 = g.moe_launch_count()
+    tl.begin()
+    ev0.record()
+    for _ in range(steps):
+        step()
+    ev1.record()
+    torch.cuda.synchronize()
+    n_rec = tl.end()
+    launches = g.moe_launch_count() - n0
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1) / steps
+    ms_max = allreduce_max(ms, world)
+    assert layer.device_error() == 0, "device error during timing"
+
+    per = {}
+    seen = {}
+    for i, (name, dur) in enumerate(tl.durations(ev0)):
+        if i % per_step_launches == 0:
+            seen = {}
+        j = seen.get(name, 0)
+        seen[name] = j + 1
+        per.setdefault(REPEATED[name][j] if name in REPEATED else name, []).append(dur)
+    kernel_ms = {k: sum(v) / len(v) for k, v in per.items()}
+
+    # the same steps with the forward reusing the block-scaled weight copies (gradient
+    # accumulation over micro-batches): the step time without weight quantisation
+    wq = None
+    if cfg.precision != "bf16":
+        layer.desc.reuse_weights = 1
+        step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k_r = max(3, steps // 2)
+        e0.record()
+        for _ in range(k_r):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        layer.desc.reuse_weights = 0
+        assert layer.device_error() == 0, "device error in the weight-reuse steps"
+        ms_reuse = allreduce_max(e0.elapsed_time(e1) / k_r, world)
+        wq = {"ms_per_step_with_weight_quant": ms_max,
+              "ms_per_step_weights_reused": ms_reuse,
+              "weight_quant_ms_in_step": sum(kernel_ms.get(k, 0.0) for k in WEIGHT_QUANT),
+              "tflops_weights_reused": job_throughput(cfg.flops_fwd_bwd(), ms_reuse, world) / 1e12}
+
+    e2e = None
+    if with_e2e:
+        e2e = measure_e2e(cfg, layer, hin, logits, x, dy, w1p, w2, fc1_bias, feat_scale, world,
+                          steps)
+    res = {"cfg": cfg, "ms": ms, "ms_max": ms_max, "per": per, "kernel_ms": kernel_ms,
+           "launches": int(launches), "timeline_events": n_rec, "clocks": clocks, "wq": wq,
+           "e2e": e2e, "t_gen": t_gen, "ws_bytes": layer.ws_bytes, "hin": hin}
+    del layer, w1p, w2, logits, x, dy
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_e2e(cfg, layer, hin, logits, x, dy, w1p, w2, fc1_bias, feat_scale, world, steps):
+    """End to end through the C ABI with host buffers: every step copies its inputs from pinned
+    host memory and its results back, inside the timed region. The copies run on two side
+    streams ordered by events so they overlap the layer's kernels: the next step's logits and
+    x load once this step's routing has gathered x, dy loads during the forward, y returns
+    during the backward, dx and d_probs during the next step."""
+    import torch
+    T = cfg.T
+    flops = cfg.flops_fwd_bwd()
+    h_logits = torch.from_numpy(hin["logits"]).pin_memory()
+    h_x = bf16_host(hin["x"]).pin_memory()
+    h_dy = bf16_host(hin["dy"]).pin_memory()
+    h_y = torch.empty(T, cfg.H, dtype=torch.bfloat16).pin_memory()
+    h_dx = torch.empty(T, cfg.H, dtype=torch.bfloat16).pin_memory()
+    h_dp = torch.empty(T, cfg.k, dtype=torch.float32).pin_memory()
+    main = torch.cuda.current_stream()
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {n: torch.cuda.Event() for n in
+          ("in", "routed", "dy", "fwd", "bwd", "y_out", "dx_out", "start")}
+
+    def load_inputs():
+        with torch.cuda.stream(h2d):
+            logits.copy_(h_logits, non_blocking=True)
+            x.copy_(h_x, non_blocking=True)
+            ev["in"].record(h2d)
+
+    def e2e_step():
+        main.wait_event(ev["in"])
+        layer.route_permute(logits, x, T)
+        ev["routed"].record(main)
+        with torch.cuda.stream(h2d):
+            h2d.wait_event(ev["bwd"])       # the previous backward has read dy
+            dy.copy_(h_dy, non_blocking=True)
+            ev["dy"].record(h2d)
+        load_inputs()                       # next step's inputs; x and logits are free
+        main.wait_event(ev["y_out"])        # the previous y has left the device
+        layer.forward(w1p, w2, T, fc1_bias=fc1_bias, feat_scale=feat_scale)
+        ev["fwd"].record(main)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(ev["fwd"])
+            h_y.copy_(layer.y[:T], non_blocking=True)
+            ev["y_out"].record(d2h)
+        main.wait_event(ev["dy"])
+        main.wait_event(ev["dx_out"])       # the previous dx / d_probs have left
+        layer.backward(dy, w1p, w2, T, feat_scale=feat_scale)
+        ev["bwd"].record(main)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(ev["bwd"])
+            h_dx.copy_(layer.dx[:T], non_blocking=True)
+            h_dp.copy_(layer.d_probs[:T], non_blocking=True)
+            ev["dx_out"].record(d2h)
+
+    def e2e_run(n):
+        for e in ("bwd", "y_out", "dx_out", "start"):
+            ev[e].record(main)
+        h2d.wait_event(ev["start"])
+        load_inputs()
+        for _ in range(n):
+            e2e_step()
+        main.wait_stream(h2d)
+        main.wait_stream(d2h)
+
+    e2e_run(3)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    k_e2e = max(10, steps // 4)
+    e0.record()
+    e2e_run(k_e2e)
+    e1.record()
+    torch.cuda.synchronize()
+    ms_e2e = allreduce_max(e0.elapsed_time(e1) / k_e2e, world)
+    bi = h_logits.numel() * 4 + h_x.numel() * 2 + h_dy.numel() * 2
+    bo = h_y.numel() * 2 + h_dx.numel() * 2 + h_dp.numel() * 4
+    return {"value": job_throughput(flops, ms_e2e, world) / 1e12, "unit": "TFLOPS",
+            "ms_per_step": ms_e2e, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "tokens_per_s": T * world / (ms_e2e / 1e3)}
+
+
+def summarise(r, args, world, peaks, peak_src):
+    """The JSON fields of one measured workload."""
+    cfg = r["cfg"]
+    flops = cfg.flops_fwd_bwd()
+    ms, ms_max = r["ms"], r["ms_max"]
+    value = job_throughput(flops, ms_max, world) / 1e12
+    p_tc, tc_kind = tensor_peak(peaks, cfg.precision, r["clocks"])
+    p_bw = peaks.get("hbm_gbs", 6800.0)
+    kb = kernel_bytes(cfg, args.recompute)
+    gf = gemm_flops(cfg, args.recompute)
+    step_bytes = sum(kb.values())
+    step_ideal_ms = 1e3 * max(flops / (p_tc * 1e12), step_bytes / (p_bw * 1e9))
+    gemm_total_ms = sum(r["kernel_ms"][k] for k in gf if k in r["kernel_ms"])
+    out = {
+        "workload": workload_name(cfg), "name": cfg.name, "ms_per_step": ms_max,
+        "value": value, "unit": "TFLOPS", "tokens_per_s": cfg.T * world / (ms_max / 1e3),
+        "dtype": DTYPE[cfg.precision], "flops_per_step": flops,
+        "pct_tensor_peak": {"value": 100 * value / world / p_tc, "peak_tflops": p_tc,
+                            "peak_kind": f"{tc_kind} ({peak_src})",
+                            "pct_of_nominal": 100 * value / world /
+                            NOMINAL_TFLOPS[cfg.precision],
+                            "nominal_tflops": NOMINAL_TFLOPS[cfg.precision]},
+        "step_roofline": {"ideal_ms": step_ideal_ms, "frac": step_ideal_ms / ms,
+                          "bytes": step_bytes,
+                          "bound": "tensor" if flops / (p_tc * 1e12) >=
+                          step_bytes / (p_bw * 1e9) else "hbm"},
+        "roofline": dominant_roofline(cfg, r["per"], r["kernel_ms"], args.recompute, p_tc, p_bw,
+                                      tc_kind, peak_src),
+        "kernels": per_kernel_table(cfg, r["per"], r["kernel_ms"], args.recompute, p_tc, p_bw),
+        "gemm_share": gemm_total_ms / ms,
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if r["wq"]:
+        out["weight_quant"] = r["wq"]
+    return out
+
+
+def maybe_spawn(args):
+    """`--gpus N` (N > 1) outside torchrun starts N replica ranks under torch.distributed.run,
+    so the line's n_gpus is the number of GPUs asked for; inside torchrun the world size must
+    match the request."""
+    ws = os.environ.get("WORLD_SIZE")
+    if args.gpus > 1 and ws is None:
+        import socket
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1", "--master-port",
+               str(port), os.path.abspath(__file__), *sys.argv[1:]]
+        os.execv(sys.executable, cmd)
+    if ws is not None and int(ws) != args.gpus and args.gpus != 1:
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={ws}")
+
+
+def extra_workloads(args):
+    if args.workloads == "none" or args.tokens or args.experts or args.extras or args.recompute:
+        return []
+    if args.workloads == "auto":
+        return list(EXTRA_WORKLOADS) if args.config == HEADLINE else []
+    names = [n.strip() for n in args.workloads.split(",") if n.strip()]
+    bad = [n for n in names if n not in synth.CONFIGS]
+    if bad:
+        sys.exit(f"bench.py: unknown workloads {bad}")
+    return [n for n in names if n != args.config]
+
+
 def main():
     args = parse()
     if args.overlap_sweep:
         overlap_sweep(args)
         return
+    maybe_spawn(args)
     if args.impl == "reference":
         run_reference(args)
         return
@@ -485,233 +831,57 @@ def main():
     barrier(world)
     g.load()
     cfg = config_of(args)
-    dev = torch.device("cuda", local)
-    t_gen = time.time()
-    hin = host_inputs(cfg)
-    t_gen = time.time() - t_gen
-
-    def bf(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
-
-    desc = g.desc_from_config(cfg, sm_margin=args.sm_margin, recompute=args.recompute,
-                              extras=args.extras)
-    layer = g.MoELayer(desc, dev)
-    fc1_bias = (torch.from_numpy(synth.gen_fc1_bias(cfg)).to(dev)
-                if args.extras & g.EXTRA_BIAS else None)
-    feat_scale = (torch.from_numpy(synth.gen_feat_scale(cfg)).to(dev)
-                  if args.extras & g.EXTRA_SCALE else None)
-    w1_log = torch.stack([bf(w) for w in hin["w1"]]).to(dev)
-    w1p = g.pack_w1(w1_log, gated=cfg.gated, ilv=cfg.ilv)
-    del w1_log
-    w2 = torch.stack([bf(w) for w in hin["w2"]]).to(dev)
-    logits = torch.from_numpy(hin["logits"]).to(dev)
-    x = bf(hin["x"]).to(dev)
-    dy = bf(hin["dy"]).to(dev)
-    T = cfg.T
-
-    def step():
-        layer.route_permute(logits, x, T)
-        layer.forward(w1p, w2, T, fc1_bias=fc1_bias, feat_scale=feat_scale)
-        layer.backward(dy, w1p, w2, T, feat_scale=feat_scale)
-
-    n_w = g.moe_launch_count()
-    for _ in range(max(args.warmup, 1)):
-        step()
-    torch.cuda.synchronize()
-    per_step_launches = (g.moe_launch_count() - n_w) // max(args.warmup, 1)
-    assert layer.device_error() == 0, "device error during warm-up"
-
-    tl = g.Timeline(min(4096, args.steps * per_step_launches + 16))
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.3)
-    n0 = g.moe_launch_count()
-    tl.begin()
-    ev0.record()
-    for _ in range(args.steps):
-        step()
-    ev1.record()
-    torch.cuda.synchronize()
-    n_rec = tl.end()
-    launches = g.moe_launch_count() - n0
-    barrier(world)
-    torch.cuda.synchronize()
-    clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    ms_max = allreduce_max(ms, world)
-    assert layer.device_error() == 0, "device error during timing"
-
-    flops = cfg.flops_fwd_bwd()
-    value = job_throughput(flops, ms_max, world) / 1e12
     peaks, peak_src = load_peaks()
 
-    # per-kernel durations from the launch timeline; repeated kernels of one step (the four
-    # MXFP8 quantiser launches) are told apart by their order within the step
-    per = {}
-    seen = {}
-    for i, (name, dur) in enumerate(tl.durations(ev0)):
-        if i % per_step_launches == 0:
-            seen = {}
-        j = seen.get(name, 0)
-        seen[name] = j + 1
-        per.setdefault(REPEATED[name][j] if name in REPEATED else name, []).append(dur)
-    kernel_ms = {k: sum(v) / len(v) for k, v in per.items()}
-    gf = gemm_flops(cfg, args.recompute)
-    kb = kernel_bytes(cfg, args.recompute)
-    # the GEMMs are timed inside a long step: sustained tensor peak of the operand type (the
-    # measured bf16 figure times the nominal rate ratio)
-    p_tc = peaks.get("bf16_tflops_sustained", 1700.0) * TENSOR_RATIO[cfg.precision]
-    p_bw = peaks.get("hbm_gbs", 6800.0)
-    dom = max((k for k in kernel_ms if k in gf or k in kb), key=lambda k: sum(per[k]))
-    dom_ms = kernel_ms[dom]
-    t_tc = gf.get(dom, 0.0) / (p_tc * 1e12)
-    t_bw = kb.get(dom, 0.0) / (p_bw * 1e9)
-    if t_tc >= t_bw:
-        bound, achieved, peak, unit = "tensor", gf[dom] / (dom_ms / 1e3) / 1e12, p_tc, "TFLOP/s"
-    else:
-        bound, achieved, peak, unit = "hbm", kb[dom] / (dom_ms / 1e3) / 1e9, p_bw, "GB/s"
-    traffic = traffic_for(dom, cfg.name)
-    gemm_total_ms = sum(kernel_ms[k] for k in gf if k in kernel_ms)
-    step_bytes = sum(kb.values())
-    step_ideal_ms = 1e3 * max(flops / (p_tc * 1e12), step_bytes / (p_bw * 1e9))
-    per_kernel = {}
-    for k, v in sorted(kernel_ms.items()):
-        ent = {"ms": round(v, 4)}
-        if k in gf:
-            ent["tflops"] = round(gf[k] / (v / 1e3) / 1e12, 1)
-            ent["frac_tensor"] = round(gf[k] / (v / 1e3) / 1e12 / p_tc, 3)
-        if k in kb:
-            ent["gbs"] = round(kb[k] / (v / 1e3) / 1e9, 1)
-            ent["frac_hbm"] = round(kb[k] / (v / 1e3) / 1e9 / p_bw, 3)
-        per_kernel[k] = ent
-
-    # end to end through the C ABI with host buffers: every step copies its inputs from pinned
-    # host memory and its results back, inside the timed region. The copies run on two side
-    # streams ordered by events so they overlap the layer's kernels: the next step's logits
-    # and x load once this step's routing has gathered x, dy loads during the forward, y
-    # returns during the backward, dx and d_probs during the next step.
-    e2e = None
-    if not args.no_e2e:
-        h_logits = torch.from_numpy(hin["logits"]).pin_memory()
-        h_x = bf(hin["x"]).pin_memory()
-        h_dy = bf(hin["dy"]).pin_memory()
-        h_y = torch.empty(T, cfg.H, dtype=torch.bfloat16).pin_memory()
-        h_dx = torch.empty(T, cfg.H, dtype=torch.bfloat16).pin_memory()
-        h_dp = torch.empty(T, cfg.k, dtype=torch.float32).pin_memory()
-        main = torch.cuda.current_stream()
-        h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
-        ev = {n: torch.cuda.Event() for n in
-              ("in", "routed", "dy", "fwd", "bwd", "y_out", "dx_out", "start")}
-
-        def load_inputs():
-            with torch.cuda.stream(h2d):
-                logits.copy_(h_logits, non_blocking=True)
-                x.copy_(h_x, non_blocking=True)
-                ev["in"].record(h2d)
-
-        def e2e_step():
-            main.wait_event(ev["in"])
-            layer.route_permute(logits, x, T)
-            ev["routed"].record(main)
-            with torch.cuda.stream(h2d):
-                h2d.wait_event(ev["bwd"])       # the previous backward has read dy
-                dy.copy_(h_dy, non_blocking=True)
-                ev["dy"].record(h2d)
-            load_inputs()                       # next step's inputs; x and logits are free
-            main.wait_event(ev["y_out"])        # the previous y has left the device
-            layer.forward(w1p, w2, T, fc1_bias=fc1_bias, feat_scale=feat_scale)
-            ev["fwd"].record(main)
-            with torch.cuda.stream(d2h):
-                d2h.wait_event(ev["fwd"])
-                h_y.copy_(layer.y[:T], non_blocking=True)
-                ev["y_out"].record(d2h)
-            main.wait_event(ev["dy"])
-            main.wait_event(ev["dx_out"])       # the previous dx / d_probs have left
-            layer.backward(dy, w1p, w2, T, feat_scale=feat_scale)
-            ev["bwd"].record(main)
-            with torch.cuda.stream(d2h):
-                d2h.wait_event(ev["bwd"])
-                h_dx.copy_(layer.dx[:T], non_blocking=True)
-                h_dp.copy_(layer.d_probs[:T], non_blocking=True)
-                ev["dx_out"].record(d2h)
-
-        def e2e_run(n):
-            for e in ("bwd", "y_out", "dx_out", "start"):
-                ev[e].record(main)
-            h2d.wait_event(ev["start"])
-            load_inputs()
-            for _ in range(n):
-                e2e_step()
-            main.wait_stream(h2d)
-            main.wait_stream(d2h)
-
-        e2e_run(3)
-        torch.cuda.synchronize()
-        barrier(world)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        k_e2e = max(10, args.steps // 4)
-        e0.record()
-        e2e_run(k_e2e)
-        e1.record()
-        torch.cuda.synchronize()
-        ms_e2e = allreduce_max(e0.elapsed_time(e1) / k_e2e, world)
-        bi = h_logits.numel() * 4 + h_x.numel() * 2 + h_dy.numel() * 2
-        bo = h_y.numel() * 2 + h_dx.numel() * 2 + h_dp.numel() * 4
-        e2e = {"value": job_throughput(flops, ms_e2e, world) / 1e12, "unit": "TFLOPS",
-               "ms_per_step": ms_e2e, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-               "tokens_per_s": T * world / (ms_e2e / 1e3)}
+    r = measure(cfg, args, world, local, args.steps, args.warmup, not args.no_e2e)
+    head = summarise(r, args, world, peaks, peak_src)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        dt, fl, sdesc, _ = oracle_sample(cfg, 512, hin)
+        dt, fl, sdesc, _ = oracle_sample(cfg, 512, r["hin"])
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOPS", "cores": blas_threads(),
+               "host_cpu_count": HOST_CORES, "blas_threads": blas_threads(),
                "kind": "oracle", "sample": sdesc, "seconds": dt,
-               "tokens_per_s_equiv": (fl / dt) / (flops / T)}
+               "tokens_per_s_equiv": (fl / dt) / (cfg.flops_fwd_bwd() / cfg.T)}
+    del r["hin"]
+
+    others = []
+    for name in extra_workloads(args):
+        rw = measure(synth.CONFIGS[name], args, world, local, args.workload_steps, 3, False)
+        del rw["hin"]
+        others.append(summarise(rw, args, world, peaks, peak_src))
 
     if rank == 0:
-        ratio = TENSOR_RATIO[cfg.precision]
-        tc_kind = (f"{ratio:g} x bf16_tflops_sustained ({cfg.precision}/bf16 nominal ratio)"
-                   if ratio != 1.0 else "bf16_tflops_sustained") + f" ({peak_src})"
         w_bytes = 2 * 2 * cfg.E * (cfg.N1 + cfg.F) * cfg.H
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "metric": METRIC, "value": head["value"], "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": DTYPE[cfg.precision],
             "data": "synthetic",
             "config": {"workload": workload_name(cfg), "parallelism": f"replicas x{world}",
                        "l2": f"no flush: each step streams {w_bytes / 1e9:.1f} GB of bf16 "
                              "weights and weight gradients, > 129 MB L2",
-                       "sm_margin": args.sm_margin, "flops_per_step": flops,
+                       "sm_margin": args.sm_margin, "flops_per_step": cfg.flops_fwd_bwd(),
                        "recompute": bool(args.recompute), "extras": args.extras,
-                       "workspace_bytes": layer.ws_bytes},
-            "tokens_per_s": cfg.T * world / (ms_max / 1e3),
-            "pct_tensor_peak": {"value": 100 * value / world / p_tc, "peak_tflops": p_tc,
-                                "peak_kind": tc_kind},
-            "step_roofline": {"ideal_ms": step_ideal_ms, "frac": step_ideal_ms / ms,
-                              "bytes": step_bytes,
-                              "bound": "tensor" if flops / (p_tc * 1e12) >=
-                              step_bytes / (p_bw * 1e9) else "hbm"},
-            "gpu_launches": int(launches),
-            "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
-                         "unit": unit, "frac": achieved / peak, "traffic": traffic,
-                         "peak_kind": tc_kind if bound == "tensor" else f"hbm_gbs ({peak_src})",
-                         "flops_per_launch": gf.get(dom), "bytes_per_launch": kb.get(dom),
-                         "ms_per_launch": dom_ms},
-            "kernels": per_kernel,
-            "gemm_share": gemm_total_ms / ms,
-            "timeline_events": n_rec,
-            "e2e": e2e,
+                       "workspace_bytes": r["ws_bytes"]},
+            "tokens_per_s": head["tokens_per_s"],
+            "pct_tensor_peak": head["pct_tensor_peak"],
+            "step_roofline": head["step_roofline"],
+            "gpu_launches": head["gpu_launches"],
+            "roofline": head["roofline"],
+            "kernels": head["kernels"],
+            "gemm_share": head["gemm_share"],
+            "timeline_events": r["timeline_events"],
+            "e2e": r["e2e"],
             "cpu_baseline": cpu,
-            "clocks": clocks,
-            "input_gen_s": round(t_gen, 1),
+            "clocks": head["clocks"],
+            "input_gen_s": round(r["t_gen"], 1),
         }
+        if head.get("weight_quant"):
+            line["weight_quant"] = head["weight_quant"]
+        if others:
+            line["workloads"] = others
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

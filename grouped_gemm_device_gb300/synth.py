@@ -89,6 +89,17 @@ CONFIGS = {
                                **_CLAMP),
     "gptoss_mxfp8": LayerConfig("gptoss_mxfp8", T=16384, E=128, k=4, H=2880, F=2880, seed=4,
                                 precision="mxfp8", align=128, **_CLAMP),
+    # the GPT-OSS-shaped layer with the other activations of the sweep
+    "gptoss_geglu_bf16": LayerConfig("gptoss_geglu_bf16", T=16384, E=128, k=4, H=2880, F=2880,
+                                     seed=4, activation="geglu"),
+    "gptoss_srelu_bf16": LayerConfig("gptoss_srelu_bf16", T=16384, E=128, k=4, H=2880, F=2880,
+                                     seed=4, activation="srelu"),
+    "gptoss_geglu_mxfp8": LayerConfig("gptoss_geglu_mxfp8", T=16384, E=128, k=4, H=2880,
+                                      F=2880, seed=4, activation="geglu", precision="mxfp8",
+                                      align=128),
+    "gptoss_srelu_mxfp8": LayerConfig("gptoss_srelu_mxfp8", T=16384, E=128, k=4, H=2880,
+                                      F=2880, seed=4, activation="srelu", precision="mxfp8",
+                                      align=128),
     "mixtral_nvfp4": LayerConfig("mixtral_nvfp4", T=16384, E=8, k=2, H=4096, F=14336,
                                  precision="nvfp4", seed=5, align=128),
     "gptoss_nvfp4": LayerConfig("gptoss_nvfp4", T=16384, E=128, k=4, H=2880, F=2880, seed=4,

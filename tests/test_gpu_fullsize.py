@@ -35,6 +35,10 @@ def _fq_rows(v, mx):
     return omx.fake_quant_rows_from(v) if mx else v
 
 
+def _bf(v, mx):
+    return om.bf16_round(v) if mx else v
+
+
 def _sample_tokens(ids, counts, k, rng):
     """Tokens whose experts all lie in the smallest set of busiest experts that holds at
     least N_TOKENS such tokens."""
@@ -48,8 +52,19 @@ def _sample_tokens(ids, counts, k, rng):
     raise AssertionError("no sample")
 
 
+def _weight_experts(experts, counts):
+    """Experts whose weight-gradient columns are sampled: the busiest of the token sample's
+    experts and the least-loaded expert that has rows (on skewed routing a segment of a few
+    rows, shorter than one 128-row tile and than one k-block)."""
+    live = np.nonzero(counts > 0)[0]
+    small = int(live[np.argmin(counts[live])])   # first of the smallest
+    return [experts[0]] + ([small] if small != experts[0] else list(experts[1:N_EXPERTS]))
+
+
 @pytest.mark.parametrize("name", ["mixtral_bf16", "mixtral_mxfp8", "gptoss_bf16",
-                                  "gptoss_mxfp8", "dsv3_mxfp8"])
+                                  "gptoss_mxfp8", "dsv3_mxfp8", "gptoss_geglu_bf16",
+                                  "gptoss_srelu_bf16", "gptoss_geglu_mxfp8",
+                                  "gptoss_srelu_mxfp8"])
 def test_fullsize_sampled_parity(lib, name):
     cfg = synth.CONFIGS[name]
     mx = cfg.precision == "mxfp8"
@@ -84,13 +99,13 @@ def test_fullsize_sampled_parity(lib, name):
     assert np.array_equal(layer.offsets().cpu().numpy(), pm.offsets)
 
     toks, experts = _sample_tokens(ids, pm.counts, cfg.k, rng)
-    wexp = experts[:N_EXPERTS]
+    wexp = _weight_experts(experts, pm.counts)
     xs, dys = om.bf16_to_f64(x[toks]), om.bf16_to_f64(dy[toks])
     y_ref = np.zeros((N_TOKENS, cfg.H))
     dx_ref = np.zeros((N_TOKENS, cfg.H))
     dp_ref = np.zeros((N_TOKENS, cfg.k))
     errs = {}
-    for e in experts:
+    for e in list(experts) + [e for e in wexp if e not in experts]:
         use_tok = [(i, j) for i in range(N_TOKENS) for j in range(cfg.k) if ids[toks[i], j] == e]
         if not use_tok and e not in wexp:
             continue
@@ -128,8 +143,10 @@ def test_fullsize_sampled_parity(lib, name):
         dW2_ref = _fq_rows(a_s, mx).T @ _fq_rows(dY[:, hs], mx)
         fs_t, hs_t = torch.as_tensor(fs, device="cuda"), torch.as_tensor(hs, device="cuda")
         errs[f"dW2[{e}]"] = rel_fro(to_np(dw2[e][fs_t][:, hs_t]), dW2_ref)
-        # dW1[h, n] = sum_r X[r, h] dZ[r, n] for n = gate f and linear f
-        dA = p * (_fq(dY, 1, mx) @ wq.w2_h[fs].T)
+        # dW1[h, n] = sum_r X[r, h] dZ[r, n] for n = gate f and linear f; in MXFP8 dZ comes
+        # from bf16 Z and bf16 dA_s (oracle reading R10)
+        dA = p * _bf(_fq(dY, 1, mx) @ wq.w2_h[fs].T, mx)
+        Zg, Zl = _bf(Zg, mx), (_bf(Zl, mx) if Zl is not None else None)
         if cfg.gated:
             dG, dL = om.act_backward(act, Zg, Zl, dA)
             dZ = np.concatenate([dG, dL], axis=1)
@@ -148,101 +165,154 @@ def test_fullsize_sampled_parity(lib, name):
     assert not bad, (name, errs)
 
 
-def test_fullsize_nvfp4(lib):
-    """The Mixtral-shaped NVFP4 layer in the benchmark's launch configuration. The per-tensor
-    scales of x, dY, W1 and W2 come from amaxes the oracle computes exactly, so everything
-    that depends only on them is checked on samples: the amax slots (plain and rotated), and
-    sampled entries of the three BF16 tensors the fused kernels emit (the saved Z, a_s and dZ,
-    each row-local given those scales: Z = Q(x) Q_H(W1), a_s = bf16(p act(Z)), dZ =
-    bf16(dact(bf16 Z, p Q(dY) Q_H(W2)^T))). The layer outputs pass through the per-tensor
-    scales of a_s and dZ, which need the whole tensor; for them the test checks properties:
-    finite, and within NVFP4's quantisation-noise band of the unquantised oracle."""
+def nvfp4_fullsize_reference(cfg, logits, x, dy, w1, w2, toks, wexp, fs, hs):
+    """fp64 oracle quantities of the NVFP4 layer (oracle.moe.layer_nvfp4's definitions) needed
+    to check a full-size run on samples, computed by streaming the experts (w1, w2: lists of
+    each expert's logical bf16 weights):
+      * every per-tensor amax, including those of a_s and dZ (plain and rotated), which need
+        the whole tensor: Z, a_s and dZ of every routed row are formed expert by expert;
+      * y, dx and d_probs of the sampled tokens `toks`;
+      * dW2[e][fs][:, hs] and dW1[e] at the gate/linear columns fs and the H columns hs, for
+        the experts `wexp` (the rotation and the column-wise quantisation act on each column
+        alone, so restricting to columns is exact).
+    Experts are worked on in parallel threads. Returns (amax dict, y [n, H], dx [n, H],
+    d_probs [n, k], {e: (dW2 cols [fs, hs], dW1 cols [hs, gate fs | linear fs])})."""
+    import concurrent.futures as cf
+    import os
     from oracle import nvfp4 as nv
 
-    cfg = synth.CONFIGS["mixtral_nvfp4"]
     act = act_params(cfg)
+    F, H = cfg.F, cfg.H
+    mask = synth.gen_rht_mask(cfg)
+    ids, probs = om.route(logits, cfg.k)
+    pm = om.permutation(ids, cfg.E, cfg.align)
+    xf, dyf = om.bf16_to_f64(x), om.bf16_to_f64(dy)
+    am = {"x": nv.amax(xf), "dy": nv.amax(dyf),
+          "w1": max(nv.amax(om.bf16_to_f64(w)) for w in w1),
+          "w2": max(nv.amax(om.bf16_to_f64(w)) for w in w2),
+          "xt": nv.rht_amax_segments([xf[tok] for tok, _ in pm.rows_of_expert], mask),
+          "dyt": nv.rht_amax_segments([dyf[tok] for tok, _ in pm.rows_of_expert], mask)}
+    S = {n: nv.encode_scale(v) for n, v in am.items()}
+    xq = nv.fake_quant(xf, 1, S["x"])
+    dyq = nv.fake_quant(dyf, 1, S["dy"])
+
+    def expert(e):
+        """amax contributions of expert e, its sampled rows, its kept columns."""
+        tok, slot = pm.rows_of_expert[e]
+        out = {"a": 0.0, "at": 0.0, "dz": 0.0, "dzt": 0.0, "rows": {}, "keep": None}
+        if not len(tok):
+            return out
+        W1, W2 = om.bf16_to_f64(w1[e]), om.bf16_to_f64(w2[e])
+        p = probs[tok, slot][:, None]
+        Z = xq[tok] @ nv.fake_quant(W1, 0, S["w1"])
+        a = om.act_forward(act, Z[:, :F], Z[:, F:]) if cfg.gated else om.act_forward(act, Z)
+        A = om.bf16_round(p * a)
+        dA_s = dyq[tok] @ nv.fake_quant(W2, 1, S["w2"]).T
+        Zb = om.bf16_round(Z)
+        del Z
+        if cfg.gated:
+            dg, dl = om.act_backward(act, Zb[:, :F], Zb[:, F:], p * dA_s)
+            dZ = om.bf16_round(np.concatenate([dg, dl], axis=1))
+            del dg, dl
+        else:
+            dZ = om.bf16_round(om.act_backward(act, Zb, None, p * dA_s)[0])
+        del Zb
+        out.update(a=nv.amax(A), dz=nv.amax(dZ), at=nv.rht_amax_segments([A], mask),
+                   dzt=nv.rht_amax_segments([dZ], mask))
+        pos = {int(t): i for i, t in enumerate(tok)}
+        for i, t in enumerate(toks):
+            for j in range(cfg.k):
+                if ids[t, j] == e:
+                    r = pos[int(t)]
+                    out["rows"][(i, j)] = (A[r], dZ[r], float((dA_s[r] * a[r]).sum()))
+        if e in wexp:
+            ncols = np.concatenate([fs, F + fs]) if cfg.gated else fs
+            out["keep"] = (A[:, fs].copy(), dyf[tok][:, hs], dZ[:, ncols].copy(), xf[tok][:, hs])
+        return out
+
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(cfg.E, (os.cpu_count() or 2) // 2))) as ex:
+        per = list(ex.map(expert, range(cfg.E)))
+    for k_ in ("a", "at", "dz", "dzt"):
+        am[k_] = max(o[k_] for o in per)
+    S.update({k_: nv.encode_scale(am[k_]) for k_ in ("a", "at", "dz", "dzt")})
+    y = np.zeros((len(toks), H))
+    dx = np.zeros((len(toks), H))
+    dp = np.zeros((len(toks), cfg.k))
+    for e, o in enumerate(per):
+        if not o["rows"]:
+            continue
+        w2_f = nv.fake_quant(om.bf16_to_f64(w2[e]), 0, S["w2"])    # FC2: W2 along F
+        w1_n = nv.fake_quant(om.bf16_to_f64(w1[e]), 1, S["w1"])    # FC1 dgrad: W1 along N1
+        for (i, j), (ra, rdz, d_prob) in o["rows"].items():
+            y[i] += nv.fake_quant(ra[None], 1, S["a"])[0] @ w2_f
+            dx[i] += nv.fake_quant(rdz[None], 1, S["dz"])[0] @ w1_n.T
+            dp[i, j] = d_prob
+    wg = {}
+    for e, o in enumerate(per):
+        if o["keep"] is None:
+            continue
+        A_f, dY_h, dZ_n, X_h = o["keep"]
+        at_q = nv.colwise_rht_segments([A_f], mask, S["at"])[0]
+        dyt_q = nv.colwise_rht_segments([dY_h], mask, S["dyt"])[0]
+        dzt_q = nv.colwise_rht_segments([dZ_n], mask, S["dzt"])[0]
+        xt_q = nv.colwise_rht_segments([X_h], mask, S["xt"])[0]
+        wg[e] = (at_q.T @ dyt_q, xt_q.T @ dzt_q)
+    return am, y, dx, dp, wg
+
+
+def test_fullsize_nvfp4(lib):
+    """The Mixtral-shaped NVFP4 layer in the benchmark's launch configuration against the
+    oracle's definitions (oracle.moe.layer_nvfp4), evaluated by streaming the experts: every
+    per-tensor amax (the ten slots, those of a_s and dZ formed from all routed rows), then y,
+    dx and d_probs of sampled tokens and sampled columns of dW1 and dW2 of the busiest experts,
+    at the NVFP4 tolerance of the small-shape layer tests (1e-2 relative Frobenius)."""
+    from .test_gpu_nvfp4 import NV_TOL
+
+    cfg = synth.CONFIGS["mixtral_nvfp4"]
     F, H, N1 = cfg.F, cfg.H, cfg.N1
     rng = np.random.default_rng(4321)
     logits, x, dy = synth.gen_logits(cfg), synth.gen_x(cfg), synth.gen_dy(cfg)
-    mask = synth.gen_rht_mask(cfg)
+    w1h = [synth.gen_w1_expert(cfg, e) for e in range(cfg.E)]
+    w2h = [synth.gen_w2_expert(cfg, e) for e in range(cfg.E)]
     layer = g.MoELayer(g.desc_from_config(cfg))
     w1p = torch.empty(cfg.E, N1, H, dtype=torch.bfloat16, device="cuda")
     w2 = torch.empty(cfg.E, F, H, dtype=torch.bfloat16, device="cuda")
-    am_w1 = am_w2 = 0.0
     for e in range(cfg.E):
-        w1e, w2e = synth.gen_w1_expert(cfg, e), synth.gen_w2_expert(cfg, e)
-        am_w1 = max(am_w1, nv.amax(om.bf16_to_f64(w1e)))
-        am_w2 = max(am_w2, nv.amax(om.bf16_to_f64(w2e)))
-        g.moe_pack_fc1_weight(bf16_dev(w1e)[None], w1p[e:e + 1], 1, H, F, 1, cfg.ilv, 0)
-        w2[e].copy_(bf16_dev(w2e))
+        g.moe_pack_fc1_weight(bf16_dev(w1h[e])[None], w1p[e:e + 1], 1, H, F, 1, cfg.ilv, 0)
+        w2[e].copy_(bf16_dev(w2h[e]))
     layer.route_permute(torch.from_numpy(logits).cuda(), bf16_dev(x), cfg.T)
     y = to_np(layer.forward(w1p, w2, cfg.T))
-    dx, _, _, dp = layer.backward(bf16_dev(dy), w1p, w2, cfg.T)
+    dx, dw1p, dw2, dp = layer.backward(bf16_dev(dy), w1p, w2, cfg.T)
     torch.cuda.synchronize()
     assert layer.device_error() == 0
     dx, dp = to_np(dx), to_np(dp)
+    got = dict(zip(g.NV_AMAX,
+                   layer.ws_view("nv_amax", torch.float32, (16,)).cpu().numpy().astype(float)))
     ids, probs = om.route(logits, cfg.k)
     pm = om.permutation(ids, cfg.E, cfg.align)
     assert np.array_equal(layer.offsets().cpu().numpy(), pm.offsets)
-    # ------------------------------------------------------------ amax slots
-    xf, dyf = om.bf16_to_f64(x), om.bf16_to_f64(dy)
-    got = dict(zip(g.NV_AMAX,
-                   layer.ws_view("nv_amax", torch.float32, (16,)).cpu().numpy().astype(float)))
-    assert got["x"] == nv.amax(xf) and got["dy"] == nv.amax(dyf)
-    assert got["w1"] == am_w1 and got["w2"] == am_w2
-    segs_x = [xf[tok] for tok, _ in pm.rows_of_expert]
-    segs_dy = [dyf[tok] for tok, _ in pm.rows_of_expert]
-    for k_, segs in (("xt", segs_x), ("dyt", segs_dy)):
-        want = nv.rht_amax_segments(segs, mask)
-        assert abs(got[k_] - want) <= 1e-6 * want, k_
-    # ------------------------------------------------------------ sampled Z, a_s, dZ entries
-    S = {k_: nv.encode_scale(v) for k_, v in (("x", nv.amax(xf)), ("dy", nv.amax(dyf)),
-                                              ("w1", am_w1), ("w2", am_w2))}
-    toks = rng.choice(cfg.T, size=4, replace=False)
-    fs = rng.choice(F, size=8, replace=False)
-    ws = layer.layout
-    R = ws.R_cap
-    Zw = layer.ws_view("z", torch.bfloat16, (R, N1))
-    Aw = layer.ws_view("a_s", torch.bfloat16, (R, F))
-    dZw = layer.ws_view("dz", torch.bfloat16, (R, N1))
-    half_ilv = lambda n: (n % F // cfg.ilv) * 2 * cfg.ilv + (n // F) * cfg.ilv + n % F % cfg.ilv  # noqa: E731
-    cols = np.concatenate([fs, F + fs])                 # gate f, linear f (logical)
-    pcols = torch.as_tensor([half_ilv(n) for n in cols], device="cuda")
-    want_z, want_a, want_dz, got_z, got_a, got_dz = [], [], [], [], [], []
-    for t in toks:
-        xq = nv.fake_quant(xf[t:t + 1], 1, S["x"])
-        dyq = nv.fake_quant(dyf[t:t + 1], 1, S["dy"])
-        for j in range(cfg.k):
-            e, r = ids[t, j], pm.row_of[t, j]
-            W1 = om.bf16_to_f64(synth.gen_w1_expert(cfg, e))[:, cols]      # [H, 16] logical
-            W2 = om.bf16_to_f64(synth.gen_w2_expert(cfg, e))[fs]           # [8, H]
-            Z = xq @ nv.fake_quant(W1, 0, S["w1"])
-            a = om.act_forward(act, Z[:, :8], Z[:, 8:])
-            Zb = om.bf16_round(Z)
-            dA = probs[t, j] * (dyq @ nv.fake_quant(W2, 1, S["w2"]).T)
-            dg, dl = om.act_backward(act, Zb[:, :8], Zb[:, 8:], dA)
-            want_z.append(Zb[0])
-            want_a.append(om.bf16_round(probs[t, j] * a)[0])
-            want_dz.append(om.bf16_round(np.concatenate([dg, dl], axis=1))[0])
-            got_z.append(to_np(Zw[r][pcols]))
-            got_a.append(to_np(Aw[r][torch.as_tensor(fs, device="cuda")]))
-            got_dz.append(to_np(dZw[r][pcols]))
-    for name, a_, b_ in (("Z", got_z, want_z), ("a_s", got_a, want_a), ("dZ", got_dz, want_dz)):
-        assert rel_fro(np.array(a_), np.array(b_)) < BF16_TOL, name
-    # ------------------------------------------------------------ outputs: properties
-    assert np.isfinite(y).all() and np.isfinite(dx).all() and np.isfinite(dp).all()
-    ref_y, ref_dx = np.zeros((len(toks), H)), np.zeros((len(toks), H))
-    for i, t in enumerate(toks):
-        for j in range(cfg.k):
-            e = ids[t, j]
-            W1 = om.bf16_to_f64(synth.gen_w1_expert(cfg, e))
-            W2 = om.bf16_to_f64(synth.gen_w2_expert(cfg, e))
-            p = probs[t, j:j + 1]
-            Z, a, a_s, Y = om.expert_forward(xf[t:t + 1], W1, W2, p, act, False)
-            _, dX, _, _, _ = om.expert_backward(xf[t:t + 1], W1, W2, p, Z, a, a_s,
-                                                dyf[t:t + 1], act, False)
-            ref_y[i] += Y[0]
-            ref_dx[i] += dX[0]
-    for name, a_, b_ in (("y", y[toks], ref_y), ("dx", dx[toks], ref_dx)):
-        rel = rel_fro(a_, b_)
-        assert 0.02 < rel < 0.5, (name, rel)
+
+    toks, experts = _sample_tokens(ids, pm.counts, cfg.k, rng)
+    wexp = experts[:N_EXPERTS]
+    fs = rng.choice(F, size=N_COLS, replace=False)
+    hs = rng.choice(H, size=N_COLS, replace=False)
+    am, y_ref, dx_ref, dp_ref, wg = nvfp4_fullsize_reference(cfg, logits, x, dy, w1h, w2h, toks,
+                                                             wexp, fs, hs)
+    # the plain amaxes are maxima of bf16 (or input) values: exact; the rotated ones are maxima
+    # of fp32 rotations (the oracle rotates in fp64)
+    for k_ in ("x", "dy", "w1", "w2", "a", "dz"):
+        assert got[k_] == am[k_], (k_, got[k_], am[k_])
+    for k_ in ("xt", "dyt", "at", "dzt"):
+        assert abs(got[k_] - am[k_]) <= 1e-6 * am[k_], (k_, got[k_], am[k_])
+    errs = {"y": rel_fro(y[toks], y_ref), "dx": rel_fro(dx[toks], dx_ref),
+            "d_probs": rel_fro(dp[toks], dp_ref)}
+    fs_t, hs_t = torch.as_tensor(fs, device="cuda"), torch.as_tensor(hs, device="cuda")
+    ncols = np.concatenate([fs, F + fs])
+    half, w = ncols // F, ncols % F
+    prow = torch.as_tensor((w // cfg.ilv) * 2 * cfg.ilv + half * cfg.ilv + w % cfg.ilv,
+                           device="cuda")
+    for e, (dW2_ref, dW1_ref) in wg.items():
+        errs[f"dW2[{e}]"] = rel_fro(to_np(dw2[e][fs_t][:, hs_t]), dW2_ref)
+        errs[f"dW1[{e}]"] = rel_fro(to_np(dw1p[e][prow][:, hs_t]).T, dW1_ref)
+    bad = {k_: v for k_, v in errs.items() if not v <= NV_TOL}
+    assert not bad, errs

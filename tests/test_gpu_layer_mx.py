@@ -55,3 +55,43 @@ def test_mx_layer_fwd_bwd_matches_oracle(lib, name):
 
 def test_mx_weight_grads_into_16_byte_aligned_buffers(lib):
     check_weight_grads_16_byte_aligned(CASES["mx_tails"])
+
+
+def test_mx_cuda_graph_capture_and_replay_with_new_routing(lib):
+    """The MXFP8 step (route, the x / dY / weight quantisers, the block-scaled GEMMs with their
+    quantising epilogues) has no host sync: capture it once, replay it after overwriting the
+    logits in place, and the new routing's layer comes out."""
+    cfg = CASES["mx_skewed"]
+    run = LayerRun(Inputs(cfg))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            run.run(sync=False)
+    lg2 = synth.gen_logits(cfg.with_(seed=97))
+    run.logits_d.copy_(torch.from_numpy(lg2))
+    graph.replay()
+    torch.cuda.synchronize()
+    check_layer(cfg, Inputs(cfg, logits=lg2), run, tol=MX_TOL)
+    # the replay is the eager step, bit for bit
+    got = [t.clone() for t in (run.y, run.dx, run.dw1p, run.dw2, run.d_probs)]
+    run.run()
+    for a, b in zip(got, (run.y, run.dx, run.dw1p, run.dw2, run.d_probs)):
+        assert torch.equal(a, b)
+
+
+def test_mx_reused_weight_copies(lib):
+    """reuse_weights: a second micro-batch that reuses the first forward's MXFP8 weight copies
+    gives bit-identical results to one that quantises the weights again."""
+    cfg = CASES["mx_clamped"]
+    run = LayerRun(Inputs(cfg))
+    run.logits_d.copy_(torch.from_numpy(synth.gen_logits(cfg.with_(seed=78))))
+    run.run()
+    want = [t.clone() for t in (run.y, run.dx, run.dw1p, run.dw2, run.d_probs)]
+    run.layer.desc.reuse_weights = 1
+    run.run()
+    run.layer.desc.reuse_weights = 0
+    assert run.layer.device_error() == 0
+    for a, b in zip((run.y, run.dx, run.dw1p, run.dw2, run.d_probs), want):
+        assert torch.equal(a, b)

@@ -141,13 +141,17 @@ def test_nvfp4_layer_parity(lib, name):
     cfg = CASES[name]
     inp = Inputs(cfg)
     run = LayerRun(inp)
+    r = check_nvfp4(cfg, inp, run)
+    if name == "clamped_skew":
+        assert (np.bincount(r.ids.ravel(), minlength=cfg.E) == 0).any()
+
+
+def check_nvfp4(cfg, inp, run):
     mask = synth.gen_rht_mask(cfg)
     r = om.layer_nvfp4(inp.logits, om.bf16_to_f64(inp.x), om.bf16_to_f64(inp.w1),
                        om.bf16_to_f64(inp.w2), cfg.k, act_params(cfg), mask,
                        dy=om.bf16_to_f64(inp.dy), align=cfg.align)
     counts = np.bincount(r.ids.ravel(), minlength=cfg.E)
-    if name == "clamped_skew":
-        assert (counts == 0).any()
     # the BF16 tensors the fused kernels emit, row by row of each expert's segment
     Z = run.unpack_cols(to_np(run.ws("z", torch.bfloat16, cfg.N1)))
     A = to_np(run.ws("a_s", torch.bfloat16, cfg.F))
@@ -174,6 +178,47 @@ def test_nvfp4_layer_parity(lib, name):
     assert rel_fro(to_np(run.d_probs), r.d_probs) < NV_TOL
     assert rel_fro(to_np(run.dw2), r.dW2) < NV_TOL
     assert rel_fro(run.dw1_logical(), r.dW1) < NV_TOL
+    return r
+
+
+def test_nvfp4_cuda_graph_capture_and_replay_with_new_routing(lib):
+    """The NVFP4 step (route with its amaxes, weight amaxes and copies, the quantisers, all
+    GEMMs and the amax resets) has no host sync: capture it once, replay it after
+    overwriting the logits in place, and the new routing's layer comes out."""
+    cfg = CASES["clamped_skew"]
+    run = LayerRun(Inputs(cfg))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            run.run(sync=False)
+    lg2 = synth.gen_logits(cfg.with_(seed=98))
+    run.logits_d.copy_(torch.from_numpy(lg2))
+    graph.replay()
+    torch.cuda.synchronize()
+    check_nvfp4(cfg, Inputs(cfg, logits=lg2), run)
+    # the replay is the eager step, bit for bit
+    got = [t.clone() for t in (run.y, run.dx, run.dw1p, run.dw2, run.d_probs)]
+    run.run()
+    for a, b in zip(got, (run.y, run.dx, run.dw1p, run.dw2, run.d_probs)):
+        assert torch.equal(a, b)
+
+
+def test_nvfp4_reused_weight_copies(lib):
+    """reuse_weights: a second micro-batch that reuses the first forward's NVFP4 weight copies
+    and amaxes gives bit-identical results to one that quantises the weights again."""
+    cfg = CASES["geglu_ragged"]
+    run = LayerRun(Inputs(cfg))
+    run.logits_d.copy_(torch.from_numpy(synth.gen_logits(cfg.with_(seed=77))))
+    run.run()
+    want = [t.clone() for t in (run.y, run.dx, run.dw1p, run.dw2, run.d_probs)]
+    run.layer.desc.reuse_weights = 1
+    run.run()
+    run.layer.desc.reuse_weights = 0
+    assert run.layer.device_error() == 0
+    for a, b in zip((run.y, run.dx, run.dw1p, run.dw2, run.d_probs), want):
+        assert torch.equal(a, b)
 
 
 def test_nvfp4_layer_is_not_the_bf16_layer(lib):

@@ -72,10 +72,11 @@ struct GemmArgs {
   int* err;
 };
 
-template <int BN, int STAGES>
+// PAIR: the CTA holds half of the B tile (the pair's MMA reads both halves).
+template <int BN, int STAGES, bool PAIR = false>
 struct Smem {
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int DATA = STAGES * STAGE_BYTES;
   static constexpr int CTRL = 4096;
@@ -99,7 +100,8 @@ struct TileInfo {
   int e, m0, n0, kbeg, klen, nkb, row_end;
 };
 
-template <int BN, bool KG>
+// Tiles are TM rows (128, or 256 for a CTA pair) by BN columns.
+template <int BN, bool KG, int TM = BM>
 MOE_DEVICE void decode_tile(int tile, const GemmArgs& p, const Ctrl& c, int MT, int NT,
                             TileInfo& t) {
   if (!KG) {
@@ -111,9 +113,9 @@ MOE_DEVICE void decode_tile(int tile, const GemmArgs& p, const Ctrl& c, int MT, 
     const int e = lo;
     const int local = tile - c.prefix[e];
     const int seg = c.off[e + 1] - c.off[e];
-    const int mt = (seg + BM - 1) / BM;
+    const int mt = (seg + TM - 1) / TM;
     t.e = e;
-    t.m0 = c.off[e] + (local % mt) * BM;
+    t.m0 = c.off[e] + (local % mt) * TM;
     t.n0 = (local / mt) * BN;
     t.kbeg = 0;
     t.klen = p.K;
@@ -126,7 +128,7 @@ MOE_DEVICE void decode_tile(int tile, const GemmArgs& p, const Ctrl& c, int MT, 
     const int e = tile / per;
     const int local = tile - e * per;
     t.e = e;
-    t.m0 = (local / NT) * BM;
+    t.m0 = (local / NT) * TM;
     t.n0 = (local % NT) * BN;
     t.kbeg = c.off[e];
     t.klen = c.off[e + 1] - c.off[e];
@@ -219,19 +221,36 @@ MOE_DEVICE void st_bf16x16(void* dst, const uint32_t (&w)[8], bool wide) {
 
 // EXT: the GLU / dGLU epilogue with the bias and feature-scale extras (a separate
 // instantiation, so the plain kernels carry none of its code or registers).
-template <int BN, int STAGES, bool A_MN, bool B_MN, int EPI, bool KG, bool B3D, bool EXT = false>
+//
+// PAIR: the kernel runs as clusters of two CTAs on neighbouring SMs, each pair computing
+// 256 x BN tiles with one cta_group::2 MMA per K step: CTA rank r loads rows 128r.. of the
+// tile's A and columns (BN/2)r.. of its B, and keeps rows 128r.. of the accumulator in its
+// own TMEM. Per K step a CTA moves 2/3 of the bytes a 128 x BN tile needs, for the same MMA
+// work per SM. The even-ranked (leader) CTA issues every MMA. Both CTAs' TMA loads of a stage
+// complete on the leader's full[s] barrier, which the leader arms with the pair's bytes; the
+// follower's epilogue warps free the accumulator on the leader's tempty barrier; the leader's
+// MMA commits reach both CTAs' empty / tfull barriers by multicast. Before it exits the
+// follower waits until the MMAs have consumed its last loads, the leader until the last
+// stages it armed have landed.
+template <int BN, int STAGES, bool A_MN, bool B_MN, int EPI, bool KG, bool B3D, bool EXT = false,
+          bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
-  using L = Smem<BN, STAGES>;
+  using L = Smem<BN, STAGES, PAIR>;
+  constexpr int TM = PAIR ? 2 * BM : BM;    // tile rows
+  constexpr int BNH = PAIR ? BN / 2 : BN;   // B columns this CTA loads
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   Ctrl& c = *reinterpret_cast<Ctrl*>(smem + L::DATA);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &c.abort;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int tile0 = PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
+  const int tstep = PAIR ? (int)nclusters_x() : (int)gridDim.x;
 
   const int NT = (p.N + BN - 1) / BN;
-  const int MT = KG ? (p.M + BM - 1) / BM : 0;
+  const int MT = KG ? (p.M + TM - 1) / TM : 0;
 
   if (threadIdx.x == 0) {
 #pragma unroll
@@ -241,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c.tfull[i], 1);
-      mbar_init(&c.tempty[i], kEpiWarps);
+      mbar_init(&c.tempty[i], PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(&c.drain, 1);
     fence_mbar_init();
@@ -260,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < p.E; ++e) {
         c.prefix[e] = total;
         if (KG) total += MT * NT;
-        else total += ((c.off[e + 1] - c.off[e] + BM - 1) / BM) * NT;
+        else total += ((c.off[e + 1] - c.off[e] + TM - 1) / TM) * NT;
       }
       c.prefix[p.E] = total;
     } else {
@@ -273,11 +292,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&p.tmB);
   }
   if (warp == 1) {
-    tmem_alloc(&c.tmem_base, 2 * BN);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(&c.tmem_base, 2 * BN);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&c.tmem_base, 2 * BN);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // both CTAs' barriers are initialised before either signals the other
+  if constexpr (PAIR) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = c.tmem_base;
   const int total = c.total_tiles;
@@ -290,33 +316,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       int armed[STAGES];
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) armed[s] = -1;
-      for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+      // pair: every load completes on the leader's full barrier
+      const uint32_t full_leader = PAIR ? mapa_shared(smem_u32(&c.full[0]), 0) : 0u;
+      for (int tile = tile0; tile < total && !*abort; tile += tstep) {
         TileInfo t;
-        decode_tile<BN, KG>(tile, p, c, MT, NT, t);
+        decode_tile<BN, KG, TM>(tile, p, c, MT, NT, t);
+        const int am0 = t.m0 + BM * (int)rank;    // this CTA's A rows
+        const int bn0 = t.n0 + BNH * (int)rank;   // this CTA's B columns
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(&c.empty[stage], phase ^ 1, abort, p.err)) break;
           uint8_t* sA = smem + stage * L::STAGE_BYTES;
           uint8_t* sB = sA + L::A_BYTES;
           uint64_t* bar = &c.full[stage];
-          mbar_arrive_expect_tx(bar, L::STAGE_BYTES);
+          const uint32_t bar_c = full_leader + stage * (uint32_t)sizeof(uint64_t);
+          if (!PAIR) mbar_arrive_expect_tx(bar, L::STAGE_BYTES);
+          else if (rank == 0) mbar_arrive_expect_tx(bar, 2 * L::STAGE_BYTES);
 #pragma unroll
           for (int s = 0; s < STAGES; ++s)
             if (s == stage) armed[s] = (int)phase;
           const int k0 = t.kbeg + kb * BK;
+          auto ld2 = [&](void* dst, const CUtensorMap* m, int x, int y) {
+            if constexpr (PAIR) tma_load_2d_pair(dst, m, bar_c, x, y);
+            else tma_load_2d(dst, m, bar, x, y);
+          };
+          auto ld3 = [&](void* dst, const CUtensorMap* m, int x, int y, int z) {
+            if constexpr (PAIR) tma_load_3d_pair(dst, m, bar_c, x, y, z);
+            else tma_load_3d(dst, m, bar, x, y, z);
+          };
           if (!A_MN) {
-            tma_load_2d(sA, &p.tmA, bar, k0, t.m0);
+            ld2(sA, &p.tmA, k0, am0);
           } else {
-            tma_load_2d(sA, &p.tmA, bar, t.m0, k0);
-            tma_load_2d(sA + 64 * 128, &p.tmA, bar, t.m0 + 64, k0);
+            ld2(sA, &p.tmA, am0, k0);
+            ld2(sA + 64 * 128, &p.tmA, am0 + 64, k0);
           }
           if (!B_MN) {
-            if (B3D) tma_load_3d(sB, &p.tmB, bar, k0, t.n0, t.e);
-            else tma_load_2d(sB, &p.tmB, bar, k0, t.n0);
+            if (B3D) ld3(sB, &p.tmB, k0, bn0, t.e);
+            else ld2(sB, &p.tmB, k0, bn0);
           } else {
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i) {
-              if (B3D) tma_load_3d(sB + i * 64 * 128, &p.tmB, bar, t.n0 + 64 * i, k0, t.e);
-              else tma_load_2d(sB + i * 64 * 128, &p.tmB, bar, t.n0 + 64 * i, k0);
+            for (int i = 0; i < BNH / 64; ++i) {
+              if (B3D) ld3(sB + i * 64 * 128, &p.tmB, bn0 + 64 * i, k0, t.e);
+              else ld2(sB + i * 64 * 128, &p.tmB, bn0 + 64 * i, k0);
             }
           }
           if (++stage == STAGES) {
@@ -325,28 +365,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // let every load this thread issued land before the CTA can exit
+      // let every load this thread issued land before the CTA can exit: the leader (or a
+      // single CTA) waits on the full barriers it armed, which also count a pair follower's
+      // bytes; a pair follower waits until the MMAs have consumed its last load of each stage
+      // (the consuming commit also arrives in its shared memory)
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) {
         if (armed[s] >= 0) {
+          const uint32_t bar_s = (PAIR && rank != 0) ? smem_u32(&c.empty[s]) : smem_u32(&c.full[s]);
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(smem_u32(&c.full[s]), (uint32_t)armed[s]) &&
+          while (!mbar_try_wait(bar_s, (uint32_t)armed[s]) &&
                  globaltimer_ns() - t0 < kWaitLimitNs) {
           }
         }
       }
     }
+  } else if (warp == 1 && PAIR && rank != 0) {
+    // pair follower: no MMAs to issue (the leader issues the pair's)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
+      constexpr uint32_t IDESC = idesc_bf16(TM, BN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int acc_i = 0;
       bool issued_any = false;
-      for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+      for (int tile = tile0; tile < total && !*abort; tile += tstep) {
         TileInfo t;
-        decode_tile<BN, KG>(tile, p, c, MT, NT, t);
+        decode_tile<BN, KG, TM>(tile, p, c, MT, NT, t);
         if (t.nkb == 0) continue;
         const int acc = acc_i & 1;
         const uint32_t acc_phase = (acc_i >> 1) & 1;
@@ -372,22 +418,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      : smem_desc_sw128(sA + ks * (UMMA_K * 2), 16, 1024);
             const uint64_t bd = B_MN ? smem_desc_sw128(sB + ks * (UMMA_K * 128), 64 * 128, 1024)
                                      : smem_desc_sw128(sB + ks * (UMMA_K * 2), 16, 1024);
-            mma_bf16_ss(d_tmem, ad, bd, IDESC, (kb | ks) != 0 ? 1u : 0u);
+            if constexpr (PAIR) mma_bf16_ss_pair(d_tmem, ad, bd, IDESC, (kb | ks) != 0 ? 1u : 0u);
+            else mma_bf16_ss(d_tmem, ad, bd, IDESC, (kb | ks) != 0 ? 1u : 0u);
           }
           issued_any = true;
-          mma_commit(&c.empty[stage]);
+          if constexpr (PAIR) mma_commit_pair_mc(&c.empty[stage], 0x3);
+          else mma_commit(&c.empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        mma_commit(&c.tfull[acc]);
+        if constexpr (PAIR) mma_commit_pair_mc(&c.tfull[acc], 0x3);
+        else mma_commit(&c.tfull[acc]);
         ++acc_i;
       }
       // drain: every MMA this thread issued completes before TMEM is released
       if (issued_any) {
-        mma_commit(&c.drain);
+        if constexpr (PAIR) mma_commit_pair_mc(&c.drain, 0x1);
+        else mma_commit(&c.drain);
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(smem_u32(&c.drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
         }
@@ -399,12 +449,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     int acc_i = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    // the accumulator is freed on the leader's barrier (a pair's MMAs write both CTAs' TMEM)
+    const uint32_t tempty_leader = PAIR ? mapa_shared(smem_u32(&c.tempty[0]), 0) : 0u;
+    for (int tile = tile0; tile < total; tile += tstep) {
       // every give-up decision is warp-uniform: the epilogue uses full-warp TMEM loads,
       // shuffles and __syncwarp, which all 32 lanes must reach together
       if (__shfl_sync(0xFFFFFFFFu, *abort, 0)) break;
       TileInfo t;
-      decode_tile<BN, KG>(tile, p, c, MT, NT, t);
+      decode_tile<BN, KG, TM>(tile, p, c, MT, NT, t);
+      t.m0 += BM * (int)rank;                    // this CTA's 128 rows of the tile
       const int row = t.m0 + q * 32 + lane;
       const bool row_ok = row < t.row_end;
       const int c0 = half * (BN / 2), c1 = c0 + BN / 2;  // this warp's accumulator columns
@@ -568,16 +621,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&c.tempty[acc]);
+      if (lane == 0) {
+        if constexpr (PAIR) mbar_arrive_cluster(tempty_leader + acc * (uint32_t)sizeof(uint64_t));
+        else mbar_arrive(&c.tempty[acc]);
+      }
       ++acc_i;
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  // a pair: neither CTA leaves while the other may still read its shared memory (the
+  // leader's MMAs) or signal its barriers
+  if constexpr (PAIR) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 2 * BN);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, 2 * BN);
+    else tmem_dealloc(tmem_base, 2 * BN);
   }
 }
 
@@ -592,8 +652,46 @@ cudaError_t launch_instance(const GemmArgs& a, int grid, cudaStream_t s, int kid
   return cudaGetLastError();
 }
 
+// Clusters of two CTAs; `ctas` (the SMs the caller allows, SM margin applied) is rounded down
+// to whole pairs and capped by the number of pairs that can be resident at once.
+template <int BN, int STAGES, bool A_MN, bool B_MN, int EPI, bool KG, bool B3D, bool EXT = false>
+cudaError_t launch_pair_instance(const GemmArgs& a, int ctas, int64_t tiles, cudaStream_t s,
+                                 int kid) {
+  auto kern = grouped_gemm_kernel<BN, STAGES, A_MN, B_MN, EPI, KG, B3D, EXT, true>;
+  constexpr int smem = Smem<BN, STAGES, true>::TOTAL;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int pairs = std::max(1, ctas / 2);
+  const int resident = max_resident_pairs(reinterpret_cast<const void*>(kern), &cfg);
+  if (resident > 0) pairs = std::min(pairs, resident);
+  pairs = (int)std::max<int64_t>(1, std::min<int64_t>(pairs, tiles));
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  e = cudaLaunchKernelEx(&cfg, kern, a);
+  count_launch(s, kid);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 constexpr int kBN = 256;
 constexpr int kStages = 4;
+constexpr int kPairStages = 6;   // 32 KB per stage and CTA
+// the grouped GEMMs run as CTA pairs (256-row tiles, cta_group::2 MMAs); 0 selects the
+// one-CTA kernels (128-row tiles)
+#ifndef MOE_GEMM_PAIR
+#define MOE_GEMM_PAIR 1
+#endif
+constexpr bool kUsePairs = MOE_GEMM_PAIR != 0;
 
 }  // namespace
 
@@ -626,21 +724,28 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
   auto aligned32 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 31) == 0; };
   const int H = p.H, F = p.F, N1 = p.N1, E = p.E;
   bool ok = true;
-  int grid = p.num_ctas;
+  const int ctas = p.num_ctas;
+  // K-major weight tiles: one box of the B columns a CTA loads (half the tile for a pair)
+  constexpr int kBRows = kUsePairs ? kBN / 2 : kBN;
+  const int64_t any_tiles = INT64_MAX;  // row-grouped tile count lives on the device
+#define MOE_LAUNCH(A_MN, B_MN, EPI, KG, B3D, EXT, TILES)                                        \
+  (kUsePairs                                                                                   \
+       ? launch_pair_instance<kBN, kPairStages, A_MN, B_MN, EPI, KG, B3D, EXT>(a, ctas, TILES, \
+                                                                               s, kid)         \
+       : launch_instance<kBN, kStages, A_MN, B_MN, EPI, KG, B3D, EXT>(                         \
+             a, (int)std::min<int64_t>(ctas, TILES), s, kid))
   switch (p.role) {
     case ROLE_FC1_FPROP:
       ok &= tmap_2d(&a.tmA, p.x_perm, H, R, 64, BM);
-      ok &= tmap_3d(&a.tmB, p.w1p, H, N1, E, 64, kBN);
+      ok &= tmap_3d(&a.tmB, p.w1p, H, N1, E, 64, kBRows);
       a.K = H; a.N = N1;
       a.out = p.out; a.ldo = N1;
       a.out2 = p.out2; a.ldo2 = F;
       if (!ok) return cudaErrorInvalidValue;
       a.wide = aligned32(a.out) && aligned32(a.out2) && a.ldo % 16 == 0 && a.ldo2 % 16 == 0 &&
                a.out_estride % 16 == 0;
-      if (a.fc1_bias || a.fscale)
-        return launch_instance<kBN, kStages, false, false, EPI_GLU, false, true, true>(a, grid, s,
-                                                                                      kid);
-      return launch_instance<kBN, kStages, false, false, EPI_GLU, false, true>(a, grid, s, kid);
+      if (a.fc1_bias || a.fscale) return MOE_LAUNCH(false, false, EPI_GLU, false, true, true, any_tiles);
+      return MOE_LAUNCH(false, false, EPI_GLU, false, true, false, any_tiles);
     case ROLE_FC2_FPROP:
       ok &= tmap_2d(&a.tmA, p.a_s, F, R, 64, BM);
       ok &= tmap_3d(&a.tmB, p.w2, H, F, E, 64, 64);
@@ -649,7 +754,7 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       if (!ok) return cudaErrorInvalidValue;
       a.wide = aligned32(a.out) && aligned32(a.out2) && a.ldo % 16 == 0 && a.ldo2 % 16 == 0 &&
                a.out_estride % 16 == 0;
-      return launch_instance<kBN, kStages, false, true, EPI_STORE, false, true>(a, grid, s, kid);
+      return MOE_LAUNCH(false, true, EPI_STORE, false, true, false, any_tiles);
     case ROLE_FC2_DGRAD:
       ok &= tmap_2d(&a.tmA, p.dy_perm, H, R, 64, BM);
       ok &= tmap_3d(&a.tmB, p.w2, H, F, E, 64, kBN);
@@ -660,10 +765,12 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       if (!ok) return cudaErrorInvalidValue;
       a.wide = aligned32(a.out) && aligned32(a.out2) && a.ldo % 16 == 0 && a.ldo2 % 16 == 0 &&
                a.out_estride % 16 == 0;
+      // the dGLU epilogue sets this kernel's pace: one-CTA tiles (measured as fast or faster,
+      // and no pair tile past a short segment's end)
       if (a.ext_part)
-        return launch_instance<kBN, kStages, false, false, EPI_DGLU, false, true, true>(a, grid, s,
+        return launch_instance<kBN, kStages, false, false, EPI_DGLU, false, true, true>(a, ctas, s,
                                                                                        kid);
-      return launch_instance<kBN, kStages, false, false, EPI_DGLU, false, true>(a, grid, s, kid);
+      return launch_instance<kBN, kStages, false, false, EPI_DGLU, false, true>(a, ctas, s, kid);
     case ROLE_FC1_DGRAD:
       ok &= tmap_2d(&a.tmA, p.dz, N1, R, 64, BM);
       ok &= tmap_3d(&a.tmB, p.w1p, H, N1, E, 64, 64);
@@ -672,7 +779,7 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       if (!ok) return cudaErrorInvalidValue;
       a.wide = aligned32(a.out) && aligned32(a.out2) && a.ldo % 16 == 0 && a.ldo2 % 16 == 0 &&
                a.out_estride % 16 == 0;
-      return launch_instance<kBN, kStages, false, true, EPI_STORE, false, true>(a, grid, s, kid);
+      return MOE_LAUNCH(false, true, EPI_STORE, false, true, false, any_tiles);
     case ROLE_FC2_WGRAD:
     case ROLE_FC1_WGRAD: {
       const bool fc2 = p.role == ROLE_FC2_WGRAD;
@@ -683,11 +790,13 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       a.out = p.out; a.ldo = H; a.out_estride = (int64_t)M * H;
       if (!ok) return cudaErrorInvalidValue;
       a.wide = aligned32(a.out) && a.ldo % 16 == 0 && a.out_estride % 16 == 0;
+      // weight gradients stay on one-CTA 128 x 256 tiles: measured faster than pairs here
       const int64_t tiles = (int64_t)E * ((M + BM - 1) / BM) * ((H + kBN - 1) / kBN);
-      grid = (int)std::min<int64_t>(grid, tiles);
-      return launch_instance<kBN, kStages, true, true, EPI_STORE, true, false>(a, grid, s, kid);
+      return launch_instance<kBN, kStages, true, true, EPI_STORE, true, false>(
+          a, (int)std::min<int64_t>(ctas, tiles), s, kid);
     }
   }
+#undef MOE_LAUNCH
   return cudaErrorInvalidValue;
 }
 

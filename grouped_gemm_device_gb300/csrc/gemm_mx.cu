@@ -32,20 +32,24 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 128;  // fp8 elements (bytes) per k-block: one 128-byte swizzle row
 constexpr int MMA_K = 32;
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 6;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxE = 256;
 constexpr int kSfCol = BN;  // first TMEM column of the per-stage scale factors
 constexpr int kPackCol = 320;  // dGLU: the drained accumulator as packed bf16 (128 columns)
 constexpr int kTmemCols = 512;
-static_assert(kSfCol + 12 * kMaxStages <= kPackCol && kPackCol + BN / 2 <= kTmemCols, "TMEM map");
+static_assert(kPackCol + BN / 2 <= kTmemCols, "TMEM map");
 
 enum { EPI_STORE = 0, EPI_GLU = 1, EPI_DGLU = 2 };
 
 struct MxArgs {
   CUtensorMap tmA;
   CUtensorMap tmB;
+  // pair kernels: the scale buffers as [bytes / 16, 16] uint8 tensors, so that a CTA's scale
+  // slabs are TMA loads that can complete on the pair leader's barrier
+  CUtensorMap tmSFA;
+  CUtensorMap tmSFB;
   const uint8_t* sfa;
   int64_t sfa_pad;
   const uint8_t* sfb;
@@ -79,7 +83,6 @@ struct MxArgs {
 
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SFA_BYTES = 512;   // 128 rows x 4 k-blocks
 constexpr int SFB_BYTES = 1024;  // 256 rows x 4 k-blocks
 constexpr int XP_ROW = 80;  // bytes per row of the per-warp 32 x 32 bf16 staging tile (+16 pad)
@@ -88,10 +91,13 @@ constexpr int ZST_WARP_BYTES = 32 * 128;  // dGLU: saved Z of one chunk, 32 rows
 
 // Shared-memory map of one kernel: four pipeline stages, except for the dGLU kernel, whose Z
 // buffer takes the fourth stage's space. STORE kernels have no quantisation staging tiles.
-template <int EPI>
+// PAIR: a CTA of a pair holds half of the B tile (and all of its scale factors), so more
+// stages fit: 6 (STORE), 5 (GLU, dGLU).
+template <int EPI, bool PAIR = false>
 struct MxSmem {
-  static constexpr int STAGES = EPI == 2 ? 3 : 4;
-  static constexpr int DATA = STAGES * STAGE_BYTES;
+  static constexpr int STAGES = PAIR ? (EPI == 0 ? 6 : 5) : (EPI == 2 ? 3 : 4);
+  static constexpr int STAGE_BYTES_ = A_BYTES + (PAIR ? B_BYTES / 2 : B_BYTES);
+  static constexpr int DATA = STAGES * STAGE_BYTES_;
   static constexpr int SF_OFF = DATA;
   static constexpr int XPOSE_OFF = SF_OFF + STAGES * (SFA_BYTES + SFB_BYTES);
   static constexpr int ZST_OFF = XPOSE_OFF + (EPI == 0 ? 0 : kEpiWarps * XPOSE_WARP_BYTES);
@@ -99,7 +105,10 @@ struct MxSmem {
   static constexpr int TOTAL = CTRL_OFF + 4096 + 1024;
   static_assert(TOTAL <= 232448, "shared memory above the sm_100 per-block limit");
   static_assert(XPOSE_OFF % 16 == 0 && ZST_OFF % 128 == 0 && CTRL_OFF % 8 == 0, "alignment");
-  static_assert(STAGES <= kMaxStages, "TMEM scale columns");
+  static_assert(STAGES <= kMaxStages, "control barriers");
+  // scale columns of every stage below the dGLU's packed accumulator
+  static_assert(EPI != 2 || kSfCol + 12 * STAGES <= kPackCol, "TMEM scale columns");
+  static_assert(kSfCol + 12 * STAGES <= kTmemCols, "TMEM scale columns");
 };
 
 struct Ctrl {
@@ -119,7 +128,8 @@ struct TileInfo {
   int e, m0, n0, kbeg, klen, nkb, row_end;
 };
 
-template <bool KG>
+// Tiles are TM rows (128, or 256 for a CTA pair) by BN columns.
+template <bool KG, int TM = BM>
 MOE_DEVICE void decode_tile(int tile, const MxArgs& p, const Ctrl& c, int MT, int NT, TileInfo& t) {
   if (!KG) {
     int lo = 0, hi = p.E;
@@ -129,9 +139,9 @@ MOE_DEVICE void decode_tile(int tile, const MxArgs& p, const Ctrl& c, int MT, in
     }
     const int e = lo;
     const int local = tile - c.prefix[e];
-    const int mt = (c.off[e + 1] - c.off[e] + BM - 1) / BM;
+    const int mt = (c.off[e + 1] - c.off[e] + TM - 1) / TM;
     t.e = e;
-    t.m0 = c.off[e] + (local % mt) * BM;
+    t.m0 = c.off[e] + (local % mt) * TM;
     t.n0 = (local / mt) * BN;
     t.kbeg = 0;
     t.klen = p.K;
@@ -142,7 +152,7 @@ MOE_DEVICE void decode_tile(int tile, const MxArgs& p, const Ctrl& c, int MT, in
     const int e = tile / per;
     const int local = tile - e * per;
     t.e = e;
-    t.m0 = (local / NT) * BM;
+    t.m0 = (local / NT) * TM;
     t.n0 = (local % NT) * BN;
     t.kbeg = c.off[e];
     t.klen = c.off[e + 1] - c.off[e];
@@ -218,19 +228,34 @@ MOE_DEVICE int gate_col(int f, int ilv) { return ((f & ~(ilv - 1)) << 1) | (f & 
 // A_MN / B_MN: the operand is a column-wise copy stored [K rows, M or N columns] (MN-major);
 // otherwise it is [M or N rows, K] (K-major). KIND: the activation of the GLU / dGLU epilogue
 // (moe_activation_t; unused by STORE). ILV: the gate/linear interleave of the GLU epilogue.
-template <int EPI, int KIND, bool KG, int ILV, bool A_MN, bool B_MN>
+//
+// PAIR: clusters of two CTAs compute 256 x 256 tiles with cta_group::2 block-scaled MMAs. CTA
+// rank r loads rows 128r.. of A, rows 128r.. of the B tile (half of it) and the scale factors
+// of its A rows and of all 256 B rows (each SM's tensor core needs the B scales in its own
+// TMEM); it keeps rows 128r.. of the accumulator. Both CTAs' loads of a stage (operands and
+// scale slabs, all TMA) complete on the leader's full barrier, which the leader arms with the
+// pair's bytes; the leader (rank 0) then copies the scales into both CTAs' TMEM and issues the
+// MMAs; MMA commits reach both CTAs by multicast; the follower's epilogue frees the
+// accumulator on the leader's barrier. Expert segments are 128-row aligned, so each CTA's
+// half of a tile lies wholly inside or wholly past its segment.
+template <int EPI, int KIND, bool KG, int ILV, bool A_MN, bool B_MN, bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __grid_constant__ MxArgs p) {
   constexpr bool kGated = KIND != MOE_ACT_SRELU;
-  using L = MxSmem<EPI>;
+  using L = MxSmem<EPI, PAIR>;
   constexpr int STAGES = L::STAGES;
+  constexpr int SBYTES = L::STAGE_BYTES_;
+  constexpr int TM = PAIR ? 2 * BM : BM;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   Ctrl& c = *reinterpret_cast<Ctrl*>(smem + L::CTRL_OFF);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &c.abort;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int tile0 = PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
+  const int tstep = PAIR ? (int)nclusters_x() : (int)gridDim.x;
   const int NT = (p.N + BN - 1) / BN;
-  const int MT = KG ? (p.M + BM - 1) / BM : 0;
+  const int MT = KG ? (p.M + TM - 1) / TM : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -238,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
       mbar_init(&c.empty[s], 1);
     }
     mbar_init(&c.tfull, 1);
-    mbar_init(&c.tempty, kEpiWarps);
+    mbar_init(&c.tempty, PAIR ? 2 * kEpiWarps : kEpiWarps);
     mbar_init(&c.drain, 1);
     fence_mbar_init();
     c.abort = 0;
@@ -255,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
     if (ok) {
       for (int e = 0; e < p.E; ++e) {
         c.prefix[e] = total;
-        total += KG ? MT * NT : ((c.off[e + 1] - c.off[e] + BM - 1) / BM) * NT;
+        total += KG ? MT * NT : ((c.off[e + 1] - c.off[e] + TM - 1) / TM) * NT;
       }
       c.prefix[p.E] = total;
     } else {
@@ -268,11 +293,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
     tma_prefetch_desc(&p.tmB);
   }
   if (warp == 1) {
-    tmem_alloc(&c.tmem_base, kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(&c.tmem_base, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&c.tmem_base, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // both CTAs' barriers are initialised before either signals the other
+  if constexpr (PAIR) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = c.tmem_base;
   const int total = c.total_tiles;
@@ -285,53 +317,74 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
       int armed[STAGES];
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) armed[s] = -1;
-      for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+      // pair: every load completes on the leader's full barrier
+      const uint32_t full_leader = PAIR ? mapa_shared(smem_u32(&c.full[0]), 0) : 0u;
+      for (int tile = tile0; tile < total && !*abort; tile += tstep) {
         TileInfo t;
-        decode_tile<KG>(tile, p, c, MT, NT, t);
-        const int a_row = t.m0 + t.e * p.a_row_e;
-        const int b_row = t.n0 + t.e * p.b_row_e;
+        decode_tile<KG, TM>(tile, p, c, MT, NT, t);
+        const int a_row = t.m0 + BM * (int)rank + t.e * p.a_row_e;  // this CTA's A rows
+        const int b_row_sf = t.n0 + t.e * p.b_row_e;                // the tile's B rows
+        const int b_row = b_row_sf + (BN / 2) * (int)rank;           // pair: this CTA's half
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(&c.empty[stage], phase ^ 1, abort, p.err)) break;
-          uint8_t* sA = smem + stage * STAGE_BYTES;
+          uint8_t* sA = smem + stage * SBYTES;
           uint8_t* sB = sA + A_BYTES;
           uint8_t* sfA = smem + L::SF_OFF + stage * (SFA_BYTES + SFB_BYTES);
           uint64_t* bar = &c.full[stage];
-          mbar_arrive_expect_tx(bar, STAGE_BYTES + SFA_BYTES + SFB_BYTES);
+          const uint32_t bar_c = full_leader + stage * (uint32_t)sizeof(uint64_t);
+          if (!PAIR) mbar_arrive_expect_tx(bar, SBYTES + SFA_BYTES + SFB_BYTES);
+          else if (rank == 0) mbar_arrive_expect_tx(bar, 2 * (SBYTES + SFA_BYTES + SFB_BYTES));
 #pragma unroll
           for (int s = 0; s < STAGES; ++s)
             if (s == stage) armed[s] = (int)phase;
           const int k0 = t.kbeg + kb * BK;
           const int a_k = k0 + t.e * p.a_k_e;
           const int b_k = k0 + t.e * p.b_k_e;
+          const int64_t sfa_off = ((int64_t)(a_k / BK) * p.sfa_pad + a_row) * 4;
+          const int64_t sfb_off = ((int64_t)(b_k / BK) * p.sfb_pad + b_row_sf) * 4;
           // boxes are 128 x 128 bytes: K-major {k, row}, MN-major {mn, k}
-          if (!A_MN) tma_load_2d(sA, &p.tmA, bar, a_k, a_row);
-          else tma_load_2d(sA, &p.tmA, bar, a_row, a_k);
-          if (!B_MN) {
-            tma_load_2d(sB, &p.tmB, bar, b_k, b_row);
-            tma_load_2d(sB + B_BYTES / 2, &p.tmB, bar, b_k, b_row + 128);
+          if constexpr (PAIR) {
+            if (!A_MN) tma_load_2d_pair(sA, &p.tmA, bar_c, a_k, a_row);
+            else tma_load_2d_pair(sA, &p.tmA, bar_c, a_row, a_k);
+            if (!B_MN) tma_load_2d_pair(sB, &p.tmB, bar_c, b_k, b_row);
+            else tma_load_2d_pair(sB, &p.tmB, bar_c, b_row, b_k);
+            // scale slabs start on 512-byte boundaries: rows of 16 bytes
+            tma_load_2d_pair(sfA, &p.tmSFA, bar_c, 0, (int)(sfa_off >> 4));
+            tma_load_2d_pair(sfA + SFA_BYTES, &p.tmSFB, bar_c, 0, (int)(sfb_off >> 4));
           } else {
-            tma_load_2d(sB, &p.tmB, bar, b_row, b_k);
-            tma_load_2d(sB + B_BYTES / 2, &p.tmB, bar, b_row + 128, b_k);
+            if (!A_MN) tma_load_2d(sA, &p.tmA, bar, a_k, a_row);
+            else tma_load_2d(sA, &p.tmA, bar, a_row, a_k);
+            if (!B_MN) {
+              tma_load_2d(sB, &p.tmB, bar, b_k, b_row);
+              tma_load_2d(sB + B_BYTES / 2, &p.tmB, bar, b_k, b_row + 128);
+            } else {
+              tma_load_2d(sB, &p.tmB, bar, b_row, b_k);
+              tma_load_2d(sB + B_BYTES / 2, &p.tmB, bar, b_row + 128, b_k);
+            }
+            bulk_load(sfA, p.sfa + sfa_off, SFA_BYTES, bar);
+            bulk_load(sfA + SFA_BYTES, p.sfb + sfb_off, SFB_BYTES, bar);
           }
-          bulk_load(sfA, p.sfa + ((int64_t)(a_k / BK) * p.sfa_pad + a_row) * 4, SFA_BYTES, bar);
-          bulk_load(sfA + SFA_BYTES, p.sfb + ((int64_t)(b_k / BK) * p.sfb_pad + b_row) * 4,
-                    SFB_BYTES, bar);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
+      // let every load this thread issued land before the CTA can exit: the leader (or a
+      // single CTA) waits on the full barriers it armed, which also count a pair follower's
+      // bytes; a pair follower waits until the MMAs have consumed its last load of each stage
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) {
         if (armed[s] >= 0) {
+          const uint32_t bar_s = (PAIR && rank != 0) ? smem_u32(&c.empty[s]) : smem_u32(&c.full[s]);
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(smem_u32(&c.full[s]), (uint32_t)armed[s]) &&
-                 globaltimer_ns() - t0 < kWaitLimitNs) {
+          while (!mbar_try_wait(bar_s, (uint32_t)armed[s]) && globaltimer_ns() - t0 < kWaitLimitNs) {
           }
         }
       }
     }
+  } else if (warp == 1 && PAIR && rank != 0) {
+    // pair follower: no MMAs to issue (the leader issues the pair's)
   } else if (warp == 1) {
     // ------------------------------------------------------------ scale copy + MMA issuer
     if (lane == 0) {
@@ -339,9 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
       uint32_t phase = 0;
       int acc_i = 0;
       bool issued_any = false;
-      for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+      for (int tile = tile0; tile < total && !*abort; tile += tstep) {
         TileInfo t;
-        decode_tile<KG>(tile, p, c, MT, NT, t);
+        decode_tile<KG, TM>(tile, p, c, MT, NT, t);
         if (t.nkb == 0) continue;
         // the single accumulator is free once every epilogue warp drained the last tile
         if (!mbar_wait(&c.tempty, (acc_i & 1) ^ 1, abort, p.err)) break;
@@ -353,14 +406,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
             break;
           }
           tc_fence_after();
-          const uint32_t sA = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sA = smem_u32(smem + stage * SBYTES);
           const uint32_t sB = sA + A_BYTES;
           const uint32_t sfA = smem_u32(smem + L::SF_OFF + stage * (SFA_BYTES + SFB_BYTES));
           const uint32_t sfa_t = tmem_base + kSfCol + stage * 12;
           const uint32_t sfb_t = sfa_t + 4;
-          tmem_cp_32x128b_warpx4(sfa_t, smem_desc_noswizzle(sfA, 0, 128));
-          tmem_cp_32x128b_warpx4(sfb_t, smem_desc_noswizzle(sfA + SFA_BYTES, 0, 128));
-          tmem_cp_32x128b_warpx4(sfb_t + 4, smem_desc_noswizzle(sfA + SFA_BYTES + 512, 0, 128));
+          if constexpr (PAIR) {
+            tmem_cp_32x128b_warpx4_pair(sfa_t, smem_desc_noswizzle(sfA, 0, 128));
+            tmem_cp_32x128b_warpx4_pair(sfb_t, smem_desc_noswizzle(sfA + SFA_BYTES, 0, 128));
+            tmem_cp_32x128b_warpx4_pair(sfb_t + 4,
+                                        smem_desc_noswizzle(sfA + SFA_BYTES + 512, 0, 128));
+          } else {
+            tmem_cp_32x128b_warpx4(sfa_t, smem_desc_noswizzle(sfA, 0, 128));
+            tmem_cp_32x128b_warpx4(sfb_t, smem_desc_noswizzle(sfA + SFA_BYTES, 0, 128));
+            tmem_cp_32x128b_warpx4(sfb_t + 4, smem_desc_noswizzle(sfA + SFA_BYTES + 512, 0, 128));
+          }
           const int rem = t.klen - kb * BK;
           const int nsub = rem >= BK ? BK / MMA_K : (rem + MMA_K - 1) / MMA_K;
           for (int ks = 0; ks < nsub; ++ks) {
@@ -371,22 +431,29 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
                                      : smem_desc_sw128(sA + ks * MMA_K, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc_sw128(sB + ks * (MMA_K * 128), B_BYTES / 2, 1024)
                                      : smem_desc_sw128(sB + ks * MMA_K, 16, 1024);
-            mma_mxf8_ss(tmem_base, ad, bd, idesc_mxf8(BM, BN, ks, A_MN, B_MN), sfa_t, sfb_t,
-                        (kb | ks) != 0 ? 1u : 0u);
+            if constexpr (PAIR)
+              mma_mxf8_ss_pair(tmem_base, ad, bd, idesc_mxf8(TM, BN, ks, A_MN, B_MN), sfa_t,
+                               sfb_t, (kb | ks) != 0 ? 1u : 0u);
+            else
+              mma_mxf8_ss(tmem_base, ad, bd, idesc_mxf8(BM, BN, ks, A_MN, B_MN), sfa_t, sfb_t,
+                          (kb | ks) != 0 ? 1u : 0u);
           }
           issued_any = true;
-          mma_commit(&c.empty[stage]);
+          if constexpr (PAIR) mma_commit_pair_mc(&c.empty[stage], 0x3);
+          else mma_commit(&c.empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        mma_commit(&c.tfull);
+        if constexpr (PAIR) mma_commit_pair_mc(&c.tfull, 0x3);
+        else mma_commit(&c.tfull);
         ++acc_i;
       }
       if (issued_any) {
-        mma_commit(&c.drain);
+        if constexpr (PAIR) mma_commit_pair_mc(&c.drain, 0x1);
+        else mma_commit(&c.drain);
         const uint64_t t0 = globaltimer_ns();
         while (!mbar_try_wait(smem_u32(&c.drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
         }
@@ -400,11 +467,25 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
     const uint8_t* zst = smem + L::ZST_OFF + (warp - 2) * ZST_WARP_BYTES;
     const uint32_t zst_a = smem_u32(zst);
     int acc_i = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    // the accumulator is freed on the leader's barrier (a pair's MMAs write both CTAs' TMEM)
+    const uint32_t tempty_leader = PAIR ? mapa_shared(smem_u32(&c.tempty), 0) : 0u;
+    auto release_acc = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (PAIR) mbar_arrive_cluster(tempty_leader);
+        else mbar_arrive(&c.tempty);
+      }
+    };
+    for (int tile = tile0; tile < total; tile += tstep) {
       // every give-up decision is warp-uniform (full-warp TMEM loads, shuffles, __syncwarp)
       if (__shfl_sync(0xFFFFFFFFu, *abort, 0)) break;
       TileInfo t;
-      decode_tile<KG>(tile, p, c, MT, NT, t);
+      decode_tile<KG, TM>(tile, p, c, MT, NT, t);
+      t.m0 += BM * (int)rank;          // this CTA's 128 rows of the tile
+      // a pair's second half can lie past the segment (segments are 128-row aligned, so a
+      // half is wholly inside or wholly outside): it only frees the accumulator
+      const bool half_live = t.m0 < t.row_end;
       const int row0 = t.m0 + q * 32;  // first row of this warp's 32-row block
       const int row = row0 + lane;
       const bool row_ok = row < t.row_end;
@@ -422,15 +503,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
       if constexpr (EPI == EPI_DGLU) {
         // the saved Z of the first chunk comes in while the MMAs run
         const int f0 = t.n0 + cb;
-        if (f0 < p.N) {
+        if (f0 < p.N && half_live) {
           const int gc = kGated ? gate_col(f0, p.ilv) : f0;
           zst_issue(zst_a, zrow + gc, zrow + gc + p.ilv, lane, kGated);
         }
       }
-      const float prob = EPI == EPI_STORE ? 0.f : p.row_prob[row];
+      const float prob = (EPI == EPI_STORE || !half_live) ? 0.f : p.row_prob[row];
       const bool got = mbar_wait(&c.tfull, acc_i & 1, abort, p.err);
       if (!__all_sync(0xFFFFFFFFu, got)) break;
       tc_fence_after();
+      if (!half_live) {
+        release_acc();
+        ++acc_i;
+        continue;
+      }
       if constexpr (EPI == EPI_GLU) {
         // GLU: drain the 128 columns as fp32 (the activation and its MXFP8 blocks are computed
         // from the fp32 accumulator), free TMEM, then work from registers
@@ -446,9 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
             for (int i = 0; i < 32; ++i) acc[32 * j + i] = __uint_as_float(r[i]);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&c.tempty);
+        release_acc();
         ++acc_i;
         // segments are 128-row aligned, so every row of the tile is inside its segment
         uint16_t* zout = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo + t.n0 + cb;
@@ -511,9 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
         }
       }
       if constexpr (EPI != EPI_STORE) tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&c.tempty);
+      release_acc();
       ++acc_i;
 
       if constexpr (EPI == EPI_STORE) {
@@ -603,9 +685,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
 
   tc_fence_before();
   __syncthreads();
+  // a pair: neither CTA leaves while the other may still read its shared memory (the
+  // leader's MMAs and scale copies) or signal its barriers
+  if constexpr (PAIR) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -619,14 +705,69 @@ bool tmap_fp8(CUtensorMap* m, const MxOperand& t, bool mn_major) {
   return make_tmap(m, t.q, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8);
 }
 
+// The scale slabs of an operand as a [bytes / 16, 16] byte tensor (no swizzle); one box is
+// `rows16` 16-byte rows (32 = one 512-byte slab of 128 rows, 64 = two). The extent is the
+// workspace's scale buffer of the operand, its 1 KB of slack included.
+bool tmap_sf(CUtensorMap* m, const MxOperand& t, uint32_t rows16) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t bytes =
+      (uint64_t)((t.cols / 32 + 3) / 4) * (uint64_t)((t.rows + 127) / 128 * 128) * 4 + 1024;
+  cuuint64_t dims[2] = {16, bytes / 16};
+  cuuint64_t strides[1] = {16};
+  cuuint32_t box[2] = {16, rows16};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, t.s, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 1: the block-scaled GEMMs run as CTA pairs (256-row tiles, cta_group::2 MMAs). Off: with a
+// single TMEM accumulator per CTA (two do not fit beside the scale factors), every tile ends
+// with the MMAs waiting until both CTAs' epilogues have drained it, and the cross-SM signals
+// lengthen that wait; measured 2-20% slower than one-CTA tiles on the Mixtral and GPT-OSS
+// layers, so the one-CTA kernels run.
+#ifndef MOE_GEMM_MX_PAIR
+#define MOE_GEMM_MX_PAIR 0
+#endif
+constexpr bool kMxPairs = MOE_GEMM_MX_PAIR != 0;
+
+// `grid`: the CTAs the caller allows (SM margin applied) or, for a pair kernel, twice the pairs
+// the tile count can use at most; pairs are further capped by how many fit at once.
 template <int EPI, int KIND, bool KG, int ILV, bool A_MN, bool B_MN>
 cudaError_t launch_mx(const MxArgs& a, int grid, cudaStream_t s, int kid) {
-  auto kern = grouped_gemm_mx_kernel<EPI, KIND, KG, ILV, A_MN, B_MN>;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), MxSmem<EPI>::TOTAL);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, MxSmem<EPI>::TOTAL, s>>>(a);
-  count_launch(s, kid);
-  return cudaGetLastError();
+  if constexpr (!kMxPairs) {
+    auto kern = grouped_gemm_mx_kernel<EPI, KIND, KG, ILV, A_MN, B_MN>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), MxSmem<EPI>::TOTAL);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, MxSmem<EPI>::TOTAL, s>>>(a);
+    count_launch(s, kid);
+    return cudaGetLastError();
+  } else {
+    auto kern = grouped_gemm_mx_kernel<EPI, KIND, KG, ILV, A_MN, B_MN, true>;
+    constexpr int smem = MxSmem<EPI, true>::TOTAL;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int pairs = std::max(1, grid / 2);
+    const int resident = max_resident_pairs(reinterpret_cast<const void*>(kern), &cfg);
+    if (resident > 0) pairs = std::min(pairs, resident);
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    e = cudaLaunchKernelEx(&cfg, kern, a);
+    count_launch(s, kid);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
 }
 
 // GLU / dGLU kernels for one activation. The dGLU epilogue takes the interleave at run time;
@@ -714,6 +855,8 @@ cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s) {
   const bool kg = p.role == ROLE_FC2_WGRAD || p.role == ROLE_FC1_WGRAD;
   const bool b_mn = kg || p.role == ROLE_FC2_FPROP || p.role == ROLE_FC1_DGRAD;
   if (!tmap_fp8(&a.tmA, *A, kg) || !tmap_fp8(&a.tmB, *B, b_mn)) return cudaErrorInvalidValue;
+  if (kMxPairs && (!tmap_sf(&a.tmSFA, *A, SFA_BYTES / 16) || !tmap_sf(&a.tmSFB, *B, SFB_BYTES / 16)))
+    return cudaErrorInvalidValue;
   a.sfa = A->s; a.sfa_pad = A->s_pad;
   a.sfb = B->s; a.sfb_pad = B->s_pad;
   a.wide = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0 && a.ldo % 16 == 0 &&
@@ -726,8 +869,9 @@ cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s) {
     case ROLE_FC1_DGRAD:
       return launch_mx<EPI_STORE, 0, false, 64, false, true>(a, grid, s, kid);
     default: {
-      const int64_t tiles = (int64_t)p.E * ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
-      grid = (int)std::min<int64_t>(grid, tiles);
+      constexpr int TMr = kMxPairs ? 2 * BM : BM;
+      const int64_t tiles = (int64_t)p.E * ((a.M + TMr - 1) / TMr) * ((a.N + BN - 1) / BN);
+      grid = (int)std::min<int64_t>(grid, kMxPairs ? 2 * tiles : tiles);
       return launch_mx<EPI_STORE, 0, true, 64, true, true>(a, grid, s, kid);
     }
   }

@@ -24,7 +24,7 @@ Readings of the pages (where they are silent or ambiguous), used consistently be
      own reduction dimension, fp32-or-better accumulation; column-wise blocks of the
      weight-gradient GEMMs start at each expert's first row.
   R9 d_prob[t, j] = sum_f dA_s * a (a unscaled); d_logits is not part of the layer.
-  R10 MXFP8 backward: dZ, whose E4M3 codes are integer decisions the pages give no precision
+  R15 MXFP8 backward: dZ, whose E4M3 codes are integer decisions the pages give no precision
      for, is formed from the fused dGLU epilogue's inputs in the precision the epilogue reads
      them: the saved FC1 output in bf16 and dA_s rounded to bf16.
 """
@@ -245,7 +245,7 @@ def expert_backward(X, W1, W2, p, Z, a, a_s, dY, act: ActParams, mx: bool,
     db1 = sum over rows of dZ and ds = sum over rows of p * dA_s * a.
     MXFP8 (R8): dY and W2 along H for dgrad; a_s and dY column-wise (along rows) for dW2;
     dZ along N1 and W1 along N1 for dX; X and dZ column-wise for dW1.
-    MXFP8, R10: the E4M3 codes of dZ are integer decisions taken on the values the fused dGLU
+    MXFP8, R15: the E4M3 codes of dZ are integer decisions taken on the values the fused dGLU
     epilogue reads, so the oracle forms dZ from the same inputs: the saved FC1 output in bf16
     (the saved activation is bf16) and the FC2-dgrad result dA_s rounded to bf16 (the
     precision in which the epilogue holds it); d_prob keeps the plain definition.

@@ -144,7 +144,7 @@ def test_fullsize_sampled_parity(lib, name):
         fs_t, hs_t = torch.as_tensor(fs, device="cuda"), torch.as_tensor(hs, device="cuda")
         errs[f"dW2[{e}]"] = rel_fro(to_np(dw2[e][fs_t][:, hs_t]), dW2_ref)
         # dW1[h, n] = sum_r X[r, h] dZ[r, n] for n = gate f and linear f; in MXFP8 dZ comes
-        # from bf16 Z and bf16 dA_s (oracle reading R10)
+        # from bf16 Z and bf16 dA_s (oracle reading R15)
         dA = p * _bf(_fq(dY, 1, mx) @ wq.w2_h[fs].T, mx)
         Zg, Zl = _bf(Zg, mx), (_bf(Zl, mx) if Zl is not None else None)
         if cfg.gated:

@@ -70,6 +70,11 @@ def parse():
                          "entry under 'workloads': 'auto' (every other configuration when the "
                          "headline is the default one), 'none', or a comma-separated list")
     ap.add_argument("--workload-steps", type=int, default=20)
+    ap.add_argument("--no-pdl-compare", dest="pdl_compare", action="store_false",
+                    help="skip timing the step with and without programmatic dependent launch")
+    ap.add_argument("--e2e-pdl", action="store_true",
+                    help="run the end-to-end pass with programmatic dependent launch (default: "
+                         "ordinary stream order, measured as fast or faster)")
     return ap.parse_args()
 
 
@@ -650,12 +655,40 @@ def measure(cfg, args, world, local, steps, warmup, with_e2e):
               "weight_quant_ms_in_step": sum(kernel_ms.get(k, 0.0) for k in WEIGHT_QUANT),
               "tflops_weights_reused": job_throughput(cfg.flops_fwd_bwd(), ms_reuse, world) / 1e12}
 
+    # the step without the per-launch timeline, in ordinary stream order and with
+    # programmatic dependent launch (each kernel's CTAs scheduled while the previous kernel's
+    # last CTAs finish); the timeline's event after every launch would serialise the launches
+    pdl = None
+    if args.pdl_compare:
+        k_p = max(5, steps // 2)
+        times = {}
+        for flag in (0, 1, 0, 1):
+            layer.desc.pdl = flag
+            step()
+            torch.cuda.synchronize()
+            barrier(world)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(k_p):
+                step()
+            e1.record()
+            torch.cuda.synchronize()
+            times.setdefault(flag, []).append(allreduce_max(e0.elapsed_time(e1) / k_p, world))
+        layer.desc.pdl = 0
+        assert layer.device_error() == 0, "device error in the launch-mode steps"
+        pdl = {"ms_per_step_stream_order": min(times[0]), "ms_per_step_pdl": min(times[1]),
+               "steps": k_p, "note": "no per-launch timeline; best of two runs each"}
+
     e2e = None
     if with_e2e:
+        layer.desc.pdl = 1 if args.e2e_pdl else 0
         e2e = measure_e2e(cfg, layer, hin, logits, x, dy, w1p, w2, fc1_bias, feat_scale, world,
                           steps)
+        e2e["pdl"] = bool(args.e2e_pdl)
+        layer.desc.pdl = 0
     res = {"cfg": cfg, "ms": ms, "ms_max": ms_max, "per": per, "kernel_ms": kernel_ms,
            "launches": int(launches), "timeline_events": n_rec, "clocks": clocks, "wq": wq,
+           "pdl": pdl,
            "e2e": e2e, "t_gen": t_gen, "ws_bytes": layer.ws_bytes, "hin": hin}
     del layer, w1p, w2, logits, x, dy
     torch.cuda.empty_cache()
@@ -777,6 +810,8 @@ def summarise(r, args, world, peaks, peak_src):
     }
     if r["wq"]:
         out["weight_quant"] = r["wq"]
+    if r["pdl"]:
+        out["launch_mode"] = r["pdl"]
     return out
 
 
@@ -880,6 +915,8 @@ def main():
         }
         if head.get("weight_quant"):
             line["weight_quant"] = head["weight_quant"]
+        if head.get("launch_mode"):
+            line["launch_mode"] = head["launch_mode"]
         if others:
             line["workloads"] = others
         print(json.dumps(line), flush=True)

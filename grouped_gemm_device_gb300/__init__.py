@@ -43,7 +43,8 @@ class LayerDesc(ctypes.Structure):
                 ("lin_hi", ctypes.c_float), ("lin_offset", ctypes.c_float),
                 ("sm_margin", ctypes.c_int32), ("ilv", ctypes.c_int32), ("align", ctypes.c_int32),
                 ("recompute", ctypes.c_int32), ("extras", ctypes.c_int32),
-                ("rht_mask", ctypes.c_uint32), ("reuse_weights", ctypes.c_int32)]
+                ("rht_mask", ctypes.c_uint32), ("reuse_weights", ctypes.c_int32),
+                ("pdl", ctypes.c_int32)]
 
 
 class WsLayout(ctypes.Structure):
@@ -138,13 +139,14 @@ def _stream(stream) -> int | None:
 def make_desc(E, k, H, F, T_max, precision="bf16", activation="swiglu", beta=1.0,
               gate_max=math.inf, lin_lo=-math.inf, lin_hi=math.inf, lin_offset=0.0,
               sm_margin=0, ilv=64, align=32, recompute=False, extras=0,
-              rht_mask=0, reuse_weights=False) -> LayerDesc:
+              rht_mask=0, reuse_weights=False, pdl=False) -> LayerDesc:
     """extras: bit 0 FC1 bias, bit 1 feature scale (EXTRA_BIAS | EXTRA_SCALE). rht_mask: the
     16 signs of the NVFP4 weight-gradient rotation (bit j set: row j of a block negated).
-    reuse_weights: the forward reuses the workspace's block-scaled weight copies."""
+    reuse_weights: the forward reuses the workspace's block-scaled weight copies. pdl: launch
+    the call's kernels with programmatic stream serialization."""
     return LayerDesc(E, k, H, F, T_max, PREC[precision], ACT[activation], beta, gate_max,
                      lin_lo, lin_hi, lin_offset, sm_margin, ilv, align, int(recompute),
-                     int(extras), int(rht_mask) & 0xFFFF, int(reuse_weights))
+                     int(extras), int(rht_mask) & 0xFFFF, int(reuse_weights), int(pdl))
 
 
 def desc_from_config(cfg, T_max=None, sm_margin=0, recompute=False, extras=0,

@@ -21,6 +21,17 @@ static int g_tl_cap = 0;
 static int g_tl_n = 0;
 static int g_tl_ids[4096];
 
+// programmatic dependent launch for the kernels of the current entry-point call
+static thread_local bool g_pdl = false;
+bool pdl_enabled() { return g_pdl; }
+namespace {
+struct PdlScope {
+  bool prev;
+  explicit PdlScope(const moe_layer_desc_t* d) : prev(g_pdl) { g_pdl = d && d->pdl == 1; }
+  ~PdlScope() { g_pdl = prev; }
+};
+}  // namespace
+
 void count_launch(cudaStream_t s, int kid) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (g_tl_events && g_tl_n < g_tl_cap) {
@@ -135,15 +146,18 @@ static moe_status_t validate_desc(const moe_layer_desc_t* d) {
   if (d->sm_margin < 0) return fail(MOE_ERR_INVALID_ARG, "sm_margin must be >= 0");
   if (d->recompute != 0 && d->recompute != 1)
     return fail(MOE_ERR_INVALID_ARG, "recompute must be 0 or 1");
-  if (d->recompute && (d->precision != MOE_PREC_BF16 || d->activation == MOE_ACT_SRELU))
-    return fail(MOE_ERR_UNSUPPORTED, "recompute needs a BF16 layer with a gated activation");
+  if (d->recompute && (d->precision == MOE_PREC_NVFP4 || d->activation == MOE_ACT_SRELU))
+    return fail(MOE_ERR_UNSUPPORTED,
+                "recompute needs a BF16 or MXFP8 layer with a gated activation");
   if (d->extras & ~3) return fail(MOE_ERR_INVALID_ARG, "extras has unknown bits");
   if (d->reuse_weights != 0 && d->reuse_weights != 1)
     return fail(MOE_ERR_INVALID_ARG, "reuse_weights must be 0 or 1");
-  if (d->extras && (d->precision != MOE_PREC_BF16 || d->activation == MOE_ACT_SRELU ||
+  if (d->pdl != 0 && d->pdl != 1) return fail(MOE_ERR_INVALID_ARG, "pdl must be 0 or 1");
+  if (d->extras && (d->precision == MOE_PREC_NVFP4 || d->activation == MOE_ACT_SRELU ||
                     d->recompute))
     return fail(MOE_ERR_UNSUPPORTED,
-                "epilogue extras need a BF16 layer with a gated activation, no recompute");
+                "epilogue extras need a BF16 or MXFP8 layer with a gated activation, no "
+                "recompute");
   if (r_cap(d) > (int64_t)INT32_MAX / 2) return fail(MOE_ERR_UNSUPPORTED, "row capacity too large");
   if (d->precision != MOE_PREC_BF16 &&
       (int64_t)d->E * round128(n1_of(d)) * d->H > (int64_t)INT32_MAX * 8)
@@ -236,7 +250,8 @@ static void compute_layout(const moe_layer_desc_t* d, moe_ws_layout_t* L) {
   const int64_t H = d->H, F = d->F, N1 = n1_of(d), E = d->E;
   const bool mx = d->precision == MOE_PREC_MXFP8;
   const bool nv = d->precision == MOE_PREC_NVFP4;
-  const int64_t nparts = mx ? dprob_parts_mx((int)F)
+  const int64_t nparts = mx ? (d->recompute ? dprob_parts_mx_recompute((int)F)
+                                            : dprob_parts_mx((int)F))
                          : nv ? dprob_parts_fp4((int)F)
                               : (d->recompute ? dprob_parts_recompute((int)F)
                                               : dprob_parts((int)F));
@@ -435,6 +450,7 @@ static void mx_quantize_operands(const void* in, int64_t M, int64_t N, int64_t G
 // arrival nobody makes; the wait gives up after limit_ns, records MOE_DEVERR_TIMEOUT and the
 // kernel returns normally.
 __global__ void selftest_wait_timeout_kernel(int* err, uint64_t limit_ns) {
+  MOE_GRIDDEP_ENTRY();
   __shared__ uint64_t bar;
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
@@ -469,6 +485,7 @@ moe_status_t moe_workspace_layout(const moe_layer_desc_t* desc, moe_ws_layout_t*
 moe_status_t moe_route_permute(const moe_layer_desc_t* d, int32_t T, const float* logits,
                                const void* x, int32_t* topk_ids, float* topk_probs,
                                int32_t* counts, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  PdlScope pdl_scope(d);
   moe_status_t st = validate_desc(d);
   if (st != MOE_OK) return st;
   if (T < 0 || T > d->T_max) return fail(MOE_ERR_INVALID_ARG, "T=%d outside [0, T_max]", T);
@@ -486,11 +503,11 @@ moe_status_t moe_route_permute(const moe_layer_desc_t* d, int32_t T, const float
   float* row_prob = w.at<float>(w.L.row_prob);
   int* err = w.at<int>(w.L.err);
   if (T > 0) {
-    route_topk_kernel<<<grid_for((T + 7) / 8, 8), 256, 0, s>>>(logits, T, d->E, d->k, topk_ids,
+    launch_kernel(route_topk_kernel, grid_for((T + 7) / 8, 8), 256, 0, s, nullptr, 0, logits, T, d->E, d->k, topk_ids,
                                                                  topk_probs, counts);
     count_launch(s, MOE_K_ROUTE_TOPK);
   }
-  assign_rows_kernel<<<d->E, 1024, 0, s>>>(topk_ids, topk_probs, counts, T, d->E, d->k, d->align,
+  launch_kernel(assign_rows_kernel, d->E, 1024, 0, s, nullptr, 0, topk_ids, topk_probs, counts, T, d->E, d->k, d->align,
                                            w.L.R_cap, offsets, row_of, src_of, row_prob, err);
   count_launch(s, MOE_K_ASSIGN_ROWS);
   if (d->precision == MOE_PREC_NVFP4) {
@@ -508,7 +525,7 @@ moe_status_t moe_route_permute(const moe_layer_desc_t* d, int32_t T, const float
     if (e != cudaSuccess) return cuda_fail(e, "route_permute launch");
     return MOE_OK;
   }
-  gather_rows_kernel<<<grid_for(w.L.R_cap, 8), 256, 0, s>>>(
+  launch_kernel(gather_rows_kernel, grid_for(w.L.R_cap, 8), 256, 0, s, nullptr, 0, 
       static_cast<const uint4*>(x), src_of, offsets, d->E, d->k, d->H / 8, w.L.R_cap,
       w.at<uint4>(w.L.x_perm));
   count_launch(s, MOE_K_GATHER_X);
@@ -526,6 +543,7 @@ moe_status_t moe_route_permute(const moe_layer_desc_t* d, int32_t T, const float
 static moe_status_t fwd_impl(const moe_layer_desc_t* d, int32_t T, const void* w1_packed,
                              const void* w2, const float* fc1_bias, const float* feat_scale,
                              void* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  PdlScope pdl_scope(d);
   moe_status_t st = validate_desc(d);
   if (st != MOE_OK) return st;
   if (((d->extras & 1) != 0) != (fc1_bias != nullptr) ||
@@ -547,15 +565,19 @@ static moe_status_t fwd_impl(const moe_layer_desc_t* d, int32_t T, const void* w
       mx_quantize_operands(w1_packed, (int64_t)d->E * m.N1, d->H, m.N1, m.N1p, m.w1, m.w1t, s);
       mx_quantize_operands(w2, (int64_t)d->E * d->F, d->H, d->F, m.Fp, m.w2, m.w2t, s);
     }
-    // FC1 + activation + probability scale + MXFP8 quantise/transpose (kernel family 2)
+    // FC1 + activation + probability scale + MXFP8 quantise/transpose (kernel family 2), with
+    // the optional bias and feature scale
     m.role = ROLE_FC1_FPROP;
-    m.out = w.at<void>(w.L.z);
+    m.out = d->recompute ? nullptr : w.at<void>(w.L.z);  // NULL: Z is not kept
+    m.fc1_bias = fc1_bias;
+    m.fscale = feat_scale;
     if ((e = launch_grouped_gemm_mx(m, s)) != cudaSuccess) return cuda_fail(e, "FC1 MX GEMM");
+    m.fc1_bias = m.fscale = nullptr;
     m.role = ROLE_FC2_FPROP;
     m.out = w.at<void>(w.L.y_perm);
     if ((e = launch_grouped_gemm_mx(m, s)) != cudaSuccess) return cuda_fail(e, "FC2 MX GEMM");
     if (T > 0) {
-      combine_rows_kernel<<<grid_for(T, 8), 256, 0, s>>>(w.at<uint4>(w.L.y_perm),
+      launch_kernel(combine_rows_kernel, grid_for(T, 8), 256, 0, s, nullptr, 0, w.at<uint4>(w.L.y_perm),
                                                         w.at<int32_t>(w.L.row_of), T, d->k,
                                                         d->H / 8, static_cast<uint4*>(y));
       count_launch(s, MOE_K_COMBINE_Y);
@@ -595,7 +617,7 @@ static moe_status_t fwd_impl(const moe_layer_desc_t* d, int32_t T, const void* w
     m.out2 = nullptr;
     if ((e = launch_grouped_gemm_fp4(m, s)) != cudaSuccess) return cuda_fail(e, "FC2 FP4 GEMM");
     if (T > 0) {
-      combine_rows_kernel<<<grid_for(T, 8), 256, 0, s>>>(w.at<uint4>(w.L.y_perm),
+      launch_kernel(combine_rows_kernel, grid_for(T, 8), 256, 0, s, nullptr, 0, w.at<uint4>(w.L.y_perm),
                                                         w.at<int32_t>(w.L.row_of), T, d->k,
                                                         d->H / 8, static_cast<uint4*>(y));
       count_launch(s, MOE_K_COMBINE_Y);
@@ -621,7 +643,7 @@ static moe_status_t fwd_impl(const moe_layer_desc_t* d, int32_t T, const void* w
   p.fc1_bias = p.fscale = nullptr;
   if ((e = launch_grouped_gemm(p, s)) != cudaSuccess) return cuda_fail(e, "FC2 grouped GEMM");
   if (T > 0) {
-    combine_rows_kernel<<<grid_for(T, 8), 256, 0, s>>>(w.at<uint4>(w.L.y_perm),
+    launch_kernel(combine_rows_kernel, grid_for(T, 8), 256, 0, s, nullptr, 0, w.at<uint4>(w.L.y_perm),
                                                       w.at<int32_t>(w.L.row_of), T, d->k,
                                                       d->H / 8, static_cast<uint4*>(y));
     count_launch(s, MOE_K_COMBINE_Y);
@@ -631,11 +653,31 @@ static moe_status_t fwd_impl(const moe_layer_desc_t* d, int32_t T, const void* w
   return MOE_OK;
 }
 
+// Per-expert sums of the dGLU epilogue's per-32-row column sums: the FC1 bias gradient (the
+// dZ columns, logical order) and the feature-scale gradient.
+static cudaError_t launch_extras_reduce(const moe_layer_desc_t* d, const Ws& w, float* d_fc1_bias,
+                                        float* d_feat_scale, cudaStream_t s) {
+  const int N1 = n1_of(d), ld = N1 + d->F;
+  const int32_t* off = w.at<int32_t>(w.L.offsets);
+  if (d_fc1_bias) {
+    launch_kernel(group_colsum_kernel, dim3((N1 + 255) / 256, d->E), 256, 0, s, nullptr, 0,
+                  w.at<float>(w.L.ext_part), ld, 0, N1, off, d_fc1_bias);
+    count_launch(s, MOE_K_EXTRAS_REDUCE);
+  }
+  if (d_feat_scale) {
+    launch_kernel(group_colsum_kernel, dim3((d->F + 255) / 256, d->E), 256, 0, s, nullptr, 0,
+                  w.at<float>(w.L.ext_part), ld, N1, d->F, off, d_feat_scale);
+    count_launch(s, MOE_K_EXTRAS_REDUCE);
+  }
+  return cudaGetLastError();
+}
+
 static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* dy,
                              const void* w1_packed, const void* w2, const float* feat_scale,
                              void* dx, void* dw1_packed, void* dw2, float* d_probs,
                              float* d_fc1_bias, float* d_feat_scale, void* ws, size_t ws_bytes,
                              moe_stream_t stream) {
+  PdlScope pdl_scope(d);
   moe_status_t st = validate_desc(d);
   if (st != MOE_OK) return st;
   if (((d->extras & 1) != 0) != (d_fc1_bias != nullptr) ||
@@ -666,7 +708,7 @@ static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* d
                             d->k, d->H, w.L.R_cap, d->rht_mask & 0xFFFFu, w.at<void>(w.L.dy_perm),
                             am + AM_DY, am + AM_DYT, device_sms(), MOE_K_GATHER_DY, s);
   } else {
-    gather_rows_kernel<<<grid_for(w.L.R_cap, 8), 256, 0, s>>>(
+    launch_kernel(gather_rows_kernel, grid_for(w.L.R_cap, 8), 256, 0, s, nullptr, 0, 
         static_cast<const uint4*>(dy), w.at<int32_t>(w.L.src_of), w.at<int32_t>(w.L.offsets),
         d->E, d->k, d->H / 8, w.L.R_cap, w.at<uint4>(w.L.dy_perm));
     count_launch(s, MOE_K_GATHER_DY);
@@ -678,12 +720,30 @@ static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* d
     // FC2 dgrad + dActivation + MXFP8 quantise/transpose of dZ (kernel family 3)
     m.role = ROLE_FC2_DGRAD;
     m.dprob_part = w.at<float>(w.L.dprob_part);
-    if ((e = launch_grouped_gemm_mx(m, s)) != cudaSuccess) return cuda_fail(e, "FC2 dgrad MX");
+    if (d->extras) {
+      m.fscale = feat_scale;
+      m.ext_part = w.at<float>(w.L.ext_part);
+    }
+    if (d->recompute) {
+      // the same kernel family with Z rebuilt from X and W1 next to dA_s
+      if ((e = launch_fc2_dgrad_recompute_mx(m, s)) != cudaSuccess)
+        return cuda_fail(e, "FC2 dgrad recompute MX");
+    } else if ((e = launch_grouped_gemm_mx(m, s)) != cudaSuccess) {
+      return cuda_fail(e, "FC2 dgrad MX");
+    }
+    m.fscale = nullptr;
+    m.ext_part = nullptr;
     if (T > 0) {
       const int n = T * d->k;
-      dprob_reduce_kernel<<<grid_for((n + 255) / 256, 4), 256, 0, s>>>(
-          w.at<float>(w.L.dprob_part), dprob_parts_mx(d->F), row_of, n, d_probs);
+      launch_kernel(dprob_reduce_kernel, grid_for((n + 255) / 256, 4), 256, 0, s, nullptr, 0,
+                    w.at<float>(w.L.dprob_part),
+                    d->recompute ? dprob_parts_mx_recompute(d->F) : dprob_parts_mx(d->F),
+                    row_of, n, d_probs);
       count_launch(s, MOE_K_DPROB_REDUCE);
+    }
+    if (d->extras) {
+      if ((e = launch_extras_reduce(d, w, d_fc1_bias, d_feat_scale, s)) != cudaSuccess)
+        return cuda_fail(e, "extras reduce");
     }
     m.role = ROLE_FC2_WGRAD;
     m.out = dw2;
@@ -692,7 +752,7 @@ static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* d
     m.out = w.at<void>(w.L.dx_perm);
     if ((e = launch_grouped_gemm_mx(m, s)) != cudaSuccess) return cuda_fail(e, "FC1 dgrad MX");
     if (T > 0) {
-      combine_rows_kernel<<<grid_for(T, 8), 256, 0, s>>>(w.at<uint4>(w.L.dx_perm), row_of, T,
+      launch_kernel(combine_rows_kernel, grid_for(T, 8), 256, 0, s, nullptr, 0, w.at<uint4>(w.L.dx_perm), row_of, T,
                                                         d->k, d->H / 8, static_cast<uint4*>(dx));
       count_launch(s, MOE_K_COMBINE_DX);
     }
@@ -715,7 +775,7 @@ static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* d
     if ((e = launch_grouped_gemm_fp4(m, s)) != cudaSuccess) return cuda_fail(e, "FC2 dgrad FP4");
     if (T > 0) {
       const int n = T * d->k;
-      dprob_reduce_kernel<<<grid_for((n + 255) / 256, 4), 256, 0, s>>>(
+      launch_kernel(dprob_reduce_kernel, grid_for((n + 255) / 256, 4), 256, 0, s, nullptr, 0, 
           w.at<float>(w.L.dprob_part), dprob_parts_fp4(d->F), row_of, n, d_probs);
       count_launch(s, MOE_K_DPROB_REDUCE);
     }
@@ -728,7 +788,7 @@ static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* d
     m.out = w.at<void>(w.L.dx_perm);
     if ((e = launch_grouped_gemm_fp4(m, s)) != cudaSuccess) return cuda_fail(e, "FC1 dgrad FP4");
     if (T > 0) {
-      combine_rows_kernel<<<grid_for(T, 8), 256, 0, s>>>(w.at<uint4>(w.L.dx_perm), row_of, T,
+      launch_kernel(combine_rows_kernel, grid_for(T, 8), 256, 0, s, nullptr, 0, w.at<uint4>(w.L.dx_perm), row_of, T,
                                                         d->k, d->H / 8, static_cast<uint4*>(dx));
       count_launch(s, MOE_K_COMBINE_DX);
     }
@@ -757,24 +817,13 @@ static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* d
   if (T > 0) {
     const int nparts = d->recompute ? dprob_parts_recompute(d->F) : dprob_parts(d->F);
     const int n = T * d->k;
-    dprob_reduce_kernel<<<grid_for((n + 255) / 256, 4), 256, 0, s>>>(
+    launch_kernel(dprob_reduce_kernel, grid_for((n + 255) / 256, 4), 256, 0, s, nullptr, 0, 
         w.at<float>(w.L.dprob_part), nparts, row_of, n, d_probs);
     count_launch(s, MOE_K_DPROB_REDUCE);
   }
   if (d->extras) {
-    // per-expert sums of the dGLU epilogue's per-32-row column sums
-    const int N1 = n1_of(d), ld = N1 + d->F;
-    const int32_t* off = w.at<int32_t>(w.L.offsets);
-    if (d_fc1_bias) {
-      group_colsum_kernel<<<dim3((N1 + 255) / 256, d->E), 256, 0, s>>>(
-          w.at<float>(w.L.ext_part), ld, 0, N1, off, d_fc1_bias);
-      count_launch(s, MOE_K_EXTRAS_REDUCE);
-    }
-    if (d_feat_scale) {
-      group_colsum_kernel<<<dim3((d->F + 255) / 256, d->E), 256, 0, s>>>(
-          w.at<float>(w.L.ext_part), ld, N1, d->F, off, d_feat_scale);
-      count_launch(s, MOE_K_EXTRAS_REDUCE);
-    }
+    if ((e = launch_extras_reduce(d, w, d_fc1_bias, d_feat_scale, s)) != cudaSuccess)
+      return cuda_fail(e, "extras reduce");
     p.fscale = nullptr;
     p.ext_part = nullptr;
   }
@@ -787,7 +836,7 @@ static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* d
   p.out = w.at<void>(w.L.dx_perm);
   if ((e = launch_grouped_gemm(p, s)) != cudaSuccess) return cuda_fail(e, "FC1 dgrad GEMM");
   if (T > 0) {
-    combine_rows_kernel<<<grid_for(T, 8), 256, 0, s>>>(w.at<uint4>(w.L.dx_perm), row_of, T,
+    launch_kernel(combine_rows_kernel, grid_for(T, 8), 256, 0, s, nullptr, 0, w.at<uint4>(w.L.dx_perm), row_of, T,
                                                       d->k, d->H / 8, static_cast<uint4*>(dx));
     count_launch(s, MOE_K_COMBINE_DX);
   }
@@ -837,7 +886,7 @@ moe_status_t moe_selftest_wait_timeout(int32_t* err, uint64_t limit_ns, moe_stre
   if (!err) return fail(MOE_ERR_INVALID_ARG, "err is NULL");
   if (limit_ns < 1000000ull || limit_ns > 10000000000ull)
     return fail(MOE_ERR_INVALID_ARG, "limit_ns must be in [1 ms, 10 s]");
-  selftest_wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err, limit_ns);
+  launch_kernel(selftest_wait_timeout_kernel, 1, 32, 0, reinterpret_cast<cudaStream_t>(stream), nullptr, 0, err, limit_ns);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
   return MOE_OK;
@@ -955,7 +1004,7 @@ moe_status_t moe_pack_fc1_weight(const void* src, void* dst, int32_t E, int32_t 
   const int N1 = gated ? 2 * F : F;
   const int64_t tiles = (int64_t)E * (N1 / 32) * (H / 32);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  pack_fc1_kernel<<<grid_for(tiles, 16), 256, 0, s>>>(static_cast<const uint16_t*>(src),
+  launch_kernel(pack_fc1_kernel, grid_for(tiles, 16), 256, 0, s, nullptr, 0, static_cast<const uint16_t*>(src),
                                                      static_cast<uint16_t*>(dst), E, H, F, N1,
                                                      gated ? 1 : 0, ilv, inverse ? 1 : 0);
   count_launch(s, MOE_K_PACK_FC1);

@@ -15,6 +15,20 @@
 
 namespace moe {
 
+// ----------------------------------------------------------------------------- PDL
+// Programmatic dependent launch: every kernel waits, before it touches memory, until the
+// previous kernel of the stream has completed and its memory is visible; the persistent GEMMs
+// let the stream's next kernel be scheduled once their tile loops are done (a grid's exiting
+// CTAs count as having let it, so the short kernels need no call). Triggering at kernel entry
+// instead was measured slower: the next kernel's waiting CTAs then share the SMs with this
+// kernel's work. Both are no-ops when the kernel was not launched with programmatic stream
+// serialization.
+MOE_DEVICE void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+MOE_DEVICE void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+#define MOE_GRIDDEP_ENTRY() griddep_wait()
+
 // ----------------------------------------------------------------------------- error word
 MOE_DEVICE void set_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);  // keep the first error

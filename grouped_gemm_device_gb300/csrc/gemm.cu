@@ -137,22 +137,6 @@ MOE_DEVICE void decode_tile(int tile, const GemmArgs& p, const Ctrl& c, int MT, 
   }
 }
 
-// Column sums over the warp's 32 rows: v[i] of every lane in, the sum of v[lane] out (a
-// butterfly that halves the values each lane keeps: 31 shuffles for 32 columns).
-MOE_DEVICE float warp_colsum32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) {
-    const bool hi = lane & w;
-#pragma unroll
-    for (int i = 0; i < w; ++i) {
-      const float send = hi ? v[i] : v[i + w];
-      const float keep = hi ? v[i + w] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, w);
-    }
-  }
-  return v[0];
-}
-
 // dGLU with the epilogue extras for one 16-column step: the feature scale s enters as
 // dA = p * s * dA_s and d_prob += dA_s * s * a; the step's column sums over the warp's rows of
 // dZ (bias gradient) and of p * dA_s * a (scale gradient) are stored to the row group's
@@ -236,6 +220,7 @@ template <int BN, int STAGES, bool A_MN, bool B_MN, int EPI, bool KG, bool B3D, 
           bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
+  MOE_GRIDDEP_ENTRY();
   using L = Smem<BN, STAGES, PAIR>;
   constexpr int TM = PAIR ? 2 * BM : BM;    // tile rows
   constexpr int BNH = PAIR ? BN / 2 : BN;   // B columns this CTA loads
@@ -629,6 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  griddep_launch_dependents();  // this CTA's tiles are done
   tc_fence_before();
   __syncthreads();
   // a pair: neither CTA leaves while the other may still read its shared memory (the
@@ -647,7 +633,7 @@ cudaError_t launch_instance(const GemmArgs& a, int grid, cudaStream_t s, int kid
   constexpr int smem = Smem<BN, STAGES>::TOTAL;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, s>>>(a);
+  launch_kernel(kern, grid, kThreads, smem, s, nullptr, 0, a);
   count_launch(s, kid);
   return cudaGetLastError();
 }
@@ -677,7 +663,7 @@ cudaError_t launch_pair_instance(const GemmArgs& a, int ctas, int64_t tiles, cud
   if (resident > 0) pairs = std::min(pairs, resident);
   pairs = (int)std::max<int64_t>(1, std::min<int64_t>(pairs, tiles));
   cfg.gridDim = dim3(2 * pairs, 1, 1);
-  e = cudaLaunchKernelEx(&cfg, kern, a);
+  e = launch_kernel(kern, cfg.gridDim, cfg.blockDim, cfg.dynamicSmemBytes, s, attr, 1, a);
   count_launch(s, kid);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -692,6 +678,11 @@ constexpr int kPairStages = 6;   // 32 KB per stage and CTA
 #define MOE_GEMM_PAIR 1
 #endif
 constexpr bool kUsePairs = MOE_GEMM_PAIR != 0;
+// weight gradients (k-grouped) on CTA pairs too; 0: one-CTA 128 x 256 tiles
+#ifndef MOE_WGRAD_PAIR
+#define MOE_WGRAD_PAIR 0
+#endif
+constexpr bool kWgradPairs = kUsePairs && MOE_WGRAD_PAIR != 0;
 
 }  // namespace
 
@@ -790,10 +781,15 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       a.out = p.out; a.ldo = H; a.out_estride = (int64_t)M * H;
       if (!ok) return cudaErrorInvalidValue;
       a.wide = aligned32(a.out) && a.ldo % 16 == 0 && a.out_estride % 16 == 0;
-      // weight gradients stay on one-CTA 128 x 256 tiles: measured faster than pairs here
-      const int64_t tiles = (int64_t)E * ((M + BM - 1) / BM) * ((H + kBN - 1) / kBN);
-      return launch_instance<kBN, kStages, true, true, EPI_STORE, true, false>(
-          a, (int)std::min<int64_t>(ctas, tiles), s, kid);
+      if constexpr (kWgradPairs) {
+        const int64_t tiles = (int64_t)E * ((M + 2 * BM - 1) / (2 * BM)) * ((H + kBN - 1) / kBN);
+        return launch_pair_instance<kBN, kPairStages, true, true, EPI_STORE, true, false>(
+            a, ctas, tiles, s, kid);
+      } else {
+        const int64_t tiles = (int64_t)E * ((M + BM - 1) / BM) * ((H + kBN - 1) / kBN);
+        return launch_instance<kBN, kStages, true, true, EPI_STORE, true, false>(
+            a, (int)std::min<int64_t>(ctas, tiles), s, kid);
+      }
     }
   }
 #undef MOE_LAUNCH

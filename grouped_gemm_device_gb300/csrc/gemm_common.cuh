@@ -128,6 +128,23 @@ MOE_DEVICE float glu_bwd16(const ActDev& a, float prob, const uint32_t (&das)[16
   if (a.kind == MOE_ACT_GEGLU) return glu_bwd16_k<MOE_ACT_GEGLU>(a, prob, das, gw, lw, dgw, dlw);
   return glu_bwd16_k<MOE_ACT_SWIGLU>(a, prob, das, gw, lw, dgw, dlw);
 }
+// Column sums over the warp's 32 rows: v[i] of every lane in, the sum of v[lane] out (a
+// butterfly that halves the values each lane keeps: 31 shuffles for 32 columns). v is
+// overwritten.
+MOE_DEVICE float warp_colsum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool hi = lane & w;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = hi ? v[i] : v[i + w];
+      const float keep = hi ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, w);
+    }
+  }
+  return v[0];
+}
+
 // 32 bytes at a 32-byte aligned global address, not allocated in L1.
 MOE_DEVICE void ld_v8_noalloc(const void* src, uint32_t (&w)[8]) {
   asm volatile("ld.global.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"

@@ -237,6 +237,7 @@ MOE_DEVICE int gate_col(int f) { return ((f & ~(ILV - 1)) << 1) | (f & (ILV - 1)
 
 template <int EPI, int KIND, bool KG>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __grid_constant__ Fp4Args p) {
+  MOE_GRIDDEP_ENTRY();
   constexpr bool kGated = KIND != MOE_ACT_SRELU;
   using L = Fp4Cfg<EPI>;
   constexpr int BN = L::BN;
@@ -632,6 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
     }
   }
 
+  griddep_launch_dependents();  // this CTA's tiles are done
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -653,7 +655,7 @@ cudaError_t launch_fp4(const Fp4Args& a, int grid, cudaStream_t s, int kid) {
   auto kern = grouped_gemm_fp4_kernel<EPI, KIND, KG>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), Fp4Cfg<EPI>::TOTAL);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, Fp4Cfg<EPI>::TOTAL, s>>>(a);
+  launch_kernel(kern, grid, kThreads, Fp4Cfg<EPI>::TOTAL, s, nullptr, 0, a);
   count_launch(s, kid);
   return cudaGetLastError();
 }

@@ -77,6 +77,14 @@ struct MxArgs {
   int nparts;
   int ilv;                             // gate/linear interleave of the packed columns
   int wide;                            // STORE: out is 32-byte aligned (256-bit stores)
+  // epilogue extras (EXT kernels): FC1 bias [E, N1] (logical [gate | linear] order) and
+  // feature scale [E, F], fp32, NULL when absent; the dGLU epilogue's per-32-row column sums
+  // of dZ (bias gradient) and of p * dA_s * a (scale gradient) go to ext_part
+  // [R_cap / 32, N1 + F]
+  const float* fc1_bias;
+  const float* fscale;
+  float* ext_part;
+  int F, N1;
   ActDev act;
   int* err;
 };
@@ -238,8 +246,12 @@ MOE_DEVICE int gate_col(int f, int ilv) { return ((f & ~(ilv - 1)) << 1) | (f & 
 // MMAs; MMA commits reach both CTAs by multicast; the follower's epilogue frees the
 // accumulator on the leader's barrier. Expert segments are 128-row aligned, so each CTA's
 // half of a tile lies wholly inside or wholly past its segment.
-template <int EPI, int KIND, bool KG, int ILV, bool A_MN, bool B_MN, bool PAIR = false>
+// EXT: the GLU / dGLU epilogues with the FC1 bias and feature-scale extras (a separate
+// instantiation, so the plain kernels carry none of its code or registers).
+template <int EPI, int KIND, bool KG, int ILV, bool A_MN, bool B_MN, bool PAIR = false,
+          bool EXT = false>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __grid_constant__ MxArgs p) {
+  MOE_GRIDDEP_ENTRY();
   constexpr bool kGated = KIND != MOE_ACT_SRELU;
   using L = MxSmem<EPI, PAIR>;
   constexpr int STAGES = L::STAGES;
@@ -534,11 +546,27 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
         }
         release_acc();
         ++acc_i;
+        if constexpr (EXT && kGated) {
+          // the bias joins Z before the activation (and is part of the saved Z); acc[c] holds
+          // packed column n0 + cb + c, whose logical column follows from the interleave
+          if (p.fc1_bias) {
+            const float* b = p.fc1_bias + (int64_t)t.e * p.N1;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+              const int pc = t.n0 + cb + c;
+              const int blk = pc / ILV;
+              const int lc = (blk >> 1) * ILV + pc % ILV + ((blk & 1) ? p.F : 0);
+              if (pc < p.N) acc[c] += b[lc];
+            }
+          }
+        }
         // segments are 128-row aligned, so every row of the tile is inside its segment
         uint16_t* zout = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo + t.n0 + cb;
+        if (p.out) {  // the saved Z (bf16); absent when the backward recomputes it
 #pragma unroll
-        for (int j = 0; j < 4; ++j)  // the saved Z (bf16)
-          if (t.n0 + cb + 32 * j < p.N) store_bf16x32_v8(zout + 32 * j, &acc[32 * j]);
+          for (int j = 0; j < 4; ++j)
+            if (t.n0 + cb + 32 * j < p.N) store_bf16x32_v8(zout + 32 * j, &acc[32 * j]);
+        }
         uint8_t* qr = p.q_row + (int64_t)row * p.ld_q_row;
         uint8_t* qc = p.q_col + (int64_t)row * p.ld_q_col;
         if constexpr (kGated) {
@@ -552,6 +580,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               v[i] = prob * act_fwd_k<KIND>(p.act, acc[g_off + i], acc[g_off + ILV + i]);
+            if constexpr (EXT) {
+              if (p.fscale) {
+                const float* sc = p.fscale + (int64_t)t.e * p.F + acol;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] *= sc[i];
+              }
+            }
             mx_row_block(v, qr + acol, p.s_row + sf_mma_offset(row, acol / 32, p.s_row_pad));
             mx_col_block(v, xs, qc + acol, p.s_col, acol, row0 / 32, p.s_col_pad, lane);
           }
@@ -634,6 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
           const int gcol = kGated ? gate_col(f0, p.ilv) : f0;
           const int lcol = gcol + p.ilv;
           float dg[32], dl[32];
+          float ts[EXT ? 32 : 1];  // extras: p * dA_s * a of this row, for the scale gradient
           // this lane's own pieces of the chunk (each lane reads only the row it copied)
           asm volatile("cp.async.wait_all;" ::: "memory");
 #pragma unroll
@@ -651,7 +687,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
               const float d = (k & 1) ? bf16_hi(cur[k >> 1]) : bf16_lo(cur[k >> 1]);
               const float g = (i & 1) ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
               float contrib;
-              if constexpr (kGated) {
+              if constexpr (EXT && kGated) {
+                // the feature scale s enters as dA = p * s * dA_s and d_prob += dA_s * s * a
+                const float l = (i & 1) ? bf16_hi(lw[i >> 1]) : bf16_lo(lw[i >> 1]);
+                const float sc = p.fscale ? p.fscale[(int64_t)t.e * p.F + f0 + k] : 1.f;
+                const float a = act_bwd_k<KIND>(p.act, g, l, prob * sc * d, dg[k], dl[k]);
+                contrib = d * sc * a;
+                ts[k] = prob * d * a;
+              } else if constexpr (kGated) {
                 const float l = (i & 1) ? bf16_hi(lw[i >> 1]) : bf16_lo(lw[i >> 1]);
                 contrib = d * act_bwd_k<KIND>(p.act, g, l, prob * d, dg[k], dl[k]);
               } else {
@@ -676,6 +719,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
           mx_col_block(dg, xs, qc + gcol, p.s_col, gcol, row0 / 32, p.s_col_pad, lane);
           if constexpr (kGated)
             mx_col_block(dl, xs, qc + lcol, p.s_col, lcol, row0 / 32, p.s_col_pad, lane);
+          if constexpr (EXT && kGated) {
+            // column sums over the warp's 32 rows (one expert's, segments being 128-row
+            // aligned) of dZ (bias gradient) and of p * dA_s * a (scale gradient), into the
+            // row group's partials: gate column f at f, linear at F + f, scale at N1 + f
+            float* part = p.ext_part + (int64_t)(row0 >> 5) * (p.N1 + p.F);
+            const float sg = warp_colsum32(dg, lane);
+            const float sl = warp_colsum32(dl, lane);
+            const float ss = warp_colsum32(ts, lane);
+            part[f0 + lane] = sg;
+            part[p.F + f0 + lane] = sl;
+            part[p.N1 + f0 + lane] = ss;
+          }
         }
         p.dprob_part[(int64_t)row * p.nparts + (t.n0 / BN) * 2 + half] = (dp0 + dp1) + (dp2 + dp3);
       }
@@ -683,6 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
     if constexpr (EPI == EPI_DGLU) asm volatile("cp.async.wait_all;" ::: "memory");
   }
 
+  griddep_launch_dependents();  // this CTA's tiles are done
   tc_fence_before();
   __syncthreads();
   // a pair: neither CTA leaves while the other may still read its shared memory (the
@@ -734,17 +790,17 @@ constexpr bool kMxPairs = MOE_GEMM_MX_PAIR != 0;
 
 // `grid`: the CTAs the caller allows (SM margin applied) or, for a pair kernel, twice the pairs
 // the tile count can use at most; pairs are further capped by how many fit at once.
-template <int EPI, int KIND, bool KG, int ILV, bool A_MN, bool B_MN>
+template <int EPI, int KIND, bool KG, int ILV, bool A_MN, bool B_MN, bool EXT = false>
 cudaError_t launch_mx(const MxArgs& a, int grid, cudaStream_t s, int kid) {
   if constexpr (!kMxPairs) {
-    auto kern = grouped_gemm_mx_kernel<EPI, KIND, KG, ILV, A_MN, B_MN>;
+    auto kern = grouped_gemm_mx_kernel<EPI, KIND, KG, ILV, A_MN, B_MN, false, EXT>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), MxSmem<EPI>::TOTAL);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, MxSmem<EPI>::TOTAL, s>>>(a);
+    launch_kernel(kern, grid, kThreads, MxSmem<EPI>::TOTAL, s, nullptr, 0, a);
     count_launch(s, kid);
     return cudaGetLastError();
   } else {
-    auto kern = grouped_gemm_mx_kernel<EPI, KIND, KG, ILV, A_MN, B_MN, true>;
+    auto kern = grouped_gemm_mx_kernel<EPI, KIND, KG, ILV, A_MN, B_MN, true, EXT>;
     constexpr int smem = MxSmem<EPI, true>::TOTAL;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
@@ -763,7 +819,7 @@ cudaError_t launch_mx(const MxArgs& a, int grid, cudaStream_t s, int kid) {
     const int resident = max_resident_pairs(reinterpret_cast<const void*>(kern), &cfg);
     if (resident > 0) pairs = std::min(pairs, resident);
     cfg.gridDim = dim3(2 * pairs, 1, 1);
-    e = cudaLaunchKernelEx(&cfg, kern, a);
+    e = launch_kernel(kern, cfg.gridDim, cfg.blockDim, cfg.dynamicSmemBytes, s, attr, 1, a);
     count_launch(s, kid);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -771,12 +827,21 @@ cudaError_t launch_mx(const MxArgs& a, int grid, cudaStream_t s, int kid) {
 }
 
 // GLU / dGLU kernels for one activation. The dGLU epilogue takes the interleave at run time;
-// the GLU epilogue indexes its registers with it, so it is compiled for 32 and 64.
+// the GLU epilogue indexes its registers with it, so it is compiled for 32 and 64. Layers with
+// epilogue extras (gated activations) take the EXT instantiations.
 template <int EPI, int KIND>
 cudaError_t launch_act(const MxArgs& a, int grid, cudaStream_t s, int kid) {
-  if constexpr (EPI == EPI_DGLU || KIND == MOE_ACT_SRELU) {
+  const bool ext = a.fc1_bias || a.fscale || a.ext_part;
+  if constexpr (KIND == MOE_ACT_SRELU) {
+    if (ext) return cudaErrorInvalidValue;
     return launch_mx<EPI, KIND, false, 64, false, false>(a, grid, s, kid);
+  } else if constexpr (EPI == EPI_DGLU) {
+    return ext ? launch_mx<EPI, KIND, false, 64, false, false, true>(a, grid, s, kid)
+               : launch_mx<EPI, KIND, false, 64, false, false>(a, grid, s, kid);
   } else {
+    if (ext)
+      return a.ilv == 32 ? launch_mx<EPI, KIND, false, 32, false, false, true>(a, grid, s, kid)
+                         : launch_mx<EPI, KIND, false, 64, false, false, true>(a, grid, s, kid);
     return a.ilv == 32 ? launch_mx<EPI, KIND, false, 32, false, false>(a, grid, s, kid)
                        : launch_mx<EPI, KIND, false, 64, false, false>(a, grid, s, kid);
   }
@@ -793,9 +858,360 @@ cudaError_t launch_glu_family(const MxArgs& a, int kind, int grid, cudaStream_t 
   }
 }
 
+
 }  // namespace
 
 int dprob_parts_mx(int F) { return 2 * ((F + BN - 1) / BN); }
+
+// ------------------------------------------------------------------------------------------
+// FC2 dgrad with the FC1 output recomputed (activation recomputation, [NV-blog] "What's
+// next"), MXFP8 operands. Per 128-row x 128-column tile of dA_s two block-scaled GEMMs share
+// one loop over H:
+//   dA_s[rows, f0..f0+127]      = Q(dY)[rows] . Q_H(W2)[f0..f0+127]^T        (128 x 128)
+//   Z[rows, 2f0 .. 2f0+255]     = Q(X)[rows]  . Q_H(W1p)[2f0 .. 2f0+255]^T   (128 x 256)
+// (the packed W1 rows 2f0.. are the gate and linear columns of dA_s columns f0.., the
+// interleave dividing 128). TMEM: dA_s in columns 0-127, Z in 128-383, the stages' scale
+// factors from 384 (20 columns a stage). A stage holds four 128-byte k-blocks (80 KB) and
+// their scale slabs; two stages. The dGLU epilogue reads dA_s and Z in fp32 straight from
+// TMEM and writes dZ as row-wise and column-wise MXFP8 plus the per-row d_prob partials, like
+// the saved-Z kernel's epilogue. One accumulator set: the next tile's MMAs start once every
+// epilogue warp has read this one.
+namespace {
+
+constexpr int RC_BNA = 128;                 // dA_s columns per tile
+constexpr int RC_BNZ = 256;                 // Z columns per tile
+constexpr int RC_STAGES = 2;
+constexpr int RC_A1 = BM * BK;              // dY k-block (16 KB)
+constexpr int RC_B1 = RC_BNA * BK;          // W2 rows
+constexpr int RC_A2 = BM * BK;              // X
+constexpr int RC_B2 = RC_BNZ * BK;          // W1p rows
+constexpr int RC_STAGE = RC_A1 + RC_B1 + RC_A2 + RC_B2;
+constexpr int RC_SF = 512 + 512 + 512 + 1024;  // scale slabs of the four k-blocks
+constexpr int RC_SF_OFF = RC_STAGES * RC_STAGE;
+constexpr int RC_XPOSE_OFF = RC_SF_OFF + RC_STAGES * RC_SF;
+constexpr int RC_CTRL_OFF = RC_XPOSE_OFF + kEpiWarps * XPOSE_WARP_BYTES;
+constexpr int RC_TOTAL = RC_CTRL_OFF + 4096 + 1024;
+constexpr int RC_ZCOL = RC_BNA;             // first TMEM column of Z
+constexpr int RC_SFCOL = RC_BNA + RC_BNZ;   // first TMEM column of the scale factors
+static_assert(RC_TOTAL <= 232448, "shared memory");
+static_assert(RC_SFCOL + 20 * RC_STAGES <= kTmemCols, "TMEM map");
+
+struct RcMxArgs {
+  CUtensorMap tmDy, tmW2, tmX, tmW1;  // row-wise MXFP8 copies, 128 x 128-byte boxes
+  const uint8_t *sf_dy, *sf_w2, *sf_x, *sf_w1;
+  int64_t pad_dy, pad_w2, pad_x, pad_w1;
+  const int32_t* offsets;
+  int E, R_cap, H, F, N1, Fp, N1p, ilv;
+  const float* row_prob;
+  uint8_t *q_row, *s_row, *q_col, *s_col;  // dZ copies, as the saved-Z dGLU writes them
+  int64_t s_row_pad, s_col_pad;
+  float* dprob_part;
+  int nparts;
+  ActDev act;
+  int* err;
+};
+
+struct RcCtrl {
+  uint64_t full[RC_STAGES];
+  uint64_t empty[RC_STAGES];
+  uint64_t tfull;
+  uint64_t tempty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int total_tiles;
+  int off[kMaxE + 1];
+  int prefix[kMaxE + 1];
+};
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    fc2_dgrad_recompute_mx_kernel(const __grid_constant__ RcMxArgs p) {
+  MOE_GRIDDEP_ENTRY();
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  RcCtrl& c = *reinterpret_cast<RcCtrl*>(smem + RC_CTRL_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort = &c.abort;
+  const int NT = (p.F + RC_BNA - 1) / RC_BNA;
+  const int nkb = (p.H + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RC_STAGES; ++s) {
+      mbar_init(&c.full[s], 1);
+      mbar_init(&c.empty[s], 1);
+    }
+    mbar_init(&c.tfull, 1);
+    mbar_init(&c.tempty, kEpiWarps);
+    mbar_init(&c.drain, 1);
+    fence_mbar_init();
+    c.abort = 0;
+    bool ok = p.E >= 1 && p.E <= kMaxE;
+    int prev = 0;
+    for (int e = 0; ok && e <= p.E; ++e) {
+      const int o = p.offsets[e];
+      if (o < prev || o > p.R_cap || (o & (BM - 1)) || (e == 0 && o != 0)) ok = false;
+      c.off[e] = o;
+      prev = o;
+    }
+    int total = 0;
+    if (ok) {
+      for (int e = 0; e < p.E; ++e) {
+        c.prefix[e] = total;
+        total += ((c.off[e + 1] - c.off[e]) / BM) * NT;
+      }
+      c.prefix[p.E] = total;
+    } else {
+      set_error(p.err, MOE_DEVERR_CAPACITY);
+    }
+    c.total_tiles = total;
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmDy);
+    tma_prefetch_desc(&p.tmW2);
+    tma_prefetch_desc(&p.tmX);
+    tma_prefetch_desc(&p.tmW1);
+  }
+  if (warp == 1) {
+    tmem_alloc(&c.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = c.tmem_base;
+  const int total = c.total_tiles;
+  // tile -> (expert, first row, first dA_s column)
+  auto decode = [&](int tile, int& e, int& m0, int& n0) {
+    int lo = 0, hi = p.E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (c.prefix[mid] <= tile) lo = mid; else hi = mid;
+    }
+    const int local = tile - c.prefix[lo];
+    const int mt = (c.off[lo + 1] - c.off[lo]) / BM;
+    e = lo;
+    m0 = c.off[lo] + (local % mt) * BM;
+    n0 = (local / mt) * RC_BNA;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed[RC_STAGES];
+#pragma unroll
+      for (int s = 0; s < RC_STAGES; ++s) armed[s] = -1;
+      for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+        int e, m0, n0;
+        decode(tile, e, m0, n0);
+        const int w2_row = e * p.Fp + n0, w1_row = e * p.N1p + 2 * n0;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&c.empty[stage], phase ^ 1, abort, p.err)) break;
+          uint8_t* s0 = smem + stage * RC_STAGE;
+          uint8_t* sf = smem + RC_SF_OFF + stage * RC_SF;
+          uint64_t* bar = &c.full[stage];
+          mbar_arrive_expect_tx(bar, RC_STAGE + RC_SF);
+#pragma unroll
+          for (int s = 0; s < RC_STAGES; ++s)
+            if (s == stage) armed[s] = (int)phase;
+          const int k0 = kb * BK;
+          tma_load_2d(s0, &p.tmDy, bar, k0, m0);
+          tma_load_2d(s0 + RC_A1, &p.tmW2, bar, k0, w2_row);
+          tma_load_2d(s0 + RC_A1 + RC_B1, &p.tmX, bar, k0, m0);
+          tma_load_2d(s0 + RC_A1 + RC_B1 + RC_A2, &p.tmW1, bar, k0, w1_row);
+          tma_load_2d(s0 + RC_A1 + RC_B1 + RC_A2 + 128 * BK, &p.tmW1, bar, k0, w1_row + 128);
+          const int64_t kg = kb;  // k-block index = group of four 32-element scale blocks
+          bulk_load(sf, p.sf_dy + (kg * p.pad_dy + m0) * 4, 512, bar);
+          bulk_load(sf + 512, p.sf_w2 + (kg * p.pad_w2 + w2_row) * 4, 512, bar);
+          bulk_load(sf + 1024, p.sf_x + (kg * p.pad_x + m0) * 4, 512, bar);
+          bulk_load(sf + 1536, p.sf_w1 + (kg * p.pad_w1 + w1_row) * 4, 1024, bar);
+          if (++stage == RC_STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < RC_STAGES; ++s) {
+        if (armed[s] >= 0) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(smem_u32(&c.full[s]), (uint32_t)armed[s]) &&
+                 globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ scale copies + MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc_i = 0;
+      bool issued_any = false;
+      for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+        if (!mbar_wait(&c.tempty, (acc_i & 1) ^ 1, abort, p.err)) break;
+        tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&c.full[stage], phase, abort, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t s0 = smem_u32(smem + stage * RC_STAGE);
+          const uint32_t sB1 = s0 + RC_A1, sA2 = sB1 + RC_B1, sB2 = sA2 + RC_A2;
+          const uint32_t sf = smem_u32(smem + RC_SF_OFF + stage * RC_SF);
+          const uint32_t t_sf = tmem_base + RC_SFCOL + stage * 20;
+          tmem_cp_32x128b_warpx4(t_sf, smem_desc_noswizzle(sf, 0, 128));              // dY
+          tmem_cp_32x128b_warpx4(t_sf + 4, smem_desc_noswizzle(sf + 512, 0, 128));    // W2
+          tmem_cp_32x128b_warpx4(t_sf + 8, smem_desc_noswizzle(sf + 1024, 0, 128));   // X
+          tmem_cp_32x128b_warpx4(t_sf + 12, smem_desc_noswizzle(sf + 1536, 0, 128));  // W1
+          tmem_cp_32x128b_warpx4(t_sf + 16, smem_desc_noswizzle(sf + 2048, 0, 128));
+          const int rem = p.H - kb * BK;
+          const int nsub = rem >= BK ? BK / MMA_K : (rem + MMA_K - 1) / MMA_K;
+          for (int ks = 0; ks < nsub; ++ks) {
+            const uint32_t acc = (kb | ks) != 0 ? 1u : 0u;
+            mma_mxf8_ss(tmem_base, smem_desc_sw128(s0 + ks * MMA_K, 16, 1024),
+                        smem_desc_sw128(sB1 + ks * MMA_K, 16, 1024),
+                        idesc_mxf8(BM, RC_BNA, ks), t_sf, t_sf + 4, acc);
+            mma_mxf8_ss(tmem_base + RC_ZCOL, smem_desc_sw128(sA2 + ks * MMA_K, 16, 1024),
+                        smem_desc_sw128(sB2 + ks * MMA_K, 16, 1024),
+                        idesc_mxf8(BM, RC_BNZ, ks), t_sf + 8, t_sf + 12, acc);
+          }
+          issued_any = true;
+          mma_commit(&c.empty[stage]);
+          if (++stage == RC_STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&c.tfull);
+        ++acc_i;
+      }
+      if (issued_any) {
+        mma_commit(&c.drain);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(&c.drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps 2..9
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;  // dA_s columns [64 * half, 64 * half + 64) of the tile
+    uint8_t* xs = smem + RC_XPOSE_OFF + (warp - 2) * XPOSE_WARP_BYTES;
+    int acc_i = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      if (__shfl_sync(0xFFFFFFFFu, *abort, 0)) break;
+      int e, m0, n0;
+      decode(tile, e, m0, n0);
+      const int row0 = m0 + q * 32;
+      const int row = row0 + lane;
+      const float prob = p.row_prob[row];  // segments are 128-row aligned: every row is inside
+      const bool got = mbar_wait(&c.tfull, acc_i & 1, abort, p.err);
+      if (!__all_sync(0xFFFFFFFFu, got)) break;
+      tc_fence_after();
+      const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
+      uint8_t* qr = p.q_row + (int64_t)row * p.N1;
+      uint8_t* qc = p.q_col + (int64_t)row * p.N1;
+      float dp = 0.f;
+#pragma unroll 1
+      for (int j = 0; j < 2; ++j) {
+        const int cc = half * 64 + 32 * j;  // dA_s column within the tile
+        if (n0 + cc >= p.F) break;
+        const int gc = (cc / p.ilv) * 2 * p.ilv + (cc % p.ilv);  // gate column within the 256
+        float dg[32], dl[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t da[16], g[16], l[16];
+          tmem_ld_32x32b_x16(tl + cc + 16 * h, da);
+          tmem_ld_32x32b_x16(tl + RC_ZCOL + gc + 16 * h, g);
+          tmem_ld_32x32b_x16(tl + RC_ZCOL + gc + p.ilv + 16 * h, l);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float d = __uint_as_float(da[i]);
+            const float a = act_bwd_k<KIND>(p.act, __uint_as_float(g[i]), __uint_as_float(l[i]),
+                                            prob * d, dg[16 * h + i], dl[16 * h + i]);
+            dp += d * a;
+          }
+        }
+        const int gcol = 2 * n0 + gc, lcol = gcol + p.ilv;  // packed dZ columns
+        mx_row_block(dg, qr + gcol, p.s_row + sf_mma_offset(row, gcol / 32, p.s_row_pad));
+        mx_row_block(dl, qr + lcol, p.s_row + sf_mma_offset(row, lcol / 32, p.s_row_pad));
+        mx_col_block(dg, xs, qc + gcol, p.s_col, gcol, row0 / 32, p.s_col_pad, lane);
+        mx_col_block(dl, xs, qc + lcol, p.s_col, lcol, row0 / 32, p.s_col_pad, lane);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.tempty);
+      ++acc_i;
+      p.dprob_part[(int64_t)row * p.nparts + (n0 / RC_BNA) * 2 + half] = dp;
+    }
+  }
+
+  griddep_launch_dependents();  // this CTA's tiles are done
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int KIND>
+cudaError_t launch_rc_mx(const RcMxArgs& a, int grid, cudaStream_t s) {
+  auto kern = fc2_dgrad_recompute_mx_kernel<KIND>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), RC_TOTAL);
+  if (e != cudaSuccess) return e;
+  launch_kernel(kern, grid, kThreads, RC_TOTAL, s, nullptr, 0, a);
+  count_launch(s, MOE_K_GEMM_FC2_DGRAD);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int dprob_parts_mx_recompute(int F) { return 2 * ((F + RC_BNA - 1) / RC_BNA); }
+
+cudaError_t launch_fc2_dgrad_recompute_mx(const MxProblem& p, cudaStream_t s) {
+  if (!p.gated || (p.ilv != 32 && p.ilv != 64)) return cudaErrorInvalidValue;
+  RcMxArgs a;
+  memset(&a, 0, sizeof(a));
+  if (!tmap_fp8(&a.tmDy, p.dy, false) || !tmap_fp8(&a.tmW2, p.w2, false) ||
+      !tmap_fp8(&a.tmX, p.x, false) || !tmap_fp8(&a.tmW1, p.w1, false))
+    return cudaErrorInvalidValue;
+  a.sf_dy = p.dy.s; a.pad_dy = p.dy.s_pad;
+  a.sf_w2 = p.w2.s; a.pad_w2 = p.w2.s_pad;
+  a.sf_x = p.x.s; a.pad_x = p.x.s_pad;
+  a.sf_w1 = p.w1.s; a.pad_w1 = p.w1.s_pad;
+  a.offsets = p.offsets;
+  a.E = p.E;
+  a.R_cap = (int)p.R_cap;
+  a.H = p.H;
+  a.F = p.F;
+  a.N1 = p.N1;
+  a.Fp = p.Fp;
+  a.N1p = p.N1p;
+  a.ilv = p.ilv;
+  a.row_prob = p.row_prob;
+  a.q_row = p.dz.q; a.s_row = p.dz.s; a.s_row_pad = p.dz.s_pad;
+  a.q_col = p.dzt.q; a.s_col = p.dzt.s; a.s_col_pad = p.dzt.s_pad;
+  a.dprob_part = p.dprob_part;
+  a.nparts = dprob_parts_mx_recompute(p.F);
+  a.act = p.act;
+  a.err = p.err;
+  const int grid = std::max(1, p.num_ctas);
+  switch (p.act.kind) {
+    case MOE_ACT_SWIGLU: return launch_rc_mx<MOE_ACT_SWIGLU>(a, grid, s);
+    case MOE_ACT_CLAMPED_SWIGLU: return launch_rc_mx<MOE_ACT_CLAMPED_SWIGLU>(a, grid, s);
+    case MOE_ACT_GEGLU: return launch_rc_mx<MOE_ACT_GEGLU>(a, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s) {
   static const int kKid[6] = {MOE_K_GEMM_FC1_FPROP, MOE_K_GEMM_FC2_FPROP, MOE_K_GEMM_FC2_DGRAD,
@@ -812,6 +1228,15 @@ cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s) {
   a.act = p.act;
   a.err = p.err;
   a.row_prob = p.row_prob;
+  a.F = p.F;
+  a.N1 = p.N1;
+  if (p.role == ROLE_FC1_FPROP) {
+    a.fc1_bias = p.fc1_bias;
+    a.fscale = p.fscale;
+  } else if (p.role == ROLE_FC2_DGRAD) {
+    a.fscale = p.fscale;
+    a.ext_part = p.ext_part;
+  }
   const int H = p.H, F = p.F, N1 = p.N1;
   const MxOperand *A = nullptr, *B = nullptr;
   int grid = p.num_ctas;

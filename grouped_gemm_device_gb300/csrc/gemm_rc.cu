@@ -121,6 +121,7 @@ MOE_DEVICE float dglu16(const ActDev& a, float prob, const uint32_t (&da)[16],
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     fc2_dgrad_recompute_kernel(const __grid_constant__ RcArgs p) {
+  MOE_GRIDDEP_ENTRY();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -307,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  griddep_launch_dependents();  // this CTA's tiles are done
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -320,7 +322,7 @@ cudaError_t launch_kind(const RcArgs& a, int grid, cudaStream_t s) {
   auto kern = fc2_dgrad_recompute_kernel<KIND>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), SMEM_TOTAL);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, SMEM_TOTAL, s>>>(a);
+  launch_kernel(kern, grid, kThreads, SMEM_TOTAL, s, nullptr, 0, a);
   count_launch(s, MOE_K_GEMM_FC2_DGRAD);
   return cudaGetLastError();
 }

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <algorithm>
+#include <utility>
 
 #include "common.cuh"
 
@@ -9,6 +10,32 @@ namespace moe {
 
 // launch accounting and the optional event timeline (api.cu); kid is a moe_kernel_id_t
 void count_launch(cudaStream_t s, int kid);
+
+// Whether the kernels the current entry-point call enqueues are launched with programmatic
+// stream serialization (desc->pdl; thread-local, set for the duration of the call by api.cu).
+bool pdl_enabled();
+// Launch `k` like <<<grid, block, smem, s>>>, with programmatic stream serialization when the
+// current call asked for it (extra_attrs: further launch attributes, e.g. a cluster shape).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          const cudaLaunchAttribute* extra_attrs, int n_extra, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[4];
+  int n = 0;
+  for (int i = 0; i < n_extra && n < 3; ++i) attrs[n++] = extra_attrs[i];
+  if (pdl_enabled()) {
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
+}
 // set the message returned by moe_last_error_string for this thread (api.cu)
 void set_last_error(const char* msg);
 
@@ -128,6 +155,12 @@ struct MxProblem {
   const void* z;             // bf16 [R_cap, N1] saved FC1 output
   void* out;                 // bf16 role output (z for FC1, y_perm, dx_perm, dW2, dW1)
   float* dprob_part;
+  // epilogue extras (gated layers; NULL when absent): FC1 bias [E, N1] in logical [gate |
+  // linear] order and feature scale [E, F], fp32; per-32-row column sums of dZ and of
+  // p * dA_s * a written by the dGLU epilogue into ext_part [R_cap / 32, N1 + F]
+  const float* fc1_bias;
+  const float* fscale;
+  float* ext_part;
   int gated, ilv;
   ActDev act;
   int* err;
@@ -136,6 +169,9 @@ struct MxProblem {
 
 int dprob_parts_mx(int F);
 cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s);
+// FC2 dgrad that recomputes the FC1 output next to dA_s (MXFP8 operands, gated activations)
+int dprob_parts_mx_recompute(int F);
+cudaError_t launch_fc2_dgrad_recompute_mx(const MxProblem& p, cudaStream_t s);
 
 // nvfp4.cu --------------------------------------------------------------------------------
 // NVFP4 quantiser arguments: in bf16 [G-row groups of the input, N]; output rows M = groups *

@@ -102,6 +102,7 @@ MOE_DEVICE void store_run32(uint8_t* dst, const uint32_t (&q)[8], bool wide) {
 }
 
 __global__ void __launch_bounds__(QT_THREADS, 2) mxfp8_quantize_kernel(const MxQuantArgs a) {
+  MOE_GRIDDEP_ENTRY();
   extern __shared__ __align__(16) uint8_t qsmem[];
   auto tiles = reinterpret_cast<uint16_t (*)[QT_ROWS][QT_LD]>(qsmem);
   float* cinv = reinterpret_cast<float*>(qsmem + QT_INV_OFF);
@@ -227,7 +228,7 @@ static void launch(MxQuantArgs a, int num_sms, cudaStream_t s) {
   // on failure the launch below fails too and the caller reports the CUDA error
   ensure_smem_attr(reinterpret_cast<const void*>(mxfp8_quantize_kernel), QT_SMEM);
   const int grid = (int)std::min<int64_t>(tiles, (int64_t)num_sms * 2);
-  mxfp8_quantize_kernel<<<grid, QT_THREADS, QT_SMEM, s>>>(a);
+  launch_kernel(mxfp8_quantize_kernel, grid, QT_THREADS, QT_SMEM, s, nullptr, 0, a);
   count_launch(s, MOE_K_MXFP8_QUANTIZE);
 }
 
@@ -246,6 +247,7 @@ constexpr int QG_THREADS = 128;
 __global__ void __launch_bounds__(QG_THREADS) mxfp8_colwise_grouped_kernel(
     const uint16_t* __restrict__ in, int64_t M, int64_t N, const int32_t* __restrict__ off,
     int G, int64_t nb, uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+  MOE_GRIDDEP_ENTRY();
   __shared__ int64_t s_rb[4], s_re[4];
   const int64_t col_items = (N + 2 * QG_THREADS - 1) / (2 * QG_THREADS);
   const int64_t items = (nb / 4) * col_items;
@@ -309,7 +311,7 @@ void launch_mxfp8_colwise_grouped(const void* in, int64_t M, int64_t N, const in
   const int64_t items = (nb / 4) * ((N + 2 * QG_THREADS - 1) / (2 * QG_THREADS));
   if (items == 0) return;
   const int grid = (int)std::min<int64_t>(items, (int64_t)num_sms * 8);
-  mxfp8_colwise_grouped_kernel<<<grid, QG_THREADS, 0, s>>>(
+  launch_kernel(mxfp8_colwise_grouped_kernel, grid, QG_THREADS, 0, s, nullptr, 0, 
       static_cast<const uint16_t*>(in), M, N, offsets, G, nb, q_col, s_col);
   count_launch(s, MOE_K_MXFP8_QUANTIZE);
 }

@@ -157,14 +157,14 @@ extern "C" moe_status_t moe_route_permute_noalloc(const moe_layer_desc_t* d, int
   }
   if (T > 0) {
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((T + 7) / 8, (int64_t)sms * 8));
-    route_topk_kernel<<<grid, 256, 0, s>>>(logits, T, d->E, d->k, topk_ids, topk_probs, counts);
+    launch_kernel(route_topk_kernel, grid, 256, 0, s, nullptr, 0, logits, T, d->E, d->k, topk_ids, topk_probs, counts);
     count_launch(s, MOE_K_ROUTE_TOPK);
   }
-  assign_rows_kernel<<<d->E, 1024, 0, s>>>(topk_ids, topk_probs, counts, T, d->E, d->k, d->align,
+  launch_kernel(assign_rows_kernel, d->E, 1024, 0, s, nullptr, 0, topk_ids, topk_probs, counts, T, d->E, d->k, d->align,
                                            R_cap, offsets, row_of, src_of, row_prob, err);
   count_launch(s, MOE_K_ASSIGN_ROWS);
   const int ggrid = (int)std::max<int64_t>(1, std::min<int64_t>(R_cap, (int64_t)sms * 8));
-  gather_rows_kernel<<<ggrid, 256, 0, s>>>(static_cast<const uint4*>(x), src_of, offsets, d->E,
+  launch_kernel(gather_rows_kernel, ggrid, 256, 0, s, nullptr, 0, static_cast<const uint4*>(x), src_of, offsets, d->E,
                                            d->k, d->H / 8, R_cap, static_cast<uint4*>(x_perm));
   count_launch(s, MOE_K_GATHER_X);
   e = cudaGetLastError();

@@ -50,6 +50,7 @@ MOE_DEVICE void stage_tile(const Nvfp4QuantArgs& p, const uint16_t* in, int64_t 
 }
 
 __global__ void __launch_bounds__(QT_THREADS, 6) nvfp4_quantize_kernel(const Nvfp4QuantArgs p) {
+  MOE_GRIDDEP_ENTRY();
   // two tile buffers: the next tile streams in while this one is quantised
   __shared__ __align__(16) uint8_t tiles[2][QT_ROWS * QT_LD];
   __shared__ float enc_row[128], enc_col[128];
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(QT_THREADS, 6) nvfp4_quantize_kernel(const Nvf
 
 // Plain amax of n bf16 values (n a multiple of 8, 16-byte aligned).
 __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const uint4* in, int64_t n8, float* out) {
+  MOE_GRIDDEP_ENTRY();
   float m = 0.f;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -153,6 +155,7 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const uint4* in, int64_
 __global__ void __launch_bounds__(256) nvfp4_rht_amax_kernel(const uint16_t* in, int64_t M,
                                                              int64_t N, uint32_t mask,
                                                              float* out, float* out_rht) {
+  MOE_GRIDDEP_ENTRY();
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t c = blockIdx.y * 128 + 4 * lane;
   const int64_t r0 = blockIdx.x * 128 + w * 16;
@@ -191,6 +194,7 @@ __global__ void __launch_bounds__(256) gather_rows_amax_kernel(const uint4* __re
                                                                uint32_t mask,
                                                                uint4* __restrict__ out,
                                                                float* amax, float* amax_rht) {
+  MOE_GRIDDEP_ENTRY();
   __shared__ int64_t src_row[16];
   const int used = offsets[E];
   float m = 0.f, mr = 0.f;
@@ -240,7 +244,7 @@ void launch_gather_rows_amax(const void* x, const int32_t* src_of, const int32_t
   const int64_t blocks = R_cap / 16;
   if (blocks <= 0) return;
   const int grid = (int)std::min<int64_t>(blocks, (int64_t)std::max(num_sms, 1) * 8);
-  gather_rows_amax_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(x), src_of, offsets, E,
+  launch_kernel(gather_rows_amax_kernel, grid, 256, 0, s, nullptr, 0, static_cast<const uint4*>(x), src_of, offsets, E,
                                                k, H / 8, R_cap, mask, static_cast<uint4*>(out),
                                                amax, amax_rht);
   count_launch(s, kid);
@@ -262,7 +266,7 @@ void launch_nvfp4_quantize(const Nvfp4QuantArgs& a, int num_sms, cudaStream_t s)
   if (tiles <= 0) return;
   // 36 KB of tile buffers a CTA: six CTAs per SM
   const int grid = (int)std::min<int64_t>(tiles, (int64_t)std::max(num_sms, 1) * 6);
-  nvfp4_quantize_kernel<<<grid, QT_THREADS, 0, s>>>(a);
+  launch_kernel(nvfp4_quantize_kernel, grid, QT_THREADS, 0, s, nullptr, 0, a);
   count_launch(s, MOE_K_NVFP4_QUANTIZE);
 }
 
@@ -270,7 +274,7 @@ void launch_nvfp4_amax(const void* in, int64_t n, float* out, int num_sms, cudaS
   const int64_t n8 = n / 8;
   if (n8 <= 0) return;
   const int grid = (int)std::min<int64_t>((n8 + 255) / 256, (int64_t)std::max(num_sms, 1) * 8);
-  nvfp4_amax_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(in), n8, out);
+  launch_kernel(nvfp4_amax_kernel, grid, 256, 0, s, nullptr, 0, static_cast<const uint4*>(in), n8, out);
   count_launch(s, MOE_K_NVFP4_AMAX);
 }
 
@@ -278,7 +282,7 @@ void launch_nvfp4_rht_amax(const void* in, int64_t M, int64_t N, uint32_t mask, 
                            float* out_rht, cudaStream_t s) {
   if (M <= 0 || N <= 0) return;
   const dim3 grid((unsigned)((M + 127) / 128), (unsigned)((N + 127) / 128));
-  nvfp4_rht_amax_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(in), M, N, mask, out,
+  launch_kernel(nvfp4_rht_amax_kernel, grid, 256, 0, s, nullptr, 0, static_cast<const uint16_t*>(in), M, N, mask, out,
                                              out_rht);
   count_launch(s, MOE_K_NVFP4_AMAX);
 }

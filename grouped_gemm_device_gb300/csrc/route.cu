@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
                                                          int E, int k, int32_t* __restrict__ ids,
                                                          float* __restrict__ probs,
                                                          int32_t* __restrict__ counts) {
+  MOE_GRIDDEP_ENTRY();
   __shared__ int hist[256];
   for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(1024) assign_rows_kernel(
     const int32_t* __restrict__ counts, int T, int E, int k, int align, int64_t R_cap,
     int32_t* __restrict__ offsets, int32_t* __restrict__ row_of, int32_t* __restrict__ src_of,
     float* __restrict__ row_prob, int* err) {
+  MOE_GRIDDEP_ENTRY();
   __shared__ int s_off[257];
   __shared__ int s_warp[32];
   __shared__ int s_base;
@@ -192,6 +194,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           const int32_t* __restrict__ offsets,
                                                           int E, int k, int H8, int64_t R_cap,
                                                           uint4* __restrict__ out) {
+  MOE_GRIDDEP_ENTRY();
   const int used = offsets[E];
   for (int64_t r = blockIdx.x; r < R_cap; r += gridDim.x) {
     int src = r < used ? src_of[r] : -1;
@@ -210,6 +213,7 @@ __global__ void __launch_bounds__(256) combine_rows_kernel(const uint4* __restri
                                                            const int32_t* __restrict__ row_of,
                                                            int T, int k, int H8,
                                                            uint4* __restrict__ out) {
+  MOE_GRIDDEP_ENTRY();
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     int rows[8];
     for (int j = 0; j < k; ++j) rows[j] = row_of[(size_t)t * k + j];
@@ -238,6 +242,7 @@ __global__ void __launch_bounds__(256) combine_rows_kernel(const uint4* __restri
 __global__ void dprob_reduce_kernel(const float* __restrict__ part, int nparts,
                                     const int32_t* __restrict__ row_of, int n,
                                     float* __restrict__ d_probs) {
+  MOE_GRIDDEP_ENTRY();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
     const float* p = part + (int64_t)row_of[i] * nparts;
     float s = 0.f;
@@ -254,6 +259,7 @@ __global__ void __launch_bounds__(256) pack_fc1_kernel(const uint16_t* __restric
                                                        uint16_t* __restrict__ dst, int E, int H,
                                                        int F, int N1, int gated, int ilv,
                                                        int inverse) {
+  MOE_GRIDDEP_ENTRY();
   __shared__ uint16_t tile[32][33];
   const int tiles_p = N1 / 32, tiles_h = H / 32;
   const int64_t per_e = (int64_t)tiles_p * tiles_h;
@@ -294,6 +300,7 @@ __global__ void __launch_bounds__(256) group_colsum_kernel(const float* __restri
                                                            int ld, int col0, int ncols,
                                                            const int32_t* __restrict__ offsets,
                                                            float* __restrict__ out) {
+  MOE_GRIDDEP_ENTRY();
   const int e = blockIdx.y;
   const int c = blockIdx.x * 256 + threadIdx.x;
   if (c >= ncols) return;

@@ -104,11 +104,11 @@ typedef struct {
                          (MXFP8, NVFP4: segments start on 128-row scale slabs)            */
   int32_t recompute;  /* 1: keep no FC1 output between forward and backward; the FC2-dgrad
                          kernel recomputes it ([NV-blog] "What's next": activation
-                         recomputation). BF16 gated activations only; 0 otherwise          */
+                         recomputation). BF16 or MXFP8 with a gated activation; 0 otherwise */
   int32_t extras;     /* epilogue extras ([NV-blog] GLU-epilogue section: bias-vector addition
                          and feature scaling): bit 0 FC1 bias, bit 1 per-feature scale of the
-                         activation output; used through the _ex entry points. BF16 gated,
-                         without recompute; 0 otherwise                                      */
+                         activation output; used through the _ex entry points. BF16 or MXFP8
+                         with a gated activation, without recompute; 0 otherwise            */
   uint32_t rht_mask;  /* NVFP4: signs of the 16-point random Hadamard rotation applied along
                          the tokens to the weight-gradient operands (bit j set: the j-th row
                          of each 16-row block is negated before H16 / 4); drawn once by the
@@ -121,6 +121,11 @@ typedef struct {
                          weights quantised before the low-precision GEMMs). The caller
                          guarantees the weights did not change since. 0 = quantise (always
                          correct). Ignored by BF16 layers                                    */
+  int32_t pdl;        /* 1: every kernel the call enqueues is launched with programmatic stream
+                         serialization (programmatic dependent launch), so that a kernel's CTAs
+                         are scheduled while the previous kernel's last CTAs finish and only its
+                         data reads wait for that kernel; 0: ordinary stream order. Results
+                         are the same either way                                              */
 } moe_layer_desc_t;
 
 /* Byte offsets (from ws) of the intermediates that live in the workspace, for inspection
@@ -221,7 +226,10 @@ moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t *desc, int32_t T, const 
  *   d_fc1_bias   fp32 [E, N1] out (bit 0; NULL otherwise)
  *   d_feat_scale fp32 [E, F]  out (bit 1; NULL otherwise)
  * Other arguments as moe_grouped_mlp_fwd / moe_grouped_mlp_bwd, which return
- * MOE_ERR_UNSUPPORTED for a layer with extras. The backward needs no bias (Z includes it). */
+ * MOE_ERR_UNSUPPORTED for a layer with extras. The backward needs no bias (Z includes it).
+ * BF16 and MXFP8 layers with a gated activation; in MXFP8 the scaled activation is what the
+ * FC1 epilogue quantises, and the dGLU epilogue takes the two column sums before dZ's
+ * quantisation, from the fp32 values. */
 moe_status_t moe_grouped_mlp_fwd_ex(const moe_layer_desc_t *desc, int32_t T,
                                     const void *w1_packed, const void *w2,
                                     const float *fc1_bias, const float *feat_scale, void *y,

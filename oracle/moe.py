@@ -26,7 +26,8 @@ Readings of the pages (where they are silent or ambiguous), used consistently be
   R9 d_prob[t, j] = sum_f dA_s * a (a unscaled); d_logits is not part of the layer.
   R15 MXFP8 backward: dZ, whose E4M3 codes are integer decisions the pages give no precision
      for, is formed from the fused dGLU epilogue's inputs in the precision the epilogue reads
-     them: the saved FC1 output in bf16 and dA_s rounded to bf16.
+     them: the saved FC1 output in bf16 and dA_s rounded to bf16 (with activation
+     recomputation: both in fp32, so unrounded).
 """
 from __future__ import annotations
 
@@ -234,7 +235,8 @@ def expert_forward(X, W1, W2, p, act: ActParams, mx: bool, wq: ExpertWeights | N
 
 
 def expert_backward(X, W1, W2, p, Z, a, a_s, dY, act: ActParams, mx: bool,
-                    wq: ExpertWeights | None = None, s=None, extras: dict | None = None):
+                    wq: ExpertWeights | None = None, s=None, extras: dict | None = None,
+                    recompute: bool = False):
     """One expert's share of the backward ([NV-blog] Figure 1: FC2 dgrad + dActivation +
     quantise fused; the weight-gradient GEMMs unfused).
 
@@ -248,14 +250,16 @@ def expert_backward(X, W1, W2, p, Z, a, a_s, dY, act: ActParams, mx: bool,
     MXFP8, R15: the E4M3 codes of dZ are integer decisions taken on the values the fused dGLU
     epilogue reads, so the oracle forms dZ from the same inputs: the saved FC1 output in bf16
     (the saved activation is bf16) and the FC2-dgrad result dA_s rounded to bf16 (the
-    precision in which the epilogue holds it); d_prob keeps the plain definition.
+    precision in which the epilogue holds it); d_prob keeps the plain definition. With
+    `recompute` (activation recomputation: the epilogue reads Z and dA_s in fp32 from the
+    tensor-core accumulators) dZ is formed from the unrounded values.
     """
     wq = wq or ExpertWeights(W1, W2, mx)
     F = W2.shape[0]
     dA_s = _q(dY, 1, mx) @ wq.w2_h.T
     sa = a * s[None, :] if s is not None else a
     d_prob = (dA_s * sa).sum(axis=1)
-    dA_in, Z_in = (bf16_round(dA_s), bf16_round(Z)) if mx else (dA_s, Z)
+    dA_in, Z_in = (bf16_round(dA_s), bf16_round(Z)) if mx and not recompute else (dA_s, Z)
     dA = p[:, None] * (dA_in * s[None, :] if s is not None else dA_in)
     if act.gated:
         dg, dl = act_backward(act, Z_in[:, :F], Z_in[:, F:], dA)
@@ -291,7 +295,7 @@ class LayerResult:
 
 def layer(logits, x, W1, W2, k: int, act: ActParams, mx: bool = False, align: int = 32,
           dy=None, keep_intermediates: bool = False, experts=None, b1=None,
-          s=None) -> LayerResult:
+          s=None, recompute: bool = False) -> LayerResult:
     """Forward (and, when dy is given, backward) of the MoE expert layer.
 
     logits fp32 [T,E]; x fp64 [T,H]; W1 fp64 [E,H,N1] (or a callable e -> [H,N1]);
@@ -331,7 +335,8 @@ def layer(logits, x, W1, W2, k: int, act: ActParams, mx: bool = False, align: in
             dY = dy[tok]
             ex = {}
             dZ, dX, dW1, dW2, d_prob = expert_backward(X, W1e, W2e, p, Z, a, a_s, dY, act, mx,
-                                                       wq, s=se, extras=ex)
+                                                       wq, s=se, extras=ex,
+                                                       recompute=recompute)
             if b1 is not None:
                 res.db1[e] = ex["db1"]
             if s is not None:

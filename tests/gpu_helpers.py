@@ -47,12 +47,12 @@ class Inputs:
         self.w2 = synth.gen_w2(cfg)
         self.dy = synth.gen_dy(cfg)
 
-    def oracle(self, backward=True, keep=True):
+    def oracle(self, backward=True, keep=True, recompute=False):
         c = self.cfg
         return om.layer(self.logits, om.bf16_to_f64(self.x), om.bf16_to_f64(self.w1),
                         om.bf16_to_f64(self.w2), c.k, act_params(c), mx=c.precision == "mxfp8",
                         align=c.align, dy=om.bf16_to_f64(self.dy) if backward else None,
-                        keep_intermediates=keep)
+                        keep_intermediates=keep, recompute=recompute)
 
 
 class LayerRun:

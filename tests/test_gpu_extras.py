@@ -1,7 +1,8 @@
 """GPU parity of the epilogue extras (an FC1 bias added before the activation and a
 per-feature scale of the activation output, with their gradients) against the fp64 oracle,
-through moe_grouped_mlp_fwd_ex / moe_grouped_mlp_bwd_ex. Bar: relative Frobenius error <= 5e-3
-per output tensor, as for the plain BF16 layer."""
+through moe_grouped_mlp_fwd_ex / moe_grouped_mlp_bwd_ex, for BF16 and MXFP8 layers. Bar:
+relative Frobenius error <= 5e-3 (BF16) / 3e-2 (MXFP8) per output tensor, as for the plain
+layers."""
 import numpy as np
 import pytest
 import torch
@@ -10,7 +11,7 @@ import grouped_gemm_device_gb300 as g
 from grouped_gemm_device_gb300 import synth
 from oracle import moe as om
 
-from .gpu_helpers import BF16_TOL, Inputs, act_params, bf16_dev, rel_fro, to_np
+from .gpu_helpers import BF16_TOL, MX_TOL, Inputs, act_params, bf16_dev, rel_fro, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -26,14 +27,30 @@ CASES = {
     "geglu": synth.LayerConfig("xge", T=500, E=4, k=2, H=256, F=512, seed=65,
                                activation="geglu", ilv=128),
 }
+MX = dict(precision="mxfp8", align=128)
+MX_CASES = {
+    "mx_multi_tile": synth.LayerConfig("xmm", T=700, E=4, k=2, H=256, F=384, seed=66, **MX),
+    # ilv 32, F and N1 not multiples of 256
+    "mx_tails": synth.LayerConfig("xmt", T=500, E=3, k=2, H=320, F=192, seed=67, ilv=32, **MX),
+    # many experts, 25 of 64 empty
+    "mx_skewed": synth.LayerConfig("xms", T=300, E=64, k=4, H=256, F=256, seed=68, zipf_s=1.1,
+                                   **MX),
+    "mx_clamped": synth.LayerConfig("xmc", T=500, E=8, k=4, H=384, F=320, seed=69,
+                                    activation="clamped_swiglu", beta=1.702, gate_max=7.0,
+                                    lin_lo=-7.0, lin_hi=7.0, lin_offset=1.0, **MX),
+    "mx_geglu": synth.LayerConfig("xmg", T=300, E=4, k=2, H=256, F=256, seed=70,
+                                  activation="geglu", **MX),
+}
 
 
 def run_extras(cfg, extras):
     inp = Inputs(cfg)
     b1 = synth.gen_fc1_bias(cfg) if extras & g.EXTRA_BIAS else None
     sc = synth.gen_feat_scale(cfg) if extras & g.EXTRA_SCALE else None
+    mx = cfg.precision == "mxfp8"
+    tol = MX_TOL if mx else BF16_TOL
     ref = om.layer(inp.logits, om.bf16_to_f64(inp.x), om.bf16_to_f64(inp.w1),
-                   om.bf16_to_f64(inp.w2), cfg.k, act_params(cfg), align=cfg.align,
+                   om.bf16_to_f64(inp.w2), cfg.k, act_params(cfg), mx=mx, align=cfg.align,
                    dy=om.bf16_to_f64(inp.dy),
                    b1=None if b1 is None else b1.astype(np.float64),
                    s=None if sc is None else sc.astype(np.float64))
@@ -62,7 +79,7 @@ def run_extras(cfg, extras):
         errs["d_fc1_bias"] = rel_fro(layer.d_fc1_bias.cpu().numpy(), ref.db1)
     if sc is not None:
         errs["d_feat_scale"] = rel_fro(layer.d_feat_scale.cpu().numpy(), ref.ds)
-    bad = {k: v for k, v in errs.items() if not v <= BF16_TOL}
+    bad = {k: v for k, v in errs.items() if not v <= tol}
     assert not bad, (bad, max(errs.values()))
     return layer, ref
 
@@ -77,8 +94,20 @@ def test_each_extra_alone_matches_oracle(lib, extras):
     run_extras(CASES["tails"], extras)
 
 
-def test_empty_expert_extras_gradients_are_zero(lib):
-    layer, ref = run_extras(CASES["skewed"], g.EXTRA_BIAS | g.EXTRA_SCALE)
+@pytest.mark.parametrize("name", list(MX_CASES))
+def test_mx_bias_and_feature_scale_match_oracle(lib, name):
+    run_extras(MX_CASES[name], g.EXTRA_BIAS | g.EXTRA_SCALE)
+
+
+@pytest.mark.parametrize("extras", [g.EXTRA_BIAS, g.EXTRA_SCALE])
+def test_mx_each_extra_alone_matches_oracle(lib, extras):
+    run_extras(MX_CASES["mx_tails"], extras)
+
+
+@pytest.mark.parametrize("cfg", [CASES["skewed"], MX_CASES["mx_skewed"]],
+                         ids=["bf16", "mxfp8"])
+def test_empty_expert_extras_gradients_are_zero(lib, cfg):
+    layer, ref = run_extras(cfg, g.EXTRA_BIAS | g.EXTRA_SCALE)
     empty = np.nonzero(ref.perm.counts == 0)[0]
     assert len(empty) > 0
     assert np.all(layer.d_fc1_bias.cpu().numpy()[empty] == 0)

@@ -53,7 +53,7 @@ def test_desc_struct_layout_matches_header(lib, tmp_path):
                    check=True)
     desc, ws, reuse = map(int, subprocess.run([str(exe)], capture_output=True, text=True,
                                               check=True).stdout.split())
-    assert ctypes.sizeof(g.LayerDesc) == desc == 19 * 4
+    assert ctypes.sizeof(g.LayerDesc) == desc == 20 * 4
     assert g.LayerDesc.reuse_weights.offset == reuse
     assert ctypes.sizeof(g.WsLayout) == ws == 19 * 8
 
@@ -95,10 +95,12 @@ def test_recompute_keeps_no_z_in_the_workspace(lib):
     (dict(H=100), 2), (dict(F=96), 2), (dict(align=16), 2), (dict(ilv=48), 2),
     (dict(F=64 * 3, ilv=128), 2), (dict(sm_margin=-1), 1),
     (dict(precision="mxfp8"), 2), (dict(precision="mxfp8", align=128, ilv=128), 2),
-    (dict(recompute=2), 1), (dict(recompute=1, precision="mxfp8", align=128), 2),
+    (dict(recompute=2), 1),
+    (dict(recompute=1, precision="mxfp8", align=128, activation="srelu"), 2),
     (dict(recompute=1, activation="srelu"), 2),
     (dict(extras=4), 1), (dict(extras=1, activation="srelu"), 2),
-    (dict(extras=3, precision="mxfp8", align=128), 2), (dict(extras=1, recompute=1), 2),
+    (dict(extras=3, precision="mxfp8", align=128, activation="srelu"), 2),
+    (dict(extras=1, recompute=1), 2),
     (dict(precision="nvfp4"), 2), (dict(precision="nvfp4", align=128, ilv=32), 2),
     (dict(precision="nvfp4", align=128, recompute=1), 2),
     (dict(precision="nvfp4", align=128, extras=1), 2),

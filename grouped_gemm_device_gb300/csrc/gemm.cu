@@ -678,9 +678,10 @@ constexpr int kPairStages = 6;   // 32 KB per stage and CTA
 #define MOE_GEMM_PAIR 1
 #endif
 constexpr bool kUsePairs = MOE_GEMM_PAIR != 0;
-// weight gradients (k-grouped) on CTA pairs too; 0: one-CTA 128 x 256 tiles
+// weight gradients (k-grouped) on CTA pairs too (same-box A/B: FC1 wgrad 2.79 -> 2.67 ms on
+// the Mixtral BF16 layer, 2.09 -> 1.96 on GPT-OSS); 0: one-CTA 128 x 256 tiles
 #ifndef MOE_WGRAD_PAIR
-#define MOE_WGRAD_PAIR 0
+#define MOE_WGRAD_PAIR 1
 #endif
 constexpr bool kWgradPairs = kUsePairs && MOE_WGRAD_PAIR != 0;
 
@@ -748,7 +749,8 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       return MOE_LAUNCH(false, true, EPI_STORE, false, true, false, any_tiles);
     case ROLE_FC2_DGRAD:
       ok &= tmap_2d(&a.tmA, p.dy_perm, H, R, 64, BM);
-      ok &= tmap_3d(&a.tmB, p.w2, H, F, E, 64, kBN);
+      ok &= tmap_3d(&a.tmB, p.w2, H, F, E, 64,
+                    (kUsePairs && p.rows_per_expert >= 1024) ? kBRows : kBN);
       a.K = H; a.N = F;
       a.out = p.out; a.ldo = N1;
       a.z = static_cast<const uint16_t*>(p.z); a.ldz = N1;
@@ -756,8 +758,14 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
       if (!ok) return cudaErrorInvalidValue;
       a.wide = aligned32(a.out) && aligned32(a.out2) && a.ldo % 16 == 0 && a.ldo2 % 16 == 0 &&
                a.out_estride % 16 == 0;
-      // the dGLU epilogue sets this kernel's pace: one-CTA tiles (measured as fast or faster,
-      // and no pair tile past a short segment's end)
+      // pairs pay for up to 255 rows past each expert's segment end, and this kernel's dGLU
+      // epilogue makes those rows expensive: pairs only when the experts average at least 1024
+      // rows (measured: Mixtral-shaped, ~2048 rows, 1.40 -> 1.34 ms on pairs; GPT-OSS-shaped,
+      // ~512 rows, 0.98 -> 1.03 ms)
+      if (kUsePairs && p.rows_per_expert >= 1024) {
+        if (a.ext_part) return MOE_LAUNCH(false, false, EPI_DGLU, false, true, true, any_tiles);
+        return MOE_LAUNCH(false, false, EPI_DGLU, false, true, false, any_tiles);
+      }
       if (a.ext_part)
         return launch_instance<kBN, kStages, false, false, EPI_DGLU, false, true, true>(a, ctas, s,
                                                                                        kid);

@@ -125,6 +125,7 @@ struct GemmProblem {
   ActDev act;
   int* err;
   int num_ctas;            // persistent grid size (SMs - margin)
+  int64_t rows_per_expert; // T_max * k / E: the routed rows an expert averages at capacity
 };
 
 int gemm_bn(int role);

@@ -26,6 +26,8 @@ CASES = {
                                  lin_lo=-7.0, lin_hi=7.0, lin_offset=1.0),
     "geglu": synth.LayerConfig("xge", T=500, E=4, k=2, H=256, F=512, seed=65,
                                activation="geglu", ilv=128),
+    # >= 1024 routed rows per expert: the dGLU epilogue with the extras on CTA pairs
+    "large_experts": synth.LayerConfig("xlg", T=2100, E=2, k=1, H=256, F=384, seed=71),
 }
 MX = dict(precision="mxfp8", align=128)
 MX_CASES = {

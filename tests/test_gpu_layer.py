@@ -27,6 +27,8 @@ CASES = {
                                ilv=128),
     "srelu": synth.LayerConfig("sr", T=500, E=4, k=2, H=256, F=384, seed=36, activation="srelu"),
     "single_expert": synth.LayerConfig("one", T=300, E=1, k=1, H=256, F=256, seed=37),
+    # >= 1024 routed rows per expert at capacity: the FC2-dgrad + dGLU kernel runs on CTA pairs
+    "large_experts": synth.LayerConfig("lg", T=2100, E=2, k=1, H=256, F=512, seed=38),
 }
 
 

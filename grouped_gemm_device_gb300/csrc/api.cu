@@ -381,6 +381,7 @@ static MxProblem mx_problem(const moe_layer_desc_t* d, const Ws& w) {
   p.act = act_of(d);
   p.err = w.at<int>(w.L.err);
   p.num_ctas = gemm_ctas(d);
+  p.rows_per_expert = (int64_t)d->T_max * d->k / d->E;
   return p;
 }
 

@@ -182,6 +182,25 @@ MOE_DEVICE void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int 
       : "memory");
 }
 
+// TMA store of a shared-memory box to a 3-D tensor (out-of-bounds elements are not written),
+// tracked in the issuing thread's bulk-async group.
+MOE_DEVICE void tma_store_3d(const CUtensorMap* m, const void* src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+MOE_DEVICE void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until this thread's bulk stores have read their shared-memory sources (reuse is safe).
+MOE_DEVICE void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until this thread's bulk stores have completed.
+MOE_DEVICE void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Make this thread's shared-memory writes visible to the async (TMA) proxy.
+MOE_DEVICE void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------------- tcgen05
 // Allocation is warp-wide (.sync.aligned); the TMEM base address is written to smem.
 MOE_DEVICE void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {

@@ -46,6 +46,8 @@ enum { EPI_STORE = 0, EPI_GLU = 1, EPI_DGLU = 2 };
 struct MxArgs {
   CUtensorMap tmA;
   CUtensorMap tmB;
+  // TST kernels: the weight-gradient output [E][M][N] bf16, box 64 x 32 x 1, 128B swizzle
+  CUtensorMap tmOut;
   // pair kernels: the scale buffers as [bytes / 16, 16] uint8 tensors, so that a CTA's scale
   // slabs are TMA loads that can complete on the pair leader's barrier
   CUtensorMap tmSFA;
@@ -96,20 +98,24 @@ constexpr int SFB_BYTES = 1024;  // 256 rows x 4 k-blocks
 constexpr int XP_ROW = 80;  // bytes per row of the per-warp 32 x 32 bf16 staging tile (+16 pad)
 constexpr int XPOSE_WARP_BYTES = 32 * XP_ROW + 32 * 4;  // staging tile + 32 column 2^-e
 constexpr int ZST_WARP_BYTES = 32 * 128;  // dGLU: saved Z of one chunk, 32 rows x 64 bf16
+constexpr int TST_WARP_BYTES = 32 * 128;  // TMA-store staging: 32 rows x 64 bf16, 128B swizzle
 
 // Shared-memory map of one kernel: four pipeline stages, except for the dGLU kernel, whose Z
 // buffer takes the fourth stage's space. STORE kernels have no quantisation staging tiles.
 // PAIR: a CTA of a pair holds half of the B tile (and all of its scale factors), so more
 // stages fit: 6 (STORE), 5 (GLU, dGLU).
-template <int EPI, bool PAIR = false>
+// TST: the weight-gradient STORE epilogue writes through shared memory and TMA stores (a
+// 32 x 64-column bf16 box a warp at a time), which takes one stage's room.
+template <int EPI, bool PAIR = false, bool TST = false>
 struct MxSmem {
-  static constexpr int STAGES = PAIR ? (EPI == 0 ? 6 : 5) : (EPI == 2 ? 3 : 4);
+  static constexpr int STAGES = TST ? 3 : PAIR ? (EPI == 0 ? 6 : 5) : (EPI == 2 ? 3 : 4);
   static constexpr int STAGE_BYTES_ = A_BYTES + (PAIR ? B_BYTES / 2 : B_BYTES);
   static constexpr int DATA = STAGES * STAGE_BYTES_;
   static constexpr int SF_OFF = DATA;
   static constexpr int XPOSE_OFF = SF_OFF + STAGES * (SFA_BYTES + SFB_BYTES);
   static constexpr int ZST_OFF = XPOSE_OFF + (EPI == 0 ? 0 : kEpiWarps * XPOSE_WARP_BYTES);
-  static constexpr int CTRL_OFF = ZST_OFF + (EPI == 2 ? kEpiWarps * ZST_WARP_BYTES : 0);
+  static constexpr int TST_OFF = (ZST_OFF + (EPI == 2 ? kEpiWarps * ZST_WARP_BYTES : 0) + 1023) / 1024 * 1024;
+  static constexpr int CTRL_OFF = TST_OFF + (TST ? kEpiWarps * TST_WARP_BYTES : 0);
   static constexpr int TOTAL = CTRL_OFF + 4096 + 1024;
   static_assert(TOTAL <= 232448, "shared memory above the sm_100 per-block limit");
   static_assert(XPOSE_OFF % 16 == 0 && ZST_OFF % 128 == 0 && CTRL_OFF % 8 == 0, "alignment");
@@ -248,12 +254,18 @@ MOE_DEVICE int gate_col(int f, int ilv) { return ((f & ~(ilv - 1)) << 1) | (f & 
 // half of a tile lies wholly inside or wholly past its segment.
 // EXT: the GLU / dGLU epilogues with the FC1 bias and feature-scale extras (a separate
 // instantiation, so the plain kernels carry none of its code or registers).
+//
+// TST (k-grouped STORE only): the weight gradients of experts with few rows are bound by the
+// epilogue's stores (per-lane row stores fill the load/store queue), so this variant writes
+// each warp's 32 x 64-column bf16 chunk to shared memory (128-byte swizzle, conflict-free) and
+// sends it with one TMA store; an expert without rows stores zeros the same way.
 template <int EPI, int KIND, bool KG, int ILV, bool A_MN, bool B_MN, bool PAIR = false,
-          bool EXT = false>
+          bool EXT = false, bool TST = false>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __grid_constant__ MxArgs p) {
   MOE_GRIDDEP_ENTRY();
   constexpr bool kGated = KIND != MOE_ACT_SRELU;
-  using L = MxSmem<EPI, PAIR>;
+  static_assert(!TST || (EPI == EPI_STORE && KG && !PAIR), "TMA stores: weight gradients");
+  using L = MxSmem<EPI, PAIR, TST>;
   constexpr int STAGES = L::STAGES;
   constexpr int SBYTES = L::STAGE_BYTES_;
   constexpr int TM = PAIR ? 2 * BM : BM;
@@ -502,6 +514,53 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
       const int row = row0 + lane;
       const bool row_ok = row < t.row_end;
       const int cb = half * 128;       // first tile column of this warp
+      if constexpr (TST) {
+        // 128 columns of the warp's 32 rows as packed bf16 (zeros for an expert without rows)
+        uint32_t pk[64];
+        if (t.nkb == 0) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) pk[i] = 0u;
+        } else {
+          const bool got = mbar_wait(&c.tfull, acc_i & 1, abort, p.err);
+          if (!__all_sync(0xFFFFFFFFu, got)) break;
+          tc_fence_after();
+          const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + cb;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tacc + 32 * j, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[16 * j + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          }
+          release_acc();
+          ++acc_i;
+        }
+        // two 32 x 64-column boxes: row `lane` of the box is 128 bytes, its 16-byte piece c at
+        // piece c ^ (lane % 8) (the 128-byte swizzle), which keeps the shared stores free of
+        // bank conflicts; rows past M and columns past N are clipped by the TMA store
+        uint8_t* buf = smem + L::TST_OFF + (warp - 2) * TST_WARP_BYTES;
+#pragma unroll
+        for (int j2 = 0; j2 < 2; ++j2) {
+          const int x = t.n0 + cb + 64 * j2;
+          if (x >= p.N) break;
+          if (lane == 0) bulk_wait_read0();  // the previous box has left the buffer
+          __syncwarp();
+#pragma unroll
+          for (int cpc = 0; cpc < 8; ++cpc)
+            *reinterpret_cast<uint4*>(buf + lane * 128 + ((cpc ^ (lane & 7)) << 4)) =
+                make_uint4(pk[32 * j2 + 4 * cpc], pk[32 * j2 + 4 * cpc + 1],
+                           pk[32 * j2 + 4 * cpc + 2], pk[32 * j2 + 4 * cpc + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&p.tmOut, buf, x, row0, t.e);
+            bulk_commit();
+          }
+        }
+        continue;
+      }
       if (t.nkb == 0) {
         if (row_ok) {
           uint16_t* o = static_cast<uint16_t*>(p.out) + (int64_t)t.e * p.out_estride +
@@ -736,6 +795,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
       }
     }
     if constexpr (EPI == EPI_DGLU) asm volatile("cp.async.wait_all;" ::: "memory");
+    if constexpr (TST) {
+      if (lane == 0) bulk_wait0();  // every box this warp stored has landed
+      __syncwarp();
+    }
   }
 
   griddep_launch_dependents();  // this CTA's tiles are done
@@ -790,13 +853,15 @@ constexpr bool kMxPairs = MOE_GEMM_MX_PAIR != 0;
 
 // `grid`: the CTAs the caller allows (SM margin applied) or, for a pair kernel, twice the pairs
 // the tile count can use at most; pairs are further capped by how many fit at once.
-template <int EPI, int KIND, bool KG, int ILV, bool A_MN, bool B_MN, bool EXT = false>
+template <int EPI, int KIND, bool KG, int ILV, bool A_MN, bool B_MN, bool EXT = false,
+          bool TST = false>
 cudaError_t launch_mx(const MxArgs& a, int grid, cudaStream_t s, int kid) {
-  if constexpr (!kMxPairs) {
-    auto kern = grouped_gemm_mx_kernel<EPI, KIND, KG, ILV, A_MN, B_MN, false, EXT>;
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), MxSmem<EPI>::TOTAL);
+  if constexpr (!kMxPairs || TST) {
+    auto kern = grouped_gemm_mx_kernel<EPI, KIND, KG, ILV, A_MN, B_MN, false, EXT, TST>;
+    constexpr int smem = MxSmem<EPI, false, TST>::TOTAL;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    launch_kernel(kern, grid, kThreads, MxSmem<EPI>::TOTAL, s, nullptr, 0, a);
+    launch_kernel(kern, grid, kThreads, smem, s, nullptr, 0, a);
     count_launch(s, kid);
     return cudaGetLastError();
   } else {
@@ -1294,6 +1359,18 @@ cudaError_t launch_grouped_gemm_mx(const MxProblem& p, cudaStream_t s) {
     case ROLE_FC1_DGRAD:
       return launch_mx<EPI_STORE, 0, false, 64, false, true>(a, grid, s, kid);
     default: {
+      // experts with few rows: the weight-gradient tiles are short and their stores dominate,
+      // so they go out through shared memory and TMA stores
+      if (!kMxPairs && p.rows_per_expert <= 256) {
+        uint64_t dims[3] = {(uint64_t)a.N, (uint64_t)a.M, (uint64_t)p.E};
+        uint64_t strides[2] = {(uint64_t)a.N * 2, (uint64_t)a.M * a.N * 2};
+        uint32_t box[3] = {64, 32, 1};
+        if (!make_tmap(&a.tmOut, a.out, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+          return cudaErrorInvalidValue;
+        const int64_t tiles = (int64_t)p.E * ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
+        grid = (int)std::min<int64_t>(grid, tiles);
+        return launch_mx<EPI_STORE, 0, true, 64, true, true, false, true>(a, grid, s, kid);
+      }
       constexpr int TMr = kMxPairs ? 2 * BM : BM;
       const int64_t tiles = (int64_t)p.E * ((a.M + TMr - 1) / TMr) * ((a.N + BN - 1) / BN);
       grid = (int)std::min<int64_t>(grid, kMxPairs ? 2 * tiles : tiles);

@@ -166,6 +166,7 @@ struct MxProblem {
   ActDev act;
   int* err;
   int num_ctas;
+  int64_t rows_per_expert;   // T_max * k / E: the routed rows an expert averages at capacity
 };
 
 int dprob_parts_mx(int F);

@@ -415,7 +415,7 @@ static Fp4Problem fp4_problem(const moe_layer_desc_t* d, const Ws& w) {
 // NVFP4 copies of a bf16 matrix [M, N] (input row groups G stored at stride Gp; rows at or
 // beyond *row_limit zero when given): the row-wise copy `row` with the encode scale of
 // amax[row_slot] and the transposed copy `col` with that of amax[col_slot], rotated when rht.
-static void nv_quantize(const void* in, int64_t M, int64_t N, int64_t G, int64_t Gp,
+static bool nv_quantize(const void* in, int64_t M, int64_t N, int64_t G, int64_t Gp,
                         const int32_t* row_limit, const Fp4Problem& p, int row_slot,
                         int col_slot, const MxOperand& row, const MxOperand& col, int rht,
                         cudaStream_t s) {
@@ -437,7 +437,8 @@ static void nv_quantize(const void* in, int64_t M, int64_t N, int64_t G, int64_t
   a.s_col_pad = col.s_pad;
   a.rht = rht;
   a.rht_mask = p.rht_mask;
-  launch_nvfp4_quantize(a, std::max(device_sms(), 1), s);
+  a.err = p.err;
+  return launch_nvfp4_quantize(a, std::max(device_sms(), 1), s);
 }
 
 // Quantise a bf16 matrix [M, N] (row groups G padded to Gp) into the row-wise and the
@@ -521,8 +522,9 @@ moe_status_t moe_route_permute(const moe_layer_desc_t* d, int32_t T, const float
     launch_gather_rows_amax(x, src_of, offsets, d->E, d->k, d->H, w.L.R_cap, p.rht_mask,
                             w.at<void>(w.L.x_perm), p.amax + AM_X, p.amax + AM_XT, device_sms(),
                             MOE_K_GATHER_X, s);
-    nv_quantize(w.at<void>(w.L.x_perm), w.L.R_cap, d->H, w.L.R_cap, w.L.R_cap, nullptr, p, AM_X,
-                AM_XT, p.x, p.xt, 1, s);
+    if (!nv_quantize(w.at<void>(w.L.x_perm), w.L.R_cap, d->H, w.L.R_cap, w.L.R_cap, nullptr, p,
+                     AM_X, AM_XT, p.x, p.xt, 1, s))
+      return fail(MOE_ERR_CUDA, "NVFP4 quantiser: tensor map or shared-memory limit");
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "route_permute launch");
     return MOE_OK;
@@ -602,18 +604,20 @@ static moe_status_t fwd_impl(const moe_layer_desc_t* d, int32_t T, const void* w
     if (!d->reuse_weights) {
       launch_nvfp4_amax(w1_packed, (int64_t)d->E * m.N1 * d->H, m.amax + AM_W1, device_sms(), s);
       launch_nvfp4_amax(w2, (int64_t)d->E * d->F * d->H, m.amax + AM_W2, device_sms(), s);
-      nv_quantize(w1_packed, (int64_t)d->E * m.N1p, d->H, m.N1, m.N1p, nullptr, m, AM_W1, AM_W1,
-                  m.w1, m.w1t, 0, s);
-      nv_quantize(w2, (int64_t)d->E * m.Fp, d->H, d->F, m.Fp, nullptr, m, AM_W2, AM_W2, m.w2,
-                  m.w2t, 0, s);
+      if (!nv_quantize(w1_packed, (int64_t)d->E * m.N1p, d->H, m.N1, m.N1p, nullptr, m, AM_W1,
+                       AM_W1, m.w1, m.w1t, 0, s) ||
+          !nv_quantize(w2, (int64_t)d->E * m.Fp, d->H, d->F, m.Fp, nullptr, m, AM_W2, AM_W2,
+                       m.w2, m.w2t, 0, s))
+        return fail(MOE_ERR_CUDA, "NVFP4 quantiser: tensor map or shared-memory limit");
     }
     // FC1 + activation + probability scale, BF16 a_s plus its amax and rotated amax
     m.role = ROLE_FC1_FPROP;
     m.out = w.at<void>(w.L.z);
     m.out2 = w.at<void>(w.L.a_s);
     if ((e = launch_grouped_gemm_fp4(m, s)) != cudaSuccess) return cuda_fail(e, "FC1 FP4 GEMM");
-    nv_quantize(w.at<void>(w.L.a_s), w.L.R_cap, d->F, w.L.R_cap, w.L.R_cap, live, m, AM_A, AM_AT,
-                m.a, m.at, 1, s);
+    if (!nv_quantize(w.at<void>(w.L.a_s), w.L.R_cap, d->F, w.L.R_cap, w.L.R_cap, live, m, AM_A,
+                     AM_AT, m.a, m.at, 1, s))
+      return fail(MOE_ERR_CUDA, "NVFP4 quantiser: tensor map or shared-memory limit");
     m.role = ROLE_FC2_FPROP;
     m.out = w.at<void>(w.L.y_perm);
     m.out2 = nullptr;
@@ -768,8 +772,9 @@ static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* d
   if (d->precision == MOE_PREC_NVFP4) {
     Fp4Problem m = fp4_problem(d, w);
     const int32_t* live = w.at<int32_t>(w.L.offsets) + d->E;
-    nv_quantize(w.at<void>(w.L.dy_perm), w.L.R_cap, d->H, w.L.R_cap, w.L.R_cap, nullptr, m,
-                AM_DY, AM_DYT, m.dy, m.dyt, 1, s);
+    if (!nv_quantize(w.at<void>(w.L.dy_perm), w.L.R_cap, d->H, w.L.R_cap, w.L.R_cap, nullptr, m,
+                     AM_DY, AM_DYT, m.dy, m.dyt, 1, s))
+      return fail(MOE_ERR_CUDA, "NVFP4 quantiser: tensor map or shared-memory limit");
     // FC2 dgrad + dActivation: BF16 dZ plus its amax and the amax of its rotated transpose
     m.role = ROLE_FC2_DGRAD;
     m.out = w.at<void>(w.L.dz);
@@ -781,8 +786,9 @@ static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* d
           w.at<float>(w.L.dprob_part), dprob_parts_fp4(d->F), row_of, n, d_probs);
       count_launch(s, MOE_K_DPROB_REDUCE);
     }
-    nv_quantize(w.at<void>(w.L.dz), w.L.R_cap, m.N1, w.L.R_cap, w.L.R_cap, live, m, AM_DZ,
-                AM_DZT, m.dz, m.dzt, 1, s);
+    if (!nv_quantize(w.at<void>(w.L.dz), w.L.R_cap, m.N1, w.L.R_cap, w.L.R_cap, live, m, AM_DZ,
+                     AM_DZT, m.dz, m.dzt, 1, s))
+      return fail(MOE_ERR_CUDA, "NVFP4 quantiser: tensor map or shared-memory limit");
     m.role = ROLE_FC2_WGRAD;
     m.out = dw2;
     if ((e = launch_grouped_gemm_fp4(m, s)) != cudaSuccess) return cuda_fail(e, "FC2 wgrad FP4");
@@ -988,7 +994,8 @@ moe_status_t nvfp4_quantize(const void* in, int64_t M, int64_t N, const float* a
   a.rht = rht ? 1 : 0;
   a.rht_mask = sign_mask & 0xFFFFu;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  launch_nvfp4_quantize(a, std::max(device_sms(), 1), s);
+  if (!launch_nvfp4_quantize(a, std::max(device_sms(), 1), s))
+    return fail(MOE_ERR_CUDA, "nvfp4_quantize: tensor map or shared-memory limit");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "nvfp4_quantize launch");
   return MOE_OK;

@@ -195,12 +195,15 @@ struct Nvfp4QuantArgs {
   int64_t s_col_pad;
   int rht;
   uint32_t rht_mask;
+  int* err;  // device error word for a load that never lands (may be null)
 };
 bool nvfp4_quantize_shape_ok(int64_t M, int64_t N);  // M % 128 == 0, N % 64 == 0
 // scale bytes of an NVFP4 GEMM operand [rows, cols] in the slab layout, with the slack the
 // 256-element k-blocks and 256-row B fetches of the FP4 GEMM read past the end
 int64_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
-void launch_nvfp4_quantize(const Nvfp4QuantArgs& a, int num_sms, cudaStream_t s);
+// false (nothing launched) unless Gp % 128 == 0, M % Gp == 0 and 0 < G <= Gp, or when the
+// tensor map or the shared-memory limit cannot be set
+bool launch_nvfp4_quantize(const Nvfp4QuantArgs& a, int num_sms, cudaStream_t s);
 // amax of n bf16 values (n % 8 == 0) max-merged into *out (caller zeroes it)
 void launch_nvfp4_amax(const void* in, int64_t n, float* out, int num_sms, cudaStream_t s);
 // NVFP4 layers: the gather of route / backward (x_perm[r] = x[token(r)], padding rows zero)

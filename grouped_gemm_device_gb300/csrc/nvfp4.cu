@@ -5,18 +5,21 @@
 // a BF16 tensor whose amax is already known: for the FC1 output a_s and for dZ the GEMM
 // epilogues provide it; for the routed input, dY and the weights the amax kernels below do.
 //
-// Quantiser: a CTA of 128 threads walks 128-row x 64-column tiles of a bf16 matrix, staged in
-// shared memory (144-byte rows, so that both the row reads and the column reads are free of
-// bank conflicts). Thread t then quantises
+// Quantiser: a persistent CTA of 128 threads walks 128-row x 64-column tiles of a bf16 matrix.
+// Tiles arrive by TMA (one 3-D box {64, 128, 1} over [groups][G][N], 128-byte swizzle) into a
+// ring of shared-memory stages; group padding rows are the box's out-of-bounds rows (zero
+// filled) and rows at or beyond the device-side row count are zeroed in shared memory, so no
+// global memory is read for them. Thread t then quantises
 //   row-wise    row t's 64 values (four 16-blocks along the row, the reduction dimension of
 //               the row-grouped GEMMs) into one 32-byte run and one 32-bit word of scales;
 //   transposed  columns 2 (t % 32), 2 (t % 32) + 1 over rows 32 (t / 32) .. + 31 (two 16-blocks
-//               along the rows per column, optionally Hadamard-rotated first) into a 16-byte
-//               run and a 16-bit scale pair per column of the transposed copy [N, M / 2]: the
-//               K-major operand of the weight-gradient GEMMs.
-// Input rows are grouped (G rows per group in the input, Gp in the output, zero padding rows)
-// and optionally cut at a device-side row count (rows at or beyond it read as zero).
-#include "kernels.cuh"
+//               along the rows per column, optionally Hadamard-rotated first) for the transposed
+//               copy [N, M / 2], the K-major operand of the weight-gradient GEMMs. Its codes and
+//               scales go through a shared-memory buffer so that each column leaves as whole
+//               32-byte runs and each scale as a whole 32-bit word.
+// Input rows are grouped (G rows per group in the input, Gp in the output, Gp a multiple of
+// 128) and optionally cut at a device-side row count (rows at or beyond it read as zero).
+#include "gemm_common.cuh"
 #include "nvfp4.cuh"
 
 namespace moe {
@@ -25,92 +28,151 @@ namespace {
 
 constexpr int QT_ROWS = 128;
 constexpr int QT_COLS = 64;
-constexpr int QT_LD = 144;  // bytes per staged row: 128 + 16
 constexpr int QT_THREADS = 128;
+constexpr int QT_STAGES = 3;
+constexpr int QT_TILE_BYTES = QT_ROWS * QT_COLS * 2;  // 16 KB: 128 rows of 128 bytes
 
-// Stage one tile: 128 rows x 8 pieces of 16 bytes, 8 consecutive threads a row's 128 bytes;
-// a zero row (group padding or past the row limit) copies nothing and reads no global memory.
-MOE_DEVICE void stage_tile(const Nvfp4QuantArgs& p, const uint16_t* in, int64_t tile_i,
-                           int64_t ntc, int64_t limit, uint32_t dst, int t) {
-  const int64_t r0 = (tile_i / ntc) * QT_ROWS;
-  const int64_t c0 = (tile_i % ntc) * QT_COLS;
+struct QtSmem {
+  uint8_t tile[QT_STAGES][QT_TILE_BYTES];  // 1024-byte aligned (the swizzle atom)
+  // transposed codes of a tile, two buffers: row j holds columns 2j and 2j + 1 (64 bytes
+  // each), its 16-byte pieces XOR-swizzled by (j mod 8)
+  uint8_t colq[2][32 * 128];
+  uint16_t cols[2][2][64][2];  // transposed scales: [buffer][slab][column][half word]
+  float enc_row[128], enc_col[128];
+  uint64_t full[QT_STAGES];
+  int abort;
+};
+constexpr int QT_SMEM = (int)sizeof(QtSmem) + 1024;
+
+struct QtArgs {
+  Nvfp4QuantArgs a;
+  CUtensorMap tm;  // input as [groups][G][N] bf16, box {64, 128, 1}, 128-byte swizzle
+};
+
+// 16 butterflies of the Hadamard rotation on column pairs whose signs are already applied;
+// the same fp32 operations as rht16_pair after its sign step.
+MOE_DEVICE void rht16_pair_signed(uint64_t (&x)[16]) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int v = t + QT_THREADS * i;
-    const int r = v >> 3, piece = v & 7;
-    const int64_t orow = r0 + r;
-    const int64_t g = orow / p.Gp, gi = orow - g * p.Gp;
-    const bool live = gi < p.G && orow < limit;
-    const uint16_t* src = live ? in + (g * p.G + gi) * p.N + c0 + piece * 8 : in;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst + r * QT_LD +
-                                                                          piece * 16),
-                 "l"(src), "r"(live ? 16 : 0)
-                 : "memory");
+  for (int m = 1; m < 16; m <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i & m) continue;
+      const uint64_t a = x[i], b = x[i | m];
+      x[i] = add_f32x2(a, b);
+      x[i | m] = sub_f32x2(a, b);
+    }
   }
+  const uint64_t quarter = pack_f32x2(0.25f, 0.25f);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) x[i] = mul_f32x2(x[i], quarter);
 }
 
-__global__ void __launch_bounds__(QT_THREADS, 6) nvfp4_quantize_kernel(const Nvfp4QuantArgs p) {
+__global__ void __launch_bounds__(QT_THREADS) nvfp4_quantize_kernel(const __grid_constant__ QtArgs q) {
   MOE_GRIDDEP_ENTRY();
-  // two tile buffers: the next tile streams in while this one is quantised
-  __shared__ __align__(16) uint8_t tiles[2][QT_ROWS * QT_LD];
-  __shared__ float enc_row[128], enc_col[128];
+  const Nvfp4QuantArgs& p = q.a;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  QtSmem& sm =
+      *reinterpret_cast<QtSmem*>(smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr));
   const int t = threadIdx.x;
-  const int64_t ntr = p.M / QT_ROWS, ntc = p.N / QT_COLS;
-  const int64_t ntiles = ntr * ntc;
+  const int64_t ntc = p.N / QT_COLS;
+  const int64_t ntiles = (p.M / QT_ROWS) * ntc;
   const int64_t limit = p.row_limit ? (int64_t)*p.row_limit : p.M;
   const float s_row = p.q_row ? nvfp4_encode_scale(*p.amax_row) : 0.f;
   const float s_col = p.q_col ? nvfp4_encode_scale(*p.amax_col) : 0.f;
-  nvfp4_fill_enc_table(enc_row, s_row, t, QT_THREADS);
-  nvfp4_fill_enc_table(enc_col, s_col, t, QT_THREADS);  // visible after the first barrier
-  const uint16_t* in = static_cast<const uint16_t*>(p.in);
-  if ((int64_t)blockIdx.x < ntiles)
-    stage_tile(p, in, blockIdx.x, ntc, limit, smem_u32(tiles[0]), t);
-  asm volatile("cp.async.commit_group;" ::: "memory");
+  nvfp4_fill_enc_table(sm.enc_row, s_row, t, QT_THREADS);
+  nvfp4_fill_enc_table(sm.enc_col, s_col, t, QT_THREADS);
+  if (t == 0) {
+    for (int s = 0; s < QT_STAGES; ++s) mbar_init(&sm.full[s], 1);
+    sm.abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&q.tm);
+  }
+  __syncthreads();
+  // thread 0: bring tile `ti` into stage s (a tile wholly at or beyond the row count is only
+  // marked arrived: its stage is zeroed instead)
+  auto issue = [&](int64_t ti, int s) {
+    const int64_t r0 = (ti / ntc) * QT_ROWS, c0 = (ti % ntc) * QT_COLS;
+    if (r0 >= limit) {
+      mbar_arrive(&sm.full[s]);
+      return;
+    }
+    mbar_arrive_expect_tx(&sm.full[s], QT_TILE_BYTES);
+    tma_load_3d(sm.tile[s], &q.tm, &sm.full[s], (int)c0, (int)(r0 % p.Gp), (int)(r0 / p.Gp));
+  };
+  if (t == 0)
+    for (int s = 0; s < QT_STAGES; ++s) {
+      const int64_t ti = blockIdx.x + (int64_t)s * gridDim.x;
+      if (ti < ntiles) issue(ti, s);
+    }
+  const uint32_t sign_mask = p.rht ? p.rht_mask : 0u;
+  volatile int* abort = &sm.abort;
   int k = 0;
   for (int64_t tile_i = blockIdx.x; tile_i < ntiles; tile_i += gridDim.x, ++k) {
-    const int64_t next = tile_i + gridDim.x;
-    if (next < ntiles) stage_tile(p, in, next, ntc, limit, smem_u32(tiles[(k + 1) & 1]), t);
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    const int s = k % QT_STAGES;
     const int64_t r0 = (tile_i / ntc) * QT_ROWS;
     const int64_t c0 = (tile_i % ntc) * QT_COLS;
-    const uint8_t* tile = tiles[k & 1];
-    __syncthreads();
+    uint8_t* tile = sm.tile[s];
+    const bool ok = mbar_wait(&sm.full[s], (uint32_t)(k / QT_STAGES) & 1u, abort, p.err);
+    if (r0 + QT_ROWS > limit) {  // CTA-uniform: rows at or beyond the row count read as zero
+      if (t >= limit - r0) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(tile + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+    }
+    if (__syncthreads_or(!ok)) {
+      // give up: wait (bounded) for the loads still in flight, then leave
+      if (t == 0) {
+        int own_abort = 0;
+        for (int j = k; j < k + QT_STAGES; ++j) {
+          const int64_t ti = blockIdx.x + (int64_t)j * gridDim.x;
+          if (ti < ntiles)
+            mbar_wait(&sm.full[j % QT_STAGES], (uint32_t)(j / QT_STAGES) & 1u, &own_abort,
+                      nullptr);
+        }
+      }
+      return;
+    }
     if (p.q_row) {
-      const uint8_t* src = tile + t * QT_LD;
+      const uint8_t* src = tile + t * 128;
       uint32_t codes[8], scales = 0;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const uint4 w0 = *reinterpret_cast<const uint4*>(src + 32 * b);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(src + 32 * b + 16);
+        const uint4 w0 = *reinterpret_cast<const uint4*>(src + (((2 * b) ^ (t & 7)) << 4));
+        const uint4 w1 = *reinterpret_cast<const uint4*>(src + (((2 * b + 1) ^ (t & 7)) << 4));
         const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        uint32_t q[2];
-        scales |= nvfp4_quant16_bf16(w, s_row, enc_row, q) << (8 * b);
-        codes[2 * b] = q[0];
-        codes[2 * b + 1] = q[1];
+        uint32_t qq[2];
+        scales |= nvfp4_quant16_bf16(w, s_row, sm.enc_row, qq) << (8 * b);
+        codes[2 * b] = qq[0];
+        codes[2 * b + 1] = qq[1];
       }
       const int64_t row = r0 + t;
       st_global_v8(p.q_row + row * (p.N / 2) + c0 / 2, codes);
       *reinterpret_cast<uint32_t*>(p.s_row + sf_mma_offset(row, c0 / 16, p.s_row_pad)) = scales;
     }
+    uint8_t* cq = sm.colq[k & 1];
     if (p.q_col) {
-      // thread t: columns 2 (t % 32) and 2 (t % 32) + 1, rows 32 (t / 32) .. + 31 (two blocks
-      // of 16 per column, the two columns as fp32 pairs); a warp's 32-bit reads of one staged
-      // row are 128 contiguous bytes
+      // thread t: columns 2 cp, 2 cp + 1 (a 32-bit word of each staged row) over rows
+      // 32 h .. 32 h + 31; a warp's reads of one row cover its 128 bytes once
       const int cp = t & 31, h = t >> 5;
-      const uint8_t* src = tile + (h * 32) * QT_LD + 4 * cp;
       uint32_t codes[2][4], scales[2] = {0, 0};
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
         uint64_t x[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(src + (16 * b + i) * QT_LD);
+          const int r = h * 32 + 16 * b + i;  // r mod 8 == i mod 8
+          uint32_t w = *reinterpret_cast<const uint32_t*>(
+              tile + r * 128 + ((((cp >> 2) ^ (i & 7)) << 4) | ((cp & 3) << 2)));
+          // the rotation's sign d_i flips both bf16 values (exactly the fp32 negation)
+          w ^= (0u - ((sign_mask >> i) & 1u)) & 0x80008000u;
           x[i] = pack_f32x2(bf16_lo(w), bf16_hi(w));
         }
-        if (p.rht) rht16_pair(x, p.rht_mask);
+        if (p.rht) rht16_pair_signed(x);
         uint32_t qa[2], qb[2];
-        const uint32_t sc = nvfp4_quant16_pair(x, s_col, enc_col, qa, qb);
+        const uint32_t sc = nvfp4_quant16_pair(x, s_col, sm.enc_col, qa, qb);
         scales[0] |= (sc & 0xFFu) << (8 * b);
         scales[1] |= (sc >> 8) << (8 * b);
         codes[0][2 * b] = qa[0];
@@ -118,20 +180,36 @@ __global__ void __launch_bounds__(QT_THREADS, 6) nvfp4_quantize_kernel(const Nvf
         codes[1][2 * b] = qb[0];
         codes[1][2 * b + 1] = qb[1];
       }
-      const int64_t rr = r0 + h * 32;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int64_t col = c0 + 2 * cp + k;
-        *reinterpret_cast<uint4*>(p.q_col + col * (p.M / 2) + rr / 2) =
-            make_uint4(codes[k][0], codes[k][1], codes[k][2], codes[k][3]);
-        *reinterpret_cast<uint16_t*>(p.s_col + sf_mma_offset(col, rr / 16, p.s_col_pad)) =
-            (uint16_t)scales[k];
+      for (int kk = 0; kk < 2; ++kk) {
+        *reinterpret_cast<uint4*>(cq + cp * 128 + (((kk * 4 + h) ^ (cp & 7)) << 4)) =
+            make_uint4(codes[kk][0], codes[kk][1], codes[kk][2], codes[kk][3]);
+        sm.cols[k & 1][h >> 1][2 * cp + kk][h & 1] = (uint16_t)scales[kk];
       }
     }
-    // every thread is done with this buffer before the next iteration refills it
+    // stage s is consumed and the transposed buffer complete
     __syncthreads();
+    if (t == 0) {
+      const int64_t next = tile_i + (int64_t)QT_STAGES * gridDim.x;
+      if (next < ntiles) issue(next, s);
+    }
+    if (p.q_col) {
+      // thread t: column c0 + j (j = t / 2), rows r0 + 64 (t % 2) .. + 63 as one 32-byte run
+      const int j = t >> 1, half = t & 1, rho = j >> 1, kk = j & 1;
+      const uint8_t* rowp = cq + rho * 128;
+      const uint4 a = *reinterpret_cast<const uint4*>(rowp + (((kk * 4 + 2 * half) ^ (rho & 7)) << 4));
+      const uint4 b =
+          *reinterpret_cast<const uint4*>(rowp + (((kk * 4 + 2 * half + 1) ^ (rho & 7)) << 4));
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      st_global_v8(p.q_col + (c0 + j) * (p.M / 2) + r0 / 2 + half * 32, w);
+      // thread t: the 32-bit scale word of column c0 + (t % 64) in slab r0 / 64 + t / 64
+      const int slab = t >> 6, jj = t & 63;
+      const uint32_t wd = (uint32_t)sm.cols[k & 1][slab][jj][0] |
+                          ((uint32_t)sm.cols[k & 1][slab][jj][1] << 16);
+      *reinterpret_cast<uint32_t*>(
+          p.s_col + sf_mma_offset(c0 + jj, r0 / 16 + 4 * slab, p.s_col_pad)) = wd;
+    }
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // Plain amax of n bf16 values (n a multiple of 8, 16-byte aligned).
@@ -261,13 +339,25 @@ int64_t nvfp4_sf_bytes(int64_t rows, int64_t cols) {
   return slabs * ((rows + 127) / 128 * 128) * 4 + 1024;
 }
 
-void launch_nvfp4_quantize(const Nvfp4QuantArgs& a, int num_sms, cudaStream_t s) {
+bool launch_nvfp4_quantize(const Nvfp4QuantArgs& a, int num_sms, cudaStream_t s) {
   const int64_t tiles = (a.M / QT_ROWS) * (a.N / QT_COLS);
-  if (tiles <= 0) return;
-  // 36 KB of tile buffers a CTA: six CTAs per SM
-  const int grid = (int)std::min<int64_t>(tiles, (int64_t)std::max(num_sms, 1) * 6);
-  launch_kernel(nvfp4_quantize_kernel, grid, QT_THREADS, 0, s, nullptr, 0, a);
+  if (tiles <= 0) return true;
+  if (a.Gp <= 0 || a.Gp % QT_ROWS || a.M % a.Gp || a.G <= 0 || a.G > a.Gp) return false;
+  QtArgs q;
+  q.a = a;
+  const uint64_t dims[3] = {(uint64_t)a.N, (uint64_t)a.G, (uint64_t)(a.M / a.Gp)};
+  const uint64_t strides[2] = {(uint64_t)a.N * 2, (uint64_t)a.G * a.N * 2};
+  const uint32_t box[3] = {QT_COLS, QT_ROWS, 1};
+  if (!make_tmap(&q.tm, a.in, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+    return false;
+  if (ensure_smem_attr(reinterpret_cast<const void*>(nvfp4_quantize_kernel), QT_SMEM) !=
+      cudaSuccess)
+    return false;
+  // three CTAs (nine tiles in flight) per SM
+  const int grid = (int)std::min<int64_t>(tiles, (int64_t)std::max(num_sms, 1) * 3);
+  launch_kernel(nvfp4_quantize_kernel, grid, QT_THREADS, QT_SMEM, s, nullptr, 0, q);
   count_launch(s, MOE_K_NVFP4_QUANTIZE);
+  return true;
 }
 
 void launch_nvfp4_amax(const void* in, int64_t n, float* out, int num_sms, cudaStream_t s) {

@@ -82,6 +82,19 @@ MOE_DEVICE uint64_t mul_f32x2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// fp32(m / 6) for m >= 0, IEEE round to nearest even, without the division routine for the
+// usual range: the product with c = RN(1/6) corrected by one exact FMA residual,
+// q = RN(q0 + RN(m - 6 q0) c) (Markstein's correction step for division by a constant). It
+// equals the IEEE quotient for m = 0 and every m in [2^-125, FLT_MAX] (checked exhaustively
+// against IEEE division over all such fp32 values); below 2^-125 (subnormal quotients), and for
+// inf and NaN, the IEEE division itself is taken.
+MOE_DEVICE float nvfp4_div6(float m) {
+  constexpr float kSixth = 0x1.555556p-3f;  // RN(1/6)
+  if ((m < 0x1p-125f && m != 0.0f) || !(m <= FLT_MAX)) return __fdiv_rn(m, 6.0f);
+  const float q0 = __fmul_rn(m, kSixth);
+  return __fmaf_rn(__fmaf_rn(-q0, 6.0f, m), kSixth, q0);
+}
+
 // The encoding factors fp32(S / s_b) of one tensor for every E4M3 scale byte b < 127 (0 for
 // b = 0: the block is all zeros), so that a block's factor is a table read instead of a
 // division, with the same IEEE result. Filled by `nthreads` threads; the caller synchronises.
@@ -104,7 +117,7 @@ MOE_DEVICE uint32_t nvfp4_quant16_bf16(const uint32_t (&bw)[8], float S, const f
     m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
     x[i] = pack_f32x2(lo, hi);
   }
-  const uint32_t sb = cvt_e4m3x2(__fmul_rn(__fdiv_rn(m, 6.0f), S), 0.f) & 0xFFu;
+  const uint32_t sb = cvt_e4m3x2(__fmul_rn(nvfp4_div6(m), S), 0.f) & 0xFFu;
   const float e = enc_tab[sb];
   const uint64_t e2 = pack_f32x2(e, e);
   float w[16];
@@ -150,8 +163,8 @@ MOE_DEVICE uint32_t nvfp4_quant16_pair(const uint64_t (&x)[16], float S, const f
     ma = fmaxf(ma, fabsf(f32x2_lo(x[i])));
     mb = fmaxf(mb, fabsf(f32x2_hi(x[i])));
   }
-  const uint32_t sa = cvt_e4m3x2(__fmul_rn(__fdiv_rn(ma, 6.0f), S), 0.f) & 0xFFu;
-  const uint32_t sb = cvt_e4m3x2(__fmul_rn(__fdiv_rn(mb, 6.0f), S), 0.f) & 0xFFu;
+  const uint32_t sa = cvt_e4m3x2(__fmul_rn(nvfp4_div6(ma), S), 0.f) & 0xFFu;
+  const uint32_t sb = cvt_e4m3x2(__fmul_rn(nvfp4_div6(mb), S), 0.f) & 0xFFu;
   const uint64_t e2 = pack_f32x2(enc_tab[sa], enc_tab[sb]);
   float wa[16], wb[16];
 #pragma unroll

@@ -77,6 +77,31 @@ def test_nvfp4_quantize_bit_exact(lib, M, N, scale, outliers):
     assert np.array_equal(cc, c_c.T)
 
 
+def test_nvfp4_quantize_blocks_with_subnormal_maxima(lib):
+    """Blocks whose maximum m is below 2^-125, so that fp32(m / 6) is subnormal, with a tensor
+    amax that makes S large enough for those blocks to get non-zero E4M3 scales (and small
+    enough that fp32(S / s_b) stays finite): the scale bytes then depend on the exact rounding
+    of m / 6, which the kernel takes on its IEEE-division branch there."""
+    M, N = 256, 128
+    rng = np.random.default_rng(91)
+    v = rng.uniform(-2.3e-38, 2.3e-38, size=(M, N)) * rng.uniform(0.02, 1.0, size=(M, 1))
+    v[5, 7] = 4.1e-33                                   # the tensor amax: S ~ 6.6e35
+    a = synth.round_to_bf16_bits(v.astype(np.float32))
+    v = om.bf16_to_f64(a)
+    am = nv.amax(v)
+    S = nv.encode_scale(am)
+    c_r, sb_r = nv.quantize_blocks(v, 1, S)
+    c_c, sb_c = nv.quantize_blocks(v, 0, S)
+    tiny = np.abs(v[:, :16]).max(axis=1) < 2.0 ** -125
+    nz = np.count_nonzero(sb_r[tiny, 0])
+    assert tiny.sum() > 100 and nz > 50 and tiny.sum() - nz > 20
+    cr, sr, cc, sc = _quantize(bf16_dev(a), M, N, am, am, 0, 0)
+    assert np.array_equal(sr, omx.e4m3_encode(sb_r))
+    assert np.array_equal(cr, c_r)
+    assert np.array_equal(sc, omx.e4m3_encode(sb_c).T)
+    assert np.array_equal(cc, c_c.T)
+
+
 def test_nvfp4_quantize_rotated_transpose(lib):
     """The rotated copy: the kernel rotates in fp32 (butterflies), the oracle in fp64 rounded
     to fp32, so a value may differ by an fp32 ulp; codes and scales may then differ only where

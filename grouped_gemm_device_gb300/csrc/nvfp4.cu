@@ -7,7 +7,7 @@
 //
 // Quantiser: a persistent CTA of 128 threads walks 128-row x 64-column tiles of a bf16 matrix.
 // Tiles arrive by TMA (one 3-D box {64, 128, 1} over [groups][G][N], 128-byte swizzle) into a
-// ring of shared-memory stages; group padding rows are the box's out-of-bounds rows (zero
+// ring of shared-memory stages (two per CTA, four or five CTAs per SM); group padding rows are the box's out-of-bounds rows (zero
 // filled) and rows at or beyond the device-side row count are zeroed in shared memory, so no
 // global memory is read for them. Thread t then quantises
 //   row-wise    row t's 64 values (four 16-blocks along the row, the reduction dimension of
@@ -29,20 +29,21 @@ namespace {
 constexpr int QT_ROWS = 128;
 constexpr int QT_COLS = 64;
 constexpr int QT_THREADS = 128;
-constexpr int QT_STAGES = 3;
 constexpr int QT_TILE_BYTES = QT_ROWS * QT_COLS * 2;  // 16 KB: 128 rows of 128 bytes
 
+template <int STAGES>
 struct QtSmem {
-  uint8_t tile[QT_STAGES][QT_TILE_BYTES];  // 1024-byte aligned (the swizzle atom)
+  uint8_t tile[STAGES][QT_TILE_BYTES];  // 1024-byte aligned (the swizzle atom)
   // transposed codes of a tile, two buffers: row j holds columns 2j and 2j + 1 (64 bytes
   // each), its 16-byte pieces XOR-swizzled by (j mod 8)
   uint8_t colq[2][32 * 128];
   uint16_t cols[2][2][64][2];  // transposed scales: [buffer][slab][column][half word]
   float enc_row[128], enc_col[128];
-  uint64_t full[QT_STAGES];
+  uint64_t full[STAGES];
   int abort;
 };
-constexpr int QT_SMEM = (int)sizeof(QtSmem) + 1024;
+template <int STAGES>
+constexpr int qt_smem_bytes() { return (int)sizeof(QtSmem<STAGES>) + 1024; }
 
 struct QtArgs {
   Nvfp4QuantArgs a;
@@ -67,13 +68,14 @@ MOE_DEVICE void rht16_pair_signed(uint64_t (&x)[16]) {
   for (int i = 0; i < 16; ++i) x[i] = mul_f32x2(x[i], quarter);
 }
 
+template <int STAGES>
 __global__ void __launch_bounds__(QT_THREADS) nvfp4_quantize_kernel(const __grid_constant__ QtArgs q) {
   MOE_GRIDDEP_ENTRY();
   const Nvfp4QuantArgs& p = q.a;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
-  QtSmem& sm =
-      *reinterpret_cast<QtSmem*>(smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr));
+  QtSmem<STAGES>& sm =
+      *reinterpret_cast<QtSmem<STAGES>*>(smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr));
   const int t = threadIdx.x;
   const int64_t ntc = p.N / QT_COLS;
   const int64_t ntiles = (p.M / QT_ROWS) * ntc;
@@ -83,7 +85,7 @@ __global__ void __launch_bounds__(QT_THREADS) nvfp4_quantize_kernel(const __grid
   nvfp4_fill_enc_table(sm.enc_row, s_row, t, QT_THREADS);
   nvfp4_fill_enc_table(sm.enc_col, s_col, t, QT_THREADS);
   if (t == 0) {
-    for (int s = 0; s < QT_STAGES; ++s) mbar_init(&sm.full[s], 1);
+    for (int s = 0; s < STAGES; ++s) mbar_init(&sm.full[s], 1);
     sm.abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&q.tm);
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(QT_THREADS) nvfp4_quantize_kernel(const __grid
     tma_load_3d(sm.tile[s], &q.tm, &sm.full[s], (int)c0, (int)(r0 % p.Gp), (int)(r0 / p.Gp));
   };
   if (t == 0)
-    for (int s = 0; s < QT_STAGES; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       const int64_t ti = blockIdx.x + (int64_t)s * gridDim.x;
       if (ti < ntiles) issue(ti, s);
     }
@@ -109,11 +111,11 @@ __global__ void __launch_bounds__(QT_THREADS) nvfp4_quantize_kernel(const __grid
   volatile int* abort = &sm.abort;
   int k = 0;
   for (int64_t tile_i = blockIdx.x; tile_i < ntiles; tile_i += gridDim.x, ++k) {
-    const int s = k % QT_STAGES;
+    const int s = k % STAGES;
     const int64_t r0 = (tile_i / ntc) * QT_ROWS;
     const int64_t c0 = (tile_i % ntc) * QT_COLS;
     uint8_t* tile = sm.tile[s];
-    const bool ok = mbar_wait(&sm.full[s], (uint32_t)(k / QT_STAGES) & 1u, abort, p.err);
+    const bool ok = mbar_wait(&sm.full[s], (uint32_t)(k / STAGES) & 1u, abort, p.err);
     if (r0 + QT_ROWS > limit) {  // CTA-uniform: rows at or beyond the row count read as zero
       if (t >= limit - r0) {
 #pragma unroll
@@ -126,10 +128,10 @@ __global__ void __launch_bounds__(QT_THREADS) nvfp4_quantize_kernel(const __grid
       // give up: wait (bounded) for the loads still in flight, then leave
       if (t == 0) {
         int own_abort = 0;
-        for (int j = k; j < k + QT_STAGES; ++j) {
+        for (int j = k; j < k + STAGES; ++j) {
           const int64_t ti = blockIdx.x + (int64_t)j * gridDim.x;
           if (ti < ntiles)
-            mbar_wait(&sm.full[j % QT_STAGES], (uint32_t)(j / QT_STAGES) & 1u, &own_abort,
+            mbar_wait(&sm.full[j % STAGES], (uint32_t)(j / STAGES) & 1u, &own_abort,
                       nullptr);
         }
       }
@@ -190,7 +192,7 @@ __global__ void __launch_bounds__(QT_THREADS) nvfp4_quantize_kernel(const __grid
     // stage s is consumed and the transposed buffer complete
     __syncthreads();
     if (t == 0) {
-      const int64_t next = tile_i + (int64_t)QT_STAGES * gridDim.x;
+      const int64_t next = tile_i + (int64_t)STAGES * gridDim.x;
       if (next < ntiles) issue(next, s);
     }
     if (p.q_col) {
@@ -339,7 +341,9 @@ int64_t nvfp4_sf_bytes(int64_t rows, int64_t cols) {
   return slabs * ((rows + 127) / 128 * 128) * 4 + 1024;
 }
 
-bool launch_nvfp4_quantize(const Nvfp4QuantArgs& a, int num_sms, cudaStream_t s) {
+// STAGES tiles in flight per CTA, CTAS CTAs per SM
+template <int STAGES, int CTAS>
+bool launch_nvfp4_quantize_cfg(const Nvfp4QuantArgs& a, int num_sms, cudaStream_t s) {
   const int64_t tiles = (a.M / QT_ROWS) * (a.N / QT_COLS);
   if (tiles <= 0) return true;
   if (a.Gp <= 0 || a.Gp % QT_ROWS || a.M % a.Gp || a.G <= 0 || a.G > a.Gp) return false;
@@ -350,14 +354,23 @@ bool launch_nvfp4_quantize(const Nvfp4QuantArgs& a, int num_sms, cudaStream_t s)
   const uint32_t box[3] = {QT_COLS, QT_ROWS, 1};
   if (!make_tmap(&q.tm, a.in, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
     return false;
-  if (ensure_smem_attr(reinterpret_cast<const void*>(nvfp4_quantize_kernel), QT_SMEM) !=
+  constexpr int smem = qt_smem_bytes<STAGES>();
+  if (ensure_smem_attr(reinterpret_cast<const void*>(nvfp4_quantize_kernel<STAGES>), smem) !=
       cudaSuccess)
     return false;
-  // three CTAs (nine tiles in flight) per SM
-  const int grid = (int)std::min<int64_t>(tiles, (int64_t)std::max(num_sms, 1) * 3);
-  launch_kernel(nvfp4_quantize_kernel, grid, QT_THREADS, QT_SMEM, s, nullptr, 0, q);
+  const int grid = (int)std::min<int64_t>(tiles, (int64_t)std::max(num_sms, 1) * CTAS);
+  launch_kernel(nvfp4_quantize_kernel<STAGES>, grid, QT_THREADS, smem, s, nullptr, 0, q);
   count_launch(s, MOE_K_NVFP4_QUANTIZE);
   return true;
+}
+
+bool launch_nvfp4_quantize(const Nvfp4QuantArgs& a, int num_sms, cudaStream_t s) {
+  // two stages a CTA; five CTAs (20 warps) per SM for the rotated copy, whose butterflies
+  // make it issue-bound, four without the rotation (measured on GB300: 4.7 against 4.1 TB/s
+  // for three CTAs of three stages on a rotated 33792 x 4096 tensor; 6.1 against 5.6 TB/s on
+  // unrotated weights)
+  return a.rht && a.q_col ? launch_nvfp4_quantize_cfg<2, 5>(a, num_sms, s)
+                          : launch_nvfp4_quantize_cfg<2, 4>(a, num_sms, s);
 }
 
 void launch_nvfp4_amax(const void* in, int64_t n, float* out, int num_sms, cudaStream_t s) {

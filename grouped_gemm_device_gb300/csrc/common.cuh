@@ -305,6 +305,13 @@ MOE_DEVICE void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
+// Arrive without release semantics: for signals that order no memory accesses of this thread
+// (an accumulator whose TMEM loads have all completed), so the arrive does not wait for the
+// thread's outstanding global stores.
+MOE_DEVICE void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
 // Store a flag into the peer CTA's shared memory.
 MOE_DEVICE void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v)

@@ -470,16 +470,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       uint32_t r[32];
       float v[32];
-      if (EPI == EPI_STORE) {
-        uint16_t* o = static_cast<uint16_t*>(p.out) + (KG ? (int64_t)t.e * p.out_estride : 0) +
-                      (int64_t)row * p.ldo + t.n0;
-        for (int cc = c0; cc < c1; cc += 32) {
-          if (t.n0 + cc >= p.N) break;
-          tmem_ld_32x32b_x32(taddr + cc, r);
+      bool released = false;
+      if constexpr (EPI == EPI_STORE) {
+        // drain this warp's 128 columns as packed bf16 and free the accumulator before any
+        // store: the release that frees it (cluster scope for a pair follower) then has no
+        // global stores of this thread to wait for
+        uint32_t pk[64];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          tmem_ld_32x32b_x32(taddr + c0 + 32 * j, r);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-          if (row_ok) store_bf16x32w(o + cc, v, p.wide);
+          for (int i = 0; i < 16; ++i)
+            pk[16 * j + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (PAIR) mbar_arrive_cluster(tempty_leader + acc * (uint32_t)sizeof(uint64_t));
+          else mbar_arrive(&c.tempty[acc]);
+        }
+        released = true;
+        if (row_ok) {
+          uint16_t* o = static_cast<uint16_t*>(p.out) + (KG ? (int64_t)t.e * p.out_estride : 0) +
+                        (int64_t)row * p.ldo + t.n0 + c0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (t.n0 + c0 + 32 * j >= p.N) break;
+            if (p.wide) {
+              st_global_v8(o + 32 * j, &pk[16 * j]);
+              st_global_v8(o + 32 * j + 16, &pk[16 * j + 8]);
+            } else {
+              uint4* d = reinterpret_cast<uint4*>(o + 32 * j);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                d[i] = make_uint4(pk[16 * j + 4 * i], pk[16 * j + 4 * i + 1],
+                                  pk[16 * j + 4 * i + 2], pk[16 * j + 4 * i + 3]);
+            }
+          }
         }
       } else if (EPI == EPI_GLU) {
         const float prob = row_ok ? p.row_prob[row] : 0.f;
@@ -604,11 +632,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (row_ok) p.dprob_part[(int64_t)row * p.nparts + (t.n0 / BN) * 2 + half] = dp;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (PAIR) mbar_arrive_cluster(tempty_leader + acc * (uint32_t)sizeof(uint64_t));
-        else mbar_arrive(&c.tempty[acc]);
+      if (!released) {
+        // every TMEM load of this warp has completed (each was waited for): the accumulator
+        // is free, and the signal need not wait for this thread's global stores
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (PAIR)
+            mbar_arrive_cluster_relaxed(tempty_leader + acc * (uint32_t)sizeof(uint64_t));
+          else mbar_arrive(&c.tempty[acc]);
+        }
       }
       ++acc_i;
     }

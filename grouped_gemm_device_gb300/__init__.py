@@ -31,7 +31,8 @@ NV_AMAX = ("x", "xt", "w1", "w2", "a", "at", "dy", "dyt", "dz", "dzt")
 EXPORTS = ("moe_timeline_begin", "moe_timeline_end", "moe_workspace_size", "moe_workspace_layout", "moe_route_permute",
            "moe_grouped_mlp_fwd", "moe_grouped_mlp_bwd", "mxfp8_quantize", "moe_pack_fc1_weight",
            "moe_get_error", "moe_clear_error", "moe_gemm_ctas", "moe_launch_count",
-           "moe_last_error_string", "moe_selftest_wait_timeout", "moe_grouped_mlp_fwd_ex",
+           "moe_last_error_string", "moe_selftest_wait_timeout", "moe_selftest_gemm_timeout",
+           "moe_grouped_mlp_fwd_ex",
            "moe_grouped_mlp_bwd_ex", "nvfp4_amax", "nvfp4_quantize")
 
 
@@ -96,6 +97,7 @@ def load():
         "moe_timeline_end": (_I32, [ctypes.POINTER(_I32)]),
         "moe_route_permute_noalloc": (_I32, [_DP, _I32, _P, _P, _P, _P, _P, _P, _P, _I64, _P]),
         "moe_selftest_wait_timeout": (_I32, [_P, ctypes.c_uint64, _P]),
+        "moe_selftest_gemm_timeout": (_I32, [_DP, _P, _SZ, _P, ctypes.c_uint64, _P]),
         "moe_grouped_mlp_fwd_ex": (_I32, [_DP, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
         "moe_grouped_mlp_bwd_ex": (_I32, [_DP, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                           _SZ, _P]),
@@ -255,6 +257,13 @@ def moe_selftest_wait_timeout(err, limit_ns, stream=None):
     """Enqueue the bounded-wait self-test: a wait nothing completes gives up after limit_ns
     and writes the timeout code into the device int32 `err`."""
     _check(load().moe_selftest_wait_timeout(_ptr(err), int(limit_ns), _stream(stream)))
+
+
+def moe_selftest_gemm_timeout(desc, ws, ws_bytes, w2, limit_ns, stream=None):
+    """Enqueue the FC2 forward GEMM of a routed BF16 layer with its loads withheld: every wait
+    of the kernel runs out after limit_ns and the workspace error word records the timeout."""
+    _check(load().moe_selftest_gemm_timeout(ctypes.byref(desc), _ptr(ws), ws_bytes, _ptr(w2),
+                                            int(limit_ns), _stream(stream)))
 
 
 def moe_get_error(desc, ws, stream=None) -> int:

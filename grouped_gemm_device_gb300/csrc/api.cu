@@ -900,6 +900,30 @@ moe_status_t moe_selftest_wait_timeout(int32_t* err, uint64_t limit_ns, moe_stre
   return MOE_OK;
 }
 
+moe_status_t moe_selftest_gemm_timeout(const moe_layer_desc_t* d, void* ws, size_t ws_bytes,
+                                       const void* w2, uint64_t limit_ns, moe_stream_t stream) {
+  moe_status_t st = validate_desc(d);
+  if (st != MOE_OK) return st;
+  if (d->precision != MOE_PREC_BF16) return fail(MOE_ERR_UNSUPPORTED, "needs a BF16 layer");
+  if (!w2 || !aligned16(w2)) return fail(MOE_ERR_INVALID_ARG, "w2 must be non-NULL, 16B aligned");
+  if (limit_ns < 1000000ull || limit_ns > 10000000000ull)
+    return fail(MOE_ERR_INVALID_ARG, "limit_ns must be in [1 ms, 10 s]");
+  Ws w;
+  if ((st = check_ws(d, ws, ws_bytes, w)) != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the FC2 forward GEMM of the routed layer, with a producer that issues no loads: every
+  // consumer wait runs out after limit_ns, the kernel records the timeout and returns
+  GemmProblem p = base_problem(d, w);
+  p.w2 = w2;
+  p.role = ROLE_FC2_FPROP;
+  p.out = w.at<void>(w.L.y_perm);
+  p.stall_loads = 1;
+  p.wait_ns = limit_ns;
+  cudaError_t e = launch_grouped_gemm(p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "self-test GEMM launch");
+  return MOE_OK;
+}
+
 moe_status_t mxfp8_quantize(const void* in, int64_t M, int64_t N, int32_t rowwise,
                             int32_t colwise, const int32_t* group_offsets, int32_t num_groups,
                             uint8_t* q_row, uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,

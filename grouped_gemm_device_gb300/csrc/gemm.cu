@@ -70,6 +70,8 @@ struct GemmArgs {
   int N1;  // FC1 output columns (2F gated)
   ActDev act;
   int* err;
+  int stall_loads;   // self-test: the producer issues no loads
+  uint64_t wait_ns;  // limit of every barrier wait
 };
 
 // PAIR: the CTA holds half of the B tile (the pair's MMA reads both halves).
@@ -303,13 +305,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < STAGES; ++s) armed[s] = -1;
       // pair: every load completes on the leader's full barrier
       const uint32_t full_leader = PAIR ? mapa_shared(smem_u32(&c.full[0]), 0) : 0u;
-      for (int tile = tile0; tile < total && !*abort; tile += tstep) {
+      for (int tile = tile0; tile < total && !*abort && !p.stall_loads; tile += tstep) {
         TileInfo t;
         decode_tile<BN, KG, TM>(tile, p, c, MT, NT, t);
         const int am0 = t.m0 + BM * (int)rank;    // this CTA's A rows
         const int bn0 = t.n0 + BNH * (int)rank;   // this CTA's B columns
         for (int kb = 0; kb < t.nkb; ++kb) {
-          if (!mbar_wait(&c.empty[stage], phase ^ 1, abort, p.err)) break;
+          if (!mbar_wait(&c.empty[stage], phase ^ 1, abort, p.err, p.wait_ns)) break;
           uint8_t* sA = smem + stage * L::STAGE_BYTES;
           uint8_t* sB = sA + L::A_BYTES;
           uint64_t* bar = &c.full[stage];
@@ -381,12 +383,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t.nkb == 0) continue;
         const int acc = acc_i & 1;
         const uint32_t acc_phase = (acc_i >> 1) & 1;
-        if (!mbar_wait(&c.tempty[acc], acc_phase ^ 1, abort, p.err)) break;
+        if (!mbar_wait(&c.tempty[acc], acc_phase ^ 1, abort, p.err, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         bool ok = true;
         for (int kb = 0; kb < t.nkb; ++kb) {
-          if (!mbar_wait(&c.full[stage], phase, abort, p.err)) {
+          if (!mbar_wait(&c.full[stage], phase, abort, p.err, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -464,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int acc = acc_i & 1;
       const uint32_t acc_phase = (acc_i >> 1) & 1;
-      const bool got = mbar_wait(&c.tfull[acc], acc_phase, abort, p.err);
+      const bool got = mbar_wait(&c.tfull[acc], acc_phase, abort, p.err, p.wait_ns);
       if (!__all_sync(0xFFFFFFFFu, got)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
@@ -473,8 +475,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool released = false;
       if constexpr (EPI == EPI_STORE) {
         // drain this warp's 128 columns as packed bf16 and free the accumulator before any
-        // store: the release that frees it (cluster scope for a pair follower) then has no
-        // global stores of this thread to wait for
+        // store of this tile; the signal is a relaxed arrive (the TMEM loads have completed,
+        // no memory access needs ordering), so it does not wait for the stores of earlier
+        // tiles either
         uint32_t pk[64];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -487,8 +490,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if constexpr (PAIR) mbar_arrive_cluster(tempty_leader + acc * (uint32_t)sizeof(uint64_t));
-          else mbar_arrive(&c.tempty[acc]);
+          if constexpr (PAIR)
+            mbar_arrive_cluster_relaxed(tempty_leader + acc * (uint32_t)sizeof(uint64_t));
+          else mbar_arrive_relaxed(&c.tempty[acc]);
         }
         released = true;
         if (row_ok) {
@@ -640,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           if constexpr (PAIR)
             mbar_arrive_cluster_relaxed(tempty_leader + acc * (uint32_t)sizeof(uint64_t));
-          else mbar_arrive(&c.tempty[acc]);
+          else mbar_arrive_relaxed(&c.tempty[acc]);
         }
       }
       ++acc_i;
@@ -740,6 +744,8 @@ cudaError_t launch_grouped_gemm(const GemmProblem& p, cudaStream_t s) {
   a.ext_part = p.ext_part;
   a.act = p.act;
   a.err = p.err;
+  a.stall_loads = p.stall_loads;
+  a.wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
   a.row_prob = p.row_prob;
   static const int kKid[6] = {MOE_K_GEMM_FC1_FPROP, MOE_K_GEMM_FC2_FPROP, MOE_K_GEMM_FC2_DGRAD,
                               MOE_K_GEMM_FC2_WGRAD, MOE_K_GEMM_FC1_DGRAD, MOE_K_GEMM_FC1_WGRAD};

@@ -126,6 +126,10 @@ struct GemmProblem {
   int* err;
   int num_ctas;            // persistent grid size (SMs - margin)
   int64_t rows_per_expert; // T_max * k / E: the routed rows an expert averages at capacity
+  // failure-detection self-test only: the TMA producer issues no loads (stall_loads = 1), so
+  // every consumer wait runs out, after wait_ns (0: the default limit)
+  int stall_loads;
+  uint64_t wait_ns;
 };
 
 int gemm_bn(int role);

@@ -7,7 +7,7 @@
 //
 // Quantiser: a persistent CTA of 128 threads walks 128-row x 64-column tiles of a bf16 matrix.
 // Tiles arrive by TMA (one 3-D box {64, 128, 1} over [groups][G][N], 128-byte swizzle) into a
-// ring of shared-memory stages (two per CTA, four or five CTAs per SM); group padding rows are the box's out-of-bounds rows (zero
+// ring of shared-memory stages (two per CTA, three or five CTAs per SM); group padding rows are the box's out-of-bounds rows (zero
 // filled) and rows at or beyond the device-side row count are zeroed in shared memory, so no
 // global memory is read for them. Thread t then quantises
 //   row-wise    row t's 64 values (four 16-blocks along the row, the reduction dimension of
@@ -366,11 +366,11 @@ bool launch_nvfp4_quantize_cfg(const Nvfp4QuantArgs& a, int num_sms, cudaStream_
 
 bool launch_nvfp4_quantize(const Nvfp4QuantArgs& a, int num_sms, cudaStream_t s) {
   // two stages a CTA; five CTAs (20 warps) per SM for the rotated copy, whose butterflies
-  // make it issue-bound, four without the rotation (measured on GB300: 4.7 against 4.1 TB/s
-  // for three CTAs of three stages on a rotated 33792 x 4096 tensor; 6.1 against 5.6 TB/s on
-  // unrotated weights)
+  // make it issue-bound, three without the rotation (measured on GB300: 4.7 against 4.1 TB/s
+  // for three CTAs of three stages on a rotated 33792 x 4096 tensor; 5.8-6.0 TB/s on the
+  // unrotated Mixtral and GPT-OSS weights, where four CTAs lost up to 22% on the latter)
   return a.rht && a.q_col ? launch_nvfp4_quantize_cfg<2, 5>(a, num_sms, s)
-                          : launch_nvfp4_quantize_cfg<2, 4>(a, num_sms, s);
+                          : launch_nvfp4_quantize_cfg<2, 3>(a, num_sms, s);
 }
 
 void launch_nvfp4_amax(const void* in, int64_t n, float* out, int num_sms, cudaStream_t s) {

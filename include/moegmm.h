@@ -359,6 +359,19 @@ moe_status_t moe_clear_error(const moe_layer_desc_t *desc, void *ws, moe_stream_
  * involved. Returns MOE_ERR_INVALID_ARG for a NULL err or a limit outside the range. */
 moe_status_t moe_selftest_wait_timeout(int32_t *err, uint64_t limit_ns, moe_stream_t stream);
 
+/* Failure-detection self-test of a GEMM kernel itself (no counterpart on the pages). For a BF16
+ * layer whose moe_route_permute (and forward) ran on ws, enqueues the FC2 forward grouped GEMM
+ * (a_s x W2 -> the workspace's permuted output; w2 as for moe_grouped_mlp_fwd) with its TMA
+ * producer issuing no loads. Every MMA and epilogue wait of the kernel then runs out after
+ * limit_ns nanoseconds (1 ms .. 10 s): the CTA raises its abort flag, MOE_DEVERR_TIMEOUT goes
+ * into the workspace error word (moe_get_error; moe_clear_error resets it), every role leaves
+ * its loop, TMEM is freed and the kernel returns, so the context stays usable. The permuted
+ * output in the workspace is left undefined until the next forward. Returns
+ * MOE_ERR_UNSUPPORTED for a non-BF16 layer, MOE_ERR_INVALID_ARG for a bad description,
+ * workspace, w2 or limit. */
+moe_status_t moe_selftest_gemm_timeout(const moe_layer_desc_t *desc, void *ws, size_t ws_bytes,
+                                       const void *w2, uint64_t limit_ns, moe_stream_t stream);
+
 /* Number of SMs the persistent GEMM uses on the current device for this description
  * (device SM count minus sm_margin, at least 1). */
 int32_t moe_gemm_ctas(const moe_layer_desc_t *desc);

@@ -43,3 +43,32 @@ def test_context_usable_after_a_timeout(lib):
     assert run.layer.device_error() == 0
     ref = inp.oracle(backward=False)
     assert rel_fro(to_np(run.y), ref.y) < BF16_TOL
+
+
+def test_gemm_waits_give_up_and_context_recovers(lib):
+    """A GEMM kernel's own bounded waits: the FC2 forward grouped GEMM of a routed BF16 layer
+    (CTA pairs) runs with its TMA producer issuing no loads, so the MMA and epilogue waits of
+    both CTAs of every pair run out after the limit. The kernel records the timeout in the
+    workspace error word, frees TMEM and returns; after the word is cleared, a full layer step
+    on the same context matches the oracle."""
+    cfg = synth.CONFIGS["tiny"]
+    inp = Inputs(cfg)
+    run = LayerRun(inp, backward=False)
+    L = run.layer
+    assert L.device_error() == 0
+    limit_ns = 5_000_000  # 5 ms
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    g.moe_selftest_gemm_timeout(L.desc, L.ws, L.ws_bytes, run.w2, limit_ns)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert L.device_error() == TIMEOUT
+    assert elapsed >= limit_ns * 1e-9
+    g.moe_clear_error(L.desc, L.ws)
+    torch.cuda.synchronize()
+    assert L.device_error() == 0
+    run.run(backward=True)
+    assert L.device_error() == 0
+    ref = inp.oracle()
+    assert rel_fro(to_np(run.y), ref.y) < BF16_TOL
+    assert rel_fro(to_np(run.dx), ref.dx) < BF16_TOL

@@ -196,6 +196,19 @@ def test_calls_validate_before_touching_the_device(lib):
     with pytest.raises(g.MoeError) as e:
         g.moe_selftest_wait_timeout(256, 10**3, 0)
     assert e.value.status == 1
+    # the GEMM self-test: BF16 layers only, a w2 and a limit in [1 ms, 10 s], checked before
+    # anything is enqueued
+    mx = g.make_desc(E=4, k=2, H=128, F=128, T_max=16, precision="mxfp8", align=128)
+    with pytest.raises(g.MoeError) as e:
+        g.moe_selftest_gemm_timeout(mx, 256, 1 << 30, 256, 10**7, 0)
+    assert e.value.status == 2
+    bf = g.make_desc(E=4, k=2, H=128, F=128, T_max=16)
+    with pytest.raises(g.MoeError) as e:
+        g.moe_selftest_gemm_timeout(bf, 256, 1 << 30, None, 10**7, 0)
+    assert e.value.status == 1
+    with pytest.raises(g.MoeError) as e:
+        g.moe_selftest_gemm_timeout(bf, 256, 1 << 30, 256, 10**3, 0)
+    assert e.value.status == 1
 
 
 def test_config_table_matches_workloads():

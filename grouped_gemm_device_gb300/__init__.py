@@ -24,7 +24,7 @@ DEVERR = {0: "none", 1: "capacity", 2: "timeout", 3: "bad_id"}
 KERNEL_NAMES = ("route_topk", "assign_rows", "gather_x", "gemm_fc1_fprop", "gemm_fc2_fprop",
                 "combine_y", "gather_dy", "gemm_fc2_dgrad", "dprob_reduce", "gemm_fc2_wgrad",
                 "gemm_fc1_dgrad", "combine_dx", "gemm_fc1_wgrad", "mxfp8_quantize", "pack_fc1",
-                "extras_reduce", "nvfp4_amax", "nvfp4_quantize")
+                "extras_reduce", "nvfp4_amax", "nvfp4_quantize", "route_export")
 # moe_ws_layout_t.nv_amax slots (fp32 [16], first 10 used)
 NV_AMAX = ("x", "xt", "w1", "w2", "a", "at", "dy", "dyt", "dz", "dzt")
 
@@ -32,6 +32,7 @@ EXPORTS = ("moe_timeline_begin", "moe_timeline_end", "moe_workspace_size", "moe_
            "moe_grouped_mlp_fwd", "moe_grouped_mlp_bwd", "mxfp8_quantize", "moe_pack_fc1_weight",
            "moe_get_error", "moe_clear_error", "moe_gemm_ctas", "moe_launch_count",
            "moe_last_error_string", "moe_selftest_wait_timeout", "moe_selftest_gemm_timeout",
+           "moe_route_export",
            "moe_grouped_mlp_fwd_ex",
            "moe_grouped_mlp_bwd_ex", "nvfp4_amax", "nvfp4_quantize")
 
@@ -98,6 +99,7 @@ def load():
         "moe_route_permute_noalloc": (_I32, [_DP, _I32, _P, _P, _P, _P, _P, _P, _P, _I64, _P]),
         "moe_selftest_wait_timeout": (_I32, [_P, ctypes.c_uint64, _P]),
         "moe_selftest_gemm_timeout": (_I32, [_DP, _P, _SZ, _P, ctypes.c_uint64, _P]),
+        "moe_route_export": (_I32, [_DP, _P, _SZ, _I32, _P, _P, _P, _P, _P]),
         "moe_grouped_mlp_fwd_ex": (_I32, [_DP, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
         "moe_grouped_mlp_bwd_ex": (_I32, [_DP, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                           _SZ, _P]),
@@ -264,6 +266,14 @@ def moe_selftest_gemm_timeout(desc, ws, ws_bytes, w2, limit_ns, stream=None):
     of the kernel runs out after limit_ns and the workspace error word records the timeout."""
     _check(load().moe_selftest_gemm_timeout(ctypes.byref(desc), _ptr(ws), ws_bytes, _ptr(w2),
                                             int(limit_ns), _stream(stream)))
+
+
+def moe_route_export(desc, ws, ws_bytes, T, offsets=None, row_of=None, src_of=None,
+                     row_prob=None, stream=None):
+    """Copy the routing maps of the last route on ws into caller tensors (any may be None)."""
+    _check(load().moe_route_export(ctypes.byref(desc), _ptr(ws), ws_bytes, int(T),
+                                   _ptr(offsets), _ptr(row_of), _ptr(src_of), _ptr(row_prob),
+                                   _stream(stream)))
 
 
 def moe_get_error(desc, ws, stream=None) -> int:

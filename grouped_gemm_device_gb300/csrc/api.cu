@@ -900,6 +900,33 @@ moe_status_t moe_selftest_wait_timeout(int32_t* err, uint64_t limit_ns, moe_stre
   return MOE_OK;
 }
 
+moe_status_t moe_route_export(const moe_layer_desc_t* d, const void* ws, size_t ws_bytes,
+                              int32_t T, int32_t* offsets, int32_t* row_of, int32_t* src_of,
+                              float* row_prob, moe_stream_t stream) {
+  moe_status_t st = validate_desc(d);
+  if (st != MOE_OK) return st;
+  if (T < 0 || T > d->T_max) return fail(MOE_ERR_INVALID_ARG, "T=%d outside [0, T_max]", T);
+  auto a4 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 3) == 0; };
+  if (!a4(offsets) || !a4(row_of) || !a4(src_of) || !a4(row_prob))
+    return fail(MOE_ERR_INVALID_ARG, "destinations must be 4-byte aligned");
+  Ws w;
+  if ((st = check_ws(d, const_cast<void*>(ws), ws_bytes, w)) != MOE_OK) return st;
+  if (!offsets && !row_of && !src_of && !row_prob) return MOE_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t n_total =
+      std::max<int64_t>(w.L.R_cap, std::max<int64_t>((int64_t)T * d->k, d->E + 1));
+  const int grid =
+      (int)std::min<int64_t>((n_total + 255) / 256, (int64_t)std::max(device_sms(), 1) * 4);
+  launch_kernel(route_export_kernel, grid, 256, 0, s, nullptr, 0, w.at<int32_t>(w.L.offsets),
+                d->E + 1, w.at<int32_t>(w.L.row_of), (int64_t)T * d->k, w.at<int32_t>(w.L.src_of),
+                w.at<float>(w.L.row_prob), (int64_t)w.L.R_cap, n_total, offsets, row_of, src_of,
+                row_prob);
+  count_launch(s, MOE_K_ROUTE_EXPORT);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "route export launch");
+  return MOE_OK;
+}
+
 moe_status_t moe_selftest_gemm_timeout(const moe_layer_desc_t* d, void* ws, size_t ws_bytes,
                                        const void* w2, uint64_t limit_ns, moe_stream_t stream) {
   moe_status_t st = validate_desc(d);

@@ -48,6 +48,11 @@ __global__ void assign_rows_kernel(const int32_t* ids, const float* probs, const
                                    float* row_prob, int* err);
 __global__ void gather_rows_kernel(const uint4* x, const int32_t* src_of, const int32_t* offsets,
                                    int E, int k, int H8, int64_t R_cap, uint4* out);
+__global__ void route_export_kernel(const int32_t* off_ws, int n_off, const int32_t* row_of_ws,
+                                    int64_t n_row_of, const int32_t* src_of_ws,
+                                    const float* prob_ws, int64_t n_rows, int64_t n_total,
+                                    int32_t* off, int32_t* row_of, int32_t* src_of,
+                                    float* row_prob);
 __global__ void combine_rows_kernel(const uint4* in, const int32_t* row_of, int T, int k, int H8,
                                     uint4* out);
 __global__ void dprob_reduce_kernel(const float* part, int nparts, const int32_t* row_of, int n,

@@ -187,6 +187,22 @@ __global__ void __launch_bounds__(1024) assign_rows_kernel(
   }
 }
 
+// Copies of the routing maps into caller buffers (any destination may be null).
+__global__ void __launch_bounds__(256) route_export_kernel(
+    const int32_t* __restrict__ off_ws, int n_off, const int32_t* __restrict__ row_of_ws,
+    int64_t n_row_of, const int32_t* __restrict__ src_of_ws, const float* __restrict__ prob_ws,
+    int64_t n_rows, int64_t n_total, int32_t* off, int32_t* row_of, int32_t* src_of,
+    float* row_prob) {
+  MOE_GRIDDEP_ENTRY();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_total; i += stride) {
+    if (off && i < n_off) off[i] = off_ws[i];
+    if (row_of && i < n_row_of) row_of[i] = row_of_ws[i];
+    if (src_of && i < n_rows) src_of[i] = src_of_ws[i];
+    if (row_prob && i < n_rows) row_prob[i] = prob_ws[i];
+  }
+}
+
 // x_perm[r, :] = x[src_of[r] / k, :] for rows in use, zero for padding rows and for rows at
 // or beyond offsets[E]. One block per row; 16-byte vectors.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,

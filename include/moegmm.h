@@ -179,6 +179,22 @@ moe_status_t moe_route_permute(const moe_layer_desc_t *desc, int32_t T, const fl
                                const void *x, int32_t *topk_ids, float *topk_probs,
                                int32_t *counts, void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/* The routing maps of the last moe_route_permute on ws, copied into caller buffers (device
+ * memory; [NV-blog] host-sync section: the per-expert counts and offsets stay on the device):
+ *   offsets  int32 [E+1]    padded segment starts; offsets[E] = rows in use
+ *   row_of   int32 [T*k]    permuted row of (token t, slot j) at t*k+j
+ *   src_of   int32 [R_cap]  t*k+j of a permuted row, -1 for a padding row
+ *   row_prob fp32  [R_cap]  routing probability of a permuted row, 0 for a padding row
+ * R_cap as in moe_workspace_layout; rows at or beyond offsets[E] carry no routing (their
+ * src_of / row_prob entries are left from earlier calls). Any of the four may be NULL (not
+ * copied); each one given
+ * must be 4-byte aligned. T must be the T of that moe_route_permute call, in [0, T_max]. One
+ * kernel on `stream`, no host synchronisation, graph-capturable. Returns MOE_ERR_INVALID_ARG
+ * for a bad description, workspace, T or pointer. */
+moe_status_t moe_route_export(const moe_layer_desc_t *desc, const void *ws, size_t ws_bytes,
+                              int32_t T, int32_t *offsets, int32_t *row_of, int32_t *src_of,
+                              float *row_prob, moe_stream_t stream);
+
 /* Fused grouped MLP forward ([NV-blog] kernel families 1 and 2, Figure 1; [TE-MoE]
  * GroupedLinear -> ScaledSwiGLU -> GroupedLinear):
  *   Z = X_e W1_e (FC1, grouped over experts from the device offsets), a = act(Z),
@@ -400,7 +416,8 @@ typedef enum {
   MOE_K_EXTRAS_REDUCE = 15,
   MOE_K_NVFP4_AMAX = 16,
   MOE_K_NVFP4_QUANTIZE = 17,
-  MOE_K_COUNT = 18
+  MOE_K_ROUTE_EXPORT = 18,
+  MOE_K_COUNT = 19
 } moe_kernel_id_t;
 
 /* Launch timeline, for measurement. Between moe_timeline_begin and moe_timeline_end the

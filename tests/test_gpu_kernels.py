@@ -141,6 +141,30 @@ def _route_check(cfg, logits):
     want = np.zeros((R, cfg.H), dtype=np.uint16)
     want[:used][live] = x[pm.src_of[live] // cfg.k]
     assert np.array_equal(xp, want)
+    # the same maps exported into caller tensors (moe_route_export), against the oracle
+    i32 = dict(dtype=torch.int32, device="cuda")
+    off_o = torch.full((cfg.E + 1,), -7, **i32)
+    row_o = torch.full((cfg.T * cfg.k,), -7, **i32)
+    src_o = torch.full((R,), -7, **i32)
+    prob_o = torch.full((R,), -7.0, dtype=torch.float32, device="cuda")
+    g.moe_route_export(d, L.ws, L.ws_bytes, cfg.T, off_o, row_o, src_o, prob_o)
+    torch.cuda.synchronize()
+    assert np.array_equal(off_o.cpu().numpy(), pm.offsets)
+    assert np.array_equal(row_o.cpu().numpy(), pm.row_of.ravel())
+    # rows at or beyond offsets[E] are outside the layout's contract: compare the used rows,
+    # and the rest with the workspace itself
+    src_all = src_o.cpu().numpy()
+    assert np.array_equal(src_all[:used], pm.src_of)
+    assert np.array_equal(src_all, L.ws_view("src_of", torch.int32, (R,)).cpu().numpy())
+    prob_all = prob_o.cpu().numpy()
+    assert np.array_equal(prob_all[:used], row_prob)
+    # a partial export writes only what it is given
+    row2 = torch.full((cfg.T * cfg.k,), -7, **i32)
+    src2 = torch.full((R,), -7, **i32)
+    g.moe_route_export(d, L.ws, L.ws_bytes, cfg.T, row_of=row2)
+    torch.cuda.synchronize()
+    assert np.array_equal(row2.cpu().numpy(), pm.row_of.ravel())
+    assert np.all(src2.cpu().numpy() == -7)
 
 
 @pytest.mark.parametrize("name", list(ROUTE_CASES))

@@ -209,6 +209,16 @@ def test_calls_validate_before_touching_the_device(lib):
     with pytest.raises(g.MoeError) as e:
         g.moe_selftest_gemm_timeout(bf, 256, 1 << 30, 256, 10**3, 0)
     assert e.value.status == 1
+    # route export: T within [0, T_max], 4-byte aligned destinations, a workspace
+    with pytest.raises(g.MoeError) as e:
+        g.moe_route_export(bf, 256, 1 << 30, 17, 256, 256, 256, 256, 0)
+    assert e.value.status == 1
+    with pytest.raises(g.MoeError) as e:
+        g.moe_route_export(bf, 256, 1 << 30, 8, 258, None, None, None, 0)
+    assert e.value.status == 1
+    with pytest.raises(g.MoeError) as e:
+        g.moe_route_export(bf, None, 1 << 30, 8, 256, None, None, None, 0)
+    assert e.value.status == 1
 
 
 def test_config_table_matches_workloads():

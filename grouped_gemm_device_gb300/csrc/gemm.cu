@@ -569,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               v[i] = prob * rr * rr;
             }
             if (row_ok) {
-              store_bf16x32w(zrow + t.n0 + cc, zz, p.wide);
+              if (p.out) store_bf16x32w(zrow + t.n0 + cc, zz, p.wide);  // saved Z, if kept
               store_bf16x32w(arow + t.n0 + cc, v, p.wide);
             }
           }

@@ -7,9 +7,11 @@
 //   dA_s[rows, f0..f0+127]       = dY_perm[rows] . W2_e[f0..f0+127]^T       (128 x 128)
 //   Z[rows, 2 f0 .. 2 f0 + 255]  = X_perm[rows]  . W1p_e[2 f0 .. 2 f0+255]^T (128 x 256)
 // (the packed W1 rows 2 f0 .. 2 f0 + 255 are exactly the gate and linear columns of dA_s
-// columns f0 .. f0 + 127, because the interleave divides 128). Both accumulate in TMEM
-// (columns 0-127 and 128-383); the dGLU epilogue reads dA_s and the fp32 Z from TMEM and
-// writes dZ (bf16, packed order) and the per-row d_prob partial of the tile.
+// columns f0 .. f0 + 127, because the interleave divides 128). For sReLU (not gated, N1 = F)
+// the Z tile is Z[rows, f0 .. f0 + 127] (128 x 128) and the epilogue is
+// dZ = p dA_s 2 relu(Z), d_prob += dA_s relu(Z)^2. Both accumulate in TMEM (columns 0-127
+// and from 128); the epilogue reads dA_s and the fp32 Z from TMEM and writes dZ (bf16,
+// packed order) and the per-row d_prob partial of the tile.
 //
 // CTA = 10 warps: warp 0 TMA, warp 1 TMEM owner + MMA issuer, warps 2-9 epilogue (two per
 // TMEM lane quadrant, 64 dA columns each). A stage holds the four k-blocks (dY, W2, X, W1p:
@@ -34,7 +36,7 @@ constexpr int kMaxE = 256;
 constexpr int A1_BYTES = BM * BK * 2;   // dY
 constexpr int B1_BYTES = BNA * BK * 2;  // W2 rows
 constexpr int A2_BYTES = BM * BK * 2;   // X
-constexpr int B2_BYTES = BNZ * BK * 2;  // W1p rows
+constexpr int B2_BYTES = BNZ * BK * 2;  // W1p rows (gated: 256; sReLU uses the first 128)
 constexpr int STAGE_BYTES = A1_BYTES + B1_BYTES + A2_BYTES + B2_BYTES;
 constexpr int DATA = STAGES * STAGE_BYTES;
 constexpr int SMEM_TOTAL = DATA + 4096 + 1024;
@@ -122,6 +124,9 @@ template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     fc2_dgrad_recompute_kernel(const __grid_constant__ RcArgs p) {
   MOE_GRIDDEP_ENTRY();
+  constexpr bool kGated = KIND != MOE_ACT_SRELU;
+  constexpr int ZN = kGated ? BNZ : BNA;                        // Z columns per tile
+  constexpr int kStageTx = STAGE_BYTES - (BNZ - ZN) * BK * 2;   // bytes a stage receives
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -192,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&c.empty[stage], phase ^ 1, abort, p.err)) break;
           uint8_t* s0 = smem + stage * STAGE_BYTES;
           uint64_t* bar = &c.full[stage];
-          mbar_arrive_expect_tx(bar, STAGE_BYTES);
+          mbar_arrive_expect_tx(bar, kStageTx);
 #pragma unroll
           for (int s = 0; s < STAGES; ++s)
             if (s == stage) armed[s] = (int)phase;
@@ -200,7 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(s0, &p.tmDy, bar, k0, t.m0);
           tma_load_3d(s0 + A1_BYTES, &p.tmW2, bar, k0, t.n0, t.e);
           tma_load_2d(s0 + A1_BYTES + B1_BYTES, &p.tmX, bar, k0, t.m0);
-          tma_load_3d(s0 + A1_BYTES + B1_BYTES + A2_BYTES, &p.tmW1, bar, k0, 2 * t.n0, t.e);
+          tma_load_3d(s0 + A1_BYTES + B1_BYTES + A2_BYTES, &p.tmW1, bar, k0,
+                      kGated ? 2 * t.n0 : t.n0, t.e);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -221,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDA = idesc_bf16(BM, BNA, false, false);
-      constexpr uint32_t IDZ = idesc_bf16(BM, BNZ, false, false);
+      constexpr uint32_t IDZ = idesc_bf16(BM, ZN, false, false);
       int stage = 0;
       uint32_t phase = 0;
       int acc_i = 0;
@@ -282,11 +288,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xFFFFFFFFu, got)) break;
       tc_fence_after();
       const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
-      uint16_t* dzrow = p.dz + (int64_t)row * p.N1 + 2 * t.n0;
+      uint16_t* dzrow = p.dz + (int64_t)row * p.N1 + (kGated ? 2 * t.n0 : t.n0);
       float dp = 0.f;
 #pragma unroll 1
       for (int cc = half * 64; cc < half * 64 + 64; cc += 16) {
         if (t.n0 + cc >= p.F) break;
+        if constexpr (!kGated) {
+          uint32_t da[16], z[16], dzw[8];
+          tmem_ld_32x32b_x16(tl + cc, da);
+          tmem_ld_32x32b_x16(tl + kZCol + cc, z);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float d0 = __uint_as_float(da[2 * i]), d1 = __uint_as_float(da[2 * i + 1]);
+            const float r0 = fmaxf(__uint_as_float(z[2 * i]), 0.f);
+            const float r1 = fmaxf(__uint_as_float(z[2 * i + 1]), 0.f);
+            dp += d0 * r0 * r0 + d1 * r1 * r1;
+            dzw[i] = pack_bf16x2(prob * d0 * 2.f * r0, prob * d1 * 2.f * r1);
+          }
+          if (row_ok) st16(dzrow + cc, dzw, p.wide);
+          continue;
+        }
         const int gc = (cc / ilv) * 2 * ilv + (cc % ilv);  // within the tile's 256 Z columns
         uint32_t da[16], g[16], l[16];
         tmem_ld_32x32b_x16(tl + cc, da);
@@ -332,7 +354,7 @@ cudaError_t launch_kind(const RcArgs& a, int grid, cudaStream_t s) {
 int dprob_parts_recompute(int F) { return 2 * ((F + BNA - 1) / BNA); }
 
 cudaError_t launch_fc2_dgrad_recompute(const GemmProblem& p, cudaStream_t s) {
-  if (!p.gated || (p.ilv != 32 && p.ilv != 64 && p.ilv != 128)) return cudaErrorInvalidValue;
+  if (p.gated && p.ilv != 32 && p.ilv != 64 && p.ilv != 128) return cudaErrorInvalidValue;
   RcArgs a;
   memset(&a, 0, sizeof(a));
   const uint64_t R = (uint64_t)p.R_cap;
@@ -340,7 +362,7 @@ cudaError_t launch_fc2_dgrad_recompute(const GemmProblem& p, cudaStream_t s) {
   ok &= tmap_2d(&a.tmDy, p.dy_perm, p.H, R, 64, BM);
   ok &= tmap_3d(&a.tmW2, p.w2, p.H, p.F, p.E, 64, BNA);
   ok &= tmap_2d(&a.tmX, p.x_perm, p.H, R, 64, BM);
-  ok &= tmap_3d(&a.tmW1, p.w1p, p.H, p.N1, p.E, 64, BNZ);
+  ok &= tmap_3d(&a.tmW1, p.w1p, p.H, p.N1, p.E, 64, p.gated ? BNZ : BNA);
   if (!ok) return cudaErrorInvalidValue;
   a.offsets = p.offsets;
   a.E = p.E;
@@ -361,6 +383,7 @@ cudaError_t launch_fc2_dgrad_recompute(const GemmProblem& p, cudaStream_t s) {
     case MOE_ACT_SWIGLU: return launch_kind<MOE_ACT_SWIGLU>(a, grid, s);
     case MOE_ACT_CLAMPED_SWIGLU: return launch_kind<MOE_ACT_CLAMPED_SWIGLU>(a, grid, s);
     case MOE_ACT_GEGLU: return launch_kind<MOE_ACT_GEGLU>(a, grid, s);
+    case MOE_ACT_SRELU: return launch_kind<MOE_ACT_SRELU>(a, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

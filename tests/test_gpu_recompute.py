@@ -24,6 +24,9 @@ CASES = {
                                  lin_lo=-7.0, lin_hi=7.0, lin_offset=1.0),
     "geglu_ilv128": synth.LayerConfig("rge", T=500, E=4, k=2, H=256, F=512, seed=45,
                                       activation="geglu", ilv=128),
+    # not gated (N1 = F): the Z tile is the dA tile's own 128 columns; F tail of 64
+    "srelu": synth.LayerConfig("rsr", T=600, E=5, k=2, H=384, F=448, seed=46,
+                               activation="srelu"),
 }
 
 

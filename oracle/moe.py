@@ -379,10 +379,12 @@ class Nvfp4Result:
     Z: list = field(default_factory=list)        # per expert: FC1 output, bf16-rounded
     A: list = field(default_factory=list)        # per expert: a_s, bf16-rounded
     dZ: list = field(default_factory=list)       # per expert: dZ, bf16-rounded
+    db1: np.ndarray | None = None                # [E, N1] FC1 bias gradient (with a bias)
+    ds: np.ndarray | None = None                 # [E, F] feature-scale gradient (with a scale)
 
 
 def layer_nvfp4(logits, x, W1, W2, k: int, act: ActParams, mask: int, dy=None,
-                align: int = 128) -> Nvfp4Result:
+                align: int = 128, b1=None, s=None) -> Nvfp4Result:
     """Forward (and, with dy, backward) of the expert layer with NVFP4 GEMM operands.
 
     The same layer as `layer` (R1-R9), with every GEMM consuming NVFP4 copies of its operands
@@ -402,6 +404,11 @@ def layer_nvfp4(logits, x, W1, W2, k: int, act: ActParams, mask: int, dy=None,
     expert's first row (zero rows pad the last block) and quantises down the columns. Every
     per-tensor amax is taken over the whole tensor (all experts). Weights: W1 [E, H, N1]
     logical, W2 [E, F, H]; W1's amax is shared by its two copies, W2's likewise.
+    Optional epilogue extras, as in `expert_forward` / `expert_backward` (reading R13): b1
+    [E, N1] logical [gate | linear] FC1 bias added to Z before it is saved, s [E, F] a
+    per-feature scale of the activation (a_s = p * (a * s); d_prob = sum_f dA_s * s * a;
+    dA = p * s * dA_s), with db1 = sum over an expert's rows of dZ (the unrounded dact
+    output) and ds = sum over its rows of p * dA_s * a.
     """
     from . import nvfp4 as nv
 
@@ -423,10 +430,13 @@ def layer_nvfp4(logits, x, W1, W2, k: int, act: ActParams, mask: int, dy=None,
     for e in range(E):
         tok, _ = segs[e]
         Ze = xq[tok] @ nv.fake_quant(W1[e], 0, S("w1"))
+        if b1 is not None:
+            Ze = Ze + np.asarray(b1[e], dtype=np.float64)[None, :]
         ae = act_forward(act, Ze[:, :F], Ze[:, F:]) if act.gated else act_forward(act, Ze)
         acts.append(ae)
         res.Z.append(bf16_round(Ze))
-        res.A.append(bf16_round(Ps[e][:, None] * ae))
+        sa = ae * np.asarray(s[e], dtype=np.float64)[None, :] if s is not None else ae
+        res.A.append(bf16_round(Ps[e][:, None] * sa))
     am["a"] = max([nv.amax(a) for a in res.A] + [0.0])
     am["at"] = nv.rht_amax_segments(res.A, mask)
     for e in range(E):
@@ -446,11 +456,16 @@ def layer_nvfp4(logits, x, W1, W2, k: int, act: ActParams, mask: int, dy=None,
     res.d_probs = np.zeros((T, k))
     res.dW1 = np.zeros((E,) + W1.shape[1:])
     res.dW2 = np.zeros((E,) + W2.shape[1:])
+    if b1 is not None:
+        res.db1 = np.zeros((E, W1.shape[2]))
+    if s is not None:
+        res.ds = np.zeros((E, F))
     for e in range(E):
         tok, slot = segs[e]
         dA_s = dyq[tok] @ nv.fake_quant(W2[e], 1, S("w2")).T
-        res.d_probs[tok, slot] = (dA_s * acts[e]).sum(axis=1)
-        dA = Ps[e][:, None] * dA_s
+        se = np.asarray(s[e], dtype=np.float64)[None, :] if s is not None else 1.0
+        res.d_probs[tok, slot] = (dA_s * se * acts[e]).sum(axis=1)
+        dA = Ps[e][:, None] * (dA_s * se)
         Zb = res.Z[e]
         if act.gated:
             dg, dl = act_backward(act, Zb[:, :F], Zb[:, F:], dA)
@@ -458,6 +473,10 @@ def layer_nvfp4(logits, x, W1, W2, k: int, act: ActParams, mask: int, dy=None,
         else:
             dZe, _ = act_backward(act, Zb, None, dA)
         res.dZ.append(bf16_round(dZe))
+        if b1 is not None:
+            res.db1[e] = dZe.sum(axis=0)
+        if s is not None:
+            res.ds[e] = (Ps[e][:, None] * dA_s * acts[e]).sum(axis=0)
     am["dz"] = max([nv.amax(d) for d in res.dZ] + [0.0])
     am["dzt"] = nv.rht_amax_segments(res.dZ, mask)
     at_q = nv.colwise_rht_segments(res.A, mask, S("at"))

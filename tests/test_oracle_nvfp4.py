@@ -236,6 +236,66 @@ def test_layer_without_quantisers_is_the_bf16_oracle(monkeypatch, kind, skew):
         assert np.allclose(a, b, rtol=1e-10, atol=1e-10)
 
 
+@pytest.mark.parametrize("kind", ["swiglu", "clamped_swiglu", "geglu"])
+def test_layer_extras_without_quantisers_are_the_bf16_oracles(monkeypatch, kind):
+    """The epilogue extras (FC1 bias, feature scale) with the quantisers and roundings taken
+    out: the layer and both extras gradients equal the plain oracle's, whose extras are
+    pinned against autograd (test_oracle_moe)."""
+    lg, x, W1, W2, dy, k = _small_layer(seed=12)
+    E, F = W1.shape[0], W2.shape[1]
+    rng = np.random.default_rng(13)
+    b1 = 0.3 * rng.standard_normal((E, 2 * F))
+    s = rng.uniform(0.5, 1.5, size=(E, F))
+    act = _ACTS[kind]
+    monkeypatch.setattr(nv, "fake_quant", lambda v, axis, S: np.asarray(v, dtype=np.float64))
+    monkeypatch.setattr(nv, "to_f32", lambda v: np.asarray(v, dtype=np.float64))
+    monkeypatch.setattr(om, "bf16_round", lambda v: np.asarray(v, dtype=np.float64))
+    got = om.layer_nvfp4(lg, x, W1, W2, k, act, 0x3C5A, dy=dy, b1=b1, s=s)
+    ref = om.layer(lg, x, W1, W2, k, act, dy=dy, b1=b1, s=s)
+    dW1, dW2 = om.stack_weight_grads(ref, E)
+    for a, b in [(got.y, ref.y), (got.dx, ref.dx), (got.dW1, dW1), (got.dW2, dW2),
+                 (got.d_probs, ref.d_probs), (got.db1, ref.db1), (got.ds, ref.ds)]:
+        assert np.allclose(a, b, rtol=1e-10, atol=1e-10)
+
+
+def test_layer_extras_neutral_values_and_power_of_two_scale():
+    """With the quantisers in place: a zero bias and a unit scale change nothing, bit for bit;
+    a feature scale of 2 doubles a_s, y, dZ, dx, both weight gradients and d_prob exactly
+    (each NVFP4 encode scale halves with its amax, so every code stays the same) and leaves
+    Z and ds unchanged."""
+    lg, x, W1, W2, dy, k = _small_layer(seed=14)
+    E, F = W1.shape[0], W2.shape[1]
+    act = om.ActParams()
+    base = om.layer_nvfp4(lg, x, W1, W2, k, act, 0x0F0F, dy=dy)
+    zero = om.layer_nvfp4(lg, x, W1, W2, k, act, 0x0F0F, dy=dy, b1=np.zeros((E, 2 * F)),
+                          s=np.ones((E, F)))
+    for a, b in [(zero.y, base.y), (zero.dx, base.dx), (zero.dW1, base.dW1),
+                 (zero.dW2, base.dW2), (zero.d_probs, base.d_probs)]:
+        assert np.array_equal(a, b)
+    two = om.layer_nvfp4(lg, x, W1, W2, k, act, 0x0F0F, dy=dy, s=np.full((E, F), 2.0))
+    for a, b in [(two.y, base.y), (two.dx, base.dx), (two.dW1, base.dW1),
+                 (two.dW2, base.dW2), (two.d_probs, base.d_probs)]:
+        assert np.array_equal(a, 2.0 * b)
+    for e in range(E):
+        assert np.array_equal(two.Z[e], base.Z[e])
+        assert np.array_equal(two.A[e], 2.0 * base.A[e])
+        assert np.array_equal(two.dZ[e], 2.0 * base.dZ[e])
+    assert np.array_equal(two.ds, zero.ds)
+
+
+def test_layer_bias_enters_the_saved_fc1_output():
+    """With W1 = 0 the FC1 output is the bias alone: every row of an expert's saved Z is its
+    bias (rounded to bf16), in logical [gate | linear] order."""
+    lg, x, W1, W2, dy, k = _small_layer(seed=15)
+    E, F = W1.shape[0], W2.shape[1]
+    b1 = om.bf16_round(np.random.default_rng(16).standard_normal((E, 2 * F)))
+    r = om.layer_nvfp4(lg, x, np.zeros_like(W1), W2, k, om.ActParams(), 0x1111, dy=dy, b1=b1)
+    for e in range(E):
+        if len(r.Z[e]):
+            assert np.array_equal(r.Z[e], np.broadcast_to(b1[e], r.Z[e].shape))
+    assert r.db1 is not None and r.ds is None
+
+
 def test_layer_error_is_the_size_of_nvfp4_quantisation_noise():
     lg, x, W1, W2, dy, k = _small_layer(seed=9)
     act = om.ActParams()

@@ -154,11 +154,9 @@ static moe_status_t validate_desc(const moe_layer_desc_t* d) {
   if (d->reuse_weights != 0 && d->reuse_weights != 1)
     return fail(MOE_ERR_INVALID_ARG, "reuse_weights must be 0 or 1");
   if (d->pdl != 0 && d->pdl != 1) return fail(MOE_ERR_INVALID_ARG, "pdl must be 0 or 1");
-  if (d->extras && (d->precision == MOE_PREC_NVFP4 || d->activation == MOE_ACT_SRELU ||
-                    d->recompute))
+  if (d->extras && (d->activation == MOE_ACT_SRELU || d->recompute))
     return fail(MOE_ERR_UNSUPPORTED,
-                "epilogue extras need a BF16 or MXFP8 layer with a gated activation, no "
-                "recompute");
+                "epilogue extras need a gated activation and no recompute");
   if (r_cap(d) > (int64_t)INT32_MAX / 2) return fail(MOE_ERR_UNSUPPORTED, "row capacity too large");
   if (d->precision != MOE_PREC_BF16 &&
       (int64_t)d->E * round128(n1_of(d)) * d->H > (int64_t)INT32_MAX * 8)
@@ -615,7 +613,10 @@ static moe_status_t fwd_impl(const moe_layer_desc_t* d, int32_t T, const void* w
     m.role = ROLE_FC1_FPROP;
     m.out = w.at<void>(w.L.z);
     m.out2 = w.at<void>(w.L.a_s);
+    m.fc1_bias = fc1_bias;
+    m.fscale = feat_scale;
     if ((e = launch_grouped_gemm_fp4(m, s)) != cudaSuccess) return cuda_fail(e, "FC1 FP4 GEMM");
+    m.fc1_bias = m.fscale = nullptr;
     if (!nv_quantize(w.at<void>(w.L.a_s), w.L.R_cap, d->F, w.L.R_cap, w.L.R_cap, live, m, AM_A,
                      AM_AT, m.a, m.at, 1, s))
       return fail(MOE_ERR_CUDA, "NVFP4 quantiser: tensor map or shared-memory limit");
@@ -780,7 +781,17 @@ static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* d
     m.role = ROLE_FC2_DGRAD;
     m.out = w.at<void>(w.L.dz);
     m.dprob_part = w.at<float>(w.L.dprob_part);
+    if (d->extras) {
+      m.fscale = feat_scale;
+      m.ext_part = w.at<float>(w.L.ext_part);
+    }
     if ((e = launch_grouped_gemm_fp4(m, s)) != cudaSuccess) return cuda_fail(e, "FC2 dgrad FP4");
+    m.fscale = nullptr;
+    m.ext_part = nullptr;
+    if (d->extras) {
+      if ((e = launch_extras_reduce(d, w, d_fc1_bias, d_feat_scale, s)) != cudaSuccess)
+        return cuda_fail(e, "extras reduce");
+    }
     if (T > 0) {
       const int n = T * d->k;
       launch_kernel(dprob_reduce_kernel, grid_for((n + 255) / 256, 4), 256, 0, s, nullptr, 0, 

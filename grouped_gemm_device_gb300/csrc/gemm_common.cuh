@@ -145,6 +145,25 @@ MOE_DEVICE float warp_colsum32(float (&v)[32], int lane) {
   return v[0];
 }
 
+// Column sums of a warp's 32 rows (lane = row) for 16 columns: lanes l and l + 16 both
+// return the sum of column l % 16 (the two half-warps are added first, then the same
+// transpose-reduce as warp_colsum32 over the 16 columns).
+MOE_DEVICE float warp_colsum16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] += __shfl_xor_sync(0xFFFFFFFFu, v[i], 16);
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {
+    const bool hi = lane & w;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = hi ? v[i] : v[i + w];
+      const float keep = hi ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, w);
+    }
+  }
+  return v[0];
+}
+
 // 32 bytes at a 32-byte aligned global address, not allocated in L1.
 MOE_DEVICE void ld_v8_noalloc(const void* src, uint32_t (&w)[8]) {
   asm volatile("ld.global.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"

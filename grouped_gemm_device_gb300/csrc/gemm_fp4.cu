@@ -111,6 +111,12 @@ struct Fp4Args {
   int wide;                            // STORE: out is 32-byte aligned (256-bit stores)
   ActDev act;
   int* err;
+  // EXT kernels: FC1 bias [E, N1] (logical [gate | linear] order), feature scale [E, F], and
+  // the dGLU's per-32-row column sums of dZ and of p * dA_s * a into ext_part [., N1 + F]
+  const float* fc1_bias;
+  const float* fscale;
+  float* ext_part;
+  int F, N1;
 };
 
 struct Ctrl {
@@ -235,10 +241,11 @@ MOE_DEVICE float rht_amax_tile32(uint32_t* xt, const uint32_t (&w)[16], uint32_t
 // ILV linear columns).
 MOE_DEVICE int gate_col(int f) { return ((f & ~(ILV - 1)) << 1) | (f & (ILV - 1)); }
 
-template <int EPI, int KIND, bool KG>
+template <int EPI, int KIND, bool KG, bool EXT = false>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __grid_constant__ Fp4Args p) {
   MOE_GRIDDEP_ENTRY();
   constexpr bool kGated = KIND != MOE_ACT_SRELU;
+  static_assert(!EXT || (kGated && EPI != EPI_STORE), "extras: gated GLU / dGLU epilogues");
   using L = Fp4Cfg<EPI>;
   constexpr int BN = L::BN;
   constexpr int NACC = L::NACC;
@@ -517,6 +524,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
         __syncwarp();
         if (lane == 0) mbar_arrive(&c.tempty[acc]);
         ++acc_i;
+        if constexpr (EXT) {
+          // the bias joins Z before the activation (and is part of the saved Z); packed
+          // column n0 + cb + c has logical column (block / 2) ILV + c % ILV (+ F if linear)
+          if (p.fc1_bias) {
+            const float* b = p.fc1_bias + (int64_t)t.e * p.N1;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+              const int pc = t.n0 + cb + c;
+              const int blk = pc / ILV;
+              const int lc = (blk >> 1) * ILV + pc % ILV + ((blk & 1) ? p.F : 0);
+              if (pc < p.N) acc_r[c] += b[lc];
+            }
+          }
+        }
         uint16_t* zout = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo + t.n0 + cb;
 #pragma unroll
         for (int j = 0; j < 4; ++j)  // the saved Z (bf16)
@@ -538,6 +559,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
             } else {
               const float rr = fmaxf(acc_r[g_off + i], 0.f);
               a = rr * rr;
+            }
+            if constexpr (EXT) {
+              if (p.fscale) a *= p.fscale[(int64_t)t.e * p.F + acol + i];
             }
             v[i] = bf16_lo(pack_bf16x2(prob * a, 0.f));
           }
@@ -585,6 +609,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
           }
           tmem_ld_wait();
           uint32_t w[16];  // dG pairs in w[0..7], dL pairs in w[8..15]
+          // extras: this row's dG, dL and p * dA_s * a for the column sums
+          float xg[EXT ? 16 : 1], xl[EXT ? 16 : 1], xs[EXT ? 16 : 1];
 #pragma unroll
           for (int i = 0; i < 16; i += 2) {
             float dg[2], dl[2] = {0.f, 0.f};
@@ -592,7 +618,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
             for (int u = 0; u < 2; ++u) {
               const float d = alpha * __uint_as_float(dr[i + u]);
               const float g = u ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
-              if constexpr (kGated) {
+              if constexpr (EXT) {
+                // the feature scale s enters as dA = p * s * dA_s and d_prob += dA_s * s * a
+                const float l = u ? bf16_hi(lw[i >> 1]) : bf16_lo(lw[i >> 1]);
+                const float sc = p.fscale ? p.fscale[(int64_t)t.e * p.F + f0 + i + u] : 1.f;
+                const float a = act_bwd_k<KIND>(p.act, g, l, prob * sc * d, dg[u], dl[u]);
+                dp += d * sc * a;
+                xg[i + u] = dg[u];
+                xl[i + u] = dl[u];
+                xs[i + u] = prob * d * a;
+              } else if constexpr (kGated) {
                 const float l = u ? bf16_hi(lw[i >> 1]) : bf16_lo(lw[i >> 1]);
                 dp += d * act_bwd_k<KIND>(p.act, g, l, prob * d, dg[u], dl[u]);
               } else {
@@ -608,6 +643,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
           for (int i = 0; i < 16; ++i)
             m_out = fmaxf(m_out, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
           st_global_v8(dzrow + gc, w);
+          if constexpr (EXT) {
+            // column sums over the warp's 32 rows (one expert's: segments are 128-row
+            // aligned) into the row group's partials: gate column f at f, linear at F + f,
+            // scale at N1 + f
+            float* part = p.ext_part + (int64_t)(row0 >> 5) * (p.N1 + p.F);
+            const float sg = warp_colsum16(xg, lane);
+            const float sl = warp_colsum16(xl, lane);
+            const float ss = warp_colsum16(xs, lane);
+            if (lane < 16) {
+              part[f0 + lane] = sg;
+              part[p.F + f0 + lane] = sl;
+              part[p.N1 + f0 + lane] = ss;
+            }
+          }
           if constexpr (kGated) {
             st_global_v8(dzrow + gc + ILV, w + 8);
             m_rht = fmaxf(m_rht, rht_amax_tile32(xt, w, p.rht_mask, lane));
@@ -650,9 +699,9 @@ bool tmap_fp4(CUtensorMap* m, const MxOperand& t) {
   return make_tmap(m, t.q, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8);
 }
 
-template <int EPI, int KIND, bool KG>
+template <int EPI, int KIND, bool KG, bool EXT = false>
 cudaError_t launch_fp4(const Fp4Args& a, int grid, cudaStream_t s, int kid) {
-  auto kern = grouped_gemm_fp4_kernel<EPI, KIND, KG>;
+  auto kern = grouped_gemm_fp4_kernel<EPI, KIND, KG, EXT>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), Fp4Cfg<EPI>::TOTAL);
   if (e != cudaSuccess) return e;
   launch_kernel(kern, grid, kThreads, Fp4Cfg<EPI>::TOTAL, s, nullptr, 0, a);
@@ -662,6 +711,15 @@ cudaError_t launch_fp4(const Fp4Args& a, int grid, cudaStream_t s, int kid) {
 
 template <int EPI>
 cudaError_t launch_act_family(const Fp4Args& a, int kind, int grid, cudaStream_t s, int kid) {
+  if (a.fc1_bias || a.fscale || a.ext_part) {  // extras: gated activations only
+    switch (kind) {
+      case MOE_ACT_SWIGLU: return launch_fp4<EPI, MOE_ACT_SWIGLU, false, true>(a, grid, s, kid);
+      case MOE_ACT_CLAMPED_SWIGLU:
+        return launch_fp4<EPI, MOE_ACT_CLAMPED_SWIGLU, false, true>(a, grid, s, kid);
+      case MOE_ACT_GEGLU: return launch_fp4<EPI, MOE_ACT_GEGLU, false, true>(a, grid, s, kid);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (kind) {
     case MOE_ACT_SWIGLU: return launch_fp4<EPI, MOE_ACT_SWIGLU, false>(a, grid, s, kid);
     case MOE_ACT_CLAMPED_SWIGLU:
@@ -694,6 +752,8 @@ cudaError_t launch_grouped_gemm_fp4(const Fp4Problem& p, cudaStream_t s) {
   a.err = p.err;
   a.row_prob = p.row_prob;
   a.rht_mask = p.rht_mask;
+  a.F = p.F;
+  a.N1 = p.N1;
   const int H = p.H, F = p.F, N1 = p.N1;
   const MxOperand *A = nullptr, *B = nullptr;
   int grid = p.num_ctas;
@@ -705,6 +765,7 @@ cudaError_t launch_grouped_gemm_fp4(const Fp4Problem& p, cudaStream_t s) {
       a.out2 = p.out2; a.ldo2 = F;
       a.amax_a = p.amax + AM_X; a.amax_b = p.amax + AM_W1;
       a.amax_out = p.amax + AM_A; a.amax_out_rht = p.amax + AM_AT;
+      a.fc1_bias = p.fc1_bias; a.fscale = p.fscale;
       break;
     case ROLE_FC2_FPROP:  // a_s x W2^T copy ([H, E*Fp]), K = F
       A = &p.a; B = &p.w2t;
@@ -720,6 +781,7 @@ cudaError_t launch_grouped_gemm_fp4(const Fp4Problem& p, cudaStream_t s) {
       a.dprob_part = p.dprob_part; a.nparts = dprob_parts_fp4(F);
       a.amax_a = p.amax + AM_DY; a.amax_b = p.amax + AM_W2;
       a.amax_out = p.amax + AM_DZ; a.amax_out_rht = p.amax + AM_DZT;
+      a.fscale = p.fscale; a.ext_part = p.ext_part;
       break;
     case ROLE_FC1_DGRAD:  // dZ x W1^T copy ([H, E*N1p]), K = N1
       A = &p.dz; B = &p.w1t;

@@ -255,6 +255,11 @@ struct Fp4Problem {
   ActDev act;
   int* err;
   int num_ctas;
+  // epilogue extras (gated; NULL when absent): FC1 bias [E, N1] logical order, feature scale
+  // [E, F]; FC2 dgrad writes per-32-row column sums into ext_part [R_cap/32, N1 + F]
+  const float* fc1_bias;
+  const float* fscale;
+  float* ext_part;
 };
 int dprob_parts_fp4(int F);
 cudaError_t launch_grouped_gemm_fp4(const Fp4Problem& p, cudaStream_t s);

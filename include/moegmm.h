@@ -108,8 +108,8 @@ typedef struct {
                          activation; 0 otherwise                                          */
   int32_t extras;     /* epilogue extras ([NV-blog] GLU-epilogue section: bias-vector addition
                          and feature scaling): bit 0 FC1 bias, bit 1 per-feature scale of the
-                         activation output; used through the _ex entry points. BF16 or MXFP8
-                         with a gated activation, without recompute; 0 otherwise            */
+                         activation output; used through the _ex entry points. Any
+                         precision with a gated activation, without recompute; 0 otherwise */
   uint32_t rht_mask;  /* NVFP4: signs of the 16-point random Hadamard rotation applied along
                          the tokens to the weight-gradient operands (bit j set: the j-th row
                          of each 16-row block is negated before H16 / 4); drawn once by the
@@ -244,9 +244,9 @@ moe_status_t moe_grouped_mlp_bwd(const moe_layer_desc_t *desc, int32_t T, const 
  *   d_feat_scale fp32 [E, F]  out (bit 1; NULL otherwise)
  * Other arguments as moe_grouped_mlp_fwd / moe_grouped_mlp_bwd, which return
  * MOE_ERR_UNSUPPORTED for a layer with extras. The backward needs no bias (Z includes it).
- * BF16 and MXFP8 layers with a gated activation; in MXFP8 the scaled activation is what the
- * FC1 epilogue quantises, and the dGLU epilogue takes the two column sums before dZ's
- * quantisation, from the fp32 values. */
+ * Layers with a gated activation (BF16, MXFP8, NVFP4); in MXFP8 the scaled activation is
+ * what the FC1 epilogue quantises, in NVFP4 what it emits in BF16 (with its amaxes), and the
+ * dGLU epilogue takes the two column sums from the fp32 values, before dZ is rounded. */
 moe_status_t moe_grouped_mlp_fwd_ex(const moe_layer_desc_t *desc, int32_t T,
                                     const void *w1_packed, const void *w2,
                                     const float *fc1_bias, const float *feat_scale, void *y,

@@ -1,8 +1,8 @@
 """GPU parity of the epilogue extras (an FC1 bias added before the activation and a
 per-feature scale of the activation output, with their gradients) against the fp64 oracle,
-through moe_grouped_mlp_fwd_ex / moe_grouped_mlp_bwd_ex, for BF16 and MXFP8 layers. Bar:
-relative Frobenius error <= 5e-3 (BF16) / 3e-2 (MXFP8) per output tensor, as for the plain
-layers."""
+through moe_grouped_mlp_fwd_ex / moe_grouped_mlp_bwd_ex, for BF16, MXFP8 and NVFP4 layers.
+Bar: relative Frobenius error <= 5e-3 (BF16) / 3e-2 (MXFP8) / 1e-2 (NVFP4, against the
+NVFP4 oracle) per output tensor, as for the plain layers."""
 import numpy as np
 import pytest
 import torch
@@ -45,17 +45,39 @@ MX_CASES = {
 }
 
 
+NV = dict(precision="nvfp4", align=128)
+NV_CASES = {
+    "nv_swiglu": synth.LayerConfig("xnv", T=300, E=4, k=2, H=256, F=256, seed=81, **NV),
+    # ragged: F = 320 (a 256 + 64 split of the dGLU's 128-column tiles), several k-blocks
+    "nv_geglu": synth.LayerConfig("xng", T=260, E=4, k=2, H=576, F=320, seed=82,
+                                  activation="geglu", **NV),
+    # skewed routing with empty experts
+    "nv_clamped": synth.LayerConfig("xnc", T=300, E=64, k=4, H=256, F=256, seed=83,
+                                    zipf_s=1.5, activation="clamped_swiglu", beta=1.702,
+                                    gate_max=7.0, lin_lo=-7.0, lin_hi=7.0, lin_offset=1.0,
+                                    **NV),
+}
+NV_TOL = 1e-2
+
+
 def run_extras(cfg, extras):
     inp = Inputs(cfg)
     b1 = synth.gen_fc1_bias(cfg) if extras & g.EXTRA_BIAS else None
     sc = synth.gen_feat_scale(cfg) if extras & g.EXTRA_SCALE else None
     mx = cfg.precision == "mxfp8"
-    tol = MX_TOL if mx else BF16_TOL
-    ref = om.layer(inp.logits, om.bf16_to_f64(inp.x), om.bf16_to_f64(inp.w1),
-                   om.bf16_to_f64(inp.w2), cfg.k, act_params(cfg), mx=mx, align=cfg.align,
-                   dy=om.bf16_to_f64(inp.dy),
-                   b1=None if b1 is None else b1.astype(np.float64),
-                   s=None if sc is None else sc.astype(np.float64))
+    nv = cfg.precision == "nvfp4"
+    tol = MX_TOL if mx else NV_TOL if nv else BF16_TOL
+    b64 = None if b1 is None else b1.astype(np.float64)
+    s64 = None if sc is None else sc.astype(np.float64)
+    if nv:
+        ref = om.layer_nvfp4(inp.logits, om.bf16_to_f64(inp.x), om.bf16_to_f64(inp.w1),
+                             om.bf16_to_f64(inp.w2), cfg.k, act_params(cfg),
+                             synth.gen_rht_mask(cfg), dy=om.bf16_to_f64(inp.dy),
+                             align=cfg.align, b1=b64, s=s64)
+    else:
+        ref = om.layer(inp.logits, om.bf16_to_f64(inp.x), om.bf16_to_f64(inp.w1),
+                       om.bf16_to_f64(inp.w2), cfg.k, act_params(cfg), mx=mx, align=cfg.align,
+                       dy=om.bf16_to_f64(inp.dy), b1=b64, s=s64)
     layer = g.MoELayer(g.desc_from_config(cfg, extras=extras))
     w1p = g.pack_w1(bf16_dev(inp.w1), gated=True, ilv=cfg.ilv)
     w2 = bf16_dev(inp.w2)
@@ -72,7 +94,10 @@ def run_extras(cfg, extras):
     errs = {"y": rel_fro(to_np(y), ref.y), "dx": rel_fro(to_np(dx), ref.dx),
             "d_probs": rel_fro(to_np(dp), ref.d_probs)}
     dw1, dw2 = to_np(dw1), to_np(dw2)
-    for e in range(cfg.E):
+    if nv:  # the NVFP4 oracle returns stacked weight gradients (zeros for empty experts)
+        errs["dW1"] = rel_fro(dw1, ref.dW1)
+        errs["dW2"] = rel_fro(dw2, ref.dW2)
+    for e in range(cfg.E if not nv else 0):
         if ref.perm.counts[e] == 0:
             continue
         errs[f"dW1[{e}]"] = rel_fro(dw1[e], ref.dW1[e])
@@ -106,8 +131,18 @@ def test_mx_each_extra_alone_matches_oracle(lib, extras):
     run_extras(MX_CASES["mx_tails"], extras)
 
 
-@pytest.mark.parametrize("cfg", [CASES["skewed"], MX_CASES["mx_skewed"]],
-                         ids=["bf16", "mxfp8"])
+@pytest.mark.parametrize("name", list(NV_CASES))
+def test_nvfp4_bias_and_feature_scale_match_oracle(lib, name):
+    run_extras(NV_CASES[name], g.EXTRA_BIAS | g.EXTRA_SCALE)
+
+
+@pytest.mark.parametrize("extras", [g.EXTRA_BIAS, g.EXTRA_SCALE])
+def test_nvfp4_each_extra_alone_matches_oracle(lib, extras):
+    run_extras(NV_CASES["nv_geglu"], extras)
+
+
+@pytest.mark.parametrize("cfg", [CASES["skewed"], MX_CASES["mx_skewed"],
+                                 NV_CASES["nv_clamped"]], ids=["bf16", "mxfp8", "nvfp4"])
 def test_empty_expert_extras_gradients_are_zero(lib, cfg):
     layer, ref = run_extras(cfg, g.EXTRA_BIAS | g.EXTRA_SCALE)
     empty = np.nonzero(ref.perm.counts == 0)[0]

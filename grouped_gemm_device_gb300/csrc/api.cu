@@ -146,10 +146,8 @@ static moe_status_t validate_desc(const moe_layer_desc_t* d) {
   if (d->sm_margin < 0) return fail(MOE_ERR_INVALID_ARG, "sm_margin must be >= 0");
   if (d->recompute != 0 && d->recompute != 1)
     return fail(MOE_ERR_INVALID_ARG, "recompute must be 0 or 1");
-  if (d->recompute && (d->precision == MOE_PREC_NVFP4 ||
-                       (d->precision == MOE_PREC_MXFP8 && d->activation == MOE_ACT_SRELU)))
-    return fail(MOE_ERR_UNSUPPORTED,
-                "recompute needs a BF16 layer, or an MXFP8 layer with a gated activation");
+  if (d->recompute && d->precision == MOE_PREC_NVFP4)
+    return fail(MOE_ERR_UNSUPPORTED, "recompute needs a BF16 or MXFP8 layer");
   if (d->extras & ~3) return fail(MOE_ERR_INVALID_ARG, "extras has unknown bits");
   if (d->reuse_weights != 0 && d->reuse_weights != 1)
     return fail(MOE_ERR_INVALID_ARG, "reuse_weights must be 0 or 1");

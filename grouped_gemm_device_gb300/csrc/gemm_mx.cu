@@ -935,7 +935,8 @@ int dprob_parts_mx(int F) { return 2 * ((F + BN - 1) / BN); }
 //   dA_s[rows, f0..f0+127]      = Q(dY)[rows] . Q_H(W2)[f0..f0+127]^T        (128 x 128)
 //   Z[rows, 2f0 .. 2f0+255]     = Q(X)[rows]  . Q_H(W1p)[2f0 .. 2f0+255]^T   (128 x 256)
 // (the packed W1 rows 2f0.. are the gate and linear columns of dA_s columns f0.., the
-// interleave dividing 128). TMEM: dA_s in columns 0-127, Z in 128-383, the stages' scale
+// interleave dividing 128; sReLU, not gated: Z[rows, f0..f0+127], a 128 x 128 GEMM with one
+// W1 box and scale slab). TMEM: dA_s in columns 0-127, Z from 128 (to 383), the stages' scale
 // factors from 384 (20 columns a stage). A stage holds four 128-byte k-blocks (80 KB) and
 // their scale slabs; two stages. The dGLU epilogue reads dA_s and Z in fp32 straight from
 // TMEM and writes dZ as row-wise and column-wise MXFP8 plus the per-row d_prob partials, like
@@ -993,6 +994,10 @@ template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     fc2_dgrad_recompute_mx_kernel(const __grid_constant__ RcMxArgs p) {
   MOE_GRIDDEP_ENTRY();
+  constexpr bool kGated = KIND != MOE_ACT_SRELU;
+  constexpr int ZN = kGated ? RC_BNZ : RC_BNA;  // Z columns per tile
+  // bytes a stage receives: sReLU loads one 128-row W1 box and one 512-byte W1 scale slab
+  constexpr uint32_t kStageTx = RC_STAGE + RC_SF - (kGated ? 0 : 128 * BK + 512);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -1072,13 +1077,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
         int e, m0, n0;
         decode(tile, e, m0, n0);
-        const int w2_row = e * p.Fp + n0, w1_row = e * p.N1p + 2 * n0;
+        const int w2_row = e * p.Fp + n0, w1_row = e * p.N1p + (kGated ? 2 * n0 : n0);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&c.empty[stage], phase ^ 1, abort, p.err)) break;
           uint8_t* s0 = smem + stage * RC_STAGE;
           uint8_t* sf = smem + RC_SF_OFF + stage * RC_SF;
           uint64_t* bar = &c.full[stage];
-          mbar_arrive_expect_tx(bar, RC_STAGE + RC_SF);
+          mbar_arrive_expect_tx(bar, kStageTx);
 #pragma unroll
           for (int s = 0; s < RC_STAGES; ++s)
             if (s == stage) armed[s] = (int)phase;
@@ -1087,12 +1092,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(s0 + RC_A1, &p.tmW2, bar, k0, w2_row);
           tma_load_2d(s0 + RC_A1 + RC_B1, &p.tmX, bar, k0, m0);
           tma_load_2d(s0 + RC_A1 + RC_B1 + RC_A2, &p.tmW1, bar, k0, w1_row);
-          tma_load_2d(s0 + RC_A1 + RC_B1 + RC_A2 + 128 * BK, &p.tmW1, bar, k0, w1_row + 128);
+          if (kGated) tma_load_2d(s0 + RC_A1 + RC_B1 + RC_A2 + 128 * BK, &p.tmW1, bar, k0, w1_row + 128);
           const int64_t kg = kb;  // k-block index = group of four 32-element scale blocks
           bulk_load(sf, p.sf_dy + (kg * p.pad_dy + m0) * 4, 512, bar);
           bulk_load(sf + 512, p.sf_w2 + (kg * p.pad_w2 + w2_row) * 4, 512, bar);
           bulk_load(sf + 1024, p.sf_x + (kg * p.pad_x + m0) * 4, 512, bar);
-          bulk_load(sf + 1536, p.sf_w1 + (kg * p.pad_w1 + w1_row) * 4, 1024, bar);
+          bulk_load(sf + 1536, p.sf_w1 + (kg * p.pad_w1 + w1_row) * 4, kGated ? 1024 : 512, bar);
           if (++stage == RC_STAGES) {
             stage = 0;
             phase ^= 1;
@@ -1134,7 +1139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_cp_32x128b_warpx4(t_sf + 4, smem_desc_noswizzle(sf + 512, 0, 128));    // W2
           tmem_cp_32x128b_warpx4(t_sf + 8, smem_desc_noswizzle(sf + 1024, 0, 128));   // X
           tmem_cp_32x128b_warpx4(t_sf + 12, smem_desc_noswizzle(sf + 1536, 0, 128));  // W1
-          tmem_cp_32x128b_warpx4(t_sf + 16, smem_desc_noswizzle(sf + 2048, 0, 128));
+          if (kGated) tmem_cp_32x128b_warpx4(t_sf + 16, smem_desc_noswizzle(sf + 2048, 0, 128));
           const int rem = p.H - kb * BK;
           const int nsub = rem >= BK ? BK / MMA_K : (rem + MMA_K - 1) / MMA_K;
           for (int ks = 0; ks < nsub; ++ks) {
@@ -1144,7 +1149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         idesc_mxf8(BM, RC_BNA, ks), t_sf, t_sf + 4, acc);
             mma_mxf8_ss(tmem_base + RC_ZCOL, smem_desc_sw128(sA2 + ks * MMA_K, 16, 1024),
                         smem_desc_sw128(sB2 + ks * MMA_K, 16, 1024),
-                        idesc_mxf8(BM, RC_BNZ, ks), t_sf + 8, t_sf + 12, acc);
+                        idesc_mxf8(BM, ZN, ks), t_sf + 8, t_sf + 12, acc);
           }
           issued_any = true;
           mma_commit(&c.empty[stage]);
@@ -1188,6 +1193,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 2; ++j) {
         const int cc = half * 64 + 32 * j;  // dA_s column within the tile
         if (n0 + cc >= p.F) break;
+        if constexpr (!kGated) {
+          // sReLU: dZ = p dA_s 2 relu(Z), d_prob += dA_s relu(Z)^2; dZ column = dA column
+          float dz[32];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t da[16], z[16];
+            tmem_ld_32x32b_x16(tl + cc + 16 * h, da);
+            tmem_ld_32x32b_x16(tl + RC_ZCOL + cc + 16 * h, z);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float d = __uint_as_float(da[i]);
+              const float rr = fmaxf(__uint_as_float(z[i]), 0.f);
+              dp += d * rr * rr;
+              dz[16 * h + i] = prob * d * 2.f * rr;
+            }
+          }
+          const int col = n0 + cc;
+          mx_row_block(dz, qr + col, p.s_row + sf_mma_offset(row, col / 32, p.s_row_pad));
+          mx_col_block(dz, xs, qc + col, p.s_col, col, row0 / 32, p.s_col_pad, lane);
+          continue;
+        }
         const int gc = (cc / p.ilv) * 2 * p.ilv + (cc % p.ilv);  // gate column within the 256
         float dg[32], dl[32];
 #pragma unroll
@@ -1243,7 +1270,7 @@ cudaError_t launch_rc_mx(const RcMxArgs& a, int grid, cudaStream_t s) {
 int dprob_parts_mx_recompute(int F) { return 2 * ((F + RC_BNA - 1) / RC_BNA); }
 
 cudaError_t launch_fc2_dgrad_recompute_mx(const MxProblem& p, cudaStream_t s) {
-  if (!p.gated || (p.ilv != 32 && p.ilv != 64)) return cudaErrorInvalidValue;
+  if (p.gated && p.ilv != 32 && p.ilv != 64) return cudaErrorInvalidValue;
   RcMxArgs a;
   memset(&a, 0, sizeof(a));
   if (!tmap_fp8(&a.tmDy, p.dy, false) || !tmap_fp8(&a.tmW2, p.w2, false) ||
@@ -1274,6 +1301,7 @@ cudaError_t launch_fc2_dgrad_recompute_mx(const MxProblem& p, cudaStream_t s) {
     case MOE_ACT_SWIGLU: return launch_rc_mx<MOE_ACT_SWIGLU>(a, grid, s);
     case MOE_ACT_CLAMPED_SWIGLU: return launch_rc_mx<MOE_ACT_CLAMPED_SWIGLU>(a, grid, s);
     case MOE_ACT_GEGLU: return launch_rc_mx<MOE_ACT_GEGLU>(a, grid, s);
+    case MOE_ACT_SRELU: return launch_rc_mx<MOE_ACT_SRELU>(a, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -68,6 +68,9 @@ MX_CASES = {
                                     lin_lo=-7.0, lin_hi=7.0, lin_offset=1.0, **MX),
     "mx_geglu": synth.LayerConfig("rmg", T=300, E=4, k=2, H=256, F=256, seed=50,
                                   activation="geglu", **MX),
+    # not gated (N1 = F): a 128-column Z tile, one W1 box and scale slab; F tail of 64
+    "mx_srelu": synth.LayerConfig("rmr", T=400, E=4, k=2, H=320, F=320, seed=51,
+                                  activation="srelu", **MX),
 }
 
 

@@ -96,7 +96,6 @@ def test_recompute_keeps_no_z_in_the_workspace(lib):
     (dict(F=64 * 3, ilv=128), 2), (dict(sm_margin=-1), 1),
     (dict(precision="mxfp8"), 2), (dict(precision="mxfp8", align=128, ilv=128), 2),
     (dict(recompute=2), 1),
-    (dict(recompute=1, precision="mxfp8", align=128, activation="srelu"), 2),
     (dict(extras=4), 1), (dict(extras=1, activation="srelu"), 2),
     (dict(extras=3, precision="mxfp8", align=128, activation="srelu"), 2),
     (dict(extras=1, recompute=1), 2),

@@ -384,7 +384,7 @@ class Nvfp4Result:
 
 
 def layer_nvfp4(logits, x, W1, W2, k: int, act: ActParams, mask: int, dy=None,
-                align: int = 128, b1=None, s=None) -> Nvfp4Result:
+                align: int = 128, b1=None, s=None, recompute: bool = False) -> Nvfp4Result:
     """Forward (and, with dy, backward) of the expert layer with NVFP4 GEMM operands.
 
     The same layer as `layer` (R1-R9), with every GEMM consuming NVFP4 copies of its operands
@@ -409,6 +409,9 @@ def layer_nvfp4(logits, x, W1, W2, k: int, act: ActParams, mask: int, dy=None,
     per-feature scale of the activation (a_s = p * (a * s); d_prob = sum_f dA_s * s * a;
     dA = p * s * dA_s), with db1 = sum over an expert's rows of dZ (the unrounded dact
     output) and ds = sum over its rows of p * dA_s * a.
+    `recompute` (activation recomputation): the backward forms dZ from the FC1 output as the
+    tensor cores recompute it (unrounded, the same quantised operands) instead of the saved
+    bf16 copy; nothing else changes.
     """
     from . import nvfp4 as nv
 
@@ -426,12 +429,13 @@ def layer_nvfp4(logits, x, W1, W2, k: int, act: ActParams, mask: int, dy=None,
     xq = nv.fake_quant(x, 1, S("x")) if T else x
     y = np.zeros((T, H))
     res = Nvfp4Result(ids, probs, perm, y, am)
-    acts = []
+    acts, z_full = [], []
     for e in range(E):
         tok, _ = segs[e]
         Ze = xq[tok] @ nv.fake_quant(W1[e], 0, S("w1"))
         if b1 is not None:
             Ze = Ze + np.asarray(b1[e], dtype=np.float64)[None, :]
+        z_full.append(Ze)
         ae = act_forward(act, Ze[:, :F], Ze[:, F:]) if act.gated else act_forward(act, Ze)
         acts.append(ae)
         res.Z.append(bf16_round(Ze))
@@ -466,7 +470,7 @@ def layer_nvfp4(logits, x, W1, W2, k: int, act: ActParams, mask: int, dy=None,
         se = np.asarray(s[e], dtype=np.float64)[None, :] if s is not None else 1.0
         res.d_probs[tok, slot] = (dA_s * se * acts[e]).sum(axis=1)
         dA = Ps[e][:, None] * (dA_s * se)
-        Zb = res.Z[e]
+        Zb = z_full[e] if recompute else res.Z[e]
         if act.gated:
             dg, dl = act_backward(act, Zb[:, :F], Zb[:, F:], dA)
             dZe = np.concatenate([dg, dl], axis=1)

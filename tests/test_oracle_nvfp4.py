@@ -296,6 +296,39 @@ def test_layer_bias_enters_the_saved_fc1_output():
     assert r.db1 is not None and r.ds is None
 
 
+def test_layer_recompute_changes_only_the_fc1_output_the_backward_reads():
+    """Recomputation: the forward and everything that does not read Z (y, a_s, its amaxes,
+    dW2) are identical; dZ is formed from the unrounded Z, so it differs from the saved-Z dZ
+    by about Z's bf16 rounding only; with the bf16 roundings taken out the two coincide."""
+    lg, x, W1, W2, dy, k = _small_layer(seed=17)
+    act = om.ActParams()
+    sv = om.layer_nvfp4(lg, x, W1, W2, k, act, 0x2222, dy=dy)
+    rc = om.layer_nvfp4(lg, x, W1, W2, k, act, 0x2222, dy=dy, recompute=True)
+    assert np.array_equal(sv.y, rc.y) and np.array_equal(sv.dW2, rc.dW2)
+    assert sv.amax["a"] == rc.amax["a"] and sv.amax["at"] == rc.amax["at"]
+    for e in range(len(sv.Z)):
+        assert np.array_equal(sv.Z[e], rc.Z[e]) and np.array_equal(sv.A[e], rc.A[e])
+        if len(sv.dZ[e]):
+            d = np.abs(sv.dZ[e] - rc.dZ[e]).max()
+            assert d <= 2.0 ** -6 * np.abs(sv.dZ[e]).max()
+    assert any(not np.array_equal(a, b) for a, b in zip(sv.dZ, rc.dZ) if len(a))
+
+
+def test_layer_recompute_without_roundings_is_the_saved_path(monkeypatch):
+    """With the quantisers and roundings taken out the saved and the recomputed Z are the same
+    value, so the two backward paths coincide exactly."""
+    lg, x, W1, W2, dy, k = _small_layer(seed=18)
+    monkeypatch.setattr(nv, "fake_quant", lambda v, axis, S: np.asarray(v, dtype=np.float64))
+    monkeypatch.setattr(nv, "to_f32", lambda v: np.asarray(v, dtype=np.float64))
+    monkeypatch.setattr(om, "bf16_round", lambda v: np.asarray(v, dtype=np.float64))
+    act = _ACTS["geglu"]
+    sv = om.layer_nvfp4(lg, x, W1, W2, k, act, 0x0F00, dy=dy)
+    rc = om.layer_nvfp4(lg, x, W1, W2, k, act, 0x0F00, dy=dy, recompute=True)
+    for a, b in [(sv.y, rc.y), (sv.dx, rc.dx), (sv.dW1, rc.dW1), (sv.dW2, rc.dW2),
+                 (sv.d_probs, rc.d_probs)]:
+        assert np.array_equal(a, b)
+
+
 def test_layer_error_is_the_size_of_nvfp4_quantisation_noise():
     lg, x, W1, W2, dy, k = _small_layer(seed=9)
     act = om.ActParams()

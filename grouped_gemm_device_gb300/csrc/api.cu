@@ -146,8 +146,6 @@ static moe_status_t validate_desc(const moe_layer_desc_t* d) {
   if (d->sm_margin < 0) return fail(MOE_ERR_INVALID_ARG, "sm_margin must be >= 0");
   if (d->recompute != 0 && d->recompute != 1)
     return fail(MOE_ERR_INVALID_ARG, "recompute must be 0 or 1");
-  if (d->recompute && d->precision == MOE_PREC_NVFP4)
-    return fail(MOE_ERR_UNSUPPORTED, "recompute needs a BF16 or MXFP8 layer");
   if (d->extras & ~3) return fail(MOE_ERR_INVALID_ARG, "extras has unknown bits");
   if (d->reuse_weights != 0 && d->reuse_weights != 1)
     return fail(MOE_ERR_INVALID_ARG, "reuse_weights must be 0 or 1");
@@ -249,7 +247,8 @@ static void compute_layout(const moe_layer_desc_t* d, moe_ws_layout_t* L) {
   const bool nv = d->precision == MOE_PREC_NVFP4;
   const int64_t nparts = mx ? (d->recompute ? dprob_parts_mx_recompute((int)F)
                                             : dprob_parts_mx((int)F))
-                         : nv ? dprob_parts_fp4((int)F)
+                         : nv ? (d->recompute ? dprob_parts_fp4_recompute((int)F)
+                                              : dprob_parts_fp4((int)F))
                               : (d->recompute ? dprob_parts_recompute((int)F)
                                               : dprob_parts((int)F));
   size_t o = 0;
@@ -609,7 +608,7 @@ static moe_status_t fwd_impl(const moe_layer_desc_t* d, int32_t T, const void* w
     }
     // FC1 + activation + probability scale, BF16 a_s plus its amax and rotated amax
     m.role = ROLE_FC1_FPROP;
-    m.out = w.at<void>(w.L.z);
+    m.out = d->recompute ? nullptr : w.at<void>(w.L.z);  // NULL: Z is not kept
     m.out2 = w.at<void>(w.L.a_s);
     m.fc1_bias = fc1_bias;
     m.fscale = feat_scale;
@@ -783,7 +782,12 @@ static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* d
       m.fscale = feat_scale;
       m.ext_part = w.at<float>(w.L.ext_part);
     }
-    if ((e = launch_grouped_gemm_fp4(m, s)) != cudaSuccess) return cuda_fail(e, "FC2 dgrad FP4");
+    if (d->recompute) {  // the FC1 output is rebuilt from the NVFP4 copies of X and W1
+      if ((e = launch_fc2_dgrad_recompute_fp4(m, s)) != cudaSuccess)
+        return cuda_fail(e, "FC2 dgrad recompute FP4");
+    } else if ((e = launch_grouped_gemm_fp4(m, s)) != cudaSuccess) {
+      return cuda_fail(e, "FC2 dgrad FP4");
+    }
     m.fscale = nullptr;
     m.ext_part = nullptr;
     if (d->extras) {
@@ -792,8 +796,10 @@ static moe_status_t bwd_impl(const moe_layer_desc_t* d, int32_t T, const void* d
     }
     if (T > 0) {
       const int n = T * d->k;
-      launch_kernel(dprob_reduce_kernel, grid_for((n + 255) / 256, 4), 256, 0, s, nullptr, 0, 
-          w.at<float>(w.L.dprob_part), dprob_parts_fp4(d->F), row_of, n, d_probs);
+      launch_kernel(dprob_reduce_kernel, grid_for((n + 255) / 256, 4), 256, 0, s, nullptr, 0,
+          w.at<float>(w.L.dprob_part),
+          d->recompute ? dprob_parts_fp4_recompute(d->F) : dprob_parts_fp4(d->F), row_of, n,
+          d_probs);
       count_launch(s, MOE_K_DPROB_REDUCE);
     }
     if (!nv_quantize(w.at<void>(w.L.dz), w.L.R_cap, m.N1, w.L.R_cap, w.L.R_cap, live, m, AM_DZ,

@@ -539,9 +539,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
           }
         }
         uint16_t* zout = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo + t.n0 + cb;
+        if (p.out) {  // the saved Z (bf16); absent when the backward recomputes it
 #pragma unroll
-        for (int j = 0; j < 4; ++j)  // the saved Z (bf16)
-          if (t.n0 + cb + 32 * j < p.N) store_bf16x32_v8(zout + 32 * j, &acc_r[32 * j]);
+          for (int j = 0; j < 4; ++j)
+            if (t.n0 + cb + 32 * j < p.N) store_bf16x32_v8(zout + 32 * j, &acc_r[32 * j]);
+        }
         uint16_t* aout = static_cast<uint16_t*>(p.out2) + (int64_t)row * p.ldo2;
         // gated: this half holds 64 gate and 64 linear columns, two 32-wide output blocks;
         // sReLU: four 32-wide blocks
@@ -820,6 +822,424 @@ cudaError_t launch_grouped_gemm_fp4(const Fp4Problem& p, cudaStream_t s) {
       grid = (int)std::min<int64_t>(grid, std::max<int64_t>(tiles, 1));
       return launch_fp4<EPI_STORE, 0, true>(a, grid, s, kid);
     }
+  }
+}
+
+
+// ----------------------------------------------------------------------------------------
+// FC2 dgrad with the FC1 output recomputed (activation recomputation, [NV-blog] "What's
+// next"), NVFP4 operands. Per 128-row x 64-column tile of dA_s two block-scaled FP4 GEMMs
+// share one loop over H (k-blocks of 256 values, four MMAs of K = 64 each):
+//   dA_s[rows, f0..f0+63]       = Q(dY)[rows] . Q_H(W2)[f0..f0+63]^T           (128 x 64)
+//   Z[rows, 2f0 .. 2f0+127]     = Q(X)[rows]  . Q_H(W1p)[2f0 .. 2f0+127]^T     (128 x 128)
+// (with the interleave of 64, packed W1 rows 2f0 .. 2f0+127 are exactly the gate and linear
+// columns of dA_s columns f0 .. f0+63; sReLU, not gated: Z[rows, f0..f0+63], 128 x 64). Both
+// scaled by 1 / (S_a S_b) of their operands. TMEM: dA_s columns 0-63, Z from 64, the stages'
+// scale factors from 192 (16 columns per MMA: dY, W2, X, W1). The 64 weight rows of a tile
+// are half of a 128-row scale slab: the whole slab is copied and the MMA's B scale address
+// starts at the slab's third column when the rows are its upper half. The epilogue reads
+// dA_s and Z in fp32 from TMEM and writes dZ in BF16 (packed order) with its amax and the amax
+// of its 16-row rotation, and the per-row d_prob partial of the tile, as the saved-Z dGLU
+// kernel does. One accumulator set; every wait is bounded.
+namespace {
+
+constexpr int RC4_BNA = 64;                   // dA_s columns per tile
+constexpr int RC4_STAGES = 3;
+constexpr int RC4_A = BM * BKB;               // 16 KB: 128 rows x 128 bytes (dY, X)
+constexpr int RC4_B1 = RC4_BNA * BKB;         // 8 KB: W2 rows
+constexpr int RC4_B2 = 2 * RC4_BNA * BKB;     // 16 KB: W1p rows (gated; sReLU uses 8 KB)
+constexpr int RC4_STAGE = RC4_A + RC4_B1 + RC4_A + RC4_B2;
+constexpr int RC4_SF = 16 * SFA_SLAB;         // four 512-byte slabs of each of the four operands
+constexpr int RC4_SF_OFF = RC4_STAGES * RC4_STAGE;
+constexpr int RC4_XT_OFF = RC4_SF_OFF + RC4_STAGES * RC4_SF;
+constexpr int RC4_CTRL_OFF = RC4_XT_OFF + kEpiWarps * XT_WARP;
+constexpr int RC4_TOTAL = RC4_CTRL_OFF + 4096 + 1024;
+constexpr int RC4_ZCOL = RC4_BNA;             // first TMEM column of Z
+constexpr int RC4_SFCOL = 192;                // first TMEM column of the scale factors
+static_assert(RC4_TOTAL <= 232448, "shared memory");
+static_assert(RC4_SFCOL + 64 * RC4_STAGES <= kTmemCols, "TMEM map");
+static_assert(RC4_STAGE % 1024 == 0 && RC4_A % 1024 == 0 && RC4_B1 % 1024 == 0, "alignment");
+
+struct Rc4Args {
+  CUtensorMap tmDy;  // dY row-wise copy [R_cap, H/2 bytes], box {128 B, 128 rows}
+  CUtensorMap tmW2;  // W2 row-wise copy [E*Fp, H/2], box {128 B, 64 rows}
+  CUtensorMap tmX;   // X row-wise copy [R_cap, H/2], box {128 B, 128 rows}
+  CUtensorMap tmW1;  // W1p row-wise copy [E*N1p, H/2], box {128 B, 128 (gated) / 64 rows}
+  const uint8_t *sf_dy, *sf_w2, *sf_x, *sf_w1;
+  int64_t pad_dy, pad_w2, pad_x, pad_w1;
+  const float *amax_dy, *amax_w2, *amax_x, *amax_w1;
+  const int32_t* offsets;
+  int E, R_cap, H, F, N1, Fp, N1p;
+  const float* row_prob;
+  uint16_t* dz;           // [R_cap, N1] bf16, packed columns
+  float* dprob_part;
+  int nparts;
+  float* amax_out;        // amax of dZ
+  float* amax_out_rht;    //   and of its 16-row rotation
+  uint32_t rht_mask;
+  ActDev act;
+  int* err;
+};
+
+struct Rc4Ctrl {
+  uint64_t full[RC4_STAGES];
+  uint64_t empty[RC4_STAGES];
+  uint64_t tfull;
+  uint64_t tempty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int total_tiles;
+  int off[kMaxE + 1];
+  int prefix[kMaxE + 1];
+};
+static_assert(sizeof(Rc4Ctrl) <= 4096, "control block");
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    fc2_dgrad_recompute_fp4_kernel(const __grid_constant__ Rc4Args p) {
+  MOE_GRIDDEP_ENTRY();
+  constexpr bool kGated = KIND != MOE_ACT_SRELU;
+  constexpr int ZN = kGated ? 2 * RC4_BNA : RC4_BNA;        // Z columns per tile
+  constexpr uint32_t kStageTx = RC4_STAGE - (kGated ? 0 : RC4_B2 / 2) + RC4_SF;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  Rc4Ctrl& c = *reinterpret_cast<Rc4Ctrl*>(smem + RC4_CTRL_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort = &c.abort;
+  const int NT = (p.F + RC4_BNA - 1) / RC4_BNA;
+  const int nkb = (p.H + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RC4_STAGES; ++s) {
+      mbar_init(&c.full[s], 1);
+      mbar_init(&c.empty[s], 1);
+    }
+    mbar_init(&c.tfull, 1);
+    mbar_init(&c.tempty, kEpiWarps);
+    mbar_init(&c.drain, 1);
+    fence_mbar_init();
+    c.abort = 0;
+    bool ok = p.E >= 1 && p.E <= kMaxE;
+    int prev = 0;
+    for (int e = 0; ok && e <= p.E; ++e) {
+      const int o = p.offsets[e];
+      if (o < prev || o > p.R_cap || (o & (BM - 1)) || (e == 0 && o != 0)) ok = false;
+      c.off[e] = o;
+      prev = o;
+    }
+    int total = 0;
+    if (ok) {
+      for (int e = 0; e < p.E; ++e) {
+        c.prefix[e] = total;
+        total += ((c.off[e + 1] - c.off[e]) / BM) * NT;
+      }
+      c.prefix[p.E] = total;
+    } else {
+      set_error(p.err, MOE_DEVERR_CAPACITY);
+    }
+    c.total_tiles = total;
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmDy);
+    tma_prefetch_desc(&p.tmW2);
+    tma_prefetch_desc(&p.tmX);
+    tma_prefetch_desc(&p.tmW1);
+  }
+  if (warp == 1) {
+    tmem_alloc(&c.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = c.tmem_base;
+  const int total = c.total_tiles;
+  // tile -> expert, first row, first dA_s column (m fastest within an expert)
+  auto decode = [&](int tile, int& e, int& m0, int& n0) {
+    int lo = 0, hi = p.E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (c.prefix[mid] <= tile) lo = mid; else hi = mid;
+    }
+    const int local = tile - c.prefix[lo];
+    const int mt = (c.off[lo + 1] - c.off[lo]) / BM;
+    e = lo;
+    m0 = c.off[lo] + (local % mt) * BM;
+    n0 = (local / mt) * RC4_BNA;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed[RC4_STAGES];
+#pragma unroll
+      for (int s = 0; s < RC4_STAGES; ++s) armed[s] = -1;
+      for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+        int e, m0, n0;
+        decode(tile, e, m0, n0);
+        const int w2_row = e * p.Fp + n0, w1_row = e * p.N1p + (kGated ? 2 * n0 : n0);
+        const int w2_slab = w2_row & ~127, w1_slab = w1_row & ~127;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&c.empty[stage], phase ^ 1, abort, p.err)) break;
+          uint8_t* s0 = smem + stage * RC4_STAGE;
+          uint8_t* sf = smem + RC4_SF_OFF + stage * RC4_SF;
+          uint64_t* bar = &c.full[stage];
+          mbar_arrive_expect_tx(bar, kStageTx);
+#pragma unroll
+          for (int s = 0; s < RC4_STAGES; ++s)
+            if (s == stage) armed[s] = (int)phase;
+          const int k0 = kb * BK;  // values; boxes start at byte column k0 / 2
+          tma_load_2d(s0, &p.tmDy, bar, k0 / 2, m0);
+          tma_load_2d(s0 + RC4_A, &p.tmW2, bar, k0 / 2, w2_row);
+          tma_load_2d(s0 + RC4_A + RC4_B1, &p.tmX, bar, k0 / 2, m0);
+          tma_load_2d(s0 + 2 * RC4_A + RC4_B1, &p.tmW1, bar, k0 / 2, w1_row);
+          // the four 64-value scale slabs of each operand (whole 128-row slabs of the weights)
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            const int64_t kg = k0 / MMA_K + s;
+            bulk_load(sf + s * SFA_SLAB, p.sf_dy + (kg * p.pad_dy + m0) * 4, SFA_SLAB, bar);
+            bulk_load(sf + 4 * SFA_SLAB + s * SFA_SLAB, p.sf_w2 + (kg * p.pad_w2 + w2_slab) * 4,
+                      SFA_SLAB, bar);
+            bulk_load(sf + 8 * SFA_SLAB + s * SFA_SLAB, p.sf_x + (kg * p.pad_x + m0) * 4,
+                      SFA_SLAB, bar);
+            bulk_load(sf + 12 * SFA_SLAB + s * SFA_SLAB, p.sf_w1 + (kg * p.pad_w1 + w1_slab) * 4,
+                      SFA_SLAB, bar);
+          }
+          if (++stage == RC4_STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < RC4_STAGES; ++s) {
+        if (armed[s] >= 0) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(smem_u32(&c.full[s]), (uint32_t)armed[s]) &&
+                 globaltimer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ scale copies + MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDA = idesc_nvf4(BM, RC4_BNA);
+      constexpr uint32_t IDZ = idesc_nvf4(BM, ZN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc_i = 0;
+      bool issued_any = false;
+      for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+        int e, m0, n0;
+        decode(tile, e, m0, n0);
+        // a 64-row weight block in the upper half of its 128-row scale slab reads the slab's
+        // columns 2-3 (scale column = row / 32 within the slab)
+        const uint32_t w2_off = ((e * p.Fp + n0) & 127) ? 2u : 0u;
+        const uint32_t w1_off = ((e * p.N1p + (kGated ? 2 * n0 : n0)) & 127) ? 2u : 0u;
+        if (!mbar_wait(&c.tempty, (acc_i & 1) ^ 1, abort, p.err)) break;
+        tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&c.full[stage], phase, abort, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA1 = smem_u32(smem + stage * RC4_STAGE);
+          const uint32_t sB1 = sA1 + RC4_A, sA2 = sB1 + RC4_B1, sB2 = sA2 + RC4_A;
+          const uint32_t sf = smem_u32(smem + RC4_SF_OFF + stage * RC4_SF);
+          const uint32_t tsf = tmem_base + RC4_SFCOL + stage * 64;
+          const int rem = p.H - kb * BK;
+          const int nsub = rem >= BK ? BK / MMA_K : (rem + MMA_K - 1) / MMA_K;
+          for (int s = 0; s < nsub; ++s) {
+            const uint32_t col = tsf + 16 * s;
+            tmem_cp_32x128b_warpx4(col, smem_desc_noswizzle(sf + s * SFA_SLAB, 0, 128));
+            tmem_cp_32x128b_warpx4(col + 4, smem_desc_noswizzle(sf + (4 + s) * SFA_SLAB, 0, 128));
+            tmem_cp_32x128b_warpx4(col + 8, smem_desc_noswizzle(sf + (8 + s) * SFA_SLAB, 0, 128));
+            tmem_cp_32x128b_warpx4(col + 12,
+                                   smem_desc_noswizzle(sf + (12 + s) * SFA_SLAB, 0, 128));
+          }
+          for (int s = 0; s < nsub; ++s) {
+            const uint32_t col = tsf + 16 * s;
+            const uint32_t acc = (kb | s) != 0 ? 1u : 0u;
+            mma_nvf4_ss(tmem_base, smem_desc_sw128(sA1 + s * (MMA_K / 2), 16, 1024),
+                        smem_desc_sw128(sB1 + s * (MMA_K / 2), 16, 1024), IDA, col,
+                        col + 4 + w2_off, acc);
+            mma_nvf4_ss(tmem_base + RC4_ZCOL, smem_desc_sw128(sA2 + s * (MMA_K / 2), 16, 1024),
+                        smem_desc_sw128(sB2 + s * (MMA_K / 2), 16, 1024), IDZ, col + 8,
+                        col + 12 + w1_off, acc);
+          }
+          issued_any = true;
+          mma_commit(&c.empty[stage]);
+          if (++stage == RC4_STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&c.tfull);
+        ++acc_i;
+      }
+      if (issued_any) {
+        mma_commit(&c.drain);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(&c.drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps 2..9
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;  // dA_s columns [32 * half, 32 * half + 32) of the tile
+    uint32_t* xt = reinterpret_cast<uint32_t*>(smem + RC4_XT_OFF + (warp - 2) * XT_WARP);
+    const float alpha_a =
+        __frcp_rn(__fmul_rn(nvfp4_encode_scale(*p.amax_dy), nvfp4_encode_scale(*p.amax_w2)));
+    const float alpha_z =
+        __frcp_rn(__fmul_rn(nvfp4_encode_scale(*p.amax_x), nvfp4_encode_scale(*p.amax_w1)));
+    float m_out = 0.f, m_rht = 0.f;
+    int acc_i = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      if (__shfl_sync(0xFFFFFFFFu, *abort, 0)) break;
+      int e, m0, n0;
+      decode(tile, e, m0, n0);
+      const int row = m0 + q * 32 + lane;
+      const float prob = p.row_prob[row];  // segments are 128-row aligned: every row is inside
+      const bool got = mbar_wait(&c.tfull, acc_i & 1, abort, p.err);
+      if (!__all_sync(0xFFFFFFFFu, got)) break;
+      tc_fence_after();
+      const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
+      uint16_t* dzrow = p.dz + (int64_t)row * p.N1;
+      float dp = 0.f;
+#pragma unroll 1
+      for (int j = 0; j < 2; ++j) {
+        const int cc = half * 32 + 16 * j;  // dA_s column within the tile
+        const int f0 = n0 + cc;
+        if (f0 >= p.F) break;
+        uint32_t da[16], gz[16], lz[16];
+        tmem_ld_32x32b_x16(tl + cc, da);
+        tmem_ld_32x32b_x16(tl + RC4_ZCOL + cc, gz);
+        if constexpr (kGated) tmem_ld_32x32b_x16(tl + RC4_ZCOL + RC4_BNA + cc, lz);
+        tmem_ld_wait();
+        uint32_t w[16];  // dG pairs in w[0..7], dL pairs in w[8..15]
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          float dg[2], dl[2] = {0.f, 0.f};
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const float d = alpha_a * __uint_as_float(da[i + u]);
+            const float g = alpha_z * __uint_as_float(gz[i + u]);
+            if constexpr (kGated) {
+              const float l = alpha_z * __uint_as_float(lz[i + u]);
+              dp += d * act_bwd_k<KIND>(p.act, g, l, prob * d, dg[u], dl[u]);
+            } else {
+              const float rr = fmaxf(g, 0.f);
+              dp += d * rr * rr;
+              dg[u] = prob * d * 2.f * rr;
+            }
+          }
+          w[i >> 1] = pack_bf16x2(dg[0], dg[1]);
+          w[8 + (i >> 1)] = pack_bf16x2(dl[0], dl[1]);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          m_out = fmaxf(m_out, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+        const int gc = kGated ? gate_col(f0) : f0;
+        st_global_v8(dzrow + gc, w);
+        if constexpr (kGated) {
+          st_global_v8(dzrow + gc + ILV, w + 8);
+          m_rht = fmaxf(m_rht, rht_amax_tile32(xt, w, p.rht_mask, lane));
+        } else {
+          uint32_t w2[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w2[i] = i < 8 ? w[i] : 0u;
+          m_rht = fmaxf(m_rht, rht_amax_tile32(xt, w2, p.rht_mask, lane));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.tempty);
+      ++acc_i;
+      p.dprob_part[(int64_t)row * p.nparts + (n0 / RC4_BNA) * 2 + half] = dp;
+    }
+    amax_flush_warp(m_out, p.amax_out);
+    amax_flush_warp(m_rht, p.amax_out_rht);
+  }
+
+  griddep_launch_dependents();  // this CTA's tiles are done
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// K-major NVFP4 copy [rows, cols] (cols/2 bytes a row) as TMA boxes of 128 bytes x box_rows
+bool tmap_fp4_rows(CUtensorMap* m, const MxOperand& t, uint32_t box_rows) {
+  uint64_t dims[2] = {(uint64_t)(t.cols / 2), (uint64_t)t.rows};
+  uint64_t strides[1] = {(uint64_t)(t.cols / 2)};
+  uint32_t box[2] = {128, box_rows};
+  return make_tmap(m, t.q, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+
+template <int KIND>
+cudaError_t launch_rc_fp4(const Rc4Args& a, int grid, cudaStream_t s) {
+  auto kern = fc2_dgrad_recompute_fp4_kernel<KIND>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), RC4_TOTAL);
+  if (e != cudaSuccess) return e;
+  launch_kernel(kern, grid, kThreads, RC4_TOTAL, s, nullptr, 0, a);
+  count_launch(s, MOE_K_GEMM_FC2_DGRAD);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int dprob_parts_fp4_recompute(int F) { return 2 * ((F + RC4_BNA - 1) / RC4_BNA); }
+
+cudaError_t launch_fc2_dgrad_recompute_fp4(const Fp4Problem& p, cudaStream_t s) {
+  if (p.gated && p.ilv != ILV) return cudaErrorInvalidValue;
+  if (p.gated != (p.act.kind != MOE_ACT_SRELU)) return cudaErrorInvalidValue;
+  Rc4Args a;
+  memset(&a, 0, sizeof(a));
+  if (!tmap_fp4_rows(&a.tmDy, p.dy, BM) || !tmap_fp4_rows(&a.tmW2, p.w2, RC4_BNA) ||
+      !tmap_fp4_rows(&a.tmX, p.x, BM) ||
+      !tmap_fp4_rows(&a.tmW1, p.w1, p.gated ? 2 * RC4_BNA : RC4_BNA))
+    return cudaErrorInvalidValue;
+  a.sf_dy = p.dy.s; a.pad_dy = p.dy.s_pad;
+  a.sf_w2 = p.w2.s; a.pad_w2 = p.w2.s_pad;
+  a.sf_x = p.x.s; a.pad_x = p.x.s_pad;
+  a.sf_w1 = p.w1.s; a.pad_w1 = p.w1.s_pad;
+  a.amax_dy = p.amax + AM_DY; a.amax_w2 = p.amax + AM_W2;
+  a.amax_x = p.amax + AM_X; a.amax_w1 = p.amax + AM_W1;
+  a.offsets = p.offsets;
+  a.E = p.E;
+  a.R_cap = (int)p.R_cap;
+  a.H = p.H;
+  a.F = p.F;
+  a.N1 = p.N1;
+  a.Fp = p.Fp;
+  a.N1p = p.N1p;
+  a.row_prob = p.row_prob;
+  a.dz = static_cast<uint16_t*>(p.out);
+  a.dprob_part = p.dprob_part;
+  a.nparts = dprob_parts_fp4_recompute(p.F);
+  a.amax_out = p.amax + AM_DZ;
+  a.amax_out_rht = p.amax + AM_DZT;
+  a.rht_mask = p.rht_mask;
+  a.act = p.act;
+  a.err = p.err;
+  const int grid = std::max(1, p.num_ctas);
+  switch (p.act.kind) {
+    case MOE_ACT_SWIGLU: return launch_rc_fp4<MOE_ACT_SWIGLU>(a, grid, s);
+    case MOE_ACT_CLAMPED_SWIGLU: return launch_rc_fp4<MOE_ACT_CLAMPED_SWIGLU>(a, grid, s);
+    case MOE_ACT_GEGLU: return launch_rc_fp4<MOE_ACT_GEGLU>(a, grid, s);
+    case MOE_ACT_SRELU: return launch_rc_fp4<MOE_ACT_SRELU>(a, grid, s);
+    default: return cudaErrorInvalidValue;
   }
 }
 

@@ -263,5 +263,9 @@ struct Fp4Problem {
 };
 int dprob_parts_fp4(int F);
 cudaError_t launch_grouped_gemm_fp4(const Fp4Problem& p, cudaStream_t s);
+// FC2 dgrad + dActivation with the FC1 output recomputed from the NVFP4 copies of X and W1
+// (activation recomputation); dZ, its amaxes and the d_prob partials as the saved-Z kernel
+int dprob_parts_fp4_recompute(int F);
+cudaError_t launch_fc2_dgrad_recompute_fp4(const Fp4Problem& p, cudaStream_t s);
 
 }  // namespace moe

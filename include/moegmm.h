@@ -104,7 +104,7 @@ typedef struct {
                          (MXFP8, NVFP4: segments start on 128-row scale slabs)            */
   int32_t recompute;  /* 1: keep no FC1 output between forward and backward; the FC2-dgrad
                          kernel recomputes it ([NV-blog] "What's next": activation
-                         recomputation). BF16 or MXFP8 (any activation); 0 otherwise    */
+                         recomputation). Any precision and activation; 0 otherwise      */
   int32_t extras;     /* epilogue extras ([NV-blog] GLU-epilogue section: bias-vector addition
                          and feature scaling): bit 0 FC1 bias, bit 1 per-feature scale of the
                          activation output; used through the _ex entry points. Any

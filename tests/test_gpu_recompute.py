@@ -1,7 +1,7 @@
 """GPU parity of the layer with activation recomputation (the forward keeps no FC1 output; the
 FC2-dgrad kernel rebuilds it next to dA_s) against the fp64 oracle, and against the same layer
-with the saved FC1 output, in BF16 and MXFP8. Same bars as the saved path: relative Frobenius
-error <= 5e-3 (BF16) / 3e-2 (MXFP8)."""
+with the saved FC1 output, in BF16, MXFP8 and NVFP4. Same bars as the saved path: relative
+Frobenius error <= 5e-3 (BF16) / 3e-2 (MXFP8) / 1e-2 (NVFP4)."""
 import numpy as np
 import pytest
 import torch
@@ -9,7 +9,9 @@ import torch
 import grouped_gemm_device_gb300 as g
 from grouped_gemm_device_gb300 import synth
 
-from .gpu_helpers import BF16_TOL, MX_TOL, LayerRun, Inputs, rel_fro, to_np
+from oracle import moe as om
+
+from .gpu_helpers import BF16_TOL, MX_TOL, LayerRun, Inputs, act_params, rel_fro, to_np
 from .test_gpu_layer import check_layer
 
 pytestmark = pytest.mark.gpu
@@ -94,3 +96,74 @@ def test_mx_recompute_forward_equals_saved_path(lib):
     rc = LayerRun(inp, recompute=True)
     assert torch.equal(keep.y, rc.y)
     assert torch.equal(keep.dw2, rc.dw2)
+
+
+NV = dict(precision="nvfp4", align=128)
+NV_TOL = 1e-2
+NV_CASES = {
+    "nv_swiglu": synth.LayerConfig("rnv", T=300, E=4, k=2, H=256, F=256, seed=61, **NV),
+    # five 64-column dA tiles (F = 320: W2 rows in both halves of a 128-row scale slab), a
+    # K tail (H = 576: two k-blocks of 256 and one MMA of 64)
+    "nv_tails": synth.LayerConfig("rnt", T=260, E=3, k=2, H=576, F=320, seed=62, **NV),
+    # empty experts and long segments
+    "nv_clamped_skew": synth.LayerConfig("rnc", T=300, E=64, k=4, H=256, F=256, seed=63,
+                                         zipf_s=1.5, activation="clamped_swiglu", beta=1.702,
+                                         gate_max=7.0, lin_lo=-7.0, lin_hi=7.0, lin_offset=1.0,
+                                         **NV),
+    "nv_geglu": synth.LayerConfig("rng", T=300, E=4, k=2, H=256, F=256, seed=64,
+                                  activation="geglu", **NV),
+    # not gated (N1 = F): the Z tile is the dA tile's own 64 columns
+    "nv_srelu": synth.LayerConfig("rns", T=300, E=4, k=2, H=256, F=384, seed=65,
+                                  activation="srelu", **NV),
+}
+
+
+def nv_oracle(cfg, inp, recompute):
+    return om.layer_nvfp4(inp.logits, om.bf16_to_f64(inp.x), om.bf16_to_f64(inp.w1),
+                          om.bf16_to_f64(inp.w2), cfg.k, act_params(cfg),
+                          synth.gen_rht_mask(cfg), dy=om.bf16_to_f64(inp.dy), align=cfg.align,
+                          recompute=recompute)
+
+
+@pytest.mark.parametrize("name", list(NV_CASES))
+def test_nvfp4_recompute_layer_matches_oracle(lib, name):
+    """NVFP4 with recomputation: the FC2-dgrad kernel runs two block-scaled FP4 GEMMs (dA_s from
+    dY and W2, the tile's Z from X and W1, all four from the forward's NVFP4 copies) and forms
+    dZ, its amaxes and the routing-weight partials from their fp32 accumulators."""
+    cfg = NV_CASES[name]
+    inp = Inputs(cfg)
+    run = LayerRun(inp, recompute=True)
+    assert run.layer.layout.z == 2 ** 64 - 1
+    r = nv_oracle(cfg, inp, recompute=True)
+    counts = np.bincount(r.ids.ravel(), minlength=cfg.E)
+    dZ = run.unpack_cols(to_np(run.ws("dz", torch.bfloat16, cfg.N1)))
+    off = r.perm.offsets
+    for e in range(cfg.E):
+        if counts[e]:
+            rows = slice(off[e], off[e] + counts[e])
+            assert rel_fro(dZ[rows], r.dZ[e]) < BF16_TOL, e
+    am = run.layer.ws_view("nv_amax", torch.float32, (16,)).cpu().numpy().astype(np.float64)
+    got = dict(zip(g.NV_AMAX, am))
+    for k in ("dz", "dzt"):
+        assert abs(got[k] - r.amax[k]) <= 2.0 ** -8 * r.amax[k], k
+    errs = {"y": rel_fro(to_np(run.y), r.y), "dx": rel_fro(to_np(run.dx), r.dx),
+            "d_probs": rel_fro(to_np(run.d_probs), r.d_probs),
+            "dW2": rel_fro(to_np(run.dw2), r.dW2), "dW1": rel_fro(run.dw1_logical(), r.dW1)}
+    bad = {k: v for k, v in errs.items() if not v <= NV_TOL}
+    assert not bad, bad
+    if name == "nv_clamped_skew":
+        assert (counts == 0).any()
+
+
+def test_nvfp4_recompute_forward_equals_saved_path(lib):
+    """The forward and FC2's weight gradient (from a_s and dY only) are bit-identical with or
+    without the saved Z, and dropping Z shrinks the workspace. The other gradients are not
+    compared with each other: a one-ulp change of Z moves some dZ values across an FP4 rounding
+    boundary, so each is held to its own oracle reading instead."""
+    cfg = NV_CASES["nv_swiglu"]
+    inp = Inputs(cfg)
+    keep = LayerRun(inp)
+    rc = LayerRun(inp, recompute=True)
+    assert torch.equal(keep.y, rc.y)
+    assert torch.equal(keep.dw2, rc.dw2)
+    assert g.moe_workspace_size(keep.desc) > g.moe_workspace_size(rc.desc)

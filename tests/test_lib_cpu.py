@@ -100,7 +100,6 @@ def test_recompute_keeps_no_z_in_the_workspace(lib):
     (dict(extras=3, precision="mxfp8", align=128, activation="srelu"), 2),
     (dict(extras=1, recompute=1), 2),
     (dict(precision="nvfp4"), 2), (dict(precision="nvfp4", align=128, ilv=32), 2),
-    (dict(precision="nvfp4", align=128, recompute=1), 2),
     (dict(precision="nvfp4", align=128, extras=1, activation="srelu"), 2),
 ])
 def test_invalid_descriptions_rejected(lib, kw, status):

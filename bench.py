@@ -64,7 +64,7 @@ def parse():
     ap.add_argument("--extras", type=int, default=0,
                     help="epilogue extras bits: 1 FC1 bias, 2 feature scale (BF16 gated)")
     ap.add_argument("--recompute", action="store_true",
-                    help="keep no FC1 output; the FC2-dgrad kernel recomputes it (BF16)")
+                    help="keep no FC1 output; the FC2-dgrad kernel recomputes it")
     ap.add_argument("--workloads", default="auto",
                     help="extra workloads timed after the headline one, each with its own "
                          "entry under 'workloads': 'auto' (every other configuration when the "
@@ -136,58 +136,49 @@ DTYPE = {"bf16": "bf16", "mxfp8": "e4m3+e8m0 (fp32 accumulate)",
 
 def kernel_bytes(cfg, recompute=False):
     """Algorithmic HBM bytes per launch: each operand read once, each result written once
-    (R = routed rows; MXFP8 data is 1 byte plus one scale byte per 32). With recomputation the
-    FC1 kernel writes no Z and the FC2-dgrad kernel reads X and W1 instead of Z."""
+    (R = routed rows; MXFP8 data is 1 byte plus one scale byte per 32, NVFP4 half a byte plus
+    one scale byte per 16). With recomputation the FC1 kernel writes no Z and the FC2-dgrad
+    kernel reads X and W1 (their quantised copies in MXFP8 and NVFP4) instead of Z."""
     R, T, E = cfg.R, cfg.T, cfg.E
     H, F, N1 = cfg.H, cfg.F, cfg.N1
     R_cap = cfg.R_cap
-    if cfg.precision == "nvfp4":
-        s = 0.5 + 1.0 / 16.0   # half a byte a value plus one E4M3 scale per 16
-        return {
-            "gemm_fc1_fprop": R * H * s + E * N1 * H * s + R * N1 * 2 + R * F * 2,
-            "gemm_fc2_fprop": R * F * s + E * F * H * s + R * H * 2,
-            "gemm_fc2_dgrad": R * H * s + E * F * H * s + R * N1 * 2 + R * N1 * 2,
-            "gemm_fc2_wgrad": R * F * s + R * H * s + E * F * H * 2,
-            "gemm_fc1_dgrad": R * N1 * s + E * N1 * H * s + R * H * 2,
-            "gemm_fc1_wgrad": R * N1 * s + R * H * s + E * N1 * H * 2,
-            "gather_x": R_cap * H * 2 + R * H * 2, "gather_dy": R_cap * H * 2 + R * H * 2,
-            "combine_y": R * H * 2 + T * H * 2, "combine_dx": R * H * 2 + T * H * 2,
-            # bf16 in, row-wise and transposed copies out
-            "nvfp4_quant_x": R_cap * H * (2 + 2 * s), "nvfp4_quant_dy": R_cap * H * (2 + 2 * s),
-            "nvfp4_quant_a": R_cap * F * (2 + 2 * s), "nvfp4_quant_dz": R_cap * N1 * (2 + 2 * s),
-            "nvfp4_quant_w1": E * N1 * H * (2 + 2 * s), "nvfp4_quant_w2": E * F * H * (2 + 2 * s),
-            "nvfp4_amax_w1": E * N1 * H * 2, "nvfp4_amax_w2": E * F * H * 2,
-        }
-    if cfg.precision == "mxfp8":
-        s = 33.0 / 32.0
-        return {
-            "gemm_fc1_fprop": R * H * s + E * N1 * H * s + R * N1 * 2 + 2 * R * F * s,
-            "gemm_fc2_fprop": R * F * s + E * F * H * s + R * H * 2,
-            "gemm_fc2_dgrad": R * H * s + E * F * H * s + R * N1 * 2 + 2 * R * N1 * s,
-            "gemm_fc2_wgrad": R * F * s + R * H * s + E * F * H * 2,
-            "gemm_fc1_dgrad": R * N1 * s + E * N1 * H * s + R * H * 2,
-            "gemm_fc1_wgrad": R * N1 * s + R * H * s + E * N1 * H * 2,
-            "gather_x": R_cap * H * 2 + R * H * 2, "gather_dy": R_cap * H * 2 + R * H * 2,
-            "combine_y": R * H * 2 + T * H * 2, "combine_dx": R * H * 2 + T * H * 2,
-            "mxfp8_quant_x": R_cap * H * (2 + 2 * s), "mxfp8_quant_dy": R_cap * H * (2 + 2 * s),
-            "mxfp8_quant_w1": E * N1 * H * (2 + 2 * s), "mxfp8_quant_w2": E * F * H * (2 + 2 * s),
-        }
-    if recompute:
-        fc1 = (R * H + E * N1 * H + R * F) * 2
-        dgrad = (R * H + E * F * H + R * H + E * N1 * H + R * N1) * 2
-    else:
-        fc1 = (R * H + E * N1 * H + R * N1 + R * F) * 2
-        dgrad = (R * H + E * F * H + 2 * R * N1) * 2
-    return {
-        "gemm_fc1_fprop": fc1,
-        "gemm_fc2_fprop": (R * F + E * F * H + R * H) * 2,
-        "gemm_fc2_dgrad": dgrad,
-        "gemm_fc2_wgrad": (R * F + R * H + E * F * H) * 2,
-        "gemm_fc1_dgrad": (R * N1 + E * N1 * H + R * H) * 2,
-        "gemm_fc1_wgrad": (R * N1 + R * H + E * N1 * H) * 2,
-        "gather_x": (R_cap * H + R * H) * 2, "gather_dy": (R_cap * H + R * H) * 2,
-        "combine_y": (R * H + T * H) * 2, "combine_dx": (R * H + T * H) * 2,
+    common = {
+        "gather_x": R_cap * H * 2 + R * H * 2, "gather_dy": R_cap * H * 2 + R * H * 2,
+        "combine_y": R * H * 2 + T * H * 2, "combine_dx": R * H * 2 + T * H * 2,
     }
+    if cfg.precision == "bf16":
+        s = 2.0
+        out = {"gemm_fc1_fprop": R * H * s + E * N1 * H * s + R * N1 * 2 + R * F * 2,
+               "gemm_fc2_dgrad": R * H * s + E * F * H * s + R * N1 * 2 + R * N1 * 2}
+    elif cfg.precision == "nvfp4":
+        s = 0.5 + 1.0 / 16.0
+        out = {"gemm_fc1_fprop": R * H * s + E * N1 * H * s + R * N1 * 2 + R * F * 2,
+               "gemm_fc2_dgrad": R * H * s + E * F * H * s + R * N1 * 2 + R * N1 * 2,
+               # bf16 in, row-wise and transposed copies out
+               "nvfp4_quant_x": R_cap * H * (2 + 2 * s), "nvfp4_quant_dy": R_cap * H * (2 + 2 * s),
+               "nvfp4_quant_a": R_cap * F * (2 + 2 * s),
+               "nvfp4_quant_dz": R_cap * N1 * (2 + 2 * s),
+               "nvfp4_quant_w1": E * N1 * H * (2 + 2 * s),
+               "nvfp4_quant_w2": E * F * H * (2 + 2 * s),
+               "nvfp4_amax_w1": E * N1 * H * 2, "nvfp4_amax_w2": E * F * H * 2}
+    else:  # mxfp8: the fused epilogues write the quantised A and dZ copies (both directions)
+        s = 33.0 / 32.0
+        out = {"gemm_fc1_fprop": R * H * s + E * N1 * H * s + R * N1 * 2 + 2 * R * F * s,
+               "gemm_fc2_dgrad": R * H * s + E * F * H * s + R * N1 * 2 + 2 * R * N1 * s,
+               "mxfp8_quant_x": R_cap * H * (2 + 2 * s), "mxfp8_quant_dy": R_cap * H * (2 + 2 * s),
+               "mxfp8_quant_w1": E * N1 * H * (2 + 2 * s),
+               "mxfp8_quant_w2": E * F * H * (2 + 2 * s)}
+    out.update({
+        "gemm_fc2_fprop": R * F * s + E * F * H * s + R * H * 2,
+        "gemm_fc2_wgrad": R * F * s + R * H * s + E * F * H * 2,
+        "gemm_fc1_dgrad": R * N1 * s + E * N1 * H * s + R * H * 2,
+        "gemm_fc1_wgrad": R * N1 * s + R * H * s + E * N1 * H * 2,
+    })
+    if recompute:  # no Z written or read; X and W1 read a second time
+        out["gemm_fc1_fprop"] -= R * N1 * 2
+        out["gemm_fc2_dgrad"] += R * H * s + E * N1 * H * s - R * N1 * 2
+    out.update(common)
+    return out
 
 
 def load_peaks():

@@ -269,7 +269,8 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // bf16 tensor map, 128-byte swizzle. dims/box innermost first; strides in bytes for dims 1..
 inline bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-               const uint64_t* strides, const uint32_t* box, CUtensorMapDataType dt) {
+               const uint64_t* strides, const uint32_t* box, CUtensorMapDataType dt,
+               CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint32_t estr[3] = {1, 1, 1};
@@ -277,7 +278,7 @@ inline bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t
                   reinterpret_cast<const cuuint64_t*>(dims),
                   reinterpret_cast<const cuuint64_t*>(strides),
                   reinterpret_cast<const cuuint32_t*>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

@@ -45,6 +45,9 @@ constexpr int kMaxStages = 5;
 constexpr int ILV = 64;       // gate/linear interleave of the packed FC1 columns
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
+#ifndef FP4_DGLU_WARPS
+#define FP4_DGLU_WARPS 8
+#endif
 constexpr int kMaxE = 256;
 constexpr int kTmemCols = 512;
 
@@ -62,7 +65,13 @@ template <int EPI>
 struct Fp4Cfg {
   static constexpr int BN = EPI == EPI_DGLU ? 128 : 256;
   static constexpr int NACC = EPI == EPI_DGLU ? 2 : 1;
-  static constexpr int STAGES = 4;
+  // the dGLU epilogue (saved-Z loads, activation gradient, rotated amax) outlasts the tile's
+  // MMAs with eight warps: it takes FP4_DGLU_WARPS, each lane quadrant's warps dealing the
+  // tile's 16-column chunks round-robin, with one stage fewer to make room for their buffers
+  static constexpr int EW = EPI == EPI_DGLU ? FP4_DGLU_WARPS : kEpiWarps;
+  static constexpr int EWQ = EW / 4;  // warps per lane quadrant
+  static constexpr int THREADS = 64 + 32 * EW;
+  static constexpr int STAGES = EPI == EPI_DGLU && EW > 8 ? 3 : 4;
   static constexpr int B_BYTES = BN * BKB;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int SFB_SLAB = BN * 4;
@@ -72,22 +81,21 @@ struct Fp4Cfg {
   static constexpr int SF_COL0 = NACC * BN;
   static constexpr int SF_OFF = STAGES * STAGE_BYTES;
   static constexpr int ZQ_OFF = SF_OFF + STAGES * SF_STAGE;
-  static constexpr int XT_OFF = ZQ_OFF + (EPI == EPI_DGLU ? kEpiWarps * ZQ_WARP : 0);
-  static constexpr int CTRL_OFF = XT_OFF + (EPI == EPI_DGLU ? kEpiWarps * XT_WARP : 0);
+  static constexpr int XT_OFF = ZQ_OFF + (EPI == EPI_DGLU ? EW * ZQ_WARP : 0);
+  static constexpr int CTRL_OFF = XT_OFF + (EPI == EPI_DGLU ? EW * XT_WARP : 0);
   static constexpr int TOTAL = CTRL_OFF + 4096 + 1024;
   static_assert(TOTAL <= 232448, "shared memory above the per-block limit");
   static_assert(SF_COL0 + STAGES * SF_COLS_STAGE <= kTmemCols, "TMEM map");
   static_assert(STAGES <= kMaxStages, "barrier arrays");
+  static_assert(EWQ * 4 == EW && THREADS <= 1024, "whole lane quadrants");
   static_assert(ZQ_OFF % 16 == 0 && XT_OFF % 16 == 0 && CTRL_OFF % 8 == 0, "alignment");
 };
 
 struct Fp4Args {
   CUtensorMap tmA;
   CUtensorMap tmB;
-  const uint8_t* sfa;
-  int64_t sfa_pad;
-  const uint8_t* sfb;
-  int64_t sfb_pad;
+  CUtensorMap tmSFA;  // A's scale slabs: boxes of 128 rows x the four slabs of a k-block
+  CUtensorMap tmSFB;  // B's: BN rows x four slabs
   const int32_t* offsets;
   int E;
   int R_cap;
@@ -242,7 +250,8 @@ MOE_DEVICE float rht_amax_tile32(uint32_t* xt, const uint32_t (&w)[16], uint32_t
 MOE_DEVICE int gate_col(int f) { return ((f & ~(ILV - 1)) << 1) | (f & (ILV - 1)); }
 
 template <int EPI, int KIND, bool KG, bool EXT = false>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __grid_constant__ Fp4Args p) {
+__global__ void __launch_bounds__(Fp4Cfg<EPI>::THREADS, 1)
+    grouped_gemm_fp4_kernel(const __grid_constant__ Fp4Args p) {
   MOE_GRIDDEP_ENTRY();
   constexpr bool kGated = KIND != MOE_ACT_SRELU;
   static_assert(!EXT || (kGated && EPI != EPI_STORE), "extras: gated GLU / dGLU epilogues");
@@ -266,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c.tfull[i], 1);
-      mbar_init(&c.tempty[i], kEpiWarps);
+      mbar_init(&c.tempty[i], L::EW);
     }
     mbar_init(&c.drain, 1);
     fence_mbar_init();
@@ -295,6 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tmA);
     tma_prefetch_desc(&p.tmB);
+    tma_prefetch_desc(&p.tmSFA);
+    tma_prefetch_desc(&p.tmSFB);
   }
   if (warp == 1) {
     tmem_alloc(&c.tmem_base, kTmemCols);
@@ -337,16 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
 #pragma unroll
           for (int h = 0; h < BN / 128; ++h)
             tma_load_2d(sB + h * (128 * BKB), &p.tmB, bar, b_k / 2, b_row + 128 * h);
-          // four 64-value scale slabs of each operand: A's 128 rows, B's BN rows
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            bulk_load(sf + s * SFA_SLAB,
-                      p.sfa + ((int64_t)(a_k / MMA_K + s) * p.sfa_pad + a_row) * 4, SFA_SLAB,
-                      bar);
-            bulk_load(sf + 4 * SFA_SLAB + s * L::SFB_SLAB,
-                      p.sfb + ((int64_t)(b_k / MMA_K + s) * p.sfb_pad + b_row) * 4, L::SFB_SLAB,
-                      bar);
-          }
+          // the four 64-value scale slabs of each operand in one copy each (A's 128 rows,
+          // B's BN rows; slab s lands at s x rows x 4 bytes)
+          tma_load_2d(sf, &p.tmSFA, bar, a_row, a_k / MMA_K);
+          tma_load_2d(sf + 4 * SFA_SLAB, &p.tmSFB, bar, b_row, b_k / MMA_K);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -428,10 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue warps 2..9
+    // ------------------------------------------------------------ epilogue warps 2..
     // Control flow stays warp-uniform (the shared-memory transposes are warp-wide).
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int half = (warp - 2) >> 2;  // STORE and GLU: which 128 (BN / 2) columns
+    const int ws = (warp - 2) >> 2;    // dGLU: this warp's slot among its quadrant's EWQ
     const uint32_t zq = smem_u32(smem + L::ZQ_OFF + (warp - 2) * ZQ_WARP);
     const uint8_t* zq_ptr = smem + L::ZQ_OFF + (warp - 2) * ZQ_WARP;
     uint32_t* xt = reinterpret_cast<uint32_t*>(smem + L::XT_OFF + (warp - 2) * XT_WARP);
@@ -459,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
       const float prob = EPI == EPI_STORE ? 0.f : p.row_prob[row];
       if constexpr (EPI == EPI_DGLU) {
         // the first step's saved Z comes in while the MMAs run
-        const int f0 = t.n0 + half * 64;
+        const int f0 = t.n0 + 16 * ws;
         if (f0 < p.N)
           zq_issue(zq, p.z + (int64_t)row * p.ldz + (kGated ? gate_col(f0) : f0), kGated, lane);
       }
@@ -574,30 +580,32 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
             m_rht = fmaxf(m_rht, fabsf(rht16_lanes(v[i], p.rht_mask, lane)));
           }
         }
-      } else {  // EPI_DGLU: accumulator = dA_s over F columns; this half: 64 of them
+      } else {  // EPI_DGLU: accumulator = dA_s over F columns; chunks ws, ws + EWQ, ...
         const uint16_t* zrow = p.z + (int64_t)row * p.ldz;
         uint16_t* dzrow = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo;
         float dp = 0.f;
+        constexpr int EWQ = L::EWQ;
 #pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
-          const int f0 = t.n0 + half * 64 + 16 * j;
+        for (int j = ws, step = 0; j < BN / 16; j += EWQ, ++step) {
+          const int f0 = t.n0 + 16 * j;
           if (f0 >= p.N) break;
           const int gc = kGated ? gate_col(f0) : f0;
           // next step's Z into the other buffer (this lane finished reading it in the previous
           // step), then wait for this step's
-          const bool more = j + 1 < 4 && f0 + 16 < p.N;
+          const int fn = f0 + 16 * EWQ;
+          const bool more = j + EWQ < BN / 16 && fn < p.N;
           if (more) {
-            zq_issue(zq + ((j + 1) & 1) * ZQ_BUF, zrow + (kGated ? gate_col(f0 + 16) : f0 + 16),
-                     kGated, lane);
+            zq_issue(zq + ((step + 1) & 1) * ZQ_BUF, zrow + (kGated ? gate_col(fn) : fn), kGated,
+                     lane);
             asm volatile("cp.async.wait_group 1;" ::: "memory");
           } else {
             asm volatile("cp.async.wait_group 0;" ::: "memory");
           }
           uint32_t dr[16];
-          tmem_ld_32x32b_x16(tacc + half * 64 + 16 * j, dr);
+          tmem_ld_32x32b_x16(tacc + 16 * j, dr);
           uint32_t gw[8], lw[8];
           {
-            const uint8_t* b = zq_ptr + (j & 1) * ZQ_BUF;
+            const uint8_t* b = zq_ptr + (step & 1) * ZQ_BUF;
             const uint4 g0 = *reinterpret_cast<const uint4*>(b + zq_slot(lane, 0));
             const uint4 g1 = *reinterpret_cast<const uint4*>(b + zq_slot(lane, 1));
             gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w;
@@ -674,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
         __syncwarp();
         if (lane == 0) mbar_arrive(&c.tempty[acc]);
         ++acc_i;
-        p.dprob_part[(int64_t)row * p.nparts + (t.n0 / BN) * 2 + half] = dp;
+        p.dprob_part[(int64_t)row * p.nparts + (t.n0 / BN) * EWQ + ws] = dp;
       }
     }
     if constexpr (EPI == EPI_DGLU) asm volatile("cp.async.wait_all;" ::: "memory");
@@ -693,6 +701,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp4_kernel(const __g
   }
 }
 
+// The E4M3 scales of a K-major NVFP4 operand: slab g (64 values of K) holds 4 bytes a row for
+// s_pad rows, slabs back to back. As a 2-D tensor of 32-bit words [slabs, s_pad], boxes of
+// box_rows words x 4 slabs: one copy brings the four slabs of a 256-value k-block, in the
+// same order in shared memory. Slabs past the operand's K read as zeros.
+bool tmap_fp4_sf(CUtensorMap* m, const MxOperand& t, uint32_t box_rows) {
+  uint64_t dims[2] = {(uint64_t)t.s_pad, (uint64_t)((t.cols + 63) / 64)};
+  uint64_t strides[1] = {(uint64_t)t.s_pad * 4};
+  uint32_t box[2] = {box_rows, 4};
+  return make_tmap(m, t.s, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT32,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 // K-major NVFP4 operand: packed codes [rows, cols / 2] bytes, boxes of 128 rows x 128 bytes.
 bool tmap_fp4(CUtensorMap* m, const MxOperand& t) {
   uint64_t dims[2] = {(uint64_t)(t.cols / 2), (uint64_t)t.rows};
@@ -706,7 +726,7 @@ cudaError_t launch_fp4(const Fp4Args& a, int grid, cudaStream_t s, int kid) {
   auto kern = grouped_gemm_fp4_kernel<EPI, KIND, KG, EXT>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), Fp4Cfg<EPI>::TOTAL);
   if (e != cudaSuccess) return e;
-  launch_kernel(kern, grid, kThreads, Fp4Cfg<EPI>::TOTAL, s, nullptr, 0, a);
+  launch_kernel(kern, grid, Fp4Cfg<EPI>::THREADS, Fp4Cfg<EPI>::TOTAL, s, nullptr, 0, a);
   count_launch(s, kid);
   return cudaGetLastError();
 }
@@ -735,8 +755,8 @@ cudaError_t launch_act_family(const Fp4Args& a, int kind, int grid, cudaStream_t
 }  // namespace
 
 int dprob_parts_fp4(int F) {
-  constexpr int bn = Fp4Cfg<EPI_DGLU>::BN;
-  return 2 * ((F + bn - 1) / bn);
+  using L = Fp4Cfg<EPI_DGLU>;
+  return L::EWQ * ((F + L::BN - 1) / L::BN);
 }
 
 cudaError_t launch_grouped_gemm_fp4(const Fp4Problem& p, cudaStream_t s) {
@@ -804,9 +824,11 @@ cudaError_t launch_grouped_gemm_fp4(const Fp4Problem& p, cudaStream_t s) {
       a.amax_a = p.amax + AM_DZT; a.amax_b = p.amax + AM_XT;
       break;
   }
-  if (!tmap_fp4(&a.tmA, *A) || !tmap_fp4(&a.tmB, *B)) return cudaErrorInvalidValue;
-  a.sfa = A->s; a.sfa_pad = A->s_pad;
-  a.sfb = B->s; a.sfb_pad = B->s_pad;
+  constexpr int bn_max = Fp4Cfg<EPI_STORE>::BN, bn_dglu = Fp4Cfg<EPI_DGLU>::BN;
+  const uint32_t sfb_rows = p.role == ROLE_FC2_DGRAD ? bn_dglu : bn_max;
+  if (!tmap_fp4(&a.tmA, *A) || !tmap_fp4(&a.tmB, *B) || !tmap_fp4_sf(&a.tmSFA, *A, BM) ||
+      !tmap_fp4_sf(&a.tmSFB, *B, sfb_rows))
+    return cudaErrorInvalidValue;
   a.wide = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0 && a.ldo % 16 == 0 &&
            a.out_estride % 16 == 0;
   const int kid = kKid[p.role];
@@ -865,8 +887,8 @@ struct Rc4Args {
   CUtensorMap tmW2;  // W2 row-wise copy [E*Fp, H/2], box {128 B, 64 rows}
   CUtensorMap tmX;   // X row-wise copy [R_cap, H/2], box {128 B, 128 rows}
   CUtensorMap tmW1;  // W1p row-wise copy [E*N1p, H/2], box {128 B, 128 (gated) / 64 rows}
-  const uint8_t *sf_dy, *sf_w2, *sf_x, *sf_w1;
-  int64_t pad_dy, pad_w2, pad_x, pad_w1;
+  // their scales: boxes of 128 rows (whole 128-row slabs for the weights) x four slabs
+  CUtensorMap tmSdy, tmSw2, tmSx, tmSw1;
   const float *amax_dy, *amax_w2, *amax_x, *amax_w1;
   const int32_t* offsets;
   int E, R_cap, H, F, N1, Fp, N1p;
@@ -946,6 +968,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&p.tmW2);
     tma_prefetch_desc(&p.tmX);
     tma_prefetch_desc(&p.tmW1);
+    tma_prefetch_desc(&p.tmSdy);
+    tma_prefetch_desc(&p.tmSw2);
+    tma_prefetch_desc(&p.tmSx);
+    tma_prefetch_desc(&p.tmSw1);
   }
   if (warp == 1) {
     tmem_alloc(&c.tmem_base, kTmemCols);
@@ -997,18 +1023,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(s0 + RC4_A, &p.tmW2, bar, k0 / 2, w2_row);
           tma_load_2d(s0 + RC4_A + RC4_B1, &p.tmX, bar, k0 / 2, m0);
           tma_load_2d(s0 + 2 * RC4_A + RC4_B1, &p.tmW1, bar, k0 / 2, w1_row);
-          // the four 64-value scale slabs of each operand (whole 128-row slabs of the weights)
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            const int64_t kg = k0 / MMA_K + s;
-            bulk_load(sf + s * SFA_SLAB, p.sf_dy + (kg * p.pad_dy + m0) * 4, SFA_SLAB, bar);
-            bulk_load(sf + 4 * SFA_SLAB + s * SFA_SLAB, p.sf_w2 + (kg * p.pad_w2 + w2_slab) * 4,
-                      SFA_SLAB, bar);
-            bulk_load(sf + 8 * SFA_SLAB + s * SFA_SLAB, p.sf_x + (kg * p.pad_x + m0) * 4,
-                      SFA_SLAB, bar);
-            bulk_load(sf + 12 * SFA_SLAB + s * SFA_SLAB, p.sf_w1 + (kg * p.pad_w1 + w1_slab) * 4,
-                      SFA_SLAB, bar);
-          }
+          // the four 64-value scale slabs of each operand, one copy each (whole 128-row
+          // slabs of the weights)
+          const int kg = k0 / MMA_K;
+          tma_load_2d(sf, &p.tmSdy, bar, m0, kg);
+          tma_load_2d(sf + 4 * SFA_SLAB, &p.tmSw2, bar, w2_slab, kg);
+          tma_load_2d(sf + 8 * SFA_SLAB, &p.tmSx, bar, m0, kg);
+          tma_load_2d(sf + 12 * SFA_SLAB, &p.tmSw1, bar, w1_slab, kg);
           if (++stage == RC4_STAGES) {
             stage = 0;
             phase ^= 1;
@@ -1210,10 +1231,9 @@ cudaError_t launch_fc2_dgrad_recompute_fp4(const Fp4Problem& p, cudaStream_t s) 
       !tmap_fp4_rows(&a.tmX, p.x, BM) ||
       !tmap_fp4_rows(&a.tmW1, p.w1, p.gated ? 2 * RC4_BNA : RC4_BNA))
     return cudaErrorInvalidValue;
-  a.sf_dy = p.dy.s; a.pad_dy = p.dy.s_pad;
-  a.sf_w2 = p.w2.s; a.pad_w2 = p.w2.s_pad;
-  a.sf_x = p.x.s; a.pad_x = p.x.s_pad;
-  a.sf_w1 = p.w1.s; a.pad_w1 = p.w1.s_pad;
+  if (!tmap_fp4_sf(&a.tmSdy, p.dy, BM) || !tmap_fp4_sf(&a.tmSw2, p.w2, BM) ||
+      !tmap_fp4_sf(&a.tmSx, p.x, BM) || !tmap_fp4_sf(&a.tmSw1, p.w1, BM))
+    return cudaErrorInvalidValue;
   a.amax_dy = p.amax + AM_DY; a.amax_w2 = p.amax + AM_W2;
   a.amax_x = p.amax + AM_X; a.amax_w1 = p.amax + AM_W1;
   a.offsets = p.offsets;

@@ -1,4 +1,4 @@
-// Helpers shared by the grouped GEMM kernels (bf16 and MXFP8): fp32 activation math of the
+// Helpers shared by the grouped GEMM kernels (BF16, MXFP8, NVFP4): fp32 activation math of the
 // GLU epilogues, 32-wide bf16 load/store, and host-side TMA tensor-map construction.
 #pragma once
 

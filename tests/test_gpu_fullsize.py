@@ -66,6 +66,18 @@ def _weight_experts(experts, counts):
                                   "gptoss_srelu_bf16", "gptoss_geglu_mxfp8",
                                   "gptoss_srelu_mxfp8"])
 def test_fullsize_sampled_parity(lib, name):
+    _sampled_parity(name, recompute=False)
+
+
+@pytest.mark.parametrize("name", ["mixtral_bf16", "mixtral_mxfp8"])
+def test_fullsize_recompute_sampled_parity(lib, name):
+    """The same sampled checks with activation recomputation (no saved FC1 output; the
+    FC2-dgrad kernel rebuilds it in fp32 next to dA_s, so the oracle forms dZ from unrounded
+    Z and dA_s), in the launch configuration `bench.py --recompute` times."""
+    _sampled_parity(name, recompute=True)
+
+
+def _sampled_parity(name, recompute):
     cfg = synth.CONFIGS[name]
     mx = cfg.precision == "mxfp8"
     tol = MX_TOL if mx else BF16_TOL
@@ -77,7 +89,9 @@ def test_fullsize_sampled_parity(lib, name):
     x = synth.gen_x(cfg)
     dy = synth.gen_dy(cfg)
     # ---------------------------------------------------------------- GPU, bench launch config
-    layer = g.MoELayer(g.desc_from_config(cfg))
+    layer = g.MoELayer(g.desc_from_config(cfg, recompute=recompute))
+    if recompute:
+        assert layer.layout.z == 2 ** 64 - 1
     w1p = torch.empty(cfg.E, cfg.N1, cfg.H, dtype=torch.bfloat16, device="cuda")
     w2 = torch.empty(cfg.E, cfg.F, cfg.H, dtype=torch.bfloat16, device="cuda")
     for e in range(cfg.E):       # upload (and repack) one expert at a time
@@ -117,7 +131,8 @@ def test_fullsize_sampled_parity(lib, name):
             p = probs[toks[i], j:j + 1]
             Z, a, a_s, Y = om.expert_forward(xs[i:i + 1], W1, W2, p, act, mx, wq)
             _, dX, _, _, d_prob = om.expert_backward(xs[i:i + 1], W1, W2, p, Z, a, a_s,
-                                                     dys[i:i + 1], act, mx, wq)
+                                                     dys[i:i + 1], act, mx, wq,
+                                                     recompute=recompute)
             y_ref[i] += Y[0]
             dx_ref[i] += dX[0]
             dp_ref[i, j] = d_prob[0]
@@ -144,9 +159,10 @@ def test_fullsize_sampled_parity(lib, name):
         fs_t, hs_t = torch.as_tensor(fs, device="cuda"), torch.as_tensor(hs, device="cuda")
         errs[f"dW2[{e}]"] = rel_fro(to_np(dw2[e][fs_t][:, hs_t]), dW2_ref)
         # dW1[h, n] = sum_r X[r, h] dZ[r, n] for n = gate f and linear f; in MXFP8 dZ comes
-        # from bf16 Z and bf16 dA_s (oracle reading R15)
-        dA = p * _bf(_fq(dY, 1, mx) @ wq.w2_h[fs].T, mx)
-        Zg, Zl = _bf(Zg, mx), (_bf(Zl, mx) if Zl is not None else None)
+        # from bf16 Z and bf16 dA_s (oracle reading R15), from fp32 ones when recomputed
+        rb = mx and not recompute
+        dA = p * _bf(_fq(dY, 1, mx) @ wq.w2_h[fs].T, rb)
+        Zg, Zl = _bf(Zg, rb), (_bf(Zl, rb) if Zl is not None else None)
         if cfg.gated:
             dG, dL = om.act_backward(act, Zg, Zl, dA)
             dZ = np.concatenate([dG, dL], axis=1)

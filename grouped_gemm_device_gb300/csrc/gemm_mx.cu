@@ -35,6 +35,12 @@ constexpr int MMA_K = 32;
 constexpr int kMaxStages = 6;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
+// epilogue warps of the one-CTA dGLU kernel, each lane quadrant's warps dealing the tile's
+// eight 32-column chunks round-robin (measured: twelve warps, 128 registers a thread, ran the
+// GPT-OSS-shaped dGLU 5% faster and the Mixtral-shaped one 4% slower than eight)
+#ifndef MX_DGLU_WARPS
+#define MX_DGLU_WARPS 8
+#endif
 constexpr int kMaxE = 256;
 constexpr int kSfCol = BN;  // first TMEM column of the per-stage scale factors
 constexpr int kPackCol = 320;  // dGLU: the drained accumulator as packed bf16 (128 columns)
@@ -95,8 +101,14 @@ constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int SFA_BYTES = 512;   // 128 rows x 4 k-blocks
 constexpr int SFB_BYTES = 1024;  // 256 rows x 4 k-blocks
-constexpr int XP_ROW = 80;  // bytes per row of the per-warp 32 x 32 bf16 staging tile (+16 pad)
-constexpr int XPOSE_WARP_BYTES = 32 * XP_ROW + 32 * 4;  // staging tile + 32 column 2^-e
+constexpr int kCtrlBytes = 2560;  // the control block (barriers, expert table), below
+
+// per-warp 32 x 32 bf16 staging tile of the column-wise quantisation: 64-byte rows whose
+// four 16-byte pieces are XOR-rotated by (row / 2) % 4, which spreads a warp's row writes over
+// all banks without padding; then 32 column factors 2^-e
+constexpr int XP_ROW = 64;
+constexpr int XPOSE_WARP_BYTES = 32 * XP_ROW + 32 * 4;
+MOE_DEVICE int xp_piece(int row, int piece) { return row * XP_ROW + ((piece ^ ((row >> 1) & 3)) << 4); }
 constexpr int ZST_WARP_BYTES = 32 * 128;  // dGLU: saved Z of one chunk, 32 rows x 64 bf16
 constexpr int TST_WARP_BYTES = 32 * 128;  // TMA-store staging: 32 rows x 64 bf16, 128B swizzle
 
@@ -108,18 +120,22 @@ constexpr int TST_WARP_BYTES = 32 * 128;  // TMA-store staging: 32 rows x 64 bf1
 // 32 x 64-column bf16 box a warp at a time), which takes one stage's room.
 template <int EPI, bool PAIR = false, bool TST = false>
 struct MxSmem {
+  static constexpr int EW = EPI == 2 && !PAIR ? MX_DGLU_WARPS : kEpiWarps;  // epilogue warps
+  static constexpr int EWQ = EW / 4;                                        // per lane quadrant
+  static constexpr int THREADS = 64 + 32 * EW;
   static constexpr int STAGES = TST ? 3 : PAIR ? (EPI == 0 ? 6 : 5) : (EPI == 2 ? 3 : 4);
   static constexpr int STAGE_BYTES_ = A_BYTES + (PAIR ? B_BYTES / 2 : B_BYTES);
   static constexpr int DATA = STAGES * STAGE_BYTES_;
   static constexpr int SF_OFF = DATA;
   static constexpr int XPOSE_OFF = SF_OFF + STAGES * (SFA_BYTES + SFB_BYTES);
-  static constexpr int ZST_OFF = XPOSE_OFF + (EPI == 0 ? 0 : kEpiWarps * XPOSE_WARP_BYTES);
-  static constexpr int TST_OFF = (ZST_OFF + (EPI == 2 ? kEpiWarps * ZST_WARP_BYTES : 0) + 1023) / 1024 * 1024;
-  static constexpr int CTRL_OFF = TST_OFF + (TST ? kEpiWarps * TST_WARP_BYTES : 0);
-  static constexpr int TOTAL = CTRL_OFF + 4096 + 1024;
+  static constexpr int ZST_OFF = XPOSE_OFF + (EPI == 0 ? 0 : EW * XPOSE_WARP_BYTES);
+  static constexpr int TST_OFF = (ZST_OFF + (EPI == 2 ? EW * ZST_WARP_BYTES : 0) + 1023) / 1024 * 1024;
+  static constexpr int CTRL_OFF = TST_OFF + (TST ? EW * TST_WARP_BYTES : 0);
+  static constexpr int TOTAL = CTRL_OFF + kCtrlBytes + 1024;
   static_assert(TOTAL <= 232448, "shared memory above the sm_100 per-block limit");
   static_assert(XPOSE_OFF % 16 == 0 && ZST_OFF % 128 == 0 && CTRL_OFF % 8 == 0, "alignment");
   static_assert(STAGES <= kMaxStages, "control barriers");
+  static_assert(EWQ * 4 == EW && THREADS <= 1024, "whole lane quadrants");
   // scale columns of every stage below the dGLU's packed accumulator
   static_assert(EPI != 2 || kSfCol + 12 * STAGES <= kPackCol, "TMEM scale columns");
   static_assert(kSfCol + 12 * STAGES <= kTmemCols, "TMEM scale columns");
@@ -137,6 +153,7 @@ struct Ctrl {
   int off[kMaxE + 1];
   int prefix[kMaxE + 1];
 };
+static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
 struct TileInfo {
   int e, m0, n0, kbeg, klen, nkb, row_end;
@@ -194,7 +211,6 @@ MOE_DEVICE void mx_row_block(const float (&v)[32], uint8_t* qdst, uint8_t* sdst)
 MOE_DEVICE void mx_col_block(const float (&v)[32], uint8_t* xs, uint8_t* qdst, uint8_t* s_col,
                              int64_t col0, int64_t kb, int64_t s_pad, int lane) {
   float* xinv = reinterpret_cast<float*>(xs + 32 * XP_ROW);
-  uint4* mine = reinterpret_cast<uint4*>(xs + lane * XP_ROW);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     uint32_t w[4];
@@ -202,17 +218,19 @@ MOE_DEVICE void mx_col_block(const float (&v)[32], uint8_t* xs, uint8_t* qdst, u
     for (int i = 0; i < 4; ++i)
       w[i] = __byte_perm(__float_as_uint(v[8 * k + 2 * i]), __float_as_uint(v[8 * k + 2 * i + 1]),
                          0x7632) & 0x7FFF7FFFu;
-    mine[k] = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(xs + xp_piece(lane, k)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   __syncwarp();
   const int jp = lane & 15, rh = lane >> 4;
-  const uint8_t* col = xs + rh * 16 * XP_ROW + 4 * jp;
+  // column pair jp sits in piece jp / 4 of every row, word jp % 4 of it (rows rh*16 + r share
+  // the piece rotation of row r, rh*16 being a multiple of 8)
+  const uint8_t* col = xs + rh * 16 * XP_ROW + 4 * (jp & 3);
   uint32_t m0 = 0, m1 = 0;
 #pragma unroll
   for (int r = 0; r < 16; r += 2) {
     uint32_t t0, t1;
-    asm("max.u16x2 %0, %1, %2;" : "=r"(t0) : "r"(m0), "r"(*reinterpret_cast<const uint32_t*>(col + r * XP_ROW)));
-    asm("max.u16x2 %0, %1, %2;" : "=r"(t1) : "r"(m1), "r"(*reinterpret_cast<const uint32_t*>(col + (r + 1) * XP_ROW)));
+    asm("max.u16x2 %0, %1, %2;" : "=r"(t0) : "r"(m0), "r"(*reinterpret_cast<const uint32_t*>(col + xp_piece(r, jp >> 2))));
+    asm("max.u16x2 %0, %1, %2;" : "=r"(t1) : "r"(m1), "r"(*reinterpret_cast<const uint32_t*>(col + xp_piece(r + 1, jp >> 2))));
     m0 = t0;
     m1 = t1;
   }
@@ -261,7 +279,8 @@ MOE_DEVICE int gate_col(int f, int ilv) { return ((f & ~(ilv - 1)) << 1) | (f & 
 // sends it with one TMA store; an expert without rows stores zeros the same way.
 template <int EPI, int KIND, bool KG, int ILV, bool A_MN, bool B_MN, bool PAIR = false,
           bool EXT = false, bool TST = false>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __grid_constant__ MxArgs p) {
+__global__ void __launch_bounds__(MxSmem<EPI, PAIR, TST>::THREADS, 1)
+    grouped_gemm_mx_kernel(const __grid_constant__ MxArgs p) {
   MOE_GRIDDEP_ENTRY();
   constexpr bool kGated = KIND != MOE_ACT_SRELU;
   static_assert(!TST || (EPI == EPI_STORE && KG && !PAIR), "TMA stores: weight gradients");
@@ -287,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
       mbar_init(&c.empty[s], 1);
     }
     mbar_init(&c.tfull, 1);
-    mbar_init(&c.tempty, PAIR ? 2 * kEpiWarps : kEpiWarps);
+    mbar_init(&c.tempty, PAIR ? 2 * L::EW : L::EW);
     mbar_init(&c.drain, 1);
     fence_mbar_init();
     c.abort = 0;
@@ -484,9 +503,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue warps 2..9
+    // ------------------------------------------------------------ epilogue warps 2..
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;  // columns [128*half, 128*half + 128) of the tile
+    const int half = (warp - 2) >> 2;  // STORE, GLU: columns [128*half, 128*half + 128)
+    // dGLU: this warp's slot among its lane quadrant's EWQ warps; it takes the tile's 32-column
+    // chunks ws, ws + EWQ, ...
+    constexpr int EWQ = L::EWQ;
+    const int ws = (warp - 2) >> 2;
     uint8_t* xs = smem + L::XPOSE_OFF + (warp - 2) * XPOSE_WARP_BYTES;
     const uint8_t* zst = smem + L::ZST_OFF + (warp - 2) * ZST_WARP_BYTES;
     const uint32_t zst_a = smem_u32(zst);
@@ -573,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
       const uint16_t* zrow = p.z + (int64_t)row * p.ldz;
       if constexpr (EPI == EPI_DGLU) {
         // the saved Z of the first chunk comes in while the MMAs run
-        const int f0 = t.n0 + cb;
+        const int f0 = t.n0 + 32 * ws;
         if (f0 < p.N && half_live) {
           const int gc = kGated ? gate_col(f0, p.ilv) : f0;
           zst_issue(zst_a, zrow + gc, zrow + gc + p.ilv, lane, kGated);
@@ -669,26 +692,33 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
       // STORE: drain 128 accumulator columns into registers as packed bf16; dGLU: pack them
       // into this warp's 64 columns of the TMEM packed area instead (registers stay free for
       // the dGLU math). Either way the fp32 accumulator is released before any other work.
-      const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + cb;
-      const uint32_t tpk = tmem_base + ((uint32_t)(q * 32) << 16) + kPackCol + half * 64;
+      const uint32_t tq = tmem_base + ((uint32_t)(q * 32) << 16);  // this lane quadrant
       uint32_t pk[EPI == EPI_STORE ? 64 : 1];
+      if constexpr (EPI == EPI_STORE) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tacc + 32 * j, r);
-        tmem_ld_wait();
-        uint32_t w[16];
+        for (int j = 0; j < 4; ++j) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tq + cb + 32 * j, r);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-        if constexpr (EPI == EPI_STORE) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pk[16 * j + i] = w[i];
-        } else {
-          tmem_st_32x32b_x16(tpk + 16 * j, w);
+          for (int i = 0; i < 16; ++i)
+            pk[16 * j + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
         }
+      } else {
+        // chunk c (32 columns) packs into TMEM columns kPackCol + 16 c
+#pragma unroll 1
+        for (int c = ws; c < BN / 32; c += EWQ) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tq + 32 * c, r);
+          tmem_ld_wait();
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          tmem_st_32x32b_x16(tq + kPackCol + 16 * c, w);
+        }
+        tmem_st_wait();
       }
-      if constexpr (EPI != EPI_STORE) tmem_st_wait();
       release_acc();
       ++acc_i;
 
@@ -716,14 +746,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
         float dp0 = 0.f, dp1 = 0.f, dp2 = 0.f, dp3 = 0.f;
         uint8_t* qr = p.q_row + (int64_t)row * p.ld_q_row;
         uint8_t* qc = p.q_col + (int64_t)row * p.ld_q_col;
-        // one copy of the chunk body (keeps the kernel inside the instruction cache); chunk j
+        // one copy of the chunk body (keeps the kernel inside the instruction cache); chunk c
         // of the packed accumulator comes back from TMEM
 #pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
-          const int f0 = t.n0 + cb + 32 * j;
+        for (int c = ws; c < BN / 32; c += EWQ) {
+          const int f0 = t.n0 + 32 * c;
           if (f0 >= p.N) break;
           uint32_t cur[16];
-          tmem_ld_32x32b_x16(tpk + 16 * j, cur);
+          tmem_ld_32x32b_x16(tq + kPackCol + 16 * c, cur);
           tmem_ld_wait();
           const int gcol = kGated ? gate_col(f0, p.ilv) : f0;
           const int lcol = gcol + p.ilv;
@@ -768,8 +798,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
             }
           }
           // the next chunk's Z goes into the same buffer: this lane has read its row already
-          if (j + 1 < 4 && f0 + 32 < p.N) {
-            const int gn = kGated ? gate_col(f0 + 32, p.ilv) : f0 + 32;
+          if (c + EWQ < BN / 32 && f0 + 32 * EWQ < p.N) {
+            const int gn = kGated ? gate_col(f0 + 32 * EWQ, p.ilv) : f0 + 32 * EWQ;
             zst_issue(zst_a, zrow + gn, zrow + gn + p.ilv, lane, kGated);
           }
           mx_row_block(dg, qr + gcol, p.s_row + sf_mma_offset(row, gcol / 32, p.s_row_pad));
@@ -791,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_mx_kernel(const __gr
             part[p.N1 + f0 + lane] = ss;
           }
         }
-        p.dprob_part[(int64_t)row * p.nparts + (t.n0 / BN) * 2 + half] = (dp0 + dp1) + (dp2 + dp3);
+        p.dprob_part[(int64_t)row * p.nparts + (t.n0 / BN) * EWQ + ws] = (dp0 + dp1) + (dp2 + dp3);
       }
     }
     if constexpr (EPI == EPI_DGLU) asm volatile("cp.async.wait_all;" ::: "memory");
@@ -861,7 +891,7 @@ cudaError_t launch_mx(const MxArgs& a, int grid, cudaStream_t s, int kid) {
     constexpr int smem = MxSmem<EPI, false, TST>::TOTAL;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    launch_kernel(kern, grid, kThreads, smem, s, nullptr, 0, a);
+    launch_kernel(kern, grid, MxSmem<EPI, false, TST>::THREADS, smem, s, nullptr, 0, a);
     count_launch(s, kid);
     return cudaGetLastError();
   } else {
@@ -875,7 +905,7 @@ cudaError_t launch_mx(const MxArgs& a, int grid, cudaStream_t s, int kid) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(MxSmem<EPI, true>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
@@ -926,7 +956,7 @@ cudaError_t launch_glu_family(const MxArgs& a, int kind, int grid, cudaStream_t 
 
 }  // namespace
 
-int dprob_parts_mx(int F) { return 2 * ((F + BN - 1) / BN); }
+int dprob_parts_mx(int F) { return MxSmem<EPI_DGLU, kMxPairs>::EWQ * ((F + BN - 1) / BN); }
 
 // ------------------------------------------------------------------------------------------
 // FC2 dgrad with the FC1 output recomputed (activation recomputation, [NV-blog] "What's

@@ -850,44 +850,50 @@ cudaError_t launch_grouped_gemm_fp4(const Fp4Problem& p, cudaStream_t s) {
 
 // ----------------------------------------------------------------------------------------
 // FC2 dgrad with the FC1 output recomputed (activation recomputation, [NV-blog] "What's
-// next"), NVFP4 operands. Per 128-row x 64-column tile of dA_s two block-scaled FP4 GEMMs
+// next"), NVFP4 operands. Per 128-row x 128-column tile of dA_s two block-scaled FP4 GEMMs
 // share one loop over H (k-blocks of 256 values, four MMAs of K = 64 each):
-//   dA_s[rows, f0..f0+63]       = Q(dY)[rows] . Q_H(W2)[f0..f0+63]^T           (128 x 64)
-//   Z[rows, 2f0 .. 2f0+127]     = Q(X)[rows]  . Q_H(W1p)[2f0 .. 2f0+127]^T     (128 x 128)
-// (with the interleave of 64, packed W1 rows 2f0 .. 2f0+127 are exactly the gate and linear
-// columns of dA_s columns f0 .. f0+63; sReLU, not gated: Z[rows, f0..f0+63], 128 x 64). Both
-// scaled by 1 / (S_a S_b) of their operands. TMEM: dA_s columns 0-63, Z from 64, the stages'
-// scale factors from 192 (16 columns per MMA: dY, W2, X, W1). The 64 weight rows of a tile
-// are half of a 128-row scale slab: the whole slab is copied and the MMA's B scale address
-// starts at the slab's third column when the rows are its upper half. The epilogue reads
-// dA_s and Z in fp32 from TMEM and writes dZ in BF16 (packed order) with its amax and the amax
-// of its 16-row rotation, and the per-row d_prob partial of the tile, as the saved-Z dGLU
-// kernel does. One accumulator set; every wait is bounded.
+//   dA_s[rows, f0..f0+127]      = Q(dY)[rows] . Q_H(W2)[f0..f0+127]^T          (128 x 128)
+//   Z[rows, 2f0 .. 2f0+255]     = Q(X)[rows]  . Q_H(W1p)[2f0 .. 2f0+255]^T     (128 x 256)
+// (with the interleave of 64, packed W1 rows 2f0 .. 2f0+255 are the gate and linear columns of
+// dA_s columns f0 .. f0+127, in blocks of 64; sReLU, not gated: Z[rows, f0..f0+127], 128 x
+// 128). Both scaled by 1 / (S_a S_b) of their operands. TMEM: dA_s columns 0-127, Z 128-383
+// and, from 384, two scale buffers of 40 columns, one per half k-block (its two MMAs x dY 4,
+// W2 4, X 4, W1p 8 columns): a half k-block's copies wait (bounded) until the MMAs that read
+// the buffer one k-block earlier have completed, which the tensor pipe reaches while the other
+// half's MMAs keep it busy. Two stages of 80 KB operands and 10 KB of scale slabs. The epilogue
+// reads dA_s and Z in fp32 from TMEM and writes dZ in BF16 (packed order) with its amax and
+// the amax of its 16-row rotation, and the per-row d_prob partial of the tile, as the saved-Z
+// dGLU kernel does. One accumulator set; every wait is bounded.
 namespace {
 
-constexpr int RC4_BNA = 64;                   // dA_s columns per tile
-constexpr int RC4_STAGES = 3;
+constexpr int RC4_BNA = 128;                  // dA_s columns per tile
+constexpr int RC4_STAGES = 2;
 constexpr int RC4_A = BM * BKB;               // 16 KB: 128 rows x 128 bytes (dY, X)
-constexpr int RC4_B1 = RC4_BNA * BKB;         // 8 KB: W2 rows
-constexpr int RC4_B2 = 2 * RC4_BNA * BKB;     // 16 KB: W1p rows (gated; sReLU uses 8 KB)
+constexpr int RC4_B1 = RC4_BNA * BKB;         // 16 KB: W2 rows
+constexpr int RC4_B2 = 2 * RC4_BNA * BKB;     // 32 KB: W1p rows (gated; sReLU uses 16 KB)
 constexpr int RC4_STAGE = RC4_A + RC4_B1 + RC4_A + RC4_B2;
-constexpr int RC4_SF = 16 * SFA_SLAB;         // four 512-byte slabs of each of the four operands
+// a stage's scale slabs: four 512-byte slabs each of dY, W2 and X, then W1p's four slabs of
+// 256 rows (1 KB each; sReLU: 128 rows, 512 bytes)
+constexpr int RC4_SF_W1 = 12 * SFA_SLAB;
+constexpr int RC4_SF = RC4_SF_W1 + 4 * 2 * SFA_SLAB;
 constexpr int RC4_SF_OFF = RC4_STAGES * RC4_STAGE;
 constexpr int RC4_XT_OFF = RC4_SF_OFF + RC4_STAGES * RC4_SF;
 constexpr int RC4_CTRL_OFF = RC4_XT_OFF + kEpiWarps * XT_WARP;
 constexpr int RC4_TOTAL = RC4_CTRL_OFF + 4096 + 1024;
 constexpr int RC4_ZCOL = RC4_BNA;             // first TMEM column of Z
-constexpr int RC4_SFCOL = 192;                // first TMEM column of the scale factors
+constexpr int RC4_SFCOL = 384;                // first TMEM column of the two scale buffers
+constexpr int RC4_SFH = 40;                   // columns of one buffer (half a k-block)
 static_assert(RC4_TOTAL <= 232448, "shared memory");
-static_assert(RC4_SFCOL + 64 * RC4_STAGES <= kTmemCols, "TMEM map");
+static_assert(RC4_ZCOL + 2 * RC4_BNA <= RC4_SFCOL && RC4_SFCOL + 2 * RC4_SFH <= kTmemCols,
+              "TMEM map");
 static_assert(RC4_STAGE % 1024 == 0 && RC4_A % 1024 == 0 && RC4_B1 % 1024 == 0, "alignment");
 
 struct Rc4Args {
   CUtensorMap tmDy;  // dY row-wise copy [R_cap, H/2 bytes], box {128 B, 128 rows}
-  CUtensorMap tmW2;  // W2 row-wise copy [E*Fp, H/2], box {128 B, 64 rows}
+  CUtensorMap tmW2;  // W2 row-wise copy [E*Fp, H/2], box {128 B, 128 rows}
   CUtensorMap tmX;   // X row-wise copy [R_cap, H/2], box {128 B, 128 rows}
-  CUtensorMap tmW1;  // W1p row-wise copy [E*N1p, H/2], box {128 B, 128 (gated) / 64 rows}
-  // their scales: boxes of 128 rows (whole 128-row slabs for the weights) x four slabs
+  CUtensorMap tmW1;  // W1p row-wise copy [E*N1p, H/2], box {128 B, 256 (gated) / 128 rows}
+  // their scales: boxes of 128 rows (W1p: 256 gated) x four slabs
   CUtensorMap tmSdy, tmSw2, tmSx, tmSw1;
   const float *amax_dy, *amax_w2, *amax_x, *amax_w1;
   const int32_t* offsets;
@@ -906,6 +912,7 @@ struct Rc4Args {
 struct Rc4Ctrl {
   uint64_t full[RC4_STAGES];
   uint64_t empty[RC4_STAGES];
+  uint64_t sfh[2];  // the MMAs that read scale buffer h have completed
   uint64_t tfull;
   uint64_t tempty;
   uint64_t drain;
@@ -923,7 +930,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   MOE_GRIDDEP_ENTRY();
   constexpr bool kGated = KIND != MOE_ACT_SRELU;
   constexpr int ZN = kGated ? 2 * RC4_BNA : RC4_BNA;        // Z columns per tile
-  constexpr uint32_t kStageTx = RC4_STAGE - (kGated ? 0 : RC4_B2 / 2) + RC4_SF;
+  constexpr int kW1Slab = kGated ? 2 * SFA_SLAB : SFA_SLAB;   // W1p scale slab bytes
+  constexpr uint32_t kStageTx = RC4_STAGE - (kGated ? 0 : RC4_B2 / 2) + RC4_SF_W1 + 4 * kW1Slab;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -941,6 +949,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&c.tfull, 1);
     mbar_init(&c.tempty, kEpiWarps);
     mbar_init(&c.drain, 1);
+    mbar_init(&c.sfh[0], 1);
+    mbar_init(&c.sfh[1], 1);
     fence_mbar_init();
     c.abort = 0;
     bool ok = p.E >= 1 && p.E <= kMaxE;
@@ -1007,8 +1017,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
         int e, m0, n0;
         decode(tile, e, m0, n0);
+        // weight blocks start on 128-row scale slabs (Fp, N1p and n0 are multiples of 128)
         const int w2_row = e * p.Fp + n0, w1_row = e * p.N1p + (kGated ? 2 * n0 : n0);
-        const int w2_slab = w2_row & ~127, w1_slab = w1_row & ~127;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&c.empty[stage], phase ^ 1, abort, p.err)) break;
           uint8_t* s0 = smem + stage * RC4_STAGE;
@@ -1023,13 +1033,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(s0 + RC4_A, &p.tmW2, bar, k0 / 2, w2_row);
           tma_load_2d(s0 + RC4_A + RC4_B1, &p.tmX, bar, k0 / 2, m0);
           tma_load_2d(s0 + 2 * RC4_A + RC4_B1, &p.tmW1, bar, k0 / 2, w1_row);
-          // the four 64-value scale slabs of each operand, one copy each (whole 128-row
-          // slabs of the weights)
+          // the four 64-value scale slabs of each operand, one copy each
           const int kg = k0 / MMA_K;
           tma_load_2d(sf, &p.tmSdy, bar, m0, kg);
-          tma_load_2d(sf + 4 * SFA_SLAB, &p.tmSw2, bar, w2_slab, kg);
+          tma_load_2d(sf + 4 * SFA_SLAB, &p.tmSw2, bar, w2_row, kg);
           tma_load_2d(sf + 8 * SFA_SLAB, &p.tmSx, bar, m0, kg);
-          tma_load_2d(sf + 12 * SFA_SLAB, &p.tmSw1, bar, w1_slab, kg);
+          tma_load_2d(sf + RC4_SF_W1, &p.tmSw1, bar, w1_row, kg);
           if (++stage == RC4_STAGES) {
             stage = 0;
             phase ^= 1;
@@ -1054,14 +1063,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int acc_i = 0;
+      int sf_use[2] = {0, 0};  // half k-blocks whose scales have gone through buffer h
       bool issued_any = false;
       for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
-        int e, m0, n0;
-        decode(tile, e, m0, n0);
-        // a 64-row weight block in the upper half of its 128-row scale slab reads the slab's
-        // columns 2-3 (scale column = row / 32 within the slab)
-        const uint32_t w2_off = ((e * p.Fp + n0) & 127) ? 2u : 0u;
-        const uint32_t w1_off = ((e * p.N1p + (kGated ? 2 * n0 : n0)) & 127) ? 2u : 0u;
         if (!mbar_wait(&c.tempty, (acc_i & 1) ^ 1, abort, p.err)) break;
         tc_fence_after();
         bool ok = true;
@@ -1074,28 +1078,46 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sA1 = smem_u32(smem + stage * RC4_STAGE);
           const uint32_t sB1 = sA1 + RC4_A, sA2 = sB1 + RC4_B1, sB2 = sA2 + RC4_A;
           const uint32_t sf = smem_u32(smem + RC4_SF_OFF + stage * RC4_SF);
-          const uint32_t tsf = tmem_base + RC4_SFCOL + stage * 64;
           const int rem = p.H - kb * BK;
           const int nsub = rem >= BK ? BK / MMA_K : (rem + MMA_K - 1) / MMA_K;
-          for (int s = 0; s < nsub; ++s) {
-            const uint32_t col = tsf + 16 * s;
-            tmem_cp_32x128b_warpx4(col, smem_desc_noswizzle(sf + s * SFA_SLAB, 0, 128));
-            tmem_cp_32x128b_warpx4(col + 4, smem_desc_noswizzle(sf + (4 + s) * SFA_SLAB, 0, 128));
-            tmem_cp_32x128b_warpx4(col + 8, smem_desc_noswizzle(sf + (8 + s) * SFA_SLAB, 0, 128));
-            tmem_cp_32x128b_warpx4(col + 12,
-                                   smem_desc_noswizzle(sf + (12 + s) * SFA_SLAB, 0, 128));
+          for (int h = 0; h < 2 && 2 * h < nsub; ++h) {
+            // buffer h is free once the MMAs of the previous half k-block that used it are done
+            if (sf_use[h] > 0 && !mbar_wait(&c.sfh[h], (uint32_t)(sf_use[h] - 1) & 1u, abort,
+                                            p.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t hb = tmem_base + RC4_SFCOL + RC4_SFH * h;
+            const int s_end = nsub < 2 * h + 2 ? nsub : 2 * h + 2;
+            for (int s = 2 * h; s < s_end; ++s) {
+              const uint32_t col = hb + 20 * (s - 2 * h);
+              tmem_cp_32x128b_warpx4(col, smem_desc_noswizzle(sf + s * SFA_SLAB, 0, 128));
+              tmem_cp_32x128b_warpx4(col + 4,
+                                     smem_desc_noswizzle(sf + (4 + s) * SFA_SLAB, 0, 128));
+              tmem_cp_32x128b_warpx4(col + 8,
+                                     smem_desc_noswizzle(sf + (8 + s) * SFA_SLAB, 0, 128));
+              tmem_cp_32x128b_warpx4(col + 12,
+                                     smem_desc_noswizzle(sf + RC4_SF_W1 + s * kW1Slab, 0, 128));
+              if constexpr (kGated)  // W1p rows 128-255 of the tile
+                tmem_cp_32x128b_warpx4(
+                    col + 16, smem_desc_noswizzle(sf + RC4_SF_W1 + s * kW1Slab + SFA_SLAB, 0, 128));
+            }
+            for (int s = 2 * h; s < s_end; ++s) {
+              const uint32_t col = hb + 20 * (s - 2 * h);
+              const uint32_t acc = (kb | s) != 0 ? 1u : 0u;
+              mma_nvf4_ss(tmem_base, smem_desc_sw128(sA1 + s * (MMA_K / 2), 16, 1024),
+                          smem_desc_sw128(sB1 + s * (MMA_K / 2), 16, 1024), IDA, col, col + 4,
+                          acc);
+              mma_nvf4_ss(tmem_base + RC4_ZCOL, smem_desc_sw128(sA2 + s * (MMA_K / 2), 16, 1024),
+                          smem_desc_sw128(sB2 + s * (MMA_K / 2), 16, 1024), IDZ, col + 8,
+                          col + 12, acc);
+            }
+            issued_any = true;
+            mma_commit(&c.sfh[h]);
+            ++sf_use[h];
           }
-          for (int s = 0; s < nsub; ++s) {
-            const uint32_t col = tsf + 16 * s;
-            const uint32_t acc = (kb | s) != 0 ? 1u : 0u;
-            mma_nvf4_ss(tmem_base, smem_desc_sw128(sA1 + s * (MMA_K / 2), 16, 1024),
-                        smem_desc_sw128(sB1 + s * (MMA_K / 2), 16, 1024), IDA, col,
-                        col + 4 + w2_off, acc);
-            mma_nvf4_ss(tmem_base + RC4_ZCOL, smem_desc_sw128(sA2 + s * (MMA_K / 2), 16, 1024),
-                        smem_desc_sw128(sB2 + s * (MMA_K / 2), 16, 1024), IDZ, col + 8,
-                        col + 12 + w1_off, acc);
-          }
-          issued_any = true;
+          if (!ok) break;
           mma_commit(&c.empty[stage]);
           if (++stage == RC4_STAGES) {
             stage = 0;
@@ -1116,7 +1138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue warps 2..9
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;  // dA_s columns [32 * half, 32 * half + 32) of the tile
+    const int half = (warp - 2) >> 2;  // dA_s columns [64 * half, 64 * half + 64) of the tile
     uint32_t* xt = reinterpret_cast<uint32_t*>(smem + RC4_XT_OFF + (warp - 2) * XT_WARP);
     const float alpha_a =
         __frcp_rn(__fmul_rn(nvfp4_encode_scale(*p.amax_dy), nvfp4_encode_scale(*p.amax_w2)));
@@ -1137,14 +1159,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint16_t* dzrow = p.dz + (int64_t)row * p.N1;
       float dp = 0.f;
 #pragma unroll 1
-      for (int j = 0; j < 2; ++j) {
-        const int cc = half * 32 + 16 * j;  // dA_s column within the tile
+      for (int j = 0; j < 4; ++j) {
+        const int cc = half * 64 + 16 * j;  // dA_s column within the tile
         const int f0 = n0 + cc;
         if (f0 >= p.F) break;
+        // gated: Z holds the packed W1p rows, blocks of 64 gate then 64 linear columns
+        const int zc = kGated ? ((cc & ~63) << 1) + (cc & 63) : cc;
         uint32_t da[16], gz[16], lz[16];
         tmem_ld_32x32b_x16(tl + cc, da);
-        tmem_ld_32x32b_x16(tl + RC4_ZCOL + cc, gz);
-        if constexpr (kGated) tmem_ld_32x32b_x16(tl + RC4_ZCOL + RC4_BNA + cc, lz);
+        tmem_ld_32x32b_x16(tl + RC4_ZCOL + zc, gz);
+        if constexpr (kGated) tmem_ld_32x32b_x16(tl + RC4_ZCOL + zc + 64, lz);
         tmem_ld_wait();
         uint32_t w[16];  // dG pairs in w[0..7], dL pairs in w[8..15]
 #pragma unroll
@@ -1231,8 +1255,9 @@ cudaError_t launch_fc2_dgrad_recompute_fp4(const Fp4Problem& p, cudaStream_t s) 
       !tmap_fp4_rows(&a.tmX, p.x, BM) ||
       !tmap_fp4_rows(&a.tmW1, p.w1, p.gated ? 2 * RC4_BNA : RC4_BNA))
     return cudaErrorInvalidValue;
-  if (!tmap_fp4_sf(&a.tmSdy, p.dy, BM) || !tmap_fp4_sf(&a.tmSw2, p.w2, BM) ||
-      !tmap_fp4_sf(&a.tmSx, p.x, BM) || !tmap_fp4_sf(&a.tmSw1, p.w1, BM))
+  if (!tmap_fp4_sf(&a.tmSdy, p.dy, BM) || !tmap_fp4_sf(&a.tmSw2, p.w2, RC4_BNA) ||
+      !tmap_fp4_sf(&a.tmSx, p.x, BM) ||
+      !tmap_fp4_sf(&a.tmSw1, p.w1, p.gated ? 2 * RC4_BNA : RC4_BNA))
     return cudaErrorInvalidValue;
   a.amax_dy = p.amax + AM_DY; a.amax_w2 = p.amax + AM_W2;
   a.amax_x = p.amax + AM_X; a.amax_w1 = p.amax + AM_W1;

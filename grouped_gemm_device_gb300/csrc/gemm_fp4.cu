@@ -63,29 +63,37 @@ constexpr int XT_WARP = (32 * XT_PITCH + 16) * 4;  // rows 16..31 shifted by 16 
 // Tile shape, pipeline depth and shared-memory / TMEM maps of one epilogue kind.
 template <int EPI>
 struct Fp4Cfg {
-  static constexpr int BN = EPI == EPI_DGLU ? 128 : 256;
-  static constexpr int NACC = EPI == EPI_DGLU ? 2 : 1;
+  static constexpr int BN = 256;
+  static constexpr int NACC = 1;
   // the dGLU epilogue (saved-Z loads, activation gradient, rotated amax) outlasts the tile's
   // MMAs with eight warps: it takes FP4_DGLU_WARPS, each lane quadrant's warps dealing the
   // tile's 16-column chunks round-robin, with one stage fewer to make room for their buffers
   static constexpr int EW = EPI == EPI_DGLU ? FP4_DGLU_WARPS : kEpiWarps;
   static constexpr int EWQ = EW / 4;  // warps per lane quadrant
   static constexpr int THREADS = 64 + 32 * EW;
-  static constexpr int STAGES = EPI == EPI_DGLU && EW > 8 ? 3 : 4;
+  static constexpr int STAGES = EPI == EPI_DGLU ? 3 : 4;
   static constexpr int B_BYTES = BN * BKB;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int SFB_SLAB = BN * 4;
   static constexpr int SF_STAGE = 4 * (SFA_SLAB + SFB_SLAB);
   static constexpr int SF_COLS_MMA = 4 + 4 * (BN / 128);  // A's 128 rows + B's BN rows
   static constexpr int SF_COLS_STAGE = 4 * SF_COLS_MMA;
-  static constexpr int SF_COL0 = NACC * BN;
+  // TMEM: the fp32 accumulator, then the stages' scale columns; the dGLU keeps instead a
+  // bf16-packed copy of its accumulator (128 columns, so the accumulator is freed for the next
+  // tile's MMAs while the epilogue works) and two scale buffers of half a k-block each, reused
+  // once the MMAs that read them have completed
+  static constexpr int PACK_COL = BN;
+  static constexpr int SF_COL0 = EPI == EPI_DGLU ? BN + BN / 2 : NACC * BN;
+  static constexpr int SF_HALF = 2 * SF_COLS_MMA;
   static constexpr int SF_OFF = STAGES * STAGE_BYTES;
   static constexpr int ZQ_OFF = SF_OFF + STAGES * SF_STAGE;
   static constexpr int XT_OFF = ZQ_OFF + (EPI == EPI_DGLU ? EW * ZQ_WARP : 0);
   static constexpr int CTRL_OFF = XT_OFF + (EPI == EPI_DGLU ? EW * XT_WARP : 0);
   static constexpr int TOTAL = CTRL_OFF + 4096 + 1024;
   static_assert(TOTAL <= 232448, "shared memory above the per-block limit");
-  static_assert(SF_COL0 + STAGES * SF_COLS_STAGE <= kTmemCols, "TMEM map");
+  static_assert(SF_COL0 + (EPI == EPI_DGLU ? 2 * SF_HALF : STAGES * SF_COLS_STAGE) <= kTmemCols,
+                "TMEM map");
+  static_assert(EPI != EPI_DGLU || PACK_COL + BN / 2 <= SF_COL0, "TMEM map: packed copy");
   static_assert(STAGES <= kMaxStages, "barrier arrays");
   static_assert(EWQ * 4 == EW && THREADS <= 1024, "whole lane quadrants");
   static_assert(ZQ_OFF % 16 == 0 && XT_OFF % 16 == 0 && CTRL_OFF % 8 == 0, "alignment");
@@ -133,6 +141,7 @@ struct Ctrl {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t sfh[2];  // dGLU: the MMAs that read scale buffer h have completed
   uint32_t tmem_base;
   int abort;
   int total_tiles;
@@ -276,6 +285,7 @@ __global__ void __launch_bounds__(Fp4Cfg<EPI>::THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&c.tfull[i], 1);
       mbar_init(&c.tempty[i], L::EW);
+      mbar_init(&c.sfh[i], 1);
     }
     mbar_init(&c.drain, 1);
     fence_mbar_init();
@@ -375,6 +385,7 @@ __global__ void __launch_bounds__(Fp4Cfg<EPI>::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       int acc_i = 0;
+      int sf_use[2] = {0, 0};  // dGLU: half k-blocks whose scales have gone through buffer h
       bool issued_any = false;
       for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
         TileInfo t;
@@ -396,9 +407,48 @@ __global__ void __launch_bounds__(Fp4Cfg<EPI>::THREADS, 1)
           const uint32_t sA = smem_u32(smem + stage * L::STAGE_BYTES);
           const uint32_t sB = sA + A_BYTES;
           const uint32_t sf = smem_u32(smem + L::SF_OFF + stage * L::SF_STAGE);
-          const uint32_t sft = tmem_base + L::SF_COL0 + stage * L::SF_COLS_STAGE;
           const int rem = t.klen - kb * BK;
           const int nsub = rem >= BK ? BK / MMA_K : (rem + MMA_K - 1) / MMA_K;
+          if constexpr (EPI == EPI_DGLU) {
+            for (int h = 0; h < 2 && 2 * h < nsub; ++h) {
+              // buffer h is free once the MMAs of its previous half k-block have completed
+              // (the tensor pipe gets there while the other half's MMAs keep it busy)
+              if (sf_use[h] > 0 && !mbar_wait(&c.sfh[h], (uint32_t)(sf_use[h] - 1) & 1u, abort,
+                                              p.err)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t hb = tmem_base + L::SF_COL0 + L::SF_HALF * h;
+              const int s_end = nsub < 2 * h + 2 ? nsub : 2 * h + 2;
+              for (int s = 2 * h; s < s_end; ++s) {
+                const uint32_t col = hb + (s - 2 * h) * L::SF_COLS_MMA;
+                tmem_cp_32x128b_warpx4(col, smem_desc_noswizzle(sf + s * SFA_SLAB, 0, 128));
+#pragma unroll
+                for (int hh = 0; hh < BN / 128; ++hh)
+                  tmem_cp_32x128b_warpx4(
+                      col + 4 + 4 * hh,
+                      smem_desc_noswizzle(sf + 4 * SFA_SLAB + s * L::SFB_SLAB + 512 * hh, 0, 128));
+              }
+              for (int s = 2 * h; s < s_end; ++s) {
+                const uint32_t col = hb + (s - 2 * h) * L::SF_COLS_MMA;
+                mma_nvf4_ss(d_tmem, smem_desc_sw128(sA + s * (MMA_K / 2), 16, 1024),
+                            smem_desc_sw128(sB + s * (MMA_K / 2), 16, 1024), IDESC, col, col + 4,
+                            (kb | s) != 0 ? 1u : 0u);
+              }
+              issued_any = true;
+              mma_commit(&c.sfh[h]);
+              ++sf_use[h];
+            }
+            if (!ok) break;
+            mma_commit(&c.empty[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
+          const uint32_t sft = tmem_base + L::SF_COL0 + stage * L::SF_COLS_STAGE;
           for (int s = 0; s < nsub; ++s) {
             const uint32_t col = sft + s * L::SF_COLS_MMA;
             tmem_cp_32x128b_warpx4(col, smem_desc_noswizzle(sf + s * SFA_SLAB, 0, 128));
@@ -585,6 +635,27 @@ __global__ void __launch_bounds__(Fp4Cfg<EPI>::THREADS, 1)
         uint16_t* dzrow = static_cast<uint16_t*>(p.out) + (int64_t)row * p.ldo;
         float dp = 0.f;
         constexpr int EWQ = L::EWQ;
+        // this warp's 16-column chunks of dA_s, scaled and rounded to bf16, into the packed
+        // copy (8 columns a chunk); then the accumulator is free for the next tile's MMAs
+        const uint32_t tpk = tmem_base + ((uint32_t)(q * 32) << 16) + L::PACK_COL;
+#pragma unroll 1
+        for (int j = ws; j < BN / 16; j += EWQ) {
+          if (t.n0 + 16 * j >= p.N) break;
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(tacc + 16 * j, r);
+          tmem_ld_wait();
+          uint32_t w8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            w8[i] = pack_bf16x2(alpha * __uint_as_float(r[2 * i]),
+                                alpha * __uint_as_float(r[2 * i + 1]));
+          tmem_st_32x32b_x8(tpk + 8 * j, w8);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.tempty[acc]);
+        ++acc_i;
 #pragma unroll 1
         for (int j = ws, step = 0; j < BN / 16; j += EWQ, ++step) {
           const int f0 = t.n0 + 16 * j;
@@ -601,8 +672,8 @@ __global__ void __launch_bounds__(Fp4Cfg<EPI>::THREADS, 1)
           } else {
             asm volatile("cp.async.wait_group 0;" ::: "memory");
           }
-          uint32_t dr[16];
-          tmem_ld_32x32b_x16(tacc + 16 * j, dr);
+          uint32_t dr[8];  // dA_s of the chunk as bf16 pairs
+          tmem_ld_32x32b_x8(tpk + 8 * j, dr);
           uint32_t gw[8], lw[8];
           {
             const uint8_t* b = zq_ptr + (step & 1) * ZQ_BUF;
@@ -626,7 +697,7 @@ __global__ void __launch_bounds__(Fp4Cfg<EPI>::THREADS, 1)
             float dg[2], dl[2] = {0.f, 0.f};
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              const float d = alpha * __uint_as_float(dr[i + u]);
+              const float d = u ? bf16_hi(dr[i >> 1]) : bf16_lo(dr[i >> 1]);
               const float g = u ? bf16_hi(gw[i >> 1]) : bf16_lo(gw[i >> 1]);
               if constexpr (EXT) {
                 // the feature scale s enters as dA = p * s * dA_s and d_prob += dA_s * s * a
@@ -678,10 +749,6 @@ __global__ void __launch_bounds__(Fp4Cfg<EPI>::THREADS, 1)
             m_rht = fmaxf(m_rht, rht_amax_tile32(xt, w2, p.rht_mask, lane));
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&c.tempty[acc]);
-        ++acc_i;
         p.dprob_part[(int64_t)row * p.nparts + (t.n0 / BN) * EWQ + ws] = dp;
       }
     }

@@ -395,8 +395,8 @@ def layer_nvfp4(logits, x, W1, W2, k: int, act: ActParams, mask: int, dy=None,
                 a_s = bf16(p * act(Z))      the FC1 kernel's BF16 output, with amax(a_s)
                 Y = Q(a_s) Q_F(W2)
       backward: dA_s = Q(dY) Q_H(W2)^T, d_prob = sum_f dA_s * a,
-                dZ = bf16(dact(bf16 Z, p * dA_s))   the FC2-dgrad kernel's BF16 output, with
-                                            the amax of its Hadamard-rotated transpose
+                dZ = bf16(dact(bf16 Z, p * bf16 dA_s))   the FC2-dgrad kernel's BF16 output,
+                                            with the amax of its Hadamard-rotated transpose
                 dX = Q(dZ) Q_N1(W1)^T
                 dW2 = Q_rows(RHT(a_s))^T Q_rows(RHT(dY)),  dW1 = Q_rows(RHT(dZ))^T Q_rows(RHT(X))
     Q(.) quantises along the row (the reduction dimension of the row-grouped GEMMs) with its
@@ -409,9 +409,14 @@ def layer_nvfp4(logits, x, W1, W2, k: int, act: ActParams, mask: int, dy=None,
     per-feature scale of the activation (a_s = p * (a * s); d_prob = sum_f dA_s * s * a;
     dA = p * s * dA_s), with db1 = sum over an expert's rows of dZ (the unrounded dact
     output) and ds = sum over its rows of p * dA_s * a.
-    `recompute` (activation recomputation): the backward forms dZ from the FC1 output as the
-    tensor cores recompute it (unrounded, the same quantised operands) instead of the saved
-    bf16 copy; nothing else changes.
+    dZ is an input of integer decisions (its NVFP4 codes) whose precision the pages do not fix,
+    so it is formed from the dGLU epilogue's inputs as the kernel holds them (reading R14, as
+    R15 for MXFP8): the saved Z in bf16 and dA_s rounded to bf16 (the epilogue keeps the FC2
+    dgrad accumulator packed to bf16 in TMEM); d_prob, db1's rows and ds keep the plain
+    definitions.
+    `recompute` (activation recomputation): the backward forms dZ from the FC1 output and
+    dA_s as the tensor cores compute them (unrounded, the same quantised operands) instead of
+    the saved bf16 copy and the packed dA_s; nothing else changes.
     """
     from . import nvfp4 as nv
 
@@ -469,7 +474,7 @@ def layer_nvfp4(logits, x, W1, W2, k: int, act: ActParams, mask: int, dy=None,
         dA_s = dyq[tok] @ nv.fake_quant(W2[e], 1, S("w2")).T
         se = np.asarray(s[e], dtype=np.float64)[None, :] if s is not None else 1.0
         res.d_probs[tok, slot] = (dA_s * se * acts[e]).sum(axis=1)
-        dA = Ps[e][:, None] * (dA_s * se)
+        dA = Ps[e][:, None] * ((dA_s if recompute else bf16_round(dA_s)) * se)
         Zb = z_full[e] if recompute else res.Z[e]
         if act.gated:
             dg, dl = act_backward(act, Zb[:, :F], Zb[:, F:], dA)

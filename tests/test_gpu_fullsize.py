@@ -227,11 +227,11 @@ def nvfp4_fullsize_reference(cfg, logits, x, dy, w1, w2, toks, wexp, fs, hs):
         Zb = om.bf16_round(Z)
         del Z
         if cfg.gated:
-            dg, dl = om.act_backward(act, Zb[:, :F], Zb[:, F:], p * dA_s)
+            dg, dl = om.act_backward(act, Zb[:, :F], Zb[:, F:], p * om.bf16_round(dA_s))
             dZ = om.bf16_round(np.concatenate([dg, dl], axis=1))
             del dg, dl
         else:
-            dZ = om.bf16_round(om.act_backward(act, Zb, None, p * dA_s)[0])
+            dZ = om.bf16_round(om.act_backward(act, Zb, None, p * om.bf16_round(dA_s))[0])
         del Zb
         out.update(a=nv.amax(A), dz=nv.amax(dZ), at=nv.rht_amax_segments([A], mask),
                    dzt=nv.rht_amax_segments([dZ], mask))

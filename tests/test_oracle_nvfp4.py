@@ -298,8 +298,9 @@ def test_layer_bias_enters_the_saved_fc1_output():
 
 def test_layer_recompute_changes_only_the_fc1_output_the_backward_reads():
     """Recomputation: the forward and everything that does not read Z (y, a_s, its amaxes,
-    dW2) are identical; dZ is formed from the unrounded Z, so it differs from the saved-Z dZ
-    by about Z's bf16 rounding only; with the bf16 roundings taken out the two coincide."""
+    dW2) are identical; dZ is formed from the unrounded Z and dA_s, so it differs from the
+    saved-path dZ by about their bf16 roundings only; with the bf16 roundings taken out the
+    two coincide."""
     lg, x, W1, W2, dy, k = _small_layer(seed=17)
     act = om.ActParams()
     sv = om.layer_nvfp4(lg, x, W1, W2, k, act, 0x2222, dy=dy)

@@ -71,7 +71,7 @@ struct Fp4Cfg {
   static constexpr int EW = EPI == EPI_DGLU ? FP4_DGLU_WARPS : kEpiWarps;
   static constexpr int EWQ = EW / 4;  // warps per lane quadrant
   static constexpr int THREADS = 64 + 32 * EW;
-  static constexpr int STAGES = EPI == EPI_DGLU ? 3 : 4;
+  static constexpr int STAGES = EPI == EPI_DGLU ? (EW > 8 ? 2 : 3) : 4;
   static constexpr int B_BYTES = BN * BKB;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int SFB_SLAB = BN * 4;

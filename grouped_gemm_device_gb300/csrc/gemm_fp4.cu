@@ -65,9 +65,9 @@ template <int EPI>
 struct Fp4Cfg {
   static constexpr int BN = 256;
   static constexpr int NACC = 1;
-  // the dGLU epilogue (saved-Z loads, activation gradient, rotated amax) runs FP4_DGLU_WARPS
-  // warps, each lane quadrant's warps dealing the tile's 16-column chunks round-robin; its
-  // per-warp buffers cost it a pipeline stage (two more above eight warps)
+  // the dGLU epilogue (saved-Z loads, activation gradient, rotated amax) outlasts the tile's
+  // MMAs with eight warps: it takes FP4_DGLU_WARPS, each lane quadrant's warps dealing the
+  // tile's 16-column chunks round-robin, with one stage fewer to make room for their buffers
   static constexpr int EW = EPI == EPI_DGLU ? FP4_DGLU_WARPS : kEpiWarps;
   static constexpr int EWQ = EW / 4;  // warps per lane quadrant
   static constexpr int THREADS = 64 + 32 * EW;
